@@ -1,0 +1,491 @@
+#!/usr/bin/env python3
+"""Throughput of the Transformer-XL relative-attention hot path on GB300.
+
+One step = one steady-state segment of the base workload (B=22, H=8, D=64,
+W=512, M=512, bf16) through every row of the path: the sinusoidal distance
+table, the memory roll of k and v (previous segment's buffer -> head of this
+segment's buffer) and the fused relative attention.  Inputs are seeded and
+synthetic (hidden ~ N(0,1) projected by N(0, 0.02^2) weights), resident in
+HBM; eight segment buffers (~0.5 GB) rotate so that consecutive steps touch
+memory larger than L2.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the float64 CPU
+oracle instead, on a bounded sample of the same workload.  Under torchrun each
+rank processes its own batch of B sequences (weak scaling, no collective on
+the data path); the barrier and the max-over-ranks timing are the only
+communication.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "relative-attention tokens/s and TFLOP/s (fraction of BF16 peak), 1×GB300 vs CPU oracle"
+UNIT = "tokens/s"
+WORKLOAD = "base"
+N_SEG_BUFFERS = 8
+KERNEL_SOURCES = ["transformer_xl_relative_txl_gb300/csrc/relattn_tc.cu",
+                  "transformer_xl_relative_txl_gb300/csrc/txl_device.cuh"]
+NCU_SUMMARY = os.path.join(ROOT, "profiles", "relattn_tc_base_counters.json")
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+
+
+# ----------------------------------------------------------------------------
+# host-side helpers (also exercised by the CPU multi-process tests)
+# ----------------------------------------------------------------------------
+
+def counted_flops(B, H, D, W, M):
+    """Three contractions (q.k, q.r, p.v) x 2 flops over the visible pairs:
+    W*M memory pairs plus W(W+1)/2 causal pairs of the segment."""
+    return 6 * B * H * D * (W * M + W * (W + 1) // 2)
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def rank_batch_range(rank, B):
+    """Global sequence indices owned by a rank: each rank owns B sequences."""
+    return rank * B, (rank + 1) * B
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+
+    backend = dist.get_backend()
+    dev = torch.device("cuda", torch.cuda.current_device()) if backend == "nccl" else torch.device("cpu")
+    t = torch.tensor([float(x)], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def whole_job_throughput(tokens_per_step_per_rank, world, steps, max_elapsed_s):
+    return tokens_per_step_per_rank * world * steps / max_elapsed_s
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic_per_launch():
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, or None when absent or taken on a different kernel source."""
+    try:
+        with open(NCU_SUMMARY) as f:
+            s = json.load(f)
+    except (OSError, ValueError):
+        return None
+    if s.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    return s.get("dram_bytes_per_launch_full_workload")
+
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons in the background."""
+
+    FIELDS = ["timestamp", "uuid", "clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.active",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, uuid=None, period_ms=50):
+        self.uuid = uuid
+        self.samples = []  # (host time, dict)
+        self.proc = None
+        self.period_ms = period_ms
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={','.join(self.FIELDS)}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period_ms}"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != len(self.FIELDS):
+                continue
+            rec = dict(zip(self.FIELDS, parts))
+            if self.uuid and rec["uuid"] != self.uuid:
+                continue
+            self.samples.append((time.time(), rec))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        inside = [r for t, r in self.samples if t0 <= t <= t1]
+        window = "timed"
+        if not inside and self.samples:
+            # timed region shorter than the sampling period: nearest samples
+            mid = 0.5 * (t0 + t1)
+            inside = [r for _, r in sorted(self.samples, key=lambda s: abs(s[0] - mid))[:3]]
+            window = "nearest"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "window": "none"}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+
+        sm = [num(r["clocks.sm"]) for r in inside if num(r["clocks.sm"]) is not None]
+        mx = [num(r["clocks.max.sm"]) for r in inside if num(r["clocks.max.sm"]) is not None]
+        reasons = set()
+        for r in inside:
+            for k in ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"):
+                if r["clocks_event_reasons." + k].lower().startswith("active"):
+                    reasons.add(k)
+        return {"sm_mhz": float(np.median(sm)) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(inside), "window": window}
+
+
+# ----------------------------------------------------------------------------
+# the GPU arm
+# ----------------------------------------------------------------------------
+
+class SegmentStream:
+    """Device buffers for N_SEG_BUFFERS consecutive steady-state segments.
+
+    Buffer t holds stream rows [tW, tW + M + W): its head (M rows) is the
+    memory, its tail (W rows) the segment.  The roll of step t writes the head
+    of buffer t from buffer t-1, which reproduces the same rows."""
+
+    def __init__(self, wl, device, seed):
+        import torch
+
+        import transformer_xl_relative_txl_gb300 as txl
+        from synthetic import make_segments, project_r
+
+        self.wl = wl
+        S = N_SEG_BUFFERS
+        rows = wl.M + S * wl.W
+        seg = make_segments(wl, seed=seed, rows=rows)
+        self.seg = seg
+        L, C = wl.M + wl.W, wl.H * wl.D
+        bf = torch.bfloat16
+
+        def dev(a, dtype=bf):
+            return torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dtype)
+
+        self.k = [dev(seg.k[:, t * wl.W:t * wl.W + L]) for t in range(S)]
+        self.v = [dev(seg.v[:, t * wl.W:t * wl.W + L]) for t in range(S)]
+        self.q = [dev(seg.q[:, t * wl.W + wl.M:t * wl.W + L]) for t in range(S)]
+        self.kf = [x.view(wl.B, L, C) for x in self.k]
+        self.vf = [x.view(wl.B, L, C) for x in self.v]
+        self.o = torch.empty(wl.B, wl.W, wl.H, wl.D, device=device, dtype=bf)
+        # the distance table comes from the library; its projection r = R W_{k,R}
+        # is the step upstream of the path (host, float64)
+        self.R = torch.empty(L, wl.d_model, device=device, dtype=torch.float32)
+        txl.txl_sinusoid_rel(self.R)
+        torch.cuda.synchronize()
+        self.r = dev(project_r(self.R.cpu().numpy(), seg.W_r, wl.H, wl.D, "bf16"))
+        self.u = dev(seg.bias_u, torch.float32)
+        self.vb = dev(seg.bias_v, torch.float32)
+        # pinned host copies of each step's inputs (new rows) and output, for e2e
+        self.q_h = [x.cpu().pin_memory() for x in self.q]
+        self.knew_h = [x[:, wl.M:].cpu().contiguous().pin_memory() for x in self.k]
+        self.vnew_h = [x[:, wl.M:].cpu().contiguous().pin_memory() for x in self.v]
+        self.o_h = torch.empty(self.o.shape, dtype=bf).pin_memory()
+
+    def step(self, t, ev=None):
+        """One pass of the hot path; returns the number of library kernels launched."""
+        import transformer_xl_relative_txl_gb300 as txl
+
+        wl = self.wl
+        S = N_SEG_BUFFERS
+        cur, prev = t % S, (t - 1) % S
+        txl.txl_sinusoid_rel(self.R)
+        txl.txl_mem_update(self.kf[prev][:, :wl.M], self.kf[prev][:, wl.M:], self.kf[cur], wl.M)
+        txl.txl_mem_update(self.vf[prev][:, :wl.M], self.vf[prev][:, wl.M:], self.vf[cur], wl.M)
+        if ev is not None:
+            ev[0].record()
+        txl.txl_relattn_forward(self.q[cur], self.k[cur], self.v[cur], self.r, self.u, self.vb, self.o, None,
+                                M=wl.M)
+        if ev is not None:
+            ev[1].record()
+        return 4
+
+    def step_e2e(self, t):
+        """The same pass through the public API with host buffers: this step's
+        new q / k / v rows go host -> device, the output comes back."""
+        wl = self.wl
+        cur = t % N_SEG_BUFFERS
+        self.q[cur].copy_(self.q_h[cur], non_blocking=True)
+        for b in range(wl.B):
+            self.k[cur][b, wl.M:].copy_(self.knew_h[cur][b], non_blocking=True)
+            self.v[cur][b, wl.M:].copy_(self.vnew_h[cur][b], non_blocking=True)
+        n = self.step(t)
+        self.o_h.copy_(self.o, non_blocking=True)
+        return n
+
+    def e2e_bytes(self):
+        e = 2  # bf16
+        wl = self.wl
+        h2d = 3 * wl.B * wl.W * wl.H * wl.D * e
+        d2h = wl.B * wl.W * wl.H * wl.D * e
+        return h2d, d2h
+
+
+def gpu_uuid(device_index):
+    import torch
+
+    try:
+        u = str(torch.cuda.get_device_properties(device_index).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+def cpu_baseline_oracle(wl, stream, max_reps=3, budget_s=12.0):
+    """Times the float64 oracle (as it stands) on one full steady-state segment
+    of the same workload: memory roll of k and v plus the attention."""
+    from oracle import txl_oracle as O
+
+    seg = stream.seg
+    L, C = wl.M + wl.W, wl.H * wl.D
+    q = seg.q[:, wl.M:L]
+    k = seg.k[:, :L]
+    v = seg.v[:, :L]
+    r = stream.r.float().cpu().numpy()
+    reps = 0
+    c0 = time.process_time()
+    t0 = time.perf_counter()
+    while True:
+        O.mem_update(k[:, :wl.M].reshape(wl.B, wl.M, C), k[:, wl.M:].reshape(wl.B, wl.W, C), wl.M)
+        O.mem_update(v[:, :wl.M].reshape(wl.B, wl.M, C), v[:, wl.M:].reshape(wl.B, wl.W, C), wl.M)
+        O.relattn_forward(q, k, v, r, seg.bias_u, seg.bias_v, wl.M)
+        reps += 1
+        el = time.perf_counter() - t0
+        if reps >= max_reps or el >= budget_s:
+            break
+    cpu = time.process_time() - c0
+    return {"value": wl.B * wl.W * reps / el, "unit": UNIT, "cores": max(1, round(cpu / el)),
+            "cores_available": len(os.sched_getaffinity(0)), "kind": "oracle",
+            "sample": f"{reps} full steady-state segment(s) of {WORKLOAD} (B={wl.B}, all {wl.H} heads, "
+                      f"roll + attention), float64 numpy, {el:.1f} s wall"}
+
+
+def run_ours(args):
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import WORKLOADS
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", init_method="env://")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    wl = WORKLOADS[WORKLOAD]
+    stream = SegmentStream(wl, device, seed=rank)
+    cs = torch.cuda.current_stream()
+
+    for t in range(args.warmup):
+        stream.step(t)
+    torch.cuda.synchronize()
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait during warm-up")
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(gpu_uuid(local))
+    sampler.start()
+    time.sleep(0.3)
+    launches = 0
+    barrier(world)
+    torch.cuda.synchronize()
+    h0 = time.time()
+    start.record(cs)
+    for t in range(K):
+        launches += stream.step(args.warmup + t, evs[t])
+    end.record(cs)
+    torch.cuda.synchronize()
+    h1 = time.time()
+    barrier(world)
+    time.sleep(0.15)
+    sampler.stop()
+    elapsed_s = start.elapsed_time(end) / 1e3
+    k1_ms = float(np.mean([a.elapsed_time(b) for a, b in evs]))
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait during the timed region")
+    max_elapsed = max_over_ranks(elapsed_s, world)
+    tokens = wl.B * wl.W
+    value = whole_job_throughput(tokens, world, K, max_elapsed)
+
+    # end to end through the public API with host buffers
+    E = max(1, min(K, 50))
+    torch.cuda.synchronize()
+    barrier(world)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(cs)
+    for t in range(E):
+        stream.step_e2e(t)
+    e1.record(cs)
+    torch.cuda.synchronize()
+    e2e_s = max_over_ranks(e0.elapsed_time(e1) / 1e3, world)
+    e2e = whole_job_throughput(tokens, world, E, e2e_s)
+    h2d, d2h = stream.e2e_bytes()
+
+    if rank != 0:
+        return None
+    peaks, peak_src = load_peaks()
+    flops = counted_flops(wl.B, wl.H, wl.D, wl.W, wl.M)
+    achieved = flops / (k1_ms / 1e3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    result = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": max_elapsed / K * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{WORKLOAD}: B={wl.B} H={wl.H} D={wl.D} W={wl.W} M={wl.M}, steady-state "
+                               f"segments, bf16 in / fp32 accumulate / bf16 out",
+                   "global_batch": wl.B * world, "seq_len": wl.W, "memory": wl.M,
+                   "parallelism": f"dp{world} (each rank its own {wl.B} sequences)",
+                   "l2": f"inputs larger than L2: {N_SEG_BUFFERS} rotating segment buffers "
+                         f"(~{N_SEG_BUFFERS * (2 * wl.B * (wl.M + wl.W) + wl.B * wl.W) * wl.H * wl.D * 2 / 1e9:.2f} GB)",
+                   "step": "txl_sinusoid_rel + txl_mem_update(k) + txl_mem_update(v) + txl_relattn_forward"},
+        "tflops": achieved,
+        "attn_ms": k1_ms,
+        "roofline": {"kernel": "relattn_tc_kernel<64>", "bound": "tensor", "achieved": achieved, "peak": peak,
+                     "unit": "TFLOP/s", "frac": achieved / peak,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)",
+                     "traffic": ncu_traffic_per_launch(),
+                     "per_launch_work": f"{flops} counted flops = 6*B*H*D*(W*M + W(W+1)/2)"},
+        "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": sampler.summary(h0, h1),
+    }
+    if world == 1:
+        result["cpu_baseline"] = cpu_baseline_oracle(wl, stream)
+    return result
+
+
+# ----------------------------------------------------------------------------
+# the reference arm: the float64 CPU oracle, bounded samples
+# ----------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    from oracle import txl_oracle as O
+    from synthetic import WORKLOADS, make_prefilled, project_r
+
+    wl = WORKLOADS[WORKLOAD]
+    q, k, v, s = make_prefilled(wl, wl.M, seed=0)
+    r = project_r(O.sinusoid_rel(wl.M + wl.W, wl.d_model), s.W_r, wl.H, wl.D, "bf16")
+    pairs = [(b, h) for b in range(wl.B) for h in range(wl.H)]
+
+    def run_heads(idx):
+        for n in idx:
+            b, h = pairs[n % len(pairs)]
+            O.relattn_forward(q[b:b + 1, :, h:h + 1], k[b:b + 1, :, h:h + 1], v[b:b + 1, :, h:h + 1],
+                              r[:, h:h + 1], s.bias_u[h:h + 1], s.bias_v[h:h + 1], wl.M)
+
+    t0 = time.perf_counter()
+    run_heads([0])
+    t_head = time.perf_counter() - t0
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n_heads = int(max(1, min(len(pairs), budget // max(t_head, 1e-6))))
+    nxt = 0
+    for _ in range(args.warmup):
+        run_heads(range(nxt, nxt + n_heads))
+        nxt += n_heads
+    c0 = time.process_time()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run_heads(range(nxt, nxt + n_heads))
+        nxt += n_heads
+    el = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    tokens_per_step = n_heads * wl.W / wl.H  # a token needs all H heads
+    value = tokens_per_step * args.steps / el
+    sample = (f"{n_heads} (batch, head) pair(s) of the {WORKLOAD} steady-state segment per step "
+              f"(of {len(pairs)}), float64 numpy oracle")
+    return {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": f"{WORKLOAD}: B={wl.B} H={wl.H} D={wl.D} W={wl.W} M={wl.M}",
+                       "seq_len": wl.W, "memory": wl.M},
+            "cpu_baseline": {"value": value, "unit": UNIT, "kind": "oracle",
+                             "cores": max(1, round(cpu / el)), "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    res = run_reference(args) if args.impl == "reference" else run_ours(args)
+    if res is not None:
+        print(json.dumps(res), flush=True)
+    if dist_env()[1] > 1 and args.impl == "ours":
+        import torch.distributed as dist
+
+        if dist.is_initialized():
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

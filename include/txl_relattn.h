@@ -1,0 +1,185 @@
+/*
+ * txl_relattn.h -- C ABI of the GB300 (sm_103a) Transformer-XL relative-position
+ * attention library.
+ *
+ * The library computes the per-segment hot path of Transformer-XL:
+ *
+ *   - txl_relattn_forward: relative multi-head attention of one W-token segment
+ *     over [memory of M cached rows ; segment] with the four-term relative score
+ *     and an in-kernel distance index (no pad-and-reshape), causal mask,
+ *     online softmax and P.V;
+ *   - txl_mem_update: the memory roll, keeping the last M rows of
+ *     [memory ; segment];
+ *   - txl_sinusoid_rel: the parameter-free sinusoidal distance table R.
+ *
+ * Conventions shared by every entry point
+ *   - Pointers marked "device" are device memory owned by the caller; the
+ *     library never allocates, frees or retains them.  Host pointers are only
+ *     read or written during the call.
+ *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
+ *     returns a txl_status code.  Argument errors are detected on the host before
+ *     any launch, and then nothing is launched.  A failed launch returns
+ *     TXL_ERR_CUDA.  Errors detected inside a kernel (a bounded wait that ran out)
+ *     are recorded in a device status word read by txl_get_device_status.
+ *   - Layouts are dense row-major ("BSHD"): the innermost index is the head
+ *     dimension D, then the head H, then the row (query, key or distance), then
+ *     the batch B.
+ *   - B == 0 or W == 0 is a valid empty call: TXL_OK, nothing is launched.
+ *   - The entry points are thread-safe; shape-keyed descriptor caches are
+ *     guarded by a mutex.
+ */
+#ifndef TXL_RELATTN_H
+#define TXL_RELATTN_H
+
+#include <cuda_runtime.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TXL_VERSION 100 /* 1.0.0 */
+
+/* Symbols of the shared library (built with hidden default visibility). */
+#if defined(__GNUC__)
+#define TXL_API __attribute__((visibility("default")))
+#else
+#define TXL_API
+#endif
+
+typedef enum {
+  TXL_F32 = 0, /* IEEE binary32 */
+  TXL_BF16 = 1 /* bfloat16 (storage); arithmetic accumulates in fp32 */
+} txl_dtype;
+
+typedef enum {
+  TXL_OK = 0,
+  TXL_ERR_INVALID_ARG = 1,    /* null pointer, negative size, r too short, ... */
+  TXL_ERR_UNSUPPORTED = 2,    /* valid request outside what this build supports */
+  TXL_ERR_ALIAS = 3,          /* an output range overlaps an input range */
+  TXL_ERR_CUDA = 4,           /* a CUDA runtime / driver call failed */
+  TXL_ERR_DEVICE_TIMEOUT = 5  /* a kernel's bounded wait expired (see below) */
+} txl_status;
+
+/*
+ * txl_relattn_forward -- relative multi-head attention of one segment.
+ *
+ * Defines the score of "Transformer-XL, explained", method step 4 (content
+ * against content, content against a sinusoidal encoding of the distance i - j,
+ * and the two global biases u and v that replace the query in a content-only
+ * and a distance-only term, with separate key projections), grouped by the
+ * query-side factor:
+ *
+ *   s[i,j] = scale * ( (q_i + u_h) . k_j  +  (q_i + v_h) . r_{M+i-j} )   j <= M+i
+ *   s[i,j] = -inf                                                          j >  M+i
+ *   o_i    = sum_j softmax_j(s[i,.]) v_j          lse_i = log sum_j exp(s[i,j])
+ *
+ * Keys and values extend over [memory ; segment] with the memory first and
+ * queries from the segment only (method step 3 and the concatenation in the
+ * symbol legend); the distance term is evaluated once per distance and each
+ * row is shifted into place (method step 5) by indexing row d = M+i-j of r
+ * inside the kernel; the mask lets query i see all M memory rows and segment
+ * rows up to i ("Implementing Transformer-XL", relative_attention's causal
+ * mask); the scale multiplies the sum of all terms (the same function's
+ * division by sqrt(d_head); the simulation's softmax(QK^T/sqrt(d))).
+ *
+ *   q      device, [B, W, H, D]   `dtype`   queries of the current segment
+ *   k      device, [B, M+W, H, D] `dtype`   keys, memory rows 0..M-1 first
+ *   v      device, [B, M+W, H, D] `dtype`   values, same row order as k
+ *   r      device, [n_r, H, D]    `dtype`   projected distance keys, row d is
+ *                                           distance d; n_r >= M+W
+ *   bias_u device, [H, D] fp32              global content bias u
+ *   bias_v device, [H, D] fp32              global distance bias v
+ *   o      device, [B, W, H, D]   `o_dtype` output (must not overlap inputs)
+ *   lse    device, [B, H, W] fp32 or NULL   natural-log softmax normaliser
+ *   M      memory rows in this call (0 for the first segment)
+ *   scale  score scale, 1/sqrt(D) by convention
+ *   dtype  TXL_BF16: tensor-core path (tcgen05), D in {64, 128}, fp32
+ *          accumulation, o_dtype TXL_BF16 or TXL_F32;
+ *          TXL_F32: exact fp32 path (CUDA cores), 1 <= D <= 256, o_dtype TXL_F32.
+ *
+ * Requirements: q, k, v, r and o 16-byte aligned (TXL_ERR_INVALID_ARG
+ * otherwise); o must not overlap q, k, v, r, bias_u, bias_v or lse
+ * (TXL_ERR_ALIAS).  Memory rows are only read (stop-gradient).
+ */
+TXL_API int txl_relattn_forward(const void* q, const void* k, const void* v, const void* r,
+                        const float* bias_u, const float* bias_v, void* o, float* lse,
+                        int B, int W, int M, int H, int D, int n_r, float scale,
+                        txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream);
+
+/*
+ * txl_mem_update -- the memory roll.
+ *
+ * Defines mem_tau = last M rows of [stop_grad(mem_{tau-1}) ; h_tau] from the
+ * "Long-context transformers" simulation's segment-recurrence equations (and
+ * the glossary loop's `memory = segment.detach()` when M equals the segment
+ * length).  Rows are copied bit for bit.
+ *
+ *   mem      device, [B, m_prev, C] rows, batch stride mem_bs elements  (may be
+ *            NULL when m_prev == 0)
+ *   h        device, [B, w, C] rows, batch stride h_bs elements
+ *   mem_out  device, [B, m', C] rows, batch stride out_bs elements, with
+ *            m' = min(m, m_prev + w); must not overlap mem or h (TXL_ERR_ALIAS)
+ *   m_out    host, receives m' (may be NULL)
+ *   dtype    element type (TXL_F32 or TXL_BF16); C >= 1
+ *
+ * A typical caller ping-pongs two [B, M+W, C] buffers: the roll writes the
+ * head of the next buffer from the current one (mem = buf, h = buf + M*C,
+ * out_bs = mem_bs = h_bs = (M+W)*C).
+ */
+TXL_API int txl_mem_update(const void* mem, int m_prev, const void* h, int w, void* mem_out, int m,
+                   int B, int C, long long mem_bs, long long h_bs, long long out_bs,
+                   int* m_out, txl_dtype dtype, cudaStream_t stream);
+
+/*
+ * txl_sinusoid_rel -- the raw sinusoidal distance table R[n_dist, dim].
+ *
+ * "Transformer-XL, explained", symbol legend: R_{i-j} is a sinusoidal encoding
+ * of the distance with no trained parameters; fixed sinusoids give encodings
+ * to distances longer than any seen in training, so no distance is clipped.
+ *
+ *   R[d, 2k]   = sin(d * w_k),   R[d, 2k+1] = cos(d * w_k),
+ *   w_k = 10000^(-2k/dim),  d = 0 .. n_dist-1
+ *
+ * The angle is formed and reduced modulo 2*pi in extended precision before the
+ * fp32 sine and cosine, so |R - exact| stays near 1e-7 for every distance.
+ *
+ *   R      device, [n_dist, dim] `dtype`
+ *   dim    even, >= 2;  n_dist >= 0 (0 is an empty call)
+ */
+TXL_API int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cudaStream_t stream);
+
+/*
+ * txl_get_device_status -- synchronises `stream`, then reads and clears the
+ * device status word of the current device.  Returns TXL_OK, or
+ * TXL_ERR_DEVICE_TIMEOUT when a kernel gave up a bounded wait (it then exits
+ * cleanly, leaving its outputs undefined, and the context stays usable), or
+ * TXL_ERR_CUDA if the synchronisation itself failed.
+ */
+TXL_API int txl_get_device_status(cudaStream_t stream);
+
+/* Human-readable name of a txl_status value (static string). */
+TXL_API const char* txl_status_string(int status);
+
+/* TXL_VERSION of the built library. */
+TXL_API int txl_version(void);
+
+/*
+ * Test hooks (not part of the numerical API).
+ *
+ * txl_debug_set_wait_limit_ns: upper bound, in nanoseconds, of every bounded
+ * wait inside the kernels (default 2e9).  Values < 1000 are rejected.
+ *
+ * txl_debug_inject_stall: when nonzero, the next txl_relattn_forward on the
+ * tensor-core path has its loader stop issuing loads after the first key tile,
+ * so the consumers' bounded waits expire and the call reports
+ * TXL_ERR_DEVICE_TIMEOUT through txl_get_device_status.  The flag clears
+ * itself after that one call.
+ */
+TXL_API int txl_debug_set_wait_limit_ns(unsigned long long ns);
+TXL_API int txl_debug_inject_stall(int on);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TXL_RELATTN_H */

@@ -1,0 +1,295 @@
+"""GPU parity: every kernel of the path against the float64 oracle on the same
+seeded inputs, through the C ABI (via the thin binding)."""
+
+import zlib
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import txl_oracle as O
+from synthetic import WORKLOADS, make_segments, project_r
+
+from gpu_util import (BF16_ATOL, F32_ATOL, assert_bf16_close, dev, prefilled_case, run_forward, to_dev,
+                      torch_dtype, workload)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import transformer_xl_relative_txl_gb300 as txl  # fails loudly if not built
+
+    torch.cuda.set_device(0)
+    txl.txl_get_device_status()
+    yield txl
+
+
+# ----------------------------------------------------------------------------
+# K4: sinusoid table
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n,dim", [(8, 16), (1, 2), (1024, 512), (1536, 1024), (1728, 1024), (3328, 1024),
+                                   (777, 6)])
+def test_sinusoid_f32(_lib, n, dim):
+    R = torch.empty(n, dim, device=dev())
+    _lib.txl_sinusoid_rel(R)
+    err = np.abs(R.cpu().numpy().astype(np.float64) - O.sinusoid_rel(n, dim)).max()
+    assert err <= 1e-6, err
+
+
+def test_sinusoid_bf16(_lib):
+    n, dim = 1728, 1024
+    R = torch.empty(n, dim, device=dev(), dtype=torch.bfloat16)
+    _lib.txl_sinusoid_rel(R)
+    want = O.sinusoid_rel(n, dim)
+    got = R.float().cpu().numpy().astype(np.float64)
+    # within half a bf16 ulp of the exact value (plus the fp32 error)
+    ulp = np.exp2(np.floor(np.log2(np.maximum(np.abs(want), 1e-30))) - 7)
+    assert np.all(np.abs(got - want) <= 0.5 * ulp + 1e-6)
+
+
+# ----------------------------------------------------------------------------
+# K3: memory roll (bit-exact)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("m_prev,w,m,C", [(0, 4, 4, 16), (4, 4, 4, 16), (512, 512, 512, 512),
+                                          (1600, 128, 1600, 1024), (128, 128, 1600, 1024),
+                                          (7, 3, 5, 33), (3, 7, 5, 9), (5, 2, 0, 8), (0, 0, 4, 8),
+                                          (10, 6, 12, 1)])
+def test_mem_roll_bit_exact(_lib, dtype, m_prev, w, m, C):
+    B = 3
+    rng = np.random.default_rng(m_prev * 131 + w * 7 + m + C)
+    td = torch_dtype(dtype)
+    pad_m, pad_h, pad_o = 2, 1, 3  # extra rows: batch strides differ from the row counts
+    mem = torch.from_numpy(rng.standard_normal((B, m_prev + pad_m, C)).astype(np.float32)).to(dev()).to(td)
+    h = torch.from_numpy(rng.standard_normal((B, w + pad_h, C)).astype(np.float32)).to(dev()).to(td)
+    keep = min(m, m_prev + w)
+    out = torch.full((B, keep + pad_o, C), -7.0, device=dev(), dtype=td)
+    got_m = _lib.txl_mem_update(mem[:, :m_prev], h[:, :w], out, m)
+    assert got_m == keep
+    want = O.mem_update(mem[:, :m_prev].cpu().float().numpy(), h[:, :w].cpu().float().numpy(), m)
+    got = out[:, :keep].cpu().float().numpy()
+    assert got.shape == want.shape
+    assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32))
+    assert torch.all(out[:, keep:] == -7.0)  # nothing written past m'
+
+
+# ----------------------------------------------------------------------------
+# K2: exact fp32 path
+# ----------------------------------------------------------------------------
+
+def test_tiny_fp32_three_segments(_lib):
+    """The pages' toy: seg_len 4, dim 16, 2 heads, three segments carrying
+    memory (first one empty), roll and attention on the GPU."""
+    wl = WORKLOADS["tiny"]
+    seg = make_segments(wl)
+    R = O.sinusoid_rel(wl.M + wl.W, wl.d_model)
+    r = project_r(R, seg.W_r, wl.H, wl.D, wl.dtype)
+    expect = O.run_segments([seg.seg("q", t) for t in range(3)], [seg.seg("k", t) for t in range(3)],
+                            [seg.seg("v", t) for t in range(3)], r, seg.bias_u, seg.bias_v, wl.M)
+    L, C = wl.M + wl.W, wl.H * wl.D
+    kb = [torch.zeros(wl.B, L, C, device=dev()) for _ in range(2)]
+    vb = [torch.zeros(wl.B, L, C, device=dev()) for _ in range(2)]
+    m_tau = 0
+    rd, ud, vd = to_dev(r, torch.float32), to_dev(seg.bias_u, torch.float32), to_dev(seg.bias_v, torch.float32)
+    for tau in range(3):
+        cur = tau % 2
+        kb[cur][:, m_tau:m_tau + wl.W] = to_dev(seg.seg("k", tau), torch.float32).view(wl.B, wl.W, C)
+        vb[cur][:, m_tau:m_tau + wl.W] = to_dev(seg.seg("v", tau), torch.float32).view(wl.B, wl.W, C)
+        q = to_dev(seg.seg("q", tau), torch.float32)
+        o = torch.empty_like(q)
+        lse = torch.empty(wl.B, wl.H, wl.W, device=dev())
+        k = kb[cur][:, :m_tau + wl.W].reshape(wl.B, m_tau + wl.W, wl.H, wl.D).contiguous()
+        v = vb[cur][:, :m_tau + wl.W].reshape(wl.B, m_tau + wl.W, wl.H, wl.D).contiguous()
+        _lib.txl_relattn_forward(q, k, v, rd, ud, vd, o, lse, M=m_tau)
+        eo, el, em = expect[tau]
+        assert em == m_tau == [0, 4, 4][tau]
+        assert np.abs(o.cpu().numpy() - eo).max() <= F32_ATOL
+        assert np.abs(lse.cpu().numpy() - el).max() <= F32_ATOL
+        nxt = 1 - cur
+        m_new = _lib.txl_mem_update(kb[cur][:, :m_tau], kb[cur][:, m_tau:m_tau + wl.W], kb[nxt], wl.M)
+        _lib.txl_mem_update(vb[cur][:, :m_tau], vb[cur][:, m_tau:m_tau + wl.W], vb[nxt], wl.M)
+        m_tau = m_new
+    assert _lib.txl_get_device_status() == 0
+
+
+@pytest.mark.parametrize("B,H,D,W,M", [(1, 2, 8, 4, 4), (2, 3, 16, 37, 50), (1, 1, 1, 5, 0), (2, 2, 64, 130, 7),
+                                       (1, 2, 256, 9, 300), (1, 1, 33, 1, 0)])
+def test_fp32_shapes(B, H, D, W, M):
+    wl = workload(B, H, D, W, M, "f32")
+    q, k, v, r, bu, bv = prefilled_case(wl, n_r_extra=3)
+    o, lse = run_forward(q, k, v, r, bu, bv, M, "f32")
+    eo, el = O.relattn_forward(q, k, v, r, bu, bv, M)
+    assert np.abs(o - eo).max() <= F32_ATOL
+    assert np.abs(lse - el).max() <= F32_ATOL
+
+
+# ----------------------------------------------------------------------------
+# K1: bf16 tensor-core path, several tiles and ragged tails
+# ----------------------------------------------------------------------------
+
+SHAPES = [
+    (1, 1, 64, 1, 0),      # a single key
+    (1, 2, 64, 128, 0),    # one full tile, empty memory
+    (2, 2, 64, 200, 150),  # ragged query tile, memory not a tile multiple
+    (1, 2, 64, 300, 384),  # three query tiles
+    (2, 1, 64, 64, 1000),  # short segment, long memory
+    (1, 2, 128, 200, 150),
+    (2, 1, 128, 256, 128),
+    (1, 1, 128, 129, 1),
+]
+
+
+@pytest.mark.parametrize("B,H,D,W,M", SHAPES)
+@pytest.mark.parametrize("o_dtype", ["bf16", "f32"])
+def test_bf16_shapes(B, H, D, W, M, o_dtype):
+    wl = workload(B, H, D, W, M)
+    q, k, v, r, bu, bv = prefilled_case(wl, n_r_extra=5)
+    o, lse = run_forward(q, k, v, r, bu, bv, M, "bf16", o_dtype=o_dtype)
+    eo, el = O.relattn_forward(q, k, v, r, bu, bv, M)
+    assert_bf16_close(o, eo, f"o {B,H,D,W,M}")
+    assert np.abs(lse - el).max() <= BF16_ATOL
+
+
+def test_bf16_scale_and_biases_matter():
+    """A scale other than 1/sqrt(D) and large biases: catches a dropped term."""
+    wl = workload(1, 2, 64, 160, 96)
+    q, k, v, r, bu, bv = prefilled_case(wl)
+    bu = bu * 40
+    bv = bv * 40
+    o, _ = run_forward(q, k, v, r, bu, bv, wl.M, "bf16", o_dtype="f32", scale=0.2)
+    eo, _ = O.relattn_forward(q, k, v, r, bu, bv, wl.M, scale=0.2)
+    assert_bf16_close(o, eo)
+
+
+def test_bf16_segments_with_roll(_lib):
+    """Four consecutive segments from empty memory (M_tau = 0, 256, 384, 384),
+    roll and attention on the GPU, against the oracle's recurrence."""
+    wl = workload(2, 2, 64, 256, 384)
+    wl = wl.__class__(wl.name, wl.cfg_id, wl.B, wl.H, wl.D, wl.d_model, wl.W, wl.M, 4, "bf16")
+    seg = make_segments(wl)
+    r = project_r(O.sinusoid_rel(wl.M + wl.W, wl.d_model), seg.W_r, wl.H, wl.D, "bf16")
+    expect = O.run_segments([seg.seg("q", t) for t in range(4)], [seg.seg("k", t) for t in range(4)],
+                            [seg.seg("v", t) for t in range(4)], r, seg.bias_u, seg.bias_v, wl.M)
+    L, C = wl.M + wl.W, wl.H * wl.D
+    bufs = [[torch.zeros(wl.B, L, C, device=dev(), dtype=torch.bfloat16) for _ in range(2)] for _ in range(2)]
+    rd = to_dev(r, torch.bfloat16)
+    ud, vd = to_dev(seg.bias_u, torch.float32), to_dev(seg.bias_v, torch.float32)
+    m_tau = 0
+    for tau in range(4):
+        cur = tau % 2
+        kb, vb = bufs[cur]
+        kb[:, m_tau:m_tau + wl.W] = to_dev(seg.seg("k", tau), torch.bfloat16).view(wl.B, wl.W, C)
+        vb[:, m_tau:m_tau + wl.W] = to_dev(seg.seg("v", tau), torch.bfloat16).view(wl.B, wl.W, C)
+        q = to_dev(seg.seg("q", tau), torch.bfloat16)
+        o = torch.empty(q.shape, device=dev(), dtype=torch.float32)
+        k = kb[:, :m_tau + wl.W].reshape(wl.B, m_tau + wl.W, wl.H, wl.D).contiguous()
+        v = vb[:, :m_tau + wl.W].reshape(wl.B, m_tau + wl.W, wl.H, wl.D).contiguous()
+        _lib.txl_relattn_forward(q, k, v, rd, ud, vd, o, None, M=m_tau)
+        eo, _, em = expect[tau]
+        assert em == m_tau
+        assert_bf16_close(o.cpu().numpy(), eo, f"segment {tau}")
+        nk, nv = bufs[1 - cur]
+        m_new = _lib.txl_mem_update(kb[:, :m_tau], kb[:, m_tau:m_tau + wl.W], nk, wl.M)
+        _lib.txl_mem_update(vb[:, :m_tau], vb[:, m_tau:m_tau + wl.W], nv, wl.M)
+        m_tau = m_new
+    assert _lib.txl_get_device_status() == 0
+
+
+def test_bf16_deterministic():
+    wl = workload(2, 2, 64, 300, 200)
+    q, k, v, r, bu, bv = prefilled_case(wl)
+    o1, l1 = run_forward(q, k, v, r, bu, bv, wl.M, "bf16")
+    o2, l2 = run_forward(q, k, v, r, bu, bv, wl.M, "bf16")
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+# ----------------------------------------------------------------------------
+# Full-size workloads, in the launch configuration the benchmark times
+# (bf16 output, no lse), checked on sampled rows computed one by one.
+# ----------------------------------------------------------------------------
+
+FULL = [("base", 512), ("large", 384), ("wide", 768), ("long", 1600), ("long", 0), ("long", 384),
+        ("long", 3200)]
+
+
+def _sample_rows(W, rng):
+    rows = {0, W - 1, min(127, W - 1), min(128, W - 1), W // 2}
+    rows |= set(int(x) for x in rng.integers(0, W, 4))
+    return sorted(rows)
+
+
+@pytest.mark.parametrize("name,M", FULL)
+def test_full_size_sampled(name, M):
+    base = WORKLOADS[name]
+    wl = base.__class__(base.name, base.cfg_id, base.B, base.H, base.D, base.d_model, base.W, M, 1, "bf16")
+    q, k, v, r, bu, bv = prefilled_case(wl)
+    o, _ = run_forward(q, k, v, r, bu, bv, M, "bf16", o_dtype="bf16", with_lse=False)
+    assert np.all(np.isfinite(o))
+    # every output row is a convex combination of value rows
+    assert np.abs(o).max() <= np.abs(v).max() * (1 + 2 ** -7)
+    rng = np.random.default_rng(zlib.crc32(f"{name}-{M}".encode()))
+    got, want = [], []
+    for _ in range(6):
+        b = int(rng.integers(0, wl.B))
+        h = int(rng.integers(0, wl.H))
+        rows = _sample_rows(wl.W, rng)
+        eo, _ = O.relattn_rows(q, k, v, r, bu, bv, M, wl.D ** -0.5, b, h, rows)
+        got.append(o[b, rows, h])
+        want.append(eo)
+    assert_bf16_close(np.concatenate(got), np.concatenate(want), f"{name} M={M}")
+
+
+def test_full_size_base_recurrence_sampled(_lib):
+    """Base workload, three segments from empty memory with the GPU roll,
+    sampled rows of every segment against the oracle."""
+    wl = WORKLOADS["base"]
+    S = 3
+    seg = make_segments(wl, n_segments=S)
+    r = project_r(O.sinusoid_rel(wl.M + wl.W, wl.d_model), seg.W_r, wl.H, wl.D, "bf16")
+    L, C = wl.M + wl.W, wl.H * wl.D
+    bufs = [[torch.zeros(wl.B, L, C, device=dev(), dtype=torch.bfloat16) for _ in range(2)] for _ in range(2)]
+    rd = to_dev(r, torch.bfloat16)
+    ud, vd = to_dev(seg.bias_u, torch.float32), to_dev(seg.bias_v, torch.float32)
+    mem_k = np.zeros((wl.B, 0, wl.H, wl.D), np.float32)
+    mem_v = np.zeros((wl.B, 0, wl.H, wl.D), np.float32)
+    rng = np.random.default_rng(5)
+    m_tau = 0
+    for tau in range(S):
+        cur = tau % 2
+        kb, vb = bufs[cur]
+        kb[:, m_tau:m_tau + wl.W] = to_dev(seg.seg("k", tau), torch.bfloat16).view(wl.B, wl.W, C)
+        vb[:, m_tau:m_tau + wl.W] = to_dev(seg.seg("v", tau), torch.bfloat16).view(wl.B, wl.W, C)
+        q = to_dev(seg.seg("q", tau), torch.bfloat16)
+        o = torch.empty(q.shape, device=dev(), dtype=torch.bfloat16)
+        k = kb[:, :m_tau + wl.W].reshape(wl.B, m_tau + wl.W, wl.H, wl.D).contiguous()
+        v = vb[:, :m_tau + wl.W].reshape(wl.B, m_tau + wl.W, wl.H, wl.D).contiguous()
+        _lib.txl_relattn_forward(q, k, v, rd, ud, vd, o, None, M=m_tau)
+        on = o.float().cpu().numpy()
+        kcpu = np.concatenate([mem_k, seg.seg("k", tau)], axis=1)
+        vcpu = np.concatenate([mem_v, seg.seg("v", tau)], axis=1)
+        got, want = [], []
+        for _ in range(4):
+            b, h = int(rng.integers(0, wl.B)), int(rng.integers(0, wl.H))
+            rows = _sample_rows(wl.W, rng)
+            eo, _ = O.relattn_rows(seg.seg("q", tau), kcpu, vcpu, r, seg.bias_u, seg.bias_v, m_tau,
+                                   wl.D ** -0.5, b, h, rows)
+            got.append(on[b, rows, h])
+            want.append(eo)
+        assert_bf16_close(np.concatenate(got), np.concatenate(want), f"segment {tau}")
+        nk, nv = bufs[1 - cur]
+        m_new = _lib.txl_mem_update(kb[:, :m_tau], kb[:, m_tau:m_tau + wl.W], nk, wl.M)
+        _lib.txl_mem_update(vb[:, :m_tau], vb[:, m_tau:m_tau + wl.W], nv, wl.M)
+        mem_k = O.mem_update(mem_k.reshape(wl.B, m_tau, C), seg.seg("k", tau).reshape(wl.B, wl.W, C),
+                             wl.M).reshape(wl.B, -1, wl.H, wl.D)
+        mem_v = O.mem_update(mem_v.reshape(wl.B, m_tau, C), seg.seg("v", tau).reshape(wl.B, wl.W, C),
+                             wl.M).reshape(wl.B, -1, wl.H, wl.D)
+        m_tau = m_new
+        # the GPU roll produced exactly the oracle's memory
+        gk = nk[:, :m_tau].float().cpu().numpy().reshape(wl.B, m_tau, wl.H, wl.D)
+        assert np.array_equal(gk, mem_k)
+    assert _lib.txl_get_device_status() == 0

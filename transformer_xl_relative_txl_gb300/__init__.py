@@ -1,0 +1,177 @@
+"""Transformer-XL relative-position attention for GB300 (sm_103a).
+
+Thin ctypes binding of the C ABI in ``include/txl_relattn.h``: each function
+has the C entry point's name and only marshals torch tensors (device memory,
+CUDA streams) into pointers, sizes and dtype codes.  All computation runs in
+the library's CUDA kernels; there is no fallback.  Importing fails loudly if
+the library has not been built (``python transformer_xl_relative_txl_gb300/build.py``).
+"""
+
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+__all__ = [
+    "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
+    "txl_relattn_forward", "txl_mem_update", "txl_sinusoid_rel",
+    "txl_get_device_status", "txl_status_string", "txl_version",
+    "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
+]
+
+TXL_F32 = 0
+TXL_BF16 = 1
+_STATUS = {0: "TXL_OK", 1: "TXL_ERR_INVALID_ARG", 2: "TXL_ERR_UNSUPPORTED", 3: "TXL_ERR_ALIAS",
+           4: "TXL_ERR_CUDA", 5: "TXL_ERR_DEVICE_TIMEOUT"}
+
+library_path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libtxl_relattn.so")
+if not os.path.exists(library_path):
+    raise ImportError(
+        f"{library_path} is missing: build it with `python transformer_xl_relative_txl_gb300/build.py`")
+lib = ctypes.CDLL(library_path)
+
+_p, _i, _ll, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
+lib.txl_relattn_forward.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
+lib.txl_relattn_forward.restype = _i
+lib.txl_mem_update.argtypes = [_p, _i, _p, _i, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i, _p]
+lib.txl_mem_update.restype = _i
+lib.txl_sinusoid_rel.argtypes = [_p, _i, _i, _i, _p]
+lib.txl_sinusoid_rel.restype = _i
+lib.txl_get_device_status.argtypes = [_p]
+lib.txl_get_device_status.restype = _i
+lib.txl_status_string.argtypes = [_i]
+lib.txl_status_string.restype = ctypes.c_char_p
+lib.txl_version.argtypes = []
+lib.txl_version.restype = _i
+lib.txl_debug_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
+lib.txl_debug_set_wait_limit_ns.restype = _i
+lib.txl_debug_inject_stall.argtypes = [_i]
+lib.txl_debug_inject_stall.restype = _i
+
+
+class TxlError(RuntimeError):
+    """A nonzero txl_status returned by the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {_STATUS.get(status, status)}")
+
+
+def _check(status: int, where: str):
+    if status != 0:
+        raise TxlError(status, where)
+
+
+def _dtype_code(t: torch.dtype) -> int:
+    if t == torch.bfloat16:
+        return TXL_BF16
+    if t == torch.float32:
+        return TXL_F32
+    raise ValueError(f"unsupported dtype {t}")
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("tensors must live in device memory")
+    return t.data_ptr() or None
+
+
+def txl_relattn_forward(q, k, v, r, bias_u, bias_v, o, lse=None, M=None, scale=None, stream=None):
+    """o <- relative attention of q [B,W,H,D] over k, v [B,M+W,H,D] with
+    distance keys r [n_r,H,D] and biases bias_u, bias_v [H,D] (fp32).
+    lse [B,H,W] fp32 is optional.  scale defaults to 1/sqrt(D)."""
+    B, W, H, D = q.shape
+    if M is None:
+        M = k.shape[1] - W
+    for t in (q, k, v, r, bias_u, bias_v, o) + ((lse,) if lse is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k.shape != (B, M + W, H, D) or v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("shape mismatch between q, k, v, o")
+    if r.dim() != 3 or r.shape[1:] != (H, D) or bias_u.shape != (H, D) or bias_v.shape != (H, D):
+        raise ValueError("r must be [n_r, H, D]; biases [H, D]")
+    if bias_u.dtype != torch.float32 or bias_v.dtype != torch.float32:
+        raise ValueError("biases are fp32")
+    if lse is not None and (lse.shape != (B, H, W) or lse.dtype != torch.float32):
+        raise ValueError("lse must be fp32 [B, H, W]")
+    if not (q.dtype == k.dtype == v.dtype == r.dtype):
+        raise ValueError("q, k, v, r must share a dtype")
+    if scale is None:
+        scale = D ** -0.5
+    st = lib.txl_relattn_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(bias_u), _ptr(bias_v), _ptr(o),
+                                 _ptr(lse), B, W, M, H, D, r.shape[0], float(scale), _dtype_code(q.dtype),
+                                 _dtype_code(o.dtype), _stream(stream))
+    _check(st, "txl_relattn_forward")
+    return o
+
+
+def _rows_view(t, name):
+    if t.dim() != 3 or t.stride(2) != 1 or (t.shape[1] > 1 and t.stride(1) != t.shape[2]):
+        raise ValueError(f"{name} must be a [B, rows, C] view with contiguous rows")
+    return t.stride(0)
+
+
+def txl_mem_update(mem, h, mem_out, m, stream=None) -> int:
+    """mem_out[:, :m'] <- last m' = min(m, m_prev + w) rows of [mem ; h].
+
+    mem [B, m_prev, C], h [B, w, C], mem_out [B, >= m', C]: row-contiguous
+    views (batch strides may differ).  Returns m'."""
+    B, m_prev, C = mem.shape
+    w = h.shape[1]
+    if h.shape[0] != B or h.shape[2] != C or mem_out.shape[0] != B or mem_out.shape[2] != C:
+        raise ValueError("mem, h, mem_out disagree on B or C")
+    if not (mem.dtype == h.dtype == mem_out.dtype):
+        raise ValueError("dtype mismatch")
+    mem_bs = _rows_view(mem, "mem")
+    h_bs = _rows_view(h, "h")
+    out_bs = _rows_view(mem_out, "mem_out")
+    keep = min(m, m_prev + w)
+    if mem_out.shape[1] < keep:
+        raise ValueError("mem_out has too few rows")
+    m_out = ctypes.c_int(0)
+    st = lib.txl_mem_update(_ptr(mem) if m_prev > 0 else None, m_prev, _ptr(h) if w > 0 else None, w,
+                            _ptr(mem_out), m, B, C, mem_bs, h_bs, out_bs, ctypes.byref(m_out),
+                            _dtype_code(mem.dtype), _stream(stream))
+    _check(st, "txl_mem_update")
+    return m_out.value
+
+
+def txl_sinusoid_rel(R, stream=None):
+    """R [n_dist, dim] <- sin / cos of distance times 10000^(-2k/dim), interleaved."""
+    if R.dim() != 2 or not R.is_contiguous():
+        raise ValueError("R must be a contiguous [n_dist, dim] tensor")
+    st = lib.txl_sinusoid_rel(_ptr(R), R.shape[0], R.shape[1], _dtype_code(R.dtype), _stream(stream))
+    _check(st, "txl_sinusoid_rel")
+    return R
+
+
+def txl_get_device_status(stream=None) -> int:
+    return lib.txl_get_device_status(_stream(stream))
+
+
+def txl_status_string(status: int) -> str:
+    return lib.txl_status_string(status).decode()
+
+
+def txl_version() -> int:
+    return lib.txl_version()
+
+
+def txl_debug_set_wait_limit_ns(ns: int) -> int:
+    return lib.txl_debug_set_wait_limit_ns(ns)
+
+
+def txl_debug_inject_stall(on: bool) -> int:
+    return lib.txl_debug_inject_stall(1 if on else 0)

@@ -1,0 +1,269 @@
+// C ABI of the library (see include/txl_relattn.h): argument validation,
+// alias checks, TMA descriptor encoding, device status word, dispatch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "txl_internal.h"
+#include "txl_relattn.h"
+
+namespace {
+
+// Device status word: kernels OR error bits into it; read and cleared by
+// txl_get_device_status.
+__device__ unsigned int g_txl_status;
+
+std::atomic<unsigned long long> g_wait_ns{2000000000ULL};
+std::atomic<int> g_inject_stall{0};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+unsigned int* g_status_ptr[kMaxDevices] = {};
+
+cudaError_t status_ptr(unsigned int** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (g_status_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_txl_status);
+    if (e != cudaSuccess) return e;
+    g_status_ptr[dev] = static_cast<unsigned int*>(p);
+  }
+  *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static std::once_flag once;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+size_t dsize(txl_dtype t) { return t == TXL_BF16 ? 2 : 4; }
+bool dtype_ok(int t) { return t == TXL_F32 || t == TXL_BF16; }
+
+struct Range {
+  uintptr_t lo, hi;  // [lo, hi)
+};
+Range range_of(const void* p, size_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+  return Range{a, a + bytes};
+}
+bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi && a.hi > a.lo && b.hi > b.lo; }
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// 2*pi split for the sinusoid's Cody-Waite reduction: c1 and c2 keep few
+// enough significant bits that n*c1 and n*c2 are exact for every multiple n
+// the table can need; c3 carries the rest.
+void two_pi_split(int n_dist, float* c1, float* c2, float* c3) {
+  const double two_pi = 6.283185307179586476925286766559;
+  int nbits = 1;
+  while (std::ldexp(1.0, nbits) < static_cast<double>(n_dist) / two_pi + 2.0) ++nbits;
+  int keep = 24 - nbits;
+  if (keep < 1) keep = 1;
+  auto keep_bits = [](double x, int bits) {
+    float f = static_cast<float>(x);
+    uint32_t u;
+    std::memcpy(&u, &f, 4);
+    const int drop = 24 - bits;
+    if (drop > 0) u &= ~((1u << drop) - 1u);
+    std::memcpy(&f, &u, 4);
+    return f;
+  };
+  *c1 = keep_bits(two_pi, keep);
+  *c2 = keep_bits(two_pi - static_cast<double>(*c1), keep);
+  *c3 = static_cast<float>(two_pi - static_cast<double>(*c1) - static_cast<double>(*c2));
+}
+
+int from_cuda(cudaError_t e) { return e == cudaSuccess ? TXL_OK : TXL_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+int txl_version(void) { return TXL_VERSION; }
+
+const char* txl_status_string(int status) {
+  switch (status) {
+    case TXL_OK: return "TXL_OK";
+    case TXL_ERR_INVALID_ARG: return "TXL_ERR_INVALID_ARG";
+    case TXL_ERR_UNSUPPORTED: return "TXL_ERR_UNSUPPORTED";
+    case TXL_ERR_ALIAS: return "TXL_ERR_ALIAS";
+    case TXL_ERR_CUDA: return "TXL_ERR_CUDA";
+    case TXL_ERR_DEVICE_TIMEOUT: return "TXL_ERR_DEVICE_TIMEOUT";
+    default: return "TXL_ERR_UNKNOWN";
+  }
+}
+
+int txl_debug_set_wait_limit_ns(unsigned long long ns) {
+  if (ns < 1000ULL) return TXL_ERR_INVALID_ARG;
+  g_wait_ns.store(ns);
+  return TXL_OK;
+}
+
+int txl_debug_inject_stall(int on) {
+  g_inject_stall.store(on ? 1 : 0);
+  return TXL_OK;
+}
+
+int txl_get_device_status(cudaStream_t stream) {
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return TXL_ERR_CUDA;
+  unsigned int* p = nullptr;
+  if (status_ptr(&p) != cudaSuccess) return TXL_ERR_CUDA;
+  unsigned int v = 0;
+  if (cudaMemcpy(&v, p, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return TXL_ERR_CUDA;
+  if (v != 0) {
+    const unsigned int zero = 0;
+    if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TXL_ERR_CUDA;
+  }
+  return (v & txl::kStatusTimeoutBit) ? TXL_ERR_DEVICE_TIMEOUT : TXL_OK;
+}
+
+int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cudaStream_t stream) {
+  if (n_dist < 0 || dim < 2 || (dim % 2) != 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
+  if (n_dist == 0) return TXL_OK;
+  if (R == nullptr || !aligned(R, 2 * dsize(dtype))) return TXL_ERR_INVALID_ARG;
+  if (n_dist > (1 << 24)) return TXL_ERR_UNSUPPORTED;  // distances must stay exact in fp32
+  float c1, c2, c3;
+  two_pi_split(n_dist, &c1, &c2, &c3);
+  return from_cuda(txl::launch_sinusoid(R, n_dist, dim, dtype == TXL_BF16, c1, c2, c3, stream));
+}
+
+int txl_mem_update(const void* mem, int m_prev, const void* h, int w, void* mem_out, int m, int B, int C,
+                   long long mem_bs, long long h_bs, long long out_bs, int* m_out, txl_dtype dtype,
+                   cudaStream_t stream) {
+  if (B < 0 || m_prev < 0 || w < 0 || m < 0 || C <= 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
+  const long long keep = std::min<long long>(m, static_cast<long long>(m_prev) + w);
+  if (m_out != nullptr) *m_out = static_cast<int>(keep);
+  if (B == 0 || keep == 0) return TXL_OK;
+  if (B > 65535) return TXL_ERR_UNSUPPORTED;
+  const long long from_h = std::min<long long>(keep, w);
+  const long long from_mem = keep - from_h;
+  if (mem_out == nullptr) return TXL_ERR_INVALID_ARG;
+  if (from_mem > 0 && mem == nullptr) return TXL_ERR_INVALID_ARG;
+  if (from_h > 0 && h == nullptr) return TXL_ERR_INVALID_ARG;
+  const long long es = static_cast<long long>(dsize(dtype));
+  if (B > 1 && (mem_bs < static_cast<long long>(m_prev) * C || h_bs < static_cast<long long>(w) * C ||
+                out_bs < keep * C))
+    return TXL_ERR_INVALID_ARG;
+  if (mem_bs < 0 || h_bs < 0 || out_bs < 0) return TXL_ERR_INVALID_ARG;
+  const long long row_bytes = static_cast<long long>(C) * es;
+  // Extents actually read / written (all batches).
+  const Range out_r = range_of(mem_out, static_cast<size_t>((B - 1) * out_bs * es + keep * row_bytes));
+  if (from_mem > 0) {
+    const char* src = static_cast<const char*>(mem) + (m_prev - from_mem) * row_bytes;
+    if (overlap(out_r, range_of(src, static_cast<size_t>((B - 1) * mem_bs * es + from_mem * row_bytes))))
+      return TXL_ERR_ALIAS;
+  }
+  if (from_h > 0) {
+    const char* src = static_cast<const char*>(h) + (w - from_h) * row_bytes;
+    if (overlap(out_r, range_of(src, static_cast<size_t>((B - 1) * h_bs * es + from_h * row_bytes))))
+      return TXL_ERR_ALIAS;
+  }
+  return from_cuda(txl::launch_mem_roll(mem, h, mem_out, B, keep, from_mem, m_prev - from_mem, w - from_h,
+                                        row_bytes, mem_bs * es, h_bs * es, out_bs * es, stream));
+}
+
+int txl_relattn_forward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                        const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r,
+                        float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {
+  if (B < 0 || W < 0 || M < 0 || H <= 0 || D <= 0 || !dtype_ok(dtype) || !dtype_ok(o_dtype))
+    return TXL_ERR_INVALID_ARG;
+  if (B == 0 || W == 0) return TXL_OK;
+  if (q == nullptr || k == nullptr || v == nullptr || r == nullptr || bias_u == nullptr || bias_v == nullptr ||
+      o == nullptr)
+    return TXL_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_r) < static_cast<long long>(M) + W) return TXL_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return TXL_ERR_INVALID_ARG;
+  const size_t in_align = (dtype == TXL_BF16) ? 16 : 4;
+  if (!aligned(q, in_align) || !aligned(k, in_align) || !aligned(v, in_align) || !aligned(r, in_align) ||
+      !aligned(o, 16) || !aligned(bias_u, 4) || !aligned(bias_v, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return TXL_ERR_INVALID_ARG;
+
+  const long long L = static_cast<long long>(M) + W;
+  const size_t es = dsize(dtype);
+  const size_t hd = static_cast<size_t>(H) * D;
+  const Range rq = range_of(q, B * static_cast<size_t>(W) * hd * es);
+  const Range rk = range_of(k, B * static_cast<size_t>(L) * hd * es);
+  const Range rv = range_of(v, B * static_cast<size_t>(L) * hd * es);
+  const Range rr = range_of(r, static_cast<size_t>(n_r) * hd * es);
+  const Range ru = range_of(bias_u, hd * 4);
+  const Range rb = range_of(bias_v, hd * 4);
+  const Range ro = range_of(o, B * static_cast<size_t>(W) * hd * dsize(o_dtype));
+  for (Range x : {rq, rk, rv, rr, ru, rb})
+    if (overlap(ro, x)) return TXL_ERR_ALIAS;
+  if (lse != nullptr) {
+    const Range rl = range_of(lse, B * static_cast<size_t>(H) * W * 4);
+    for (Range x : {rq, rk, rv, rr, ru, rb, ro})
+      if (overlap(rl, x)) return TXL_ERR_ALIAS;
+  }
+
+  if (dtype == TXL_F32) {
+    if (o_dtype != TXL_F32 || D > 256 || B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
+    if (sizeof(float) * (2 * static_cast<size_t>(D) + L) > 220 * 1024) return TXL_ERR_UNSUPPORTED;
+    return from_cuda(txl::launch_relattn_f32(
+        static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
+        static_cast<const float*>(r), bias_u, bias_v, static_cast<float*>(o), lse, B, W, M, H, D, scale,
+        stream));
+  }
+
+  // bf16 tensor-core path
+  if (D != 64 && D != 128) return TXL_ERR_UNSUPPORTED;
+  const long long nqt = (W + 127) / 128;
+  if (nqt * B * H > 0x7FFFFFFFLL || L > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return TXL_ERR_CUDA;
+  CUtensorMap tm_k, tm_v, tm_r;
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(L) * hd * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    if (encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TXL_ERR_CUDA;
+    if (encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TXL_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(n_r)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, hd * 2};
+    const cuuint32_t box[3] = {64, 1, 128};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    if (encode(&tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(r), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+      return TXL_ERR_CUDA;
+  }
+  txl::WaitCtl wc;
+  if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
+  wc.limit_ns = g_wait_ns.load();
+  wc.inject_stall = g_inject_stall.exchange(0);
+  return from_cuda(txl::launch_relattn_tc(tm_k, tm_v, tm_r, q, bias_u, bias_v, o, lse, B, W, M, H, D,
+                                          o_dtype == TXL_BF16, scale, wc, stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,42 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Arguments are validated by the caller.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace txl {
+
+// Bits of the device status word.
+constexpr unsigned int kStatusTimeoutBit = 1u;  // a bounded wait expired
+
+struct WaitCtl {
+  unsigned int* status;           // device status word
+  unsigned long long limit_ns;    // bound of every wait
+  int inject_stall;               // loader stops after the first key tile
+};
+
+// Sinusoidal distance table.  c1..c3: 2*pi split into three floats whose
+// products with small integers are exact (Cody-Waite reduction constants).
+cudaError_t launch_sinusoid(void* R, int n_dist, int dim, bool bf16, float c1, float c2, float c3,
+                            cudaStream_t stream);
+
+// Memory roll over raw bytes.
+cudaError_t launch_mem_roll(const void* mem, const void* h, void* out, int B, long long rows_out,
+                            long long n_from_mem, long long mem_row0, long long h_row0, long long row_bytes,
+                            long long mem_bs_bytes, long long h_bs_bytes, long long out_bs_bytes,
+                            cudaStream_t stream);
+
+// Exact fp32 relative attention (CUDA cores).
+cudaError_t launch_relattn_f32(const float* q, const float* k, const float* v, const float* r,
+                               const float* bias_u, const float* bias_v, float* o, float* lse, int B,
+                               int W, int M, int H, int D, float scale, cudaStream_t stream);
+
+// bf16 tensor-core relative attention (tcgen05 + TMEM + TMA).
+cudaError_t launch_relattn_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_r,
+                              const void* q, const float* bias_u, const float* bias_v, void* o,
+                              float* lse, int B, int W, int M, int H, int D, bool o_bf16, float scale,
+                              const WaitCtl& wc, cudaStream_t stream);
+
+}  // namespace txl
