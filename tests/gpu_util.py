@@ -29,7 +29,8 @@ def torch_dtype(name):
 
 
 def workload(B, H, D, W, M, dtype="bf16", cfg_id=100):
-    return Workload(f"t{B}x{H}x{D}x{W}x{M}", cfg_id, B, H, D, H * D, W, M, 1, dtype)
+    d_model = H * D + (H * D) % 2  # the sinusoid width must be even
+    return Workload(f"t{B}x{H}x{D}x{W}x{M}", cfg_id, B, H, D, d_model, W, M, 1, dtype)
 
 
 def prefilled_case(wl, seed=0, n_r_extra=0):

@@ -144,7 +144,11 @@ int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cudaStream_t
   if (n_dist > (1 << 24)) return TXL_ERR_UNSUPPORTED;  // distances must stay exact in fp32
   float c1, c2, c3;
   two_pi_split(n_dist, &c1, &c2, &c3);
-  return from_cuda(txl::launch_sinusoid(R, n_dist, dim, dtype == TXL_BF16, c1, c2, c3, stream));
+  const double rho = std::pow(10000.0, -2.0 / static_cast<double>(dim));
+  const float rho_hi = static_cast<float>(rho);
+  const float rho_lo = static_cast<float>(rho - static_cast<double>(rho_hi));
+  return from_cuda(
+      txl::launch_sinusoid(R, n_dist, dim, dtype == TXL_BF16, rho_hi, rho_lo, c1, c2, c3, stream));
 }
 
 int txl_mem_update(const void* mem, int m_prev, const void* h, int w, void* mem_out, int m, int B, int C,
@@ -231,38 +235,41 @@ int txl_relattn_forward(const void* q, const void* k, const void* v, const void*
   if (nqt * B * H > 0x7FFFFFFFLL || L > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return TXL_ERR_CUDA;
-  CUtensorMap tm_k, tm_v, tm_r;
+  CUtensorMap tm_q, tm_k, tm_v, tm_r;
+  auto encode_bf16 = [&](CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                         const cuuint64_t* strides, const cuuint32_t* box) {
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(W) * hd * 2};
+    const cuuint32_t box[4] = {64, 1, 128, 1};
+    if (!encode_bf16(&tm_q, q, 4, dims, strides, box)) return TXL_ERR_CUDA;
+  }
   {
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
     const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(L) * hd * 2};
-    const cuuint32_t box[4] = {64, 1, 128, 1};
-    const cuuint32_t estr[4] = {1, 1, 1, 1};
-    if (encode(&tm_k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(k), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return TXL_ERR_CUDA;
-    if (encode(&tm_v, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(v), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    const cuuint32_t box[4] = {64, 1, 64, 1};
+    if (!encode_bf16(&tm_k, k, 4, dims, strides, box) || !encode_bf16(&tm_v, v, 4, dims, strides, box))
       return TXL_ERR_CUDA;
   }
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                                 static_cast<cuuint64_t>(n_r)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, hd * 2};
-    const cuuint32_t box[3] = {64, 1, 128};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    if (encode(&tm_r, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(r), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
-      return TXL_ERR_CUDA;
+    const cuuint32_t box[3] = {64, 1, 64};
+    if (!encode_bf16(&tm_r, r, 3, dims, strides, box)) return TXL_ERR_CUDA;
   }
   txl::WaitCtl wc;
   if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
   wc.limit_ns = g_wait_ns.load();
   wc.inject_stall = g_inject_stall.exchange(0);
-  return from_cuda(txl::launch_relattn_tc(tm_k, tm_v, tm_r, q, bias_u, bias_v, o, lse, B, W, M, H, D,
+  return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H, D,
                                           o_dtype == TXL_BF16, scale, wc, stream));
 }
 

@@ -8,36 +8,47 @@
 // [memory ; segment], queries from the segment, the four-term relative score
 // (grouped here by its query-side factor), and the distance term computed once
 // against every distance and shifted into place per row.  The shift is an
-// index, not a pad-and-reshape: row a of a 128-query tile against key tile t
-// needs distances base_t + a - c (c = key column, base_t = M + i0 - 128 t),
-// which all lie in two 128-distance tiles [base_t - 128, base_t) and
-// [base_t, base_t + 128).  Consecutive key tiles share one of them, so each
-// step issues one new 128x128 distance MMA into a two-slot TMEM ring and the
+// index, not a pad-and-reshape: for query row a of a 128-row tile and key
+// column c of the 64-key step t, the distance is base_t + a - c with
+// base_t = M + i0 - 64 t.  The distances one step needs span three 64-row
+// tiles of r; consecutive steps share two of them, so each step computes one
+// new 128x64 distance tile G = (q+v) r^T into a three-slot TMEM ring and the
 // distance work equals the content work (step 5: "the cost stays that of
-// ordinary attention").
+// ordinary attention").  Each softmax thread reads its 64-distance window of
+// the ring at a warp-uniform column, packs it to bf16 pairs and applies the
+// remaining per-lane offset (0..31) with a five-stage select network on the
+// packed registers plus one byte permute for the odd half; the shifted term
+// is then added to the content score in mixed precision (fp32 + bf16).
 //
-// CTA = one (batch, head, 128-query tile); 6 warps:
-//   warps 0-3  softmax: thread a owns query row a (TMEM lane a).  Builds the
-//              bf16 (q+u) and (q+v) tiles in shared memory, then per key tile
-//              reads S and its 159-distance window of the ring, shifts the
-//              window per lane (5-stage select network, the lane-dependent
-//              part of the index), adds, masks j > M+i, runs the online
-//              softmax, rescales O when the row max grows, writes P (bf16)
-//              over the S columns, and finally normalises O and stores o, lse.
-//   warp 4     loader: TMA tile loads of K, V (4-D maps, zero fill past M+W)
-//              and R (3-D map, zero fill outside [0, n_r)) into 128B-swizzled
-//              stage rings.
-//   warp 5     MMA issuer (one thread): S = (q+u) K^T, G_t = (q+v) R_t^T into
-//              the ring, O += P V with P read from TMEM; tcgen05.commit
-//              signals the barriers.  Also owns the TMEM allocation.
+// Persistent CTAs (one per SM) walk the (batch, head, query tile) units in
+// longest-first order.  Per CTA, 11 warps:
+//   warps 0-7  softmax.  Thread (warp w, lane l) owns query row 32*(w%4)+l
+//              (its TMEM lane); warps 0-3 take key columns 0-31 of each step,
+//              warps 4-7 columns 32-63, and the two halves exchange their row
+//              maxima through shared memory (mbarrier hand-over, bounded).
+//              Lazy rescaling: the running max only moves when a row max
+//              exceeds it by 2^8, and then warps 0-3 rescale their O rows.
+//              Warps 4-7 also build the next unit's (q+u), (q+v) operands
+//              while warps 0-3 normalise and store this unit's output.
+//   warp 8     loader: TMA tile loads of q (128 rows), K, V (64 rows) and R
+//              (64 distances) into 128B-swizzled shared-memory rings; zero
+//              fill outside the tensors.
+//   warp 9     score MMA issuer: S_t = (q+u) K_t^T into one of two S buffers
+//              as soon as the softmax has read the previous occupant, G into
+//              the ring once its slot is released; runs up to one step ahead
+//              of the softmax.
+//   warp 10    PV MMA issuer: O += P_t V_t when P_t is ready.  Two issuing
+//              threads on different schedulers keep each serial chain of
+//              waits, MMAs and commits short; each commits its own MMAs.
 //
-// TMEM (512 columns): S / P [0,128) | ring slot 0 [128,256) | slot 1
-// [256,384) | O [384, 384+D).
+// TMEM (512 columns): D = 64: (q+u) [0,32) (q+v) [32,64) O [64,128);
+// D = 128: O [0,128) with (q+u), (q+v) in shared memory.  Both: P0, P1
+// [128,192) (bf16 pairs), S0, S1 [192,320), distance ring [320,512).
 //
 // Every wait is bounded (globaltimer); a wait that runs out raises a CTA
-// abort flag and the device status word, and every role unwinds: the loader
-// waits for its own copies in flight, the MMA thread for its own MMAs, and
-// the TMEM is freed before exit.
+// abort flag and the device status word, every role unwinds (the loader and
+// the MMA thread wait for their own operations in flight) and the TMEM is
+// freed before exit.
 #include <cmath>
 #include <cstdint>
 
@@ -47,119 +58,206 @@
 namespace txl {
 namespace {
 
-constexpr int BM = 128;         // query rows per CTA
-constexpr int BN = 128;         // keys per step
-constexpr int kThreads = 192;
-constexpr int kLoaderWarp = 4;
-constexpr int kMmaWarp = 5;
-constexpr uint32_t kColS = 0;
-constexpr uint32_t kColG0 = 128;
-constexpr uint32_t kColG1 = 256;
-constexpr uint32_t kColO = 384;
+constexpr int BM = 128;  // query rows per unit (TMEM lanes)
+constexpr int BN = 64;   // keys per step, distances per ring tile
+constexpr int kLoaderWarp = 8;
+constexpr int kMmaWarp = 9;   // S = (q+u)K^T and G = (q+v)R^T issuer; owns the TMEM allocation
+constexpr int kPvWarp = 10;   // O += P V issuer
+constexpr int kThreads = 352;
+constexpr uint32_t kColP = 128;  // P0, P1: 32 columns each
+constexpr uint32_t kColS = 192;  // S0, S1: 64 columns each
+constexpr uint32_t kColG = 320;  // distance ring: 3 slots of 64 columns
+constexpr int kSlots = 3;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kChunkBytes = BM * 64 * 2;  // one 128-row x 64-element bf16 block (16 KB)
+constexpr float kLazy = 8.0f;  // log2 headroom before the running max moves
 
 template <int D>
 struct Cfg {
+  static constexpr bool kQTmem = (D == 64);
   static constexpr int kChunks = D / 64;
-  static constexpr int kTileBytes = BM * D * 2;
-  static constexpr int NK = (D == 64) ? 2 : 1;
-  static constexpr int NV = (D == 64) ? 2 : 1;
-  static constexpr int NR = 2;
-  static constexpr int kOffQu = 0;
-  static constexpr int kOffQv = kOffQu + kTileBytes;
-  static constexpr int kOffK = kOffQv + kTileBytes;
-  static constexpr int kOffV = kOffK + NK * kTileBytes;
-  static constexpr int kOffR = kOffV + NV * kTileBytes;
-  static constexpr int kOffBar = kOffR + NR * kTileBytes;
-  static constexpr int kBarBytes = 256;
+  static constexpr int kRowChunk = BN * 128;          // 64 rows x 128 B
+  static constexpr int kRowTile = kChunks * kRowChunk;
+  static constexpr int kQChunk = BM * 128;            // 128 rows x 128 B
+  static constexpr int kQTile = kChunks * kQChunk;
+  static constexpr int NK = (D == 64) ? 4 : 2;
+  static constexpr int NV = (D == 64) ? 4 : 2;
+  static constexpr int NR = (D == 64) ? 4 : 2;
+  static constexpr int NQ = (D == 64) ? 2 : 1;
+  static constexpr uint32_t kColQu = 0, kColQv = 32;  // D == 64
+  static constexpr uint32_t kColO = kQTmem ? 64 : 0;
+  static constexpr int kOffQ = 0;
+  static constexpr int kOffQu = kOffQ + NQ * kQTile;  // D == 128: (q+u), (q+v) tiles
+  static constexpr int kOffQv = kOffQu + (kQTmem ? 0 : kQTile);
+  static constexpr int kOffK = kOffQv + (kQTmem ? 0 : kQTile);
+  static constexpr int kOffV = kOffK + NK * kRowTile;
+  static constexpr int kOffR = kOffV + NV * kRowTile;
+  static constexpr int kOffRed = kOffR + NR * kRowTile;
+  static constexpr int kRedFloats = 2 * 2 * BM + 2 * BM;  // [step parity][half][row] maxima, [unit parity][row] sums
+  static constexpr int kOffBar = kOffRed + kRedFloats * 4;
+  static constexpr int kBarBytes = 512;
   static constexpr int kSmemBytes = kOffBar + kBarBytes + 1024;  // + alignment slack
 };
 
 struct Params {
-  const __nv_bfloat16* q;
   const float* bias_u;
   const float* bias_v;
   void* o;
   float* lse;
   int B, W, M, H;
-  float scale_log2e;
+  int nqt, n_units;
+  float scale_log2e;  // |scale| * log2(e)
+  float qsign;        // sign of scale, folded into (q+u), (q+v)
   unsigned int* status;
   unsigned long long wait_ns;
   int inject_stall;
 };
 
-// Barrier block layout (8-byte slots) after the tiles.
 struct Bars {
-  uint64_t fullK[2], emptyK[2], fullV[2], emptyV[2], fullR[2], emptyR[2];
-  uint64_t q_ready, s_full, p_full, o_done, mma_final;
+  uint64_t fullK[4], emptyK[4], fullV[4], emptyV[4], fullR[4], emptyR[4];
+  uint64_t q_full[2], q_empty[2];
+  uint64_t q_ready, s_full[2], s_free[2], p_full[2], pv_done[2], o_full, o_free, g_free[kSlots], mma_final,
+      pv_final;
+  uint64_t xbar[4];  // row-max exchange of warps quad and quad+4 (64 arrivals per step)
+  uint64_t lbar[4];  // row-sum hand-over at the end of a unit (32 arrivals)
   uint32_t tmem_base;
   int abort;
 };
-static_assert(sizeof(Bars) <= 256, "barrier block too large");
+static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
-// Five-stage select network: on return arr[m] == in[m + sh] for m in [1, 32],
-// where in[] is the original arr[0..63] and 0 <= sh < 32 differs per lane.
-__device__ __forceinline__ void lane_shift(float (&arr)[64], int sh) {
-  const bool b16 = sh & 16, b8 = sh & 8, b4 = sh & 4, b2 = sh & 2, b1 = sh & 1;
+struct Unit {
+  int b, h, i0, nks;
+};
+
+__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
+  const int BH = p.B * p.H;
+  const int qt = p.nqt - 1 - u / BH;  // longest query tiles first
+  const int bh = u % BH;
+  Unit r;
+  r.b = bh / p.H;
+  r.h = bh % p.H;
+  r.i0 = qt * BM;
+  const int kmax = min(p.M + r.i0 + BM - 1, p.M + p.W - 1);
+  r.nks = kmax / BN + 1;
+  return r;
+}
+
+__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
+// fp32 + bf16 (low or high half of a packed pair), one rounding.
+__device__ __forceinline__ float add_bf16lo(uint32_t pk, float s) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
+      : "=f"(r) : "r"(pk), "f"(s));
+  return r;
+}
+__device__ __forceinline__ float add_bf16hi(uint32_t pk, float s) {
+  float r;
+  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
+      : "=f"(r) : "r"(pk), "f"(s));
+  return r;
+}
+
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Per-lane window shift.  x0, x1 hold the fp32 window X[0..63]; on return
+// out[j] packs (Y[2j], Y[2j+1]) as bf16 (low half first) with
+// Y[k] = X[lane + 1 + k], k = 0..31.  The window is packed to bf16 pairs,
+// shifted by whole registers with a five-stage select network on
+// (lane + 1) / 2, and the odd half-register shift is one byte permute.
+__device__ __forceinline__ void window_shift(const uint32_t (&x0)[32], const uint32_t (&x1)[32], int lane,
+                                             uint32_t (&out)[16]) {
+  uint32_t R[32];
 #pragma unroll
-  for (int m = 1; m <= 47; ++m) arr[m] = b16 ? arr[m + 16] : arr[m];
+  for (int i = 0; i < 16; ++i) {
+    R[i] = pack_bf16x2(__uint_as_float(x0[2 * i]), __uint_as_float(x0[2 * i + 1]));
+    R[16 + i] = pack_bf16x2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1]));
+  }
+  const int sh = lane + 1;
+  const int q = sh >> 1;
+  const bool b16 = q & 16, b8 = q & 8, b4 = q & 4, b2 = q & 2, b1 = q & 1;
 #pragma unroll
-  for (int m = 1; m <= 39; ++m) arr[m] = b8 ? arr[m + 8] : arr[m];
+  for (int j = 0; j <= 15; ++j) R[j] = b16 ? R[j + 16] : R[j];
 #pragma unroll
-  for (int m = 1; m <= 35; ++m) arr[m] = b4 ? arr[m + 4] : arr[m];
+  for (int j = 0; j <= 23; ++j) R[j] = b8 ? R[j + 8] : R[j];
 #pragma unroll
-  for (int m = 1; m <= 33; ++m) arr[m] = b2 ? arr[m + 2] : arr[m];
+  for (int j = 0; j <= 19; ++j) R[j] = b4 ? R[j + 4] : R[j];
 #pragma unroll
-  for (int m = 1; m <= 32; ++m) arr[m] = b1 ? arr[m + 1] : arr[m];
+  for (int j = 0; j <= 17; ++j) R[j] = b2 ? R[j + 2] : R[j];
+#pragma unroll
+  for (int j = 0; j <= 16; ++j) R[j] = b1 ? R[j + 1] : R[j];
+  const uint32_t sel = (sh & 1) ? 0x5432u : 0x3210u;
+#pragma unroll
+  for (int j = 0; j < 16; ++j) out[j] = byte_perm(R[j], R[j + 1], sel);
+}
+
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t ns, volatile int* abort) {
+  const bool got = mbar_wait(bar, parity, ns, abort);
+  return __all_sync(0xffffffffu, got);
+}
+
+// Elected-lane arrive after every lane's tcgen05 accesses are complete.
+__device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
+  tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
 template <int D, bool O_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
-    relattn_tc_kernel(const __grid_constant__ CUtensorMap tm_k, const __grid_constant__ CUtensorMap tm_v,
-                      const __grid_constant__ CUtensorMap tm_r, const Params p) {
+    relattn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
+                      const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
+  uint8_t* sQ = smem + C::kOffQ;
   uint8_t* sQu = smem + C::kOffQu;
   uint8_t* sQv = smem + C::kOffQv;
   uint8_t* sK = smem + C::kOffK;
   uint8_t* sV = smem + C::kOffV;
   uint8_t* sR = smem + C::kOffR;
+  float* red = reinterpret_cast<float*>(smem + C::kOffRed);
+  float* lred = red + 2 * 2 * BM;
   Bars* bars = reinterpret_cast<Bars*>(smem + C::kOffBar);
   volatile int* abort = &bars->abort;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
-  // ---- work unit: longest query tiles first --------------------------------
-  const int nqt = (p.W + BM - 1) / BM;
-  const int BH = p.B * p.H;
-  const int qt = nqt - 1 - static_cast<int>(blockIdx.x / BH);
-  const int bh = static_cast<int>(blockIdx.x % BH);
-  const int b = bh / p.H;
-  const int h = bh % p.H;
-  const int i0 = qt * BM;
-  const int L = p.M + p.W;
-  const int kmax = min(p.M + i0 + BM - 1, L - 1);
-  const int nkt = kmax / BN + 1;
-
-  // ---- setup ---------------------------------------------------------------
   if (threadIdx.x == 0) {
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 4; ++s) {
       mbar_init(&bars->fullK[s], 1);
       mbar_init(&bars->emptyK[s], 1);
       mbar_init(&bars->fullV[s], 1);
       mbar_init(&bars->emptyV[s], 1);
       mbar_init(&bars->fullR[s], 1);
       mbar_init(&bars->emptyR[s], 1);
+      if (s < kSlots) mbar_init(&bars->g_free[s], 8);
+      mbar_init(&bars->xbar[s], 64);
+      mbar_init(&bars->lbar[s], 32);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 128);
+      mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->s_free[s], 8);
+      mbar_init(&bars->p_full[s], 8);
+      mbar_init(&bars->pv_done[s], 1);
     }
     mbar_init(&bars->q_ready, 128);
-    mbar_init(&bars->s_full, 1);
-    mbar_init(&bars->p_full, 128);
-    mbar_init(&bars->o_done, 1);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_free, 4);
     mbar_init(&bars->mma_final, 1);
+    mbar_init(&bars->pv_final, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -174,283 +272,379 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t wait_ns = p.wait_ns;
 
   if (warp == kLoaderWarp) {
-    // ======================= TMA loader ====================================
+    // ============================ TMA loader ===============================
     if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
       tma_prefetch_desc(&tm_k);
       tma_prefetch_desc(&tm_v);
       tma_prefetch_desc(&tm_r);
-      int nK = 0, nV = 0, nR = 0;
-      bool ok = true;
-      auto load_r = [&](int d0) -> bool {
-        const int s = nR % C::NR;
-        if (!mbar_wait(&bars->emptyR[s], ((nR / C::NR) & 1) ^ 1, wait_ns, abort)) return false;
-        mbar_arrive_expect_tx(&bars->fullR[s], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_3d(sR + s * C::kTileBytes + c * kChunkBytes, &tm_r, &bars->fullR[s], c * 64, h, d0);
-        ++nR;
+      uint32_t nQ = 0, nK = 0, nV = 0, nR = 0;
+      bool ok = true, stop = false;
+      auto acquire = [&](uint64_t* empty, uint64_t* full, uint32_t n, int ns, int bytes) -> bool {
+        const int s = static_cast<int>(n % ns);
+        if (!mbar_wait(&empty[s], ((n / ns) & 1) ^ 1, wait_ns, abort)) return false;
+        mbar_arrive_expect_tx(&full[s], bytes);
         return true;
       };
-      auto load_k = [&](int t) -> bool {
-        const int s = nK % C::NK;
-        if (!mbar_wait(&bars->emptyK[s], ((nK / C::NK) & 1) ^ 1, wait_ns, abort)) return false;
-        mbar_arrive_expect_tx(&bars->fullK[s], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sK + s * C::kTileBytes + c * kChunkBytes, &tm_k, &bars->fullK[s], c * 64, h, t * BN, b);
-        ++nK;
-        return true;
-      };
-      auto load_v = [&](int t) -> bool {
-        const int s = nV % C::NV;
-        if (!mbar_wait(&bars->emptyV[s], ((nV / C::NV) & 1) ^ 1, wait_ns, abort)) return false;
-        mbar_arrive_expect_tx(&bars->fullV[s], C::kTileBytes);
-        for (int c = 0; c < C::kChunks; ++c)
-          tma_load_4d(sV + s * C::kTileBytes + c * kChunkBytes, &tm_v, &bars->fullV[s], c * 64, h, t * BN, b);
-        ++nV;
-        return true;
-      };
-      ok = load_r(p.M + i0);  // hi tile of the first step
-      for (int t = 0; ok && t < nkt; ++t) {
-        if (p.inject_stall && t == 1) break;  // test hook: starve the consumers
-        ok = load_k(t) && load_r(p.M + i0 - BN * (t + 1)) && load_v(t);
+      for (int u = blockIdx.x; ok && !stop && u < p.n_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        {
+          if (!(ok = acquire(bars->q_empty, bars->q_full, nQ, C::NQ, C::kQTile))) break;
+          const int s = nQ % C::NQ;
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(sQ + s * C::kQTile + c * C::kQChunk, &tm_q, &bars->q_full[s], c * 64, w.h, w.i0, w.b);
+          ++nQ;
+        }
+        auto load_r = [&](int d0) -> bool {
+          if (!acquire(bars->emptyR, bars->fullR, nR, C::NR, C::kRowTile)) return false;
+          const int s = nR % C::NR;
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_3d(sR + s * C::kRowTile + c * C::kRowChunk, &tm_r, &bars->fullR[s], c * 64, w.h, d0);
+          ++nR;
+          return true;
+        };
+        auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, int ns,
+                           const CUtensorMap* map, int t) -> bool {
+          if (!acquire(empty, full, n, ns, C::kRowTile)) return false;
+          const int s = n % ns;
+          for (int c = 0; c < C::kChunks; ++c)
+            tma_load_4d(dst + s * C::kRowTile + c * C::kRowChunk, map, &full[s], c * 64, w.h, t * BN, w.b);
+          ++n;
+          return true;
+        };
+        ok = load_r(p.M + w.i0 + BN) && load_r(p.M + w.i0);  // distance tiles -2 and -1
+        for (int t = 0; ok && t < w.nks; ++t) {
+          if (p.inject_stall && t == 1) {  // test hook: starve the consumers
+            stop = true;
+            break;
+          }
+          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, C::NK, &tm_k, t) && load_r(p.M + w.i0 - BN * (t + 1)) &&
+               load_kv(bars->emptyV, bars->fullV, sV, nV, C::NV, &tm_v, t);
+        }
       }
       if (!ok) report_timeout(abort, p.status);
-      // Wait for this thread's own copies in flight before the CTA may exit.
-      auto drain = [&](uint64_t* full, int n, int ns) {
-        for (int s = 0; s < ns && s < n; ++s) {
-          const int last = s + ((n - 1 - s) / ns) * ns;
+      // Let this thread's own copies land before the CTA may exit.
+      auto drain = [&](uint64_t* full, uint32_t n, int ns) {
+        for (int s = 0; s < ns && static_cast<uint32_t>(s) < n; ++s) {
+          const uint32_t last = s + ((n - 1 - s) / ns) * ns;
           mbar_wait_own(&full[s], (last / ns) & 1, wait_ns);
         }
       };
+      drain(bars->q_full, nQ, C::NQ);
       drain(bars->fullK, nK, C::NK);
       drain(bars->fullV, nV, C::NV);
       drain(bars->fullR, nR, C::NR);
     }
   } else if (warp == kMmaWarp) {
-    // ======================= MMA issuer ====================================
+    // ============================ MMA issuer ===============================
     if (lane == 0) {
-      constexpr uint32_t idesc_s = idesc_bf16(128, 128, false, false);
-      constexpr uint32_t idesc_o = idesc_bf16(128, D, false, true);
-      const uint32_t aQu = smem_u32(sQu), aQv = smem_u32(sQv);
-      const uint32_t aK = smem_u32(sK), aV = smem_u32(sV), aR = smem_u32(sR);
-      bool ok = mbar_wait(&bars->q_ready, 0, wait_ns, abort);
-      tc_fence_after();
-      int nR = 0;
-      for (int t = 0; ok && t < nkt; ++t) {
-        const int sk = t % C::NK;
-        ok = mbar_wait(&bars->fullK[sk], (t / C::NK) & 1, wait_ns, abort);
-        if (ok && t > 0) ok = mbar_wait(&bars->o_done, (t - 1) & 1, wait_ns, abort);  // P_{t-1} consumed
-        if (!ok) break;
+      constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
+      // Descriptor bases; the start-address field holds address / 16 in its
+      // low 14 bits, so byte offsets inside shared memory are added as
+      // offset / 16 (no carry: shared addresses stay below 256 KB).
+      const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
+      const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
+      constexpr uint32_t kTile16 = C::kRowTile >> 4;
+      uint32_t nK = 0, nR = 0, gt = 0, un = 0;
+      uint32_t gsu[kSlots] = {0, 0, 0};
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t koff = (kk / 4) * kChunkBytes + (kk % 4) * 32;
-          mma_ss(tmem + kColS, sdesc_sw128(aQu + koff, 16, 1024),
-                 sdesc_sw128(aK + sk * C::kTileBytes + koff, 16, 1024), idesc_s, kk > 0);
-        }
-        tc_commit(&bars->emptyK[sk]);
-        const int ntiles = (t == 0) ? 2 : 1;
-        for (int z = 0; z < ntiles; ++z) {
-          const uint32_t slot = (t == 0 && z == 0) ? 1u : static_cast<uint32_t>(t & 1);
-          const int sr = nR % C::NR;
-          ok = mbar_wait(&bars->fullR[sr], (nR / C::NR) & 1, wait_ns, abort);
-          if (!ok) break;
+        const uint32_t g0 = gt;
+        for (int t = 0; t < w.nks; ++t) {
+          const uint32_t g = g0 + t, sb = g & 1;
+          if (g >= 2 && !(ok = mbar_wait(&bars->s_free[sb], ((g - 2) >> 1) & 1, wait_ns, abort))) break;
+          const int sk = nK % C::NK;
+          if (!(ok = mbar_wait(&bars->fullK[sk], (nK / C::NK) & 1, wait_ns, abort))) break;
           tc_fence_after();
+          {
+            const uint64_t dk = dK + sk * kTile16;
+            const uint32_t sd = tmem + kColS + sb * BN;
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t koff = (kk / 4) * kChunkBytes + (kk % 4) * 32;
-            mma_ss(tmem + (slot ? kColG1 : kColG0), sdesc_sw128(aQv + koff, 16, 1024),
-                   sdesc_sw128(aR + sr * C::kTileBytes + koff, 16, 1024), idesc_s, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff16 = ((kk / 4) * C::kRowChunk + (kk % 4) * 32) >> 4;
+              if constexpr (C::kQTmem)
+                mma_ts(sd, tmem + C::kColQu + kk * 8, dk + koff16, idS, kk > 0);
+              else
+                mma_ss(sd, dQu + (((kk / 4) * C::kQChunk + (kk % 4) * 32) >> 4), dk + koff16, idS, kk > 0);
+            }
           }
-          tc_commit(&bars->emptyR[sr]);
-          ++nR;
-        }
-        if (!ok) break;
-        tc_commit(&bars->s_full);
-        const int sv = t % C::NV;
-        ok = mbar_wait(&bars->p_full, t & 1, wait_ns, abort);
-        if (ok) ok = mbar_wait(&bars->fullV[sv], (t / C::NV) & 1, wait_ns, abort);
-        if (!ok) break;
-        tc_fence_after();
+          tc_commit(&bars->emptyK[sk]);
+          ++nK;
+          for (int e = (t == 0 ? -2 : t); ok && e <= t; ++e) {
+            const int slot = (e + 2) % kSlots;
+            if (gsu[slot] > 0 && !(ok = mbar_wait(&bars->g_free[slot], (gsu[slot] - 1) & 1, wait_ns, abort)))
+              break;
+            const int sr = nR % C::NR;
+            if (!(ok = mbar_wait(&bars->fullR[sr], (nR / C::NR) & 1, wait_ns, abort))) break;
+            tc_fence_after();
+            const uint64_t dr = dR + sr * kTile16;
+            const uint32_t gd = tmem + kColG + slot * BN;
 #pragma unroll
-        for (int kk = 0; kk < BN / 16; ++kk) {
-          // V tile: keys are the K dimension (rows of 128 B), D the N dimension
-          // (MN-major); the second 64-column block, if any, sits 16 KB further.
-          mma_ts(tmem + kColO, tmem + kColS + kk * 8,
-                 sdesc_sw128(aV + sv * C::kTileBytes + kk * 16 * 128, kChunkBytes, 1024), idesc_o,
-                 (t > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff16 = ((kk / 4) * C::kRowChunk + (kk % 4) * 32) >> 4;
+              if constexpr (C::kQTmem)
+                mma_ts(gd, tmem + C::kColQv + kk * 8, dr + koff16, idS, kk > 0);
+              else
+                mma_ss(gd, dQv + (((kk / 4) * C::kQChunk + (kk % 4) * 32) >> 4), dr + koff16, idS, kk > 0);
+            }
+            tc_commit(&bars->emptyR[sr]);
+            ++nR;
+            ++gsu[slot];
+          }
+          if (!ok) break;
+          tc_commit(&bars->s_full[sb]);
         }
-        tc_commit(&bars->emptyV[sv]);
-        tc_commit(&bars->o_done);
+        if (!ok) break;
+        gt = g0 + w.nks;
+        ++un;
       }
       if (!ok) report_timeout(abort, p.status);
       tc_commit(&bars->mma_final);
       mbar_wait_own(&bars->mma_final, 0, wait_ns);
     }
+  } else if (warp == kPvWarp) {
+    // ============================ PV issuer ================================
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      const uint64_t dV = sdesc_sw128(smem_u32(sV), C::kRowChunk, 1024);
+      constexpr uint32_t kTile16 = C::kRowTile >> 4;
+      uint32_t nV = 0, g = 0, un = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p);
+        for (int t = 0; t < w.nks; ++t, ++g) {
+          if (!(ok = mbar_wait(&bars->p_full[g & 1], (g >> 1) & 1, wait_ns, abort))) break;
+          const int sv = nV % C::NV;
+          if (!(ok = mbar_wait(&bars->fullV[sv], (nV / C::NV) & 1, wait_ns, abort))) break;
+          if (t == 0 && un > 0 && !(ok = mbar_wait(&bars->o_free, (un - 1) & 1, wait_ns, abort))) break;
+          tc_fence_after();
+          const uint64_t dv = dV + sv * kTile16;
+          const uint32_t pa = tmem + kColP + (g & 1) * 32;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(tmem + C::kColO, pa + kk * 8, dv + ((kk * 16 * 128) >> 4), idO, (t > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&bars->emptyV[sv]);
+          tc_commit(&bars->pv_done[g & 1]);
+          ++nV;
+        }
+        if (!ok) break;
+        tc_commit(&bars->o_full);
+        ++un;
+      }
+      if (!ok) report_timeout(abort, p.status);
+      tc_commit(&bars->pv_final);
+      mbar_wait_own(&bars->pv_final, 0, wait_ns);
+    }
   } else {
-    // ======================= softmax warps =================================
-    const int a = threadIdx.x;  // row within the tile == TMEM lane
-    const int i = i0 + a;
-    const bool row_valid = i < p.W;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
+    // ============================ softmax warps ============================
+    const int half = warp >> 2;  // 0: key columns 0-31 of a step, 1: columns 32-63
+    const int quad = warp & 3;   // TMEM lane quadrant
+    const int a = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.scale_log2e;
+    uint32_t gt = 0, un = 0, nQ = 0;
+    bool ok = true;
 
-    // (q + u), (q + v) rows -> bf16, 128B-swizzled K-major tiles.
-    {
-      const __nv_bfloat16* qrow = p.q + ((static_cast<size_t>(b) * p.W + (row_valid ? i : 0)) * p.H + h) * D;
-      const float* bu = p.bias_u + h * D;
-      const float* bv = p.bias_v + h * D;
+    // (q + u), (q + v) for this thread's row of unit w: bf16, into TMEM (D=64)
+    // or 128B-swizzled K-major shared-memory tiles (D=128).
+    auto build_q = [&](const Unit& w) -> bool {
+      const int s = nQ % C::NQ;
+      if (!warp_wait(&bars->q_full[s], (nQ / C::NQ) & 1, wait_ns, abort)) return false;
+      const float* bu = p.bias_u + w.h * D;
+      const float* bv = p.bias_v + w.h * D;
+      uint32_t qu[D / 2], qv[D / 2];
 #pragma unroll
       for (int c = 0; c < D / 8; ++c) {
-        uint4 raw = make_uint4(0, 0, 0, 0);
-        if (row_valid) raw = *reinterpret_cast<const uint4*>(qrow + c * 8);
+        const int kc = c / 8, cc = c % 8;
+        const int off = kc * C::kQChunk + (a / 8) * 1024 + (a % 8) * 128 + ((cc ^ (a % 8)) * 16);
+        const uint4 raw = *reinterpret_cast<const uint4*>(sQ + s * C::kQTile + off);
         const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-        uint32_t pu[4], pv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
           const int d = c * 8 + 2 * e;
-          pu[e] = pack_bf16x2(x0 + bu[d], x1 + bu[d + 1]);
-          pv[e] = pack_bf16x2(x0 + bv[d], x1 + bv[d + 1]);
+          const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+          qu[c * 4 + e] = pack_bf16x2((x0 + __ldg(bu + d)) * p.qsign, (x1 + __ldg(bu + d + 1)) * p.qsign);
+          qv[c * 4 + e] = pack_bf16x2((x0 + __ldg(bv + d)) * p.qsign, (x1 + __ldg(bv + d + 1)) * p.qsign);
         }
-        const int kc = c / 8, cc = c % 8;
-        const int off = kc * kChunkBytes + (a / 8) * 1024 + (a % 8) * 128 + ((cc ^ (a % 8)) * 16);
-        *reinterpret_cast<uint4*>(sQu + off) = make_uint4(pu[0], pu[1], pu[2], pu[3]);
-        *reinterpret_cast<uint4*>(sQv + off) = make_uint4(pv[0], pv[1], pv[2], pv[3]);
       }
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->q_ready);
-    }
-
-    float m_run = -INFINITY;  // running row max (log2 units)
-    float l_run = 0.f;        // running row sum
-    bool ok = true;
-    const float sl2 = p.scale_log2e;
-    for (int t = 0; t < nkt; ++t) {
-      bool got = mbar_wait(&bars->s_full, t & 1, wait_ns, abort);
-      if (!__all_sync(0xffffffffu, got)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      const int base = p.M + i0 - BN * t;  // distance of (row 0, key column 0)
-      const uint32_t col_lo = (t & 1) ? kColG1 : kColG0;  // distances [base-128, base)
-      const uint32_t col_hi = (t & 1) ? kColG0 : kColG1;  // distances [base, base+128)
-      const int lim = base + a;  // key column c is visible iff c <= lim
-      float s2[BN];
+      mbar_arrive(&bars->q_empty[s]);
+      ++nQ;
+      if constexpr (C::kQTmem) {
+        tmem_st32(tmem + lane_base + C::kColQu, *reinterpret_cast<uint32_t(*)[32]>(qu));
+        tmem_st32(tmem + lane_base + C::kColQv, *reinterpret_cast<uint32_t(*)[32]>(qv));
+        tmem_wait_st();
+        tc_fence_before();
+      } else {
 #pragma unroll
-      for (int ch = 0; ch < 4; ++ch) {
+        for (int c = 0; c < D / 8; ++c) {
+          const int kc = c / 8, cc = c % 8;
+          const int off = kc * C::kQChunk + (a / 8) * 1024 + (a % 8) * 128 + ((cc ^ (a % 8)) * 16);
+          *reinterpret_cast<uint4*>(sQu + off) = make_uint4(qu[4 * c], qu[4 * c + 1], qu[4 * c + 2], qu[4 * c + 3]);
+          *reinterpret_cast<uint4*>(sQv + off) = make_uint4(qv[4 * c], qv[4 * c + 1], qv[4 * c + 2], qv[4 * c + 3]);
+        }
+        fence_proxy_async_smem();
+      }
+      mbar_arrive(&bars->q_ready);
+      return true;
+    };
+
+    if (half == 1 && blockIdx.x < p.n_units) ok = build_q(decode_unit(blockIdx.x, p));
+
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const Unit w = decode_unit(u, p);
+      float m_use = -INFINITY;  // running max in log2 units (lazy)
+      float l_half = 0.f;       // row sum over this half's columns
+      const uint32_t g0 = gt;
+      for (int t = 0; t < w.nks; ++t) {
+        const uint32_t g = g0 + t, sb = g & 1;
+        if (!(ok = warp_wait(&bars->s_full[sb], (g >> 1) & 1, wait_ns, abort))) break;
+        tc_fence_after();
         uint32_t sraw[32], x0[32], x1[32];
-        tmem_ld32(tmem + lane_base + kColS + ch * 32, sraw);
-        // Window of the [lo | hi] distance row that this warp's lanes need:
-        // columns zq .. zq+63 with zq = 96 + 32*warp - 32*ch (warp-uniform).
-        const int zq = 32 * (3 + warp - ch);
-        const uint32_t z0 = (zq < 128) ? col_lo + zq : col_hi + (zq - 128);
-        const uint32_t z1 = (zq + 32 < 128) ? col_lo + zq + 32 : col_hi + (zq + 32 - 128);
-        tmem_ld32(tmem + lane_base + z0, x0);
-        tmem_ld32(tmem + lane_base + z1, x1);
+        tmem_ld32(tmem + lane_base + kColS + sb * BN + 32 * half, sraw);
+        // Distance window of this warp: ring-relative index z = 64 + a - c
+        // (z < 64: tile t, < 128: tile t-1, else tile t-2); the warp reads
+        // z in [zq, zq + 64) and lane l uses z = zq + 32 + l - k for column k.
+        const int zq = 32 * (1 + quad - half);
+        const uint32_t c0 = kColG + ((t - (zq >> 6) + 2) % kSlots) * BN + (zq & 63);
+        const uint32_t c1 = kColG + ((t - ((zq + 32) >> 6) + 2) % kSlots) * BN + ((zq + 32) & 63);
+        tmem_ld32(tmem + lane_base + c0, x0);
+        tmem_ld32(tmem + lane_base + c1, x1);
         tmem_wait_ld(sraw);
         tmem_wait_ld(x0);
         tmem_wait_ld(x1);
-        float arr[64];
-#pragma unroll
-        for (int n = 0; n < 32; ++n) {
-          arr[n] = __uint_as_float(x0[n]);
-          arr[n + 32] = __uint_as_float(x1[n]);
-        }
-        lane_shift(arr, lane);  // arr[m] = window[m + lane]
+        warp_arrive_tc(&bars->s_free[sb]);              // S buffer may be refilled
+        warp_arrive_tc(&bars->g_free[t % kSlots]);      // distance tile t-2: last read
+        uint32_t bd[16];
+        window_shift(x0, x1, lane, bd);
+        // x[k] = content + distance score of key column 32*half + k; the
+        // distance value sits at window position 31 - k.
+        float x[32];
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
-          const int c = ch * 32 + k;
-          // distance base + a - c sits at window index lane + 32 - k
-          const float sv = (__uint_as_float(sraw[k]) + arr[32 - k]) * sl2;
-          s2[c] = (c <= lim) ? sv : -INFINITY;
+          const int i = 31 - k;
+          x[k] = (i & 1) ? add_bf16hi(bd[i >> 1], __uint_as_float(sraw[k]))
+                         : add_bf16lo(bd[i >> 1], __uint_as_float(sraw[k]));
         }
+        const int lim = p.M + w.i0 - BN * t + a - 32 * half;  // column k visible iff k <= lim
+        if (p.M + w.i0 - BN * t + quad * 32 - 32 * half < 31) {  // some lane of the warp masks
+#pragma unroll
+          for (int k = 0; k < 32; ++k) x[k] = (k <= lim) ? x[k] : -INFINITY;
+        }
+        float t3[11];
+#pragma unroll
+        for (int n = 0; n < 10; ++n) t3[n] = max3f(x[3 * n], x[3 * n + 1], x[3 * n + 2]);
+        t3[10] = fmaxf(x[30], x[31]);
+        float mx = max3f(max3f(t3[0], t3[1], t3[2]), max3f(t3[3], t3[4], t3[5]),
+                         max3f(max3f(t3[6], t3[7], t3[8]), t3[9], t3[10]));
+        // row max over both halves of the step
+        float* rs = red + (g & 1) * 2 * BM;
+        rs[half * BM + a] = mx;
+        mbar_arrive(&bars->xbar[quad]);
+        if (!(ok = warp_wait(&bars->xbar[quad], g & 1, wait_ns, abort))) break;
+        mx = fmaxf(mx, rs[(1 - half) * BM + a]) * sl2;
+        float m_new = m_use, alpha = 1.f;
+        if (mx > m_use + kLazy) {
+          m_new = mx;
+          alpha = ex2(m_use - mx);
+        }
+        uint32_t pk[16];
+        float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+        const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_new, -m_new);
+#pragma unroll
+        for (int n = 0; n < 16; ++n) {
+          const float2 y = __ffma2_rn(make_float2(x[2 * n], x[2 * n + 1]), sc2, nm2);
+          const float2 e = make_float2(ex2(y.x), ex2(y.y));
+          if (n & 1)
+            acc1 = __fadd2_rn(acc1, e);
+          else
+            acc0 = __fadd2_rn(acc0, e);
+          pk[n] = pack_bf16x2(e.x, e.y);
+        }
+        l_half = l_half * alpha + ((acc0.x + acc0.y) + (acc1.x + acc1.y));
+        if (half == 0 && t > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+          // O holds PV up to step t-1; rescale once that PV has completed.
+          if (!(ok = warp_wait(&bars->pv_done[(g - 1) & 1], ((g - 1) >> 1) & 1, wait_ns, abort))) break;
+          tc_fence_after();
+#pragma unroll
+          for (int oc = 0; oc < D / 32; ++oc) {
+            uint32_t ov[32];
+            tmem_ld32(tmem + lane_base + C::kColO + oc * 32, ov);
+            tmem_wait_ld(ov);
+#pragma unroll
+            for (int n = 0; n < 32; ++n) ov[n] = __float_as_uint(__uint_as_float(ov[n]) * alpha);
+            tmem_st32(tmem + lane_base + C::kColO + oc * 32, ov);
+          }
+        }
+        m_use = m_new;
+        // P buffer sb was last read by the PV of step g-2.
+        if (g >= 2 && !(ok = warp_wait(&bars->pv_done[sb], ((g - 2) >> 1) & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        tmem_st16(tmem + lane_base + kColP + sb * 32 + 16 * half, pk);
+        tmem_wait_st();
+        warp_arrive_tc(&bars->p_full[sb]);
       }
-      float mx8[8];
-#pragma unroll
-      for (int u = 0; u < 8; ++u) mx8[u] = s2[u];
-#pragma unroll
-      for (int c = 8; c < BN; ++c) mx8[c & 7] = fmaxf(mx8[c & 7], s2[c]);
-      const float mt = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
-      const float m_new = fmaxf(m_run, mt);
-      const float alpha = ex2(m_run - m_new);
-      float sum8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-      uint32_t pk0[32], pk1[32];
-#pragma unroll
-      for (int n = 0; n < BN / 2; ++n) {
-        const float e0 = ex2(s2[2 * n] - m_new);
-        const float e1 = ex2(s2[2 * n + 1] - m_new);
-        sum8[n & 7] += e0 + e1;
-        if (n < 32)
-          pk0[n] = pack_bf16x2(e0, e1);
-        else
-          pk1[n - 32] = pack_bf16x2(e0, e1);
+      if (!ok) break;
+      // Distance tiles nks-2 and nks-1 are not read any more in this unit.
+      warp_arrive_tc(&bars->g_free[w.nks % kSlots]);
+      warp_arrive_tc(&bars->g_free[(w.nks + 1) % kSlots]);
+      float* ls = lred + (un & 1) * BM;
+      if (half == 1) {
+        ls[a] = l_half;
+        mbar_arrive(&bars->lbar[quad]);
       }
-      const float sum = ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
-      l_run = l_run * alpha + sum;
-      const bool need = (t > 0) && (m_new > m_run);
-      m_run = m_new;
-      if (__any_sync(0xffffffffu, need)) {
-        // PV_{t-1} completed before s_full(t) fired: O is stable here.
+      if (half == 0) {
+        if (!(ok = warp_wait(&bars->lbar[quad], un & 1, wait_ns, abort))) break;
+        const float l = l_half + ls[a];
+        if (!(ok = warp_wait(&bars->o_full, un & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        const int i = w.i0 + a;
+        uint32_t ov[D];
 #pragma unroll
         for (int oc = 0; oc < D / 32; ++oc) {
-          uint32_t ov[32];
-          tmem_ld32(tmem + lane_base + kColO + oc * 32, ov);
-          tmem_wait_ld(ov);
+          uint32_t tmp[32];
+          tmem_ld32(tmem + lane_base + C::kColO + oc * 32, tmp);
+          tmem_wait_ld(tmp);
 #pragma unroll
-          for (int n = 0; n < 32; ++n) ov[n] = __float_as_uint(__uint_as_float(ov[n]) * alpha);
-          tmem_st32(tmem + lane_base + kColO + oc * 32, ov);
+          for (int n = 0; n < 32; ++n) ov[oc * 32 + n] = tmp[n];
         }
-      }
-      tmem_st32(tmem + lane_base + kColS, pk0);
-      tmem_st32(tmem + lane_base + kColS + 32, pk1);
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bars->p_full);
-    }
-
-    if (ok) {
-      bool got = mbar_wait(&bars->o_done, (nkt - 1) & 1, wait_ns, abort);
-      ok = __all_sync(0xffffffffu, got);
-    }
-    if (ok) {
-      tc_fence_after();
-      const float inv_l = 1.f / l_run;
-      uint32_t ov[D];
+        warp_arrive_tc(&bars->o_free);
+        if (i < p.W) {
+          const float inv_l = 1.f / l;
+          const size_t orow = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D;
+          if (O_BF16) {
+            uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow);
 #pragma unroll
-      for (int oc = 0; oc < D / 32; ++oc) {
-        uint32_t tmp[32];
-        tmem_ld32(tmem + lane_base + kColO + oc * 32, tmp);
-        tmem_wait_ld(tmp);
+            for (int c = 0; c < D / 8; ++c) {
+              uint32_t w4[4];
 #pragma unroll
-        for (int n = 0; n < 32; ++n) ov[oc * 32 + n] = tmp[n];
-      }
-      if (row_valid) {
-        const size_t orow = ((static_cast<size_t>(b) * p.W + i) * p.H + h) * D;
-        if (O_BF16) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow);
+              for (int e = 0; e < 4; ++e)
+                w4[e] = pack_bf16x2(__uint_as_float(ov[c * 8 + 2 * e]) * inv_l,
+                                    __uint_as_float(ov[c * 8 + 2 * e + 1]) * inv_l);
+              dst[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            }
+          } else {
+            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
 #pragma unroll
-          for (int c = 0; c < D / 8; ++c) {
-            uint32_t w4[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-              w4[e] = pack_bf16x2(__uint_as_float(ov[c * 8 + 2 * e]) * inv_l,
-                                  __uint_as_float(ov[c * 8 + 2 * e + 1]) * inv_l);
-            dst[c] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+            for (int c = 0; c < D / 4; ++c)
+              dst[c] = make_float4(__uint_as_float(ov[4 * c]) * inv_l, __uint_as_float(ov[4 * c + 1]) * inv_l,
+                                   __uint_as_float(ov[4 * c + 2]) * inv_l, __uint_as_float(ov[4 * c + 3]) * inv_l);
           }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
-#pragma unroll
-          for (int c = 0; c < D / 4; ++c)
-            dst[c] = make_float4(__uint_as_float(ov[4 * c]) * inv_l, __uint_as_float(ov[4 * c + 1]) * inv_l,
-                                 __uint_as_float(ov[4 * c + 2]) * inv_l, __uint_as_float(ov[4 * c + 3]) * inv_l);
+          if (p.lse != nullptr)
+            p.lse[(static_cast<size_t>(w.b) * p.H + w.h) * p.W + i] = (m_use + __log2f(l)) * 0.69314718055994531f;
         }
-        if (p.lse != nullptr)
-          p.lse[(static_cast<size_t>(b) * p.H + h) * p.W + i] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      } else {
+        const int nu = u + gridDim.x;
+        if (nu < p.n_units && !(ok = build_q(decode_unit(nu, p)))) break;
       }
-    } else {
-      report_timeout(abort, p.status);
+      gt = g0 + w.nks;
+      ++un;
     }
+    if (!ok) report_timeout(abort, p.status);
   }
 
   // ---- teardown ------------------------------------------------------------
@@ -463,9 +657,21 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
 template <int D, bool O_BF16>
-cudaError_t launch_typed(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_r,
-                         const Params& prm, cudaStream_t stream) {
+cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                         const CUtensorMap& tm_r, const Params& prm, cudaStream_t stream) {
   auto kern = relattn_tc_kernel<D, O_BF16>;
   constexpr int smem = Cfg<D>::kSmemBytes;
   static int configured_mask = 0;  // one bit per device ordinal < 32
@@ -477,20 +683,18 @@ cudaError_t launch_typed(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const
     if (e != cudaSuccess) return e;
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
-  const long long nqt = (prm.W + BM - 1) / BM;
-  const long long nblocks = nqt * prm.B * prm.H;
-  kern<<<static_cast<unsigned>(nblocks), kThreads, smem, stream>>>(tm_k, tm_v, tm_r, prm);
+  const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
+  kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_relattn_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_r,
-                              const void* q, const float* bias_u, const float* bias_v, void* o,
+cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                              const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
                               float* lse, int B, int W, int M, int H, int D, bool o_bf16, float scale,
                               const WaitCtl& wc, cudaStream_t stream) {
   Params prm;
-  prm.q = static_cast<const __nv_bfloat16*>(q);
   prm.bias_u = bias_u;
   prm.bias_v = bias_v;
   prm.o = o;
@@ -499,16 +703,22 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, 
   prm.W = W;
   prm.M = M;
   prm.H = H;
-  prm.scale_log2e = scale * 1.4426950408889634f;
+  prm.nqt = (W + BM - 1) / BM;
+  prm.n_units = prm.nqt * B * H;
+  // The sign of the scale is folded into (q+u), (q+v) (exact in bf16); a zero
+  // scale becomes 1e-30, for which every visible exponent rounds to 2^0 in
+  // fp32 exactly as with 0, while masked keys keep an exponent of -inf.
+  prm.qsign = scale < 0.f ? -1.f : 1.f;
+  prm.scale_log2e = fmaxf(fabsf(scale), 1e-30f) * 1.4426950408889634f;
   prm.status = wc.status;
   prm.wait_ns = wc.limit_ns;
   prm.inject_stall = wc.inject_stall;
   if (D == 64)
-    return o_bf16 ? launch_typed<64, true>(tm_k, tm_v, tm_r, prm, stream)
-                  : launch_typed<64, false>(tm_k, tm_v, tm_r, prm, stream);
+    return o_bf16 ? launch_typed<64, true>(tm_q, tm_k, tm_v, tm_r, prm, stream)
+                  : launch_typed<64, false>(tm_q, tm_k, tm_v, tm_r, prm, stream);
   if (D == 128)
-    return o_bf16 ? launch_typed<128, true>(tm_k, tm_v, tm_r, prm, stream)
-                  : launch_typed<128, false>(tm_k, tm_v, tm_r, prm, stream);
+    return o_bf16 ? launch_typed<128, true>(tm_q, tm_k, tm_v, tm_r, prm, stream)
+                  : launch_typed<128, false>(tm_q, tm_k, tm_v, tm_r, prm, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -3,15 +3,18 @@
 // ("Transformer-XL, explained", symbol legend: R_{i-j} is a parameter-free
 // sinusoid of the distance; no clipping, so every distance has an encoding).
 //
-// Precision: the product d * w_k is carried as an unevaluated sum of floats
-// (w_k split into hi + lo parts; the rounding error of d * w_hi recovered
-// exactly with an FMA), and reduced modulo 2*pi with a three-constant
-// Cody-Waite split before the fp32 sine / cosine.  The result stays within a
-// few 1e-7 of the exact table for every distance this library meets, where a
-// plain fp32 angle would lose ~1e-4 rad at d ~ 3000.
+// Precision without fp64 on the device: the host passes rho = 10000^(-2/dim)
+// as an unevaluated sum of two floats; w_k = rho^k is formed by binary
+// exponentiation in double-float arithmetic (Dekker products with FMA, ~44
+// significant bits); the product d * w_k is again carried as hi + lo (the
+// rounding error of d * w_hi recovered exactly with an FMA) and reduced
+// modulo 2*pi with a three-constant Cody-Waite split before the fp32 sine /
+// cosine.  The result stays within a few 1e-7 of the exact table for every
+// distance this library meets, where a plain fp32 angle would lose ~1e-4 rad
+// at d ~ 3000.
 //
-// Launch: block (64, 4) covers 64 frequencies x 64 distances; grid
-// (ceil(dim/2 / 64), ceil(n_dist / 64)).  HBM-write bound, tiny.
+// Launch: block (64, 4) covers 64 frequencies x 16 distances; grid
+// (ceil(dim/2 / 64), ceil(n_dist / 16)).  HBM-write bound, tiny.
 #include <cuda_bf16.h>
 
 #include "txl_internal.h"
@@ -20,24 +23,45 @@ namespace txl {
 namespace {
 
 constexpr int kPairsPerBlock = 64;
-constexpr int kRowsPerBlock = 64;
+constexpr int kRowsPerBlock = 16;
+
+struct DF {
+  float hi, lo;  // value hi + lo, |lo| <= ulp(hi) / 2
+};
+
+// Dekker product of two double-float numbers using FMA for the exact
+// rounding error of hi * hi.
+__device__ __forceinline__ DF df_mul(DF a, DF b) {
+  const float p = a.hi * b.hi;
+  float e = fmaf(a.hi, b.hi, -p);
+  e = fmaf(a.hi, b.lo, e);
+  e = fmaf(a.lo, b.hi, e);
+  const float hi = p + e;
+  return DF{hi, e - (hi - p)};
+}
+
+// base^k for k >= 0 by repeated squaring.
+__device__ __forceinline__ DF df_pow(DF base, int k) {
+  DF r{1.f, 0.f};
+  while (k > 0) {
+    if (k & 1) r = df_mul(r, base);
+    base = df_mul(base, base);
+    k >>= 1;
+  }
+  return r;
+}
 
 template <bool BF16>
-__global__ void __launch_bounds__(256) sinusoid_kernel(void* __restrict__ R, int n_dist, int dim, float c1,
-                                                       float c2, float c3) {
+__global__ void __launch_bounds__(256) sinusoid_kernel(void* __restrict__ R, int n_dist, int dim, float rho_hi,
+                                                       float rho_lo, float c1, float c2, float c3) {
   __shared__ float s_whi[kPairsPerBlock];
   __shared__ float s_wlo[kPairsPerBlock];
   const int npairs = dim / 2;
   const int k = blockIdx.x * kPairsPerBlock + threadIdx.x;
   if (threadIdx.y == 0) {
-    float hi = 0.f, lo = 0.f;
-    if (k < npairs) {
-      const double w = pow(10000.0, -2.0 * static_cast<double>(k) / static_cast<double>(dim));
-      hi = static_cast<float>(w);
-      lo = static_cast<float>(w - static_cast<double>(hi));
-    }
-    s_whi[threadIdx.x] = hi;
-    s_wlo[threadIdx.x] = lo;
+    const DF w = df_pow(DF{rho_hi, rho_lo}, k < npairs ? k : 0);
+    s_whi[threadIdx.x] = w.hi;
+    s_wlo[threadIdx.x] = w.lo;
   }
   __syncthreads();
   if (k >= npairs) return;
@@ -73,15 +97,15 @@ __global__ void __launch_bounds__(256) sinusoid_kernel(void* __restrict__ R, int
 
 }  // namespace
 
-cudaError_t launch_sinusoid(void* R, int n_dist, int dim, bool bf16, float c1, float c2, float c3,
-                            cudaStream_t stream) {
+cudaError_t launch_sinusoid(void* R, int n_dist, int dim, bool bf16, float rho_hi, float rho_lo, float c1,
+                            float c2, float c3, cudaStream_t stream) {
   const int npairs = dim / 2;
   dim3 block(kPairsPerBlock, 4);
   dim3 grid((npairs + kPairsPerBlock - 1) / kPairsPerBlock, (n_dist + kRowsPerBlock - 1) / kRowsPerBlock);
   if (bf16)
-    sinusoid_kernel<true><<<grid, block, 0, stream>>>(R, n_dist, dim, c1, c2, c3);
+    sinusoid_kernel<true><<<grid, block, 0, stream>>>(R, n_dist, dim, rho_hi, rho_lo, c1, c2, c3);
   else
-    sinusoid_kernel<false><<<grid, block, 0, stream>>>(R, n_dist, dim, c1, c2, c3);
+    sinusoid_kernel<false><<<grid, block, 0, stream>>>(R, n_dist, dim, rho_hi, rho_lo, c1, c2, c3);
   return cudaGetLastError();
 }
 

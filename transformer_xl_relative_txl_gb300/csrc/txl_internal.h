@@ -17,10 +17,11 @@ struct WaitCtl {
   int inject_stall;               // loader stops after the first key tile
 };
 
-// Sinusoidal distance table.  c1..c3: 2*pi split into three floats whose
-// products with small integers are exact (Cody-Waite reduction constants).
-cudaError_t launch_sinusoid(void* R, int n_dist, int dim, bool bf16, float c1, float c2, float c3,
-                            cudaStream_t stream);
+// Sinusoidal distance table.  rho_hi + rho_lo: 10000^(-2/dim) as a
+// double-float; c1..c3: 2*pi split into three floats whose products with the
+// needed multiples are exact (Cody-Waite reduction constants).
+cudaError_t launch_sinusoid(void* R, int n_dist, int dim, bool bf16, float rho_hi, float rho_lo, float c1,
+                            float c2, float c3, cudaStream_t stream);
 
 // Memory roll over raw bytes.
 cudaError_t launch_mem_roll(const void* mem, const void* h, void* out, int B, long long rows_out,
@@ -34,8 +35,11 @@ cudaError_t launch_relattn_f32(const float* q, const float* k, const float* v, c
                                int W, int M, int H, int D, float scale, cudaStream_t stream);
 
 // bf16 tensor-core relative attention (tcgen05 + TMEM + TMA).
-cudaError_t launch_relattn_tc(const CUtensorMap& tm_k, const CUtensorMap& tm_v, const CUtensorMap& tm_r,
-                              const void* q, const float* bias_u, const float* bias_v, void* o,
+// Tensor maps: q over {D, H, W, B} with a {64, 1, 128, 1} box; k and v over
+// {D, H, M+W, B} with {64, 1, 64, 1}; r over {D, H, n_r} with {64, 1, 64};
+// all bf16, 128-byte swizzle, zero fill out of bounds.
+cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                              const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
                               float* lse, int B, int W, int M, int H, int D, bool o_bf16, float scale,
                               const WaitCtl& wc, cudaStream_t stream);
 
