@@ -269,6 +269,9 @@ int txl_relattn_forward(const void* q, const void* k, const void* v, const void*
   if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
   wc.limit_ns = g_wait_ns.load();
   wc.inject_stall = g_inject_stall.exchange(0);
+  if (D == 64)
+    return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H,
+                                              o_dtype == TXL_BF16, scale, wc, stream));
   return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H, D,
                                           o_dtype == TXL_BF16, scale, wc, stream));
 }

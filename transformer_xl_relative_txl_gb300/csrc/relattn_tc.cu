@@ -1,5 +1,6 @@
 // bf16 relative-position attention on the sm_103a tensor cores (tcgen05 + TMEM
-// + TMA), fp32 accumulation.
+// + TMA), fp32 accumulation; the head-dimension-128 path (D = 64 has its own
+// specialisation in relattn_tc64.cu).
 //
 //   s[i,j] = scale * ((q_i + u) . k_j + (q_i + v) . r_{M+i-j}),   j <= M+i
 //   o_i = softmax(s[i,.]) V
@@ -52,6 +53,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "relattn_tc_common.cuh"
 #include "txl_device.cuh"
 #include "txl_internal.h"
 
@@ -123,92 +125,6 @@ struct Bars {
   int abort;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
-
-struct Unit {
-  int b, h, i0, nks;
-};
-
-__device__ __forceinline__ Unit decode_unit(int u, const Params& p) {
-  const int BH = p.B * p.H;
-  const int qt = p.nqt - 1 - u / BH;  // longest query tiles first
-  const int bh = u % BH;
-  Unit r;
-  r.b = bh / p.H;
-  r.h = bh % p.H;
-  r.i0 = qt * BM;
-  const int kmax = min(p.M + r.i0 + BM - 1, p.M + p.W - 1);
-  r.nks = kmax / BN + 1;
-  return r;
-}
-
-__device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
-}
-
-// fp32 + bf16 (low or high half of a packed pair), one rounding.
-__device__ __forceinline__ float add_bf16lo(uint32_t pk, float s) {
-  float r;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, lo, %2;\n\t}"
-      : "=f"(r) : "r"(pk), "f"(s));
-  return r;
-}
-__device__ __forceinline__ float add_bf16hi(uint32_t pk, float s) {
-  float r;
-  asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %1;\n\tadd.rn.f32.bf16 %0, hi, %2;\n\t}"
-      : "=f"(r) : "r"(pk), "f"(s));
-  return r;
-}
-
-__device__ __forceinline__ float max3f(float a, float b, float c) {
-  float r;
-  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-  return r;
-}
-
-// Per-lane window shift.  x0, x1 hold the fp32 window X[0..63]; on return
-// out[j] packs (Y[2j], Y[2j+1]) as bf16 (low half first) with
-// Y[k] = X[lane + 1 + k], k = 0..31.  The window is packed to bf16 pairs,
-// shifted by whole registers with a five-stage select network on
-// (lane + 1) / 2, and the odd half-register shift is one byte permute.
-__device__ __forceinline__ void window_shift(const uint32_t (&x0)[32], const uint32_t (&x1)[32], int lane,
-                                             uint32_t (&out)[16]) {
-  uint32_t R[32];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) {
-    R[i] = pack_bf16x2(__uint_as_float(x0[2 * i]), __uint_as_float(x0[2 * i + 1]));
-    R[16 + i] = pack_bf16x2(__uint_as_float(x1[2 * i]), __uint_as_float(x1[2 * i + 1]));
-  }
-  const int sh = lane + 1;
-  const int q = sh >> 1;
-  const bool b16 = q & 16, b8 = q & 8, b4 = q & 4, b2 = q & 2, b1 = q & 1;
-#pragma unroll
-  for (int j = 0; j <= 15; ++j) R[j] = b16 ? R[j + 16] : R[j];
-#pragma unroll
-  for (int j = 0; j <= 23; ++j) R[j] = b8 ? R[j + 8] : R[j];
-#pragma unroll
-  for (int j = 0; j <= 19; ++j) R[j] = b4 ? R[j + 4] : R[j];
-#pragma unroll
-  for (int j = 0; j <= 17; ++j) R[j] = b2 ? R[j + 2] : R[j];
-#pragma unroll
-  for (int j = 0; j <= 16; ++j) R[j] = b1 ? R[j + 1] : R[j];
-  const uint32_t sel = (sh & 1) ? 0x5432u : 0x3210u;
-#pragma unroll
-  for (int j = 0; j < 16; ++j) out[j] = byte_perm(R[j], R[j + 1], sel);
-}
-
-__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t ns, volatile int* abort) {
-  const bool got = mbar_wait(bar, parity, ns, abort);
-  return __all_sync(0xffffffffu, got);
-}
-
-// Elected-lane arrive after every lane's tcgen05 accesses are complete.
-__device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
-  tc_fence_before();
-  __syncwarp();
-  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
-}
 
 template <int D, bool O_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -287,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       for (int u = blockIdx.x; ok && !stop && u < p.n_units; u += gridDim.x) {
-        const Unit w = decode_unit(u, p);
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         {
           if (!(ok = acquire(bars->q_empty, bars->q_full, nQ, C::NQ, C::kQTile))) break;
           const int s = nQ % C::NQ;
@@ -348,10 +264,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
       constexpr uint32_t kTile16 = C::kRowTile >> 4;
       uint32_t nK = 0, nR = 0, gt = 0, un = 0;
-      uint32_t gsu[kSlots] = {0, 0, 0};
+      uint32_t gsu0 = 0, gsu1 = 0, gsu2 = 0;  // writes per ring slot so far
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const Unit w = decode_unit(u, p);
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
         const uint32_t g0 = gt;
@@ -377,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nK;
           for (int e = (t == 0 ? -2 : t); ok && e <= t; ++e) {
             const int slot = (e + 2) % kSlots;
-            if (gsu[slot] > 0 && !(ok = mbar_wait(&bars->g_free[slot], (gsu[slot] - 1) & 1, wait_ns, abort)))
-              break;
+            const uint32_t used = slot == 0 ? gsu0 : (slot == 1 ? gsu1 : gsu2);
+            if (used > 0 && !(ok = mbar_wait(&bars->g_free[slot], (used - 1) & 1, wait_ns, abort))) break;
             const int sr = nR % C::NR;
             if (!(ok = mbar_wait(&bars->fullR[sr], (nR / C::NR) & 1, wait_ns, abort))) break;
             tc_fence_after();
@@ -394,7 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             tc_commit(&bars->emptyR[sr]);
             ++nR;
-            ++gsu[slot];
+            gsu0 += slot == 0;
+            gsu1 += slot == 1;
+            gsu2 += slot == 2;
           }
           if (!ok) break;
           tc_commit(&bars->s_full[sb]);
@@ -416,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nV = 0, g = 0, un = 0;
       bool ok = true;
       for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-        const Unit w = decode_unit(u, p);
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         for (int t = 0; t < w.nks; ++t, ++g) {
           if (!(ok = mbar_wait(&bars->p_full[g & 1], (g >> 1) & 1, wait_ns, abort))) break;
           const int sv = nV % C::NV;
@@ -493,10 +411,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    if (half == 1 && blockIdx.x < p.n_units) ok = build_q(decode_unit(blockIdx.x, p));
+    if (half == 1 && blockIdx.x < p.n_units) ok = build_q(decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt));
 
     for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
-      const Unit w = decode_unit(u, p);
+      const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
       float m_use = -INFINITY;  // running max in log2 units (lazy)
       float l_half = 0.f;       // row sum over this half's columns
       const uint32_t g0 = gt;
@@ -639,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       } else {
         const int nu = u + gridDim.x;
-        if (nu < p.n_units && !(ok = build_q(decode_unit(nu, p)))) break;
+        if (nu < p.n_units && !(ok = build_q(decode_unit(nu, p.B, p.H, p.W, p.M, p.nqt)))) break;
       }
       gt = g0 + w.nks;
       ++un;
@@ -713,9 +631,6 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
   prm.status = wc.status;
   prm.wait_ns = wc.limit_ns;
   prm.inject_stall = wc.inject_stall;
-  if (D == 64)
-    return o_bf16 ? launch_typed<64, true>(tm_q, tm_k, tm_v, tm_r, prm, stream)
-                  : launch_typed<64, false>(tm_q, tm_k, tm_v, tm_r, prm, stream);
   if (D == 128)
     return o_bf16 ? launch_typed<128, true>(tm_q, tm_k, tm_v, tm_r, prm, stream)
                   : launch_typed<128, false>(tm_q, tm_k, tm_v, tm_r, prm, stream);

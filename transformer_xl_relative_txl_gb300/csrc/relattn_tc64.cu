@@ -1,0 +1,659 @@
+// bf16 relative-position attention on the sm_103a tensor cores, head dimension
+// 64 (tcgen05 + TMEM + TMA, fp32 accumulation).
+//
+//   s[i,j] = scale * ((q_i + u) . k_j + (q_i + v) . r_{M+i-j}),   j <= M+i
+//   o_i = softmax(s[i,.]) V
+//
+// Same operation, tiling and distance indexing as the general kernel in
+// relattn_tc.cu ("Transformer-XL, explained", method steps 3-5: keys and
+// values over [memory ; segment], the four-term relative score grouped by its
+// query-side factor, the distance term computed once per distance in a
+// three-slot ring of 64-distance tiles and shifted into place per row by an
+// index).  What differs is how the softmax work is spread at D = 64, where
+// the per-element softmax work, not the tensor core, bounds the kernel:
+//
+//   * The two softmax warps that share a TMEM lane quadrant take alternate
+//     64-key steps instead of halves of every step.  Each warp owns a whole
+//     step (one 96-distance window per 64 columns, no per-step exchange of
+//     row maxima) and its own output accumulator, O0 for even steps and O1
+//     for odd ones; the epilogue merges the two with their running maxima
+//     and sums.  Each warp has two steps' time for one step, which hides the
+//     latency of its dependent chains behind the other warp.
+//   * P has its own two TMEM buffers, so the S buffer of step t+2 can be
+//     refilled as soon as step t's softmax has read it.
+//   * (q+u) and (q+v) live in shared memory (128B-swizzled K-major tiles).
+//
+// TMEM (512 columns): O0 [0,64) O1 [64,128) P0 [128,160) P1 [160,192)
+// S0 [192,256) S1 [256,320) distance ring [320,512).
+//
+// Warps: 0-7 softmax (warp w: lane quadrant w%4, step parity w/4; parity-1
+// warps also build the next unit's (q+u), (q+v)); 8 TMA loader; 9 content-
+// score MMA issuer (owns the TMEM allocation); 10 PV MMA issuer; 11 distance-
+// score MMA issuer.  A tcgen05.mma costs tens of cycles to issue and each
+// barrier wait or commit more under load, so the three MMA streams get their
+// own threads; their waits overlap and each commits its own MMAs.  Persistent CTAs walk
+// (batch, head, 128-query tile) units longest first.  Every wait is bounded;
+// a wait that runs out raises a CTA abort flag and the device status word,
+// every role unwinds (the loader and the issuers wait for their own
+// operations in flight) and the TMEM is freed before exit.
+#include <cmath>
+#include <cstdint>
+#include <type_traits>
+
+#include "relattn_tc_common.cuh"
+#include "txl_device.cuh"
+#include "txl_internal.h"
+
+namespace txl {
+namespace {
+
+constexpr int BM = kTileRows;
+constexpr int BN = kStepKeys;
+constexpr int D = 64;
+constexpr int kLoaderWarp = 8;
+constexpr int kMmaWarp = 9;
+constexpr int kPvWarp = 10;
+constexpr int kQrWarp = 11;
+constexpr int kThreads = 384;  // 3 warpgroups: 2 softmax, 1 producer (loader, three MMA issuers)
+// Register split (launch: 168 per thread, 384 x 168 = 64512): softmax
+// warpgroups 224, producer warpgroup 56; 2*128*224 + 128*56 = 64512, and per
+// scheduler 224 + 224 + 56 = 504 <= 512 per thread-slot.
+constexpr uint32_t kRegsSoftmax = 224;
+constexpr uint32_t kRegsProducer = 56;
+static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= kThreads * 168, "register split");
+constexpr uint32_t kColO = 0;    // O0, O1: 64 columns each
+constexpr uint32_t kColP = 128;  // P0, P1: 32 columns each (bf16 pairs)
+constexpr uint32_t kColS = 192;  // S0, S1: 64 columns each
+constexpr uint32_t kColG = 320;  // distance ring: 3 slots of 64 columns
+constexpr int kSlots = 3;
+constexpr uint32_t kTmemCols = 512;
+constexpr float kLazy = 8.0f;  // log2 headroom before a running max moves
+
+constexpr int kRowTile = BN * 128;  // 64 rows x 64 bf16 (8 KB)
+constexpr int kQTile = BM * 128;    // 128 rows x 64 bf16 (16 KB)
+constexpr int NK = 4, NV = 4, NR = 4, NQ = 2;
+constexpr int kOffQ = 0;
+constexpr int kOffQu = kOffQ + NQ * kQTile;
+constexpr int kOffQv = kOffQu + kQTile;
+constexpr int kOffK = kOffQv + kQTile;
+constexpr int kOffV = kOffK + NK * kRowTile;
+constexpr int kOffR = kOffV + NV * kRowTile;
+constexpr int kOffRed = kOffR + NR * kRowTile;  // [unit parity][m, l][row] of the odd-step warps
+constexpr int kOffBar = kOffRed + 2 * 2 * BM * 4;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;
+
+struct Params {
+  const float* bias_u;
+  const float* bias_v;
+  void* o;
+  float* lse;
+  int B, W, M, H;
+  int nqt, n_units;
+  float scale_log2e;  // |scale| * log2(e)
+  float qsign;        // sign of scale, folded into (q+u), (q+v)
+  unsigned int* status;
+  unsigned long long wait_ns;
+  int inject_stall;
+};
+
+struct Bars {
+  uint64_t fullK[NK], emptyK[NK], fullV[NV], emptyV[NV], fullR[NR], emptyR[NR];
+  uint64_t q_full[NQ], q_empty[NQ];
+  uint64_t q_ready, s_full[2], s_free[2], p_full[2], pv_done[2], o_full, o_free, g_free[kSlots];
+  uint64_t mma_final, pv_final, qr_final;
+  uint64_t lbar[4];  // odd-step warp -> even-step warp of a quadrant: (m, l) of a unit
+  uint32_t tmem_base;
+  int abort;
+};
+static_assert(sizeof(Bars) <= 512, "barrier block too large");
+
+// Does the warp of step parity `first` (local steps first, first+2, ...)
+// read distance tile e of a unit with steps 0..tl?  Step t reads tiles t-2..t.
+__device__ __forceinline__ bool reads_tile(int e, int first, int tl) {
+  const int lo = e < 0 ? 0 : e;
+  const int t = lo + ((first - lo) & 1);
+  return t <= e + 2 && t <= tl;
+}
+
+template <bool O_BF16>
+__global__ void __launch_bounds__(kThreads, 1)
+    relattn_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
+                        const Params p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sQ = smem + kOffQ;
+  uint8_t* sQu = smem + kOffQu;
+  uint8_t* sQv = smem + kOffQv;
+  uint8_t* sK = smem + kOffK;
+  uint8_t* sV = smem + kOffV;
+  uint8_t* sR = smem + kOffR;
+  float* red = reinterpret_cast<float*>(smem + kOffRed);
+  Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
+  volatile int* abort = &bars->abort;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < 4; ++s) {
+      mbar_init(&bars->fullK[s], 1);
+      mbar_init(&bars->emptyK[s], 1);
+      mbar_init(&bars->fullV[s], 1);
+      mbar_init(&bars->emptyV[s], 1);
+      mbar_init(&bars->fullR[s], 1);
+      mbar_init(&bars->emptyR[s], 1);
+      mbar_init(&bars->lbar[s], 32);
+      if (s < kSlots) mbar_init(&bars->g_free[s], 8);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bars->q_full[s], 1);
+      mbar_init(&bars->q_empty[s], 128);
+      mbar_init(&bars->s_full[s], 2);  // content and distance MMAs of a step
+      mbar_init(&bars->s_free[s], 4);
+      mbar_init(&bars->p_full[s], 4);
+      mbar_init(&bars->pv_done[s], 1);
+    }
+    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->o_full, 1);
+    mbar_init(&bars->o_free, 4);
+    mbar_init(&bars->mma_final, 1);
+    mbar_init(&bars->pv_final, 1);
+    mbar_init(&bars->qr_final, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == kMmaWarp) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint64_t wait_ns = p.wait_ns;
+
+  if (warp == kLoaderWarp) {
+    // ============================ TMA loader ===============================
+    setmaxnreg_dec<kRegsProducer>();
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_q);
+      tma_prefetch_desc(&tm_k);
+      tma_prefetch_desc(&tm_v);
+      tma_prefetch_desc(&tm_r);
+      uint32_t nQ = 0, nK = 0, nV = 0, nR = 0;
+      bool ok = true, stop = false;
+      auto acquire = [&](uint64_t* empty, uint64_t* full, uint32_t n, int ns, int bytes) -> bool {
+        const int s = static_cast<int>(n % ns);
+        if (!mbar_wait(&empty[s], ((n / ns) & 1) ^ 1, wait_ns, abort)) return false;
+        mbar_arrive_expect_tx(&full[s], bytes);
+        return true;
+      };
+      for (int u = blockIdx.x; ok && !stop && u < p.n_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        if (!(ok = acquire(bars->q_empty, bars->q_full, nQ, NQ, kQTile))) break;
+        tma_load_4d(sQ + (nQ % NQ) * kQTile, &tm_q, &bars->q_full[nQ % NQ], 0, w.h, w.i0, w.b);
+        ++nQ;
+        auto load_r = [&](int d0) -> bool {
+          if (!acquire(bars->emptyR, bars->fullR, nR, NR, kRowTile)) return false;
+          tma_load_3d(sR + (nR % NR) * kRowTile, &tm_r, &bars->fullR[nR % NR], 0, w.h, d0);
+          ++nR;
+          return true;
+        };
+        auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, const CUtensorMap* map,
+                           int t) -> bool {
+          if (!acquire(empty, full, n, 4, kRowTile)) return false;
+          tma_load_4d(dst + (n % 4) * kRowTile, map, &full[n % 4], 0, w.h, t * BN, w.b);
+          ++n;
+          return true;
+        };
+        ok = load_r(p.M + w.i0 + BN) && load_r(p.M + w.i0);  // distance tiles -2 and -1
+        for (int t = 0; ok && t < w.nks; ++t) {
+          if (p.inject_stall && t == 1) {  // test hook: starve the consumers
+            stop = true;
+            break;
+          }
+          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t) && load_r(p.M + w.i0 - BN * (t + 1)) &&
+               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t);
+        }
+      }
+      if (!ok) report_timeout(abort, p.status);
+      auto drain = [&](uint64_t* full, uint32_t n, int ns) {
+        for (int s = 0; s < ns && static_cast<uint32_t>(s) < n; ++s) {
+          const uint32_t last = s + ((n - 1 - s) / ns) * ns;
+          mbar_wait_own(&full[s], (last / ns) & 1, wait_ns);
+        }
+      };
+      drain(bars->q_full, nQ, NQ);
+      drain(bars->fullK, nK, NK);
+      drain(bars->fullV, nV, NV);
+      drain(bars->fullR, nR, NR);
+    }
+  } else if (warp == kMmaWarp) {
+    // ===================== content-score MMA issuer ========================
+    setmaxnreg_dec<kRegsProducer>();
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
+      const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
+      const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+      constexpr uint32_t kTile16 = kRowTile >> 4;
+      uint32_t nK = 0, gt = 0, un = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        const uint32_t g0 = gt;
+        for (int t = 0; t < w.nks; ++t) {
+          const uint32_t g = g0 + t, sb = g & 1;
+          if (g >= 2 && !(ok = mbar_wait(&bars->s_free[sb], ((g - 2) >> 1) & 1, wait_ns, abort))) break;
+          const int sk = nK % NK;
+          if (!(ok = mbar_wait(&bars->fullK[sk], (nK / NK) & 1, wait_ns, abort))) break;
+          tc_fence_after();
+          const uint64_t dk = dK + sk * kTile16;
+          const uint32_t sd = tmem + kColS + sb * BN;
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss(sd, dQu + kk * 2, dk + kk * 2, idS, kk > 0);
+          tc_commit(&bars->emptyK[sk]);
+          tc_commit(&bars->s_full[sb]);
+          ++nK;
+        }
+        if (!ok) break;
+        gt = g0 + w.nks;
+        ++un;
+      }
+      if (!ok) report_timeout(abort, p.status);
+      tc_commit(&bars->mma_final);
+      mbar_wait_own(&bars->mma_final, 0, wait_ns);
+    }
+  } else if (warp == kQrWarp) {
+    // ==================== distance-score MMA issuer ========================
+    setmaxnreg_dec<kRegsProducer>();
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
+      const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
+      const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
+      constexpr uint32_t kTile16 = kRowTile >> 4;
+      uint32_t nR = 0, gt = 0, un = 0;
+      uint32_t gsu0 = 0, gsu1 = 0, gsu2 = 0;  // writes per ring slot so far
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        const uint32_t g0 = gt;
+        for (int t = 0; ok && t < w.nks; ++t) {
+          const uint32_t sb = (g0 + t) & 1;
+          for (int e = (t == 0 ? -2 : t); e <= t; ++e) {
+            const int slot = (e + 2) % kSlots;
+            const uint32_t used = slot == 0 ? gsu0 : (slot == 1 ? gsu1 : gsu2);
+            if (used > 0 && !(ok = mbar_wait(&bars->g_free[slot], (used - 1) & 1, wait_ns, abort))) break;
+            const int sr = nR % NR;
+            if (!(ok = mbar_wait(&bars->fullR[sr], (nR / NR) & 1, wait_ns, abort))) break;
+            tc_fence_after();
+            const uint64_t dr = dR + sr * kTile16;
+            const uint32_t gd = tmem + kColG + slot * BN;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) mma_ss(gd, dQv + kk * 2, dr + kk * 2, idS, kk > 0);
+            tc_commit(&bars->emptyR[sr]);
+            ++nR;
+            gsu0 += slot == 0;
+            gsu1 += slot == 1;
+            gsu2 += slot == 2;
+          }
+          if (!ok) break;
+          tc_commit(&bars->s_full[sb]);
+        }
+        if (!ok) break;
+        gt = g0 + w.nks;
+        ++un;
+      }
+      if (!ok) report_timeout(abort, p.status);
+      tc_commit(&bars->qr_final);
+      mbar_wait_own(&bars->qr_final, 0, wait_ns);
+    }
+  } else if (warp == kPvWarp) {
+    // ============================ PV issuer ================================
+    setmaxnreg_dec<kRegsProducer>();
+    if (lane == 0) {
+      constexpr uint32_t idO = idesc_bf16(128, D, false, true);
+      const uint64_t dV = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
+      constexpr uint32_t kTile16 = kRowTile >> 4;
+      uint32_t nV = 0, g = 0, un = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        for (int t = 0; t < w.nks; ++t, ++g) {
+          if (!(ok = mbar_wait(&bars->p_full[g & 1], (g >> 1) & 1, wait_ns, abort))) break;
+          const int sv = nV % NV;
+          if (!(ok = mbar_wait(&bars->fullV[sv], (nV / NV) & 1, wait_ns, abort))) break;
+          // The first PV into each accumulator of a unit overwrites it: the
+          // previous unit's epilogue must have read both.
+          if (t < 2 && un > 0 && !(ok = mbar_wait(&bars->o_free, (un - 1) & 1, wait_ns, abort))) break;
+          tc_fence_after();
+          const uint64_t dv = dV + sv * kTile16;
+          const uint32_t pa = tmem + kColP + (g & 1) * 32;
+          const uint32_t od = tmem + kColO + (g & 1) * D;
+#pragma unroll
+          for (int kk = 0; kk < BN / 16; ++kk)
+            mma_ts(od, pa + kk * 8, dv + ((kk * 16 * 128) >> 4), idO, (t >= 2 || kk > 0) ? 1u : 0u);
+          tc_commit(&bars->emptyV[sv]);
+          tc_commit(&bars->pv_done[g & 1]);
+          ++nV;
+        }
+        if (!ok) break;
+        tc_commit(&bars->o_full);
+        ++un;
+      }
+      if (!ok) report_timeout(abort, p.status);
+      tc_commit(&bars->pv_final);
+      mbar_wait_own(&bars->pv_final, 0, wait_ns);
+    }
+  } else {
+    // ============================ softmax warps ============================
+    setmaxnreg_inc<kRegsSoftmax>();
+    const int par = warp >> 2;  // step parity taken by this warp
+    const int quad = warp & 3;  // TMEM lane quadrant
+    const int a = quad * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const float sl2 = p.scale_log2e;
+    uint32_t gt = 0, un = 0, nQ = 0;
+    bool ok = true;
+
+    // (q + u), (q + v) rows of unit w into 128B-swizzled K-major smem tiles.
+    auto build_q = [&](const Unit& w) -> bool {
+      const int s = nQ % NQ;
+      if (!warp_wait(&bars->q_full[s], (nQ / NQ) & 1, wait_ns, abort)) return false;
+      const float* bu = p.bias_u + w.h * D;
+      const float* bv = p.bias_v + w.h * D;
+#pragma unroll
+      for (int c = 0; c < D / 8; ++c) {
+        const int off = (a / 8) * 1024 + (a % 8) * 128 + ((c ^ (a % 8)) * 16);
+        const uint4 raw = *reinterpret_cast<const uint4*>(sQ + s * kQTile + off);
+        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+        uint32_t qu[4], qv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int d = c * 8 + 2 * e;
+          const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+          qu[e] = pack_bf16x2((x0 + __ldg(bu + d)) * p.qsign, (x1 + __ldg(bu + d + 1)) * p.qsign);
+          qv[e] = pack_bf16x2((x0 + __ldg(bv + d)) * p.qsign, (x1 + __ldg(bv + d + 1)) * p.qsign);
+        }
+        *reinterpret_cast<uint4*>(sQu + off) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+        *reinterpret_cast<uint4*>(sQv + off) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+      }
+      mbar_arrive(&bars->q_empty[s]);
+      ++nQ;
+      fence_proxy_async_smem();
+      mbar_arrive(&bars->q_ready);
+      return true;
+    };
+
+    if (par == 1 && blockIdx.x < p.n_units) ok = build_q(decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt));
+
+    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+      const uint32_t g0 = gt;
+      const int tl = w.nks - 1;
+      const int first = (par - static_cast<int>(g0)) & 1;  // first local step of this warp
+      float m_use = -INFINITY;  // running max in log2 units (lazy)
+      float l_run = 0.f;
+      // Distance tile -2 is read by step 0 only: the warps of odd local steps
+      // release its slot now, before they wait for tiles that reuse the slot.
+      if (!reads_tile(-2, first, tl)) warp_arrive_tc(&bars->g_free[0]);
+      for (int t = first; t <= tl; t += 2) {
+        const uint32_t g = g0 + t, sb = g & 1;
+        if (!(ok = warp_wait(&bars->s_full[sb], (g >> 1) & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        // Distance window of this warp: ring-relative index z = 64 + a - c
+        // (z < 64: tile t, < 128: tile t-1, else tile t-2).  Columns 0-31 use
+        // z in [32 quad + 32, 32 quad + 96), columns 32-63 z in
+        // [32 quad, 32 quad + 64); lane l of column k (within its half) sits
+        // at window position l + 32 - k.
+        auto zcol = [&](int z) -> uint32_t {
+          return kColG + ((t - (z >> 6) + 2) % kSlots) * BN + (z & 63);
+        };
+        const uint32_t sc = tmem + lane_base + kColS + sb * BN;
+        const int lim = p.M + w.i0 - BN * t + a;  // column c visible iff c <= lim
+        const bool diag = p.M + w.i0 - BN * t + quad * 32 < 63;  // some lane of the warp masks
+        const float m_old = m_use;
+        float m_new = m_use;
+        float sum = 0.f;
+        uint32_t pk[32];
+        uint32_t pb[16];
+        // One 32-column half: distance-window shift, scores, lazy running max,
+        // exponentials packed to bf16 pairs into pk[16h .. 16h+15].
+        auto half_step = [&](const uint32_t (&sraw)[32], const uint32_t (&lo)[16], const uint32_t (&hi)[16], auto hc) {
+          constexpr int h = decltype(hc)::value;
+          uint32_t bd[16];
+          window_shift_packed(lo, hi, lane, bd);
+          float x[32];
+          add_window(sraw, bd, x);
+          if (diag) {
+#pragma unroll
+            for (int k = 0; k < 32; ++k) x[k] = (32 * h + k <= lim) ? x[k] : -INFINITY;
+          }
+          float t3[11];
+#pragma unroll
+          for (int n = 0; n < 10; ++n) t3[n] = max3f(x[3 * n], x[3 * n + 1], x[3 * n + 2]);
+          t3[10] = fmaxf(x[30], x[31]);
+          const float mx = max3f(max3f(t3[0], t3[1], t3[2]), max3f(t3[3], t3[4], t3[5]),
+                                 max3f(max3f(t3[6], t3[7], t3[8]), t3[9], t3[10])) * sl2;
+          if (mx > m_new + kLazy) {
+            if constexpr (h == 1) {  // rare: rescale the first half to the new max
+              const float r = ex2(m_new - mx);
+              sum *= r;
+#pragma unroll
+              for (int n = 0; n < 16; ++n) pk[n] = pack_bf16x2(bf16_lo(pk[n]) * r, bf16_hi(pk[n]) * r);
+            }
+            m_new = mx;
+          }
+          // A row with no visible key yet keeps m_new = -inf; its exponents
+          // are then taken against 0 (all -inf, so every p is 0).
+          const float m_eff = (m_new == -INFINITY) ? 0.f : m_new;
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_eff, -m_eff);
+#pragma unroll
+          for (int n = 0; n < 16; ++n) {
+            const float2 y = __ffma2_rn(make_float2(x[2 * n], x[2 * n + 1]), sc2, nm2);
+            const float2 e = make_float2(ex2(y.x), ex2(y.y));
+            if (n & 1)
+              acc1 = __fadd2_rn(acc1, e);
+            else
+              acc0 = __fadd2_rn(acc0, e);
+            pk[16 * h + n] = pack_bf16x2(e.x, e.y);
+          }
+          sum += (acc0.x + acc0.y) + (acc1.x + acc1.y);
+        };
+        // Load the whole 96-distance window first and release its ring slots
+        // right away: the distance MMAs of later steps wait for them.
+        uint32_t pa[16], pc[16];
+        {
+          uint32_t xa[32], xb[32], xc[32];
+          tmem_ld32(tmem + lane_base + zcol(32 * quad), xa);
+          tmem_ld32(tmem + lane_base + zcol(32 * quad + 32), xb);
+          tmem_ld32(tmem + lane_base + zcol(32 * quad + 64), xc);
+          tmem_wait_ld(xa);
+          tmem_wait_ld(xb);
+          tmem_wait_ld(xc);
+          warp_arrive_tc(&bars->g_free[t % kSlots]);        // tile t-2: last read by this warp
+          warp_arrive_tc(&bars->g_free[(t + 1) % kSlots]);  // tile t-1
+          if (t + 2 > tl) warp_arrive_tc(&bars->g_free[(t + 2) % kSlots]);  // tile t
+          pack32(xa, pa);
+          pack32(xb, pb);
+          pack32(xc, pc);
+        }
+        {
+          uint32_t sraw[32];
+          tmem_ld32(sc, sraw);
+          tmem_wait_ld(sraw);
+          half_step(sraw, pb, pc, std::integral_constant<int, 0>{});
+        }
+        {
+          uint32_t sraw[32];
+          tmem_ld32(sc + 32, sraw);
+          tmem_wait_ld(sraw);
+          warp_arrive_tc(&bars->s_free[sb]);
+          half_step(sraw, pa, pb, std::integral_constant<int, 1>{});
+        }
+        const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);  // m_new >= m_old
+        l_run = l_run * alpha + sum;
+        // The PV of step g-2 (same P buffer, same accumulator) must be done
+        // before P is overwritten or O rescaled.
+        if (g >= 2 && !(ok = warp_wait(&bars->pv_done[sb], ((g - 2) >> 1) & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        if (t > first && __any_sync(0xffffffffu, m_new > m_old)) {
+          // O of this parity holds PV up to step t-2; rescale it in place.
+          const uint32_t oc0 = tmem + lane_base + kColO + par * D;
+#pragma unroll
+          for (int oc = 0; oc < D / 32; ++oc) {
+            uint32_t ov[32];
+            tmem_ld32(oc0 + oc * 32, ov);
+            tmem_wait_ld(ov);
+#pragma unroll
+            for (int n = 0; n < 32; ++n) ov[n] = __float_as_uint(__uint_as_float(ov[n]) * alpha);
+            tmem_st32(oc0 + oc * 32, ov);
+          }
+        }
+        m_use = m_new;
+        tmem_st32(tmem + lane_base + kColP + sb * 32, pk);
+        tmem_wait_st();
+        warp_arrive_tc(&bars->p_full[sb]);
+      }
+      if (!ok) break;
+      // Remaining distance tiles of this unit that this warp never reads.
+      for (int e = -1; e <= tl; ++e)
+        if (!reads_tile(e, first, tl)) warp_arrive_tc(&bars->g_free[(e + 2) % kSlots]);
+      float* rm = red + (un & 1) * 2 * BM;
+      if (par == 1) {
+        // (q+u), (q+v) of this unit must stay until its last score MMAs ran.
+        const uint32_t gl = g0 + tl;
+        if ((gl & 1) != 1 && !(ok = warp_wait(&bars->s_full[gl & 1], (gl >> 1) & 1, wait_ns, abort))) break;
+        rm[a] = m_use;
+        rm[BM + a] = l_run;
+        mbar_arrive(&bars->lbar[quad]);
+        const int nu = u + gridDim.x;
+        if (nu < p.n_units && !(ok = build_q(decode_unit(nu, p.B, p.H, p.W, p.M, p.nqt)))) break;
+      } else {
+        if (!(ok = warp_wait(&bars->lbar[quad], un & 1, wait_ns, abort))) break;
+        const float m1 = rm[a], l1 = rm[BM + a];
+        if (!(ok = warp_wait(&bars->o_full, un & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        // merge the even- and odd-step accumulators
+        const bool has0 = first <= tl;           // this warp (even parity) had steps
+        const bool has1 = (first ^ 1) <= tl;     // the odd-parity warp had steps
+        const float m = fmaxf(has0 ? m_use : -INFINITY, has1 ? m1 : -INFINITY);
+        const float a0 = has0 ? ex2(m_use - m) : 0.f;
+        const float a1 = has1 ? ex2(m1 - m) : 0.f;
+        const float l = a0 * l_run + a1 * l1;
+        const float inv_l = 1.f / l;
+        const float c0 = a0 * inv_l, c1 = a1 * inv_l;
+        const int i = w.i0 + a;
+        const size_t orow = ((static_cast<size_t>(w.b) * p.W + (i < p.W ? i : 0)) * p.H + w.h) * D;
+#pragma unroll
+        for (int oc = 0; oc < D / 32; ++oc) {
+          uint32_t t0[32], t1[32];
+          if (has0) {
+            tmem_ld32(tmem + lane_base + kColO + oc * 32, t0);
+            tmem_wait_ld(t0);
+          }
+          if (has1) {
+            tmem_ld32(tmem + lane_base + kColO + D + oc * 32, t1);
+            tmem_wait_ld(t1);
+          }
+          float ov[32];
+#pragma unroll
+          for (int n = 0; n < 32; ++n)
+            ov[n] = (has0 ? __uint_as_float(t0[n]) * c0 : 0.f) + (has1 ? __uint_as_float(t1[n]) * c1 : 0.f);
+          if (i < p.W) {
+            if (O_BF16) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow + oc * 32);
+#pragma unroll
+              for (int c = 0; c < 4; ++c)
+                dst[c] = make_uint4(pack_bf16x2(ov[8 * c], ov[8 * c + 1]), pack_bf16x2(ov[8 * c + 2], ov[8 * c + 3]),
+                                    pack_bf16x2(ov[8 * c + 4], ov[8 * c + 5]),
+                                    pack_bf16x2(ov[8 * c + 6], ov[8 * c + 7]));
+            } else {
+              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + oc * 32);
+#pragma unroll
+              for (int c = 0; c < 8; ++c) dst[c] = make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+            }
+          }
+        }
+        warp_arrive_tc(&bars->o_free);
+        if (i < p.W && p.lse != nullptr)
+          p.lse[(static_cast<size_t>(w.b) * p.H + w.h) * p.W + i] = (m + __log2f(l)) * 0.69314718055994531f;
+      }
+      gt = g0 + w.nks;
+      ++un;
+    }
+    if (!ok) report_timeout(abort, p.status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == kMmaWarp) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <bool O_BF16>
+cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                         const CUtensorMap& tm_r, const Params& prm, cudaStream_t stream) {
+  auto kern = relattn_tc64_kernel<O_BF16>;
+  static int configured_mask = 0;  // one bit per device ordinal < 32
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev >= 32 || !(__atomic_load_n(&configured_mask, __ATOMIC_ACQUIRE) & (1 << dev))) {
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+    if (e != cudaSuccess) return e;
+    if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
+  }
+  const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, prm);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
+                                float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
+                                cudaStream_t stream) {
+  Params prm;
+  prm.bias_u = bias_u;
+  prm.bias_v = bias_v;
+  prm.o = o;
+  prm.lse = lse;
+  prm.B = B;
+  prm.W = W;
+  prm.M = M;
+  prm.H = H;
+  prm.nqt = (W + BM - 1) / BM;
+  prm.n_units = prm.nqt * B * H;
+  prm.qsign = scale < 0.f ? -1.f : 1.f;
+  prm.scale_log2e = fmaxf(fabsf(scale), 1e-30f) * 1.4426950408889634f;
+  prm.status = wc.status;
+  prm.wait_ns = wc.limit_ns;
+  prm.inject_stall = wc.inject_stall;
+  return o_bf16 ? launch_typed<true>(tm_q, tm_k, tm_v, tm_r, prm, stream)
+                : launch_typed<false>(tm_q, tm_k, tm_v, tm_r, prm, stream);
+}
+
+}  // namespace txl

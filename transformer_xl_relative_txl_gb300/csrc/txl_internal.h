@@ -43,4 +43,10 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
                               float* lse, int B, int W, int M, int H, int D, bool o_bf16, float scale,
                               const WaitCtl& wc, cudaStream_t stream);
 
+// Specialisation for D = 64 (same tensor maps).
+cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
+                                float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
+                                cudaStream_t stream);
+
 }  // namespace txl
