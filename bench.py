@@ -37,9 +37,10 @@ METRIC = "relative-attention tokens/s and TFLOP/s (fraction of BF16 peak), 1×GB
 UNIT = "tokens/s"
 WORKLOAD = "base"
 N_SEG_BUFFERS = 8
-KERNEL_SOURCES = ["transformer_xl_relative_txl_gb300/csrc/relattn_tc.cu",
+KERNEL_SOURCES = ["transformer_xl_relative_txl_gb300/csrc/relattn_tc64.cu",
+                  "transformer_xl_relative_txl_gb300/csrc/relattn_tc_common.cuh",
                   "transformer_xl_relative_txl_gb300/csrc/txl_device.cuh"]
-NCU_SUMMARY = os.path.join(ROOT, "profiles", "relattn_tc_base_counters.json")
+NCU_SUMMARY = os.path.join(ROOT, "profiles", "relattn_tc64_base_counters.json")
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 
 
@@ -240,8 +241,6 @@ class SegmentStream:
         self.knew_h = [x[:, wl.M:].cpu().contiguous().pin_memory() for x in self.k]
         self.vnew_h = [x[:, wl.M:].cpu().contiguous().pin_memory() for x in self.v]
         self.o_h = torch.empty(self.o.shape, dtype=bf).pin_memory()
-        self.side = torch.cuda.Stream(device=device)
-        self.rolled = {}
 
     def roll(self, t):
         """Memory update feeding segment t: the last M rows of segment t-1's
@@ -255,12 +254,11 @@ class SegmentStream:
         txl.txl_mem_update(self.vf[prev][:, :wl.M], self.vf[prev][:, wl.M:], self.vf[cur], wl.M)
 
     def step(self, t, ev=None):
-        """One pass of the hot path for segment t: distance table, memory roll
-        of k and v, relative attention.  The roll for segment t+1 is issued on
-        a side stream right after this segment's roll, so it overlaps this
-        segment's attention (it reads segment t's buffer and writes segment
-        t+1's, disjoint from what the attention touches); the attention of
-        t+1 waits for it.  Returns the number of library kernels launched."""
+        """One pass of the hot path for segment t, in order on one stream: the
+        distance table, the memory roll of k and v (segment t-1's buffer ->
+        the head of segment t's), and the relative attention.  (The attention
+        is a persistent kernel that fills every SM, so nothing is overlapped
+        with it.)  Returns the number of library kernels launched."""
         import torch
 
         import transformer_xl_relative_txl_gb300 as txl
@@ -268,22 +266,14 @@ class SegmentStream:
         wl = self.wl
         cur = t % N_SEG_BUFFERS
         main = torch.cuda.current_stream()
-        if not self.rolled.get(t, False):  # first step of a run: roll inline
-            self.roll(t)
-        self.side.wait_stream(main)
-        with torch.cuda.stream(self.side):
-            txl.txl_sinusoid_rel(self.R)
-            self.roll(t + 1)
-        self.rolled = {t + 1: True}
-        roll_done = torch.cuda.Event()
-        roll_done.record(self.side)
+        txl.txl_sinusoid_rel(self.R)
+        self.roll(t)
         if ev is not None:
             ev[0].record(main)
         txl.txl_relattn_forward(self.q[cur], self.k[cur], self.v[cur], self.r, self.u, self.vb, self.o, None,
                                 M=wl.M)
         if ev is not None:
             ev[1].record(main)
-        main.wait_event(roll_done)
         return 4
 
     def step_e2e(self, t):
@@ -426,11 +416,11 @@ def run_ours(args):
                    "parallelism": f"dp{world} (each rank its own {wl.B} sequences)",
                    "l2": f"inputs larger than L2: {N_SEG_BUFFERS} rotating segment buffers "
                          f"(~{N_SEG_BUFFERS * (2 * wl.B * (wl.M + wl.W) + wl.B * wl.W) * wl.H * wl.D * 2 / 1e9:.2f} GB)",
-                   "step": "txl_sinusoid_rel + txl_mem_update(k) + txl_mem_update(v) + txl_relattn_forward; "
-                           "the roll for the next segment runs on a side stream during this attention"},
+                   "step": "txl_sinusoid_rel + txl_mem_update(k) + txl_mem_update(v) + txl_relattn_forward, "
+                           "in order on one stream"},
         "tflops": achieved,
         "attn_ms": k1_ms,
-        "roofline": {"kernel": "relattn_tc_kernel<64>", "bound": "tensor", "achieved": achieved, "peak": peak,
+        "roofline": {"kernel": "relattn_tc64_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,
                      "unit": "TFLOP/s", "frac": achieved / peak,
                      "peak_source": f"{peak_src} bf16_tflops (burst)",
                      "traffic": ncu_traffic_per_launch(),

@@ -265,13 +265,23 @@ int txl_relattn_forward(const void* q, const void* k, const void* v, const void*
     const cuuint32_t box[3] = {64, 1, 64};
     if (!encode_bf16(&tm_r, r, 3, dims, strides, box)) return TXL_ERR_CUDA;
   }
+  // bf16 output of the D = 64 kernel leaves through TMA stores of 32-row boxes.
+  CUtensorMap tm_o;
+  const bool o_tma = D == 64 && o_dtype == TXL_BF16;
+  if (o_tma) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(W) * hd * 2};
+    const cuuint32_t box[4] = {64, 1, 32, 1};
+    if (!encode_bf16(&tm_o, o, 4, dims, strides, box)) return TXL_ERR_CUDA;
+  }
   txl::WaitCtl wc;
   if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
   wc.limit_ns = g_wait_ns.load();
   wc.inject_stall = g_inject_stall.exchange(0);
   if (D == 64)
-    return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H,
-                                              o_dtype == TXL_BF16, scale, wc, stream));
+    return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, o_tma ? &tm_o : nullptr, bias_u, bias_v, o,
+                                              lse, B, W, M, H, o_dtype == TXL_BF16, scale, wc, stream));
   return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H, D,
                                           o_dtype == TXL_BF16, scale, wc, stream));
 }

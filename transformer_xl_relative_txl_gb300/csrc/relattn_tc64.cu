@@ -7,35 +7,51 @@
 // Same operation, tiling and distance indexing as the general kernel in
 // relattn_tc.cu ("Transformer-XL, explained", method steps 3-5: keys and
 // values over [memory ; segment], the four-term relative score grouped by its
-// query-side factor, the distance term computed once per distance in a
-// three-slot ring of 64-distance tiles and shifted into place per row by an
-// index).  What differs is how the softmax work is spread at D = 64, where
-// the per-element softmax work, not the tensor core, bounds the kernel:
+// query-side factor, the distance term computed once per distance in a ring
+// of 64-distance tiles and shifted into place per row by an index).  What
+// differs is how the work is spread at D = 64, where the per-element softmax
+// work, not the tensor core, bounds the kernel:
 //
 //   * The two softmax warps that share a TMEM lane quadrant take alternate
 //     64-key steps instead of halves of every step.  Each warp owns a whole
 //     step (one 96-distance window per 64 columns, no per-step exchange of
 //     row maxima) and its own output accumulator, O0 for even steps and O1
-//     for odd ones; the epilogue merges the two with their running maxima
-//     and sums.  Each warp has two steps' time for one step, which hides the
-//     latency of its dependent chains behind the other warp.
-//   * P has its own two TMEM buffers, so the S buffer of step t+2 can be
-//     refilled as soon as step t's softmax has read it.
-//   * (q+u) and (q+v) live in shared memory (128B-swizzled K-major tiles).
+//     for odd ones; the warps of a unit's last step merge the two with their
+//     running maxima and sums while the other parity starts the next unit.
+//     Each warp has two steps' time for one step, which hides the latency of
+//     its dependent chains behind the other warp.
+//   * The distance ring has four slots: the tile that step t adds reuses the
+//     slot of tile t-4, last read by step t-2, so the distance MMAs run a
+//     full step ahead of the softmax instead of waiting on its previous step.
+//     The ring continues across units, so the next unit's first tiles are
+//     computed while this unit's last step runs.
+//   * A softmax warp reads everything a step needs from TMEM (S and the
+//     distance window) in one batch and signals it with a single arrival
+//     (one barrier per step modulo 4); the content-MMA issuer reuses the S
+//     buffer and the distance-MMA issuer a ring slot once the steps that
+//     read them have signalled.
+//     The TMEM for the fourth slot comes from keeping P in shared memory
+//     (both PV operands are then shared-memory descriptors).
+//   * (q+u) and (q+v) are double-buffered in shared memory (128B-swizzled
+//     K-major tiles) and the next unit's pair is built right after each
+//     warp's first step of the current unit, half of the head dimensions by
+//     each step parity, so no unit boundary waits for it.
+//   * bf16 output is staged in the epilogue warp's idle P quadrant and
+//     written by a TMA store.
 //
-// TMEM (512 columns): O0 [0,64) O1 [64,128) P0 [128,160) P1 [160,192)
-// S0 [192,256) S1 [256,320) distance ring [320,512).
+// TMEM (512 columns): O0 [0,64) O1 [64,128) S0 [128,192) S1 [192,256)
+// distance ring [256,512).
 //
-// Warps: 0-7 softmax (warp w: lane quadrant w%4, step parity w/4; parity-1
-// warps also build the next unit's (q+u), (q+v)); 8 TMA loader; 9 content-
-// score MMA issuer (owns the TMEM allocation); 10 PV MMA issuer; 11 distance-
-// score MMA issuer.  A tcgen05.mma costs tens of cycles to issue and each
-// barrier wait or commit more under load, so the three MMA streams get their
-// own threads; their waits overlap and each commits its own MMAs.  Persistent CTAs walk
-// (batch, head, 128-query tile) units longest first.  Every wait is bounded;
-// a wait that runs out raises a CTA abort flag and the device status word,
-// every role unwinds (the loader and the issuers wait for their own
-// operations in flight) and the TMEM is freed before exit.
+// Warps: 0-7 softmax (warp w: lane quadrant w%4, step parity w/4); 8 TMA
+// loader; 9 content-score MMA issuer (owns the TMEM allocation); 10 PV MMA
+// issuer; 11 distance-score MMA issuer.  A tcgen05.mma costs tens of cycles
+// to issue and each barrier wait or commit more under load, so the three MMA
+// streams get their own threads; their waits overlap and each commits its own
+// MMAs.  Persistent CTAs walk (batch, head, 128-query tile) units longest
+// first, dealt to the CTAs in a snake order.  Every wait is bounded; a wait
+// that runs out raises a CTA abort flag and the device status word, every
+// role unwinds (the loader and the issuers wait for their own operations in
+// flight) and the TMEM is freed before exit.
 #include <cmath>
 #include <cstdint>
 #include <type_traits>
@@ -62,25 +78,28 @@ constexpr uint32_t kRegsSoftmax = 224;
 constexpr uint32_t kRegsProducer = 56;
 static_assert(2 * 128 * kRegsSoftmax + 128 * kRegsProducer <= kThreads * 168, "register split");
 constexpr uint32_t kColO = 0;    // O0, O1: 64 columns each
-constexpr uint32_t kColP = 128;  // P0, P1: 32 columns each (bf16 pairs)
-constexpr uint32_t kColS = 192;  // S0, S1: 64 columns each
-constexpr uint32_t kColG = 320;  // distance ring: 3 slots of 64 columns
-constexpr int kSlots = 3;
+constexpr uint32_t kColS = 128;  // S0, S1: 64 columns each
+constexpr uint32_t kColG = 256;  // distance ring: 4 slots of 64 columns
+constexpr int kSlots = 4;
+static_assert(kSlots == 4, "ring slot counters and barrier init assume four slots");
 constexpr uint32_t kTmemCols = 512;
 constexpr float kLazy = 8.0f;  // log2 headroom before a running max moves
 
 constexpr int kRowTile = BN * 128;  // 64 rows x 64 bf16 (8 KB)
 constexpr int kQTile = BM * 128;    // 128 rows x 64 bf16 (16 KB)
-constexpr int NK = 4, NV = 4, NR = 4, NQ = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffQu = kOffQ + NQ * kQTile;
-constexpr int kOffQv = kOffQu + kQTile;
-constexpr int kOffK = kOffQv + kQTile;
+constexpr int NK = 4, NV = 4, NR = 4;
+constexpr int kOffQ = 0;                        // raw q tile of the next unit (TMA)
+constexpr int kOffQu = kOffQ + kQTile;          // (q+u): 2 buffers
+constexpr int kOffQv = kOffQu + 2 * kQTile;     // (q+v): 2 buffers
+constexpr int kOffK = kOffQv + 2 * kQTile;
 constexpr int kOffV = kOffK + NK * kRowTile;
 constexpr int kOffR = kOffV + NV * kRowTile;
-constexpr int kOffRed = kOffR + NR * kRowTile;  // [unit parity][m, l][row] of the odd-step warps
-constexpr int kOffBar = kOffRed + 2 * 2 * BM * 4;
+constexpr int kOffP = kOffR + NR * kRowTile;    // P (bf16): 2 buffers, same layout as (q+u)
+constexpr int kOffRed = kOffP + 2 * kQTile;     // [unit parity][m, l][row] handed to the epilogue
+constexpr int kOffBias = kOffRed + 2 * 2 * BM * 4;  // per softmax warp: 32 dims of u, then of v (fp32)
+constexpr int kOffBar = kOffBias + 8 * 64 * 4;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;
+static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 struct Params {
   const float* bias_u;
@@ -98,28 +117,22 @@ struct Params {
 
 struct Bars {
   uint64_t fullK[NK], emptyK[NK], fullV[NV], emptyV[NV], fullR[NR], emptyR[NR];
-  uint64_t q_full[NQ], q_empty[NQ];
-  uint64_t q_ready, s_full[2], s_free[2], p_full[2], pv_done[2], o_full, o_free, g_free[kSlots];
+  uint64_t q_full, q_empty;
+  uint64_t q_ready, s_full[2], p_full[2], pv_done[2], o_full, o_free;
+  uint64_t sread[4];  // step g's S and distance window have been read (index g % 4, phase g / 4)
   uint64_t mma_final, pv_final, qr_final;
-  uint64_t lbar[4];  // odd-step warp -> even-step warp of a quadrant: (m, l) of a unit
+  uint64_t lbar[4];   // per quadrant: the non-owning warp's (m, l) of a unit is in `red`
+  uint64_t lfree[4];  // per quadrant: the epilogue has read it
   uint32_t tmem_base;
   int abort;
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
-// Does the warp of step parity `first` (local steps first, first+2, ...)
-// read distance tile e of a unit with steps 0..tl?  Step t reads tiles t-2..t.
-__device__ __forceinline__ bool reads_tile(int e, int first, int tl) {
-  const int lo = e < 0 ? 0 : e;
-  const int t = lo + ((first - lo) & 1);
-  return t <= e + 2 && t <= tl;
-}
-
 template <bool O_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     relattn_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
-                        const Params p) {
+                        const __grid_constant__ CUtensorMap tm_o, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -129,7 +142,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sK = smem + kOffK;
   uint8_t* sV = smem + kOffV;
   uint8_t* sR = smem + kOffR;
+  uint8_t* sP = smem + kOffP;
   float* red = reinterpret_cast<float*>(smem + kOffRed);
+  float* sbias = reinterpret_cast<float*>(smem + kOffBias);
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort = &bars->abort;
 
@@ -145,17 +160,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->fullR[s], 1);
       mbar_init(&bars->emptyR[s], 1);
       mbar_init(&bars->lbar[s], 32);
-      if (s < kSlots) mbar_init(&bars->g_free[s], 8);
+      mbar_init(&bars->lfree[s], 1);
+      mbar_init(&bars->sread[s], 4);
     }
     for (int s = 0; s < 2; ++s) {
-      mbar_init(&bars->q_full[s], 1);
-      mbar_init(&bars->q_empty[s], 128);
       mbar_init(&bars->s_full[s], 2);  // content and distance MMAs of a step
-      mbar_init(&bars->s_free[s], 4);
       mbar_init(&bars->p_full[s], 4);
       mbar_init(&bars->pv_done[s], 1);
     }
-    mbar_init(&bars->q_ready, 128);
+    mbar_init(&bars->q_full, 1);
+    mbar_init(&bars->q_empty, 8);
+    mbar_init(&bars->q_ready, 8);
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, 4);
     mbar_init(&bars->mma_final, 1);
@@ -190,11 +205,23 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full[s], bytes);
         return true;
       };
-      for (int u = blockIdx.x; ok && !stop && u < p.n_units; u += gridDim.x) {
+      // The raw q tile of a unit is loaded one unit ahead: the softmax warps
+      // build (q+u), (q+v) from it during the unit before.
+      auto load_q = [&](int u) -> bool {
+        if (!mbar_wait(&bars->q_empty, (nQ & 1) ^ 1, wait_ns, abort)) return false;
+        mbar_arrive_expect_tx(&bars->q_full, kQTile);
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
-        if (!(ok = acquire(bars->q_empty, bars->q_full, nQ, NQ, kQTile))) break;
-        tma_load_4d(sQ + (nQ % NQ) * kQTile, &tm_q, &bars->q_full[nQ % NQ], 0, w.h, w.i0, w.b);
+        tma_load_4d(sQ, &tm_q, &bars->q_full, 0, w.h, w.i0, w.b);
         ++nQ;
+        return true;
+      };
+      if (sched_unit(0, blockIdx.x, gridDim.x) < p.n_units) ok = load_q(sched_unit(0, blockIdx.x, gridDim.x));
+      for (int rd = 0;; ++rd) {
+        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        if (!ok || stop || u >= p.n_units) break;
+        const int un_next = sched_unit(rd + 1, blockIdx.x, gridDim.x);
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        if (un_next < p.n_units && !(ok = load_q(un_next))) break;
         auto load_r = [&](int d0) -> bool {
           if (!acquire(bars->emptyR, bars->fullR, nR, NR, kRowTile)) return false;
           tma_load_3d(sR + (nR % NR) * kRowTile, &tm_r, &bars->fullR[nR % NR], 0, w.h, d0);
@@ -225,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_wait_own(&full[s], (last / ns) & 1, wait_ns);
         }
       };
-      drain(bars->q_full, nQ, NQ);
+      drain(&bars->q_full, nQ, 1);
       drain(bars->fullK, nK, NK);
       drain(bars->fullV, nV, NV);
       drain(bars->fullR, nR, NR);
@@ -240,21 +267,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kTile16 = kRowTile >> 4;
       uint32_t nK = 0, gt = 0, un = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int rd = 0;; ++rd) {
+        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        if (!ok || u >= p.n_units) break;
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
         const uint32_t g0 = gt;
         for (int t = 0; t < w.nks; ++t) {
           const uint32_t g = g0 + t, sb = g & 1;
-          if (g >= 2 && !(ok = mbar_wait(&bars->s_free[sb], ((g - 2) >> 1) & 1, wait_ns, abort))) break;
+          // S buffer sb was last read by step g-2.
+          if (g >= 2 && !(ok = mbar_wait(&bars->sread[(g - 2) & 3], ((g - 2) >> 2) & 1, wait_ns, abort))) break;
           const int sk = nK % NK;
           if (!(ok = mbar_wait(&bars->fullK[sk], (nK / NK) & 1, wait_ns, abort))) break;
           tc_fence_after();
           const uint64_t dk = dK + sk * kTile16;
           const uint32_t sd = tmem + kColS + sb * BN;
+          const uint64_t dq = dQu + (un & 1) * (kQTile >> 4);
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) mma_ss(sd, dQu + kk * 2, dk + kk * 2, idS, kk > 0);
+          for (int kk = 0; kk < D / 16; ++kk) mma_ss(sd, dq + kk * 2, dk + kk * 2, idS, kk > 0);
           tc_commit(&bars->emptyK[sk]);
           tc_commit(&bars->s_full[sb]);
           ++nK;
@@ -276,31 +307,44 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
       constexpr uint32_t kTile16 = kRowTile >> 4;
       uint32_t nR = 0, gt = 0, un = 0;
-      uint32_t gsu0 = 0, gsu1 = 0, gsu2 = 0;  // writes per ring slot so far
+      // Last global step that reads the tile now in each ring slot (-1: none).
+      int last0 = -1, last1 = -1, last2 = -1, last3 = -1;
+      int rb = 0;  // ring slot of the first distance tile (-2) of the unit
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int rd = 0;; ++rd) {
+        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        if (!ok || u >= p.n_units) break;
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
         const uint32_t g0 = gt;
+        const uint64_t dq = dQv + (un & 1) * (kQTile >> 4);
         for (int t = 0; ok && t < w.nks; ++t) {
           const uint32_t sb = (g0 + t) & 1;
           for (int e = (t == 0 ? -2 : t); e <= t; ++e) {
-            const int slot = (e + 2) % kSlots;
-            const uint32_t used = slot == 0 ? gsu0 : (slot == 1 ? gsu1 : gsu2);
-            if (used > 0 && !(ok = mbar_wait(&bars->g_free[slot], (used - 1) & 1, wait_ns, abort))) break;
+            const int slot = (rb + e + 2) & (kSlots - 1);
+            // The slot's previous tile is free once every step up to its
+            // last reader L has read: steps of one parity read in order, so
+            // waiting for steps L and L-1 covers both parities.  (Four
+            // barriers by step % 4 keep these waits from aliasing: step L+3
+            // cannot have read before this tile exists.)
+            const int L = slot == 0 ? last0 : (slot == 1 ? last1 : (slot == 2 ? last2 : last3));
+            if (L >= 0 && !(ok = mbar_wait(&bars->sread[L & 3], (L >> 2) & 1, wait_ns, abort))) break;
+            if (L >= 1 && !(ok = mbar_wait(&bars->sread[(L - 1) & 3], ((L - 1) >> 2) & 1, wait_ns, abort))) break;
             const int sr = nR % NR;
             if (!(ok = mbar_wait(&bars->fullR[sr], (nR / NR) & 1, wait_ns, abort))) break;
             tc_fence_after();
             const uint64_t dr = dR + sr * kTile16;
             const uint32_t gd = tmem + kColG + slot * BN;
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) mma_ss(gd, dQv + kk * 2, dr + kk * 2, idS, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk) mma_ss(gd, dq + kk * 2, dr + kk * 2, idS, kk > 0);
             tc_commit(&bars->emptyR[sr]);
             ++nR;
-            gsu0 += slot == 0;
-            gsu1 += slot == 1;
-            gsu2 += slot == 2;
+            const int lr = static_cast<int>(g0) + min(e + 2, w.nks - 1);  // tile e's last reader
+            last0 = slot == 0 ? lr : last0;
+            last1 = slot == 1 ? lr : last1;
+            last2 = slot == 2 ? lr : last2;
+            last3 = slot == 3 ? lr : last3;
           }
           if (!ok) break;
           tc_commit(&bars->s_full[sb]);
@@ -308,6 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok) break;
         gt = g0 + w.nks;
         ++un;
+        rb = (rb + w.nks + 2) & (kSlots - 1);
       }
       if (!ok) report_timeout(abort, p.status);
       tc_commit(&bars->qr_final);
@@ -319,10 +364,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       constexpr uint32_t idO = idesc_bf16(128, D, false, true);
       const uint64_t dV = sdesc_sw128(smem_u32(sV), BN * 128, 1024);
+      const uint64_t dP = sdesc_sw128(smem_u32(sP), 16, 1024);
       constexpr uint32_t kTile16 = kRowTile >> 4;
       uint32_t nV = 0, g = 0, un = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int rd = 0;; ++rd) {
+        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        if (!ok || u >= p.n_units) break;
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         for (int t = 0; t < w.nks; ++t, ++g) {
           if (!(ok = mbar_wait(&bars->p_full[g & 1], (g >> 1) & 1, wait_ns, abort))) break;
@@ -333,11 +381,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (t < 2 && un > 0 && !(ok = mbar_wait(&bars->o_free, (un - 1) & 1, wait_ns, abort))) break;
           tc_fence_after();
           const uint64_t dv = dV + sv * kTile16;
-          const uint32_t pa = tmem + kColP + (g & 1) * 32;
+          const uint64_t dp = dP + (g & 1) * (kQTile >> 4);
           const uint32_t od = tmem + kColO + (g & 1) * D;
 #pragma unroll
           for (int kk = 0; kk < BN / 16; ++kk)
-            mma_ts(od, pa + kk * 8, dv + ((kk * 16 * 128) >> 4), idO, (t >= 2 || kk > 0) ? 1u : 0u);
+            mma_ss(od, dp + kk * 2, dv + ((kk * 16 * 128) >> 4), idO, t >= 2 || kk > 0);
           tc_commit(&bars->emptyV[sv]);
           tc_commit(&bars->pv_done[g & 1]);
           ++nV;
@@ -359,49 +407,66 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const float sl2 = p.scale_log2e;
     uint32_t gt = 0, un = 0, nQ = 0;
+    int rb = 0;  // ring slot of the unit's distance tile -2 (continues across units)
+    bool store_pending = false;  // lane 0 has a TMA store out of this warp's P quadrant
     bool ok = true;
 
-    // (q + u), (q + v) rows of unit w into 128B-swizzled K-major smem tiles.
-    auto build_q = [&](const Unit& w) -> bool {
-      const int s = nQ % NQ;
-      if (!warp_wait(&bars->q_full[s], (nQ / NQ) & 1, wait_ns, abort)) return false;
-      const float* bu = p.bias_u + w.h * D;
-      const float* bv = p.bias_v + w.h * D;
+    // (q + u), (q + v) of unit w into buffer `buf` (128B-swizzled K-major
+    // tiles): this warp's row, head dimensions [32 par, 32 par + 32).
+    auto build_q = [&](const Unit& w, int buf) -> bool {
+      // This warp's 32 dims of u and v, staged once for broadcast reads.
+      float* sb_w = sbias + warp * 64;
+      sb_w[lane] = __ldg(p.bias_u + w.h * D + 32 * par + lane);
+      sb_w[32 + lane] = __ldg(p.bias_v + w.h * D + 32 * par + lane);
+      __syncwarp();
+      if (!warp_wait(&bars->q_full, nQ & 1, wait_ns, abort)) return false;
+      uint4 raw[4];
 #pragma unroll
-      for (int c = 0; c < D / 8; ++c) {
-        const int off = (a / 8) * 1024 + (a % 8) * 128 + ((c ^ (a % 8)) * 16);
-        const uint4 raw = *reinterpret_cast<const uint4*>(sQ + s * kQTile + off);
-        const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * par + j;
+        raw[j] = *reinterpret_cast<const uint4*>(sQ + (a / 8) * 1024 + (a % 8) * 128 + ((c ^ (a % 8)) * 16));
+      }
+      warp_arrive(&bars->q_empty);
+      ++nQ;
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const int c = 4 * par + j;
+        const int off = buf * kQTile + (a / 8) * 1024 + (a % 8) * 128 + ((c ^ (a % 8)) * 16);
+        const uint32_t w4[4] = {raw[j].x, raw[j].y, raw[j].z, raw[j].w};
+        const float4 u0 = *reinterpret_cast<const float4*>(sb_w + 8 * j);
+        const float4 u1 = *reinterpret_cast<const float4*>(sb_w + 8 * j + 4);
+        const float4 v0 = *reinterpret_cast<const float4*>(sb_w + 32 + 8 * j);
+        const float4 v1 = *reinterpret_cast<const float4*>(sb_w + 32 + 8 * j + 4);
+        const float ub[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+        const float vb[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
         uint32_t qu[4], qv[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const int d = c * 8 + 2 * e;
           const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
-          qu[e] = pack_bf16x2((x0 + __ldg(bu + d)) * p.qsign, (x1 + __ldg(bu + d + 1)) * p.qsign);
-          qv[e] = pack_bf16x2((x0 + __ldg(bv + d)) * p.qsign, (x1 + __ldg(bv + d + 1)) * p.qsign);
+          qu[e] = pack_bf16x2((x0 + ub[2 * e]) * p.qsign, (x1 + ub[2 * e + 1]) * p.qsign);
+          qv[e] = pack_bf16x2((x0 + vb[2 * e]) * p.qsign, (x1 + vb[2 * e + 1]) * p.qsign);
         }
         *reinterpret_cast<uint4*>(sQu + off) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
         *reinterpret_cast<uint4*>(sQv + off) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
       }
-      mbar_arrive(&bars->q_empty[s]);
-      ++nQ;
-      fence_proxy_async_smem();
-      mbar_arrive(&bars->q_ready);
+      warp_arrive_smem(&bars->q_ready);
+      __syncwarp();  // sb_w is rewritten by the next build
       return true;
     };
 
-    if (par == 1 && blockIdx.x < p.n_units) ok = build_q(decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt));
+    if (sched_unit(0, blockIdx.x, gridDim.x) < p.n_units)
+      ok = build_q(decode_unit(sched_unit(0, blockIdx.x, gridDim.x), p.B, p.H, p.W, p.M, p.nqt), 0);
 
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (int rd = 0;; ++rd) {
+      const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+      if (!ok || u >= p.n_units) break;
+      const int un_next = sched_unit(rd + 1, blockIdx.x, gridDim.x);
       const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
       const uint32_t g0 = gt;
       const int tl = w.nks - 1;
       const int first = (par - static_cast<int>(g0)) & 1;  // first local step of this warp
       float m_use = -INFINITY;  // running max in log2 units (lazy)
       float l_run = 0.f;
-      // Distance tile -2 is read by step 0 only: the warps of odd local steps
-      // release its slot now, before they wait for tiles that reuse the slot.
-      if (!reads_tile(-2, first, tl)) warp_arrive_tc(&bars->g_free[0]);
       for (int t = first; t <= tl; t += 2) {
         const uint32_t g = g0 + t, sb = g & 1;
         if (!(ok = warp_wait(&bars->s_full[sb], (g >> 1) & 1, wait_ns, abort))) break;
@@ -412,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // [32 quad, 32 quad + 64); lane l of column k (within its half) sits
         // at window position l + 32 - k.
         auto zcol = [&](int z) -> uint32_t {
-          return kColG + ((t - (z >> 6) + 2) % kSlots) * BN + (z & 63);
+          return kColG + ((rb + t - (z >> 6) + 2) & (kSlots - 1)) * BN + (z & 63);
         };
         const uint32_t sc = tmem + lane_base + kColS + sb * BN;
         const int lim = p.M + w.i0 - BN * t + a;  // column c visible iff c <= lim
@@ -466,37 +531,30 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           sum += (acc0.x + acc0.y) + (acc1.x + acc1.y);
         };
-        // Load the whole 96-distance window first and release its ring slots
-        // right away: the distance MMAs of later steps wait for them.
+        // All of this step's TMEM reads at once -- the 96-distance window and
+        // both halves of S -- then one arrival hands the S buffer and the
+        // ring slots back to the MMA issuers.
         uint32_t pa[16], pc[16];
+        uint32_t s0[32], s1[32];
         {
           uint32_t xa[32], xb[32], xc[32];
           tmem_ld32(tmem + lane_base + zcol(32 * quad), xa);
           tmem_ld32(tmem + lane_base + zcol(32 * quad + 32), xb);
           tmem_ld32(tmem + lane_base + zcol(32 * quad + 64), xc);
+          tmem_ld32(sc, s0);
+          tmem_ld32(sc + 32, s1);
           tmem_wait_ld(xa);
           tmem_wait_ld(xb);
           tmem_wait_ld(xc);
-          warp_arrive_tc(&bars->g_free[t % kSlots]);        // tile t-2: last read by this warp
-          warp_arrive_tc(&bars->g_free[(t + 1) % kSlots]);  // tile t-1
-          if (t + 2 > tl) warp_arrive_tc(&bars->g_free[(t + 2) % kSlots]);  // tile t
+          tmem_wait_ld(s0);
+          tmem_wait_ld(s1);
+          warp_arrive_tc(&bars->sread[g & 3]);
           pack32(xa, pa);
           pack32(xb, pb);
           pack32(xc, pc);
         }
-        {
-          uint32_t sraw[32];
-          tmem_ld32(sc, sraw);
-          tmem_wait_ld(sraw);
-          half_step(sraw, pb, pc, std::integral_constant<int, 0>{});
-        }
-        {
-          uint32_t sraw[32];
-          tmem_ld32(sc + 32, sraw);
-          tmem_wait_ld(sraw);
-          warp_arrive_tc(&bars->s_free[sb]);
-          half_step(sraw, pa, pb, std::integral_constant<int, 1>{});
-        }
+        half_step(s0, pb, pc, std::integral_constant<int, 0>{});
+        half_step(s1, pa, pb, std::integral_constant<int, 1>{});
         const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);  // m_new >= m_old
         l_run = l_run * alpha + sum;
         // The PV of step g-2 (same P buffer, same accumulator) must be done
@@ -515,80 +573,121 @@ __global__ void __launch_bounds__(kThreads, 1)
             for (int n = 0; n < 32; ++n) ov[n] = __float_as_uint(__uint_as_float(ov[n]) * alpha);
             tmem_st32(oc0 + oc * 32, ov);
           }
+          tmem_wait_st();
         }
         m_use = m_new;
-        tmem_st32(tmem + lane_base + kColP + sb * 32, pk);
-        tmem_wait_st();
-        warp_arrive_tc(&bars->p_full[sb]);
+        if (store_pending) {  // the last epilogue staged its output here
+          if (lane == 0) bulk_wait_group_read0();
+          __syncwarp();
+          store_pending = false;
+        }
+        {
+          // P row a into buffer sb (128B-swizzled K-major, as (q+u)).
+          uint8_t* prow = sP + sb * kQTile + (a / 8) * 1024 + (a % 8) * 128;
+#pragma unroll
+          for (int c = 0; c < BN / 8; ++c)
+            *reinterpret_cast<uint4*>(prow + ((c ^ (a % 8)) * 16)) =
+                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+        }
+        tc_fence_before();  // orders the O rescale's tcgen05.st before the arrive
+        warp_arrive_smem(&bars->p_full[sb]);
+        // The next unit's (q+u), (q+v) go to the other buffer once this
+        // warp's first step of this unit has seen its scores: the MMAs of the
+        // unit before, which read that buffer, are complete by then.
+        if (t == first && un_next < p.n_units &&
+            !(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1)))
+          break;
       }
       if (!ok) break;
-      // Remaining distance tiles of this unit that this warp never reads.
-      for (int e = -1; e <= tl; ++e)
-        if (!reads_tile(e, first, tl)) warp_arrive_tc(&bars->g_free[(e + 2) % kSlots]);
-      float* rm = red + (un & 1) * 2 * BM;
-      if (par == 1) {
-        // (q+u), (q+v) of this unit must stay until its last score MMAs ran.
+      if (first > tl && un_next < p.n_units) {
+        // No step of this unit: build after its last step's scores instead.
         const uint32_t gl = g0 + tl;
-        if ((gl & 1) != 1 && !(ok = warp_wait(&bars->s_full[gl & 1], (gl >> 1) & 1, wait_ns, abort))) break;
+        if (!(ok = warp_wait(&bars->s_full[gl & 1], (gl >> 1) & 1, wait_ns, abort))) break;
+        if (!(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1))) break;
+      }
+      // The warps of the unit's last step merge the two accumulators and
+      // write the output; the other parity hands over its (m, l) and moves on
+      // to the next unit, whose first step is its own.
+      float* rm = red + (un & 1) * 2 * BM;
+      const int owner = static_cast<int>((g0 + tl) & 1);
+      if (par != owner) {
+        // The owner of the previous unit has read that unit's (m, l).
+        if (un > 0 && !(ok = warp_wait(&bars->lfree[quad], (un - 1) & 1, wait_ns, abort))) break;
         rm[a] = m_use;
         rm[BM + a] = l_run;
         mbar_arrive(&bars->lbar[quad]);
-        const int nu = u + gridDim.x;
-        if (nu < p.n_units && !(ok = build_q(decode_unit(nu, p.B, p.H, p.W, p.M, p.nqt)))) break;
       } else {
         if (!(ok = warp_wait(&bars->lbar[quad], un & 1, wait_ns, abort))) break;
         const float m1 = rm[a], l1 = rm[BM + a];
+        warp_arrive(&bars->lfree[quad]);
         if (!(ok = warp_wait(&bars->o_full, un & 1, wait_ns, abort))) break;
         tc_fence_after();
-        // merge the even- and odd-step accumulators
-        const bool has0 = first <= tl;           // this warp (even parity) had steps
-        const bool has1 = (first ^ 1) <= tl;     // the odd-parity warp had steps
+        // merge this parity's accumulator (0) with the other's (1)
+        const bool has0 = first <= tl;        // this warp had steps
+        const bool has1 = (first ^ 1) <= tl;  // the other parity's warp had steps
         const float m = fmaxf(has0 ? m_use : -INFINITY, has1 ? m1 : -INFINITY);
         const float a0 = has0 ? ex2(m_use - m) : 0.f;
         const float a1 = has1 ? ex2(m1 - m) : 0.f;
         const float l = a0 * l_run + a1 * l1;
         const float inv_l = 1.f / l;
         const float c0 = a0 * inv_l, c1 = a1 * inv_l;
-        const int i = w.i0 + a;
-        const size_t orow = ((static_cast<size_t>(w.b) * p.W + (i < p.W ? i : 0)) * p.H + w.h) * D;
+        // Read both accumulators into registers and hand them back to the PV
+        // issuer before the stores.
+        float ov[D];
 #pragma unroll
         for (int oc = 0; oc < D / 32; ++oc) {
           uint32_t t0[32], t1[32];
           if (has0) {
-            tmem_ld32(tmem + lane_base + kColO + oc * 32, t0);
+            tmem_ld32(tmem + lane_base + kColO + par * D + oc * 32, t0);
             tmem_wait_ld(t0);
           }
           if (has1) {
-            tmem_ld32(tmem + lane_base + kColO + D + oc * 32, t1);
+            tmem_ld32(tmem + lane_base + kColO + (par ^ 1) * D + oc * 32, t1);
             tmem_wait_ld(t1);
           }
-          float ov[32];
 #pragma unroll
           for (int n = 0; n < 32; ++n)
-            ov[n] = (has0 ? __uint_as_float(t0[n]) * c0 : 0.f) + (has1 ? __uint_as_float(t1[n]) * c1 : 0.f);
-          if (i < p.W) {
-            if (O_BF16) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow + oc * 32);
-#pragma unroll
-              for (int c = 0; c < 4; ++c)
-                dst[c] = make_uint4(pack_bf16x2(ov[8 * c], ov[8 * c + 1]), pack_bf16x2(ov[8 * c + 2], ov[8 * c + 3]),
-                                    pack_bf16x2(ov[8 * c + 4], ov[8 * c + 5]),
-                                    pack_bf16x2(ov[8 * c + 6], ov[8 * c + 7]));
-            } else {
-              float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow + oc * 32);
-#pragma unroll
-              for (int c = 0; c < 8; ++c) dst[c] = make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
-            }
-          }
+            ov[oc * 32 + n] =
+                (has0 ? __uint_as_float(t0[n]) * c0 : 0.f) + (has1 ? __uint_as_float(t1[n]) * c1 : 0.f);
         }
         warp_arrive_tc(&bars->o_free);
+        const int i = w.i0 + a;
+        if (O_BF16) {
+          // bf16 rows into this warp's quadrant of its own P buffer (free
+          // until its next step: the last PV that read it is complete), then
+          // one TMA store of the 32-row box; rows past W are not written.
+          uint8_t* orow_s = sP + par * kQTile + (a / 8) * 1024 + (a % 8) * 128;
+#pragma unroll
+          for (int c = 0; c < D / 8; ++c)
+            *reinterpret_cast<uint4*>(orow_s + ((c ^ (a % 8)) * 16)) =
+                make_uint4(pack_bf16x2(ov[8 * c], ov[8 * c + 1]), pack_bf16x2(ov[8 * c + 2], ov[8 * c + 3]),
+                           pack_bf16x2(ov[8 * c + 4], ov[8 * c + 5]), pack_bf16x2(ov[8 * c + 6], ov[8 * c + 7]));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (w.i0 + 32 * quad < p.W) {
+            if (lane == 0) {
+              tma_store_4d(&tm_o, sP + par * kQTile + quad * 4096, 0, w.h, w.i0 + 32 * quad, w.b);
+              bulk_commit_group();
+            }
+            store_pending = true;
+          }
+        } else if (i < p.W) {
+          const size_t orow = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D;
+          float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+        }
         if (i < p.W && p.lse != nullptr)
           p.lse[(static_cast<size_t>(w.b) * p.H + w.h) * p.W + i] = (m + __log2f(l)) * 0.69314718055994531f;
       }
       gt = g0 + w.nks;
       ++un;
+      rb = (rb + w.nks + 2) & (kSlots - 1);
     }
     if (!ok) report_timeout(abort, p.status);
+    // Output stores in flight must finish before the CTA's shared memory goes.
+    if (lane == 0) bulk_wait_group0();
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -614,7 +713,7 @@ int num_sms() {
 
 template <bool O_BF16>
 cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                         const CUtensorMap& tm_r, const Params& prm, cudaStream_t stream) {
+                         const CUtensorMap& tm_r, const CUtensorMap& tm_o, const Params& prm, cudaStream_t stream) {
   auto kern = relattn_tc64_kernel<O_BF16>;
   static int configured_mask = 0;  // one bit per device ordinal < 32
   int dev = 0;
@@ -626,14 +725,15 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
   const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, prm);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_o, prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
+                                const CUtensorMap& tm_r, const CUtensorMap* tm_o, const float* bias_u,
+                                const float* bias_v, void* o,
                                 float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
                                 cudaStream_t stream) {
   Params prm;
@@ -652,8 +752,10 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   prm.status = wc.status;
   prm.wait_ns = wc.limit_ns;
   prm.inject_stall = wc.inject_stall;
-  return o_bf16 ? launch_typed<true>(tm_q, tm_k, tm_v, tm_r, prm, stream)
-                : launch_typed<false>(tm_q, tm_k, tm_v, tm_r, prm, stream);
+  if (o_bf16 && tm_o == nullptr) return cudaErrorInvalidValue;
+  // fp32 output is written with plain stores; tm_q stands in for the unused map.
+  return o_bf16 ? launch_typed<true>(tm_q, tm_k, tm_v, tm_r, *tm_o, prm, stream)
+                : launch_typed<false>(tm_q, tm_k, tm_v, tm_r, tm_q, prm, stream);
 }
 
 }  // namespace txl

@@ -30,6 +30,14 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int H, int W, int M, i
   return r;
 }
 
+// Unit of round r for CTA c of P: units are sorted longest first and dealt
+// in a snake order (c, then 2P-1-c, then 2P+c, ...), which pairs long units
+// with short ones.  Returns a value >= n_units once the CTA has no more (and
+// every later round is then past the end as well).
+__device__ __forceinline__ int sched_unit(int r, int c, int P) {
+  return r * P + ((r & 1) ? P - 1 - c : c);
+}
+
 __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
@@ -120,6 +128,20 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64
 // Elected-lane arrive after every lane's tcgen05 accesses are complete.
 __device__ __forceinline__ void warp_arrive_tc(uint64_t* bar) {
   tc_fence_before();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Elected-lane arrive after every lane's shared-memory writes are made
+// visible to the async proxy (the tensor core reads them next).
+__device__ __forceinline__ void warp_arrive_smem(uint64_t* bar) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Elected-lane arrive after every lane's generic accesses.
+__device__ __forceinline__ void warp_arrive(uint64_t* bar) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }

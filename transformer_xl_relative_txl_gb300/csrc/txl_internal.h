@@ -44,8 +44,10 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
                               const WaitCtl& wc, cudaStream_t stream);
 
 // Specialisation for D = 64 (same tensor maps).
+// tm_o: the bf16 output's map (box 64 x 1 x 32 x 1); required when o_bf16.
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
+                                const CUtensorMap& tm_r, const CUtensorMap* tm_o, const float* bias_u,
+                                const float* bias_v, void* o,
                                 float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
                                 cudaStream_t stream);
 
