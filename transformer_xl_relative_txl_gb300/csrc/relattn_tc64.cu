@@ -413,11 +413,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // (q + u), (q + v) of unit w into buffer `buf` (128B-swizzled K-major
     // tiles): this warp's row, head dimensions [32 par, 32 par + 32).
-    auto build_q = [&](const Unit& w, int buf) -> bool {
+    // bu_l, bv_l: this lane's dims 32 par + lane of the unit's u and v (loaded
+    // ahead by the caller, so their latency overlaps other work).
+    auto build_q = [&](const Unit& w, int buf, float bu_l, float bv_l) -> bool {
       // This warp's 32 dims of u and v, staged once for broadcast reads.
       float* sb_w = sbias + warp * 64;
-      sb_w[lane] = __ldg(p.bias_u + w.h * D + 32 * par + lane);
-      sb_w[32 + lane] = __ldg(p.bias_v + w.h * D + 32 * par + lane);
+      sb_w[lane] = bu_l;
+      sb_w[32 + lane] = bv_l;
       __syncwarp();
       if (!warp_wait(&bars->q_full, nQ & 1, wait_ns, abort)) return false;
       uint4 raw[4];
@@ -454,8 +456,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    if (sched_unit(0, blockIdx.x, gridDim.x) < p.n_units)
-      ok = build_q(decode_unit(sched_unit(0, blockIdx.x, gridDim.x), p.B, p.H, p.W, p.M, p.nqt), 0);
+    auto bias_of = [&](int u, const float* bias) -> float {
+      return __ldg(bias + decode_unit(u, p.B, p.H, p.W, p.M, p.nqt).h * D + 32 * par + lane);
+    };
+    if (sched_unit(0, blockIdx.x, gridDim.x) < p.n_units) {
+      const int u0 = sched_unit(0, blockIdx.x, gridDim.x);
+      ok = build_q(decode_unit(u0, p.B, p.H, p.W, p.M, p.nqt), 0, bias_of(u0, p.bias_u), bias_of(u0, p.bias_v));
+    }
 
     for (int rd = 0;; ++rd) {
       const int u = sched_unit(rd, blockIdx.x, gridDim.x);
@@ -463,6 +470,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int un_next = sched_unit(rd + 1, blockIdx.x, gridDim.x);
       const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
       const uint32_t g0 = gt;
+      const bool has_next = un_next < p.n_units;
+      const float bu_next = has_next ? bias_of(un_next, p.bias_u) : 0.f;
+      const float bv_next = has_next ? bias_of(un_next, p.bias_v) : 0.f;
       const int tl = w.nks - 1;
       const int first = (par - static_cast<int>(g0)) & 1;  // first local step of this warp
       float m_use = -INFINITY;  // running max in log2 units (lazy)
@@ -484,77 +494,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool diag = p.M + w.i0 - BN * t + quad * 32 < 63;  // some lane of the warp masks
         const float m_old = m_use;
         float m_new = m_use;
-        float sum = 0.f;
-        uint32_t pk[32];
-        uint32_t pb[16];
-        // One 32-column half: distance-window shift, scores, lazy running max,
-        // exponentials packed to bf16 pairs into pk[16h .. 16h+15].
-        auto half_step = [&](const uint32_t (&sraw)[32], const uint32_t (&lo)[16], const uint32_t (&hi)[16], auto hc) {
-          constexpr int h = decltype(hc)::value;
-          uint32_t bd[16];
-          window_shift_packed(lo, hi, lane, bd);
-          float x[32];
-          add_window(sraw, bd, x);
-          if (diag) {
-#pragma unroll
-            for (int k = 0; k < 32; ++k) x[k] = (32 * h + k <= lim) ? x[k] : -INFINITY;
+        // All of this step's TMEM reads at once -- the 96-distance window and
+        // both halves of S -- then one arrival hands the S buffer and the
+        // ring slots back to the MMA issuers.
+        float x[64];  // scores of the step's 64 columns
+        {
+          uint32_t bd0[16], bd1[16];
+          uint32_t s0[32], s1[32];
+          {
+            uint32_t xa[32], xb[32], xc[32];
+            tmem_ld32(tmem + lane_base + zcol(32 * quad), xa);
+            tmem_ld32(tmem + lane_base + zcol(32 * quad + 32), xb);
+            tmem_ld32(tmem + lane_base + zcol(32 * quad + 64), xc);
+            tmem_ld32(sc, s0);
+            tmem_ld32(sc + 32, s1);
+            tmem_wait_ld(xa);
+            tmem_wait_ld(xb);
+            tmem_wait_ld(xc);
+            tmem_wait_ld(s0);
+            tmem_wait_ld(s1);
+            warp_arrive_tc(&bars->sread[g & 3]);
+            uint32_t pa[16], pb[16], pc[16];
+            pack32(xa, pa);
+            pack32(xb, pb);
+            pack32(xc, pc);
+            // columns 0-31 use window positions [32, 96), columns 32-63 [0, 64)
+            window_shift_packed(pb, pc, lane, bd0);
+            window_shift_packed(pa, pb, lane, bd1);
           }
-          float t3[11];
+          float* x0 = x;
+          float* x1 = x + 32;
+          add_window(s0, bd0, x0);
+          add_window(s1, bd1, x1);
+        }
+        if (diag) {
 #pragma unroll
-          for (int n = 0; n < 10; ++n) t3[n] = max3f(x[3 * n], x[3 * n + 1], x[3 * n + 2]);
-          t3[10] = fmaxf(x[30], x[31]);
-          const float mx = max3f(max3f(t3[0], t3[1], t3[2]), max3f(t3[3], t3[4], t3[5]),
-                                 max3f(max3f(t3[6], t3[7], t3[8]), t3[9], t3[10])) * sl2;
-          if (mx > m_new + kLazy) {
-            if constexpr (h == 1) {  // rare: rescale the first half to the new max
-              const float r = ex2(m_new - mx);
-              sum *= r;
+          for (int k = 0; k < 64; ++k) x[k] = (k <= lim) ? x[k] : -INFINITY;
+        }
+        // Lazy running max over the step's 64 scores (log2 units).
+        float t3[22];
 #pragma unroll
-              for (int n = 0; n < 16; ++n) pk[n] = pack_bf16x2(bf16_lo(pk[n]) * r, bf16_hi(pk[n]) * r);
-            }
-            m_new = mx;
-          }
-          // A row with no visible key yet keeps m_new = -inf; its exponents
-          // are then taken against 0 (all -inf, so every p is 0).
-          const float m_eff = (m_new == -INFINITY) ? 0.f : m_new;
+        for (int n = 0; n < 21; ++n) t3[n] = max3f(x[3 * n], x[3 * n + 1], x[3 * n + 2]);
+        t3[21] = x[63];
+        float u7[8];
+#pragma unroll
+        for (int n = 0; n < 7; ++n) u7[n] = max3f(t3[3 * n], t3[3 * n + 1], t3[3 * n + 2]);
+        u7[7] = t3[21];
+        const float mx = max3f(max3f(u7[0], u7[1], u7[2]), max3f(u7[3], u7[4], u7[5]), fmaxf(u7[6], u7[7])) * sl2;
+        if (mx > m_new + kLazy) m_new = mx;
+        // A row with no visible key yet keeps m_new = -inf; its exponents are
+        // then taken against 0 (all -inf, so every p is 0).
+        const float m_eff = (m_new == -INFINITY) ? 0.f : m_new;
+        uint32_t pk[32];  // P row, bf16 pairs
+        float sum;
+        {
           float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
           const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_eff, -m_eff);
 #pragma unroll
-          for (int n = 0; n < 16; ++n) {
+          for (int n = 0; n < 32; ++n) {
             const float2 y = __ffma2_rn(make_float2(x[2 * n], x[2 * n + 1]), sc2, nm2);
             const float2 e = make_float2(ex2(y.x), ex2(y.y));
             if (n & 1)
               acc1 = __fadd2_rn(acc1, e);
             else
               acc0 = __fadd2_rn(acc0, e);
-            pk[16 * h + n] = pack_bf16x2(e.x, e.y);
+            pk[n] = pack_bf16x2(e.x, e.y);
           }
-          sum += (acc0.x + acc0.y) + (acc1.x + acc1.y);
-        };
-        // All of this step's TMEM reads at once -- the 96-distance window and
-        // both halves of S -- then one arrival hands the S buffer and the
-        // ring slots back to the MMA issuers.
-        uint32_t pa[16], pc[16];
-        uint32_t s0[32], s1[32];
-        {
-          uint32_t xa[32], xb[32], xc[32];
-          tmem_ld32(tmem + lane_base + zcol(32 * quad), xa);
-          tmem_ld32(tmem + lane_base + zcol(32 * quad + 32), xb);
-          tmem_ld32(tmem + lane_base + zcol(32 * quad + 64), xc);
-          tmem_ld32(sc, s0);
-          tmem_ld32(sc + 32, s1);
-          tmem_wait_ld(xa);
-          tmem_wait_ld(xb);
-          tmem_wait_ld(xc);
-          tmem_wait_ld(s0);
-          tmem_wait_ld(s1);
-          warp_arrive_tc(&bars->sread[g & 3]);
-          pack32(xa, pa);
-          pack32(xb, pb);
-          pack32(xc, pc);
+          sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
-        half_step(s0, pb, pc, std::integral_constant<int, 0>{});
-        half_step(s1, pa, pb, std::integral_constant<int, 1>{});
         const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);  // m_new >= m_old
         l_run = l_run * alpha + sum;
         // The PV of step g-2 (same P buffer, same accumulator) must be done
@@ -594,16 +601,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The next unit's (q+u), (q+v) go to the other buffer once this
         // warp's first step of this unit has seen its scores: the MMAs of the
         // unit before, which read that buffer, are complete by then.
-        if (t == first && un_next < p.n_units &&
-            !(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1)))
+        if (t == first && has_next &&
+            !(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1, bu_next, bv_next)))
           break;
       }
       if (!ok) break;
-      if (first > tl && un_next < p.n_units) {
+      if (first > tl && has_next) {
         // No step of this unit: build after its last step's scores instead.
         const uint32_t gl = g0 + tl;
         if (!(ok = warp_wait(&bars->s_full[gl & 1], (gl >> 1) & 1, wait_ns, abort))) break;
-        if (!(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1))) break;
+        if (!(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1, bu_next, bv_next))) break;
       }
       // The warps of the unit's last step merge the two accumulators and
       // write the output; the other parity hands over its (m, l) and moves on
