@@ -542,28 +542,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         u7[7] = t3[21];
         const float mx = max3f(max3f(u7[0], u7[1], u7[2]), max3f(u7[3], u7[4], u7[5]), fmaxf(u7[6], u7[7])) * sl2;
         if (mx > m_new + kLazy) m_new = mx;
-        // A row with no visible key yet keeps m_new = -inf; its exponents are
-        // then taken against 0 (all -inf, so every p is 0).
-        const float m_eff = (m_new == -INFINITY) ? 0.f : m_new;
-        uint32_t pk[32];  // P row, bf16 pairs
-        float sum;
-        {
-          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
-          const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_eff, -m_eff);
-#pragma unroll
-          for (int n = 0; n < 32; ++n) {
-            const float2 y = __ffma2_rn(make_float2(x[2 * n], x[2 * n + 1]), sc2, nm2);
-            const float2 e = make_float2(ex2(y.x), ex2(y.y));
-            if (n & 1)
-              acc1 = __fadd2_rn(acc1, e);
-            else
-              acc0 = __fadd2_rn(acc0, e);
-            pk[n] = pack_bf16x2(e.x, e.y);
-          }
-          sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
-        }
         const float alpha = (m_old == -INFINITY) ? 0.f : ex2(m_old - m_new);  // m_new >= m_old
-        l_run = l_run * alpha + sum;
         // The PV of step g-2 (same P buffer, same accumulator) must be done
         // before P is overwritten or O rescaled.
         if (g >= 2 && !(ok = warp_wait(&bars->pv_done[sb], ((g - 2) >> 1) & 1, wait_ns, abort))) break;
@@ -588,14 +567,35 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
           store_pending = false;
         }
+        // A row with no visible key yet keeps m_new = -inf; its exponents are
+        // then taken against 0 (all -inf, so every p is 0).
+        const float m_eff = (m_new == -INFINITY) ? 0.f : m_new;
+        float sum;
         {
-          // P row a into buffer sb (128B-swizzled K-major, as (q+u)).
+          // Exponentials, their row sum, and the P row a into buffer sb
+          // (128B-swizzled K-major, as (q+u)), eight columns per store.
           uint8_t* prow = sP + sb * kQTile + (a / 8) * 1024 + (a % 8) * 128;
+          float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+          const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_eff, -m_eff);
 #pragma unroll
-          for (int c = 0; c < BN / 8; ++c)
-            *reinterpret_cast<uint4*>(prow + ((c ^ (a % 8)) * 16)) =
-                make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
+          for (int c = 0; c < BN / 8; ++c) {
+            uint32_t pk[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const int n = 4 * c + i;
+              const float2 y = __ffma2_rn(make_float2(x[2 * n], x[2 * n + 1]), sc2, nm2);
+              const float2 e = make_float2(ex2(y.x), ex2(y.y));
+              if (i & 1)
+                acc1 = __fadd2_rn(acc1, e);
+              else
+                acc0 = __fadd2_rn(acc0, e);
+              pk[i] = pack_bf16x2(e.x, e.y);
+            }
+            *reinterpret_cast<uint4*>(prow + ((c ^ (a % 8)) * 16)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+          }
+          sum = (acc0.x + acc0.y) + (acc1.x + acc1.y);
         }
+        l_run = l_run * alpha + sum;
         tc_fence_before();  // orders the O rescale's tcgen05.st before the arrive
         warp_arrive_smem(&bars->p_full[sb]);
         // The next unit's (q+u), (q+v) go to the other buffer once this
