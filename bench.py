@@ -3,8 +3,8 @@
 
 One step = one steady-state segment of the base workload (B=22, H=8, D=64,
 W=512, M=512, bf16) through every row of the path: the sinusoidal distance
-table, the memory roll of k and v (previous segment's buffer -> head of this
-segment's buffer) and the fused relative attention.  Inputs are seeded and
+table and the fused relative attention, which also performs the memory roll
+of k and v (this segment's buffer -> head of the next segment's buffer).  Inputs are seeded and
 synthetic (hidden ~ N(0,1) projected by N(0, 0.02^2) weights), resident in
 HBM; eight segment buffers (~0.5 GB) rotate so that consecutive steps touch
 memory larger than L2.
@@ -203,7 +203,7 @@ class SegmentStream:
 
     Buffer t holds stream rows [tW, tW + M + W): its head (M rows) is the
     memory, its tail (W rows) the segment.  The roll of step t writes the head
-    of buffer t from buffer t-1, which reproduces the same rows."""
+    of buffer t+1 from buffer t, which reproduces the same rows."""
 
     def __init__(self, wl, device, seed):
         import torch
@@ -225,8 +225,6 @@ class SegmentStream:
         self.k = [dev(seg.k[:, t * wl.W:t * wl.W + L]) for t in range(S)]
         self.v = [dev(seg.v[:, t * wl.W:t * wl.W + L]) for t in range(S)]
         self.q = [dev(seg.q[:, t * wl.W + wl.M:t * wl.W + L]) for t in range(S)]
-        self.kf = [x.view(wl.B, L, C) for x in self.k]
-        self.vf = [x.view(wl.B, L, C) for x in self.v]
         # two output buffers: step t writes o[t % 2] while step t-1's is read back
         self.o2 = [torch.empty(wl.B, wl.W, wl.H, wl.D, device=device, dtype=bf) for _ in range(2)]
         # the distance table comes from the library; its projection r = R W_{k,R}
@@ -245,39 +243,27 @@ class SegmentStream:
         self.h2d_stream = torch.cuda.Stream(device=device)
         self.d2h_stream = torch.cuda.Stream(device=device)
 
-    def roll(self, t):
-        """Memory update feeding segment t: the last M rows of segment t-1's
-        [memory ; segment] buffer become the head of segment t's buffer."""
-        import transformer_xl_relative_txl_gb300 as txl
-
-        wl = self.wl
-        S = N_SEG_BUFFERS
-        cur, prev = t % S, (t - 1) % S
-        txl.txl_mem_update(self.kf[prev][:, :wl.M], self.kf[prev][:, wl.M:], self.kf[cur], wl.M)
-        txl.txl_mem_update(self.vf[prev][:, :wl.M], self.vf[prev][:, wl.M:], self.vf[cur], wl.M)
-
     def step(self, t, ev=None):
         """One pass of the hot path for segment t, in order on one stream: the
-        distance table, the memory roll of k and v (segment t-1's buffer ->
-        the head of segment t's), and the relative attention.  (The attention
-        is a persistent kernel that fills every SM, so nothing is overlapped
-        with it.)  Returns the number of library kernels launched."""
+        distance table, then the relative attention with the memory roll of k
+        and v in the same call (the last M rows of this segment's buffer go to
+        the head of segment t+1's).  Returns the number of library kernels
+        launched."""
         import torch
 
         import transformer_xl_relative_txl_gb300 as txl
 
         wl = self.wl
-        cur = t % N_SEG_BUFFERS
+        cur, nxt = t % N_SEG_BUFFERS, (t + 1) % N_SEG_BUFFERS
         main = torch.cuda.current_stream()
         txl.txl_sinusoid_rel(self.R)
-        self.roll(t)
         if ev is not None:
             ev[0].record(main)
-        txl.txl_relattn_forward(self.q[cur], self.k[cur], self.v[cur], self.r, self.u, self.vb, self.o2[t % 2], None,
-                                M=wl.M)
+        txl.txl_relattn_forward_roll(self.q[cur], self.k[cur], self.v[cur], self.r, self.u, self.vb,
+                                     self.o2[t % 2], self.k[nxt][:, :wl.M], self.v[nxt][:, :wl.M], wl.M, M=wl.M)
         if ev is not None:
             ev[1].record(main)
-        return 4
+        return 2
 
     def run_e2e(self, t0, E):
         """E steps through the public API with host buffers, pipelined the way
@@ -453,8 +439,8 @@ def run_ours(args):
                    "parallelism": f"dp{world} (each rank its own {wl.B} sequences)",
                    "l2": f"inputs larger than L2: {N_SEG_BUFFERS} rotating segment buffers "
                          f"(~{N_SEG_BUFFERS * (2 * wl.B * (wl.M + wl.W) + wl.B * wl.W) * wl.H * wl.D * 2 / 1e9:.2f} GB)",
-                   "step": "txl_sinusoid_rel + txl_mem_update(k) + txl_mem_update(v) + txl_relattn_forward, "
-                           "in order on one stream"},
+                   "step": "txl_sinusoid_rel + txl_relattn_forward_roll (attention and the memory roll of k "
+                           "and v in one kernel), in order on one stream"},
         "tflops": achieved,
         "attn_ms": k1_ms,
         "roofline": {"kernel": "relattn_tc64_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,

@@ -10,6 +10,8 @@
  *     online softmax and P.V;
  *   - txl_mem_update: the memory roll, keeping the last M rows of
  *     [memory ; segment];
+ *   - txl_relattn_forward_roll: both of the above in one call (the roll
+ *     done by the attention kernel from the tiles it loads, where it can);
  *   - txl_sinusoid_rel: the parameter-free sinusoidal distance table R.
  *
  * Conventions shared by every entry point
@@ -37,7 +39,7 @@
 extern "C" {
 #endif
 
-#define TXL_VERSION 100 /* 1.0.0 */
+#define TXL_VERSION 110 /* 1.1.0 */
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -129,6 +131,41 @@ TXL_API int txl_relattn_forward(const void* q, const void* k, const void* v, con
 TXL_API int txl_mem_update(const void* mem, int m_prev, const void* h, int w, void* mem_out, int m,
                    int B, int C, long long mem_bs, long long h_bs, long long out_bs,
                    int* m_out, txl_dtype dtype, cudaStream_t stream);
+
+/*
+ * txl_relattn_forward_roll -- txl_relattn_forward and the memory roll of its
+ * keys and values in one call.
+ *
+ * The result is exactly that of txl_relattn_forward(q, k, v, ...) followed
+ * by txl_mem_update on k and on v, each with mem = the call's memory rows
+ * (m_prev = M), h = its segment rows (w = W) and the batch stride of k and v
+ * ((M+W)*H*D elements): k_mem_out and v_mem_out receive the last
+ * m' = min(m, M+W) rows of [memory ; segment] of every sequence, bit for bit
+ * ("Long-context transformers", segment recurrence: the cache for the next
+ * segment is the tail of this one's keys and values).
+ *
+ *   k_mem_out, v_mem_out  device, [B, m', H, D] rows with batch stride
+ *                         mem_out_bs elements (>= m'*H*D), `dtype`; must not
+ *                         overlap each other or any input or output of the
+ *                         attention (TXL_ERR_ALIAS)
+ *   m                     memory length to keep (>= 0)
+ *   m_out                 host, receives m' (may be NULL)
+ *
+ * On the bf16 D = 64 path, when the kept rows start on a 64-row tile
+ * boundary of k and v (M+W-m' a multiple of 64) and k_mem_out, v_mem_out and
+ * the stride are 16-byte aligned, the attention kernel writes the kept rows
+ * itself, from the key and value tiles it has already loaded, with tensor
+ * stores; otherwise the call runs the attention and then the roll kernel.
+ * Other arguments and errors as txl_relattn_forward and txl_mem_update.  This
+ * fused form has no counterpart on the pages: it is a scheduling of their
+ * two steps.
+ */
+TXL_API int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const void* r,
+                             const float* bias_u, const float* bias_v, void* o, float* lse,
+                             int B, int W, int M, int H, int D, int n_r, float scale,
+                             txl_dtype dtype, txl_dtype o_dtype,
+                             void* k_mem_out, void* v_mem_out, int m, long long mem_out_bs, int* m_out,
+                             cudaStream_t stream);
 
 /*
  * txl_sinusoid_rel -- the raw sinusoidal distance table R[n_dist, dim].

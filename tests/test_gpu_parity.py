@@ -8,7 +8,7 @@ import pytest
 import torch
 
 from oracle import txl_oracle as O
-from synthetic import WORKLOADS, make_segments, project_r
+from synthetic import WORKLOADS, make_prefilled, make_segments, project_r
 
 from gpu_util import (BF16_ATOL, F32_ATOL, assert_bf16_close, dev, prefilled_case, run_forward, to_dev,
                       torch_dtype, workload)
@@ -292,4 +292,82 @@ def test_full_size_base_recurrence_sampled(_lib):
         # the GPU roll produced exactly the oracle's memory
         gk = nk[:, :m_tau].float().cpu().numpy().reshape(wl.B, m_tau, wl.H, wl.D)
         assert np.array_equal(gk, mem_k)
+    assert _lib.txl_get_device_status() == 0
+
+
+# ----------------------------------------------------------------------------
+# Attention with the memory roll in one call (txl_relattn_forward_roll)
+# ----------------------------------------------------------------------------
+
+ROLL_CASES = [
+    # B, H, D, W, M, m        (M+W-m' a multiple of 64 -> written by the attention kernel)
+    (2, 2, 64, 128, 64, 64),     # fused: kept rows are segment rows
+    (2, 1, 64, 256, 256, 256),   # fused
+    (1, 2, 64, 64, 1000, 1000),  # fused: kept rows start inside the memory
+    (1, 1, 64, 128, 0, 512),     # fused: m > M+W keeps every row
+    (1, 2, 64, 300, 384, 100),   # fused: 684-100 = 584 is not a multiple of 64 -> separate roll
+    (2, 2, 64, 200, 150, 150),   # separate roll (350-150 = 200)
+    (1, 2, 128, 200, 150, 64),   # D = 128: separate roll
+    (2, 2, 64, 128, 64, 0),      # m = 0: no roll
+]
+
+
+@pytest.mark.parametrize("B,H,D,W,M,m", ROLL_CASES)
+def test_forward_roll(_lib, B, H, D, W, M, m):
+    wl = workload(B, H, D, W, M)
+    q, k, v, r, bu, bv = prefilled_case(wl, n_r_extra=3)
+    L, keep = M + W, min(m, M + W)
+    qd, kd, vd, rd = (to_dev(x, torch.bfloat16) for x in (q, k, v, r))
+    o = torch.empty(qd.shape, device=dev(), dtype=torch.bfloat16)
+    # memory outputs: the head of larger buffers (batch stride != keep rows), prefilled with a sentinel
+    rows = max(keep, 1) + 37
+    km = torch.full((B, rows, H, D), 7.0, device=dev(), dtype=torch.bfloat16)
+    vm = torch.full((B, rows, H, D), -7.0, device=dev(), dtype=torch.bfloat16)
+    got_keep = _lib.txl_relattn_forward_roll(qd, kd, vd, rd, to_dev(bu, torch.float32), to_dev(bv, torch.float32),
+                                             o, km[:, :max(keep, 1)], vm[:, :max(keep, 1)], m, M=M)
+    assert _lib.txl_get_device_status() == 0
+    assert got_keep == keep
+    eo, _ = O.relattn_forward(q, k, v, r, bu, bv, M)
+    assert_bf16_close(o.float().cpu().numpy(), eo, f"o {B,H,D,W,M,m}")
+    C = H * D
+    for dev_out, src, fill in ((km, k, 7.0), (vm, v, -7.0)):
+        out = dev_out.float().cpu().numpy()
+        want = O.mem_update(src[:, :M].reshape(B, M, C), src[:, M:].reshape(B, W, C), m).reshape(B, keep, H, D)
+        assert np.array_equal(out[:, :keep], want), "kept rows differ"
+        assert np.all(out[:, keep:] == fill), "rows past m' were written"
+
+
+def test_forward_roll_base_segments(_lib):
+    """Base workload, three segments from a full memory: each call's fused
+    roll feeds the next call, against the separate attention + roll calls."""
+    wl = WORKLOADS["base"]
+    seg = make_segments(wl, n_segments=3)
+    r = project_r(O.sinusoid_rel(wl.M + wl.W, wl.d_model), seg.W_r, wl.H, wl.D, "bf16")
+    L = wl.M + wl.W
+    rd = to_dev(r, torch.bfloat16)
+    ud, vd = to_dev(seg.bias_u, torch.float32), to_dev(seg.bias_v, torch.float32)
+    q0, k0, v0, _ = make_prefilled(wl, wl.M, seed=1)
+    bufs = {n: [torch.empty(wl.B, L, wl.H, wl.D, device=dev(), dtype=torch.bfloat16) for _ in range(2)]
+            for n in ("fk", "fv", "sk", "sv")}
+    for n, src in (("fk", k0), ("fv", v0), ("sk", k0), ("sv", v0)):
+        bufs[n][0].copy_(to_dev(src, torch.bfloat16))
+    for tau in range(3):
+        cur, nxt = tau % 2, 1 - tau % 2
+        qt = to_dev(seg.seg("q", tau), torch.bfloat16)
+        for n in ("fk", "sk"):
+            bufs[n][cur][:, wl.M:] = to_dev(seg.seg("k", tau), torch.bfloat16)
+        for n in ("fv", "sv"):
+            bufs[n][cur][:, wl.M:] = to_dev(seg.seg("v", tau), torch.bfloat16)
+        of = torch.empty(qt.shape, device=dev(), dtype=torch.bfloat16)
+        os_ = torch.empty(qt.shape, device=dev(), dtype=torch.bfloat16)
+        _lib.txl_relattn_forward_roll(qt, bufs["fk"][cur], bufs["fv"][cur], rd, ud, vd, of,
+                                      bufs["fk"][nxt][:, :wl.M], bufs["fv"][nxt][:, :wl.M], wl.M, M=wl.M)
+        _lib.txl_relattn_forward(qt, bufs["sk"][cur], bufs["sv"][cur], rd, ud, vd, os_, None, M=wl.M)
+        C = wl.H * wl.D
+        for n in ("sk", "sv"):
+            b = bufs[n][cur].view(wl.B, L, C)
+            _lib.txl_mem_update(b[:, :wl.M], b[:, wl.M:], bufs[n][nxt].view(wl.B, L, C), wl.M)
+        assert torch.equal(of, os_), f"segment {tau}: outputs differ"
+        assert torch.equal(bufs["fk"][nxt][:, :wl.M], bufs["sk"][nxt][:, :wl.M]), f"segment {tau}: k memory"
+        assert torch.equal(bufs["fv"][nxt][:, :wl.M], bufs["sv"][nxt][:, :wl.M]), f"segment {tau}: v memory"
     assert _lib.txl_get_device_status() == 0

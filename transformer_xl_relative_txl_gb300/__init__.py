@@ -16,7 +16,7 @@ import torch
 
 __all__ = [
     "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
-    "txl_relattn_forward", "txl_mem_update", "txl_sinusoid_rel",
+    "txl_relattn_forward", "txl_relattn_forward_roll", "txl_mem_update", "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
 ]
@@ -35,6 +35,9 @@ lib = ctypes.CDLL(library_path)
 _p, _i, _ll, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
 lib.txl_relattn_forward.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
 lib.txl_relattn_forward.restype = _i
+lib.txl_relattn_forward_roll.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _i,
+                                         _p, _p, _i, _ll, ctypes.POINTER(_i), _p]
+lib.txl_relattn_forward_roll.restype = _i
 lib.txl_mem_update.argtypes = [_p, _i, _p, _i, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i, _p]
 lib.txl_mem_update.restype = _i
 lib.txl_sinusoid_rel.argtypes = [_p, _i, _i, _i, _p]
@@ -115,6 +118,47 @@ def txl_relattn_forward(q, k, v, r, bias_u, bias_v, o, lse=None, M=None, scale=N
                                  _dtype_code(o.dtype), _stream(stream))
     _check(st, "txl_relattn_forward")
     return o
+
+
+def txl_relattn_forward_roll(q, k, v, r, bias_u, bias_v, o, k_mem_out, v_mem_out, m, lse=None, M=None, scale=None,
+                             stream=None) -> int:
+    """txl_relattn_forward, then the memory roll of k and v: k_mem_out and
+    v_mem_out [B, >= m', H, D] (row-contiguous views; batch strides may be
+    any, equal for both) receive the last m' = min(m, M+W) rows of k and v.
+    Returns m'."""
+    B, W, H, D = q.shape
+    if M is None:
+        M = k.shape[1] - W
+    for t in (q, k, v, r, bias_u, bias_v, o) + ((lse,) if lse is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k.shape != (B, M + W, H, D) or v.shape != k.shape or o.shape != q.shape:
+        raise ValueError("shape mismatch between q, k, v, o")
+    if r.dim() != 3 or r.shape[1:] != (H, D) or bias_u.shape != (H, D) or bias_v.shape != (H, D):
+        raise ValueError("r must be [n_r, H, D]; biases [H, D]")
+    if bias_u.dtype != torch.float32 or bias_v.dtype != torch.float32:
+        raise ValueError("biases are fp32")
+    if lse is not None and (lse.shape != (B, H, W) or lse.dtype != torch.float32):
+        raise ValueError("lse must be fp32 [B, H, W]")
+    if not (q.dtype == k.dtype == v.dtype == r.dtype == k_mem_out.dtype == v_mem_out.dtype):
+        raise ValueError("q, k, v, r and the memory outputs must share a dtype")
+    keep = min(m, M + W)
+    for t, name in ((k_mem_out, "k_mem_out"), (v_mem_out, "v_mem_out")):
+        if t.dim() != 4 or t.shape[0] != B or t.shape[2:] != (H, D) or t.shape[1] < keep:
+            raise ValueError(f"{name} must be [B, >= m', H, D]")
+        if t.stride(3) != 1 or t.stride(2) != D or (t.shape[1] > 1 and t.stride(1) != H * D):
+            raise ValueError(f"{name} rows must be contiguous")
+    if k_mem_out.stride(0) != v_mem_out.stride(0):
+        raise ValueError("k_mem_out and v_mem_out must share a batch stride")
+    if scale is None:
+        scale = D ** -0.5
+    m_out = ctypes.c_int(0)
+    st = lib.txl_relattn_forward_roll(_ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(bias_u), _ptr(bias_v), _ptr(o),
+                                      _ptr(lse), B, W, M, H, D, r.shape[0], float(scale), _dtype_code(q.dtype),
+                                      _dtype_code(o.dtype), _ptr(k_mem_out), _ptr(v_mem_out), m,
+                                      k_mem_out.stride(0), ctypes.byref(m_out), _stream(stream))
+    _check(st, "txl_relattn_forward_roll")
+    return m_out.value
 
 
 def _rows_view(t, name):

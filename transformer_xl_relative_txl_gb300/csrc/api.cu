@@ -186,9 +186,27 @@ int txl_mem_update(const void* mem, int m_prev, const void* h, int w, void* mem_
                                         row_bytes, mem_bs * es, h_bs * es, out_bs * es, stream));
 }
 
-int txl_relattn_forward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
-                        const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r,
-                        float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {
+}  // extern "C"
+
+namespace {
+
+// Memory roll done by the attention kernel itself: the kept rows
+// [src0, M+W) of k and v go to k_out / v_out (batch stride out_bs elements).
+struct FusedRoll {
+  void* k_out;
+  void* v_out;
+  long long keep, src0, out_bs;
+};
+
+// The attention (validated arguments); `roll` non-null asks the D = 64
+// kernel to write the memory roll too (the caller has checked it can).
+int forward_impl(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                 const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
+                 txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, cudaStream_t stream);
+
+int check_forward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                  const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
+                  txl_dtype dtype, txl_dtype o_dtype) {
   if (B < 0 || W < 0 || M < 0 || H <= 0 || D <= 0 || !dtype_ok(dtype) || !dtype_ok(o_dtype))
     return TXL_ERR_INVALID_ARG;
   if (B == 0 || W == 0) return TXL_OK;
@@ -219,10 +237,23 @@ int txl_relattn_forward(const void* q, const void* k, const void* v, const void*
     for (Range x : {rq, rk, rv, rr, ru, rb, ro})
       if (overlap(rl, x)) return TXL_ERR_ALIAS;
   }
-
   if (dtype == TXL_F32) {
     if (o_dtype != TXL_F32 || D > 256 || B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
     if (sizeof(float) * (2 * static_cast<size_t>(D) + L) > 220 * 1024) return TXL_ERR_UNSUPPORTED;
+  } else {
+    if (D != 64 && D != 128) return TXL_ERR_UNSUPPORTED;
+    const long long nqt = (W + 127) / 128;
+    if (nqt * B * H > 0x7FFFFFFFLL || L > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
+  }
+  return TXL_OK;
+}
+
+int forward_impl(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                 const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
+                 txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, cudaStream_t stream) {
+  const long long L = static_cast<long long>(M) + W;
+  const size_t hd = static_cast<size_t>(H) * D;
+  if (dtype == TXL_F32) {
     return from_cuda(txl::launch_relattn_f32(
         static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
         static_cast<const float*>(r), bias_u, bias_v, static_cast<float*>(o), lse, B, W, M, H, D, scale,
@@ -230,9 +261,6 @@ int txl_relattn_forward(const void* q, const void* k, const void* v, const void*
   }
 
   // bf16 tensor-core path
-  if (D != 64 && D != 128) return TXL_ERR_UNSUPPORTED;
-  const long long nqt = (W + 127) / 128;
-  if (nqt * B * H > 0x7FFFFFFFLL || L > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return TXL_ERR_CUDA;
   CUtensorMap tm_q, tm_k, tm_v, tm_r;
@@ -275,15 +303,101 @@ int txl_relattn_forward(const void* q, const void* k, const void* v, const void*
     const cuuint32_t box[4] = {64, 1, 32, 1};
     if (!encode_bf16(&tm_o, o, 4, dims, strides, box)) return TXL_ERR_CUDA;
   }
+  // Memory-roll outputs: [B, keep, H, D] with batch stride out_bs, stored
+  // from the kernel's 64-row key and value tiles.
+  CUtensorMap tm_km, tm_vm;
+  if (roll != nullptr) {
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(roll->keep), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2,
+                                   static_cast<cuuint64_t>(roll->out_bs) * 2};
+    const cuuint32_t box[4] = {64, 1, 64, 1};
+    if (!encode_bf16(&tm_km, roll->k_out, 4, dims, strides, box) ||
+        !encode_bf16(&tm_vm, roll->v_out, 4, dims, strides, box))
+      return TXL_ERR_CUDA;
+  }
   txl::WaitCtl wc;
   if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
   wc.limit_ns = g_wait_ns.load();
   wc.inject_stall = g_inject_stall.exchange(0);
   if (D == 64)
-    return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, o_tma ? &tm_o : nullptr, bias_u, bias_v, o,
-                                              lse, B, W, M, H, o_dtype == TXL_BF16, scale, wc, stream));
+    return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, o_tma ? &tm_o : nullptr,
+                                              roll ? &tm_km : nullptr, roll ? &tm_vm : nullptr,
+                                              roll ? static_cast<int>(roll->src0) : -1, bias_u, bias_v, o, lse, B,
+                                              W, M, H, o_dtype == TXL_BF16, scale, wc, stream));
   return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H, D,
                                           o_dtype == TXL_BF16, scale, wc, stream));
+}
+
+}  // namespace
+
+extern "C" {
+
+int txl_relattn_forward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                        const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r,
+                        float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {
+  const int st = check_forward(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype);
+  if (st != TXL_OK || B == 0 || W == 0) return st;
+  return forward_impl(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype, nullptr,
+                      stream);
+}
+
+int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                             const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r,
+                             float scale, txl_dtype dtype, txl_dtype o_dtype, void* k_mem_out, void* v_mem_out,
+                             int m, long long mem_out_bs, int* m_out, cudaStream_t stream) {
+  const int st = check_forward(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype);
+  if (st != TXL_OK) return st;
+  if (m < 0) return TXL_ERR_INVALID_ARG;
+  const long long L = static_cast<long long>(M) + W;
+  const long long keep = std::min<long long>(m, L);
+  const long long C = static_cast<long long>(H) * D;
+  if (B == 0 || W == 0) {
+    if (m_out != nullptr) *m_out = static_cast<int>(keep);
+    return TXL_OK;
+  }
+  if (keep > 0) {
+    if (k_mem_out == nullptr || v_mem_out == nullptr || mem_out_bs < 0) return TXL_ERR_INVALID_ARG;
+    if (B > 1 && mem_out_bs < keep * C) return TXL_ERR_INVALID_ARG;
+    // Roll outputs against each other and against everything the attention touches.
+    const size_t es = dsize(dtype);
+    const size_t out_bytes = static_cast<size_t>(((B - 1) * mem_out_bs + keep * C) * static_cast<long long>(es));
+    const Range rkm = range_of(k_mem_out, out_bytes), rvm = range_of(v_mem_out, out_bytes);
+    if (overlap(rkm, rvm)) return TXL_ERR_ALIAS;
+    const size_t hd = static_cast<size_t>(C);
+    const Range others[] = {range_of(q, B * static_cast<size_t>(W) * hd * es),
+                            range_of(k, B * static_cast<size_t>(L) * hd * es),
+                            range_of(v, B * static_cast<size_t>(L) * hd * es),
+                            range_of(r, static_cast<size_t>(n_r) * hd * es),
+                            range_of(bias_u, hd * 4),
+                            range_of(bias_v, hd * 4),
+                            range_of(o, B * static_cast<size_t>(W) * hd * dsize(o_dtype)),
+                            range_of(lse, lse ? B * static_cast<size_t>(H) * W * 4 : 0)};
+    for (const Range& x : others)
+      if (overlap(rkm, x) || overlap(rvm, x)) return TXL_ERR_ALIAS;
+  }
+  if (m_out != nullptr) *m_out = static_cast<int>(keep);
+  // Fused when the kept rows start on a 64-row tile of the D = 64 bf16 kernel.
+  const bool fused = keep > 0 && dtype == TXL_BF16 && D == 64 && (L - keep) % 64 == 0 &&
+                     aligned(k_mem_out, 16) && aligned(v_mem_out, 16) && (mem_out_bs * 2) % 16 == 0 &&
+                     keep <= 0x7FFFFFFFLL;
+  if (fused) {
+    const FusedRoll fr{k_mem_out, v_mem_out, keep, L - keep, mem_out_bs};
+    return forward_impl(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype, &fr,
+                        stream);
+  }
+  int rc = forward_impl(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype, nullptr,
+                        stream);
+  if (rc != TXL_OK || keep == 0) return rc;
+  const long long bs = L * C;
+  const size_t es = dsize(dtype);
+  const char* kb = static_cast<const char*>(k);
+  const char* vb = static_cast<const char*>(v);
+  rc = txl_mem_update(kb, M, kb + static_cast<size_t>(M) * C * es, W, k_mem_out, m, B, static_cast<int>(C), bs,
+                      bs, mem_out_bs, nullptr, dtype, stream);
+  if (rc != TXL_OK) return rc;
+  return txl_mem_update(vb, M, vb + static_cast<size_t>(M) * C * es, W, v_mem_out, m, B, static_cast<int>(C), bs,
+                        bs, mem_out_bs, nullptr, dtype, stream);
 }
 
 }  // extern "C"

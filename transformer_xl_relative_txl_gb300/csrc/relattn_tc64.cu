@@ -87,7 +87,8 @@ constexpr float kLazy = 8.0f;  // log2 headroom before a running max moves
 
 constexpr int kRowTile = BN * 128;  // 64 rows x 64 bf16 (8 KB)
 constexpr int kQTile = BM * 128;    // 128 rows x 64 bf16 (16 KB)
-constexpr int NK = 4, NV = 4, NR = 4;
+constexpr int NK = 4, NV = 4, NR = 4;  // K, V, R tile stages
+static_assert(NK == NV, "K and V tiles share the loader's stage logic");
 constexpr int kOffQ = 0;                        // raw q tile of the next unit (TMA)
 constexpr int kOffQu = kOffQ + kQTile;          // (q+u): 2 buffers
 constexpr int kOffQv = kOffQu + 2 * kQTile;     // (q+v): 2 buffers
@@ -113,6 +114,7 @@ struct Params {
   unsigned int* status;
   unsigned long long wait_ns;
   int inject_stall;
+  int roll_src0;  // >= 0: memory roll of k, v rows [roll_src0, M+W) by the last query tile's units
 };
 
 struct Bars {
@@ -132,7 +134,8 @@ template <bool O_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     relattn_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
-                        const __grid_constant__ CUtensorMap tm_o, const Params p) {
+                        const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_km,
+                        const __grid_constant__ CUtensorMap tm_vm, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -199,6 +202,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_r);
       uint32_t nQ = 0, nK = 0, nV = 0, nR = 0;
       bool ok = true, stop = false;
+      // Memory roll: the unit of the last query tile of each (batch, head)
+      // loads every key and value row once.  A K or V tile whose rows lie in
+      // the kept range is stored from its stage to the memory output just
+      // before the stage is refilled (its MMA has consumed it by then), or at
+      // the end.  Per K and per V stage: destination row of the pending store
+      // (-1: none), batch and head (kept apart for K and V: a K stage is
+      // refilled before the V stage of the same index).
+      int pk_row[NK], pk_b[NK], pk_h[NK], pv_row[NK], pv_b[NK], pv_h[NK];
+#pragma unroll
+      for (int s = 0; s < NK; ++s) pk_row[s] = pv_row[s] = -1;
+      auto flush_store = [&](int* prow, const int* pb, const int* ph, int s, const CUtensorMap* map,
+                             uint8_t* stage) {
+        if (prow[s] >= 0) {
+          tma_store_4d(map, stage, 0, ph[s], prow[s], pb[s]);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the stage is refilled next
+          prow[s] = -1;
+        }
+      };
       auto acquire = [&](uint64_t* empty, uint64_t* full, uint32_t n, int ns, int bytes) -> bool {
         const int s = static_cast<int>(n % ns);
         if (!mbar_wait(&empty[s], ((n / ns) & 1) ^ 1, wait_ns, abort)) return false;
@@ -228,10 +250,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nR;
           return true;
         };
+        const bool rolls = p.roll_src0 >= 0 && w.i0 + BM >= p.W;  // last query tile
         auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, const CUtensorMap* map,
-                           int t) -> bool {
-          if (!acquire(empty, full, n, 4, kRowTile)) return false;
-          tma_load_4d(dst + (n % 4) * kRowTile, map, &full[n % 4], 0, w.h, t * BN, w.b);
+                           int t, int* prow, int* pb, int* ph, const CUtensorMap* rmap) -> bool {
+          const int s = static_cast<int>(n % NK);
+          if (!mbar_wait(&empty[s], ((n / NK) & 1) ^ 1, wait_ns, abort)) return false;
+          flush_store(prow, pb, ph, s, rmap, dst + s * kRowTile);
+          mbar_arrive_expect_tx(&full[s], kRowTile);
+          tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, t * BN, w.b);
+          prow[s] = (rolls && t * BN >= p.roll_src0) ? t * BN - p.roll_src0 : -1;
+          pb[s] = w.b;
+          ph[s] = w.h;
           ++n;
           return true;
         };
@@ -241,8 +270,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t) && load_r(p.M + w.i0 - BN * (t + 1)) &&
-               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t);
+          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t, pk_row, pk_b, pk_h, &tm_km) &&
+               load_r(p.M + w.i0 - BN * (t + 1)) &&
+               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t, pv_row, pv_b, pv_h, &tm_vm);
         }
       }
       if (!ok) report_timeout(abort, p.status);
@@ -256,6 +286,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain(bars->fullK, nK, NK);
       drain(bars->fullV, nV, NV);
       drain(bars->fullR, nR, NR);
+      // Roll stores still pending: each waits for the MMAs that read its
+      // stage's last tile (the stage's data stays until then), then stores.
+      if (ok && !stop) {
+        for (int s = 0; s < NK; ++s) {
+          const uint32_t last = static_cast<uint32_t>(s) + ((nK - 1 - s) / NK) * NK;  // nK == nV
+          if (pk_row[s] >= 0 && mbar_wait(&bars->emptyK[s], (last / NK) & 1, wait_ns, abort))
+            flush_store(pk_row, pk_b, pk_h, s, &tm_km, sK + s * kRowTile);
+          if (pv_row[s] >= 0 && mbar_wait(&bars->emptyV[s], (last / NV) & 1, wait_ns, abort))
+            flush_store(pv_row, pv_b, pv_h, s, &tm_vm, sV + s * kRowTile);
+        }
+      }
+      bulk_wait_group0();  // every roll store is complete before the CTA exits
     }
   } else if (warp == kMmaWarp) {
     // ===================== content-score MMA issuer ========================
@@ -720,7 +762,8 @@ int num_sms() {
 
 template <bool O_BF16>
 cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                         const CUtensorMap& tm_r, const CUtensorMap& tm_o, const Params& prm, cudaStream_t stream) {
+                         const CUtensorMap& tm_r, const CUtensorMap& tm_o, const CUtensorMap& tm_km,
+                         const CUtensorMap& tm_vm, const Params& prm, cudaStream_t stream) {
   auto kern = relattn_tc64_kernel<O_BF16>;
   static int configured_mask = 0;  // one bit per device ordinal < 32
   int dev = 0;
@@ -732,14 +775,15 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
   const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_o, prm);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_o, tm_km, tm_vm, prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const CUtensorMap& tm_r, const CUtensorMap* tm_o, const float* bias_u,
+                                const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
+                                const CUtensorMap* tm_vm, int roll_src0, const float* bias_u,
                                 const float* bias_v, void* o,
                                 float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
                                 cudaStream_t stream) {
@@ -759,10 +803,15 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   prm.status = wc.status;
   prm.wait_ns = wc.limit_ns;
   prm.inject_stall = wc.inject_stall;
+  prm.roll_src0 = (tm_km != nullptr && tm_vm != nullptr) ? roll_src0 : -1;
+  if (prm.roll_src0 >= 0 && prm.roll_src0 % BN != 0) return cudaErrorInvalidValue;
   if (o_bf16 && tm_o == nullptr) return cudaErrorInvalidValue;
-  // fp32 output is written with plain stores; tm_q stands in for the unused map.
-  return o_bf16 ? launch_typed<true>(tm_q, tm_k, tm_v, tm_r, *tm_o, prm, stream)
-                : launch_typed<false>(tm_q, tm_k, tm_v, tm_r, tm_q, prm, stream);
+  // Unused maps (fp32 output is written with plain stores; no roll) are
+  // stood in for by tm_q and never touched.
+  const CUtensorMap& km = prm.roll_src0 >= 0 ? *tm_km : tm_q;
+  const CUtensorMap& vm = prm.roll_src0 >= 0 ? *tm_vm : tm_q;
+  return o_bf16 ? launch_typed<true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, prm, stream)
+                : launch_typed<false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, prm, stream);
 }
 
 }  // namespace txl

@@ -45,8 +45,12 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 
 // Specialisation for D = 64 (same tensor maps).
 // tm_o: the bf16 output's map (box 64 x 1 x 32 x 1); required when o_bf16.
+// roll_src0 >= 0: also store rows [roll_src0, M+W) of k and v (a multiple of
+// 64) to the memory outputs described by tm_km / tm_vm (box 64 x 1 x 64 x 1,
+// rows counted from roll_src0); -1: no roll.
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                const CUtensorMap& tm_r, const CUtensorMap* tm_o, const float* bias_u,
+                                const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
+                                const CUtensorMap* tm_vm, int roll_src0, const float* bias_u,
                                 const float* bias_v, void* o,
                                 float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
                                 cudaStream_t stream);
