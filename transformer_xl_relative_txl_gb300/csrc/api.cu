@@ -9,7 +9,9 @@
 #include <cmath>
 #include <cstdint>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "txl_internal.h"
 #include "txl_relattn.h"
@@ -40,6 +42,49 @@ cudaError_t status_ptr(unsigned int** out) {
     g_status_ptr[dev] = static_cast<unsigned int*>(p);
   }
   *out = g_status_ptr[dev];
+  return cudaSuccess;
+}
+
+// Scratch for split key ranges, per (device, stream) so that calls on
+// different streams never share it: the chunks' partial results, and the
+// merge counters, which live in their own buffer because the kernel relies on
+// them being zero at launch (it leaves them at zero; a new counter buffer is
+// zeroed).  Buffers grow on demand (the stream is synchronised before an old
+// one is freed) and live until the process exits.
+struct ScratchBuf {
+  void* ptr = nullptr;
+  size_t bytes = 0;
+  int* cnt = nullptr;
+  size_t cnt_n = 0;
+};
+std::map<std::pair<int, cudaStream_t>, ScratchBuf> g_scratch;
+
+cudaError_t split_scratch(cudaStream_t stream, size_t bytes, size_t n_counters, void** out, int** counters) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  ScratchBuf& b = g_scratch[{dev, stream}];
+  if (b.bytes < bytes || b.cnt_n < n_counters) {
+    if ((b.ptr != nullptr || b.cnt != nullptr) && (e = cudaStreamSynchronize(stream)) != cudaSuccess) return e;
+    if (b.bytes < bytes) {
+      if (b.ptr != nullptr && (e = cudaFree(b.ptr)) != cudaSuccess) return e;
+      b.ptr = nullptr;
+      b.bytes = 0;
+      if ((e = cudaMalloc(&b.ptr, bytes)) != cudaSuccess) return e;
+      b.bytes = bytes;
+    }
+    if (b.cnt_n < n_counters) {
+      if (b.cnt != nullptr && (e = cudaFree(b.cnt)) != cudaSuccess) return e;
+      b.cnt = nullptr;
+      b.cnt_n = 0;
+      if ((e = cudaMalloc(&b.cnt, n_counters * sizeof(int))) != cudaSuccess) return e;
+      b.cnt_n = n_counters;
+      if ((e = cudaMemsetAsync(b.cnt, 0, n_counters * sizeof(int), stream)) != cudaSuccess) return e;
+    }
+  }
+  *out = b.ptr;
+  *counters = b.cnt;
   return cudaSuccess;
 }
 
@@ -134,7 +179,19 @@ int txl_get_device_status(cudaStream_t stream) {
     const unsigned int zero = 0;
     if (cudaMemcpy(p, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return TXL_ERR_CUDA;
   }
-  return (v & txl::kStatusTimeoutBit) ? TXL_ERR_DEVICE_TIMEOUT : TXL_OK;
+  if (v & txl::kStatusTimeoutBit) {
+    // A kernel that gave up a wait may have left split-merge counters
+    // counted: zero this device's scratch buffers (after the device is idle).
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return TXL_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mutex);
+    for (auto& kv : g_scratch)
+      if (kv.first.first == dev && kv.second.cnt != nullptr &&
+          cudaMemset(kv.second.cnt, 0, kv.second.cnt_n * sizeof(int)) != cudaSuccess)
+        return TXL_ERR_CUDA;
+    return TXL_ERR_DEVICE_TIMEOUT;
+  }
+  return TXL_OK;
 }
 
 int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cudaStream_t stream) {
@@ -320,11 +377,28 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
   if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
   wc.limit_ns = g_wait_ns.load();
   wc.inject_stall = g_inject_stall.exchange(0);
-  if (D == 64)
+  if (D == 64) {
+    // Too few units to fill the SMs: split each unit's key steps into
+    // chunks whose partial results a merge kernel combines.
+    const int nsplit = txl::relattn_tc64_split(B, H, W, M);
+    float* part_o = nullptr;
+    float* part_lse = nullptr;
+    int* part_cnt = nullptr;
+    if (nsplit > 1) {
+      const size_t units = static_cast<size_t>((W + 127) / 128) * B * H;
+      const size_t rows = units * nsplit * 128;
+      void* buf = nullptr;
+      if (split_scratch(stream, rows * (D + 1) * sizeof(float), units * 4, &buf, &part_cnt) != cudaSuccess)
+        return TXL_ERR_CUDA;
+      part_o = static_cast<float*>(buf);
+      part_lse = part_o + rows * D;
+    }
     return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, o_tma ? &tm_o : nullptr,
                                               roll ? &tm_km : nullptr, roll ? &tm_vm : nullptr,
                                               roll ? static_cast<int>(roll->src0) : -1, bias_u, bias_v, o, lse, B,
-                                              W, M, H, o_dtype == TXL_BF16, scale, wc, stream));
+                                              W, M, H, o_dtype == TXL_BF16, scale, nsplit, part_o, part_lse,
+                                              part_cnt, wc, stream));
+  }
   return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H, D,
                                           o_dtype == TXL_BF16, scale, wc, stream));
 }

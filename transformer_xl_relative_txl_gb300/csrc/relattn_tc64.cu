@@ -108,7 +108,11 @@ struct Params {
   void* o;
   float* lse;
   int B, W, M, H;
-  int nqt, n_units;
+  int nqt, n_units;  // n_units: work items (units x nsplit)
+  int nsplit;        // > 1: key steps split into chunks; partial results go to part_o / part_lse
+  float* part_o;     // [item][128 rows][D] fp32, o of the chunk (normalised by its own sum)
+  float* part_lse;   // [item][128 rows] fp32, log2-domain lse of the chunk (-inf: no visible key)
+  int* part_cnt;     // [unit][4 quadrants] chunks finished; zero between launches
   float scale_log2e;  // |scale| * log2(e)
   float qsign;        // sign of scale, folded into (q+u), (q+v)
   unsigned int* status;
@@ -130,7 +134,7 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
-template <bool O_BF16>
+template <bool O_BF16, bool SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     relattn_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -150,6 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   float* sbias = reinterpret_cast<float*>(smem + kOffBias);
   Bars* bars = reinterpret_cast<Bars*>(smem + kOffBar);
   volatile int* abort = &bars->abort;
+  const int kSplit = SPLIT ? p.nsplit : 1;  // chunks per unit
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -232,7 +237,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       auto load_q = [&](int u) -> bool {
         if (!mbar_wait(&bars->q_empty, (nQ & 1) ^ 1, wait_ns, abort)) return false;
         mbar_arrive_expect_tx(&bars->q_full, kQTile);
-        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         tma_load_4d(sQ, &tm_q, &bars->q_full, 0, w.h, w.i0, w.b);
         ++nQ;
         return true;
@@ -242,7 +247,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int u = sched_unit(rd, blockIdx.x, gridDim.x);
         if (!ok || stop || u >= p.n_units) break;
         const int un_next = sched_unit(rd + 1, blockIdx.x, gridDim.x);
-        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         if (un_next < p.n_units && !(ok = load_q(un_next))) break;
         auto load_r = [&](int d0) -> bool {
           if (!acquire(bars->emptyR, bars->fullR, nR, NR, kRowTile)) return false;
@@ -257,21 +262,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait(&empty[s], ((n / NK) & 1) ^ 1, wait_ns, abort)) return false;
           flush_store(prow, pb, ph, s, rmap, dst + s * kRowTile);
           mbar_arrive_expect_tx(&full[s], kRowTile);
-          tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, t * BN, w.b);
-          prow[s] = (rolls && t * BN >= p.roll_src0) ? t * BN - p.roll_src0 : -1;
+          const int kr = (w.t0 + t) * BN;  // first key row of the tile
+          tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, kr, w.b);
+          prow[s] = (rolls && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
           pb[s] = w.b;
           ph[s] = w.h;
           ++n;
           return true;
         };
-        ok = load_r(p.M + w.i0 + BN) && load_r(p.M + w.i0);  // distance tiles -2 and -1
+        // distance tiles -2 and -1 of the item's first step
+        ok = load_r(p.M + w.i0 - BN * (w.t0 - 1)) && load_r(p.M + w.i0 - BN * w.t0);
         for (int t = 0; ok && t < w.nks; ++t) {
           if (p.inject_stall && t == 1) {  // test hook: starve the consumers
             stop = true;
             break;
           }
           ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t, pk_row, pk_b, pk_h, &tm_km) &&
-               load_r(p.M + w.i0 - BN * (t + 1)) &&
+               load_r(p.M + w.i0 - BN * (w.t0 + t + 1)) &&
                load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t, pv_row, pv_b, pv_h, &tm_vm);
         }
       }
@@ -312,7 +319,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rd = 0;; ++rd) {
         const int u = sched_unit(rd, blockIdx.x, gridDim.x);
         if (!ok || u >= p.n_units) break;
-        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
         const uint32_t g0 = gt;
@@ -356,7 +363,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rd = 0;; ++rd) {
         const int u = sched_unit(rd, blockIdx.x, gridDim.x);
         if (!ok || u >= p.n_units) break;
-        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
         const uint32_t g0 = gt;
@@ -413,7 +420,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int rd = 0;; ++rd) {
         const int u = sched_unit(rd, blockIdx.x, gridDim.x);
         if (!ok || u >= p.n_units) break;
-        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         for (int t = 0; t < w.nks; ++t, ++g) {
           if (!(ok = mbar_wait(&bars->p_full[g & 1], (g >> 1) & 1, wait_ns, abort))) break;
           const int sv = nV % NV;
@@ -499,18 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
 
     auto bias_of = [&](int u, const float* bias) -> float {
-      return __ldg(bias + decode_unit(u, p.B, p.H, p.W, p.M, p.nqt).h * D + 32 * par + lane);
+      return __ldg(bias + decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt).h * D + 32 * par + lane);
     };
     if (sched_unit(0, blockIdx.x, gridDim.x) < p.n_units) {
       const int u0 = sched_unit(0, blockIdx.x, gridDim.x);
-      ok = build_q(decode_unit(u0, p.B, p.H, p.W, p.M, p.nqt), 0, bias_of(u0, p.bias_u), bias_of(u0, p.bias_v));
+      ok = build_q(decode_item(u0, kSplit, p.B, p.H, p.W, p.M, p.nqt), 0, bias_of(u0, p.bias_u), bias_of(u0, p.bias_v));
     }
 
     for (int rd = 0;; ++rd) {
       const int u = sched_unit(rd, blockIdx.x, gridDim.x);
       if (!ok || u >= p.n_units) break;
       const int un_next = sched_unit(rd + 1, blockIdx.x, gridDim.x);
-      const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+      const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
       const uint32_t g0 = gt;
       const bool has_next = un_next < p.n_units;
       const float bu_next = has_next ? bias_of(un_next, p.bias_u) : 0.f;
@@ -532,8 +539,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           return kColG + ((rb + t - (z >> 6) + 2) & (kSlots - 1)) * BN + (z & 63);
         };
         const uint32_t sc = tmem + lane_base + kColS + sb * BN;
-        const int lim = p.M + w.i0 - BN * t + a;  // column c visible iff c <= lim
-        const bool diag = p.M + w.i0 - BN * t + quad * 32 < 63;  // some lane of the warp masks
+        const int kt = w.t0 + t;                 // key step of the tile
+        const int lim = p.M + w.i0 - BN * kt + a;  // column c visible iff c <= lim
+        const bool diag = p.M + w.i0 - BN * kt + quad * 32 < 63;  // some lane of the warp masks
         const float m_old = m_use;
         float m_new = m_use;
         // All of this step's TMEM reads at once -- the 96-distance window and
@@ -644,7 +652,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // warp's first step of this unit has seen its scores: the MMAs of the
         // unit before, which read that buffer, are complete by then.
         if (t == first && has_next &&
-            !(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1, bu_next, bv_next)))
+            !(ok = build_q(decode_item(un_next, kSplit, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1, bu_next, bv_next)))
           break;
       }
       if (!ok) break;
@@ -652,7 +660,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // No step of this unit: build after its last step's scores instead.
         const uint32_t gl = g0 + tl;
         if (!(ok = warp_wait(&bars->s_full[gl & 1], (gl >> 1) & 1, wait_ns, abort))) break;
-        if (!(ok = build_q(decode_unit(un_next, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1, bu_next, bv_next))) break;
+        if (!(ok = build_q(decode_item(un_next, kSplit, p.B, p.H, p.W, p.M, p.nqt), (un + 1) & 1, bu_next, bv_next))) break;
       }
       // The warps of the unit's last step merge the two accumulators and
       // write the output; the other parity hands over its (m, l) and moves on
@@ -675,10 +683,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool has0 = first <= tl;        // this warp had steps
         const bool has1 = (first ^ 1) <= tl;  // the other parity's warp had steps
         const float m = fmaxf(has0 ? m_use : -INFINITY, has1 ? m1 : -INFINITY);
-        const float a0 = has0 ? ex2(m_use - m) : 0.f;
-        const float a1 = has1 ? ex2(m1 - m) : 0.f;
+        // A row can see no key of an item only when the key steps are split.
+        const bool any = m != -INFINITY;
+        const float a0 = (has0 && any) ? ex2(m_use - m) : 0.f;
+        const float a1 = (has1 && any) ? ex2(m1 - m) : 0.f;
         const float l = a0 * l_run + a1 * l1;
-        const float inv_l = 1.f / l;
+        const float inv_l = any ? 1.f / l : 0.f;
         const float c0 = a0 * inv_l, c1 = a1 * inv_l;
         // Read both accumulators into registers and hand them back to the PV
         // issuer before the stores.
@@ -701,7 +711,83 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         warp_arrive_tc(&bars->o_free);
         const int i = w.i0 + a;
-        if (O_BF16) {
+        if (SPLIT) {
+          // This chunk's result for the warp's 32 rows goes to the scratch;
+          // the warp that finishes a unit's rows last merges all chunks.
+          const size_t it = static_cast<size_t>(u);
+          float4* po = reinterpret_cast<float4*>(p.part_o + (it * BM + a) * D);
+#pragma unroll
+          for (int c = 0; c < D / 4; ++c) po[c] = make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
+          const float lse2 = any ? m + __log2f(l) : -INFINITY;
+          p.part_lse[it * BM + a] = lse2;
+          __threadfence();  // this chunk's rows are visible before it is counted
+          __syncwarp();
+          const int unit = u / kSplit;
+          int done = 0;
+          if (lane == 0) done = atomicAdd(&p.part_cnt[unit * 4 + quad], 1);
+          done = __shfl_sync(0xffffffffu, done, 0);
+          if (done == kSplit - 1) {
+            __threadfence();
+            // weights 2^(lse_c - max) of the chunks (lse -inf: no visible key),
+            // summed in chunk order whichever chunk merges (the result does
+            // not depend on which finished last); this chunk's own result is
+            // taken from registers, the same values it stored.
+            const size_t it0 = static_cast<size_t>(unit) * kSplit;
+            const int own = static_cast<int>(it - it0);
+            float mx = lse2;
+            for (int c = 0; c < kSplit; ++c)
+              if (c != own) mx = fmaxf(mx, p.part_lse[(it0 + c) * BM + a]);
+            float wsum = 0.f;
+            float acc[D];
+#pragma unroll
+            for (int n = 0; n < D; ++n) acc[n] = 0.f;
+            for (int c = 0; c < kSplit; ++c) {
+              const float l2 = c == own ? lse2 : p.part_lse[(it0 + c) * BM + a];
+              if (l2 == -INFINITY) continue;
+              const float wt = ex2(l2 - mx);
+              wsum += wt;
+              if (c == own) {
+#pragma unroll
+                for (int n = 0; n < D; ++n) acc[n] = fmaf(wt, ov[n], acc[n]);
+              } else {
+                const float4* src = reinterpret_cast<const float4*>(p.part_o + ((it0 + c) * BM + a) * D);
+                float4 x4[D / 4];
+#pragma unroll
+                for (int q4 = 0; q4 < D / 4; ++q4) x4[q4] = src[q4];
+#pragma unroll
+                for (int q4 = 0; q4 < D / 4; ++q4) {
+                  acc[4 * q4] = fmaf(wt, x4[q4].x, acc[4 * q4]);
+                  acc[4 * q4 + 1] = fmaf(wt, x4[q4].y, acc[4 * q4 + 1]);
+                  acc[4 * q4 + 2] = fmaf(wt, x4[q4].z, acc[4 * q4 + 2]);
+                  acc[4 * q4 + 3] = fmaf(wt, x4[q4].w, acc[4 * q4 + 3]);
+                }
+              }
+            }
+            if (i < p.W) {
+              const float inv = 1.f / wsum;
+              const size_t orow = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D;
+              if (O_BF16) {
+                uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.o) + orow);
+#pragma unroll
+                for (int c = 0; c < D / 8; ++c)
+                  dst[c] = make_uint4(pack_bf16x2(acc[8 * c] * inv, acc[8 * c + 1] * inv),
+                                      pack_bf16x2(acc[8 * c + 2] * inv, acc[8 * c + 3] * inv),
+                                      pack_bf16x2(acc[8 * c + 4] * inv, acc[8 * c + 5] * inv),
+                                      pack_bf16x2(acc[8 * c + 6] * inv, acc[8 * c + 7] * inv));
+              } else {
+                float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.o) + orow);
+#pragma unroll
+                for (int c = 0; c < D / 4; ++c)
+                  dst[c] = make_float4(acc[4 * c] * inv, acc[4 * c + 1] * inv, acc[4 * c + 2] * inv,
+                                       acc[4 * c + 3] * inv);
+              }
+              if (p.lse != nullptr)
+                p.lse[(static_cast<size_t>(w.b) * p.H + w.h) * p.W + i] =
+                    (mx + __log2f(wsum)) * 0.69314718055994531f;
+            }
+            if (lane == 0) p.part_cnt[unit * 4 + quad] = 0;  // ready for the next launch
+          }
+        } else if (O_BF16) {
           // bf16 rows into this warp's quadrant of its own P buffer (free
           // until its next step: the last PV that read it is complete), then
           // one TMA store of the 32-row box; rows past W are not written.
@@ -726,7 +812,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < D / 4; ++c) dst[c] = make_float4(ov[4 * c], ov[4 * c + 1], ov[4 * c + 2], ov[4 * c + 3]);
         }
-        if (i < p.W && p.lse != nullptr)
+        if (!SPLIT && i < p.W && p.lse != nullptr)
           p.lse[(static_cast<size_t>(w.b) * p.H + w.h) * p.W + i] = (m + __log2f(l)) * 0.69314718055994531f;
       }
       gt = g0 + w.nks;
@@ -760,11 +846,11 @@ int num_sms() {
   return cached[dev];
 }
 
-template <bool O_BF16>
+template <bool O_BF16, bool SPLIT>
 cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                          const CUtensorMap& tm_r, const CUtensorMap& tm_o, const CUtensorMap& tm_km,
                          const CUtensorMap& tm_vm, const Params& prm, cudaStream_t stream) {
-  auto kern = relattn_tc64_kernel<O_BF16>;
+  auto kern = relattn_tc64_kernel<O_BF16, SPLIT>;
   static int configured_mask = 0;  // one bit per device ordinal < 32
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -781,11 +867,36 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
 
 }  // namespace
 
+int relattn_tc64_split(int B, int H, int W, int M) {
+  // Cost in key steps of the slowest CTA: waves of work items times the
+  // steps of the longest item, plus a unit boundary per item and, when
+  // split, about the cost of the merge launch.
+  constexpr double kBoundary = 1.5, kMerge = 4.0;
+  const long long nqt = (W + BM - 1) / BM;
+  const long long units = nqt * B * H;
+  const long long sms = num_sms();
+  if (units >= sms) return 1;
+  const int nks_max = (M + W - 1) / BN + 1;
+  const int nks_min = (min(M + BM - 1, M + W - 1)) / BN + 1;
+  int best = 1;
+  double best_cost = static_cast<double>((units + sms - 1) / sms) * (nks_max + kBoundary);
+  for (int s = 2; s <= nks_min && s <= 16; ++s) {
+    const double waves = static_cast<double>((units * s + sms - 1) / sms);
+    const double cost = waves * ((nks_max + s - 1) / s + kBoundary) + kMerge;
+    if (cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
                                 const CUtensorMap* tm_vm, int roll_src0, const float* bias_u,
                                 const float* bias_v, void* o,
-                                float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
+                                float* lse, int B, int W, int M, int H, bool o_bf16, float scale, int nsplit,
+                                float* part_o, float* part_lse, int* part_cnt, const WaitCtl& wc,
                                 cudaStream_t stream) {
   Params prm;
   prm.bias_u = bias_u;
@@ -797,7 +908,13 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   prm.M = M;
   prm.H = H;
   prm.nqt = (W + BM - 1) / BM;
-  prm.n_units = prm.nqt * B * H;
+  prm.nsplit = nsplit;
+  prm.part_o = part_o;
+  prm.part_lse = part_lse;
+  prm.part_cnt = part_cnt;
+  prm.n_units = prm.nqt * B * H * nsplit;
+  if (nsplit < 1 || (nsplit > 1 && (part_o == nullptr || part_lse == nullptr || part_cnt == nullptr)))
+    return cudaErrorInvalidValue;
   prm.qsign = scale < 0.f ? -1.f : 1.f;
   prm.scale_log2e = fmaxf(fabsf(scale), 1e-30f) * 1.4426950408889634f;
   prm.status = wc.status;
@@ -810,8 +927,11 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   // stood in for by tm_q and never touched.
   const CUtensorMap& km = prm.roll_src0 >= 0 ? *tm_km : tm_q;
   const CUtensorMap& vm = prm.roll_src0 >= 0 ? *tm_vm : tm_q;
-  return o_bf16 ? launch_typed<true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, prm, stream)
-                : launch_typed<false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, prm, stream);
+  if (nsplit > 1)
+    return o_bf16 ? launch_typed<true, true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, prm, stream)
+                  : launch_typed<false, true>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, prm, stream);
+  return o_bf16 ? launch_typed<true, false>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, prm, stream)
+                : launch_typed<false, false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, prm, stream);
 }
 
 }  // namespace txl

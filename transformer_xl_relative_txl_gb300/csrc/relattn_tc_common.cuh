@@ -12,8 +12,11 @@ namespace txl {
 constexpr int kTileRows = 128;  // query rows per unit (TMEM lanes)
 constexpr int kStepKeys = 64;   // keys per step, distances per ring tile
 
+// A (batch, head, 128-query tile) unit, or a chunk of one: key steps
+// [t0, t0 + nks) of the tile's visible range.
 struct Unit {
   int b, h, i0, nks;
+  int t0;
 };
 
 // Units are ordered longest query tile first; u in [0, nqt * B * H).
@@ -27,6 +30,21 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int H, int W, int M, i
   r.i0 = qt * kTileRows;
   const int kmax = min(M + r.i0 + kTileRows - 1, M + W - 1);
   r.nks = kmax / kStepKeys + 1;
+  r.t0 = 0;
+  return r;
+}
+
+// Work item it of a launch whose units are split into nsplit chunks of
+// their key steps (chunk c of unit it / nsplit: steps [c*n/nsplit,
+// (c+1)*n/nsplit)); nsplit never exceeds a unit's step count.
+__device__ __forceinline__ Unit decode_item(int it, int nsplit, int B, int H, int W, int M, int nqt) {
+  Unit r = decode_unit(it / nsplit, B, H, W, M, nqt);
+  if (nsplit > 1) {
+    const int c = it % nsplit;
+    const int lo = (c * r.nks) / nsplit, hi = ((c + 1) * r.nks) / nsplit;
+    r.t0 = lo;
+    r.nks = hi - lo;
+  }
   return r;
 }
 

@@ -48,11 +48,21 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 // roll_src0 >= 0: also store rows [roll_src0, M+W) of k and v (a multiple of
 // 64) to the memory outputs described by tm_km / tm_vm (box 64 x 1 x 64 x 1,
 // rows counted from roll_src0); -1: no roll.
+// nsplit > 1: every unit's key steps are split into nsplit chunks run as
+// separate work items; their results go to part_o
+// [units*nsplit][128][64] fp32 and part_lse [units*nsplit][128] fp32; the
+// last chunk to finish a unit's rows merges them into o and lse, counting in
+// part_cnt [units][4], which must be zero before the launch (and is again
+// after it).
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
                                 const CUtensorMap* tm_vm, int roll_src0, const float* bias_u,
-                                const float* bias_v, void* o,
-                                float* lse, int B, int W, int M, int H, bool o_bf16, float scale, const WaitCtl& wc,
-                                cudaStream_t stream);
+                                const float* bias_v, void* o, float* lse, int B, int W, int M, int H, bool o_bf16,
+                                float scale, int nsplit, float* part_o, float* part_lse, int* part_cnt,
+                                const WaitCtl& wc, cudaStream_t stream);
+
+// Number of chunks the D = 64 kernel should split each unit's key steps
+// into (1: no split), from the shape and the device's SM count.
+int relattn_tc64_split(int B, int H, int W, int M);
 
 }  // namespace txl
