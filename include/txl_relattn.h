@@ -109,6 +109,27 @@ TXL_API int txl_relattn_forward(const void* q, const void* k, const void* v, con
                         txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream);
 
 /*
+ * txl_relattn_forward_static -- txl_relattn_forward that allocates nothing.
+ *
+ * Same arguments, result and errors as txl_relattn_forward (bit for bit: the
+ * same kernels run).  When a launch has too few (batch, head, query-tile)
+ * units to fill the GPU, txl_relattn_forward splits each unit's key range
+ * across CTAs and keeps the partial results in scratch that the library
+ * allocates per (device, stream) on first use.  This entry point uses instead
+ * a fixed 16 MiB device array inside the library (at most 4096 units x 4
+ * merge counters, then the partial results); a split that needs more returns
+ * TXL_ERR_UNSUPPORTED.  It makes no allocation of any kind, so it may be
+ * called where allocating is not allowed (for instance while a stream is
+ * being captured into a graph).  The array is shared by all such calls on a
+ * device: they must not run concurrently on different streams.  The pages
+ * have no counterpart; this is a property of the implementation only.
+ */
+TXL_API int txl_relattn_forward_static(const void* q, const void* k, const void* v, const void* r,
+                               const float* bias_u, const float* bias_v, void* o, float* lse,
+                               int B, int W, int M, int H, int D, int n_r, float scale,
+                               txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream);
+
+/*
  * txl_mem_update -- the memory roll.
  *
  * Defines mem_tau = last M rows of [stop_grad(mem_{tau-1}) ; h_tau] from the

@@ -36,7 +36,8 @@ def declared_functions():
 
 def test_header_declares_the_three_calls():
     names = declared_functions()
-    for n in ("txl_relattn_forward", "txl_relattn_forward_roll", "txl_mem_update", "txl_sinusoid_rel",
+    for n in ("txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_mem_update",
+              "txl_sinusoid_rel",
               "txl_get_device_status",
               "txl_status_string", "txl_version"):
         assert n in names

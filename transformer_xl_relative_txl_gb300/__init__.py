@@ -16,7 +16,8 @@ import torch
 
 __all__ = [
     "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
-    "txl_relattn_forward", "txl_relattn_forward_roll", "txl_mem_update", "txl_sinusoid_rel",
+    "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_mem_update",
+    "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
 ]
@@ -35,6 +36,8 @@ lib = ctypes.CDLL(library_path)
 _p, _i, _ll, _f = ctypes.c_void_p, ctypes.c_int, ctypes.c_longlong, ctypes.c_float
 lib.txl_relattn_forward.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
 lib.txl_relattn_forward.restype = _i
+lib.txl_relattn_forward_static.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
+lib.txl_relattn_forward_static.restype = _i
 lib.txl_relattn_forward_roll.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _i,
                                          _p, _p, _i, _ll, ctypes.POINTER(_i), _p]
 lib.txl_relattn_forward_roll.restype = _i
@@ -95,6 +98,18 @@ def txl_relattn_forward(q, k, v, r, bias_u, bias_v, o, lse=None, M=None, scale=N
     """o <- relative attention of q [B,W,H,D] over k, v [B,M+W,H,D] with
     distance keys r [n_r,H,D] and biases bias_u, bias_v [H,D] (fp32).
     lse [B,H,W] fp32 is optional.  scale defaults to 1/sqrt(D)."""
+    return _forward(lib.txl_relattn_forward, "txl_relattn_forward", q, k, v, r, bias_u, bias_v, o, lse, M, scale,
+                    stream)
+
+
+def txl_relattn_forward_static(q, k, v, r, bias_u, bias_v, o, lse=None, M=None, scale=None, stream=None):
+    """txl_relattn_forward without any allocation: split key ranges keep
+    their partial results in the library's fixed device array."""
+    return _forward(lib.txl_relattn_forward_static, "txl_relattn_forward_static", q, k, v, r, bias_u, bias_v, o,
+                    lse, M, scale, stream)
+
+
+def _forward(fn, name, q, k, v, r, bias_u, bias_v, o, lse, M, scale, stream):
     B, W, H, D = q.shape
     if M is None:
         M = k.shape[1] - W
@@ -113,10 +128,9 @@ def txl_relattn_forward(q, k, v, r, bias_u, bias_v, o, lse=None, M=None, scale=N
         raise ValueError("q, k, v, r must share a dtype")
     if scale is None:
         scale = D ** -0.5
-    st = lib.txl_relattn_forward(_ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(bias_u), _ptr(bias_v), _ptr(o),
-                                 _ptr(lse), B, W, M, H, D, r.shape[0], float(scale), _dtype_code(q.dtype),
-                                 _dtype_code(o.dtype), _stream(stream))
-    _check(st, "txl_relattn_forward")
+    st = fn(_ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(bias_u), _ptr(bias_v), _ptr(o), _ptr(lse), B, W, M, H, D,
+            r.shape[0], float(scale), _dtype_code(q.dtype), _dtype_code(o.dtype), _stream(stream))
+    _check(st, name)
     return o
 
 

@@ -88,6 +88,30 @@ cudaError_t split_scratch(cudaStream_t stream, size_t bytes, size_t n_counters, 
   return cudaSuccess;
 }
 
+// Fixed scratch of txl_relattn_forward_static, which allocates nothing: the
+// merge counters (kStaticCounters ints, zero at module load and left at zero
+// by the kernel), then the chunks' partial results.  Shared by every call on
+// the device, so such calls must not run concurrently.
+constexpr size_t kStaticScratchBytes = size_t(16) << 20;
+constexpr size_t kStaticCounters = 4096;  // units x 4 lane quadrants
+static __device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+unsigned char* g_static_ptr[kMaxDevices] = {};
+
+cudaError_t static_scratch(unsigned char** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if ((e = cudaGetSymbolAddress(&p, g_static_scratch)) != cudaSuccess) return e;
+    g_static_ptr[dev] = static_cast<unsigned char*>(p);
+  }
+  *out = g_static_ptr[dev];
+  return cudaSuccess;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   static std::once_flag once;
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -189,6 +213,9 @@ int txl_get_device_status(cudaStream_t stream) {
       if (kv.first.first == dev && kv.second.cnt != nullptr &&
           cudaMemset(kv.second.cnt, 0, kv.second.cnt_n * sizeof(int)) != cudaSuccess)
         return TXL_ERR_CUDA;
+    if (dev < kMaxDevices && g_static_ptr[dev] != nullptr &&
+        cudaMemset(g_static_ptr[dev], 0, kStaticCounters * sizeof(int)) != cudaSuccess)
+      return TXL_ERR_CUDA;
     return TXL_ERR_DEVICE_TIMEOUT;
   }
   return TXL_OK;
@@ -259,7 +286,8 @@ struct FusedRoll {
 // kernel to write the memory roll too (the caller has checked it can).
 int forward_impl(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                  const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
-                 txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, cudaStream_t stream);
+                 txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, bool static_scratch_only,
+                 cudaStream_t stream);
 
 int check_forward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                   const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
@@ -307,7 +335,8 @@ int check_forward(const void* q, const void* k, const void* v, const void* r, co
 
 int forward_impl(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                  const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
-                 txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, cudaStream_t stream) {
+                 txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, bool static_scratch_only,
+                 cudaStream_t stream) {
   const long long L = static_cast<long long>(M) + W;
   const size_t hd = static_cast<size_t>(H) * D;
   if (dtype == TXL_F32) {
@@ -379,7 +408,7 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
   wc.inject_stall = g_inject_stall.exchange(0);
   if (D == 64) {
     // Too few units to fill the SMs: split each unit's key steps into
-    // chunks whose partial results a merge kernel combines.
+    // chunks; the last chunk of each unit merges their partial results.
     const int nsplit = txl::relattn_tc64_split(B, H, W, M);
     float* part_o = nullptr;
     float* part_lse = nullptr;
@@ -387,10 +416,19 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
     if (nsplit > 1) {
       const size_t units = static_cast<size_t>((W + 127) / 128) * B * H;
       const size_t rows = units * nsplit * 128;
-      void* buf = nullptr;
-      if (split_scratch(stream, rows * (D + 1) * sizeof(float), units * 4, &buf, &part_cnt) != cudaSuccess)
-        return TXL_ERR_CUDA;
-      part_o = static_cast<float*>(buf);
+      const size_t part_bytes = rows * (D + 1) * sizeof(float);
+      if (static_scratch_only) {
+        if (units * 4 > kStaticCounters || kStaticCounters * sizeof(int) + part_bytes > kStaticScratchBytes)
+          return TXL_ERR_UNSUPPORTED;
+        unsigned char* base = nullptr;
+        if (static_scratch(&base) != cudaSuccess) return TXL_ERR_CUDA;
+        part_cnt = reinterpret_cast<int*>(base);
+        part_o = reinterpret_cast<float*>(base + kStaticCounters * sizeof(int));
+      } else {
+        void* buf = nullptr;
+        if (split_scratch(stream, part_bytes, units * 4, &buf, &part_cnt) != cudaSuccess) return TXL_ERR_CUDA;
+        part_o = static_cast<float*>(buf);
+      }
       part_lse = part_o + rows * D;
     }
     return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, o_tma ? &tm_o : nullptr,
@@ -413,7 +451,16 @@ int txl_relattn_forward(const void* q, const void* k, const void* v, const void*
   const int st = check_forward(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype);
   if (st != TXL_OK || B == 0 || W == 0) return st;
   return forward_impl(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype, nullptr,
-                      stream);
+                      false, stream);
+}
+
+int txl_relattn_forward_static(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                               const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r,
+                               float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {
+  const int st = check_forward(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype);
+  if (st != TXL_OK || B == 0 || W == 0) return st;
+  return forward_impl(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype, nullptr,
+                      true, stream);
 }
 
 int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
@@ -458,10 +505,10 @@ int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const 
   if (fused) {
     const FusedRoll fr{k_mem_out, v_mem_out, keep, L - keep, mem_out_bs};
     return forward_impl(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype, &fr,
-                        stream);
+                        false, stream);
   }
   int rc = forward_impl(q, k, v, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype, nullptr,
-                        stream);
+                        false, stream);
   if (rc != TXL_OK || keep == 0) return rc;
   const long long bs = L * C;
   const size_t es = dsize(dtype);
