@@ -37,10 +37,15 @@ design notes):
 * no distance clipping, no softmax epsilon;
 * sinusoid layout interleaved: R[d, 2k] = sin(d w_k), R[d, 2k+1] = cos(d w_k),
   w_k = 10000^(-2k/dim);
-* memory = the layer's input rows, rolled as projected K/V rows.
+* memory = the layer's input rows, rolled as projected K/V rows;
+* backward: the stop-gradient drops the memory rows' dk / dv only; r, u and
+  v are shared by every pair and take their whole gradient.
 
 Parity status: every function here is pinned by tests in
-``tests/test_oracle.py`` (closed forms, library routines, brute force).
+``tests/test_oracle.py`` (closed forms, library routines, brute force); the
+backward by ``tests/test_oracle_backward.py`` (finite differences of the
+forward, automatic differentiation of an independent torch forward, and
+identities of the score's structure).
 """
 
 from __future__ import annotations
@@ -52,6 +57,7 @@ __all__ = [
     "relattn_forward",
     "relattn_forward_bruteforce",
     "relattn_rows",
+    "relattn_backward",
     "mem_update",
     "run_segments",
     "counted_flops",
@@ -160,6 +166,94 @@ def relattn_forward(q, k, v, r, bias_u, bias_v, M, scale=None, return_probs=Fals
     if return_probs:
         return o, lse, probs
     return o, lse
+
+
+def _one_head_backward(qh, kh, vh, rh, u, vb, M, scale, doh):
+    """Gradients of L = sum(doh * o) for one (batch, head) pair, float64.
+
+    Follows the forward of ``_one_head`` backwards, step by step:
+      o = P V                     ->  dV = P^T dO,  dP = dO V^T
+      P = softmax over visible j  ->  dS = P * (dP - rowsum(P * dP))
+      s = scale * (ac + bd)       ->  G = scale * dS (zero where masked)
+      ac = (q + u) K^T            ->  d(q+u) = G K,  dK = G^T (q+u)
+      bd[i, j] = g[i, M+i-j]      ->  dg[i, d] = sum of G[i, j] over j = M+i-d
+      g = (q + v) r^T             ->  d(q+v) = dg r,  dr = dg^T (q+v)
+    Returns d(q+u) [W, D], d(q+v) [W, D], dK, dV [M+W, D] (every row) and
+    dr [n_r, D].
+    """
+    W = qh.shape[0]
+    L = kh.shape[0]
+    n_r = rh.shape[0]
+    qu = qh + u
+    qv = qh + vb
+    ac = qu @ kh.T
+    g = qv @ rh.T
+    i = np.arange(W)[:, None]
+    j = np.arange(L)[None, :]
+    dist = M + i - j
+    visible = dist >= 0
+    bd = np.take_along_axis(g, np.clip(dist, 0, n_r - 1), axis=1)
+    s = np.where(visible, scale * (ac + bd), -np.inf)
+    e = np.exp(s - s.max(axis=1, keepdims=True))
+    P = e / e.sum(axis=1, keepdims=True)
+    dV = P.T @ doh
+    dP = doh @ vh.T
+    dS = P * (dP - (P * dP).sum(axis=1, keepdims=True))
+    G = scale * dS  # P is 0 on masked pairs, so G is too
+    d_qu = G @ kh
+    dK = G.T @ qu
+    dg = np.zeros((W, n_r))
+    ii, jj = np.nonzero(visible)
+    np.add.at(dg, (ii, dist[ii, jj]), G[ii, jj])
+    d_qv = dg @ rh
+    dr = dg.T @ qv
+    return d_qu, d_qv, dK, dV, dr
+
+
+def relattn_backward(q, k, v, r, bias_u, bias_v, M, dout, scale=None, memory_grads=False):
+    """Gradients of the relative attention of one segment (float64).
+
+    Differentiates L = sum(dout * o) with o = relattn_forward(...).  Returns a
+    dict with dq [B, W, H, D], dk and dv [B, W, H, D] for the segment's own
+    key / value rows, dr [n_r, H, D], dbias_u and dbias_v [H, D].
+
+    "Transformer-XL, explained", method step 2 and the symbol SG(.): the
+    memory is read as a fixed input and backpropagation stays inside the
+    current segment, so the memory rows of k and v (rows 0 .. M-1) get no
+    gradient.  ``memory_grads=True`` also returns ``dk_all`` / ``dv_all``
+    [B, M+W, H, D] -- the plain derivatives over every key row, for tests
+    only (they are what the stop-gradient discards).  r, u and v are shared
+    parameters of every pair, so they take the whole gradient.
+    """
+    q, k, v, r = _f64(q), _f64(k), _f64(v), _f64(r)
+    bias_u, bias_v, dout = _f64(bias_u), _f64(bias_v), _f64(dout)
+    B, W, H, D = _check_shapes(q, k, v, r, bias_u, bias_v, M)
+    if dout.shape != q.shape:
+        raise ValueError("dout must be [B, W, H, D]")
+    if scale is None:
+        scale = 1.0 / np.sqrt(D)
+    dq = np.zeros((B, W, H, D))
+    dk_all = np.zeros((B, M + W, H, D))
+    dv_all = np.zeros((B, M + W, H, D))
+    dr = np.zeros(r.shape)
+    dbu = np.zeros((H, D))
+    dbv = np.zeros((H, D))
+    for b in range(B):
+        for h in range(H):
+            d_qu, d_qv, dK, dV, drh = _one_head_backward(q[b, :, h], k[b, :, h], v[b, :, h], r[:, h],
+                                                         bias_u[h], bias_v[h], M, float(scale), dout[b, :, h])
+            dq[b, :, h] = d_qu + d_qv  # q enters through both (q + u) and (q + v)
+            dk_all[b, :, h] = dK
+            dv_all[b, :, h] = dV
+            dr[:, h] += drh
+            dbu[h] += d_qu.sum(axis=0)
+            dbv[h] += d_qv.sum(axis=0)
+    out = {"dq": dq, "dk": dk_all[:, M:].copy(), "dv": dv_all[:, M:].copy(), "dr": dr,
+           "dbias_u": dbu, "dbias_v": dbv}
+    if memory_grads:
+        out["dk_all"] = dk_all
+        out["dv_all"] = dv_all
+    return out
 
 
 def relattn_rows(q, k, v, r, bias_u, bias_v, M, scale, b, h, rows):
