@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define TXL_VERSION 110 /* 1.1.0 */
+#define TXL_VERSION 120 /* 1.2.0 */
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -187,6 +187,49 @@ TXL_API int txl_relattn_forward_roll(const void* q, const void* k, const void* v
                              txl_dtype dtype, txl_dtype o_dtype,
                              void* k_mem_out, void* v_mem_out, int m, long long mem_out_bs, int* m_out,
                              cudaStream_t stream);
+
+/*
+ * txl_relattn_backward -- gradients of txl_relattn_forward.
+ *
+ * Given dout = dL/do for the forward's o, writes the gradients of L through
+ * the score of txl_relattn_forward:
+ *
+ *   p[i,j] = exp(s[i,j] - lse_i),  Delta_i = dout_i . o_i
+ *   g[i,j] = scale * p[i,j] * (dout_i . v_j - Delta_i)
+ *   dq_i   = sum_j g[i,j] (k_j + r_{M+i-j})
+ *   dk_j, dv_j (segment rows j = M..M+W-1 only):
+ *          dk_j = sum_i g[i,j] (q_i + u),   dv_j = sum_i p[i,j] dout_i
+ *   dr_d   = sum over pairs with M+i-j = d of g[i,j] (q_i + v)
+ *   dbias_u = sum_{b,i} sum_j g[i,j] k_j,   dbias_v = sum_{b,i} sum_j g[i,j] r_{M+i-j}
+ *
+ * "Transformer-XL, explained", method step 2 and the symbol SG(.): the memory
+ * is read as a fixed input and backpropagation stays inside the current
+ * segment, so the memory rows of k and v receive no gradient; r, u and v are
+ * shared by every pair and receive all of theirs.
+ *
+ *   q, k, v, r, bias_u, bias_v, B, W, M, H, D, n_r, scale, dtype
+ *                as in the forward call that produced o and lse
+ *   o      device, [B, W, H, D] `go_dtype`  the forward's output
+ *   lse    device, [B, H, W] fp32            the forward's lse (required)
+ *   dout   device, [B, W, H, D] `go_dtype`  gradient of the output
+ *   dq     device, [B, W, H, D] fp32
+ *   dk, dv device, [B, W, H, D] fp32   gradients of k, v rows M..M+W-1
+ *   dr     device, [n_r, H, D] fp32    rows no pair uses (d >= M+W) are zero
+ *   dbias_u, dbias_v  device, [H, D] fp32
+ *
+ * Every output is overwritten (not accumulated into).  Outputs must not
+ * overlap each other or any input (TXL_ERR_ALIAS); every pointer 16-byte
+ * aligned (TXL_ERR_INVALID_ARG).  D <= 256 (TXL_ERR_UNSUPPORTED otherwise).
+ * Library scratch of [B, H, W] + [B, W/4, H, 2, D] floats per (device,
+ * stream) is allocated on first use and reused.  Results are deterministic
+ * (no atomics).
+ */
+TXL_API int txl_relattn_backward(const void* q, const void* k, const void* v, const void* r,
+                         const float* bias_u, const float* bias_v, const void* o, const float* lse,
+                         const void* dout, float* dq, float* dk, float* dv, float* dr,
+                         float* dbias_u, float* dbias_v,
+                         int B, int W, int M, int H, int D, int n_r, float scale,
+                         txl_dtype dtype, txl_dtype go_dtype, cudaStream_t stream);
 
 /*
  * txl_sinusoid_rel -- the raw sinusoidal distance table R[n_dist, dim].

@@ -30,6 +30,7 @@ __all__ = [
     "make_segments",
     "make_prefilled",
     "project_r",
+    "make_dout",
 ]
 
 
@@ -159,3 +160,13 @@ def project_r(R, W_r, H, D, dtype):
     R = np.asarray(R, dtype=np.float64)
     y = R @ np.asarray(W_r, dtype=np.float64)
     return _round(y, dtype).reshape(R.shape[0], H, D)
+
+
+def make_dout(wl: Workload, seed: int = 0, batch: int | None = None) -> np.ndarray:
+    """Output gradient dL/do [B, W, H, D] for the backward: its own generator
+    ``np.random.default_rng([seed, cfg_id, 1])`` (the forward's draws are
+    unchanged), entries ~ N(0, 1) rounded to the workload's storage type."""
+    B = wl.B if batch is None else batch
+    rng = np.random.default_rng([seed, wl.cfg_id, 1])
+    g = _draw(rng, (B, wl.W, wl.H, wl.D), 1.0, wl.dtype == "bf16")
+    return _round(g, wl.dtype)

@@ -1,0 +1,135 @@
+"""GPU parity of txl_relattn_backward against the float64 oracle's backward.
+
+The forward runs first on the device (its o and lse feed the backward, as in
+training); the oracle differentiates the same seeded inputs from scratch.
+Tolerances: fp32 inputs max |err| <= 1e-5 * max(1, max |want|); bf16 inputs
+rel-L2 <= 5e-3 and max |err| <= 2e-2 * max(1, max |want|) per gradient
+tensor (the only rounding besides fp32 arithmetic is the forward's bf16 o,
+which enters through Delta_i = dout_i . o_i).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import txl_oracle as O
+from synthetic import make_dout
+
+from gpu_util import dev, prefilled_case, to_dev, torch_dtype, workload
+
+pytestmark = pytest.mark.gpu
+
+KEYS = ["dq", "dk", "dv", "dr", "dbias_u", "dbias_v"]
+
+
+@pytest.fixture(scope="module")
+def txl():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import transformer_xl_relative_txl_gb300 as lib  # fails loudly if not built
+
+    torch.cuda.set_device(0)
+    lib.txl_get_device_status()
+    return lib
+
+
+def _case(B, H, D, W, M, dtype, n_r_extra=0, seed=0):
+    wl = workload(B, H, D, W, M, dtype)
+    q, k, v, r, bu, bv = prefilled_case(wl, seed=seed, n_r_extra=n_r_extra)
+    dout = make_dout(wl, seed=seed)
+    return q, k, v, r, bu, bv, dout
+
+
+def _run(txl, q, k, v, r, bu, bv, dout, M, dtype, o_dtype=None, scale=None):
+    td = torch_dtype(dtype)
+    od = td if o_dtype is None else torch_dtype(o_dtype)
+    qd, kd, vd, rd = (to_dev(x, td) for x in (q, k, v, r))
+    bud, bvd = to_dev(bu, torch.float32), to_dev(bv, torch.float32)
+    B, W, H, D = q.shape
+    o = torch.empty(qd.shape, device=dev(), dtype=od)
+    lse = torch.empty(B, H, W, device=dev(), dtype=torch.float32)
+    txl.txl_relattn_forward(qd, kd, vd, rd, bud, bvd, o, lse, M=M, scale=scale)
+    g = txl.txl_relattn_backward(qd, kd, vd, rd, bud, bvd, o, lse, to_dev(dout, od), M=M, scale=scale)
+    assert txl.txl_get_device_status() == 0
+    return {key: t.cpu().numpy() for key, t in g.items()}
+
+
+def _compare(got, want, dtype):
+    for key in KEYS:
+        a = got[key].astype(np.float64)
+        b = want[key]
+        assert a.shape == b.shape, key
+        assert np.all(np.isfinite(a)), key
+        scale = max(1.0, float(np.abs(b).max()) if b.size else 1.0)
+        err = np.abs(a - b).max() if a.size else 0.0
+        if dtype == "f32":
+            assert err <= 1e-5 * scale, f"{key}: max abs {err:.3e} (scale {scale:.3e})"
+        else:
+            rel = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
+            assert rel <= 5e-3 and err <= 2e-2 * scale, f"{key}: rel-L2 {rel:.3e}, max abs {err:.3e}"
+
+
+CASES = [
+    # B, H, D, W, M, dtype, n_r_extra
+    (1, 2, 8, 4, 4, "f32", 0),       # the tiny configuration
+    (1, 2, 8, 4, 0, "f32", 0),       # first segment: empty memory
+    (2, 2, 16, 37, 29, "f32", 3),    # ragged, unused distance rows
+    (1, 1, 5, 6, 2, "f32", 1),       # odd head dim (scalar row loads)
+    (2, 2, 64, 130, 70, "bf16", 0),  # several tiles, ragged
+    (1, 2, 128, 64, 0, "bf16", 2),
+    (1, 1, 64, 5, 3, "bf16", 0),     # fewer rows than a warp
+    (1, 2, 256, 40, 24, "f32", 0),   # largest head dim
+]
+
+
+@pytest.mark.parametrize("B,H,D,W,M,dtype,extra", CASES)
+def test_backward_matches_oracle(txl, B, H, D, W, M, dtype, extra):
+    q, k, v, r, bu, bv, dout = _case(B, H, D, W, M, dtype, extra)
+    scale = D ** -0.5
+    got = _run(txl, q, k, v, r, bu, bv, dout, M, dtype)
+    want = O.relattn_backward(q, k, v, r, bu, bv, M, dout, scale)
+    _compare(got, want, dtype)
+    assert np.all(got["dr"][M + W:] == 0)
+
+
+def test_backward_fp32_output_gradient_with_bf16_inputs(txl):
+    """bf16 q, k, v, r with an fp32 o and dout."""
+    q, k, v, r, bu, bv, dout = _case(2, 2, 64, 70, 60, "bf16")
+    got = _run(txl, q, k, v, r, bu, bv, dout, 60, "bf16", o_dtype="f32")
+    want = O.relattn_backward(q, k, v, r, bu, bv, 60, dout, 64 ** -0.5)
+    _compare(got, want, "bf16")
+
+
+def test_backward_custom_scale(txl):
+    q, k, v, r, bu, bv, dout = _case(1, 2, 16, 9, 7, "f32")
+    got = _run(txl, q, k, v, r, bu, bv, dout, 7, "f32", scale=0.31)
+    want = O.relattn_backward(q, k, v, r, bu, bv, 7, dout, 0.31)
+    _compare(got, want, "f32")
+
+
+def test_backward_deterministic(txl):
+    q, k, v, r, bu, bv, dout = _case(2, 2, 64, 130, 70, "bf16")
+    a = _run(txl, q, k, v, r, bu, bv, dout, 70, "bf16")
+    b = _run(txl, q, k, v, r, bu, bv, dout, 70, "bf16")
+    for key in KEYS:
+        assert np.array_equal(a[key], b[key]), key
+
+
+def test_backward_rejects_bad_arguments(txl):
+    q, k, v, r, bu, bv, dout = _case(1, 2, 8, 4, 4, "f32")
+    qd, kd, vd, rd = (to_dev(x, torch.float32) for x in (q, k, v, r))
+    bud, bvd = to_dev(bu, torch.float32), to_dev(bv, torch.float32)
+    o = torch.empty(qd.shape, device=dev())
+    lse = torch.empty(1, 2, 4, device=dev())
+    txl.txl_relattn_forward(qd, kd, vd, rd, bud, bvd, o, lse, M=4)
+    dd = to_dev(dout, torch.float32)
+    # an output aliasing an input
+    with pytest.raises(txl.TxlError) as e:
+        txl.txl_relattn_backward(qd, kd, vd, rd, bud, bvd, o, lse, dd, M=4, grads={"dq": dd})
+    assert e.value.status == 3
+    # two outputs overlapping each other
+    buf = torch.empty(qd.shape, device=dev())
+    with pytest.raises(txl.TxlError) as e:
+        txl.txl_relattn_backward(qd, kd, vd, rd, bud, bvd, o, lse, dd, M=4, grads={"dk": buf, "dv": buf})
+    assert e.value.status == 3
+    assert txl.txl_get_device_status() == 0

@@ -36,7 +36,8 @@ def declared_functions():
 
 def test_header_declares_the_three_calls():
     names = declared_functions()
-    for n in ("txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_mem_update",
+    for n in ("txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll",
+              "txl_relattn_backward", "txl_mem_update",
               "txl_sinusoid_rel",
               "txl_get_device_status",
               "txl_status_string", "txl_version"):
@@ -55,7 +56,7 @@ def test_library_exports_every_declared_symbol():
     for n in declared_functions():
         getattr(lib, n)
     lib.txl_version.restype = ctypes.c_int
-    assert lib.txl_version() == 110
+    assert lib.txl_version() == 120
     lib.txl_status_string.restype = ctypes.c_char_p
     assert lib.txl_status_string(5) == b"TXL_ERR_DEVICE_TIMEOUT"
 

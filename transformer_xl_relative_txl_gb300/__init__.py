@@ -16,7 +16,8 @@ import torch
 
 __all__ = [
     "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
-    "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_mem_update",
+    "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_relattn_backward",
+    "txl_mem_update",
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
@@ -41,6 +42,8 @@ lib.txl_relattn_forward_static.restype = _i
 lib.txl_relattn_forward_roll.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _i, _f, _i, _i,
                                          _p, _p, _i, _ll, ctypes.POINTER(_i), _p]
 lib.txl_relattn_forward_roll.restype = _i
+lib.txl_relattn_backward.argtypes = [_p] * 15 + [_i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
+lib.txl_relattn_backward.restype = _i
 lib.txl_mem_update.argtypes = [_p, _i, _p, _i, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i, _p]
 lib.txl_mem_update.restype = _i
 lib.txl_sinusoid_rel.argtypes = [_p, _i, _i, _i, _p]
@@ -107,6 +110,48 @@ def txl_relattn_forward_static(q, k, v, r, bias_u, bias_v, o, lse=None, M=None, 
     their partial results in the library's fixed device array."""
     return _forward(lib.txl_relattn_forward_static, "txl_relattn_forward_static", q, k, v, r, bias_u, bias_v, o,
                     lse, M, scale, stream)
+
+
+def txl_relattn_backward(q, k, v, r, bias_u, bias_v, o, lse, dout, M=None, scale=None, grads=None, stream=None):
+    """Gradients of txl_relattn_forward for dout = dL/do: returns a dict of
+    fp32 tensors dq [B,W,H,D], dk and dv [B,W,H,D] (the segment's key and
+    value rows; memory rows get none), dr [n_r,H,D], dbias_u and dbias_v
+    [H,D].  o and lse are the forward's outputs; o and dout share a dtype.
+    ``grads`` may pass preallocated output tensors under the same keys."""
+    B, W, H, D = q.shape
+    if M is None:
+        M = k.shape[1] - W
+    for t in (q, k, v, r, bias_u, bias_v, o, lse, dout):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k.shape != (B, M + W, H, D) or v.shape != k.shape or o.shape != q.shape or dout.shape != q.shape:
+        raise ValueError("shape mismatch between q, k, v, o, dout")
+    if r.dim() != 3 or r.shape[1:] != (H, D) or bias_u.shape != (H, D) or bias_v.shape != (H, D):
+        raise ValueError("r must be [n_r, H, D]; biases [H, D]")
+    if bias_u.dtype != torch.float32 or bias_v.dtype != torch.float32:
+        raise ValueError("biases are fp32")
+    if lse.shape != (B, H, W) or lse.dtype != torch.float32:
+        raise ValueError("lse must be fp32 [B, H, W]")
+    if not (q.dtype == k.dtype == v.dtype == r.dtype) or o.dtype != dout.dtype:
+        raise ValueError("q, k, v, r share a dtype; so do o and dout")
+    shapes = {"dq": q.shape, "dk": q.shape, "dv": q.shape, "dr": r.shape, "dbias_u": bias_u.shape,
+              "dbias_v": bias_v.shape}
+    g = dict(grads or {})
+    for key, shp in shapes.items():
+        if key not in g:
+            g[key] = torch.empty(shp, device=q.device, dtype=torch.float32)
+        t = g[key]
+        if t.shape != shp or t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError(f"{key} must be a contiguous fp32 tensor of shape {tuple(shp)}")
+    if scale is None:
+        scale = D ** -0.5
+    st = lib.txl_relattn_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(r), _ptr(bias_u), _ptr(bias_v), _ptr(o),
+                                  _ptr(lse), _ptr(dout), _ptr(g["dq"]), _ptr(g["dk"]), _ptr(g["dv"]),
+                                  _ptr(g["dr"]), _ptr(g["dbias_u"]), _ptr(g["dbias_v"]), B, W, M, H, D,
+                                  r.shape[0], float(scale), _dtype_code(q.dtype), _dtype_code(o.dtype),
+                                  _stream(stream))
+    _check(st, "txl_relattn_backward")
+    return g
 
 
 def _forward(fn, name, q, k, v, r, bias_u, bias_v, o, lse, M, scale, stream):

@@ -445,6 +445,55 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
 
 extern "C" {
 
+int txl_relattn_backward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
+                         const float* bias_v, const void* o, const float* lse, const void* dout, float* dq,
+                         float* dk, float* dv, float* dr, float* dbias_u, float* dbias_v, int B, int W, int M,
+                         int H, int D, int n_r, float scale, txl_dtype dtype, txl_dtype go_dtype,
+                         cudaStream_t stream) {
+  if (B < 0 || W < 0 || M < 0 || H <= 0 || D <= 0 || !dtype_ok(dtype) || !dtype_ok(go_dtype))
+    return TXL_ERR_INVALID_ARG;
+  if (B == 0 || W == 0) return TXL_OK;
+  const void* ins[] = {q, k, v, r, bias_u, bias_v, o, lse, dout};
+  const void* outs[] = {dq, dk, dv, dr, dbias_u, dbias_v};
+  for (const void* p : ins)
+    if (p == nullptr || !aligned(p, 16)) return TXL_ERR_INVALID_ARG;
+  for (const void* p : outs)
+    if (p == nullptr || !aligned(p, 16)) return TXL_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_r) < static_cast<long long>(M) + W || !std::isfinite(scale))
+    return TXL_ERR_INVALID_ARG;
+  if (D > 256 || B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
+  const long long L = static_cast<long long>(M) + W;
+  if (L > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
+  const size_t es = dsize(dtype), gs = dsize(go_dtype);
+  const size_t hd = static_cast<size_t>(H) * D, bw = static_cast<size_t>(B) * W;
+  const Range in_r[] = {range_of(q, bw * hd * es),
+                        range_of(k, B * static_cast<size_t>(L) * hd * es),
+                        range_of(v, B * static_cast<size_t>(L) * hd * es),
+                        range_of(r, static_cast<size_t>(n_r) * hd * es),
+                        range_of(bias_u, hd * 4),
+                        range_of(bias_v, hd * 4),
+                        range_of(o, bw * hd * gs),
+                        range_of(lse, bw * H * 4),
+                        range_of(dout, bw * hd * gs)};
+  const Range out_r[] = {range_of(dq, bw * hd * 4), range_of(dk, bw * hd * 4), range_of(dv, bw * hd * 4),
+                         range_of(dr, static_cast<size_t>(n_r) * hd * 4), range_of(dbias_u, hd * 4),
+                         range_of(dbias_v, hd * 4)};
+  for (size_t x = 0; x < 6; ++x) {
+    for (const Range& y : in_r)
+      if (overlap(out_r[x], y)) return TXL_ERR_ALIAS;
+    for (size_t z = x + 1; z < 6; ++z)
+      if (overlap(out_r[x], out_r[z])) return TXL_ERR_ALIAS;
+  }
+  void* scratch = nullptr;
+  int* unused = nullptr;
+  if (split_scratch(stream, txl::relattn_bwd_simt_scratch_bytes(B, W, H, D), 0, &scratch, &unused) != cudaSuccess)
+    return TXL_ERR_CUDA;
+  const bool vec16 = (D * es) % 16 == 0;  // with 16-byte aligned bases, every row is then aligned
+  return from_cuda(txl::launch_relattn_bwd_simt(q, k, v, r, bias_u, bias_v, o, lse, dout, dq, dk, dv, dr, dbias_u,
+                                                dbias_v, B, W, M, H, D, n_r, scale, dtype == TXL_BF16,
+                                                go_dtype == TXL_BF16, vec16, scratch, stream));
+}
+
 int txl_relattn_forward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                         const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r,
                         float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {

@@ -61,6 +61,18 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
                                 float scale, int nsplit, float* part_o, float* part_lse, int* part_cnt,
                                 const WaitCtl& wc, cudaStream_t stream);
 
+// Backward on CUDA cores (fp32 arithmetic; q, k, v, r fp32 or bf16, o and
+// dout fp32 or bf16; D <= 256).  dk, dv cover the segment's key rows.
+// scratch: relattn_bwd_simt_scratch_bytes(B, W, H, D) bytes.  vec16: every
+// row of q, k, v, r starts on a 16-byte boundary and D is a multiple of the
+// 16-byte vector width.
+size_t relattn_bwd_simt_scratch_bytes(int B, int W, int H, int D);
+cudaError_t launch_relattn_bwd_simt(const void* q, const void* k, const void* v, const void* r,
+                                    const float* bias_u, const float* bias_v, const void* o, const float* lse,
+                                    const void* dout, float* dq, float* dk, float* dv, float* dr, float* du,
+                                    float* dvb, int B, int W, int M, int H, int D, int n_r, float scale, bool bf16,
+                                    bool go_bf16, bool vec16, void* scratch, cudaStream_t stream);
+
 // Number of chunks the D = 64 kernel should split each unit's key steps
 // into (1: no split), from the shape and the device's SM count.
 int relattn_tc64_split(int B, int H, int W, int M);
