@@ -220,9 +220,13 @@ TXL_API int txl_relattn_forward_roll(const void* q, const void* k, const void* v
  * Every output is overwritten (not accumulated into).  Outputs must not
  * overlap each other or any input (TXL_ERR_ALIAS); every pointer 16-byte
  * aligned (TXL_ERR_INVALID_ARG).  D <= 256 (TXL_ERR_UNSUPPORTED otherwise).
- * Library scratch of [B, H, W] + [B, W/4, H, 2, D] floats per (device,
- * stream) is allocated on first use and reused.  Results are deterministic
- * (no atomics).
+ * Paths: bf16 q, k, v, r with bf16 o and dout and D = 64 run on the tensor
+ * cores (tcgen05): a dq kernel over query tiles (which also sums dr and the
+ * bias gradients) and a dk/dv kernel over 64-key blocks; there dr arrives by
+ * fp32 atomic adds, so its last bits may differ between calls.  Every other
+ * case runs on CUDA cores in fp32 arithmetic, fully deterministic.  Library
+ * scratch (per-row Delta and per-tile partial sums) is allocated per (device,
+ * stream) on first use and reused.
  */
 TXL_API int txl_relattn_backward(const void* q, const void* k, const void* v, const void* r,
                          const float* bias_u, const float* bias_v, const void* o, const float* lse,

@@ -79,6 +79,11 @@ CASES = [
     (1, 2, 128, 64, 0, "bf16", 2),
     (1, 1, 64, 5, 3, "bf16", 0),     # fewer rows than a warp
     (1, 2, 256, 40, 24, "f32", 0),   # largest head dim
+    # bf16, D = 64: the tensor-core kernels
+    (2, 3, 64, 300, 37, "bf16", 5),  # memory not a multiple of the key step
+    (1, 2, 64, 256, 0, "bf16", 0),   # first segment, whole tiles
+    (1, 2, 64, 128, 512, "bf16", 0), # memory longer than the segment
+    (3, 1, 64, 64, 64, "bf16", 64),  # half a query tile
 ]
 
 
@@ -107,12 +112,36 @@ def test_backward_custom_scale(txl):
     _compare(got, want, "f32")
 
 
-def test_backward_deterministic(txl):
-    q, k, v, r, bu, bv, dout = _case(2, 2, 64, 130, 70, "bf16")
-    a = _run(txl, q, k, v, r, bu, bv, dout, 70, "bf16")
-    b = _run(txl, q, k, v, r, bu, bv, dout, 70, "bf16")
+@pytest.mark.parametrize("dtype,o_dtype", [("bf16", "f32"), ("f32", "f32"), ("bf16", "bf16")])
+def test_backward_deterministic(txl, dtype, o_dtype):
+    """Bit-identical on repeated calls, except dr on the tensor-core path
+    (bf16 o and dout, D = 64), whose slot sums arrive by fp32 atomics in any
+    order: there the two results agree to fp32 rounding."""
+    q, k, v, r, bu, bv, dout = _case(2, 2, 64, 130, 70, dtype)
+    a = _run(txl, q, k, v, r, bu, bv, dout, 70, dtype, o_dtype=o_dtype)
+    b = _run(txl, q, k, v, r, bu, bv, dout, 70, dtype, o_dtype=o_dtype)
+    tc = dtype == "bf16" and o_dtype == "bf16"
     for key in KEYS:
-        assert np.array_equal(a[key], b[key]), key
+        if tc and key == "dr":
+            np.testing.assert_allclose(a[key], b[key], rtol=1e-5, atol=1e-6)
+        else:
+            assert np.array_equal(a[key], b[key]), key
+
+
+def test_backward_base_size_sampled_head(txl):
+    """The base workload at full size (B=22, H=8, D=64, W=512, M=512) in one
+    call; the oracle checks every gradient of one head (dq, dk, dv of all 22
+    sequences, and dr, dbias_u, dbias_v, which sum over them)."""
+    B, H, D, W, M = 22, 8, 64, 512, 512
+    q, k, v, r, bu, bv, dout = _case(B, H, D, W, M, "bf16")
+    got = _run(txl, q, k, v, r, bu, bv, dout, M, "bf16")
+    h = 3
+    sl = slice(h, h + 1)
+    want = O.relattn_backward(q[:, :, sl], k[:, :, sl], v[:, :, sl], r[:, sl], bu[sl], bv[sl], M, dout[:, :, sl],
+                              D ** -0.5)
+    head = {"dq": got["dq"][:, :, sl], "dk": got["dk"][:, :, sl], "dv": got["dv"][:, :, sl],
+            "dr": got["dr"][:, sl], "dbias_u": got["dbias_u"][sl], "dbias_v": got["dbias_v"][sl]}
+    _compare(head, want, "bf16")
 
 
 def test_backward_rejects_bad_arguments(txl):

@@ -486,6 +486,53 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
   }
   void* scratch = nullptr;
   int* unused = nullptr;
+  if (dtype == TXL_BF16 && go_dtype == TXL_BF16 && D == 64) {
+    // tensor-core path
+    if (split_scratch(stream, txl::relattn_bwd_tc64_scratch_bytes(B, W, H), 0, &scratch, &unused) != cudaSuccess)
+      return TXL_ERR_CUDA;
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (encode == nullptr) return TXL_ERR_CUDA;
+    auto encode_bf16 = [&](CUtensorMap* m, const void* base, int rank, const cuuint64_t* dims,
+                           const cuuint64_t* strides, const cuuint32_t* box) {
+      const cuuint32_t estr[4] = {1, 1, 1, 1};
+      return encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    };
+    CUtensorMap tm_q, tm_do, tm_k, tm_v, tm_rw;
+    {
+      const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                  static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(B)};
+      const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(W) * hd * 2};
+      const cuuint32_t box[4] = {64, 1, 128, 1};
+      if (!encode_bf16(&tm_q, q, 4, dims, strides, box) || !encode_bf16(&tm_do, dout, 4, dims, strides, box))
+        return TXL_ERR_CUDA;
+    }
+    {
+      const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                  static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
+      const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(L) * hd * 2};
+      const cuuint32_t box[4] = {64, 1, 64, 1};
+      if (!encode_bf16(&tm_k, k, 4, dims, strides, box) || !encode_bf16(&tm_v, v, 4, dims, strides, box))
+        return TXL_ERR_CUDA;
+    }
+    {
+      const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                  static_cast<cuuint64_t>(n_r)};
+      const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2, hd * 2};
+      const cuuint32_t box[3] = {64, 1, 192};
+      if (!encode_bf16(&tm_rw, r, 3, dims, strides, box)) return TXL_ERR_CUDA;
+    }
+    txl::WaitCtl wc;
+    if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
+    wc.limit_ns = g_wait_ns.load();
+    wc.inject_stall = 0;
+    const long long nqt = (W + 127) / 128;
+    if (nqt * B * H > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
+    return from_cuda(txl::launch_relattn_bwd_tc64(tm_q, tm_k, tm_v, tm_rw, tm_do, bias_u, bias_v, lse, o, dout, dq,
+                                                  dk, dv, dr, dbias_u, dbias_v, B, W, M, H, n_r, scale, scratch, wc,
+                                                  stream));
+  }
   if (split_scratch(stream, txl::relattn_bwd_simt_scratch_bytes(B, W, H, D), 0, &scratch, &unused) != cudaSuccess)
     return TXL_ERR_CUDA;
   const bool vec16 = (D * es) % 16 == 0;  // with 16-byte aligned bases, every row is then aligned

@@ -387,6 +387,12 @@ cudaError_t launch_typed(BwdArgs a, float* du, float* dvb, cudaStream_t stream) 
 
 }  // namespace
 
+cudaError_t launch_bwd_bias(const float* part, int n_part, int H, int D, float* du, float* dvb,
+                            cudaStream_t stream) {
+  bwd_bias_kernel<<<H, 256, 0, stream>>>(part, n_part, H, D, du, dvb);
+  return cudaGetLastError();
+}
+
 size_t relattn_bwd_simt_scratch_bytes(int B, int W, int H, int D) {
   const size_t nb = (static_cast<size_t>(W) + kWarps - 1) / kWarps;
   return sizeof(float) * (static_cast<size_t>(B) * H * W + static_cast<size_t>(B) * nb * H * 2 * D);

@@ -1,0 +1,764 @@
+// Backward of the relative attention on the tensor cores: bf16 q, k, v, r,
+// o and dout, D = 64, fp32 accumulation and gradients.
+//
+// The gradients (see relattn_bwd.cu for the formulas and the stop-gradient)
+// come from two kernels that each rebuild the scores of the forward:
+//
+//   dq kernel, one CTA per 128-query tile of a (batch, head), 64-key steps:
+//     S = (q+u) K^T, dP = dout V^T and the 192-distance window (q+v) R^T of
+//     the step (three MMAs); each thread owns one query row (TMEM lane) and
+//     forms p = exp(s - lse), g = scale p (dP - Delta), with the distance
+//     term shifted into key order as in the forward.  g goes to shared
+//     memory twice: in key order (G, the A operand of d(q+u) += G K) and
+//     skewed into distance order (Gs: row i, column d = M+i-j).  A distance
+//     slot of 64 rows receives its last values two steps after its first;
+//     then d(q+v) += Gs R and dr += Gs^T (q+v) (an M = 64 MMA) run on it, and
+//     the slot's dr rows are added to the output with fp32 vector atomics.
+//   dk/dv kernel, one CTA per 64 segment keys of a (batch, head), looping
+//     over the 128-query tiles that see them: the same three MMAs and the
+//     same p, g; then dV += P^T dout and dK += G^T (q+u) with P and G read
+//     as MN-major A operands (M = 64 keys).
+//
+// Both kernels are synchronous: thread 0 issues the TMA loads (double
+// buffered, one step ahead) and the MMAs; all 128 threads wait on the MMA
+// barriers.  Every wait is bounded; a timeout raises the device status word
+// and the CTA drains its own copies and MMAs before it exits.
+//
+// TMEM (512 columns): S [0, 64), dP [64, 128), distance window [128, 320)
+// (reused for the dr slot result, M = 64 layout), d(q+u) or dV [320, 384),
+// d(q+v) or dK [384, 448).  An M = 64 result keeps its row r in lane
+// 32 (r / 16) + r % 16.
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include <cstdint>
+
+#include "relattn_tc_common.cuh"
+#include "txl_device.cuh"
+#include "txl_internal.h"
+
+namespace txl {
+namespace {
+
+constexpr int kThreads = 128;
+constexpr int D = 64;
+constexpr int BM = 128;     // query rows per tile
+constexpr int BN = 64;      // keys per step / block
+constexpr int kWin = 192;   // distance rows of a step's window
+constexpr int kTile = BM * 128;          // 128 rows x 64 bf16
+constexpr int kKTile = BN * 128;         // 64 rows x 64 bf16
+constexpr int kWinTile = kWin * 128;     // 192 rows x 64 bf16
+constexpr uint32_t kColS = 0, kColDP = 64, kColWin = 128, kColA = 320, kColB = 384, kTmemCols = 512;
+constexpr float kLog2e = 1.4426950408889634f;
+
+// dq kernel shared memory
+constexpr int kQOffQu = 0;
+constexpr int kQOffQv = kQOffQu + kTile;
+constexpr int kQOffDO = kQOffQv + kTile;
+constexpr int kQOffK = kQOffDO + kTile;          // 2 stages
+constexpr int kQOffV = kQOffK + 2 * kKTile;      // 2 stages
+constexpr int kQOffR = kQOffV + 2 * kKTile;      // 2 stages
+constexpr int kQOffG = kQOffR + 2 * kWinTile;    // G in key order (also the raw q tile at the start)
+constexpr int kQOffGs = kQOffG + kTile;          // 4 distance slots
+constexpr int kQOffBar = kQOffGs + 4 * kTile;
+constexpr int kQSmem = kQOffBar + 256 + 1024;
+static_assert(kQSmem <= 232448, "shared memory budget");
+
+// dk/dv kernel shared memory
+constexpr int kKOffK = 0;
+constexpr int kKOffV = kKOffK + kKTile;
+constexpr int kKOffQu = kKOffV + kKTile;
+constexpr int kKOffQv = kKOffQu + kTile;
+constexpr int kKOffQ = kKOffQv + kTile;          // raw q, 2 stages
+constexpr int kKOffDO = kKOffQ + 2 * kTile;      // 2 stages
+constexpr int kKOffR = kKOffDO + 2 * kTile;      // 2 stages
+constexpr int kKOffP = kKOffR + 2 * kWinTile;
+constexpr int kKOffG = kKOffP + kTile;
+constexpr int kKOffBar = kKOffG + kTile;
+constexpr int kKSmem = kKOffBar + 256 + 1024;
+static_assert(kKSmem <= 232448, "shared memory budget");
+
+struct BwdParams {
+  const float* bias_u;
+  const float* bias_v;
+  const float* lse;         // [B, H, W]
+  const __nv_bfloat16* o;   // [B, W, H, D]
+  const __nv_bfloat16* dout;
+  float* dq;                // [B, W, H, D]
+  float* dk;                // [B, W, H, D]
+  float* dv;
+  float* dr;                // [n_r, H, D], zeroed before the dq kernel
+  float* delta;             // [B, H, W] scratch: written by the dq kernel, read by the dk/dv kernel
+  float* part;              // [B * nqt][H][2][D] scratch: per-tile sums of d(q+u), d(q+v)
+  int B, W, M, H, n_r, nqt;
+  float scale, scale_log2e;
+  unsigned int* status;
+  unsigned long long wait_ns;
+};
+
+struct QBars {
+  uint64_t q, kv[2], r[2], m1, m2, fin;
+  uint32_t tmem_base;
+  int abort;
+};
+struct KBars {
+  uint64_t kv, in[2], m1, m2, fin;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Byte offset of bf16 element (row, col) in a 128B-swizzled tile of 64-column rows.
+__device__ __forceinline__ uint32_t swz(int row, int col) {
+  return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ (row & 7))) << 4) +
+                               ((col & 7) << 1));
+}
+
+// Row a of (q+u) and (q+v) from the raw q row (all three 128B-swizzled
+// tiles); bu, bv: the head's u and v in global memory.
+__device__ __forceinline__ void build_qu_qv(const uint8_t* sQ, uint8_t* sQu, uint8_t* sQv, int a,
+                                            const float* __restrict__ bu, const float* __restrict__ bv) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t off = (a >> 3) * 1024 + (a & 7) * 128 + ((c ^ (a & 7)) << 4);
+    const uint4 raw = *reinterpret_cast<const uint4*>(sQ + off);
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    const float4 u0 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c));
+    const float4 u1 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c + 4));
+    const float4 v0 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c));
+    const float4 v1 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c + 4));
+    const float ub[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    const float vb[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t qu[4], qv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+      qu[e] = pack_bf16x2(x0 + ub[2 * e], x1 + ub[2 * e + 1]);
+      qv[e] = pack_bf16x2(x0 + vb[2 * e], x1 + vb[2 * e + 1]);
+    }
+    *reinterpret_cast<uint4*>(sQu + off) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+    *reinterpret_cast<uint4*>(sQv + off) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+  }
+}
+
+// Delta_i = dout_i . o_i over the 64 bf16 of each row.
+__device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bfloat16* g) {
+  float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint4 a = __ldg(reinterpret_cast<const uint4*>(o) + c);
+    const uint4 b = __ldg(reinterpret_cast<const uint4*>(g) + c);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      s0 = fmaf(bf16_lo(aw[e]), bf16_lo(bw[e]), s0);
+      s1 = fmaf(bf16_hi(aw[e]), bf16_hi(bw[e]), s1);
+    }
+  }
+  return s0 + s1;
+}
+
+// The step's probabilities p and gradients g for this thread's row, from
+// S, dP and the distance window in TMEM.  quad: the warp's lane quadrant;
+// lane: the row within it; visible(c): key column c is visible to the row.
+// Returns the row's p and g for the step's 64 key columns.
+template <typename Vis>
+__device__ __forceinline__ void step_grads(uint32_t tmem, int quad, int lane, float lse2, float delta,
+                                           float scale, float scale_log2e, Vis visible, float (&g)[64],
+                                           float (&p)[64]) {
+  const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  uint32_t bd0[16], bd1[16];
+  uint32_t s0[32], s1[32];
+  {
+    uint32_t xa[32], xb[32], xc[32];
+    tmem_ld32(lb + kColWin + 32 * quad, xa);
+    tmem_ld32(lb + kColWin + 32 * quad + 32, xb);
+    tmem_ld32(lb + kColWin + 32 * quad + 64, xc);
+    tmem_ld32(lb + kColS, s0);
+    tmem_ld32(lb + kColS + 32, s1);
+    tmem_wait_ld(xa);
+    tmem_wait_ld(xb);
+    tmem_wait_ld(xc);
+    tmem_wait_ld(s0);
+    tmem_wait_ld(s1);
+    uint32_t pa[16], pb[16], pc[16];
+    pack32(xa, pa);
+    pack32(xb, pb);
+    pack32(xc, pc);
+    // columns 0-31 use window positions [32, 96) of the warp's 96, columns 32-63 [0, 64)
+    window_shift_packed(pb, pc, lane, bd0);
+    window_shift_packed(pa, pb, lane, bd1);
+  }
+  add_window(s0, bd0, p);
+  add_window(s1, bd1, p + 32);
+  {
+    uint32_t d0[32], d1[32];
+    tmem_ld32(lb + kColDP, d0);
+    tmem_ld32(lb + kColDP + 32, d1);
+    tmem_wait_ld(d0);
+    tmem_wait_ld(d1);
+#pragma unroll
+    for (int c = 0; c < 64; ++c) {
+      const float e = visible(c) ? ex2(fmaf(p[c], scale_log2e, -lse2)) : 0.f;
+      const float dp = __uint_as_float(c < 32 ? d0[c] : d1[c - 32]);
+      p[c] = e;
+      g[c] = scale * e * (dp - delta);
+    }
+  }
+}
+
+// Row a of a 128B-swizzled [128 x 64] bf16 tile from 64 floats.
+__device__ __forceinline__ void store_row(uint8_t* tile, int a, const float (&x)[64]) {
+  uint8_t* row = tile + (a >> 3) * 1024 + (a & 7) * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t w0 = pack_bf16x2(x[8 * c], x[8 * c + 1]), w1 = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+    const uint32_t w2 = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), w3 = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+    *reinterpret_cast<uint4*>(row + ((c ^ (a & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
+  }
+}
+
+// ============================================================================
+// dq kernel
+// ============================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dq_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
+                       const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sQu = smem + kQOffQu;
+  uint8_t* sQv = smem + kQOffQv;
+  uint8_t* sDO = smem + kQOffDO;
+  uint8_t* sK = smem + kQOffK;
+  uint8_t* sV = smem + kQOffV;
+  uint8_t* sR = smem + kQOffR;
+  uint8_t* sG = smem + kQOffG;
+  uint8_t* sGs = smem + kQOffGs;
+  QBars* bars = reinterpret_cast<QBars*>(smem + kQOffBar);
+  volatile int* abort = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp, a = tid;
+  const uint64_t wait_ns = p.wait_ns;
+
+  const Unit w = decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt);
+  const int T = w.nks;
+  const int i = w.i0 + a;  // this thread's query row
+  const int L = p.M + p.W;
+
+  if (tid == 0) {
+    mbar_init(&bars->q, 1);
+    mbar_init(&bars->kv[0], 1);
+    mbar_init(&bars->kv[1], 1);
+    mbar_init(&bars->r[0], 1);
+    mbar_init(&bars->r[1], 1);
+    mbar_init(&bars->m1, 1);
+    mbar_init(&bars->m2, 1);
+    mbar_init(&bars->fin, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  // Distance slots start at zero: a slot entry no step writes is a pair
+  // that does not exist.
+  for (int x = tid; x < 4 * kTile / 16; x += kThreads)
+    reinterpret_cast<uint4*>(sGs)[x] = make_uint4(0u, 0u, 0u, 0u);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  // Window of step t: distance rows [wb(t), wb(t) + 192), wb = M + i0 - 64 t - 64.
+  auto wbase = [&](int t) { return p.M + w.i0 - BN * t - BN; };
+  uint32_t n_ld[2] = {0, 0};  // loads issued per stage (thread 0)
+  auto issue_step_loads = [&](int t) {
+    const int s = t & 1;
+    mbar_arrive_expect_tx(&bars->kv[s], 2 * kKTile);
+    tma_load_4d(sK + s * kKTile, &tm_k, &bars->kv[s], 0, w.h, BN * t, w.b);
+    tma_load_4d(sV + s * kKTile, &tm_v, &bars->kv[s], 0, w.h, BN * t, w.b);
+    mbar_arrive_expect_tx(&bars->r[s], kWinTile);
+    tma_load_3d(sR + s * kWinTile, &tm_rw, &bars->r[s], 0, w.h, wbase(t));
+    ++n_ld[s];
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_rw);
+    tma_prefetch_desc(&tm_do);
+    mbar_arrive_expect_tx(&bars->q, 2 * kTile);
+    tma_load_4d(sG, &tm_q, &bars->q, 0, w.h, w.i0, w.b);  // raw q, into the G tile for now
+    tma_load_4d(sDO, &tm_do, &bars->q, 0, w.h, w.i0, w.b);
+    issue_step_loads(0);
+  }
+
+  // Per-row constants: lse (log2 domain), Delta, u and v of the head.
+  const long long row_id = (static_cast<long long>(w.b) * p.H + w.h) * p.W + i;
+  float lse2 = INFINITY, delta = 0.f;  // rows past W: every p is 0
+  if (i < p.W) {
+    lse2 = p.lse[row_id] * kLog2e;
+    const long long off = ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D;
+    delta = row_delta(p.o + off, p.dout + off);
+    p.delta[row_id] = delta;
+  }
+  bool ok = mbar_wait(&bars->q, 0, wait_ns, abort);
+  if (ok) build_qu_qv(sG, sQu, sQv, a, p.bias_u + w.h * D, p.bias_v + w.h * D);
+  if (!ok) report_timeout(abort, p.status);
+  fence_proxy_async_smem();
+  ok = __syncthreads_and(ok) != 0;
+
+  constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
+  constexpr uint32_t id192 = idesc_bf16(128, 192, false, false);
+  constexpr uint32_t idMN = idesc_bf16(128, 64, false, true);   // B MN-major
+  constexpr uint32_t idT = idesc_bf16(64, 64, true, true);      // A and B MN-major, M = 64
+  const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
+  const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
+  const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
+  const uint64_t dG = sdesc_sw128(smem_u32(sG), 16, 1024);
+  const uint64_t dQvMN = sdesc_sw128(smem_u32(sQv), 8192, 1024);
+  uint32_t n_m2 = 0;  // MMA2 rounds (commits on m2)
+  int n_slot = 0;     // distance slots finished
+
+  // d(q+v) += Gs R and dr_slot = Gs^T (q+v) for distance slot tau, whose R
+  // rows are rows [64 r_row, 64 r_row + 64) of window stage rs.
+  auto slot_mmas = [&](int tau, int rs, int r_row) {
+    const int gi = (tau + 2) & 3;
+    const uint64_t dGs = sdesc_sw128(smem_u32(sGs + gi * kTile), 16, 1024);
+    const uint64_t dGsT = sdesc_sw128(smem_u32(sGs + gi * kTile), 8192, 1024);
+    const uint64_t dRs = sdesc_sw128(smem_u32(sR + rs * kWinTile + r_row * kKTile), 8192, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColB, dGs + 2 * kk, dRs + 128 * kk, idMN, n_slot > 0 || kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColWin, dGsT + 128 * kk, dQvMN + 128 * kk, idT, kk > 0);
+    ++n_slot;
+  };
+  // Adds the dr rows of the finished slot tau (now in TMEM at the window
+  // columns, M = 64 layout) to the output.
+  auto flush_dr = [&](int tau) {
+    uint32_t v0[32], v1[32];
+    const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColWin;
+    tmem_ld32(lb, v0);
+    tmem_ld32(lb + 32, v1);
+    tmem_wait_ld(v0);
+    tmem_wait_ld(v1);
+    const int r = 16 * warp + lane;  // row of the slot
+    const int d = p.M + w.i0 - BN * tau - BN + r;
+    if (lane < 16 && d >= 0 && d < L) {
+      float4* dst = reinterpret_cast<float4*>(p.dr + (static_cast<long long>(d) * p.H + w.h) * D);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        atomicAdd(dst + e, make_float4(__uint_as_float(v0[4 * e]), __uint_as_float(v0[4 * e + 1]),
+                                       __uint_as_float(v0[4 * e + 2]), __uint_as_float(v0[4 * e + 3])));
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        atomicAdd(dst + 8 + e, make_float4(__uint_as_float(v1[4 * e]), __uint_as_float(v1[4 * e + 1]),
+                                           __uint_as_float(v1[4 * e + 2]), __uint_as_float(v1[4 * e + 3])));
+    }
+  };
+
+  for (int t = 0; t < T && ok; ++t) {
+    const int s = t & 1;
+    // (A) thread 0: the step's score MMAs, then the next step's loads.
+    bool ok0 = true;
+    if (tid == 0) {
+      tc_fence_after();
+      ok0 = mbar_wait(&bars->kv[s], (t >> 1) & 1, wait_ns, abort) &&
+            mbar_wait(&bars->r[s], (t >> 1) & 1, wait_ns, abort);
+      if (ok0) {
+        const uint64_t dK = sdesc_sw128(smem_u32(sK + s * kKTile), 16, 1024);
+        const uint64_t dV = sdesc_sw128(smem_u32(sV + s * kKTile), 16, 1024);
+        const uint64_t dR = sdesc_sw128(smem_u32(sR + s * kWinTile), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColS, dQu + 2 * kk, dK + 2 * kk, id64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColDP, dDO + 2 * kk, dV + 2 * kk, id64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColWin, dQv + 2 * kk, dR + 2 * kk, id192, kk > 0);
+        tc_commit(&bars->m1);
+        if (t + 1 < T) issue_step_loads(t + 1);  // stage s^1 was last read by step t-1's MMAs, all done
+      } else {
+        report_timeout(abort, p.status);
+      }
+    }
+    // (B) everyone: the step's gradients.
+    ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort) && ok0;
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    {
+      float g[64], pr[64];
+      const int lim = p.M + i - BN * t;  // key column c visible iff c <= lim
+      step_grads(tmem, quad, lane, lse2, delta, p.scale, p.scale_log2e, [&](int c) { return c <= lim; }, g,
+                 pr);
+      store_row(sG, a, g);
+      // Skewed copy: key column c of step t sits at window position
+      // z = 64 + a - c, i.e. in distance slot t - z / 64, column z % 64.
+#pragma unroll
+      for (int c = 0; c < 64; ++c) {
+        const int z = 64 + a - c;
+        const int gi = (t - (z >> 6) + 2) & 3;
+        *reinterpret_cast<__nv_bfloat16*>(sGs + gi * kTile + swz(a, z & 63)) = __float2bfloat16_rn(g[c]);
+      }
+      // The slot that step t+1 opens held slot t-3, whose MMAs ran at step t-1.
+      uint4* nxt = reinterpret_cast<uint4*>(sGs + ((t + 3) & 3) * kTile);
+      for (int x = tid; x < kTile / 16; x += kThreads) nxt[x] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // (C) thread 0: d(q+u) += G K, and the slot that step t finished (t-2).
+    if (tid == 0) {
+      tc_fence_after();
+      const uint64_t dKmn = sdesc_sw128(smem_u32(sK + s * kKTile), 8192, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColA, dG + 2 * kk, dKmn + 128 * kk, idMN, t > 0 || kk > 0);
+      slot_mmas(t - 2, s, 2);
+      tc_commit(&bars->m2);
+    }
+    ok = mbar_wait(&bars->m2, n_m2 & 1, wait_ns, abort);
+    ++n_m2;
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    flush_dr(t - 2);
+    tc_fence_before();
+    __syncthreads();
+  }
+  // The last two slots are finished once the last step has written them.
+  for (int k = 0; k < 2 && ok; ++k) {
+    const int tau = T - 2 + k;
+    if (tid == 0) {
+      tc_fence_after();
+      slot_mmas(tau, (T - 1) & 1, T - 1 - tau);
+      tc_commit(&bars->m2);
+    }
+    ok = mbar_wait(&bars->m2, n_m2 & 1, wait_ns, abort);
+    ++n_m2;
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    flush_dr(tau);
+    tc_fence_before();
+    __syncthreads();
+  }
+
+  if (ok) {
+    // dq = d(q+u) + d(q+v) for this row; the tile's column sums of both go
+    // to the bias partials (through shared memory, XOR-staggered columns).
+    uint32_t u0[32], u1[32], v0[32], v1[32];
+    const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    tmem_ld32(lb + kColA, u0);
+    tmem_ld32(lb + kColA + 32, u1);
+    tmem_ld32(lb + kColB, v0);
+    tmem_ld32(lb + kColB + 32, v1);
+    tmem_wait_ld(u0);
+    tmem_wait_ld(u1);
+    tmem_wait_ld(v0);
+    tmem_wait_ld(v1);
+    if (i < p.W) {
+      float4* dst = reinterpret_cast<float4*>(p.dq + ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D);
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        dst[e] = make_float4(__uint_as_float(u0[4 * e]) + __uint_as_float(v0[4 * e]),
+                             __uint_as_float(u0[4 * e + 1]) + __uint_as_float(v0[4 * e + 1]),
+                             __uint_as_float(u0[4 * e + 2]) + __uint_as_float(v0[4 * e + 2]),
+                             __uint_as_float(u0[4 * e + 3]) + __uint_as_float(v0[4 * e + 3]));
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        dst[8 + e] = make_float4(__uint_as_float(u1[4 * e]) + __uint_as_float(v1[4 * e]),
+                                 __uint_as_float(u1[4 * e + 1]) + __uint_as_float(v1[4 * e + 1]),
+                                 __uint_as_float(u1[4 * e + 2]) + __uint_as_float(v1[4 * e + 2]),
+                                 __uint_as_float(u1[4 * e + 3]) + __uint_as_float(v1[4 * e + 3]));
+    }
+    // red[x][row ^ (x & 31)]: column x of the row sums (x < 64: d(q+u)).
+    float* red = reinterpret_cast<float*>(sGs);
+#pragma unroll
+    for (int x = 0; x < 32; ++x) {
+      red[x * BM + (a ^ x)] = __uint_as_float(u0[x]);
+      red[(32 + x) * BM + (a ^ x)] = __uint_as_float(u1[x]);
+      red[(64 + x) * BM + (a ^ x)] = __uint_as_float(v0[x]);
+      red[(96 + x) * BM + (a ^ x)] = __uint_as_float(v1[x]);
+    }
+    __syncthreads();
+    float sum = 0.f;
+    for (int r = 0; r < BM; ++r) sum += red[tid * BM + (r ^ (tid & 31))];
+    const int qt = w.i0 / BM;
+    p.part[((static_cast<long long>(w.b) * p.nqt + qt) * p.H + w.h) * 2 * D + tid] = sum;
+  }
+  // Let this CTA's own copies and MMAs finish before the memory is released.
+  if (tid == 0) {
+    for (int s = 0; s < 2; ++s)
+      if (n_ld[s] > 0) mbar_wait_own(&bars->kv[s], (n_ld[s] - 1) & 1, wait_ns);
+    for (int s = 0; s < 2; ++s)
+      if (n_ld[s] > 0) mbar_wait_own(&bars->r[s], (n_ld[s] - 1) & 1, wait_ns);
+    mbar_wait_own(&bars->q, 0, wait_ns);
+    tc_commit(&bars->fin);
+    mbar_wait_own(&bars->fin, 0, wait_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ============================================================================
+// dk / dv kernel
+// ============================================================================
+__global__ void __launch_bounds__(kThreads, 1)
+    bwd_dkdv_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
+                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sK = smem + kKOffK;
+  uint8_t* sV = smem + kKOffV;
+  uint8_t* sQu = smem + kKOffQu;
+  uint8_t* sQv = smem + kKOffQv;
+  uint8_t* sQ = smem + kKOffQ;
+  uint8_t* sDO = smem + kKOffDO;
+  uint8_t* sR = smem + kKOffR;
+  uint8_t* sP = smem + kKOffP;
+  uint8_t* sG = smem + kKOffG;
+  KBars* bars = reinterpret_cast<KBars*>(smem + kKOffBar);
+  volatile int* abort = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp, a = tid;
+  const uint64_t wait_ns = p.wait_ns;
+
+  // Block of 64 segment keys jj0 .. jj0+63 (rows M+jj of k and v) of (b, h).
+  const int nkb = (p.W + BN - 1) / BN;
+  const int bh = blockIdx.x / nkb;
+  const int b = bh / p.H, h = bh % p.H;
+  const int jj0 = (blockIdx.x % nkb) * BN;
+  const int qt0 = jj0 / BM;             // first query tile with a row i >= jj0
+  const int NT = p.nqt - qt0;
+
+  if (tid == 0) {
+    mbar_init(&bars->kv, 1);
+    mbar_init(&bars->in[0], 1);
+    mbar_init(&bars->in[1], 1);
+    mbar_init(&bars->m1, 1);
+    mbar_init(&bars->m2, 1);
+    mbar_init(&bars->fin, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem_base, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  uint32_t n_ld[2] = {0, 0};
+  auto issue_tile_loads = [&](int s) {  // query tile qt0 + s
+    const int st = s & 1, i0 = (qt0 + s) * BM;
+    mbar_arrive_expect_tx(&bars->in[st], 2 * kTile + kWinTile);
+    tma_load_4d(sQ + st * kTile, &tm_q, &bars->in[st], 0, h, i0, b);
+    tma_load_4d(sDO + st * kTile, &tm_do, &bars->in[st], 0, h, i0, b);
+    tma_load_3d(sR + st * kWinTile, &tm_rw, &bars->in[st], 0, h, i0 - jj0 - BN);
+    ++n_ld[st];
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_rw);
+    tma_prefetch_desc(&tm_do);
+    mbar_arrive_expect_tx(&bars->kv, 2 * kKTile);
+    tma_load_4d(sK, &tm_k, &bars->kv, 0, h, p.M + jj0, b);
+    tma_load_4d(sV, &tm_v, &bars->kv, 0, h, p.M + jj0, b);
+    issue_tile_loads(0);
+  }
+
+  constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
+  constexpr uint32_t id192 = idesc_bf16(128, 192, false, false);
+  constexpr uint32_t idT = idesc_bf16(64, 64, true, true);
+  const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
+  const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
+  const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+  const uint64_t dV = sdesc_sw128(smem_u32(sV), 16, 1024);
+  const uint64_t dPT = sdesc_sw128(smem_u32(sP), 8192, 1024);
+  const uint64_t dGT = sdesc_sw128(smem_u32(sG), 8192, 1024);
+  const uint64_t dQuMN = sdesc_sw128(smem_u32(sQu), 8192, 1024);
+
+  bool ok = true;
+  for (int s = 0; s < NT && ok; ++s) {
+    const int st = s & 1;
+    const int i = (qt0 + s) * BM + a;
+    // (A) everyone: this tile's rows of (q+u), (q+v); lse and Delta.
+    float lse2 = INFINITY, delta = 0.f;
+    if (i < p.W) {
+      const long long row_id = (static_cast<long long>(b) * p.H + h) * p.W + i;
+      lse2 = p.lse[row_id] * kLog2e;
+      delta = p.delta[row_id];
+    }
+    ok = mbar_wait(&bars->in[st], (s >> 1) & 1, wait_ns, abort);
+    if (ok) build_qu_qv(sQ + st * kTile, sQu, sQv, a, p.bias_u + h * D, p.bias_v + h * D);
+    fence_proxy_async_smem();
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    // (B) thread 0: the score MMAs, then the next tile's loads.
+    bool ok0 = true;
+    if (tid == 0) {
+      tc_fence_after();
+      ok0 = s > 0 || mbar_wait(&bars->kv, 0, wait_ns, abort);
+      if (ok0) {
+        const uint64_t dDO = sdesc_sw128(smem_u32(sDO + st * kTile), 16, 1024);
+        const uint64_t dR = sdesc_sw128(smem_u32(sR + st * kWinTile), 16, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColS, dQu + 2 * kk, dK + 2 * kk, id64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColDP, dDO + 2 * kk, dV + 2 * kk, id64, kk > 0);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColWin, dQv + 2 * kk, dR + 2 * kk, id192, kk > 0);
+        tc_commit(&bars->m1);
+        if (s + 1 < NT) issue_tile_loads(s + 1);  // stage st^1 was last read by tile s-1's MMAs, all done
+      } else {
+        report_timeout(abort, p.status);
+      }
+    }
+    ok = mbar_wait(&bars->m1, s & 1, wait_ns, abort) && ok0;
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+    // (C) everyone: p and g of the tile's rows against the key block.
+    {
+      float g[64], pr[64];
+      // key jj0 + c is visible to row i iff jj0 + c <= i and it exists
+      const int lim = min(i - jj0, p.W - 1 - jj0);
+      step_grads(tmem, quad, lane, lse2, delta, p.scale, p.scale_log2e, [&](int c) { return c <= lim; }, g,
+                 pr);
+      store_row(sP, a, pr);
+      store_row(sG, a, g);
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    __syncthreads();
+    // (D) thread 0: dV += P^T dout, dK += G^T (q+u)  (M = 64 keys, K = 128 queries).
+    if (tid == 0) {
+      tc_fence_after();
+      const uint64_t dDOmn = sdesc_sw128(smem_u32(sDO + st * kTile), 8192, 1024);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColA, dPT + 128 * kk, dDOmn + 128 * kk, idT, s > 0 || kk > 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColB, dGT + 128 * kk, dQuMN + 128 * kk, idT, s > 0 || kk > 0);
+      tc_commit(&bars->m2);
+    }
+    ok = mbar_wait(&bars->m2, s & 1, wait_ns, abort);
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    tc_fence_after();
+  }
+
+  if (ok) {
+    // Rows of the M = 64 results: lanes 0-15 of each warp, row 16 warp + lane.
+    uint32_t v0[32], v1[32], k0[32], k1[32];
+    const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+    tmem_ld32(lb + kColA, v0);
+    tmem_ld32(lb + kColA + 32, v1);
+    tmem_ld32(lb + kColB, k0);
+    tmem_ld32(lb + kColB + 32, k1);
+    tmem_wait_ld(v0);
+    tmem_wait_ld(v1);
+    tmem_wait_ld(k0);
+    tmem_wait_ld(k1);
+    const int jj = jj0 + 16 * warp + lane;
+    if (lane < 16 && jj < p.W) {
+      const long long off = ((static_cast<long long>(b) * p.W + jj) * p.H + h) * D;
+      float4* dvp = reinterpret_cast<float4*>(p.dv + off);
+      float4* dkp = reinterpret_cast<float4*>(p.dk + off);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        dvp[e] = make_float4(__uint_as_float(v0[4 * e]), __uint_as_float(v0[4 * e + 1]),
+                             __uint_as_float(v0[4 * e + 2]), __uint_as_float(v0[4 * e + 3]));
+        dvp[8 + e] = make_float4(__uint_as_float(v1[4 * e]), __uint_as_float(v1[4 * e + 1]),
+                                 __uint_as_float(v1[4 * e + 2]), __uint_as_float(v1[4 * e + 3]));
+        dkp[e] = make_float4(__uint_as_float(k0[4 * e]), __uint_as_float(k0[4 * e + 1]),
+                             __uint_as_float(k0[4 * e + 2]), __uint_as_float(k0[4 * e + 3]));
+        dkp[8 + e] = make_float4(__uint_as_float(k1[4 * e]), __uint_as_float(k1[4 * e + 1]),
+                                 __uint_as_float(k1[4 * e + 2]), __uint_as_float(k1[4 * e + 3]));
+      }
+    }
+  }
+  if (tid == 0) {
+    mbar_wait_own(&bars->kv, 0, wait_ns);
+    for (int s = 0; s < 2; ++s)
+      if (n_ld[s] > 0) mbar_wait_own(&bars->in[s], (n_ld[s] - 1) & 1, wait_ns);
+    tc_commit(&bars->fin);
+    mbar_wait_own(&bars->fin, 0, wait_ns);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+}  // namespace
+
+size_t relattn_bwd_tc64_scratch_bytes(int B, int W, int H) {
+  const size_t nqt = (static_cast<size_t>(W) + BM - 1) / BM;
+  return sizeof(float) * (static_cast<size_t>(B) * H * W + static_cast<size_t>(B) * nqt * H * 2 * D);
+}
+
+cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                    const CUtensorMap& tm_rw, const CUtensorMap& tm_do, const float* bias_u,
+                                    const float* bias_v, const float* lse, const void* o, const void* dout,
+                                    float* dq, float* dk, float* dv, float* dr, float* du, float* dvb, int B,
+                                    int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
+                                    cudaStream_t stream) {
+  cudaError_t e;
+  if ((e = cudaFuncSetAttribute(bwd_dq_tc64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kQSmem)) !=
+      cudaSuccess)
+    return e;
+  if ((e = cudaFuncSetAttribute(bwd_dkdv_tc64_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kKSmem)) !=
+      cudaSuccess)
+    return e;
+  BwdParams p;
+  p.bias_u = bias_u;
+  p.bias_v = bias_v;
+  p.lse = lse;
+  p.o = static_cast<const __nv_bfloat16*>(o);
+  p.dout = static_cast<const __nv_bfloat16*>(dout);
+  p.dq = dq;
+  p.dk = dk;
+  p.dv = dv;
+  p.dr = dr;
+  p.delta = static_cast<float*>(scratch);
+  p.nqt = (W + BM - 1) / BM;
+  p.part = p.delta + static_cast<size_t>(B) * H * W;
+  p.B = B;
+  p.W = W;
+  p.M = M;
+  p.H = H;
+  p.n_r = n_r;
+  p.scale = scale;
+  p.scale_log2e = scale * kLog2e;
+  p.status = wc.status;
+  p.wait_ns = wc.limit_ns;
+  if ((e = cudaMemsetAsync(dr, 0, sizeof(float) * static_cast<size_t>(n_r) * H * D, stream)) != cudaSuccess)
+    return e;
+  const int units = p.nqt * B * H;
+  bwd_dq_tc64_kernel<<<units, kThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const int nkb = (W + BN - 1) / BN;
+  bwd_dkdv_tc64_kernel<<<nkb * B * H, kThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_bwd_bias(p.part, B * p.nqt, H, D, du, dvb, stream);
+}
+
+}  // namespace txl

@@ -73,6 +73,24 @@ cudaError_t launch_relattn_bwd_simt(const void* q, const void* k, const void* v,
                                     float* dvb, int B, int W, int M, int H, int D, int n_r, float scale, bool bf16,
                                     bool go_bf16, bool vec16, void* scratch, cudaStream_t stream);
 
+// du, dv_bias of each head from per-tile partial sums part [n_part][H][2][D]
+// (d(q+u) columns, then d(q+v)), summed in order.
+cudaError_t launch_bwd_bias(const float* part, int n_part, int H, int D, float* du, float* dvb,
+                            cudaStream_t stream);
+
+// Backward on the tensor cores, bf16 inputs, o and dout, D = 64.  Tensor
+// maps as the forward's (q and dout over {D, H, W, B} with a {64, 1, 128, 1}
+// box, k and v {64, 1, 64, 1}); tm_rw: r over {D, H, n_r} with a
+// {64, 1, 192} box.  dr is zeroed here, then receives atomic sums.
+// scratch: relattn_bwd_tc64_scratch_bytes(B, W, H) bytes.
+size_t relattn_bwd_tc64_scratch_bytes(int B, int W, int H);
+cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
+                                    const CUtensorMap& tm_rw, const CUtensorMap& tm_do, const float* bias_u,
+                                    const float* bias_v, const float* lse, const void* o, const void* dout,
+                                    float* dq, float* dk, float* dv, float* dr, float* du, float* dvb, int B,
+                                    int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
+                                    cudaStream_t stream);
+
 // Number of chunks the D = 64 kernel should split each unit's key steps
 // into (1: no split), from the shape and the device's SM count.
 int relattn_tc64_split(int B, int H, int W, int M);
