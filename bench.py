@@ -336,6 +336,88 @@ def gpu_uuid(device_index):
         return None
 
 
+def backward_flops(B, H, D, W, M):
+    """Counted work of the backward: the gradient contractions over visible
+    pairs, two flops per multiply-add -- dP = dout V^T, d(q+u) = G K,
+    d(q+v) = G r and dr = G^T (q+v) over every visible pair; dK = G^T (q+u)
+    and dV = P^T dout over the segment's own keys only (the memory is under
+    the stop-gradient).  The scores rebuilt from q, k, r are not counted."""
+    p_all = W * M + W * (W + 1) // 2
+    p_seg = W * (W + 1) // 2
+    return 2 * B * H * D * (4 * p_all + 2 * p_seg)
+
+
+def measure_backward(stream, wl, steps, warmup, peak, peak_src):
+    """txl_relattn_backward on segment buffer 0 of the workload (its forward
+    output and lse, a seeded output gradient), each call timed with CUDA
+    events on its stream, L2 flushed between calls (outside the events)."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import make_dout
+
+    dev_ = stream.q[0].device
+    q, k, v = stream.q[0], stream.k[0], stream.v[0]
+    o = torch.empty(q.shape, device=dev_, dtype=torch.bfloat16)
+    lse = torch.empty(wl.B, wl.H, wl.W, device=dev_, dtype=torch.float32)
+    txl.txl_relattn_forward(q, k, v, stream.r, stream.u, stream.vb, o, lse, M=wl.M)
+    dout = torch.from_numpy(make_dout(wl)).to(dev_).to(torch.bfloat16)
+    grads = txl.txl_relattn_backward(q, k, v, stream.r, stream.u, stream.vb, o, lse, dout, M=wl.M)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev_)
+    cs = torch.cuda.current_stream()
+    ts = []
+    for it in range(warmup + steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cs)
+        txl.txl_relattn_backward(q, k, v, stream.r, stream.u, stream.vb, o, lse, dout, M=wl.M, grads=grads)
+        b.record(cs)
+        if it >= warmup:
+            ts.append((a, b))
+    torch.cuda.synchronize()
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait in the backward")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    flops = backward_flops(wl.B, wl.H, wl.D, wl.W, wl.M)
+    achieved = flops / (ms / 1e3) / 1e12
+    return {"call": "txl_relattn_backward (dq kernel, dk/dv kernel, bias sums)",
+            "value": wl.B * wl.W / (ms / 1e3), "unit": "tokens/s", "ms": ms, "calls": len(ts),
+            "gpu_launches_per_call": 3, "l2": "flushed between calls (256 MB write, outside the events)",
+            "roofline": {"kernel": "bwd_dq_tc64_kernel + bwd_dkdv_tc64_kernel", "bound": "tensor",
+                         "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)", "traffic": None,
+                         "per_launch_work": f"{flops} counted flops = 2*B*H*D*(4*(W*M + W(W+1)/2) + 2*W(W+1)/2)"}}
+
+
+def cpu_baseline_backward(wl, stream, batch=4, budget_s=10.0):
+    """The float64 oracle's backward (as it stands) on `batch` sequences of
+    segment buffer 0, all heads."""
+    from oracle import txl_oracle as O
+    from synthetic import make_dout
+
+    seg = stream.seg
+    L = wl.M + wl.W
+    q = seg.q[:batch, wl.M:L]
+    k = seg.k[:batch, :L]
+    v = seg.v[:batch, :L]
+    r = stream.r.float().cpu().numpy()
+    dout = make_dout(wl)[:batch]
+    reps = 0
+    c0 = time.process_time()
+    t0 = time.perf_counter()
+    while True:
+        O.relattn_backward(q, k, v, r, seg.bias_u, seg.bias_v, wl.M, dout)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s or reps >= 3:
+            break
+    cpu = time.process_time() - c0
+    return {"value": batch * wl.W * reps / el, "unit": "tokens/s", "cores": max(1, round(cpu / el)),
+            "kind": "oracle",
+            "sample": f"{reps} backward call(s) on {batch} of the {wl.B} sequences, all {wl.H} heads, "
+                      f"float64 numpy, {el:.1f} s wall"}
+
+
 def cpu_baseline_oracle(wl, stream, max_reps=3, budget_s=12.0):
     """Times the float64 oracle (as it stands) on one full steady-state segment
     of the same workload: memory roll of k and v plus the attention."""
@@ -459,8 +541,10 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": sampler.summary(h0, h1),
     }
+    result["backward"] = measure_backward(stream, wl, max(5, min(K, 50)), 3, peak, peak_src)
     if world == 1:
         result["cpu_baseline"] = cpu_baseline_oracle(wl, stream)
+        result["backward"]["cpu_baseline"] = cpu_baseline_backward(wl, stream)
     return result
 
 

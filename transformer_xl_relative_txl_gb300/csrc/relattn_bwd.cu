@@ -359,17 +359,21 @@ __global__ void __launch_bounds__(kThreads) bwd_dr_kernel(BwdArgs a) {
   }
 }
 
-// du, dv_bias of head h: the dq kernel's partials summed in order.
+// du, dv_bias of head h from the partials: one warp per column, lanes over
+// the partials in a fixed order, then a fixed shuffle tree.
 __global__ void bwd_bias_kernel(const float* __restrict__ part, int n_part, int H, int D, float* __restrict__ du,
                                 float* __restrict__ dvb) {
-  const int h = blockIdx.x;
-  for (int x = threadIdx.x; x < 2 * D; x += blockDim.x) {
+  const int h = blockIdx.x, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int x = threadIdx.x >> 5; x < 2 * D; x += nw) {
     float s = 0.f;
-    for (int p = 0; p < n_part; ++p) s += part[(static_cast<long long>(p) * H + h) * 2 * D + x];
-    if (x < D)
-      du[h * D + x] = s;
-    else
-      dvb[h * D + x - D] = s;
+    for (int q = lane; q < n_part; q += 32) s += part[(static_cast<long long>(q) * H + h) * 2 * D + x];
+    s = warp_sum(s);
+    if (lane == 0) {
+      if (x < D)
+        du[h * D + x] = s;
+      else
+        dvb[h * D + x - D] = s;
+    }
   }
 }
 

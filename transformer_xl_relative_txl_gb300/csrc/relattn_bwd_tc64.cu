@@ -140,6 +140,34 @@ __device__ __forceinline__ void build_qu_qv(const uint8_t* sQ, uint8_t* sQu, uin
   }
 }
 
+// Chunks [4 half, 4 half + 4) (head dims 32 half .. 32 half + 31) of row a
+// of (q+u) and (q+v).
+__device__ __forceinline__ void build_qu_qv_half(const uint8_t* sQ, uint8_t* sQu, uint8_t* sQv, int a, int half,
+                                                 const float* __restrict__ bu, const float* __restrict__ bv) {
+#pragma unroll
+  for (int cc = 0; cc < 4; ++cc) {
+    const int c = 4 * half + cc;
+    const uint32_t off = (a >> 3) * 1024 + (a & 7) * 128 + ((c ^ (a & 7)) << 4);
+    const uint4 raw = *reinterpret_cast<const uint4*>(sQ + off);
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    const float4 u0 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c));
+    const float4 u1 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c + 4));
+    const float4 v0 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c));
+    const float4 v1 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c + 4));
+    const float ub[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
+    const float vb[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    uint32_t qu[4], qv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+      qu[e] = pack_bf16x2(x0 + ub[2 * e], x1 + ub[2 * e + 1]);
+      qv[e] = pack_bf16x2(x0 + vb[2 * e], x1 + vb[2 * e + 1]);
+    }
+    *reinterpret_cast<uint4*>(sQu + off) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
+    *reinterpret_cast<uint4*>(sQv + off) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+  }
+}
+
 // Delta_i = dout_i . o_i over the 64 bf16 of each row.
 __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bfloat16* g) {
   float s0 = 0.f, s1 = 0.f;
@@ -218,9 +246,60 @@ __device__ __forceinline__ void store_row(uint8_t* tile, int a, const float (&x)
 }
 
 // ============================================================================
-// dq kernel
+// dq kernel: 8 warps, two per TMEM lane quadrant (key columns 0-31 and
+// 32-63 of the same rows).  Per step t, after the gradients of step t are in
+// shared memory, thread 0 issues the step's d(q+u) / slot MMAs and right
+// behind them the score MMAs of step t+1; the dr rows of the finished slot
+// are flushed while those run.
 // ============================================================================
-__global__ void __launch_bounds__(kThreads, 1)
+constexpr int kQThreads = 256;
+constexpr uint32_t kColDr = 448;  // the finished slot's dr rows (M = 64 layout)
+
+template <typename Vis>
+__device__ __forceinline__ void step_grads_half(uint32_t tmem, int quad, int half, int lane, float lse2,
+                                                float delta, float scale, float scale_log2e, Vis visible,
+                                                float (&g)[32], float (&p)[32]) {
+  const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  uint32_t bd[16], sx[32], dpv[32];
+  {
+    uint32_t xlo[32], xhi[32];
+    // key columns 0-31 use window positions [32 quad + 32, 32 quad + 96),
+    // columns 32-63 [32 quad, 32 quad + 64)
+    const uint32_t w0 = kColWin + 32 * quad + (half ? 0 : 32);
+    tmem_ld32(lb + w0, xlo);
+    tmem_ld32(lb + w0 + 32, xhi);
+    tmem_ld32(lb + kColS + 32 * half, sx);
+    tmem_ld32(lb + kColDP + 32 * half, dpv);
+    tmem_wait_ld(xlo);
+    tmem_wait_ld(xhi);
+    tmem_wait_ld(sx);
+    tmem_wait_ld(dpv);
+    uint32_t plo[16], phi[16];
+    pack32(xlo, plo);
+    pack32(xhi, phi);
+    window_shift_packed(plo, phi, lane, bd);
+  }
+  add_window(sx, bd, p);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float e = visible(32 * half + c) ? ex2(fmaf(p[c], scale_log2e, -lse2)) : 0.f;
+    p[c] = e;
+    g[c] = scale * e * (__uint_as_float(dpv[c]) - delta);
+  }
+}
+
+// Columns [32 half, 32 half + 32) of row a of a 128B-swizzled [128 x 64] bf16 tile.
+__device__ __forceinline__ void store_row_half(uint8_t* tile, int a, int half, const float (&x)[32]) {
+  uint8_t* row = tile + (a >> 3) * 1024 + (a & 7) * 128;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const uint32_t w0 = pack_bf16x2(x[8 * c], x[8 * c + 1]), w1 = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
+    const uint32_t w2 = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), w3 = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
+    *reinterpret_cast<uint4*>(row + (((4 * half + c) ^ (a & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
+  }
+}
+
+__global__ void __launch_bounds__(kQThreads, 1)
     bwd_dq_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
                        const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
@@ -237,12 +316,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sGs = smem + kQOffGs;
   QBars* bars = reinterpret_cast<QBars*>(smem + kQOffBar);
   volatile int* abort = &bars->abort;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp, a = tid;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int a = quad * 32 + lane;  // this thread's row of the tile
   const uint64_t wait_ns = p.wait_ns;
 
   const Unit w = decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt);
   const int T = w.nks;
-  const int i = w.i0 + a;  // this thread's query row
+  const int i = w.i0 + a;  // query row
   const int L = p.M + p.W;
 
   if (tid == 0) {
@@ -263,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   // Distance slots start at zero: a slot entry no step writes is a pair
   // that does not exist.
-  for (int x = tid; x < 4 * kTile / 16; x += kThreads)
+  for (int x = tid; x < 4 * kTile / 16; x += kQThreads)
     reinterpret_cast<uint4*>(sGs)[x] = make_uint4(0u, 0u, 0u, 0u);
   tc_fence_before();
   __syncthreads();
@@ -292,20 +373,21 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_4d(sG, &tm_q, &bars->q, 0, w.h, w.i0, w.b);  // raw q, into the G tile for now
     tma_load_4d(sDO, &tm_do, &bars->q, 0, w.h, w.i0, w.b);
     issue_step_loads(0);
+    if (T > 1) issue_step_loads(1);
   }
 
-  // Per-row constants: lse (log2 domain), Delta, u and v of the head.
+  // Per-row constants: lse (log2 domain) and Delta.
   const long long row_id = (static_cast<long long>(w.b) * p.H + w.h) * p.W + i;
   float lse2 = INFINITY, delta = 0.f;  // rows past W: every p is 0
   if (i < p.W) {
     lse2 = p.lse[row_id] * kLog2e;
     const long long off = ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D;
     delta = row_delta(p.o + off, p.dout + off);
-    p.delta[row_id] = delta;
+    if (half == 0) p.delta[row_id] = delta;
   }
   bool ok = mbar_wait(&bars->q, 0, wait_ns, abort);
-  if (ok) build_qu_qv(sG, sQu, sQv, a, p.bias_u + w.h * D, p.bias_v + w.h * D);
-  if (!ok) report_timeout(abort, p.status);
+  if (ok) build_qu_qv_half(sG, sQu, sQv, a, half, p.bias_u + w.h * D, p.bias_v + w.h * D);
+  else report_timeout(abort, p.status);
   fence_proxy_async_smem();
   ok = __syncthreads_and(ok) != 0;
 
@@ -318,11 +400,30 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
   const uint64_t dG = sdesc_sw128(smem_u32(sG), 16, 1024);
   const uint64_t dQvMN = sdesc_sw128(smem_u32(sQv), 8192, 1024);
-  uint32_t n_m2 = 0;  // MMA2 rounds (commits on m2)
-  int n_slot = 0;     // distance slots finished
+  uint32_t n_m2 = 0;  // commits on m2
+  int n_slot = 0;     // distance slots issued (thread 0)
 
-  // d(q+v) += Gs R and dr_slot = Gs^T (q+v) for distance slot tau, whose R
-  // rows are rows [64 r_row, 64 r_row + 64) of window stage rs.
+  // Thread 0: the score MMAs of step t (S, dP, distance window).
+  auto score_mmas = [&](int t) -> bool {
+    const int s = t & 1;
+    if (!mbar_wait(&bars->kv[s], (t >> 1) & 1, wait_ns, abort) ||
+        !mbar_wait(&bars->r[s], (t >> 1) & 1, wait_ns, abort))
+      return false;
+    tc_fence_after();
+    const uint64_t dK = sdesc_sw128(smem_u32(sK + s * kKTile), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(sV + s * kKTile), 16, 1024);
+    const uint64_t dR = sdesc_sw128(smem_u32(sR + s * kWinTile), 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColS, dQu + 2 * kk, dK + 2 * kk, id64, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColDP, dDO + 2 * kk, dV + 2 * kk, id64, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColWin, dQv + 2 * kk, dR + 2 * kk, id192, kk > 0);
+    tc_commit(&bars->m1);
+    return true;
+  };
+  // Thread 0: d(q+v) += Gs R and dr_slot = Gs^T (q+v) for distance slot tau,
+  // whose R rows are rows [64 r_row, 64 r_row + 64) of window stage rs.
   auto slot_mmas = [&](int tau, int rs, int r_row) {
     const int gi = (tau + 2) & 3;
     const uint64_t dGs = sdesc_sw128(smem_u32(sGs + gi * kTile), 16, 1024);
@@ -331,86 +432,56 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
     for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColB, dGs + 2 * kk, dRs + 128 * kk, idMN, n_slot > 0 || kk > 0);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColWin, dGsT + 128 * kk, dQvMN + 128 * kk, idT, kk > 0);
+    for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColDr, dGsT + 128 * kk, dQvMN + 128 * kk, idT, kk > 0);
     ++n_slot;
   };
-  // Adds the dr rows of the finished slot tau (now in TMEM at the window
-  // columns, M = 64 layout) to the output.
+  // Everyone: add the dr rows of slot tau (TMEM, M = 64 layout: row
+  // 16 quad + lane in lanes 0-15 of each quadrant) to the output; this warp
+  // takes head dims [32 half, 32 half + 32).
   auto flush_dr = [&](int tau) {
-    uint32_t v0[32], v1[32];
-    const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16) + kColWin;
-    tmem_ld32(lb, v0);
-    tmem_ld32(lb + 32, v1);
-    tmem_wait_ld(v0);
-    tmem_wait_ld(v1);
-    const int r = 16 * warp + lane;  // row of the slot
-    const int d = p.M + w.i0 - BN * tau - BN + r;
+    uint32_t v[32];
+    tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kColDr + 32 * half, v);
+    tmem_wait_ld(v);
+    const int d = p.M + w.i0 - BN * tau - BN + 16 * quad + lane;
     if (lane < 16 && d >= 0 && d < L) {
-      float4* dst = reinterpret_cast<float4*>(p.dr + (static_cast<long long>(d) * p.H + w.h) * D);
+      float4* dst = reinterpret_cast<float4*>(p.dr + (static_cast<long long>(d) * p.H + w.h) * D + 32 * half);
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        atomicAdd(dst + e, make_float4(__uint_as_float(v0[4 * e]), __uint_as_float(v0[4 * e + 1]),
-                                       __uint_as_float(v0[4 * e + 2]), __uint_as_float(v0[4 * e + 3])));
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        atomicAdd(dst + 8 + e, make_float4(__uint_as_float(v1[4 * e]), __uint_as_float(v1[4 * e + 1]),
-                                           __uint_as_float(v1[4 * e + 2]), __uint_as_float(v1[4 * e + 3])));
+        atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
+                                       __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
     }
   };
 
+  if (tid == 0 && ok && !score_mmas(0)) report_timeout(abort, p.status);
   for (int t = 0; t < T && ok; ++t) {
     const int s = t & 1;
-    // (A) thread 0: the step's score MMAs, then the next step's loads.
-    bool ok0 = true;
-    if (tid == 0) {
-      tc_fence_after();
-      ok0 = mbar_wait(&bars->kv[s], (t >> 1) & 1, wait_ns, abort) &&
-            mbar_wait(&bars->r[s], (t >> 1) & 1, wait_ns, abort);
-      if (ok0) {
-        const uint64_t dK = sdesc_sw128(smem_u32(sK + s * kKTile), 16, 1024);
-        const uint64_t dV = sdesc_sw128(smem_u32(sV + s * kKTile), 16, 1024);
-        const uint64_t dR = sdesc_sw128(smem_u32(sR + s * kWinTile), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColS, dQu + 2 * kk, dK + 2 * kk, id64, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColDP, dDO + 2 * kk, dV + 2 * kk, id64, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColWin, dQv + 2 * kk, dR + 2 * kk, id192, kk > 0);
-        tc_commit(&bars->m1);
-        if (t + 1 < T) issue_step_loads(t + 1);  // stage s^1 was last read by step t-1's MMAs, all done
-      } else {
-        report_timeout(abort, p.status);
-      }
-    }
-    // (B) everyone: the step's gradients.
-    ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort) && ok0;
+    // (1) everyone: the step's gradients into G (key order) and the slots.
+    ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
     tc_fence_after();
     {
-      float g[64], pr[64];
+      float g[32], pr[32];
       const int lim = p.M + i - BN * t;  // key column c visible iff c <= lim
-      step_grads(tmem, quad, lane, lse2, delta, p.scale, p.scale_log2e, [&](int c) { return c <= lim; }, g,
-                 pr);
-      store_row(sG, a, g);
+      step_grads_half(tmem, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
+                      [&](int c) { return c <= lim; }, g, pr);
+      store_row_half(sG, a, half, g);
       // Skewed copy: key column c of step t sits at window position
       // z = 64 + a - c, i.e. in distance slot t - z / 64, column z % 64.
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const int z = 64 + a - c;
+      for (int c = 0; c < 32; ++c) {
+        const int z = 64 + a - (32 * half + c);
         const int gi = (t - (z >> 6) + 2) & 3;
         *reinterpret_cast<__nv_bfloat16*>(sGs + gi * kTile + swz(a, z & 63)) = __float2bfloat16_rn(g[c]);
       }
-      // The slot that step t+1 opens held slot t-3, whose MMAs ran at step t-1.
-      uint4* nxt = reinterpret_cast<uint4*>(sGs + ((t + 3) & 3) * kTile);
-      for (int x = tid; x < kTile / 16; x += kThreads) nxt[x] = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // (C) thread 0: d(q+u) += G K, and the slot that step t finished (t-2).
+    // (2) thread 0: d(q+u) += G K and the slot step t finished (t-2); then
+    // the next step's score MMAs.
     if (tid == 0) {
       tc_fence_after();
       const uint64_t dKmn = sdesc_sw128(smem_u32(sK + s * kKTile), 8192, 1024);
@@ -418,7 +489,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColA, dG + 2 * kk, dKmn + 128 * kk, idMN, t > 0 || kk > 0);
       slot_mmas(t - 2, s, 2);
       tc_commit(&bars->m2);
+      if (t + 1 < T && !score_mmas(t + 1)) report_timeout(abort, p.status);
     }
+    // (3) everyone: flush the slot's dr rows; the slot's buffer is free again
+    // and becomes slot t+2; thread 0 refills this step's load stage.
     ok = mbar_wait(&bars->m2, n_m2 & 1, wait_ns, abort);
     ++n_m2;
     if (!__syncthreads_and(ok)) {
@@ -427,12 +501,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     tc_fence_after();
     flush_dr(t - 2);
+    {
+      uint4* nxt = reinterpret_cast<uint4*>(sGs + (t & 3) * kTile);
+      for (int x = tid; x < kTile / 16; x += kQThreads) nxt[x] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (tid == 0 && t + 2 < T) issue_step_loads(t + 2);  // stage s: step t's MMAs are done
     tc_fence_before();
-    __syncthreads();
   }
   // The last two slots are finished once the last step has written them.
   for (int k = 0; k < 2 && ok; ++k) {
     const int tau = T - 2 + k;
+    __syncthreads();
     if (tid == 0) {
       tc_fence_after();
       slot_mmas(tau, (T - 1) & 1, T - 1 - tau);
@@ -447,51 +526,43 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     flush_dr(tau);
     tc_fence_before();
-    __syncthreads();
   }
 
   if (ok) {
-    // dq = d(q+u) + d(q+v) for this row; the tile's column sums of both go
-    // to the bias partials (through shared memory, XOR-staggered columns).
-    uint32_t u0[32], u1[32], v0[32], v1[32];
-    const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    tmem_ld32(lb + kColA, u0);
-    tmem_ld32(lb + kColA + 32, u1);
-    tmem_ld32(lb + kColB, v0);
-    tmem_ld32(lb + kColB + 32, v1);
-    tmem_wait_ld(u0);
-    tmem_wait_ld(u1);
-    tmem_wait_ld(v0);
-    tmem_wait_ld(v1);
+    // dq = d(q+u) + d(q+v) for this row's 32 head dims; the tile's column
+    // sums of both go to the bias partials through shared memory
+    // (XOR-staggered columns).
+    __syncthreads();  // the slot buffers are free for the column sums
+    uint32_t u[32], v[32];
+    const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    tmem_ld32(lb + kColA + 32 * half, u);
+    tmem_ld32(lb + kColB + 32 * half, v);
+    tmem_wait_ld(u);
+    tmem_wait_ld(v);
     if (i < p.W) {
-      float4* dst = reinterpret_cast<float4*>(p.dq + ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D);
+      float4* dst = reinterpret_cast<float4*>(p.dq + ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D +
+                                              32 * half);
 #pragma unroll
       for (int e = 0; e < 8; ++e)
-        dst[e] = make_float4(__uint_as_float(u0[4 * e]) + __uint_as_float(v0[4 * e]),
-                             __uint_as_float(u0[4 * e + 1]) + __uint_as_float(v0[4 * e + 1]),
-                             __uint_as_float(u0[4 * e + 2]) + __uint_as_float(v0[4 * e + 2]),
-                             __uint_as_float(u0[4 * e + 3]) + __uint_as_float(v0[4 * e + 3]));
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        dst[8 + e] = make_float4(__uint_as_float(u1[4 * e]) + __uint_as_float(v1[4 * e]),
-                                 __uint_as_float(u1[4 * e + 1]) + __uint_as_float(v1[4 * e + 1]),
-                                 __uint_as_float(u1[4 * e + 2]) + __uint_as_float(v1[4 * e + 2]),
-                                 __uint_as_float(u1[4 * e + 3]) + __uint_as_float(v1[4 * e + 3]));
+        dst[e] = make_float4(__uint_as_float(u[4 * e]) + __uint_as_float(v[4 * e]),
+                             __uint_as_float(u[4 * e + 1]) + __uint_as_float(v[4 * e + 1]),
+                             __uint_as_float(u[4 * e + 2]) + __uint_as_float(v[4 * e + 2]),
+                             __uint_as_float(u[4 * e + 3]) + __uint_as_float(v[4 * e + 3]));
     }
     // red[x][row ^ (x & 31)]: column x of the row sums (x < 64: d(q+u)).
     float* red = reinterpret_cast<float*>(sGs);
 #pragma unroll
     for (int x = 0; x < 32; ++x) {
-      red[x * BM + (a ^ x)] = __uint_as_float(u0[x]);
-      red[(32 + x) * BM + (a ^ x)] = __uint_as_float(u1[x]);
-      red[(64 + x) * BM + (a ^ x)] = __uint_as_float(v0[x]);
-      red[(96 + x) * BM + (a ^ x)] = __uint_as_float(v1[x]);
+      red[(32 * half + x) * BM + (a ^ x)] = __uint_as_float(u[x]);
+      red[(64 + 32 * half + x) * BM + (a ^ x)] = __uint_as_float(v[x]);
     }
     __syncthreads();
-    float sum = 0.f;
-    for (int r = 0; r < BM; ++r) sum += red[tid * BM + (r ^ (tid & 31))];
-    const int qt = w.i0 / BM;
-    p.part[((static_cast<long long>(w.b) * p.nqt + qt) * p.H + w.h) * 2 * D + tid] = sum;
+    if (tid < 2 * D) {
+      float sum = 0.f;
+      for (int r = 0; r < BM; ++r) sum += red[tid * BM + (r ^ (tid & 31))];
+      const int qt = w.i0 / BM;
+      p.part[((static_cast<long long>(w.b) * p.nqt + qt) * p.H + w.h) * 2 * D + tid] = sum;
+    }
   }
   // Let this CTA's own copies and MMAs finish before the memory is released.
   if (tid == 0) {
@@ -753,7 +824,7 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   if ((e = cudaMemsetAsync(dr, 0, sizeof(float) * static_cast<size_t>(n_r) * H * D, stream)) != cudaSuccess)
     return e;
   const int units = p.nqt * B * H;
-  bwd_dq_tc64_kernel<<<units, kThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
+  bwd_dq_tc64_kernel<<<units, kQThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nkb = (W + BN - 1) / BN;
   bwd_dkdv_tc64_kernel<<<nkb * B * H, kThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
