@@ -40,7 +40,6 @@
 namespace txl {
 namespace {
 
-constexpr int kThreads = 128;
 constexpr int D = 64;
 constexpr int BM = 128;     // query rows per tile
 constexpr int BN = 64;      // keys per step / block
@@ -67,9 +66,9 @@ static_assert(kQSmem <= 232448, "shared memory budget");
 // dk/dv kernel shared memory
 constexpr int kKOffK = 0;
 constexpr int kKOffV = kKOffK + kKTile;
-constexpr int kKOffQu = kKOffV + kKTile;
-constexpr int kKOffQv = kKOffQu + kTile;
-constexpr int kKOffQ = kKOffQv + kTile;          // raw q, 2 stages
+constexpr int kKOffQu = kKOffV + kKTile;         // 2 buffers
+constexpr int kKOffQv = kKOffQu + 2 * kTile;     // 2 buffers
+constexpr int kKOffQ = kKOffQv + 2 * kTile;      // raw q, 2 stages
 constexpr int kKOffDO = kKOffQ + 2 * kTile;      // 2 stages
 constexpr int kKOffR = kKOffDO + 2 * kTile;      // 2 stages
 constexpr int kKOffP = kKOffR + 2 * kWinTile;
@@ -97,7 +96,7 @@ struct BwdParams {
 };
 
 struct QBars {
-  uint64_t q, kv[2], r[2], m1, m2, fin;
+  uint64_t q, kv[2], r[2], m1, m2, fin, fin2;
   uint32_t tmem_base;
   int abort;
 };
@@ -111,33 +110,6 @@ struct KBars {
 __device__ __forceinline__ uint32_t swz(int row, int col) {
   return static_cast<uint32_t>((row >> 3) * 1024 + (row & 7) * 128 + ((((col >> 3) ^ (row & 7))) << 4) +
                                ((col & 7) << 1));
-}
-
-// Row a of (q+u) and (q+v) from the raw q row (all three 128B-swizzled
-// tiles); bu, bv: the head's u and v in global memory.
-__device__ __forceinline__ void build_qu_qv(const uint8_t* sQ, uint8_t* sQu, uint8_t* sQv, int a,
-                                            const float* __restrict__ bu, const float* __restrict__ bv) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t off = (a >> 3) * 1024 + (a & 7) * 128 + ((c ^ (a & 7)) << 4);
-    const uint4 raw = *reinterpret_cast<const uint4*>(sQ + off);
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    const float4 u0 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c));
-    const float4 u1 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c + 4));
-    const float4 v0 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c));
-    const float4 v1 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c + 4));
-    const float ub[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
-    const float vb[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    uint32_t qu[4], qv[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
-      qu[e] = pack_bf16x2(x0 + ub[2 * e], x1 + ub[2 * e + 1]);
-      qv[e] = pack_bf16x2(x0 + vb[2 * e], x1 + vb[2 * e + 1]);
-    }
-    *reinterpret_cast<uint4*>(sQu + off) = make_uint4(qu[0], qu[1], qu[2], qu[3]);
-    *reinterpret_cast<uint4*>(sQv + off) = make_uint4(qv[0], qv[1], qv[2], qv[3]);
-  }
 }
 
 // Chunks [4 half, 4 half + 4) (head dims 32 half .. 32 half + 31) of row a
@@ -168,6 +140,13 @@ __device__ __forceinline__ void build_qu_qv_half(const uint8_t* sQ, uint8_t* sQu
   }
 }
 
+// dst[0..3] += (x0..x3) (fp32 bit patterns), one vector reduction in L2 with
+// no value returned.
+__device__ __forceinline__ void red_add_v4(float* dst, uint32_t x0, uint32_t x1, uint32_t x2, uint32_t x3) {
+  asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "r"(x0), "r"(x1), "r"(x2), "r"(x3)
+               : "memory");
+}
+
 // Delta_i = dout_i . o_i over the 64 bf16 of each row.
 __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bfloat16* g) {
   float s0 = 0.f, s1 = 0.f;
@@ -185,66 +164,6 @@ __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bf
   return s0 + s1;
 }
 
-// The step's probabilities p and gradients g for this thread's row, from
-// S, dP and the distance window in TMEM.  quad: the warp's lane quadrant;
-// lane: the row within it; visible(c): key column c is visible to the row.
-// Returns the row's p and g for the step's 64 key columns.
-template <typename Vis>
-__device__ __forceinline__ void step_grads(uint32_t tmem, int quad, int lane, float lse2, float delta,
-                                           float scale, float scale_log2e, Vis visible, float (&g)[64],
-                                           float (&p)[64]) {
-  const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-  uint32_t bd0[16], bd1[16];
-  uint32_t s0[32], s1[32];
-  {
-    uint32_t xa[32], xb[32], xc[32];
-    tmem_ld32(lb + kColWin + 32 * quad, xa);
-    tmem_ld32(lb + kColWin + 32 * quad + 32, xb);
-    tmem_ld32(lb + kColWin + 32 * quad + 64, xc);
-    tmem_ld32(lb + kColS, s0);
-    tmem_ld32(lb + kColS + 32, s1);
-    tmem_wait_ld(xa);
-    tmem_wait_ld(xb);
-    tmem_wait_ld(xc);
-    tmem_wait_ld(s0);
-    tmem_wait_ld(s1);
-    uint32_t pa[16], pb[16], pc[16];
-    pack32(xa, pa);
-    pack32(xb, pb);
-    pack32(xc, pc);
-    // columns 0-31 use window positions [32, 96) of the warp's 96, columns 32-63 [0, 64)
-    window_shift_packed(pb, pc, lane, bd0);
-    window_shift_packed(pa, pb, lane, bd1);
-  }
-  add_window(s0, bd0, p);
-  add_window(s1, bd1, p + 32);
-  {
-    uint32_t d0[32], d1[32];
-    tmem_ld32(lb + kColDP, d0);
-    tmem_ld32(lb + kColDP + 32, d1);
-    tmem_wait_ld(d0);
-    tmem_wait_ld(d1);
-#pragma unroll
-    for (int c = 0; c < 64; ++c) {
-      const float e = visible(c) ? ex2(fmaf(p[c], scale_log2e, -lse2)) : 0.f;
-      const float dp = __uint_as_float(c < 32 ? d0[c] : d1[c - 32]);
-      p[c] = e;
-      g[c] = scale * e * (dp - delta);
-    }
-  }
-}
-
-// Row a of a 128B-swizzled [128 x 64] bf16 tile from 64 floats.
-__device__ __forceinline__ void store_row(uint8_t* tile, int a, const float (&x)[64]) {
-  uint8_t* row = tile + (a >> 3) * 1024 + (a & 7) * 128;
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t w0 = pack_bf16x2(x[8 * c], x[8 * c + 1]), w1 = pack_bf16x2(x[8 * c + 2], x[8 * c + 3]);
-    const uint32_t w2 = pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), w3 = pack_bf16x2(x[8 * c + 6], x[8 * c + 7]);
-    *reinterpret_cast<uint4*>(row + ((c ^ (a & 7)) << 4)) = make_uint4(w0, w1, w2, w3);
-  }
-}
-
 // ============================================================================
 // dq kernel: 8 warps, two per TMEM lane quadrant (key columns 0-31 and
 // 32-63 of the same rows).  Per step t, after the gradients of step t are in
@@ -253,6 +172,7 @@ __device__ __forceinline__ void store_row(uint8_t* tile, int a, const float (&x)
 // are flushed while those run.
 // ============================================================================
 constexpr int kQThreads = 256;
+constexpr int kIssuer2 = 128;  // lane 0 of warp 4: the dq kernel's gradient / slot MMAs
 constexpr uint32_t kColDr = 448;  // the finished slot's dr rows (M = 64 layout)
 
 template <typename Vis>
@@ -335,6 +255,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(&bars->m1, 1);
     mbar_init(&bars->m2, 1);
     mbar_init(&bars->fin, 1);
+    mbar_init(&bars->fin2, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
@@ -401,7 +322,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint64_t dG = sdesc_sw128(smem_u32(sG), 16, 1024);
   const uint64_t dQvMN = sdesc_sw128(smem_u32(sQv), 8192, 1024);
   uint32_t n_m2 = 0;  // commits on m2
-  int n_slot = 0;     // distance slots issued (thread 0)
+  int n_slot = 0;     // distance slots issued (the slot issuer, kIssuer2)
 
   // Thread 0: the score MMAs of step t (S, dP, distance window).
   auto score_mmas = [&](int t) -> bool {
@@ -444,11 +365,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tmem_wait_ld(v);
     const int d = p.M + w.i0 - BN * tau - BN + 16 * quad + lane;
     if (lane < 16 && d >= 0 && d < L) {
-      float4* dst = reinterpret_cast<float4*>(p.dr + (static_cast<long long>(d) * p.H + w.h) * D + 32 * half);
+      float* dst = p.dr + (static_cast<long long>(d) * p.H + w.h) * D + 32 * half;
 #pragma unroll
-      for (int e = 0; e < 8; ++e)
-        atomicAdd(dst + e, make_float4(__uint_as_float(v[4 * e]), __uint_as_float(v[4 * e + 1]),
-                                       __uint_as_float(v[4 * e + 2]), __uint_as_float(v[4 * e + 3])));
+      for (int e = 0; e < 8; ++e) red_add_v4(dst + 4 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
     }
   };
 
@@ -480,16 +399,18 @@ __global__ void __launch_bounds__(kQThreads, 1)
     fence_proxy_async_smem();
     tc_fence_before();
     __syncthreads();
-    // (2) thread 0: d(q+u) += G K and the slot step t finished (t-2); then
-    // the next step's score MMAs.
+    // (2) the next step's score MMAs (thread 0) and, issued alongside from
+    // another warp, d(q+u) += G K and the slot step t finished (t-2).
     if (tid == 0) {
+      tc_fence_after();
+      if (t + 1 < T && !score_mmas(t + 1)) report_timeout(abort, p.status);
+    } else if (tid == kIssuer2) {
       tc_fence_after();
       const uint64_t dKmn = sdesc_sw128(smem_u32(sK + s * kKTile), 8192, 1024);
 #pragma unroll
       for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColA, dG + 2 * kk, dKmn + 128 * kk, idMN, t > 0 || kk > 0);
       slot_mmas(t - 2, s, 2);
       tc_commit(&bars->m2);
-      if (t + 1 < T && !score_mmas(t + 1)) report_timeout(abort, p.status);
     }
     // (3) everyone: flush the slot's dr rows; the slot's buffer is free again
     // and becomes slot t+2; thread 0 refills this step's load stage.
@@ -512,7 +433,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   for (int k = 0; k < 2 && ok; ++k) {
     const int tau = T - 2 + k;
     __syncthreads();
-    if (tid == 0) {
+    if (tid == kIssuer2) {
       tc_fence_after();
       slot_mmas(tau, (T - 1) & 1, T - 1 - tau);
       tc_commit(&bars->m2);
@@ -574,15 +495,21 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tc_commit(&bars->fin);
     mbar_wait_own(&bars->fin, 0, wait_ns);
   }
+  if (tid == kIssuer2) {
+    tc_commit(&bars->fin2);
+    mbar_wait_own(&bars->fin2, 0, wait_ns);
+  }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
 // ============================================================================
-// dk / dv kernel
+// dk / dv kernel: 8 warps as in the dq kernel.  (q+u), (q+v) of the next
+// query tile are built while the current tile's gradient MMAs run, and that
+// tile's score MMAs are issued right behind them.
 // ============================================================================
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kQThreads, 1)
     bwd_dkdv_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
                          const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
@@ -591,8 +518,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = smem_raw + pad;
   uint8_t* sK = smem + kKOffK;
   uint8_t* sV = smem + kKOffV;
-  uint8_t* sQu = smem + kKOffQu;
-  uint8_t* sQv = smem + kKOffQv;
+  uint8_t* sQu = smem + kKOffQu;  // 2 buffers
+  uint8_t* sQv = smem + kKOffQv;  // 2 buffers
   uint8_t* sQ = smem + kKOffQ;
   uint8_t* sDO = smem + kKOffDO;
   uint8_t* sR = smem + kKOffR;
@@ -600,7 +527,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sG = smem + kKOffG;
   KBars* bars = reinterpret_cast<KBars*>(smem + kKOffBar);
   volatile int* abort = &bars->abort;
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quad = warp, a = tid;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int a = quad * 32 + lane;
   const uint64_t wait_ns = p.wait_ns;
 
   // Block of 64 segment keys jj0 .. jj0+63 (rows M+jj of k and v) of (b, h).
@@ -608,7 +537,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int bh = blockIdx.x / nkb;
   const int b = bh / p.H, h = bh % p.H;
   const int jj0 = (blockIdx.x % nkb) * BN;
-  const int qt0 = jj0 / BM;             // first query tile with a row i >= jj0
+  const int qt0 = jj0 / BM;  // first query tile with a row i >= jj0
   const int NT = p.nqt - qt0;
 
   if (tid == 0) {
@@ -649,121 +578,126 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_load_4d(sK, &tm_k, &bars->kv, 0, h, p.M + jj0, b);
     tma_load_4d(sV, &tm_v, &bars->kv, 0, h, p.M + jj0, b);
     issue_tile_loads(0);
+    if (NT > 1) issue_tile_loads(1);
   }
+  const float* bu = p.bias_u + h * D;
+  const float* bv = p.bias_v + h * D;
 
   constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
   constexpr uint32_t id192 = idesc_bf16(128, 192, false, false);
   constexpr uint32_t idT = idesc_bf16(64, 64, true, true);
-  const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
-  const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
   const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
   const uint64_t dV = sdesc_sw128(smem_u32(sV), 16, 1024);
   const uint64_t dPT = sdesc_sw128(smem_u32(sP), 8192, 1024);
   const uint64_t dGT = sdesc_sw128(smem_u32(sG), 8192, 1024);
-  const uint64_t dQuMN = sdesc_sw128(smem_u32(sQu), 8192, 1024);
 
-  bool ok = true;
+  // Thread 0: the score MMAs of tile s (its (q+u), (q+v) in buffer s & 1).
+  auto score_mmas = [&](int s) -> bool {
+    const int st = s & 1;
+    if (s == 0 && !mbar_wait(&bars->kv, 0, wait_ns, abort)) return false;
+    tc_fence_after();
+    const uint64_t dQu = sdesc_sw128(smem_u32(sQu + st * kTile), 16, 1024);
+    const uint64_t dQv = sdesc_sw128(smem_u32(sQv + st * kTile), 16, 1024);
+    const uint64_t dDO = sdesc_sw128(smem_u32(sDO + st * kTile), 16, 1024);
+    const uint64_t dR = sdesc_sw128(smem_u32(sR + st * kWinTile), 16, 1024);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColS, dQu + 2 * kk, dK + 2 * kk, id64, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColDP, dDO + 2 * kk, dV + 2 * kk, id64, kk > 0);
+#pragma unroll
+    for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColWin, dQv + 2 * kk, dR + 2 * kk, id192, kk > 0);
+    tc_commit(&bars->m1);
+    return true;
+  };
+  // Everyone: this warp's half of (q+u), (q+v) of tile s, from its raw q.
+  auto build = [&](int s) -> bool {
+    const int st = s & 1;
+    if (!mbar_wait(&bars->in[st], (s >> 1) & 1, wait_ns, abort)) return false;
+    build_qu_qv_half(sQ + st * kTile, sQu + st * kTile, sQv + st * kTile, a, half, bu, bv);
+    return true;
+  };
+
+  bool ok = build(0);
+  if (!ok) report_timeout(abort, p.status);
+  fence_proxy_async_smem();
+  ok = __syncthreads_and(ok) != 0;
+  if (tid == 0 && ok && !score_mmas(0)) report_timeout(abort, p.status);
+
   for (int s = 0; s < NT && ok; ++s) {
     const int st = s & 1;
     const int i = (qt0 + s) * BM + a;
-    // (A) everyone: this tile's rows of (q+u), (q+v); lse and Delta.
     float lse2 = INFINITY, delta = 0.f;
     if (i < p.W) {
       const long long row_id = (static_cast<long long>(b) * p.H + h) * p.W + i;
       lse2 = p.lse[row_id] * kLog2e;
       delta = p.delta[row_id];
     }
-    ok = mbar_wait(&bars->in[st], (s >> 1) & 1, wait_ns, abort);
-    if (ok) build_qu_qv(sQ + st * kTile, sQu, sQv, a, p.bias_u + h * D, p.bias_v + h * D);
-    fence_proxy_async_smem();
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    // (B) thread 0: the score MMAs, then the next tile's loads.
-    bool ok0 = true;
-    if (tid == 0) {
-      tc_fence_after();
-      ok0 = s > 0 || mbar_wait(&bars->kv, 0, wait_ns, abort);
-      if (ok0) {
-        const uint64_t dDO = sdesc_sw128(smem_u32(sDO + st * kTile), 16, 1024);
-        const uint64_t dR = sdesc_sw128(smem_u32(sR + st * kWinTile), 16, 1024);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColS, dQu + 2 * kk, dK + 2 * kk, id64, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColDP, dDO + 2 * kk, dV + 2 * kk, id64, kk > 0);
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColWin, dQv + 2 * kk, dR + 2 * kk, id192, kk > 0);
-        tc_commit(&bars->m1);
-        if (s + 1 < NT) issue_tile_loads(s + 1);  // stage st^1 was last read by tile s-1's MMAs, all done
-      } else {
-        report_timeout(abort, p.status);
-      }
-    }
-    ok = mbar_wait(&bars->m1, s & 1, wait_ns, abort) && ok0;
+    // (1) everyone: p and g of the tile's rows against the key block; then
+    // the next tile's (q+u), (q+v).
+    ok = mbar_wait(&bars->m1, s & 1, wait_ns, abort);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
     tc_fence_after();
-    // (C) everyone: p and g of the tile's rows against the key block.
     {
-      float g[64], pr[64];
+      float g[32], pr[32];
       // key jj0 + c is visible to row i iff jj0 + c <= i and it exists
       const int lim = min(i - jj0, p.W - 1 - jj0);
-      step_grads(tmem, quad, lane, lse2, delta, p.scale, p.scale_log2e, [&](int c) { return c <= lim; }, g,
-                 pr);
-      store_row(sP, a, pr);
-      store_row(sG, a, g);
+      step_grads_half(tmem, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
+                      [&](int c) { return c <= lim; }, g, pr);
+      store_row_half(sP, a, half, pr);
+      store_row_half(sG, a, half, g);
     }
+    if (s + 1 < NT && !build(s + 1)) ok = false;
     fence_proxy_async_smem();
     tc_fence_before();
-    __syncthreads();
-    // (D) thread 0: dV += P^T dout, dK += G^T (q+u)  (M = 64 keys, K = 128 queries).
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    // (2) thread 0: dV += P^T dout, dK += G^T (q+u)  (M = 64 keys, K = 128
+    // queries); then the next tile's score MMAs.
     if (tid == 0) {
       tc_fence_after();
       const uint64_t dDOmn = sdesc_sw128(smem_u32(sDO + st * kTile), 8192, 1024);
+      const uint64_t dQuMN = sdesc_sw128(smem_u32(sQu + st * kTile), 8192, 1024);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColA, dPT + 128 * kk, dDOmn + 128 * kk, idT, s > 0 || kk > 0);
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColB, dGT + 128 * kk, dQuMN + 128 * kk, idT, s > 0 || kk > 0);
       tc_commit(&bars->m2);
+      if (s + 1 < NT && !score_mmas(s + 1)) report_timeout(abort, p.status);
     }
+    // (3) everyone: the tile's MMAs are done; thread 0 refills its stage.
     ok = mbar_wait(&bars->m2, s & 1, wait_ns, abort);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
-    tc_fence_after();
+    if (tid == 0 && s + 2 < NT) issue_tile_loads(s + 2);
   }
 
   if (ok) {
-    // Rows of the M = 64 results: lanes 0-15 of each warp, row 16 warp + lane.
-    uint32_t v0[32], v1[32], k0[32], k1[32];
-    const uint32_t lb = tmem + (static_cast<uint32_t>(warp * 32) << 16);
-    tmem_ld32(lb + kColA, v0);
-    tmem_ld32(lb + kColA + 32, v1);
-    tmem_ld32(lb + kColB, k0);
-    tmem_ld32(lb + kColB + 32, k1);
-    tmem_wait_ld(v0);
-    tmem_wait_ld(v1);
-    tmem_wait_ld(k0);
-    tmem_wait_ld(k1);
-    const int jj = jj0 + 16 * warp + lane;
+    // Rows of the M = 64 results: lanes 0-15 of each quadrant, row 16 quad + lane.
+    tc_fence_after();
+    uint32_t vv[32], kv[32];
+    const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    tmem_ld32(lb + kColA + 32 * half, vv);
+    tmem_ld32(lb + kColB + 32 * half, kv);
+    tmem_wait_ld(vv);
+    tmem_wait_ld(kv);
+    const int jj = jj0 + 16 * quad + lane;
     if (lane < 16 && jj < p.W) {
-      const long long off = ((static_cast<long long>(b) * p.W + jj) * p.H + h) * D;
+      const long long off = ((static_cast<long long>(b) * p.W + jj) * p.H + h) * D + 32 * half;
       float4* dvp = reinterpret_cast<float4*>(p.dv + off);
       float4* dkp = reinterpret_cast<float4*>(p.dk + off);
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
-        dvp[e] = make_float4(__uint_as_float(v0[4 * e]), __uint_as_float(v0[4 * e + 1]),
-                             __uint_as_float(v0[4 * e + 2]), __uint_as_float(v0[4 * e + 3]));
-        dvp[8 + e] = make_float4(__uint_as_float(v1[4 * e]), __uint_as_float(v1[4 * e + 1]),
-                                 __uint_as_float(v1[4 * e + 2]), __uint_as_float(v1[4 * e + 3]));
-        dkp[e] = make_float4(__uint_as_float(k0[4 * e]), __uint_as_float(k0[4 * e + 1]),
-                             __uint_as_float(k0[4 * e + 2]), __uint_as_float(k0[4 * e + 3]));
-        dkp[8 + e] = make_float4(__uint_as_float(k1[4 * e]), __uint_as_float(k1[4 * e + 1]),
-                                 __uint_as_float(k1[4 * e + 2]), __uint_as_float(k1[4 * e + 3]));
+        dvp[e] = make_float4(__uint_as_float(vv[4 * e]), __uint_as_float(vv[4 * e + 1]),
+                             __uint_as_float(vv[4 * e + 2]), __uint_as_float(vv[4 * e + 3]));
+        dkp[e] = make_float4(__uint_as_float(kv[4 * e]), __uint_as_float(kv[4 * e + 1]),
+                             __uint_as_float(kv[4 * e + 2]), __uint_as_float(kv[4 * e + 3]));
       }
     }
   }
@@ -827,7 +761,7 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   bwd_dq_tc64_kernel<<<units, kQThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nkb = (W + BN - 1) / BN;
-  bwd_dkdv_tc64_kernel<<<nkb * B * H, kThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
+  bwd_dkdv_tc64_kernel<<<nkb * B * H, kQThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_bwd_bias(p.part, B * p.nqt, H, D, du, dvb, stream);
 }
