@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define TXL_VERSION 120 /* 1.2.0 */
+#define TXL_VERSION 130 /* 1.3.0 */
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -187,6 +187,58 @@ TXL_API int txl_relattn_forward_roll(const void* q, const void* k, const void* v
                              txl_dtype dtype, txl_dtype o_dtype,
                              void* k_mem_out, void* v_mem_out, int m, long long mem_out_bs, int* m_out,
                              cudaStream_t stream);
+
+/*
+ * txl_relattn_forward_ring -- txl_relattn_forward with the memory held in a
+ * ring buffer instead of in front of the segment's rows.
+ *
+ * The result is exactly that of txl_relattn_forward with
+ *   k = [memory rows in ring order ; k_seg],  v likewise,
+ * where memory row m (m = 0 .. M-1, oldest first) is row (start + m) % cap
+ * of k_mem / v_mem.  "Transformer-XL, explained", method step 7: with
+ * relative positions the memory can be much longer at evaluation time; a
+ * ring keeps it in place, so moving to the next segment writes only the
+ * segment's own rows (txl_mem_ring_append) instead of copying M rows.  The
+ * ring layout has no counterpart on the pages; it stores the same memory.
+ *
+ *   k_mem, v_mem  device, [B, cap, H, D] `dtype` (may be NULL when M = 0)
+ *   cap           ring rows per sequence (>= M)
+ *   start         ring row of memory row 0 (0 <= start < cap when M > 0)
+ *   M             memory rows in this call
+ *   k_seg, v_seg  device, [B, W, H, D] `dtype`  the segment's keys and values
+ * Other arguments and errors as txl_relattn_forward.
+ *
+ * On the bf16 D = 64 path with cap, start and M multiples of 64 the kernel
+ * reads the ring in place (a key tile never wraps); otherwise the call first
+ * copies [memory ; segment] into library scratch per (device, stream),
+ * allocated on first use.
+ */
+TXL_API int txl_relattn_forward_ring(const void* q, const void* k_mem, const void* v_mem, int cap, int start,
+                             int M, const void* k_seg, const void* v_seg, const void* r,
+                             const float* bias_u, const float* bias_v, void* o, float* lse,
+                             int B, int W, int H, int D, int n_r, float scale,
+                             txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream);
+
+/*
+ * txl_mem_ring_append -- the memory roll of a ring buffer.
+ *
+ * The ring holds m rows (memory row x at ring row (start + x) % cap).  After
+ * the call it holds the last min(cap, m + w) rows of [memory ; h], oldest
+ * first from ring row *start_out -- the rows txl_mem_update(mem, m, h, w,
+ * out, cap) would give, without moving the ones that stay ("Long-context
+ * transformers", segment recurrence: the next memory is the last M rows of
+ * [memory ; segment]).  Only the new rows are written: ring rows
+ * (start + m + x) % cap for x >= max(0, w - cap).
+ *
+ *   mem      device, [B, cap, C] `dtype`, batch stride cap*C elements
+ *   h        device, [B, w, C] rows with batch stride h_bs elements (>= w*C)
+ *   start_out, m_out  host, receive the new start and row count (may be NULL)
+ *
+ * Run it after the attention that reads the ring (stream order): it
+ * overwrites the oldest rows.  h must not overlap the ring (TXL_ERR_ALIAS).
+ */
+TXL_API int txl_mem_ring_append(void* mem, int cap, int start, int m, const void* h, int w, int B, int C,
+                        long long h_bs, int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream);
 
 /*
  * txl_relattn_backward -- gradients of txl_relattn_forward.

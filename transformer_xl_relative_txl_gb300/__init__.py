@@ -10,14 +10,15 @@ the library has not been built (``python transformer_xl_relative_txl_gb300/build
 from __future__ import annotations
 
 import ctypes
+import math
 import os
 
 import torch
 
 __all__ = [
     "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
-    "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_relattn_backward",
-    "txl_mem_update",
+    "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_relattn_forward_ring",
+    "txl_relattn_backward", "txl_mem_update", "txl_mem_ring_append",
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
@@ -44,6 +45,12 @@ lib.txl_relattn_forward_roll.argtypes = [_p, _p, _p, _p, _p, _p, _p, _p, _i, _i,
 lib.txl_relattn_forward_roll.restype = _i
 lib.txl_relattn_backward.argtypes = [_p] * 15 + [_i, _i, _i, _i, _i, _i, _f, _i, _i, _p]
 lib.txl_relattn_backward.restype = _i
+lib.txl_relattn_forward_ring.argtypes = [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _f,
+                                         _i, _i, _p]
+lib.txl_relattn_forward_ring.restype = _i
+lib.txl_mem_ring_append.argtypes = [_p, _i, _i, _i, _p, _i, _i, _i, _ll, ctypes.POINTER(_i), ctypes.POINTER(_i),
+                                    _i, _p]
+lib.txl_mem_ring_append.restype = _i
 lib.txl_mem_update.argtypes = [_p, _i, _p, _i, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i, _p]
 lib.txl_mem_update.restype = _i
 lib.txl_sinusoid_rel.argtypes = [_p, _i, _i, _i, _p]
@@ -152,6 +159,56 @@ def txl_relattn_backward(q, k, v, r, bias_u, bias_v, o, lse, dout, M=None, scale
                                   _stream(stream))
     _check(st, "txl_relattn_backward")
     return g
+
+
+def txl_relattn_forward_ring(q, k_mem, v_mem, start, M, k_seg, v_seg, r, bias_u, bias_v, o, lse=None, scale=None,
+                             stream=None):
+    """Relative attention of q [B,W,H,D] over [memory ; segment]: memory row
+    m (m < M) is row (start + m) % cap of the rings k_mem, v_mem [B,cap,H,D];
+    the segment's keys and values are k_seg, v_seg [B,W,H,D]."""
+    B, W, H, D = q.shape
+    for t in (q, k_seg, v_seg, r, bias_u, bias_v, o) + ((lse,) if lse is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k_mem.dim() != 4 or k_mem.shape[0] != B or k_mem.shape[2:] != (H, D) or v_mem.shape != k_mem.shape:
+        raise ValueError("k_mem, v_mem must be [B, cap, H, D]")
+    if not (k_mem.is_contiguous() and v_mem.is_contiguous()):
+        raise ValueError("rings must be contiguous")
+    if k_seg.shape != q.shape or v_seg.shape != q.shape or o.shape != q.shape:
+        raise ValueError("k_seg, v_seg, o must be [B, W, H, D]")
+    if r.dim() != 3 or r.shape[1:] != (H, D) or bias_u.shape != (H, D) or bias_v.shape != (H, D):
+        raise ValueError("r must be [n_r, H, D]; biases [H, D]")
+    if not (q.dtype == k_mem.dtype == v_mem.dtype == k_seg.dtype == v_seg.dtype == r.dtype):
+        raise ValueError("q, rings, segment rows and r must share a dtype")
+    if scale is None:
+        scale = D ** -0.5
+    st = lib.txl_relattn_forward_ring(_ptr(q), _ptr(k_mem), _ptr(v_mem), k_mem.shape[1], int(start), int(M),
+                                      _ptr(k_seg), _ptr(v_seg), _ptr(r), _ptr(bias_u), _ptr(bias_v), _ptr(o),
+                                      _ptr(lse), B, W, H, D, r.shape[0], float(scale), _dtype_code(q.dtype),
+                                      _dtype_code(o.dtype), _stream(stream))
+    _check(st, "txl_relattn_forward_ring")
+    return o
+
+
+def txl_mem_ring_append(mem, start, m, h, stream=None):
+    """Append the rows of h [B, w, ...] (row-contiguous, any batch stride) to
+    the ring mem [B, cap, ...] that holds m rows from ring row `start`;
+    returns the new (start, m)."""
+    B, cap = mem.shape[0], mem.shape[1]
+    C = math.prod(mem.shape[2:])
+    w = h.shape[1]
+    if not mem.is_contiguous():
+        raise ValueError("the ring must be contiguous")
+    if h.shape[0] != B or math.prod(h.shape[2:]) != C or (w > 0 and not h[0].is_contiguous()):
+        raise ValueError("h must be [B, w, ...] with rows of the ring's width")
+    if mem.dtype != h.dtype:
+        raise ValueError("mem and h must share a dtype")
+    s_out, m_out = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.txl_mem_ring_append(_ptr(mem), cap, int(start), int(m), _ptr(h) if w > 0 else None, w, B, C,
+                                 h.stride(0) if B > 1 else w * C, ctypes.byref(s_out), ctypes.byref(m_out),
+                                 _dtype_code(mem.dtype), _stream(stream))
+    _check(st, "txl_mem_ring_append")
+    return s_out.value, m_out.value
 
 
 def _forward(fn, name, q, k, v, r, bias_u, bias_v, o, lse, M, scale, stream):

@@ -10,6 +10,7 @@
 #include <cstdint>
 #include <cstring>
 #include <map>
+#include <vector>
 #include <mutex>
 #include <utility>
 
@@ -85,6 +86,28 @@ cudaError_t split_scratch(cudaStream_t stream, size_t bytes, size_t n_counters, 
   }
   *out = b.ptr;
   *counters = b.cnt;
+  return cudaSuccess;
+}
+
+// Contiguous copies of a ring's keys and values for the ring calls the
+// kernels cannot read in place, per (device, stream); grows on demand.
+std::map<std::pair<int, cudaStream_t>, std::pair<void*, size_t>> g_gather;
+
+cudaError_t gather_scratch(cudaStream_t stream, size_t bytes, void** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_mutex);
+  auto& b = g_gather[{dev, stream}];
+  if (b.second < bytes) {
+    if (b.first != nullptr) {
+      if ((e = cudaStreamSynchronize(stream)) != cudaSuccess || (e = cudaFree(b.first)) != cudaSuccess) return e;
+      b = {nullptr, 0};
+    }
+    if ((e = cudaMalloc(&b.first, bytes)) != cudaSuccess) return e;
+    b.second = bytes;
+  }
+  *out = b.first;
   return cudaSuccess;
 }
 
@@ -282,12 +305,34 @@ struct FusedRoll {
   long long keep, src0, out_bs;
 };
 
+// Keys and values of a ring-buffer call: k and v passed to forward_impl are
+// then the rings [B, cap, H, D]; the segment rows come from k_seg, v_seg.
+struct RingArgs {
+  const void* k_seg;
+  const void* v_seg;
+  int cap, start;
+};
+
 // The attention (validated arguments); `roll` non-null asks the D = 64
 // kernel to write the memory roll too (the caller has checked it can).
 int forward_impl(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                  const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
                  txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, bool static_scratch_only,
-                 cudaStream_t stream);
+                 cudaStream_t stream, const RingArgs* ring = nullptr);
+
+// Shapes and dtypes the forward kernels take (TXL_OK or TXL_ERR_UNSUPPORTED).
+int shape_support(int B, int W, int M, int H, int D, txl_dtype dtype, txl_dtype o_dtype) {
+  const long long L = static_cast<long long>(M) + W;
+  if (dtype == TXL_F32) {
+    if (o_dtype != TXL_F32 || D > 256 || B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
+    if (sizeof(float) * (2 * static_cast<size_t>(D) + L) > 220 * 1024) return TXL_ERR_UNSUPPORTED;
+  } else {
+    if (D != 64 && D != 128) return TXL_ERR_UNSUPPORTED;
+    const long long nqt = (W + 127) / 128;
+    if (nqt * B * H > 0x7FFFFFFFLL || L > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
+  }
+  return TXL_OK;
+}
 
 int check_forward(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                   const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
@@ -322,23 +367,16 @@ int check_forward(const void* q, const void* k, const void* v, const void* r, co
     for (Range x : {rq, rk, rv, rr, ru, rb, ro})
       if (overlap(rl, x)) return TXL_ERR_ALIAS;
   }
-  if (dtype == TXL_F32) {
-    if (o_dtype != TXL_F32 || D > 256 || B > 65535 || H > 65535) return TXL_ERR_UNSUPPORTED;
-    if (sizeof(float) * (2 * static_cast<size_t>(D) + L) > 220 * 1024) return TXL_ERR_UNSUPPORTED;
-  } else {
-    if (D != 64 && D != 128) return TXL_ERR_UNSUPPORTED;
-    const long long nqt = (W + 127) / 128;
-    if (nqt * B * H > 0x7FFFFFFFLL || L > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
-  }
-  return TXL_OK;
+  return shape_support(B, W, M, H, D, dtype, o_dtype);
 }
 
 int forward_impl(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                  const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
                  txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, bool static_scratch_only,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, const RingArgs* ring) {
   const long long L = static_cast<long long>(M) + W;
   const size_t hd = static_cast<size_t>(H) * D;
+  if (ring != nullptr && (dtype != TXL_BF16 || D != 64)) return TXL_ERR_UNSUPPORTED;
   if (dtype == TXL_F32) {
     return from_cuda(txl::launch_relattn_f32(
         static_cast<const float*>(q), static_cast<const float*>(k), static_cast<const float*>(v),
@@ -365,12 +403,28 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
     if (!encode_bf16(&tm_q, q, 4, dims, strides, box)) return TXL_ERR_CUDA;
   }
   {
+    // k, v rows: L per sequence, or the ring's cap
+    const long long rows = ring != nullptr ? ring->cap : L;
     const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
-                                static_cast<cuuint64_t>(L), static_cast<cuuint64_t>(B)};
-    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(L) * hd * 2};
+                                static_cast<cuuint64_t>(rows), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2,
+                                   static_cast<cuuint64_t>(rows) * hd * 2};
     const cuuint32_t box[4] = {64, 1, 64, 1};
     if (!encode_bf16(&tm_k, k, 4, dims, strides, box) || !encode_bf16(&tm_v, v, 4, dims, strides, box))
       return TXL_ERR_CUDA;
+  }
+  txl::RingMaps ring_maps;
+  if (ring != nullptr) {
+    if (D != 64 || roll != nullptr) return TXL_ERR_UNSUPPORTED;
+    const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                static_cast<cuuint64_t>(W), static_cast<cuuint64_t>(B)};
+    const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 2, hd * 2, static_cast<cuuint64_t>(W) * hd * 2};
+    const cuuint32_t box[4] = {64, 1, 64, 1};
+    if (!encode_bf16(&ring_maps.tm_ks, ring->k_seg, 4, dims, strides, box) ||
+        !encode_bf16(&ring_maps.tm_vs, ring->v_seg, 4, dims, strides, box))
+      return TXL_ERR_CUDA;
+    ring_maps.cap = ring->cap;
+    ring_maps.start = ring->start;
   }
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
@@ -433,7 +487,8 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
     }
     return from_cuda(txl::launch_relattn_tc64(tm_q, tm_k, tm_v, tm_r, o_tma ? &tm_o : nullptr,
                                               roll ? &tm_km : nullptr, roll ? &tm_vm : nullptr,
-                                              roll ? static_cast<int>(roll->src0) : -1, bias_u, bias_v, o, lse, B,
+                                              roll ? static_cast<int>(roll->src0) : -1,
+                                              ring != nullptr ? &ring_maps : nullptr, bias_u, bias_v, o, lse, B,
                                               W, M, H, o_dtype == TXL_BF16, scale, nsplit, part_o, part_lse,
                                               part_cnt, wc, stream));
   }
@@ -615,6 +670,115 @@ int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const 
   if (rc != TXL_OK) return rc;
   return txl_mem_update(vb, M, vb + static_cast<size_t>(M) * C * es, W, v_mem_out, m, B, static_cast<int>(C), bs,
                         bs, mem_out_bs, nullptr, dtype, stream);
+}
+
+int txl_relattn_forward_ring(const void* q, const void* k_mem, const void* v_mem, int cap, int start, int M,
+                             const void* k_seg, const void* v_seg, const void* r, const float* bias_u,
+                             const float* bias_v, void* o, float* lse, int B, int W, int H, int D, int n_r,
+                             float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {
+  if (B < 0 || W < 0 || M < 0 || H <= 0 || D <= 0 || cap < M || !dtype_ok(dtype) || !dtype_ok(o_dtype))
+    return TXL_ERR_INVALID_ARG;
+  if (M > 0 && (start < 0 || start >= cap)) return TXL_ERR_INVALID_ARG;
+  if (B == 0 || W == 0) return TXL_OK;
+  if (q == nullptr || k_seg == nullptr || v_seg == nullptr || r == nullptr || bias_u == nullptr ||
+      bias_v == nullptr || o == nullptr || (M > 0 && (k_mem == nullptr || v_mem == nullptr)))
+    return TXL_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_r) < static_cast<long long>(M) + W || !std::isfinite(scale))
+    return TXL_ERR_INVALID_ARG;
+  const size_t in_align = (dtype == TXL_BF16) ? 16 : 4;
+  for (const void* x : {q, k_seg, v_seg, r})
+    if (!aligned(x, in_align)) return TXL_ERR_INVALID_ARG;
+  if (M > 0 && (!aligned(k_mem, in_align) || !aligned(v_mem, in_align))) return TXL_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(bias_u, 4) || !aligned(bias_v, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return TXL_ERR_INVALID_ARG;
+  const size_t es = dsize(dtype), hd = static_cast<size_t>(H) * D, bw = static_cast<size_t>(B) * W;
+  std::vector<Range> ins = {range_of(q, bw * hd * es), range_of(k_seg, bw * hd * es), range_of(v_seg, bw * hd * es),
+                            range_of(r, static_cast<size_t>(n_r) * hd * es), range_of(bias_u, hd * 4),
+                            range_of(bias_v, hd * 4)};
+  if (M > 0) {
+    ins.push_back(range_of(k_mem, static_cast<size_t>(B) * cap * hd * es));
+    ins.push_back(range_of(v_mem, static_cast<size_t>(B) * cap * hd * es));
+  }
+  const Range ro = range_of(o, bw * hd * dsize(o_dtype));
+  for (const Range& x : ins)
+    if (overlap(ro, x)) return TXL_ERR_ALIAS;
+  if (lse != nullptr) {
+    const Range rl = range_of(lse, bw * H * 4);
+    if (overlap(rl, ro)) return TXL_ERR_ALIAS;
+    for (const Range& x : ins)
+      if (overlap(rl, x)) return TXL_ERR_ALIAS;
+  }
+  const int sup = shape_support(B, W, M, H, D, dtype, o_dtype);
+  if (sup != TXL_OK) return sup;
+  if (M == 0)  // no memory: the segment alone
+    return forward_impl(q, k_seg, v_seg, r, bias_u, bias_v, o, lse, B, W, 0, H, D, n_r, scale, dtype, o_dtype,
+                        nullptr, false, stream);
+  if (dtype == TXL_BF16 && D == 64 && M % 64 == 0 && cap % 64 == 0 && start % 64 == 0) {
+    // the kernel reads the ring in place
+    const RingArgs ra{k_seg, v_seg, cap, start};
+    return forward_impl(q, k_mem, v_mem, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype,
+                        nullptr, false, stream, &ra);
+  }
+  if (B > 65535) return TXL_ERR_UNSUPPORTED;
+  // Otherwise: [memory in ring order ; segment] into contiguous scratch, then
+  // the ordinary call.
+  const long long L = static_cast<long long>(M) + W;
+  const long long row_bytes = static_cast<long long>(hd * es);
+  void* buf = nullptr;
+  if (gather_scratch(stream, 2 * static_cast<size_t>(B) * L * row_bytes, &buf) != cudaSuccess) return TXL_ERR_CUDA;
+  char* lin[2] = {static_cast<char*>(buf), static_cast<char*>(buf) + static_cast<size_t>(B) * L * row_bytes};
+  const void* mem[2] = {k_mem, v_mem};
+  const void* seg[2] = {k_seg, v_seg};
+  const long long n1 = M > 0 ? std::min<long long>(M, cap - start) : 0;  // rows before the ring wraps
+  for (int x = 0; x < 2; ++x) {
+    if (n1 > 0 &&
+        txl::launch_mem_roll(mem[x], nullptr, lin[x], B, n1, n1, start, 0, row_bytes, cap * row_bytes, 0,
+                             L * row_bytes, stream) != cudaSuccess)
+      return TXL_ERR_CUDA;
+    if (txl::launch_mem_roll(mem[x], seg[x], lin[x] + n1 * row_bytes, B, L - n1, M - n1, 0, 0, row_bytes,
+                             cap * row_bytes, W * row_bytes, L * row_bytes, stream) != cudaSuccess)
+      return TXL_ERR_CUDA;
+  }
+  return forward_impl(q, lin[0], lin[1], r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype,
+                      nullptr, false, stream);
+}
+
+int txl_mem_ring_append(void* mem, int cap, int start, int m, const void* h, int w, int B, int C, long long h_bs,
+                        int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream) {
+  if (B < 0 || cap <= 0 || m < 0 || m > cap || w < 0 || C <= 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
+  if (m > 0 && (start < 0 || start >= cap)) return TXL_ERR_INVALID_ARG;
+  if (m == 0) start = 0;
+  const long long total = static_cast<long long>(m) + w;
+  const long long drop = total > cap ? total - cap : 0;  // oldest rows pushed out
+  const int new_start = static_cast<int>((start + drop) % cap);
+  const int new_m = static_cast<int>(std::min<long long>(total, cap));
+  if (B == 0 || w == 0) {
+    if (start_out != nullptr) *start_out = new_start;
+    if (m_out != nullptr) *m_out = new_m;
+    return TXL_OK;
+  }
+  if (mem == nullptr || h == nullptr || (B > 1 && h_bs < static_cast<long long>(w) * C) || h_bs < 0)
+    return TXL_ERR_INVALID_ARG;
+  if (B > 65535) return TXL_ERR_UNSUPPORTED;
+  const long long es = static_cast<long long>(dsize(dtype)), row_bytes = static_cast<long long>(C) * es;
+  if (overlap(range_of(mem, static_cast<size_t>(B) * cap * row_bytes),
+              range_of(h, static_cast<size_t>((B - 1) * h_bs * es + w * row_bytes))))
+    return TXL_ERR_ALIAS;
+  // rows x0 .. w-1 of h go to ring rows (start + m + x) % cap: one or two runs
+  const long long x0 = w > cap ? w - cap : 0;
+  long long x = x0;
+  while (x < w) {
+    const long long dst = (start + m + x) % cap;
+    const long long n = std::min<long long>(w - x, cap - dst);
+    if (txl::launch_mem_roll(nullptr, static_cast<const char*>(h) + x * row_bytes,
+                             static_cast<char*>(mem) + dst * row_bytes, B, n, 0, 0, 0, row_bytes, 0, h_bs * es,
+                             cap * row_bytes, stream) != cudaSuccess)
+      return TXL_ERR_CUDA;
+    x += n;
+  }
+  if (start_out != nullptr) *start_out = new_start;
+  if (m_out != nullptr) *m_out = new_m;
+  return TXL_OK;
 }
 
 }  // extern "C"

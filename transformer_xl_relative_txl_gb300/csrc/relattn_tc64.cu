@@ -119,6 +119,11 @@ struct Params {
   unsigned long long wait_ns;
   int inject_stall;
   int roll_src0;  // >= 0: memory roll of k, v rows [roll_src0, M+W) by the last query tile's units
+  // ring_cap > 0: keys and values come from two places -- memory row m
+  // (m < M) is row (ring_start + m) % ring_cap of the ring maps tm_k / tm_v,
+  // segment row x is row x of tm_ks / tm_vs.  ring_start, ring_cap and M are
+  // multiples of 64, so a key tile never wraps or straddles the two.
+  int ring_cap, ring_start;
 };
 
 struct Bars {
@@ -139,7 +144,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     relattn_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                         const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_km,
-                        const __grid_constant__ CUtensorMap tm_vm, const Params p) {
+                        const __grid_constant__ CUtensorMap tm_vm, const __grid_constant__ CUtensorMap tm_ks,
+                        const __grid_constant__ CUtensorMap tm_vs, const Params p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -257,13 +263,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         const bool rolls = p.roll_src0 >= 0 && w.i0 + BM >= p.W;  // last query tile
         auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, const CUtensorMap* map,
-                           int t, int* prow, int* pb, int* ph, const CUtensorMap* rmap) -> bool {
+                           int t, int* prow, int* pb, int* ph, const CUtensorMap* rmap,
+                           const CUtensorMap* smap) -> bool {
           const int s = static_cast<int>(n % NK);
           if (!mbar_wait(&empty[s], ((n / NK) & 1) ^ 1, wait_ns, abort)) return false;
           flush_store(prow, pb, ph, s, rmap, dst + s * kRowTile);
           mbar_arrive_expect_tx(&full[s], kRowTile);
           const int kr = (w.t0 + t) * BN;  // first key row of the tile
-          tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, kr, w.b);
+          if (p.ring_cap > 0) {
+            if (kr < p.M)
+              tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, (p.ring_start + kr) % p.ring_cap, w.b);
+            else
+              tma_load_4d(dst + s * kRowTile, smap, &full[s], 0, w.h, kr - p.M, w.b);
+          } else {
+            tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, kr, w.b);
+          }
           prow[s] = (rolls && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
           pb[s] = w.b;
           ph[s] = w.h;
@@ -277,9 +291,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t, pk_row, pk_b, pk_h, &tm_km) &&
+          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t, pk_row, pk_b, pk_h, &tm_km, &tm_ks) &&
                load_r(p.M + w.i0 - BN * (w.t0 + t + 1)) &&
-               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t, pv_row, pv_b, pv_h, &tm_vm);
+               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t, pv_row, pv_b, pv_h, &tm_vm, &tm_vs);
         }
       }
       if (!ok) report_timeout(abort, p.status);
@@ -849,7 +863,8 @@ int num_sms() {
 template <bool O_BF16, bool SPLIT>
 cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                          const CUtensorMap& tm_r, const CUtensorMap& tm_o, const CUtensorMap& tm_km,
-                         const CUtensorMap& tm_vm, const Params& prm, cudaStream_t stream) {
+                         const CUtensorMap& tm_vm, const CUtensorMap& tm_ks, const CUtensorMap& tm_vs,
+                         const Params& prm, cudaStream_t stream) {
   auto kern = relattn_tc64_kernel<O_BF16, SPLIT>;
   static int configured_mask = 0;  // one bit per device ordinal < 32
   int dev = 0;
@@ -861,7 +876,7 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
   const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_o, tm_km, tm_vm, prm);
+  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_o, tm_km, tm_vm, tm_ks, tm_vs, prm);
   return cudaGetLastError();
 }
 
@@ -893,8 +908,8 @@ int relattn_tc64_split(int B, int H, int W, int M) {
 
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
-                                const CUtensorMap* tm_vm, int roll_src0, const float* bias_u,
-                                const float* bias_v, void* o,
+                                const CUtensorMap* tm_vm, int roll_src0, const RingMaps* ring,
+                                const float* bias_u, const float* bias_v, void* o,
                                 float* lse, int B, int W, int M, int H, bool o_bf16, float scale, int nsplit,
                                 float* part_o, float* part_lse, int* part_cnt, const WaitCtl& wc,
                                 cudaStream_t stream) {
@@ -922,16 +937,23 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   prm.inject_stall = wc.inject_stall;
   prm.roll_src0 = (tm_km != nullptr && tm_vm != nullptr) ? roll_src0 : -1;
   if (prm.roll_src0 >= 0 && prm.roll_src0 % BN != 0) return cudaErrorInvalidValue;
+  prm.ring_cap = ring != nullptr ? ring->cap : 0;
+  prm.ring_start = ring != nullptr ? ring->start : 0;
+  if (ring != nullptr && (prm.roll_src0 >= 0 || ring->cap % BN != 0 || ring->start % BN != 0 || M % BN != 0 ||
+                          M > ring->cap || ring->start < 0 || ring->start >= ring->cap))
+    return cudaErrorInvalidValue;
   if (o_bf16 && tm_o == nullptr) return cudaErrorInvalidValue;
   // Unused maps (fp32 output is written with plain stores; no roll) are
   // stood in for by tm_q and never touched.
   const CUtensorMap& km = prm.roll_src0 >= 0 ? *tm_km : tm_q;
   const CUtensorMap& vm = prm.roll_src0 >= 0 ? *tm_vm : tm_q;
+  const CUtensorMap& ks = ring != nullptr ? ring->tm_ks : tm_q;
+  const CUtensorMap& vs = ring != nullptr ? ring->tm_vs : tm_q;
   if (nsplit > 1)
-    return o_bf16 ? launch_typed<true, true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, prm, stream)
-                  : launch_typed<false, true>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, prm, stream);
-  return o_bf16 ? launch_typed<true, false>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, prm, stream)
-                : launch_typed<false, false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, prm, stream);
+    return o_bf16 ? launch_typed<true, true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
+                  : launch_typed<false, true>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
+  return o_bf16 ? launch_typed<true, false>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
+                : launch_typed<false, false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
 }
 
 }  // namespace txl

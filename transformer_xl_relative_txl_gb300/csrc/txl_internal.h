@@ -43,6 +43,16 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
                               float* lse, int B, int W, int M, int H, int D, bool o_bf16, float scale,
                               const WaitCtl& wc, cudaStream_t stream);
 
+// Keys and values split between a ring of memory rows and the segment: the
+// maps of launch_relattn_tc64's tm_k / tm_v then describe the rings
+// {D, H, cap, B} (memory row m at ring row (start + m) % cap), and tm_ks /
+// tm_vs the segment rows {D, H, W, B}, all with a {64, 1, 64, 1} box.  cap,
+// start and M are multiples of 64 and M <= cap.
+struct RingMaps {
+  CUtensorMap tm_ks, tm_vs;
+  int cap, start;
+};
+
 // Specialisation for D = 64 (same tensor maps).
 // tm_o: the bf16 output's map (box 64 x 1 x 32 x 1); required when o_bf16.
 // roll_src0 >= 0: also store rows [roll_src0, M+W) of k and v (a multiple of
@@ -56,10 +66,10 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 // after it).
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
-                                const CUtensorMap* tm_vm, int roll_src0, const float* bias_u,
-                                const float* bias_v, void* o, float* lse, int B, int W, int M, int H, bool o_bf16,
-                                float scale, int nsplit, float* part_o, float* part_lse, int* part_cnt,
-                                const WaitCtl& wc, cudaStream_t stream);
+                                const CUtensorMap* tm_vm, int roll_src0, const RingMaps* ring,
+                                const float* bias_u, const float* bias_v, void* o, float* lse, int B, int W, int M,
+                                int H, bool o_bf16, float scale, int nsplit, float* part_o, float* part_lse,
+                                int* part_cnt, const WaitCtl& wc, cudaStream_t stream);
 
 // Backward on CUDA cores (fp32 arithmetic; q, k, v, r fp32 or bf16, o and
 // dout fp32 or bf16; D <= 256).  dk, dv cover the segment's key rows.
