@@ -389,6 +389,76 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
                          "per_launch_work": f"{flops} counted flops = 2*B*H*D*(4*(W*M + W(W+1)/2) + 2*W(W+1)/2)"}}
 
 
+def measure_long_memory(device, steps, warmup, peak, peak_src):
+    """The long workload (B=4 H=16 D=64 W=128 M=1600): one steady segment per
+    step, memory kept two ways -- rolled (txl_relattn_forward_roll: the
+    attention kernel also writes the last M rows of k and v into the next
+    segment's buffer) and as a ring of M + W rows
+    (txl_relattn_forward_ring_append: the kernel reads the memory in place and
+    writes the W new rows of k and v into the free slots).  Each step timed
+    with CUDA events, L2 flushed in between."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import WORKLOADS, make_prefilled, project_r
+
+    wl = WORKLOADS["long"]
+    B, H, D, W, M = wl.B, wl.H, wl.D, wl.W, wl.M
+    q, k, v, seg = make_prefilled(wl, M)
+    bf = torch.bfloat16
+    to = lambda a, dt=bf: torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dt)
+    qd, kd, vd = to(q), to(k), to(v)
+    R = torch.empty(M + W, wl.d_model, device=device)
+    txl.txl_sinusoid_rel(R)
+    rd = to(project_r(R.cpu().numpy(), seg.W_r, H, D, "bf16"))
+    ud, vbd = to(seg.bias_u, torch.float32), to(seg.bias_v, torch.float32)
+    o = torch.empty(qd.shape, device=device, dtype=bf)
+    # roll: ping-pong between two [B, M+W] buffers
+    kb = [kd, kd.clone()]
+    vb = [vd, vd.clone()]
+    # ring: cap = M + W rows, memory rows first; the segment's own rows apart
+    k_ring, v_ring = kd.clone(), vd.clone()
+    k_seg, v_seg = kd[:, M:].contiguous(), vd[:, M:].contiguous()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    cs = torch.cuda.current_stream()
+    state = {"start": 0}
+
+    def roll_step(t):
+        a, b = t % 2, (t + 1) % 2
+        txl.txl_relattn_forward_roll(qd, kb[a], vb[a], rd, ud, vbd, o, kb[b][:, :M], vb[b][:, :M], M, M=M)
+
+    def ring_step(t):
+        s2, m2 = txl.txl_relattn_forward_ring_append(qd, k_ring, v_ring, state["start"], M, k_seg, v_seg, rd, ud,
+                                                     vbd, o)
+        state["start"] = (s2 + m2 - M) % (M + W)  # the next memory: the last M rows
+
+    out = {"workload": f"long: B={B} H={H} D={D} W={W} M={M}, steady-state segment, bf16",
+           "l2": "flushed between steps (256 MB write, outside the events)"}
+    flops = counted_flops(B, H, D, W, M)
+    for name, fn, note in (("roll", roll_step, "txl_relattn_forward_roll (copies the M kept rows)"),
+                           ("ring", ring_step, "txl_relattn_forward_ring_append, ring of M+W rows (one launch; "
+                                                "writes the W new rows)")):
+        ts = []
+        for it in range(warmup + steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cs)
+            fn(it)
+            b.record(cs)
+            if it >= warmup:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+        tf = flops / (ms / 1e3) / 1e12
+        out[name] = {"call": note, "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "steps": len(ts),
+                     "tflops": tf, "frac_of_bf16_peak": tf / peak}
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait in the long-memory steps")
+    out["peak_source"] = f"{peak_src} bf16_tflops (burst)"
+    out["per_step_work"] = f"{flops} counted flops = 6*B*H*D*(W*M + W(W+1)/2)"
+    return out
+
+
 def cpu_baseline_backward(wl, stream, batch=4, budget_s=10.0):
     """The float64 oracle's backward (as it stands) on `batch` sequences of
     segment buffer 0, all heads."""
@@ -542,6 +612,7 @@ def run_ours(args):
         "clocks": sampler.summary(h0, h1),
     }
     result["backward"] = measure_backward(stream, wl, max(5, min(K, 50)), 3, peak, peak_src)
+    result["long_memory"] = measure_long_memory(device, max(5, min(K, 50)), 3, peak, peak_src)
     if world == 1:
         result["cpu_baseline"] = cpu_baseline_oracle(wl, stream)
         result["backward"]["cpu_baseline"] = cpu_baseline_backward(wl, stream)

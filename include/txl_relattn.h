@@ -220,6 +220,23 @@ TXL_API int txl_relattn_forward_ring(const void* q, const void* k_mem, const voi
                              txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream);
 
 /*
+ * txl_relattn_forward_ring_append -- txl_relattn_forward_ring, then
+ * txl_mem_ring_append of k_seg into k_mem and of v_seg into v_mem: the
+ * result, the rings afterwards and *start_out / *m_out are exactly those of
+ * the three calls in order.  With bf16, D = 64, cap, start, M and W
+ * multiples of 64 and M + W <= cap, it is one launch: the new rows go to ring
+ * slots the memory does not occupy, so the attention kernel stores them from
+ * the tiles it loads while it runs.  Otherwise the three calls run in order.
+ * Arguments as in the two calls; k_seg and v_seg must not overlap the rings.
+ */
+TXL_API int txl_relattn_forward_ring_append(void* k_mem, void* v_mem, int cap, int start, int M,
+                                    const void* q, const void* k_seg, const void* v_seg, const void* r,
+                                    const float* bias_u, const float* bias_v, void* o, float* lse,
+                                    int B, int W, int H, int D, int n_r, float scale,
+                                    txl_dtype dtype, txl_dtype o_dtype, int* start_out, int* m_out,
+                                    cudaStream_t stream);
+
+/*
  * txl_mem_ring_append -- the memory roll of a ring buffer.
  *
  * The ring holds m rows (memory row x at ring row (start + x) % cap).  After

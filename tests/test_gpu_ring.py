@@ -98,6 +98,38 @@ def test_ring_append_bit_exact(txl, cap, start, m, w, dtype):
     assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32))
 
 
+@pytest.mark.parametrize("B,H,D,W,M,cap,start,dtype", [
+    (2, 2, 64, 128, 512, 640, 128, "bf16"),    # one launch: slots for the new rows, wraps
+    (1, 2, 64, 128, 1600, 1728, 1664, "bf16"), # one launch with split key ranges
+    (2, 2, 64, 64, 0, 128, 0, "bf16"),         # one launch, empty memory
+    (2, 2, 64, 128, 512, 512, 128, "bf16"),    # full ring: read in place, then the appends
+    (2, 2, 64, 100, 256, 512, 64, "bf16"),     # W off the tile grid
+    (1, 2, 8, 4, 4, 6, 5, "f32"),              # fp32
+])
+def test_ring_append_call_equals_sequence(txl, B, H, D, W, M, cap, start, dtype):
+    q, k, v, r, bu, bv = prefilled_case(workload(B, H, D, W, M, dtype))
+    td = torch_dtype(dtype)
+    qd, kd, vd, rd = (to_dev(x, td) for x in (q, k, v, r))
+    bud, bvd = to_dev(bu, torch.float32), to_dev(bv, torch.float32)
+    ks, vs = kd[:, M:].contiguous(), vd[:, M:].contiguous()
+    rings = [_ring_of(kd, M, cap, start), _ring_of(vd, M, cap, start)]
+    ref = [x.clone() for x in rings]
+    o1 = torch.empty(qd.shape, device=dev(), dtype=td)
+    l1 = torch.empty(B, H, W, device=dev())
+    txl.txl_relattn_forward_ring(qd, ref[0], ref[1], start, M, ks, vs, rd, bud, bvd, o1, l1)
+    s1, m1 = txl.txl_mem_ring_append(ref[0], start, M, ks)
+    txl.txl_mem_ring_append(ref[1], start, M, vs)
+    o2 = torch.empty(qd.shape, device=dev(), dtype=td)
+    l2 = torch.empty(B, H, W, device=dev())
+    s2, m2 = txl.txl_relattn_forward_ring_append(qd, rings[0], rings[1], start, M, ks, vs, rd, bud, bvd, o2, l2)
+    assert txl.txl_get_device_status() == 0
+    assert (s1, m1) == (s2, m2)
+    assert torch.equal(o1, o2) and torch.equal(l1, l2)
+    for got, want in zip(rings, ref):
+        idx = (s2 + torch.arange(m2, device=dev())) % cap
+        assert torch.equal(got[:, idx], want[:, idx])
+
+
 def test_ring_recurrence_matches_oracle(txl):
     """Five segments through a ring of M = 128 rows (W = 64, bf16, D = 64):
     attention reads the ring in place, then the segment's k, v rows are

@@ -18,7 +18,7 @@ import torch
 __all__ = [
     "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
     "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_relattn_forward_ring",
-    "txl_relattn_backward", "txl_mem_update", "txl_mem_ring_append",
+    "txl_relattn_forward_ring_append", "txl_relattn_backward", "txl_mem_update", "txl_mem_ring_append",
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
@@ -48,6 +48,9 @@ lib.txl_relattn_backward.restype = _i
 lib.txl_relattn_forward_ring.argtypes = [_p, _p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i, _f,
                                          _i, _i, _p]
 lib.txl_relattn_forward_ring.restype = _i
+lib.txl_relattn_forward_ring_append.argtypes = [_p, _p, _i, _i, _i, _p, _p, _p, _p, _p, _p, _p, _p, _i, _i, _i, _i, _i,
+                                                _f, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i), _p]
+lib.txl_relattn_forward_ring_append.restype = _i
 lib.txl_mem_ring_append.argtypes = [_p, _i, _i, _i, _p, _i, _i, _i, _ll, ctypes.POINTER(_i), ctypes.POINTER(_i),
                                     _i, _p]
 lib.txl_mem_ring_append.restype = _i
@@ -188,6 +191,34 @@ def txl_relattn_forward_ring(q, k_mem, v_mem, start, M, k_seg, v_seg, r, bias_u,
                                       _dtype_code(o.dtype), _stream(stream))
     _check(st, "txl_relattn_forward_ring")
     return o
+
+
+def txl_relattn_forward_ring_append(q, k_mem, v_mem, start, M, k_seg, v_seg, r, bias_u, bias_v, o, lse=None,
+                                    scale=None, stream=None):
+    """txl_relattn_forward_ring, then the segment's k, v rows appended to
+    the rings; returns the rings' new (start, m)."""
+    B, W, H, D = q.shape
+    for t in (q, k_mem, v_mem, k_seg, v_seg, r, bias_u, bias_v, o) + ((lse,) if lse is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if k_mem.dim() != 4 or k_mem.shape[0] != B or k_mem.shape[2:] != (H, D) or v_mem.shape != k_mem.shape:
+        raise ValueError("k_mem, v_mem must be [B, cap, H, D]")
+    if k_seg.shape != q.shape or v_seg.shape != q.shape or o.shape != q.shape:
+        raise ValueError("k_seg, v_seg, o must be [B, W, H, D]")
+    if r.dim() != 3 or r.shape[1:] != (H, D) or bias_u.shape != (H, D) or bias_v.shape != (H, D):
+        raise ValueError("r must be [n_r, H, D]; biases [H, D]")
+    if not (q.dtype == k_mem.dtype == v_mem.dtype == k_seg.dtype == v_seg.dtype == r.dtype):
+        raise ValueError("q, rings, segment rows and r must share a dtype")
+    if scale is None:
+        scale = D ** -0.5
+    s_out, m_out = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.txl_relattn_forward_ring_append(_ptr(k_mem), _ptr(v_mem), k_mem.shape[1], int(start), int(M), _ptr(q),
+                                             _ptr(k_seg), _ptr(v_seg), _ptr(r), _ptr(bias_u), _ptr(bias_v),
+                                             _ptr(o), _ptr(lse), B, W, H, D, r.shape[0], float(scale),
+                                             _dtype_code(q.dtype), _dtype_code(o.dtype), ctypes.byref(s_out),
+                                             ctypes.byref(m_out), _stream(stream))
+    _check(st, "txl_relattn_forward_ring_append")
+    return s_out.value, m_out.value
 
 
 def txl_mem_ring_append(mem, start, m, h, stream=None):

@@ -311,6 +311,7 @@ struct RingArgs {
   const void* k_seg;
   const void* v_seg;
   int cap, start;
+  bool append;  // the kernel also writes the segment's rows into the ring
 };
 
 // The attention (validated arguments); `roll` non-null asks the D = 64
@@ -425,6 +426,7 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
       return TXL_ERR_CUDA;
     ring_maps.cap = ring->cap;
     ring_maps.start = ring->start;
+    ring_maps.append = ring->append;
   }
   {
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
@@ -672,77 +674,6 @@ int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const 
                         bs, mem_out_bs, nullptr, dtype, stream);
 }
 
-int txl_relattn_forward_ring(const void* q, const void* k_mem, const void* v_mem, int cap, int start, int M,
-                             const void* k_seg, const void* v_seg, const void* r, const float* bias_u,
-                             const float* bias_v, void* o, float* lse, int B, int W, int H, int D, int n_r,
-                             float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {
-  if (B < 0 || W < 0 || M < 0 || H <= 0 || D <= 0 || cap < M || !dtype_ok(dtype) || !dtype_ok(o_dtype))
-    return TXL_ERR_INVALID_ARG;
-  if (M > 0 && (start < 0 || start >= cap)) return TXL_ERR_INVALID_ARG;
-  if (B == 0 || W == 0) return TXL_OK;
-  if (q == nullptr || k_seg == nullptr || v_seg == nullptr || r == nullptr || bias_u == nullptr ||
-      bias_v == nullptr || o == nullptr || (M > 0 && (k_mem == nullptr || v_mem == nullptr)))
-    return TXL_ERR_INVALID_ARG;
-  if (static_cast<long long>(n_r) < static_cast<long long>(M) + W || !std::isfinite(scale))
-    return TXL_ERR_INVALID_ARG;
-  const size_t in_align = (dtype == TXL_BF16) ? 16 : 4;
-  for (const void* x : {q, k_seg, v_seg, r})
-    if (!aligned(x, in_align)) return TXL_ERR_INVALID_ARG;
-  if (M > 0 && (!aligned(k_mem, in_align) || !aligned(v_mem, in_align))) return TXL_ERR_INVALID_ARG;
-  if (!aligned(o, 16) || !aligned(bias_u, 4) || !aligned(bias_v, 4) || (lse != nullptr && !aligned(lse, 4)))
-    return TXL_ERR_INVALID_ARG;
-  const size_t es = dsize(dtype), hd = static_cast<size_t>(H) * D, bw = static_cast<size_t>(B) * W;
-  std::vector<Range> ins = {range_of(q, bw * hd * es), range_of(k_seg, bw * hd * es), range_of(v_seg, bw * hd * es),
-                            range_of(r, static_cast<size_t>(n_r) * hd * es), range_of(bias_u, hd * 4),
-                            range_of(bias_v, hd * 4)};
-  if (M > 0) {
-    ins.push_back(range_of(k_mem, static_cast<size_t>(B) * cap * hd * es));
-    ins.push_back(range_of(v_mem, static_cast<size_t>(B) * cap * hd * es));
-  }
-  const Range ro = range_of(o, bw * hd * dsize(o_dtype));
-  for (const Range& x : ins)
-    if (overlap(ro, x)) return TXL_ERR_ALIAS;
-  if (lse != nullptr) {
-    const Range rl = range_of(lse, bw * H * 4);
-    if (overlap(rl, ro)) return TXL_ERR_ALIAS;
-    for (const Range& x : ins)
-      if (overlap(rl, x)) return TXL_ERR_ALIAS;
-  }
-  const int sup = shape_support(B, W, M, H, D, dtype, o_dtype);
-  if (sup != TXL_OK) return sup;
-  if (M == 0)  // no memory: the segment alone
-    return forward_impl(q, k_seg, v_seg, r, bias_u, bias_v, o, lse, B, W, 0, H, D, n_r, scale, dtype, o_dtype,
-                        nullptr, false, stream);
-  if (dtype == TXL_BF16 && D == 64 && M % 64 == 0 && cap % 64 == 0 && start % 64 == 0) {
-    // the kernel reads the ring in place
-    const RingArgs ra{k_seg, v_seg, cap, start};
-    return forward_impl(q, k_mem, v_mem, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype,
-                        nullptr, false, stream, &ra);
-  }
-  if (B > 65535) return TXL_ERR_UNSUPPORTED;
-  // Otherwise: [memory in ring order ; segment] into contiguous scratch, then
-  // the ordinary call.
-  const long long L = static_cast<long long>(M) + W;
-  const long long row_bytes = static_cast<long long>(hd * es);
-  void* buf = nullptr;
-  if (gather_scratch(stream, 2 * static_cast<size_t>(B) * L * row_bytes, &buf) != cudaSuccess) return TXL_ERR_CUDA;
-  char* lin[2] = {static_cast<char*>(buf), static_cast<char*>(buf) + static_cast<size_t>(B) * L * row_bytes};
-  const void* mem[2] = {k_mem, v_mem};
-  const void* seg[2] = {k_seg, v_seg};
-  const long long n1 = M > 0 ? std::min<long long>(M, cap - start) : 0;  // rows before the ring wraps
-  for (int x = 0; x < 2; ++x) {
-    if (n1 > 0 &&
-        txl::launch_mem_roll(mem[x], nullptr, lin[x], B, n1, n1, start, 0, row_bytes, cap * row_bytes, 0,
-                             L * row_bytes, stream) != cudaSuccess)
-      return TXL_ERR_CUDA;
-    if (txl::launch_mem_roll(mem[x], seg[x], lin[x] + n1 * row_bytes, B, L - n1, M - n1, 0, 0, row_bytes,
-                             cap * row_bytes, W * row_bytes, L * row_bytes, stream) != cudaSuccess)
-      return TXL_ERR_CUDA;
-  }
-  return forward_impl(q, lin[0], lin[1], r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype,
-                      nullptr, false, stream);
-}
-
 int txl_mem_ring_append(void* mem, int cap, int start, int m, const void* h, int w, int B, int C, long long h_bs,
                         int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream) {
   if (B < 0 || cap <= 0 || m < 0 || m > cap || w < 0 || C <= 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
@@ -779,6 +710,143 @@ int txl_mem_ring_append(void* mem, int cap, int start, int m, const void* h, int
   if (start_out != nullptr) *start_out = new_start;
   if (m_out != nullptr) *m_out = new_m;
   return TXL_OK;
+}
+
+}  // extern "C"
+
+namespace {
+// [memory in ring order ; segment] into contiguous scratch, then the
+// ordinary call.
+int linear_ring_forward(const void* q, const void* k_mem, const void* v_mem, int cap, int start, int M,
+                        const void* k_seg, const void* v_seg, const void* r, const float* bias_u, const float* bias_v,
+                        void* o, float* lse, int B, int W, int H, int D, int n_r, float scale, txl_dtype dtype,
+                        txl_dtype o_dtype, cudaStream_t stream) {
+  if (B > 65535) return TXL_ERR_UNSUPPORTED;
+  const size_t es = dsize(dtype), hd = static_cast<size_t>(H) * D;
+  const long long L = static_cast<long long>(M) + W;
+  const long long row_bytes = static_cast<long long>(hd * es);
+  void* buf = nullptr;
+  if (gather_scratch(stream, 2 * static_cast<size_t>(B) * L * row_bytes, &buf) != cudaSuccess) return TXL_ERR_CUDA;
+  char* lin[2] = {static_cast<char*>(buf), static_cast<char*>(buf) + static_cast<size_t>(B) * L * row_bytes};
+  const void* mem[2] = {k_mem, v_mem};
+  const void* seg[2] = {k_seg, v_seg};
+  const long long n1 = M > 0 ? std::min<long long>(M, cap - start) : 0;  // rows before the ring wraps
+  for (int x = 0; x < 2; ++x) {
+    if (n1 > 0 &&
+        txl::launch_mem_roll(mem[x], nullptr, lin[x], B, n1, n1, start, 0, row_bytes, cap * row_bytes, 0,
+                             L * row_bytes, stream) != cudaSuccess)
+      return TXL_ERR_CUDA;
+    if (txl::launch_mem_roll(mem[x], seg[x], lin[x] + n1 * row_bytes, B, L - n1, M - n1, 0, 0, row_bytes,
+                             cap * row_bytes, W * row_bytes, L * row_bytes, stream) != cudaSuccess)
+      return TXL_ERR_CUDA;
+  }
+  return forward_impl(q, lin[0], lin[1], r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype,
+                      nullptr, false, stream);
+}
+
+
+int ring_impl(const void* q, const void* k_mem, const void* v_mem, int cap, int start, int M, const void* k_seg,
+              const void* v_seg, const void* r, const float* bias_u, const float* bias_v, void* o, float* lse, int B,
+              int W, int H, int D, int n_r, float scale, txl_dtype dtype, txl_dtype o_dtype, bool append,
+              int* start_out, int* m_out, cudaStream_t stream) {
+  if (B < 0 || W < 0 || M < 0 || H <= 0 || D <= 0 || cap < M || !dtype_ok(dtype) || !dtype_ok(o_dtype))
+    return TXL_ERR_INVALID_ARG;
+  if (M > 0 && (start < 0 || start >= cap)) return TXL_ERR_INVALID_ARG;
+  if (append && (cap <= 0 || k_mem == nullptr || v_mem == nullptr)) return TXL_ERR_INVALID_ARG;
+  if (M == 0) start = 0;
+  if (append) {  // the ring after the call: the last min(cap, M + W) rows of [memory ; segment]
+    const long long total = static_cast<long long>(M) + W;
+    if (start_out != nullptr) *start_out = static_cast<int>((start + (total > cap ? total - cap : 0)) % cap);
+    if (m_out != nullptr) *m_out = static_cast<int>(std::min<long long>(total, cap));
+  }
+  if (B == 0 || W == 0) return TXL_OK;
+  if (q == nullptr || k_seg == nullptr || v_seg == nullptr || r == nullptr || bias_u == nullptr ||
+      bias_v == nullptr || o == nullptr || (M > 0 && (k_mem == nullptr || v_mem == nullptr)))
+    return TXL_ERR_INVALID_ARG;
+  if (static_cast<long long>(n_r) < static_cast<long long>(M) + W || !std::isfinite(scale))
+    return TXL_ERR_INVALID_ARG;
+  const size_t in_align = (dtype == TXL_BF16) ? 16 : 4;
+  for (const void* x : {q, k_seg, v_seg, r})
+    if (!aligned(x, in_align)) return TXL_ERR_INVALID_ARG;
+  if (M > 0 && (!aligned(k_mem, in_align) || !aligned(v_mem, in_align))) return TXL_ERR_INVALID_ARG;
+  if (!aligned(o, 16) || !aligned(bias_u, 4) || !aligned(bias_v, 4) || (lse != nullptr && !aligned(lse, 4)))
+    return TXL_ERR_INVALID_ARG;
+  const size_t es = dsize(dtype), hd = static_cast<size_t>(H) * D, bw = static_cast<size_t>(B) * W;
+  std::vector<Range> ins = {range_of(q, bw * hd * es), range_of(k_seg, bw * hd * es), range_of(v_seg, bw * hd * es),
+                            range_of(r, static_cast<size_t>(n_r) * hd * es), range_of(bias_u, hd * 4),
+                            range_of(bias_v, hd * 4)};
+  if (M > 0 || append) {
+    ins.push_back(range_of(k_mem, static_cast<size_t>(B) * cap * hd * es));
+    ins.push_back(range_of(v_mem, static_cast<size_t>(B) * cap * hd * es));
+  }
+  if (append) {  // the rings are written: they must not overlap the segment rows or each other
+    const Range rk = range_of(k_mem, static_cast<size_t>(B) * cap * hd * es);
+    const Range rv = range_of(v_mem, static_cast<size_t>(B) * cap * hd * es);
+    if (overlap(rk, rv)) return TXL_ERR_ALIAS;
+    for (size_t x = 0; x < 6; ++x)
+      if (overlap(rk, ins[x]) || overlap(rv, ins[x])) return TXL_ERR_ALIAS;
+  }
+  const Range ro = range_of(o, bw * hd * dsize(o_dtype));
+  for (const Range& x : ins)
+    if (overlap(ro, x)) return TXL_ERR_ALIAS;
+  if (lse != nullptr) {
+    const Range rl = range_of(lse, bw * H * 4);
+    if (overlap(rl, ro)) return TXL_ERR_ALIAS;
+    for (const Range& x : ins)
+      if (overlap(rl, x)) return TXL_ERR_ALIAS;
+  }
+  const int sup = shape_support(B, W, M, H, D, dtype, o_dtype);
+  if (sup != TXL_OK) return sup;
+  const bool in_place = dtype == TXL_BF16 && D == 64 && M % 64 == 0 && cap % 64 == 0 && start % 64 == 0;
+  if (append && in_place && W % 64 == 0 && static_cast<long long>(M) + W <= cap) {
+    // one launch: the kernel reads the ring in place and stores the
+    // segment's rows into ring slots the memory does not use
+    const RingArgs ra{k_seg, v_seg, cap, start, true};
+    return forward_impl(q, k_mem, v_mem, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype,
+                        nullptr, false, stream, &ra);
+  }
+  int st = TXL_OK;
+  if (M == 0) {  // no memory: the segment alone
+    st = forward_impl(q, k_seg, v_seg, r, bias_u, bias_v, o, lse, B, W, 0, H, D, n_r, scale, dtype, o_dtype, nullptr,
+                      false, stream);
+  } else if (in_place) {  // the kernel reads the ring in place
+    const RingArgs ra{k_seg, v_seg, cap, start, false};
+    st = forward_impl(q, k_mem, v_mem, r, bias_u, bias_v, o, lse, B, W, M, H, D, n_r, scale, dtype, o_dtype,
+                      nullptr, false, stream, &ra);
+  } else {
+    st = linear_ring_forward(q, k_mem, v_mem, cap, start, M, k_seg, v_seg, r, bias_u, bias_v, o, lse, B, W, H, D,
+                             n_r, scale, dtype, o_dtype, stream);
+  }
+  if (st != TXL_OK || !append) return st;
+  // then the segment's rows into the rings (after the attention, in stream order)
+  const int C = H * D;
+  if ((st = txl_mem_ring_append(const_cast<void*>(k_mem), cap, start, M, k_seg, W, B, C,
+                                static_cast<long long>(W) * C, nullptr, nullptr, dtype, stream)) != TXL_OK)
+    return st;
+  return txl_mem_ring_append(const_cast<void*>(v_mem), cap, start, M, v_seg, W, B, C, static_cast<long long>(W) * C,
+                             nullptr, nullptr, dtype, stream);
+}
+
+
+}  // namespace
+
+extern "C" {
+
+int txl_relattn_forward_ring(const void* q, const void* k_mem, const void* v_mem, int cap, int start, int M,
+                             const void* k_seg, const void* v_seg, const void* r, const float* bias_u,
+                             const float* bias_v, void* o, float* lse, int B, int W, int H, int D, int n_r,
+                             float scale, txl_dtype dtype, txl_dtype o_dtype, cudaStream_t stream) {
+  return ring_impl(q, k_mem, v_mem, cap, start, M, k_seg, v_seg, r, bias_u, bias_v, o, lse, B, W, H, D, n_r, scale,
+                   dtype, o_dtype, false, nullptr, nullptr, stream);
+}
+
+int txl_relattn_forward_ring_append(void* k_mem, void* v_mem, int cap, int start, int M, const void* q,
+                                    const void* k_seg, const void* v_seg, const void* r, const float* bias_u,
+                                    const float* bias_v, void* o, float* lse, int B, int W, int H, int D, int n_r,
+                                    float scale, txl_dtype dtype, txl_dtype o_dtype, int* start_out, int* m_out,
+                                    cudaStream_t stream) {
+  return ring_impl(q, k_mem, v_mem, cap, start, M, k_seg, v_seg, r, bias_u, bias_v, o, lse, B, W, H, D, n_r, scale,
+                   dtype, o_dtype, true, start_out, m_out, stream);
 }
 
 }  // extern "C"

@@ -124,6 +124,7 @@ struct Params {
   // segment row x is row x of tm_ks / tm_vs.  ring_start, ring_cap and M are
   // multiples of 64, so a key tile never wraps or straddles the two.
   int ring_cap, ring_start;
+  int ring_append;  // ring: also store the segment's k, v tiles into ring rows (start + M + x) % cap
 };
 
 struct Bars {
@@ -139,7 +140,7 @@ struct Bars {
 };
 static_assert(sizeof(Bars) <= 512, "barrier block too large");
 
-template <bool O_BF16, bool SPLIT>
+template <bool O_BF16, bool SPLIT, bool RING>
 __global__ void __launch_bounds__(kThreads, 1)
     relattn_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -261,7 +262,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           ++nR;
           return true;
         };
-        const bool rolls = p.roll_src0 >= 0 && w.i0 + BM >= p.W;  // last query tile
+        // last query tile: the roll (or, for a ring, the append of the
+        // segment's rows into ring rows (start + M + x) % cap, which no unit
+        // of this launch reads)
+        const bool rolls = (RING ? p.ring_append != 0 : p.roll_src0 >= 0) && w.i0 + BM >= p.W;
         auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, const CUtensorMap* map,
                            int t, int* prow, int* pb, int* ph, const CUtensorMap* rmap,
                            const CUtensorMap* smap) -> bool {
@@ -270,7 +274,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           flush_store(prow, pb, ph, s, rmap, dst + s * kRowTile);
           mbar_arrive_expect_tx(&full[s], kRowTile);
           const int kr = (w.t0 + t) * BN;  // first key row of the tile
-          if (p.ring_cap > 0) {
+          if constexpr (RING) {
             if (kr < p.M)
               tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, (p.ring_start + kr) % p.ring_cap, w.b);
             else
@@ -278,7 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
           } else {
             tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, kr, w.b);
           }
-          prow[s] = (rolls && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
+          if constexpr (RING)
+            prow[s] = (rolls && kr >= p.M) ? (p.ring_start + kr) % p.ring_cap : -1;
+          else
+            prow[s] = (rolls && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
           pb[s] = w.b;
           ph[s] = w.h;
           ++n;
@@ -291,9 +298,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t, pk_row, pk_b, pk_h, &tm_km, &tm_ks) &&
+          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t, pk_row, pk_b, pk_h, RING ? &tm_k : &tm_km,
+                       &tm_ks) &&
                load_r(p.M + w.i0 - BN * (w.t0 + t + 1)) &&
-               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t, pv_row, pv_b, pv_h, &tm_vm, &tm_vs);
+               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t, pv_row, pv_b, pv_h, RING ? &tm_v : &tm_vm,
+                       &tm_vs);
         }
       }
       if (!ok) report_timeout(abort, p.status);
@@ -313,9 +322,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < NK; ++s) {
           const uint32_t last = static_cast<uint32_t>(s) + ((nK - 1 - s) / NK) * NK;  // nK == nV
           if (pk_row[s] >= 0 && mbar_wait(&bars->emptyK[s], (last / NK) & 1, wait_ns, abort))
-            flush_store(pk_row, pk_b, pk_h, s, &tm_km, sK + s * kRowTile);
+            flush_store(pk_row, pk_b, pk_h, s, RING ? &tm_k : &tm_km, sK + s * kRowTile);
           if (pv_row[s] >= 0 && mbar_wait(&bars->emptyV[s], (last / NV) & 1, wait_ns, abort))
-            flush_store(pv_row, pv_b, pv_h, s, &tm_vm, sV + s * kRowTile);
+            flush_store(pv_row, pv_b, pv_h, s, RING ? &tm_v : &tm_vm, sV + s * kRowTile);
         }
       }
       bulk_wait_group0();  // every roll store is complete before the CTA exits
@@ -860,12 +869,12 @@ int num_sms() {
   return cached[dev];
 }
 
-template <bool O_BF16, bool SPLIT>
+template <bool O_BF16, bool SPLIT, bool RING>
 cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                          const CUtensorMap& tm_r, const CUtensorMap& tm_o, const CUtensorMap& tm_km,
                          const CUtensorMap& tm_vm, const CUtensorMap& tm_ks, const CUtensorMap& tm_vs,
                          const Params& prm, cudaStream_t stream) {
-  auto kern = relattn_tc64_kernel<O_BF16, SPLIT>;
+  auto kern = relattn_tc64_kernel<O_BF16, SPLIT, RING>;
   static int configured_mask = 0;  // one bit per device ordinal < 32
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -939,9 +948,12 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   if (prm.roll_src0 >= 0 && prm.roll_src0 % BN != 0) return cudaErrorInvalidValue;
   prm.ring_cap = ring != nullptr ? ring->cap : 0;
   prm.ring_start = ring != nullptr ? ring->start : 0;
+  prm.ring_append = ring != nullptr && ring->append ? 1 : 0;
   if (ring != nullptr && (prm.roll_src0 >= 0 || ring->cap % BN != 0 || ring->start % BN != 0 || M % BN != 0 ||
                           M > ring->cap || ring->start < 0 || ring->start >= ring->cap))
     return cudaErrorInvalidValue;
+  // the appended rows must land in slots outside the memory, whole tiles only
+  if (prm.ring_append && (W % BN != 0 || M + W > ring->cap)) return cudaErrorInvalidValue;
   if (o_bf16 && tm_o == nullptr) return cudaErrorInvalidValue;
   // Unused maps (fp32 output is written with plain stores; no roll) are
   // stood in for by tm_q and never touched.
@@ -949,11 +961,20 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   const CUtensorMap& vm = prm.roll_src0 >= 0 ? *tm_vm : tm_q;
   const CUtensorMap& ks = ring != nullptr ? ring->tm_ks : tm_q;
   const CUtensorMap& vs = ring != nullptr ? ring->tm_vs : tm_q;
+  // The ring form is its own instantiation: the loader of the ordinary one
+  // stays as small as it was.
+  if (ring != nullptr) {
+    if (nsplit > 1)
+      return o_bf16 ? launch_typed<true, true, true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
+                    : launch_typed<false, true, true>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
+    return o_bf16 ? launch_typed<true, false, true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
+                  : launch_typed<false, false, true>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
+  }
   if (nsplit > 1)
-    return o_bf16 ? launch_typed<true, true>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
-                  : launch_typed<false, true>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
-  return o_bf16 ? launch_typed<true, false>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
-                : launch_typed<false, false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
+    return o_bf16 ? launch_typed<true, true, false>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
+                  : launch_typed<false, true, false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
+  return o_bf16 ? launch_typed<true, false, false>(tm_q, tm_k, tm_v, tm_r, *tm_o, km, vm, ks, vs, prm, stream)
+                : launch_typed<false, false, false>(tm_q, tm_k, tm_v, tm_r, tm_q, km, vm, ks, vs, prm, stream);
 }
 
 }  // namespace txl

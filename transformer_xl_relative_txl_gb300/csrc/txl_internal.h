@@ -47,10 +47,13 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
 // maps of launch_relattn_tc64's tm_k / tm_v then describe the rings
 // {D, H, cap, B} (memory row m at ring row (start + m) % cap), and tm_ks /
 // tm_vs the segment rows {D, H, W, B}, all with a {64, 1, 64, 1} box.  cap,
-// start and M are multiples of 64 and M <= cap.
+// start and M are multiples of 64 and M <= cap.  append: the kernel also
+// stores the segment's rows into ring rows (start + M + x) % cap (needs
+// W % 64 == 0 and M + W <= cap, so they miss the memory being read).
 struct RingMaps {
   CUtensorMap tm_ks, tm_vs;
   int cap, start;
+  bool append;
 };
 
 // Specialisation for D = 64 (same tensor maps).
