@@ -60,7 +60,8 @@ constexpr int kQOffR = kQOffV + 2 * kKTile;      // 2 stages
 constexpr int kQOffG = kQOffR + 2 * kWinTile;    // G in key order (also the raw q tile at the start)
 constexpr int kQOffGs = kQOffG + kTile;          // 4 distance slots
 constexpr int kQOffBar = kQOffGs + 4 * kTile;
-constexpr int kQSmem = kQOffBar + 256 + 1024;
+constexpr int kQOffBias = kQOffBar + 256;        // u, then v of the head (fp32)
+constexpr int kQSmem = kQOffBias + 2 * 64 * 4 + 1024;
 static_assert(kQSmem <= 232448, "shared memory budget");
 
 // dk/dv kernel shared memory
@@ -74,7 +75,8 @@ constexpr int kKOffR = kKOffDO + 2 * kTile;      // 2 stages
 constexpr int kKOffP = kKOffR + 2 * kWinTile;
 constexpr int kKOffG = kKOffP + kTile;
 constexpr int kKOffBar = kKOffG + kTile;
-constexpr int kKSmem = kKOffBar + 256 + 1024;
+constexpr int kKOffBias = kKOffBar + 256;        // u, then v of the head (fp32)
+constexpr int kKSmem = kKOffBias + 2 * 64 * 4 + 1024;
 static_assert(kKSmem <= 232448, "shared memory budget");
 
 struct BwdParams {
@@ -113,19 +115,19 @@ __device__ __forceinline__ uint32_t swz(int row, int col) {
 }
 
 // Chunks [4 half, 4 half + 4) (head dims 32 half .. 32 half + 31) of row a
-// of (q+u) and (q+v).
+// of (q+u) and (q+v); bu, bv: the head's u and v staged in shared memory.
 __device__ __forceinline__ void build_qu_qv_half(const uint8_t* sQ, uint8_t* sQu, uint8_t* sQv, int a, int half,
-                                                 const float* __restrict__ bu, const float* __restrict__ bv) {
+                                                 const float* bu, const float* bv) {
 #pragma unroll
   for (int cc = 0; cc < 4; ++cc) {
     const int c = 4 * half + cc;
     const uint32_t off = (a >> 3) * 1024 + (a & 7) * 128 + ((c ^ (a & 7)) << 4);
     const uint4 raw = *reinterpret_cast<const uint4*>(sQ + off);
     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    const float4 u0 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c));
-    const float4 u1 = __ldg(reinterpret_cast<const float4*>(bu + 8 * c + 4));
-    const float4 v0 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c));
-    const float4 v1 = __ldg(reinterpret_cast<const float4*>(bv + 8 * c + 4));
+    const float4 u0 = *reinterpret_cast<const float4*>(bu + 8 * c);
+    const float4 u1 = *reinterpret_cast<const float4*>(bu + 8 * c + 4);
+    const float4 v0 = *reinterpret_cast<const float4*>(bv + 8 * c);
+    const float4 v1 = *reinterpret_cast<const float4*>(bv + 8 * c + 4);
     const float ub[8] = {u0.x, u0.y, u0.z, u0.w, u1.x, u1.y, u1.z, u1.w};
     const float vb[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     uint32_t qu[4], qv[4];
@@ -235,6 +237,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* sG = smem + kQOffG;
   uint8_t* sGs = smem + kQOffGs;
   QBars* bars = reinterpret_cast<QBars*>(smem + kQOffBar);
+  float* sBias = reinterpret_cast<float*>(smem + kQOffBias);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
@@ -263,6 +266,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  if (tid < 2 * D) sBias[tid] = tid < D ? p.bias_u[w.h * D + tid] : p.bias_v[w.h * D + tid - D];
   // Distance slots start at zero: a slot entry no step writes is a pair
   // that does not exist.
   for (int x = tid; x < 4 * kTile / 16; x += kQThreads)
@@ -307,7 +311,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (half == 0) p.delta[row_id] = delta;
   }
   bool ok = mbar_wait(&bars->q, 0, wait_ns, abort);
-  if (ok) build_qu_qv_half(sG, sQu, sQv, a, half, p.bias_u + w.h * D, p.bias_v + w.h * D);
+  if (ok) build_qu_qv_half(sG, sQu, sQv, a, half, sBias, sBias + D);
   else report_timeout(abort, p.status);
   fence_proxy_async_smem();
   ok = __syncthreads_and(ok) != 0;
@@ -526,6 +530,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* sP = smem + kKOffP;
   uint8_t* sG = smem + kKOffG;
   KBars* bars = reinterpret_cast<KBars*>(smem + kKOffBar);
+  float* sBias = reinterpret_cast<float*>(smem + kKOffBias);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
@@ -554,6 +559,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  if (tid < 2 * D) sBias[tid] = tid < D ? p.bias_u[h * D + tid] : p.bias_v[h * D + tid - D];
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -580,8 +586,6 @@ __global__ void __launch_bounds__(kQThreads, 1)
     issue_tile_loads(0);
     if (NT > 1) issue_tile_loads(1);
   }
-  const float* bu = p.bias_u + h * D;
-  const float* bv = p.bias_v + h * D;
 
   constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
   constexpr uint32_t id192 = idesc_bf16(128, 192, false, false);
@@ -613,7 +617,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   auto build = [&](int s) -> bool {
     const int st = s & 1;
     if (!mbar_wait(&bars->in[st], (s >> 1) & 1, wait_ns, abort)) return false;
-    build_qu_qv_half(sQ + st * kTile, sQu + st * kTile, sQv + st * kTile, a, half, bu, bv);
+    build_qu_qv_half(sQ + st * kTile, sQu + st * kTile, sQv + st * kTile, a, half, sBias, sBias + D);
     return true;
   };
 
@@ -623,15 +627,25 @@ __global__ void __launch_bounds__(kQThreads, 1)
   ok = __syncthreads_and(ok) != 0;
   if (tid == 0 && ok && !score_mmas(0)) report_timeout(abort, p.status);
 
+  // lse (log2 domain) and Delta of this thread's row in tile s; rows past W
+  // get lse = +inf, so every p is 0.  Loaded one tile ahead.
+  auto row_consts = [&](int s, float& l2, float& dl) {
+    const int i = (qt0 + s) * BM + a;
+    l2 = INFINITY;
+    dl = 0.f;
+    if (s < NT && i < p.W) {
+      const long long row_id = (static_cast<long long>(b) * p.H + h) * p.W + i;
+      l2 = p.lse[row_id] * kLog2e;
+      dl = p.delta[row_id];
+    }
+  };
+  float lse_next, delta_next;
+  row_consts(0, lse_next, delta_next);
   for (int s = 0; s < NT && ok; ++s) {
     const int st = s & 1;
     const int i = (qt0 + s) * BM + a;
-    float lse2 = INFINITY, delta = 0.f;
-    if (i < p.W) {
-      const long long row_id = (static_cast<long long>(b) * p.H + h) * p.W + i;
-      lse2 = p.lse[row_id] * kLog2e;
-      delta = p.delta[row_id];
-    }
+    const float lse2 = lse_next, delta = delta_next;
+    row_consts(s + 1, lse_next, delta_next);
     // (1) everyone: p and g of the tile's rows against the key block; then
     // the next tile's (q+u), (q+v).
     ok = mbar_wait(&bars->m1, s & 1, wait_ns, abort);
