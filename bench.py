@@ -459,6 +459,56 @@ def measure_long_memory(device, steps, warmup, peak, peak_src):
     return out
 
 
+def measure_cached_vs_recompute(device, long_ring_ms, steps, warmup):
+    """Evaluation with the cache against the vanilla sliding window, on the
+    attention of the long workload's shapes (B=4 H=16 D=64, context
+    L = M + W = 1728): the cached path runs one W=128-token segment against
+    M=1600 memory rows per call (the ring step timed in `long_memory`); the
+    sliding window recomputes, for every new token, the causal attention of
+    its whole L-token window (M = 0, W = L queries), as a vanilla layer does
+    when the window moves by one token.  Per token: cached = one segment's
+    time / W, recompute = one window's time."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import WORKLOADS, make_segments, project_r
+
+    wl = WORKLOADS["long"]
+    B, H, D, L = wl.B, wl.H, wl.D, wl.M + wl.W
+    seg = make_segments(wl, rows=L)  # one L-row window of the stream
+    q, k, v = seg.q, seg.k, seg.v
+    bf = torch.bfloat16
+    to = lambda a, dt=bf: torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dt)
+    qd, kd, vd = to(q), to(k), to(v)
+    R = torch.empty(L, wl.d_model, device=device)
+    txl.txl_sinusoid_rel(R)
+    rd = to(project_r(R.cpu().numpy(), seg.W_r, H, D, "bf16"))
+    ud, vbd = to(seg.bias_u, torch.float32), to(seg.bias_v, torch.float32)
+    o = torch.empty(qd.shape, device=device, dtype=bf)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    cs = torch.cuda.current_stream()
+    ts = []
+    for it in range(warmup + steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cs)
+        txl.txl_relattn_forward(qd, kd, vd, rd, ud, vbd, o, M=0)
+        b.record(cs)
+        if it >= warmup:
+            ts.append((a, b))
+    torch.cuda.synchronize()
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait in the sliding-window calls")
+    win_ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    cached_ms = long_ring_ms / wl.W
+    return {"workload": f"attention of B={B} H={H} D={D}, context L={L}: cached = W={wl.W} segments over M={wl.M} "
+                        f"memory rows (ring); recompute = one causal L-row window per token",
+            "cached_ms_per_token": cached_ms, "recompute_ms_per_token": win_ms,
+            "speedup": win_ms / cached_ms,
+            "pairs_per_token": {"cached": wl.M + (wl.W + 1) / 2, "recompute": L * (L + 1) / 2},
+            "scope": "one attention layer of the path; the pages' comparison is a whole model"}
+
+
 def cpu_baseline_backward(wl, stream, batch=4, budget_s=10.0):
     """The float64 oracle's backward (as it stands) on `batch` sequences of
     segment buffer 0, all heads."""
@@ -613,6 +663,7 @@ def run_ours(args):
     }
     result["backward"] = measure_backward(stream, wl, max(5, min(K, 50)), 3, peak, peak_src)
     result["long_memory"] = measure_long_memory(device, max(5, min(K, 50)), 3, peak, peak_src)
+    result["cached_vs_recompute"] = measure_cached_vs_recompute(device, result["long_memory"]["ring"]["ms"], 10, 3)
     if world == 1:
         result["cpu_baseline"] = cpu_baseline_oracle(wl, stream)
         result["backward"]["cpu_baseline"] = cpu_baseline_backward(wl, stream)
