@@ -39,13 +39,19 @@ design notes):
   w_k = 10000^(-2k/dim);
 * memory = the layer's input rows, rolled as projected K/V rows;
 * backward: the stop-gradient drops the memory rows' dk / dv only; r, u and
-  v are shared by every pair and take their whole gradient.
+  v are shared by every pair and take their whole gradient;
+* layer: post-residual normalisation with the population standard deviation
+  plus 1e-6 (outside the root), ReLU feed-forward with biases, output
+  projection after the attention ("Implementing Transformer-XL").
 
 Parity status: every function here is pinned by tests in
 ``tests/test_oracle.py`` (closed forms, library routines, brute force); the
 backward by ``tests/test_oracle_backward.py`` (finite differences of the
 forward, automatic differentiation of an independent torch forward, and
-identities of the score's structure).
+identities of the score's structure); the layer and the stack by
+``tests/test_oracle_layer.py`` (closed forms of the normalisation, blocks
+switched off, the memory cached as rows or as projected keys and values, the
+reach growing with depth).
 """
 
 from __future__ import annotations
@@ -61,6 +67,9 @@ __all__ = [
     "mem_update",
     "run_segments",
     "counted_flops",
+    "layer_norm",
+    "layer_forward",
+    "stack_forward",
 ]
 
 
@@ -360,3 +369,93 @@ def counted_flops(B, H, D, W, M):
     flops per multiply-add, over the visible (query, key) pairs only:
     W*M memory pairs plus W(W+1)/2 causal pairs in the current segment."""
     return 6 * B * H * D * (W * M + W * (W + 1) // 2)
+
+
+# ----------------------------------------------------------------------------
+# The layer and the stack around the attention
+# ----------------------------------------------------------------------------
+
+def layer_norm(x, gamma, beta, eps=1e-6):
+    """Normalisation over the last axis as "Implementing Transformer-XL"
+    writes it (recurrent-memory chapter, layer_norm): subtract the mean,
+    divide by the population standard deviation plus eps (eps outside the
+    root), then scale by gamma and shift by beta."""
+    x = _f64(x)
+    mean = x.mean(axis=-1, keepdims=True)
+    std = x.std(axis=-1, keepdims=True)
+    return _f64(gamma) * (x - mean) / (std + eps) + _f64(beta)
+
+
+def _heads(x, H):
+    B, T, C = x.shape
+    return x.reshape(B, T, H, C // H)
+
+
+def layer_forward(h, mem, P, R, H, scale=None, mem_kv=None):
+    """One Transformer-XL layer on a segment, float64.
+
+    h [B, W, d]: the layer's input rows of the segment; mem [B, M, d]: its
+    input rows of the previous segment (the memory, read as a fixed input);
+    P: weights -- Wq, WkE, WkR, Wv [d, H*D], u, v [H, D], Wo [H*D, d],
+    g1, b1n, g2, b2n [d] (the two normalisations), W1 [d, d_ff], b1 [d_ff],
+    W2 [d_ff, d], b2 [d]; R [n_r, d]: the raw distance table.
+
+    "Implementing Transformer-XL", recurrent-memory chapter, forward and
+    feed_forward: the attention over [memory ; segment] with the output
+    projection, then x = LN1(h + attention), out = LN2(x + FFN(x)) with
+    FFN(x) = ReLU(x W1 + b1) W2 + b2.  Keys and values come from
+    [memory ; segment] through the content key and value projections, the
+    distance keys from R through W_{k,R} ("Transformer-XL, explained", symbol
+    legend), queries from the segment.
+
+    mem_kv = (k_mem, v_mem) [B, M, H, D]: the memory given as its projected
+    keys and values instead of its rows (the same numbers, since the
+    projections act row by row); mem is then unused.
+    """
+    h = _f64(h)
+    B, W, d = h.shape
+    hk = h @ _f64(P["WkE"])
+    hv = h @ _f64(P["Wv"])
+    if mem_kv is not None:
+        k = np.concatenate([_f64(mem_kv[0]), _heads(hk, H)], axis=1)
+        v = np.concatenate([_f64(mem_kv[1]), _heads(hv, H)], axis=1)
+        M = k.shape[1] - W
+    else:
+        mem = np.zeros((B, 0, d)) if mem is None else _f64(mem)
+        M = mem.shape[1]
+        ext = np.concatenate([mem, h], axis=1)
+        k = _heads(ext @ _f64(P["WkE"]), H)
+        v = _heads(ext @ _f64(P["Wv"]), H)
+    q = _heads(h @ _f64(P["Wq"]), H)
+    r = _heads((_f64(R) @ _f64(P["WkR"]))[None], H)[0]
+    a, _ = relattn_forward(q, k, v, r, P["u"], P["v"], M, scale)
+    y = a.reshape(B, W, -1) @ _f64(P["Wo"])
+    x = layer_norm(h + y, P["g1"], P["b1n"])
+    f = np.maximum(0.0, x @ _f64(P["W1"]) + _f64(P["b1"])) @ _f64(P["W2"]) + _f64(P["b2"])
+    return layer_norm(x + f, P["g2"], P["b2n"])
+
+
+def stack_forward(segments, layers, R, H, M, scale=None):
+    """A stack of layers over consecutive segments, float64.
+
+    segments: list of [B, W, d] inputs; layers: list of weight dicts.  Layer
+    n's memory is its own input rows of the previous segment, the last M
+    rows of [memory ; input] ("Transformer-XL, explained", method steps 2 and
+    6: every layer caches its states, and layer n of segment t+1 reads layer
+    n-1 of segment t, so the reach grows with depth).  Returns, per segment,
+    the list of every layer's output.
+    """
+    mems = [None] * len(layers)
+    out = []
+    for h in segments:
+        x = _f64(h)
+        outs = []
+        for n, P in enumerate(layers):
+            y = layer_forward(x, mems[n], P, R, H, scale)
+            prev = np.zeros((x.shape[0], 0, x.shape[2])) if mems[n] is None else mems[n]
+            mems[n] = mem_update(prev, x, M)
+            outs.append(y)
+            x = y
+        out.append(outs)
+    return out
+
