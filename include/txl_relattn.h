@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define TXL_VERSION 130 /* 1.3.0 */
+#define TXL_VERSION 140 /* 1.4.0 */
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -256,6 +256,64 @@ TXL_API int txl_relattn_forward_ring_append(void* k_mem, void* v_mem, int cap, i
  */
 TXL_API int txl_mem_ring_append(void* mem, int cap, int start, int m, const void* h, int w, int B, int C,
                         long long h_bs, int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream);
+
+/*
+ * txl_layer_forward -- one Transformer-XL layer on a segment, the attention
+ * memory kept as a ring of projected keys and values.
+ *
+ * "Implementing Transformer-XL", recurrent-memory chapter (forward,
+ * layer_norm, feed_forward), with the attention of txl_relattn_forward:
+ *
+ *   q = h W_q,  k_seg = h W_k,  v_seg = h W_v,  r = R W_r
+ *   a = relative attention of q over [memory ; segment] (the ring's M rows)
+ *   x = LN1(h + a W_o)
+ *   out = LN2(x + ReLU(x W_1 + b_1) W_2 + b_2)
+ *   LN(z) = gamma (z - mean(z)) / (std(z) + 1e-6) + beta  (population std)
+ *
+ * then k_seg and v_seg are appended to the rings (txl_mem_ring_append
+ * semantics; *start_out, *m_out receive the rings' new state).  The
+ * memory's keys and values are cached already projected: the projections act
+ * row by row, so this equals caching the layer's input rows and projecting
+ * [memory ; segment] again ("Transformer-XL, explained", method step 2).
+ *
+ *   h, out     device, [B, W, d_model] bf16 (out must not overlap h)
+ *   k_mem, v_mem  device, [B, cap, H, D] bf16 rings (memory row m at
+ *              ring row (start + m) % cap)
+ *   w          host struct of device weight pointers (below); bf16 matrices
+ *              row-major [in, out], fp32 vectors
+ *   R          device, [n_r, d_model] bf16 raw distance table (txl_sinusoid_rel),
+ *              n_r >= M + W
+ *   workspace  device, txl_layer_workspace_bytes(...) bytes, 256-byte aligned
+ *   D          64 or 128; d_model and d_ff multiples of 8, d_model <= 1024
+ *
+ * The GEMMs are plain library GEMMs (cuBLASLt, bf16 in, fp32 accumulation,
+ * bf16 out); every other step runs in this library's kernels.
+ */
+typedef struct {
+  const void* W_q;        /* [d_model, H*D] */
+  const void* W_k;        /* [d_model, H*D]  content keys (W_{k,E}) */
+  const void* W_v;        /* [d_model, H*D] */
+  const void* W_r;        /* [d_model, H*D]  distance keys (W_{k,R}) */
+  const float* bias_u;    /* [H, D] */
+  const float* bias_v;    /* [H, D] */
+  const void* W_o;        /* [H*D, d_model] */
+  const float* ln1_gamma; /* [d_model] */
+  const float* ln1_beta;  /* [d_model] */
+  const void* W_1;        /* [d_model, d_ff] */
+  const float* b_1;       /* [d_ff] */
+  const void* W_2;        /* [d_ff, d_model] */
+  const float* b_2;       /* [d_model] */
+  const float* ln2_gamma; /* [d_model] */
+  const float* ln2_beta;  /* [d_model] */
+} txl_layer_weights;
+
+TXL_API size_t txl_layer_workspace_bytes(int B, int W, int d_model, int H, int D, int d_ff, int n_r);
+
+TXL_API int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int cap, int start, int M,
+                      const txl_layer_weights* w, const void* R, int n_r,
+                      int B, int W, int d_model, int H, int D, int d_ff, float scale,
+                      void* workspace, size_t workspace_bytes, int* start_out, int* m_out,
+                      cudaStream_t stream);
 
 /*
  * txl_relattn_backward -- gradients of txl_relattn_forward.

@@ -31,6 +31,7 @@ __all__ = [
     "make_prefilled",
     "project_r",
     "make_dout",
+    "make_layer_weights",
 ]
 
 
@@ -170,3 +171,24 @@ def make_dout(wl: Workload, seed: int = 0, batch: int | None = None) -> np.ndarr
     rng = np.random.default_rng([seed, wl.cfg_id, 1])
     g = _draw(rng, (B, wl.W, wl.H, wl.D), 1.0, wl.dtype == "bf16")
     return _round(g, wl.dtype)
+
+
+def make_layer_weights(d_model: int, H: int, D: int, d_ff: int, seed: int = 0, layer: int = 0) -> dict:
+    """Weights of one layer: ``np.random.default_rng([seed, 7, layer])``,
+    draw order W_q, W_k, W_v, W_r, W_o, W_1, W_2 (matrices ~ N(0, 0.02^2),
+    rounded to bf16, row-major [in, out]), then u, v ~ N(0, 0.02^2), b_1,
+    b_2 ~ N(0, 0.02^2), the normalisations' gains ~ 1 + N(0, 0.1^2) and
+    shifts ~ N(0, 0.02^2) (float32)."""
+    rng = np.random.default_rng([seed, 7, layer])
+    HD = H * D
+    mats = {}
+    for name, shape in (("W_q", (d_model, HD)), ("W_k", (d_model, HD)), ("W_v", (d_model, HD)),
+                        ("W_r", (d_model, HD)), ("W_o", (HD, d_model)), ("W_1", (d_model, d_ff)),
+                        ("W_2", (d_ff, d_model))):
+        mats[name] = round_bf16(rng.standard_normal(shape, dtype=np.float32) * np.float32(0.02))
+    f32 = lambda shape, std, mean=0.0: (mean + rng.standard_normal(shape) * std).astype(np.float32)
+    mats.update(bias_u=f32((H, D), 0.02), bias_v=f32((H, D), 0.02), b_1=f32((d_ff,), 0.02),
+                b_2=f32((d_model,), 0.02), ln1_gamma=f32((d_model,), 0.1, 1.0), ln1_beta=f32((d_model,), 0.02),
+                ln2_gamma=f32((d_model,), 0.1, 1.0), ln2_beta=f32((d_model,), 0.02))
+    return mats
+

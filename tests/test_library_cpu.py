@@ -31,7 +31,7 @@ def _build_if_missing():
 def declared_functions():
     text = open(HEADER).read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
-    return sorted(set(re.findall(r"^\s*(?:TXL_API\s+)?(?:int|const char\*|txl_status)\s+(txl_\w+)\s*\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^\s*(?:TXL_API\s+)?(?:int|size_t|const char\*|txl_status)\s+(txl_\w+)\s*\(", text, flags=re.M)))
 
 
 def test_header_declares_the_three_calls():
@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol():
     for n in declared_functions():
         getattr(lib, n)
     lib.txl_version.restype = ctypes.c_int
-    assert lib.txl_version() == 130
+    assert lib.txl_version() == 140
     lib.txl_status_string.restype = ctypes.c_char_p
     assert lib.txl_status_string(5) == b"TXL_ERR_DEVICE_TIMEOUT"
 

@@ -19,6 +19,7 @@ __all__ = [
     "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
     "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_relattn_forward_ring",
     "txl_relattn_forward_ring_append", "txl_relattn_backward", "txl_mem_update", "txl_mem_ring_append",
+    "txl_layer_forward", "txl_layer_workspace_bytes", "LAYER_WEIGHT_NAMES",
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
@@ -54,6 +55,19 @@ lib.txl_relattn_forward_ring_append.restype = _i
 lib.txl_mem_ring_append.argtypes = [_p, _i, _i, _i, _p, _i, _i, _i, _ll, ctypes.POINTER(_i), ctypes.POINTER(_i),
                                     _i, _p]
 lib.txl_mem_ring_append.restype = _i
+LAYER_WEIGHT_NAMES = ("W_q", "W_k", "W_v", "W_r", "bias_u", "bias_v", "W_o", "ln1_gamma", "ln1_beta", "W_1", "b_1",
+                      "W_2", "b_2", "ln2_gamma", "ln2_beta")
+
+
+class _LayerWeights(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_void_p) for n in LAYER_WEIGHT_NAMES]
+
+
+lib.txl_layer_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+lib.txl_layer_workspace_bytes.restype = ctypes.c_size_t
+lib.txl_layer_forward.argtypes = [_p, _p, _p, _p, _i, _i, _i, ctypes.POINTER(_LayerWeights), _p, _i, _i, _i, _i, _i,
+                                  _i, _i, _f, _p, ctypes.c_size_t, ctypes.POINTER(_i), ctypes.POINTER(_i), _p]
+lib.txl_layer_forward.restype = _i
 lib.txl_mem_update.argtypes = [_p, _i, _p, _i, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i, _p]
 lib.txl_mem_update.restype = _i
 lib.txl_sinusoid_rel.argtypes = [_p, _i, _i, _i, _p]
@@ -218,6 +232,46 @@ def txl_relattn_forward_ring_append(q, k_mem, v_mem, start, M, k_seg, v_seg, r, 
                                              _dtype_code(q.dtype), _dtype_code(o.dtype), ctypes.byref(s_out),
                                              ctypes.byref(m_out), _stream(stream))
     _check(st, "txl_relattn_forward_ring_append")
+    return s_out.value, m_out.value
+
+
+def txl_layer_workspace_bytes(B, W, d_model, H, D, d_ff, n_r):
+    return int(lib.txl_layer_workspace_bytes(B, W, d_model, H, D, d_ff, n_r))
+
+
+def txl_layer_forward(h, out, k_mem, v_mem, start, M, weights, R, workspace, scale=None, stream=None):
+    """One layer on the segment h [B, W, d_model] (bf16) into out; the
+    attention memory is the rings k_mem, v_mem [B, cap, H, D] holding M
+    projected rows from ring row `start`; weights: dict with
+    LAYER_WEIGHT_NAMES (bf16 matrices [in, out], fp32 vectors); R: the raw
+    distance table [n_r, d_model] bf16; workspace: uint8 device tensor of at
+    least txl_layer_workspace_bytes(...) bytes.  Returns the rings' new
+    (start, m)."""
+    B, W, d_model = h.shape
+    _, cap, H, D = k_mem.shape
+    d_ff = weights["W_1"].shape[1]
+    for t in (h, out, k_mem, v_mem, R, workspace) + tuple(weights[n] for n in LAYER_WEIGHT_NAMES):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if out.shape != h.shape or h.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("h and out must be bf16 [B, W, d_model]")
+    if v_mem.shape != k_mem.shape or k_mem.shape[0] != B or k_mem.dtype != torch.bfloat16:
+        raise ValueError("rings must be bf16 [B, cap, H, D]")
+    for n in ("W_q", "W_k", "W_v", "W_r", "W_o", "W_1", "W_2"):
+        if weights[n].dtype != torch.bfloat16:
+            raise ValueError(f"{n} must be bf16")
+    for n in ("bias_u", "bias_v", "ln1_gamma", "ln1_beta", "b_1", "b_2", "ln2_gamma", "ln2_beta"):
+        if weights[n].dtype != torch.float32:
+            raise ValueError(f"{n} must be fp32")
+    if scale is None:
+        scale = D ** -0.5
+    wts = _LayerWeights(*[_ptr(weights[n]) for n in LAYER_WEIGHT_NAMES])
+    s_out, m_out = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.txl_layer_forward(_ptr(h), _ptr(out), _ptr(k_mem), _ptr(v_mem), cap, int(start), int(M),
+                               ctypes.byref(wts), _ptr(R), R.shape[0], B, W, d_model, H, D, d_ff, float(scale),
+                               _ptr(workspace), workspace.numel() * workspace.element_size(), ctypes.byref(s_out),
+                               ctypes.byref(m_out), _stream(stream))
+    _check(st, "txl_layer_forward")
     return s_out.value, m_out.value
 
 

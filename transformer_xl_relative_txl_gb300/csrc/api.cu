@@ -849,4 +849,72 @@ int txl_relattn_forward_ring_append(void* k_mem, void* v_mem, int cap, int start
                    dtype, o_dtype, true, start_out, m_out, stream);
 }
 
+namespace {
+constexpr size_t kGemmWs = size_t(32) << 20;  // cuBLASLt workspace inside the layer's workspace
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+}  // namespace
+
+size_t txl_layer_workspace_bytes(int B, int W, int d_model, int H, int D, int d_ff, int n_r) {
+  if (B <= 0 || W <= 0 || d_model <= 0 || H <= 0 || D <= 0 || d_ff <= 0 || n_r <= 0) return 0;
+  const size_t bw = static_cast<size_t>(B) * W, hd = static_cast<size_t>(H) * D;
+  return kGemmWs + 4 * align256(bw * hd * 2) + align256(static_cast<size_t>(n_r) * hd * 2) +
+         3 * align256(bw * d_model * 2) + align256(bw * d_ff * 2);
+}
+
+int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int cap, int start, int M,
+                      const txl_layer_weights* w, const void* R, int n_r, int B, int W, int d_model, int H, int D,
+                      int d_ff, float scale, void* workspace, size_t workspace_bytes, int* start_out, int* m_out,
+                      cudaStream_t stream) {
+  if (w == nullptr || h == nullptr || out == nullptr || R == nullptr || workspace == nullptr || B <= 0 || W <= 0 ||
+      d_model <= 0 || H <= 0 || D <= 0 || d_ff <= 0 || M < 0 || cap < M || cap <= 0)
+    return TXL_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->W_q, w->W_k, w->W_v, w->W_r, w->bias_u, w->bias_v, w->W_o, w->ln1_gamma, w->ln1_beta,
+                        w->W_1, w->b_1, w->W_2, w->b_2, w->ln2_gamma, w->ln2_beta, k_mem, v_mem};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return TXL_ERR_INVALID_ARG;
+  if (!aligned(h, 16) || !aligned(out, 16) || !aligned(R, 16) || !aligned(workspace, 256))
+    return TXL_ERR_INVALID_ARG;
+  if (d_model % 8 != 0 || d_model > 1024 || d_ff % 8 != 0) return TXL_ERR_UNSUPPORTED;
+  if (workspace_bytes < txl_layer_workspace_bytes(B, W, d_model, H, D, d_ff, n_r)) return TXL_ERR_INVALID_ARG;
+  const size_t bw = static_cast<size_t>(B) * W, hd = static_cast<size_t>(H) * D;
+  if (overlap(range_of(out, bw * d_model * 2), range_of(h, bw * d_model * 2))) return TXL_ERR_ALIAS;
+  // workspace carve-up
+  char* p = static_cast<char*>(workspace);
+  auto take = [&](size_t bytes) {
+    char* r = p;
+    p += align256(bytes);
+    return r;
+  };
+  void* gws = take(kGemmWs);
+  void* q = take(bw * hd * 2);
+  void* ks = take(bw * hd * 2);
+  void* vs = take(bw * hd * 2);
+  void* a = take(bw * hd * 2);
+  void* r = take(static_cast<size_t>(n_r) * hd * 2);
+  void* y = take(bw * d_model * 2);
+  void* x = take(bw * d_model * 2);
+  void* z = take(bw * d_model * 2);
+  void* f = take(bw * d_ff * 2);
+  const int rows = static_cast<int>(bw);
+  const int HD = static_cast<int>(hd);
+  if (txl::gemm_bf16(h, w->W_q, q, rows, HD, d_model, gws, kGemmWs, stream) ||
+      txl::gemm_bf16(h, w->W_k, ks, rows, HD, d_model, gws, kGemmWs, stream) ||
+      txl::gemm_bf16(h, w->W_v, vs, rows, HD, d_model, gws, kGemmWs, stream) ||
+      txl::gemm_bf16(R, w->W_r, r, n_r, HD, d_model, gws, kGemmWs, stream))
+    return TXL_ERR_CUDA;
+  int st = txl_relattn_forward_ring_append(k_mem, v_mem, cap, start, M, q, ks, vs, r, w->bias_u, w->bias_v, a,
+                                           nullptr, B, W, H, D, n_r, scale, TXL_BF16, TXL_BF16, start_out, m_out,
+                                           stream);
+  if (st != TXL_OK) return st;
+  if (txl::gemm_bf16(a, w->W_o, y, rows, d_model, HD, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
+  if (txl::launch_add_ln(h, y, nullptr, w->ln1_gamma, w->ln1_beta, x, rows, d_model, stream) != cudaSuccess)
+    return TXL_ERR_CUDA;
+  if (txl::gemm_bf16(x, w->W_1, f, rows, d_ff, d_model, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
+  if (txl::launch_bias_relu(f, w->b_1, rows, d_ff, stream) != cudaSuccess) return TXL_ERR_CUDA;
+  if (txl::gemm_bf16(f, w->W_2, z, rows, d_model, d_ff, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
+  if (txl::launch_add_ln(x, z, w->b_2, w->ln2_gamma, w->ln2_beta, out, rows, d_model, stream) != cudaSuccess)
+    return TXL_ERR_CUDA;
+  return TXL_OK;
+}
+
 }  // extern "C"

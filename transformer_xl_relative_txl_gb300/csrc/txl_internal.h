@@ -104,6 +104,18 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
                                     int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
                                     cudaStream_t stream);
 
+// The layer around the attention (layer.cu).  Row-major bf16 GEMM
+// C [m, n] = A [m, k] B [k, n] with fp32 accumulation (cuBLASLt); returns 0
+// on success.  ws: cuBLASLt workspace.
+int gemm_bf16(const void* A, const void* B, void* C, int m, int n, int k, void* ws, size_t ws_bytes,
+              cudaStream_t stream);
+// out = LN(a + b (+ bias)) row by row over d columns (bf16 rows, fp32 gamma,
+// beta, bias; d a multiple of 8, <= 1024).
+cudaError_t launch_add_ln(const void* a, const void* b, const float* bias, const float* gamma, const float* beta,
+                          void* out, long long rows, int d, cudaStream_t stream);
+// f = ReLU(f + bias) over bf16 [rows, n] (n a multiple of 8).
+cudaError_t launch_bias_relu(void* f, const float* bias, long long rows, int n, cudaStream_t stream);
+
 // Number of chunks the D = 64 kernel should split each unit's key steps
 // into (1: no split), from the shape and the device's SM count.
 int relattn_tc64_split(int B, int H, int W, int M);
