@@ -509,6 +509,72 @@ def measure_cached_vs_recompute(device, long_ring_ms, steps, warmup):
             "scope": "one attention layer of the path; the pages' comparison is a whole model"}
 
 
+LAYER_D_FF = 2048  # feed-forward width of the measured layer (4 x d_model)
+
+
+def layer_flops(B, W, M, d_model, H, D, d_ff):
+    """Counted work of one layer on a segment: the GEMMs (q, k, v of the
+    segment rows, r of the M+W distances, the output projection, the two
+    feed-forward matrices) plus the attention's counted flops."""
+    bw, hd, n_r = B * W, H * D, M + W
+    gemm = 2 * bw * d_model * 3 * hd + 2 * n_r * d_model * hd + 2 * bw * hd * d_model + 4 * bw * d_model * d_ff
+    return gemm + counted_flops(B, H, D, W, M)
+
+
+def measure_layer(device, steps, warmup, peak, peak_src):
+    """txl_layer_forward at the base shapes (B=22, W=512, M=512, d_model=512,
+    8 heads of 64, d_ff=2048): one steady segment per call, the layer's
+    memory a ring of M+W projected rows, each call timed with CUDA events, L2
+    flushed in between."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import WORKLOADS, make_layer_weights
+
+    wl = WORKLOADS["base"]
+    B, W, M, H, D, d = wl.B, wl.W, wl.M, wl.H, wl.D, wl.H * wl.D
+    w = make_layer_weights(d, H, D, LAYER_D_FF)
+    dw = {k: torch.from_numpy(v).to(device).to(torch.bfloat16 if k.startswith("W_") else torch.float32)
+          for k, v in w.items()}
+    g = torch.Generator(device=device).manual_seed(0)
+    h = torch.randn(B, W, d, device=device, generator=g).to(torch.bfloat16)
+    out = torch.empty_like(h)
+    cap = M + W
+    k_ring = (torch.randn(B, cap, H, D, device=device, generator=g) * 0.3).to(torch.bfloat16)
+    v_ring = torch.randn(B, cap, H, D, device=device, generator=g).to(torch.bfloat16)
+    R = torch.empty(M + W, d, device=device, dtype=torch.bfloat16)
+    txl.txl_sinusoid_rel(R)
+    ws = torch.empty(txl.txl_layer_workspace_bytes(B, W, d, H, D, LAYER_D_FF, M + W), device=device,
+                     dtype=torch.uint8)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    cs = torch.cuda.current_stream()
+    start = 0
+    ts = []
+    for it in range(warmup + steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(cs)
+        s2, m2 = txl.txl_layer_forward(h, out, k_ring, v_ring, start, M, dw, R, ws)
+        b.record(cs)
+        start = (s2 + m2 - M) % cap  # the next memory: the last M rows
+        if it >= warmup:
+            ts.append((a, b))
+    torch.cuda.synchronize()
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait in the layer")
+    ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+    flops = layer_flops(B, W, M, d, H, D, LAYER_D_FF)
+    tf = flops / (ms / 1e3) / 1e12
+    return {"call": "txl_layer_forward (q/k/v/r/o/FFN GEMMs on cuBLASLt; attention, normalisations, bias+ReLU "
+                    "and the memory append in this library's kernels)",
+            "workload": f"base segment through one layer: B={B} W={W} M={M} d_model={d} H={H} D={D} "
+                        f"d_ff={LAYER_D_FF}, memory a ring of M+W projected rows",
+            "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "calls": len(ts),
+            "tflops": tf, "frac_of_bf16_peak": tf / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
+            "per_call_work": f"{flops} counted flops (GEMMs + the attention's 6*B*H*D*(W*M + W(W+1)/2))",
+            "l2": "flushed between calls (256 MB write, outside the events)"}
+
+
 def cpu_baseline_backward(wl, stream, batch=4, budget_s=10.0):
     """The float64 oracle's backward (as it stands) on `batch` sequences of
     segment buffer 0, all heads."""
@@ -664,6 +730,7 @@ def run_ours(args):
     result["backward"] = measure_backward(stream, wl, max(5, min(K, 50)), 3, peak, peak_src)
     result["long_memory"] = measure_long_memory(device, max(5, min(K, 50)), 3, peak, peak_src)
     result["cached_vs_recompute"] = measure_cached_vs_recompute(device, result["long_memory"]["ring"]["ms"], 10, 3)
+    result["layer"] = measure_layer(device, max(5, min(K, 30)), 3, peak, peak_src)
     if world == 1:
         result["cpu_baseline"] = cpu_baseline_oracle(wl, stream)
         result["backward"]["cpu_baseline"] = cpu_baseline_backward(wl, stream)
