@@ -275,15 +275,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[s], kRowTile);
           const int kr = (w.t0 + t) * BN;  // first key row of the tile
           if constexpr (RING) {
-            if (kr < p.M)
-              tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, (p.ring_start + kr) % p.ring_cap, w.b);
+            if (kr < p.M)  // start + kr < 2 cap: one conditional wrap
+              tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h,
+                          p.ring_start + kr - (p.ring_start + kr >= p.ring_cap ? p.ring_cap : 0), w.b);
             else
               tma_load_4d(dst + s * kRowTile, smap, &full[s], 0, w.h, kr - p.M, w.b);
           } else {
             tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, kr, w.b);
           }
           if constexpr (RING)
-            prow[s] = (rolls && kr >= p.M) ? (p.ring_start + kr) % p.ring_cap : -1;
+            prow[s] = (rolls && kr >= p.M)  // start + kr < start + M + W <= 2 cap
+                          ? p.ring_start + kr - (p.ring_start + kr >= p.ring_cap ? p.ring_cap : 0)
+                          : -1;
           else
             prow[s] = (rolls && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
           pb[s] = w.b;
