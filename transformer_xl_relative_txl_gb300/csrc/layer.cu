@@ -27,8 +27,17 @@ __device__ __forceinline__ float warp_sum(float x) {
   return x;
 }
 
+// Eight fp32 values at p (32-byte aligned) as two vector loads.
+__device__ __forceinline__ void load8(const float* __restrict__ p, float (&v)[8]) {
+  const float4 x = __ldg(reinterpret_cast<const float4*>(p));
+  const float4 y = __ldg(reinterpret_cast<const float4*>(p) + 1);
+  v[0] = x.x, v[1] = x.y, v[2] = x.z, v[3] = x.w, v[4] = y.x, v[5] = y.y, v[6] = y.z, v[7] = y.w;
+}
+
 // out[row] = LN(a[row] + b[row] (+ bias)), one warp per row of d columns
 // (d a multiple of 8, at most 1024): each lane holds up to 4 chunks of 8.
+// All of a row's loads are issued before any arithmetic, and the per-column
+// vectors are read as float4.
 __global__ void __launch_bounds__(256) add_ln_kernel(const __nv_bfloat16* __restrict__ a,
                                                      const __nv_bfloat16* __restrict__ b,
                                                      const float* __restrict__ bias,
@@ -39,21 +48,30 @@ __global__ void __launch_bounds__(256) add_ln_kernel(const __nv_bfloat16* __rest
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
   const int nchunk = d / 8;
+  uint4 va[4], vb[4];
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    const int ch = lane + 32 * c;
+    if (ch < nchunk) {
+      va[c] = __ldg(reinterpret_cast<const uint4*>(a + row * d) + ch);
+      vb[c] = __ldg(reinterpret_cast<const uint4*>(b + row * d) + ch);
+    }
+  }
   float x[4][8];
   float s = 0.f;
 #pragma unroll
   for (int c = 0; c < 4; ++c) {
     const int ch = lane + 32 * c;
     if (ch < nchunk) {
-      const uint4 va = *reinterpret_cast<const uint4*>(a + row * d + 8 * ch);
-      const uint4 vb = *reinterpret_cast<const uint4*>(b + row * d + 8 * ch);
-      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&va);
-      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&vb);
+      float bb[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      if (bias != nullptr) load8(bias + 8 * ch, bb);
+      const __nv_bfloat162* pa = reinterpret_cast<const __nv_bfloat162*>(&va[c]);
+      const __nv_bfloat162* pb = reinterpret_cast<const __nv_bfloat162*>(&vb[c]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const float2 fa = __bfloat1622float2(pa[e]), fb = __bfloat1622float2(pb[e]);
-        x[c][2 * e] = fa.x + fb.x + (bias ? bias[8 * ch + 2 * e] : 0.f);
-        x[c][2 * e + 1] = fa.y + fb.y + (bias ? bias[8 * ch + 2 * e + 1] : 0.f);
+        x[c][2 * e] = fa.x + fb.x + bb[2 * e];
+        x[c][2 * e + 1] = fa.y + fb.y + bb[2 * e + 1];
         s += x[c][2 * e] + x[c][2 * e + 1];
       }
     }
@@ -70,34 +88,47 @@ __global__ void __launch_bounds__(256) add_ln_kernel(const __nv_bfloat16* __rest
   for (int c = 0; c < 4; ++c) {
     const int ch = lane + 32 * c;
     if (ch < nchunk) {
+      float g[8], bt[8];
+      load8(gamma + 8 * ch, g);
+      load8(beta + 8 * ch, bt);
       uint32_t w[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
-        const int col = 8 * ch + 2 * e;
-        const float y0 = gamma[col] * (x[c][2 * e] - mean) * inv + beta[col];
-        const float y1 = gamma[col + 1] * (x[c][2 * e + 1] - mean) * inv + beta[col + 1];
-        const __nv_bfloat162 p = __floats2bfloat162_rn(y0, y1);
-        w[e] = *reinterpret_cast<const uint32_t*>(&p);
+        const __nv_bfloat162 p2 = __floats2bfloat162_rn(g[2 * e] * (x[c][2 * e] - mean) * inv + bt[2 * e],
+                                                        g[2 * e + 1] * (x[c][2 * e + 1] - mean) * inv + bt[2 * e + 1]);
+        w[e] = *reinterpret_cast<const uint32_t*>(&p2);
       }
       *reinterpret_cast<uint4*>(out + row * d + 8 * ch) = make_uint4(w[0], w[1], w[2], w[3]);
     }
   }
 }
 
-// f = ReLU(f + bias) in place over [rows, n] (n a multiple of 8).
+// f = ReLU(f + bias) in place over [rows, n] (n a multiple of 8): four
+// independent 16-byte vectors a thread per round, all loaded first.
 __global__ void __launch_bounds__(256) bias_relu_kernel(__nv_bfloat16* __restrict__ f,
                                                         const float* __restrict__ bias, long long n_vec, int n) {
-  for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < n_vec;
-       i += static_cast<long long>(gridDim.x) * blockDim.x) {
-    uint4 v = reinterpret_cast<uint4*>(f)[i];
-    __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&v);
-    const int col = static_cast<int>((i * 8) % n);
+  const long long stride = static_cast<long long>(gridDim.x) * blockDim.x;
+  for (long long base = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; base < n_vec;
+       base += 4 * stride) {
+    uint4 v[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const float2 x = __bfloat1622float2(p[e]);
-      p[e] = __floats2bfloat162_rn(fmaxf(x.x + bias[col + 2 * e], 0.f), fmaxf(x.y + bias[col + 2 * e + 1], 0.f));
+    for (int u = 0; u < 4; ++u)
+      if (base + u * stride < n_vec) v[u] = reinterpret_cast<const uint4*>(f)[base + u * stride];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long i = base + u * stride;
+      if (i < n_vec) {
+        float bb[8];
+        load8(bias + (i * 8) % n, bb);
+        __nv_bfloat162* p = reinterpret_cast<__nv_bfloat162*>(&v[u]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float2 x = __bfloat1622float2(p[e]);
+          p[e] = __floats2bfloat162_rn(fmaxf(x.x + bb[2 * e], 0.f), fmaxf(x.y + bb[2 * e + 1], 0.f));
+        }
+        reinterpret_cast<uint4*>(f)[i] = v[u];
+      }
     }
-    reinterpret_cast<uint4*>(f)[i] = v;
   }
 }
 
