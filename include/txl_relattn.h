@@ -409,6 +409,10 @@ TXL_API int txl_version(void);
  */
 TXL_API int txl_debug_set_wait_limit_ns(unsigned long long ns);
 TXL_API int txl_debug_inject_stall(int on);
+/* Test hook: nsplit > 0 makes the bf16 D = 64 forward split every unit's
+ * key steps into min(nsplit, steps of the shortest unit) chunks instead of
+ * the count its cost model picks; 0 restores the model. */
+TXL_API int txl_debug_force_split(int nsplit);
 
 #ifdef __cplusplus
 }

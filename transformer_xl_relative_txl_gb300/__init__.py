@@ -22,7 +22,7 @@ __all__ = [
     "txl_layer_forward", "txl_layer_workspace_bytes", "LAYER_WEIGHT_NAMES",
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
-    "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall",
+    "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall", "txl_debug_force_split",
 ]
 
 TXL_F32 = 0
@@ -82,6 +82,8 @@ lib.txl_debug_set_wait_limit_ns.argtypes = [ctypes.c_ulonglong]
 lib.txl_debug_set_wait_limit_ns.restype = _i
 lib.txl_debug_inject_stall.argtypes = [_i]
 lib.txl_debug_inject_stall.restype = _i
+lib.txl_debug_force_split.argtypes = [_i]
+lib.txl_debug_force_split.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -420,3 +422,9 @@ def txl_debug_set_wait_limit_ns(ns: int) -> int:
 
 def txl_debug_inject_stall(on: bool) -> int:
     return lib.txl_debug_inject_stall(1 if on else 0)
+
+
+def txl_debug_force_split(nsplit):
+    """Test hook: force the D = 64 forward's split count (0: its cost model)."""
+    _check(lib.txl_debug_force_split(int(nsplit)), "txl_debug_force_split")
+

@@ -25,6 +25,7 @@ __device__ unsigned int g_txl_status;
 
 std::atomic<unsigned long long> g_wait_ns{2000000000ULL};
 std::atomic<int> g_inject_stall{0};
+std::atomic<int> g_force_split{0};  // test hook: > 0 forces the D = 64 kernel's split count
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -213,6 +214,12 @@ int txl_debug_set_wait_limit_ns(unsigned long long ns) {
 
 int txl_debug_inject_stall(int on) {
   g_inject_stall.store(on ? 1 : 0);
+  return TXL_OK;
+}
+
+int txl_debug_force_split(int nsplit) {
+  if (nsplit < 0 || nsplit > 64) return TXL_ERR_INVALID_ARG;
+  g_force_split.store(nsplit);
   return TXL_OK;
 }
 
@@ -465,7 +472,12 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
   if (D == 64) {
     // Too few units to fill the SMs: split each unit's key steps into
     // chunks; the last chunk of each unit merges their partial results.
-    const int nsplit = txl::relattn_tc64_split(B, H, W, M);
+    int nsplit = txl::relattn_tc64_split(B, H, W, M);
+    if (const int f = g_force_split.load(); f > 0) {
+      // never more chunks than the shortest unit has key steps
+      const int nks_min = (std::min(M + 127, M + W - 1)) / 64 + 1;
+      nsplit = std::min(f, nks_min);
+    }
     float* part_o = nullptr;
     float* part_lse = nullptr;
     int* part_cnt = nullptr;

@@ -756,37 +756,29 @@ __global__ void __launch_bounds__(kThreads, 1)
             __threadfence();
             // weights 2^(lse_c - max) of the chunks (lse -inf: no visible key),
             // summed in chunk order whichever chunk merges (the result does
-            // not depend on which finished last); this chunk's own result is
-            // taken from registers, the same values it stored.
+            // not depend on which finished last).  Every chunk's rows, this
+            // one's included, are read back from the scratch, so that its
+            // result registers are dead here.
             const size_t it0 = static_cast<size_t>(unit) * kSplit;
-            const int own = static_cast<int>(it - it0);
-            float mx = lse2;
-            for (int c = 0; c < kSplit; ++c)
-              if (c != own) mx = fmaxf(mx, p.part_lse[(it0 + c) * BM + a]);
+            float mx = -INFINITY;
+            for (int c = 0; c < kSplit; ++c) mx = fmaxf(mx, p.part_lse[(it0 + c) * BM + a]);
             float wsum = 0.f;
             float acc[D];
 #pragma unroll
             for (int n = 0; n < D; ++n) acc[n] = 0.f;
             for (int c = 0; c < kSplit; ++c) {
-              const float l2 = c == own ? lse2 : p.part_lse[(it0 + c) * BM + a];
+              const float l2 = p.part_lse[(it0 + c) * BM + a];
               if (l2 == -INFINITY) continue;
               const float wt = ex2(l2 - mx);
               wsum += wt;
-              if (c == own) {
+              const float4* src = reinterpret_cast<const float4*>(p.part_o + ((it0 + c) * BM + a) * D);
 #pragma unroll
-                for (int n = 0; n < D; ++n) acc[n] = fmaf(wt, ov[n], acc[n]);
-              } else {
-                const float4* src = reinterpret_cast<const float4*>(p.part_o + ((it0 + c) * BM + a) * D);
-                float4 x4[D / 4];
-#pragma unroll
-                for (int q4 = 0; q4 < D / 4; ++q4) x4[q4] = src[q4];
-#pragma unroll
-                for (int q4 = 0; q4 < D / 4; ++q4) {
-                  acc[4 * q4] = fmaf(wt, x4[q4].x, acc[4 * q4]);
-                  acc[4 * q4 + 1] = fmaf(wt, x4[q4].y, acc[4 * q4 + 1]);
-                  acc[4 * q4 + 2] = fmaf(wt, x4[q4].z, acc[4 * q4 + 2]);
-                  acc[4 * q4 + 3] = fmaf(wt, x4[q4].w, acc[4 * q4 + 3]);
-                }
+              for (int q4 = 0; q4 < D / 4; ++q4) {
+                const float4 x = src[q4];
+                acc[4 * q4] = fmaf(wt, x.x, acc[4 * q4]);
+                acc[4 * q4 + 1] = fmaf(wt, x.y, acc[4 * q4 + 1]);
+                acc[4 * q4 + 2] = fmaf(wt, x.z, acc[4 * q4 + 2]);
+                acc[4 * q4 + 3] = fmaf(wt, x.w, acc[4 * q4 + 3]);
               }
             }
             if (i < p.W) {
