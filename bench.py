@@ -577,6 +577,8 @@ def measure_layer(device, steps, warmup, peak, peak_src):
     w = make_layer_weights(d, H, D, LAYER_D_FF)
     dw = {k: torch.from_numpy(v).to(device).to(torch.bfloat16 if k.startswith("W_") else torch.float32)
           for k, v in w.items()}
+    qkv = torch.stack([dw["W_q"], dw["W_k"], dw["W_v"]])  # packed: one batched projection GEMM
+    dw["W_q"], dw["W_k"], dw["W_v"] = qkv[0], qkv[1], qkv[2]
     g = torch.Generator(device=device).manual_seed(0)
     h = torch.randn(B, W, d, device=device, generator=g).to(torch.bfloat16)
     out = torch.empty_like(h)
@@ -606,10 +608,11 @@ def measure_layer(device, steps, warmup, peak, peak_src):
     ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
     flops = layer_flops(B, W, M, d, H, D, LAYER_D_FF)
     tf = flops / (ms / 1e3) / 1e12
-    return {"call": "txl_layer_forward (q/k/v/r/o/FFN GEMMs on cuBLASLt; attention, normalisations, bias+ReLU "
-                    "and the memory append in this library's kernels)",
+    return {"call": "txl_layer_forward (GEMMs on cuBLASLt: q/k/v as one batched GEMM over packed weights, r, o, "
+                    "and the FFN with b_1 + ReLU and b_2 in their epilogues; attention, normalisations and the "
+                    "memory append in this library's kernels)",
             "workload": f"base segment through one layer: B={B} W={W} M={M} d_model={d} H={H} D={D} "
-                        f"d_ff={LAYER_D_FF}, memory a ring of M+W projected rows",
+                        f"d_ff={LAYER_D_FF}, memory a ring of M+W projected rows, W_q/W_k/W_v packed",
             "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "calls": len(ts),
             "tflops": tf, "frac_of_bf16_peak": tf / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
             "per_call_work": f"{flops} counted flops (GEMMs + the attention's 6*B*H*D*(W*M + W(W+1)/2))",

@@ -39,7 +39,7 @@
 extern "C" {
 #endif
 
-#define TXL_VERSION 140 /* 1.4.0 */
+#define TXL_VERSION 150 /* 1.5.0 */
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)
@@ -287,7 +287,13 @@ TXL_API int txl_mem_ring_append(void* mem, int cap, int start, int m, const void
  *   D          64 or 128; d_model and d_ff multiples of 8, d_model <= 1024
  *
  * The GEMMs are plain library GEMMs (cuBLASLt, bf16 in, fp32 accumulation,
- * bf16 out); every other step runs in this library's kernels.
+ * bf16 out).  b_1 with the ReLU, and b_2, ride in the feed-forward GEMMs'
+ * epilogues, rounded to bf16 (the bias type cuBLASLt's bias epilogues take)
+ * and added to the fp32 accumulator, where cuBLASLt has them for the shape;
+ * else this library's kernels add the fp32 vectors to the rounded
+ * products.  When W_k starts right after W_q and W_v right after W_k (one
+ * [3, d_model, H*D] allocation), the three projections run as one batched
+ * GEMM.  Every other step runs in this library's kernels.
  */
 typedef struct {
   const void* W_q;        /* [d_model, H*D] */
@@ -413,6 +419,10 @@ TXL_API int txl_debug_inject_stall(int on);
  * key steps into min(nsplit, steps of the shortest unit) chunks instead of
  * the count its cost model picks; 0 restores the model. */
 TXL_API int txl_debug_force_split(int nsplit);
+/* Test hook: on != 0 makes txl_layer_forward add b_1 (with the ReLU) and
+ * b_2 in this library's own kernels after plain GEMMs instead of in the
+ * GEMMs' epilogues; 0 restores the epilogues. */
+TXL_API int txl_debug_force_bias_kernels(int on);
 
 #ifdef __cplusplus
 }

@@ -36,11 +36,16 @@ def txl():
     return lib
 
 
-def _weights(d, H, D, dff, layer=0):
+def _weights(d, H, D, dff, layer=0, packed=False):
+    """Oracle and device weights; packed puts W_q, W_k, W_v back to back in
+    one [3, d, H*D] allocation (the layer's batched-projection path)."""
     w = make_layer_weights(d, H, D, dff, seed=3, layer=layer)
     P = {ORACLE_NAMES[k]: v.astype(np.float64) for k, v in w.items()}
     dw = {k: torch.from_numpy(v).to(dev()).to(torch.bfloat16 if k.startswith("W_") else torch.float32).contiguous()
           for k, v in w.items()}
+    if packed:
+        qkv = torch.stack([dw["W_q"], dw["W_k"], dw["W_v"]])
+        dw["W_q"], dw["W_k"], dw["W_v"] = qkv[0], qkv[1], qkv[2]
     return P, dw
 
 
@@ -53,14 +58,17 @@ def _close(got, want, what):
     return rel
 
 
-@pytest.mark.parametrize("B,W,M,H,D,dff", [
-    (2, 128, 128, 4, 64, 1024),   # ring of M+W rows: the append runs inside the attention kernel
-    (1, 96, 40, 2, 64, 256),      # memory and segment off the tile grid
-    (2, 64, 0, 2, 128, 512),      # first segment, D = 128
+@pytest.mark.parametrize("B,W,M,H,D,dff,bias_kernels,packed", [
+    (2, 128, 128, 4, 64, 1024, False, False),  # ring of M+W rows: the append runs inside the attention kernel
+    (2, 128, 128, 4, 64, 1024, True, False),   # the same, the FFN biases by the library's kernels
+    (2, 128, 128, 4, 64, 1024, False, True),   # the same, q/k/v projections as one batched GEMM
+    (1, 72, 40, 2, 64, 256, False, True),      # memory, segment and rows (72) off the tile grids
+    (2, 64, 0, 2, 128, 512, False, False),     # first segment, D = 128
+    (3, 64, 64, 16, 64, 128, True, True),      # d_model = 1024, the widest normalisation
 ])
-def test_layer_matches_oracle(txl, B, W, M, H, D, dff):
+def test_layer_matches_oracle(txl, B, W, M, H, D, dff, bias_kernels, packed):
     d = H * D
-    P, dw = _weights(d, H, D, dff)
+    P, dw = _weights(d, H, D, dff, packed=packed)
     rng = np.random.default_rng(B * 1000 + W + M)
     h = round_bf16(rng.standard_normal((B, W, d)).astype(np.float32)).astype(np.float64)
     mem = round_bf16(rng.standard_normal((B, M, d)).astype(np.float32)).astype(np.float64)
@@ -79,7 +87,11 @@ def test_layer_matches_oracle(txl, B, W, M, H, D, dff):
     Rd = torch.from_numpy(R).to(dev()).to(torch.bfloat16)
     out = torch.empty_like(hd)
     ws = torch.empty(txl.txl_layer_workspace_bytes(B, W, d, H, D, dff, n_r), device=dev(), dtype=torch.uint8)
-    s2, m2 = txl.txl_layer_forward(hd, out, k_ring, v_ring, start, M, dw, Rd, ws)
+    txl.txl_debug_force_bias_kernels(bias_kernels)
+    try:
+        s2, m2 = txl.txl_layer_forward(hd, out, k_ring, v_ring, start, M, dw, Rd, ws)
+    finally:
+        txl.txl_debug_force_bias_kernels(False)
     assert txl.txl_get_device_status() == 0
     assert (s2, m2) == (0, M + W)
     want = O.layer_forward(h, None, P, R.astype(np.float64), H, mem_kv=(k_mem, v_mem))

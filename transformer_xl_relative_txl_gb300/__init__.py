@@ -23,6 +23,7 @@ __all__ = [
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall", "txl_debug_force_split",
+    "txl_debug_force_bias_kernels",
 ]
 
 TXL_F32 = 0
@@ -84,6 +85,8 @@ lib.txl_debug_inject_stall.argtypes = [_i]
 lib.txl_debug_inject_stall.restype = _i
 lib.txl_debug_force_split.argtypes = [_i]
 lib.txl_debug_force_split.restype = _i
+lib.txl_debug_force_bias_kernels.argtypes = [_i]
+lib.txl_debug_force_bias_kernels.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -428,3 +431,8 @@ def txl_debug_force_split(nsplit):
     """Test hook: force the D = 64 forward's split count (0: its cost model)."""
     _check(lib.txl_debug_force_split(int(nsplit)), "txl_debug_force_split")
 
+
+def txl_debug_force_bias_kernels(on):
+    """Test hook: the layer's b_1 + ReLU and b_2 by this library's kernels
+    instead of the GEMM epilogues (False restores the epilogues)."""
+    _check(lib.txl_debug_force_bias_kernels(1 if on else 0), "txl_debug_force_bias_kernels")

@@ -26,6 +26,7 @@ __device__ unsigned int g_txl_status;
 std::atomic<unsigned long long> g_wait_ns{2000000000ULL};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_split{0};  // test hook: > 0 forces the D = 64 kernel's split count
+std::atomic<int> g_force_bias_kernels{0};  // test hook: the layer's b_1 + ReLU and b_2 by this library's kernels
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -220,6 +221,11 @@ int txl_debug_inject_stall(int on) {
 int txl_debug_force_split(int nsplit) {
   if (nsplit < 0 || nsplit > 64) return TXL_ERR_INVALID_ARG;
   g_force_split.store(nsplit);
+  return TXL_OK;
+}
+
+int txl_debug_force_bias_kernels(int on) {
+  g_force_bias_kernels.store(on ? 1 : 0);
   return TXL_OK;
 }
 
@@ -870,7 +876,8 @@ size_t txl_layer_workspace_bytes(int B, int W, int d_model, int H, int D, int d_
   if (B <= 0 || W <= 0 || d_model <= 0 || H <= 0 || D <= 0 || d_ff <= 0 || n_r <= 0) return 0;
   const size_t bw = static_cast<size_t>(B) * W, hd = static_cast<size_t>(H) * D;
   return kGemmWs + 4 * align256(bw * hd * 2) + align256(static_cast<size_t>(n_r) * hd * 2) +
-         3 * align256(bw * d_model * 2) + align256(bw * d_ff * 2);
+         3 * align256(bw * d_model * 2) + align256(bw * d_ff * 2) + align256(static_cast<size_t>(d_ff) * 2) +
+         align256(static_cast<size_t>(d_model) * 2);
 }
 
 int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int cap, int start, int M,
@@ -907,24 +914,49 @@ int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int ca
   void* x = take(bw * d_model * 2);
   void* z = take(bw * d_model * 2);
   void* f = take(bw * d_ff * 2);
+  void* b1h = take(static_cast<size_t>(d_ff) * 2);     // b_1 in bf16, for the FFN GEMMs' epilogues
+  void* b2h = take(static_cast<size_t>(d_model) * 2);  // b_2 in bf16
   const int rows = static_cast<int>(bw);
   const int HD = static_cast<int>(hd);
-  if (txl::gemm_bf16(h, w->W_q, q, rows, HD, d_model, gws, kGemmWs, stream) ||
-      txl::gemm_bf16(h, w->W_k, ks, rows, HD, d_model, gws, kGemmWs, stream) ||
-      txl::gemm_bf16(h, w->W_v, vs, rows, HD, d_model, gws, kGemmWs, stream) ||
-      txl::gemm_bf16(R, w->W_r, r, n_r, HD, d_model, gws, kGemmWs, stream))
+  // W_q, W_k, W_v packed back to back: the three projections as one batched GEMM
+  const size_t wbytes = static_cast<size_t>(d_model) * hd * 2;
+  const bool packed = static_cast<const char*>(w->W_k) == static_cast<const char*>(w->W_q) + wbytes &&
+                      static_cast<const char*>(w->W_v) == static_cast<const char*>(w->W_k) + wbytes;
+  const long long qkv_stride = static_cast<long long>((static_cast<char*>(ks) - static_cast<char*>(q)) / 2);
+  if (packed) {
+    if (txl::gemm_bf16_batched(h, w->W_q, q, rows, HD, d_model, 3, qkv_stride, gws, kGemmWs, stream))
+      return TXL_ERR_CUDA;
+  } else if (txl::gemm_bf16(h, w->W_q, q, rows, HD, d_model, gws, kGemmWs, stream) ||
+             txl::gemm_bf16(h, w->W_k, ks, rows, HD, d_model, gws, kGemmWs, stream) ||
+             txl::gemm_bf16(h, w->W_v, vs, rows, HD, d_model, gws, kGemmWs, stream)) {
     return TXL_ERR_CUDA;
+  }
+  if (txl::gemm_bf16(R, w->W_r, r, n_r, HD, d_model, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
   int st = txl_relattn_forward_ring_append(k_mem, v_mem, cap, start, M, q, ks, vs, r, w->bias_u, w->bias_v, a,
                                            nullptr, B, W, H, D, n_r, scale, TXL_BF16, TXL_BF16, start_out, m_out,
                                            stream);
   if (st != TXL_OK) return st;
   if (txl::gemm_bf16(a, w->W_o, y, rows, d_model, HD, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
-  if (txl::launch_add_ln(h, y, nullptr, w->ln1_gamma, w->ln1_beta, x, rows, d_model, stream) != cudaSuccess)
+  // b_1 + ReLU and b_2 go in the FFN GEMMs' epilogues (bf16 biases, rounded by the first
+  // normalisation's side jobs) where cuBLASLt has them, else in this library's kernels (fp32).
+  const bool epi = g_force_bias_kernels.load() == 0;
+  txl::CvtJobs cvt;
+  if (epi) {
+    cvt.src[0] = w->b_1, cvt.dst[0] = static_cast<__nv_bfloat16*>(b1h), cvt.n[0] = d_ff;
+    cvt.src[1] = w->b_2, cvt.dst[1] = static_cast<__nv_bfloat16*>(b2h), cvt.n[1] = d_model;
+  }
+  if (txl::launch_add_ln(h, y, nullptr, w->ln1_gamma, w->ln1_beta, x, rows, d_model, stream, cvt) != cudaSuccess)
     return TXL_ERR_CUDA;
-  if (txl::gemm_bf16(x, w->W_1, f, rows, d_ff, d_model, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
-  if (txl::launch_bias_relu(f, w->b_1, rows, d_ff, stream) != cudaSuccess) return TXL_ERR_CUDA;
-  if (txl::gemm_bf16(f, w->W_2, z, rows, d_model, d_ff, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
-  if (txl::launch_add_ln(x, z, w->b_2, w->ln2_gamma, w->ln2_beta, out, rows, d_model, stream) != cudaSuccess)
+  int e = epi ? txl::gemm_bf16(x, w->W_1, f, rows, d_ff, d_model, gws, kGemmWs, stream, b1h, true) : 2;
+  if (e == 1) return TXL_ERR_CUDA;
+  if (e == 2 && (txl::gemm_bf16(x, w->W_1, f, rows, d_ff, d_model, gws, kGemmWs, stream) ||
+                 txl::launch_bias_relu(f, w->b_1, rows, d_ff, stream) != cudaSuccess))
+    return TXL_ERR_CUDA;
+  e = epi ? txl::gemm_bf16(f, w->W_2, z, rows, d_model, d_ff, gws, kGemmWs, stream, b2h, false) : 2;
+  if (e == 1) return TXL_ERR_CUDA;
+  if (e == 2 && txl::gemm_bf16(f, w->W_2, z, rows, d_model, d_ff, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
+  if (txl::launch_add_ln(x, z, e == 2 ? w->b_2 : nullptr, w->ln2_gamma, w->ln2_beta, out, rows, d_model, stream) !=
+      cudaSuccess)
     return TXL_ERR_CUDA;
   return TXL_OK;
 }
