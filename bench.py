@@ -694,6 +694,12 @@ def run_ours(args):
     stream = SegmentStream(wl, device, seed=rank)
     cs = torch.cuda.current_stream()
 
+    # the clock sampler starts first, so the warm-up runs right before the
+    # timed region: a GPU left idle in between (0.3 s) ran the first timed
+    # step at half speed (163 against 76 us)
+    sampler = ClockSampler(gpu_uuid(local))
+    sampler.start()
+    time.sleep(0.3)
     for t in range(args.warmup):
         stream.step(t)
     torch.cuda.synchronize()
@@ -701,15 +707,19 @@ def run_ours(args):
         raise RuntimeError("device status reported a timed-out wait during warm-up")
 
     K = args.steps
-    # the attention kernel is bracketed by events on every EVENT_EVERY-th
-    # step only: an event pair between kernels costs a few microseconds of
-    # stream serialisation, which would otherwise be charged to every step
+    # the attention kernel is bracketed by events on the last step of every
+    # EVENT_EVERY only: an event pair between kernels costs a few
+    # microseconds of stream serialisation, which would otherwise be charged
+    # to every step; and the timed region's first step starts on an idle
+    # queue, where the first event would also time the host's launch of it
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(0, K, EVENT_EVERY)]
+           for _ in range(max(1, K // EVENT_EVERY))]
+
+    def sampled(t):  # the event pair of timed step t, or None
+        if t % EVENT_EVERY == EVENT_EVERY - 1:
+            return evs[t // EVENT_EVERY]
+        return evs[0] if K < EVENT_EVERY and t == K - 1 else None
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(gpu_uuid(local))
-    sampler.start()
-    time.sleep(0.3)
     launches = 0
     barrier(world)
     torch.cuda.synchronize()
@@ -717,7 +727,7 @@ def run_ours(args):
     start.record(cs)
     stream.table_stream.wait_stream(cs)
     for t in range(K):
-        launches += stream.step(args.warmup + t, evs[t // EVENT_EVERY] if t % EVENT_EVERY == 0 else None)
+        launches += stream.step(args.warmup + t, sampled(t))
     cs.wait_stream(stream.table_stream)
     end.record(cs)
     torch.cuda.synchronize()
@@ -761,8 +771,9 @@ def run_ours(args):
                    "step": "txl_sinusoid_rel (on a stream of its own: no kernel of the step reads the table) "
                            "+ txl_relattn_forward_roll (attention and the memory roll of k and v in one kernel); "
                            "the timed region waits for both streams",
-                   "kernel_timing": f"attention kernel bracketed by CUDA events on every {EVENT_EVERY}th "
-                                    f"timed step ({len(evs)} samples)"},
+                   "kernel_timing": f"attention kernel bracketed by CUDA events on the last timed step of "
+                                    f"every {EVENT_EVERY} ({len(evs)} samples; the first step, launched onto "
+                                    f"an idle queue, is not sampled)"},
         "tflops": achieved,
         "attn_ms": k1_ms,
         "roofline": {"kernel": "relattn_tc64_kernel", "bound": "tensor", "achieved": achieved, "peak": peak,

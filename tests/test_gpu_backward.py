@@ -115,8 +115,9 @@ def test_backward_custom_scale(txl):
 @pytest.mark.parametrize("dtype,o_dtype", [("bf16", "f32"), ("f32", "f32"), ("bf16", "bf16")])
 def test_backward_deterministic(txl, dtype, o_dtype):
     """Bit-identical on repeated calls, except dr on the tensor-core path
-    (bf16 o and dout, D = 64), whose slot sums arrive by fp32 atomics in any
-    order: there the two results agree to fp32 rounding."""
+    (bf16 o and dout, D = 64), whose slot sums arrive by atomic fp32 adds
+    (TMA bulk reductions) in any order: there the two results agree to fp32
+    rounding."""
     q, k, v, r, bu, bv, dout = _case(2, 2, 64, 130, 70, dtype)
     a = _run(txl, q, k, v, r, bu, bv, dout, 70, dtype, o_dtype=o_dtype)
     b = _run(txl, q, k, v, r, bu, bv, dout, 70, dtype, o_dtype=o_dtype)

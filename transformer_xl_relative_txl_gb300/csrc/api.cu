@@ -598,13 +598,26 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
       const cuuint32_t box[3] = {64, 1, 192};
       if (!encode_bf16(&tm_rw, r, 3, dims, strides, box)) return TXL_ERR_CUDA;
     }
+    CUtensorMap tm_dr;  // fp32 [n_r, H, D]: boxes of 64 distances x 32 dims of one head, for the TMA reductions
+    {
+      const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                                  static_cast<cuuint64_t>(n_r)};
+      const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 4, hd * 4};
+      const cuuint32_t box[3] = {32, 1, 64};
+      const cuuint32_t estr[3] = {1, 1, 1};
+      if (encode(&tm_dr, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, dr, dims, strides, box, estr,
+                 CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return TXL_ERR_CUDA;
+    }
     txl::WaitCtl wc;
     if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
     wc.limit_ns = g_wait_ns.load();
     wc.inject_stall = 0;
     const long long nqt = (W + 127) / 128;
     if (nqt * B * H > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
-    return from_cuda(txl::launch_relattn_bwd_tc64(tm_q, tm_k, tm_v, tm_rw, tm_do, bias_u, bias_v, lse, o, dout, dq,
+    return from_cuda(txl::launch_relattn_bwd_tc64(tm_q, tm_k, tm_v, tm_rw, tm_do, tm_dr, bias_u, bias_v, lse, o,
+                                                  dout, dq,
                                                   dk, dv, dr, dbias_u, dbias_v, B, W, M, H, n_r, scale, scratch, wc,
                                                   stream));
   }

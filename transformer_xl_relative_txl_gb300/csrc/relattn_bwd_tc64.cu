@@ -13,7 +13,9 @@
 //     skewed into distance order (Gs: row i, column d = M+i-j).  A distance
 //     slot of 64 rows receives its last values two steps after its first;
 //     then d(q+v) += Gs R and dr += Gs^T (q+v) (an M = 64 MMA) run on it, and
-//     the slot's dr rows are added to the output with fp32 vector atomics.
+//     the slot's dr rows are staged in shared memory and added to the output
+//     by one TMA bulk reduction (fp32 vector atomics for a slot that starts
+//     below distance 0).
 //   dk/dv kernel, one CTA per 64 segment keys of a (batch, head), looping
 //     over the 128-query tiles that see them: the same three MMAs and the
 //     same p, g; then dV += P^T dout and dK += G^T (q+u) with P and G read
@@ -59,7 +61,8 @@ constexpr int kQOffV = kQOffK + 2 * kKTile;      // 2 stages
 constexpr int kQOffR = kQOffV + 2 * kKTile;      // 2 stages
 constexpr int kQOffG = kQOffR + 2 * kWinTile;    // G in key order (also the raw q tile at the start)
 constexpr int kQOffGs = kQOffG + kTile;          // 4 distance slots
-constexpr int kQOffBar = kQOffGs + 4 * kTile;
+constexpr int kQOffDr = kQOffGs + 4 * kTile;     // a finished slot's dr rows: 2 boxes [64][32] fp32, 128B-swizzled
+constexpr int kQOffBar = kQOffDr + BN * D * 4;
 constexpr int kQOffBias = kQOffBar + 256;        // u, then v of the head (fp32)
 constexpr int kQSmem = kQOffBias + 2 * 64 * 4 + 1024;
 static_assert(kQSmem <= 232448, "shared memory budget");
@@ -224,7 +227,8 @@ __device__ __forceinline__ void store_row_half(uint8_t* tile, int a, int half, c
 __global__ void __launch_bounds__(kQThreads, 1)
     bwd_dq_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
-                       const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                       const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dr,
+                       const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -238,6 +242,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* sGs = smem + kQOffGs;
   QBars* bars = reinterpret_cast<QBars*>(smem + kQOffBar);
   float* sBias = reinterpret_cast<float*>(smem + kQOffBias);
+  uint8_t* sDr = smem + kQOffDr;
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
@@ -294,6 +299,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_rw);
     tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dr);
     mbar_arrive_expect_tx(&bars->q, 2 * kTile);
     tma_load_4d(sG, &tm_q, &bars->q, 0, w.h, w.i0, w.b);  // raw q, into the G tile for now
     tma_load_4d(sDO, &tm_do, &bars->q, 0, w.h, w.i0, w.b);
@@ -360,30 +366,67 @@ __global__ void __launch_bounds__(kQThreads, 1)
     for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColDr, dGsT + 128 * kk, dQvMN + 128 * kk, idT, kk > 0);
     ++n_slot;
   };
-  // Everyone: add the dr rows of slot tau (TMEM, M = 64 layout: row
-  // 16 quad + lane in lanes 0-15 of each quadrant) to the output; this warp
-  // takes head dims [32 half, 32 half + 32).
-  auto flush_dr = [&](int tau) {
+  // Everyone: the dr rows of slot tau (TMEM, M = 64 layout: row 16 quad +
+  // lane in lanes 0-15 of each quadrant; this warp takes head dims
+  // [32 half, 32 half + 32)), distance rows d0 .. d0 + 63.  A slot that starts
+  // at d0 >= 0 is staged in sDr, box `half` holding dims [32 half, +32) as 64
+  // rows of 128 bytes with 16-byte chunk c of row r at chunk c ^ (r & 7) (the
+  // TMA's 128-byte swizzle: two lanes a bank group), for two TMA reductions
+  // that thread 0 issues after the next block barrier; rows past the tensor
+  // are dropped by the TMA, and rows from M+W on hold zeros (no query row
+  // reaches them).  A slot that straddles distance 0 adds its rows d >= 0
+  // with vector atomics.  Returns whether reductions are pending.
+  auto stage_dr = [&](int tau) -> bool {
+    const int d0 = p.M + w.i0 - BN * tau - BN;
+    if (d0 + BN <= 0) return false;
     uint32_t v[32];
     tmem_ld32(tmem + (static_cast<uint32_t>(quad * 32) << 16) + kColDr + 32 * half, v);
     tmem_wait_ld(v);
-    const int d = p.M + w.i0 - BN * tau - BN + 16 * quad + lane;
-    if (lane < 16 && d >= 0 && d < L) {
-      float* dst = p.dr + (static_cast<long long>(d) * p.H + w.h) * D + 32 * half;
+    const int rr = 16 * quad + lane;
+    const int d = d0 + rr;
+    if (d0 < 0) {
+      if (lane < 16 && d >= 0 && d < L) {
+        float* dst = p.dr + (static_cast<long long>(d) * p.H + w.h) * D + 32 * half;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) red_add_v4(dst + 4 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+        for (int e = 0; e < 8; ++e) red_add_v4(dst + 4 * e, v[4 * e], v[4 * e + 1], v[4 * e + 2], v[4 * e + 3]);
+      }
+      return false;
     }
+    if (lane < 16) {
+      uint8_t* row = sDr + half * (BN * 128) + rr * 128;
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        *reinterpret_cast<uint4*>(row + ((e ^ (rr & 7)) << 4)) = make_uint4(v[4 * e], v[4 * e + 1], v[4 * e + 2],
+                                                                             v[4 * e + 3]);
+    }
+    fence_proxy_async_smem();
+    return true;
+  };
+  int dr_d0 = -1;  // distance row of the staged slot awaiting its reduction (-1: none)
+  // Thread 0, after a block barrier that follows the staging: the reduction.
+  auto issue_dr = [&]() {
+    if (dr_d0 >= 0) {
+      tma_reduce_add_3d(&tm_dr, sDr, 0, w.h, dr_d0);
+      tma_reduce_add_3d(&tm_dr, sDr + BN * 128, 32, w.h, dr_d0);
+      bulk_commit_group();
+    }
+    dr_d0 = -1;
+  };
+  auto flush_dr = [&](int tau) {
+    if (stage_dr(tau)) dr_d0 = p.M + w.i0 - BN * tau - BN;
   };
 
   if (tid == 0 && ok && !score_mmas(0)) report_timeout(abort, p.status);
   for (int t = 0; t < T && ok; ++t) {
     const int s = t & 1;
-    // (1) everyone: the step's gradients into G (key order) and the slots.
+    // (1) everyone: the step's gradients into G (key order) and the slots;
+    // thread 0 hands the slot staged at the end of the last step to the TMA.
     ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
+    if (tid == 0) issue_dr();
     tc_fence_after();
     {
       float g[32], pr[32];
@@ -417,7 +460,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       tc_commit(&bars->m2);
     }
     // (3) everyone: flush the slot's dr rows; the slot's buffer is free again
-    // and becomes slot t+2; thread 0 refills this step's load stage.
+    // and becomes slot t+2; thread 0 refills this step's load stage.  sDr is
+    // free once the last reduction has read it (thread 0 waits before the
+    // barrier).
+    if (tid == 0) bulk_wait_group_read0();
     ok = mbar_wait(&bars->m2, n_m2 & 1, wait_ns, abort);
     ++n_m2;
     if (!__syncthreads_and(ok)) {
@@ -442,6 +488,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       slot_mmas(tau, (T - 1) & 1, T - 1 - tau);
       tc_commit(&bars->m2);
     }
+    if (tid == 0) {
+      issue_dr();
+      bulk_wait_group_read0();
+    }
     ok = mbar_wait(&bars->m2, n_m2 & 1, wait_ns, abort);
     ++n_m2;
     if (!__syncthreads_and(ok)) {
@@ -458,6 +508,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     // sums of both go to the bias partials through shared memory
     // (XOR-staggered columns).
     __syncthreads();  // the slot buffers are free for the column sums
+    if (tid == 0) issue_dr();
     uint32_t u[32], v[32];
     const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     tmem_ld32(lb + kColA + 32 * half, u);
@@ -489,8 +540,10 @@ __global__ void __launch_bounds__(kQThreads, 1)
       p.part[((static_cast<long long>(w.b) * p.nqt + qt) * p.H + w.h) * 2 * D + tid] = sum;
     }
   }
-  // Let this CTA's own copies and MMAs finish before the memory is released.
+  // Let this CTA's own copies, reductions and MMAs finish before the memory
+  // is released.
   if (tid == 0) {
+    bulk_wait_group0();
     for (int s = 0; s < 2; ++s)
       if (n_ld[s] > 0) mbar_wait_own(&bars->kv[s], (n_ld[s] - 1) & 1, wait_ns);
     for (int s = 0; s < 2; ++s)
@@ -735,7 +788,8 @@ size_t relattn_bwd_tc64_scratch_bytes(int B, int W, int H) {
 }
 
 cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                    const CUtensorMap& tm_rw, const CUtensorMap& tm_do, const float* bias_u,
+                                    const CUtensorMap& tm_rw, const CUtensorMap& tm_do, const CUtensorMap& tm_dr,
+                                    const float* bias_u,
                                     const float* bias_v, const float* lse, const void* o, const void* dout,
                                     float* dq, float* dk, float* dv, float* dr, float* du, float* dvb, int B,
                                     int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
@@ -772,7 +826,7 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   if ((e = cudaMemsetAsync(dr, 0, sizeof(float) * static_cast<size_t>(n_r) * H * D, stream)) != cudaSuccess)
     return e;
   const int units = p.nqt * B * H;
-  bwd_dq_tc64_kernel<<<units, kQThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
+  bwd_dq_tc64_kernel<<<units, kQThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, tm_dr, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int nkb = (W + BN - 1) / BN;
   bwd_dkdv_tc64_kernel<<<nkb * B * H, kQThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);

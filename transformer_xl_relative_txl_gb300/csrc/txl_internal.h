@@ -99,7 +99,8 @@ cudaError_t launch_bwd_bias(const float* part, int n_part, int H, int D, float* 
 // scratch: relattn_bwd_tc64_scratch_bytes(B, W, H) bytes.
 size_t relattn_bwd_tc64_scratch_bytes(int B, int W, int H);
 cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                                    const CUtensorMap& tm_rw, const CUtensorMap& tm_do, const float* bias_u,
+                                    const CUtensorMap& tm_rw, const CUtensorMap& tm_do, const CUtensorMap& tm_dr,
+                                    const float* bias_u,
                                     const float* bias_v, const float* lse, const void* o, const void* dout,
                                     float* dq, float* dk, float* dv, float* dr, float* du, float* dvb, int B,
                                     int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
