@@ -104,6 +104,35 @@ def test_layer_matches_oracle(txl, B, W, M, H, D, dff, bias_kernels, packed):
     assert torch.equal(k_ring[:, :M].cpu(), torch.from_numpy(k_mem).to(torch.bfloat16))  # memory untouched
 
 
+def test_layer_base_size(txl):
+    """The layer at the bench's shapes (B=22 W=512 M=512, 8 heads of 64,
+    d_ff=2048, packed projections, a ring of M+W rows) in one call, against
+    the oracle's layer on every output row."""
+    B, W, M, H, D, dff = 22, 512, 512, 8, 64, 2048
+    d = H * D
+    P, dw = _weights(d, H, D, dff, packed=True)
+    rng = np.random.default_rng(11)
+    h = round_bf16(rng.standard_normal((B, W, d)).astype(np.float32)).astype(np.float64)
+    mem = round_bf16(rng.standard_normal((B, M, d)).astype(np.float32)).astype(np.float64)
+    k_mem = round_bf16((mem @ P["WkE"]).astype(np.float32)).reshape(B, M, H, D)
+    v_mem = round_bf16((mem @ P["Wv"]).astype(np.float32)).reshape(B, M, H, D)
+    n_r = M + W
+    R = round_bf16(O.sinusoid_rel(n_r, d).astype(np.float32))
+    cap = M + W
+    k_ring = torch.zeros(B, cap, H, D, device=dev(), dtype=torch.bfloat16)
+    v_ring = torch.zeros_like(k_ring)
+    k_ring[:, :M] = torch.from_numpy(k_mem).to(dev()).to(torch.bfloat16)
+    v_ring[:, :M] = torch.from_numpy(v_mem).to(dev()).to(torch.bfloat16)
+    hd = torch.from_numpy(h.astype(np.float32)).to(dev()).to(torch.bfloat16)
+    Rd = torch.from_numpy(R).to(dev()).to(torch.bfloat16)
+    out = torch.empty_like(hd)
+    ws = torch.empty(txl.txl_layer_workspace_bytes(B, W, d, H, D, dff, n_r), device=dev(), dtype=torch.uint8)
+    assert txl.txl_layer_forward(hd, out, k_ring, v_ring, 0, M, dw, Rd, ws) == (0, M + W)
+    assert txl.txl_get_device_status() == 0
+    want = O.layer_forward(h, None, P, R.astype(np.float64), H, mem_kv=(k_mem, v_mem))
+    _close(out.float().cpu().numpy(), want, "layer output at base size")
+
+
 def test_stack_matches_oracle(txl):
     """Two layers over four segments (B=2, W=64, M=64, d=128): each layer
     keeps its own rings (M+W rows) and reads the last M of them; every

@@ -78,8 +78,8 @@ constexpr int kKOffR = kKOffDO + 2 * kTile;      // 2 stages
 constexpr int kKOffP = kKOffR + 2 * kWinTile;
 constexpr int kKOffG = kKOffP + kTile;
 constexpr int kKOffBar = kKOffG + kTile;
-constexpr int kKOffBias = kKOffBar + 256;        // u, then v of the head (fp32)
-constexpr int kKSmem = kKOffBias + 2 * 64 * 4 + 1024;
+constexpr int kKOffBias = kKOffBar + 256;        // per item parity: u, then v of the item's head (fp32)
+constexpr int kKSmem = kKOffBias + 2 * 2 * 64 * 4 + 1024;
 static_assert(kKSmem <= 232448, "shared memory budget");
 
 struct BwdParams {
@@ -562,14 +562,43 @@ __global__ void __launch_bounds__(kQThreads, 1)
 }
 
 // ============================================================================
-// dk / dv kernel: 8 warps as in the dq kernel.  (q+u), (q+v) of the next
-// query tile are built while the current tile's gradient MMAs run, and that
-// tile's score MMAs are issued right behind them.
+// dk / dv kernel: 8 warps as in the dq kernel, persistent.  An item is a
+// block of 64 segment keys of a (batch, head) with the query tiles that see
+// them; items are ordered longest first (the key block varies slowest) and
+// dealt to the CTAs in a snake order.  A CTA walks one stream of query tiles
+// across its items, so its barriers, TMEM and load pipeline carry from item
+// to item: the next item's keys and values load as soon as the last tile's
+// score MMAs have read the current ones, and its first score MMAs are
+// issued behind the last tile's gradient MMAs.  (q+u), (q+v) of the next
+// tile are built while the current tile's gradient MMAs run.
 // ============================================================================
+struct KItem {
+  int b, h, jj0, qt0, nt;  // keys jj0 .. jj0+63; query tiles qt0 .. qt0+nt-1
+};
+
+__device__ __forceinline__ KItem kitem(int it, int B, int H, int nqt) {
+  const int BH = B * H;
+  const int bh = it % BH;
+  KItem r;
+  r.b = bh / H;
+  r.h = bh % H;
+  r.jj0 = (it / BH) * BN;
+  r.qt0 = r.jj0 / BM;  // first query tile with a row i >= jj0
+  r.nt = nqt - r.qt0;
+  return r;
+}
+
+// Position in a CTA's tile stream: its k-th item and that item's s-th tile.
+struct KPos {
+  int k, s;
+  bool valid;
+  KItem w;
+};
+
 __global__ void __launch_bounds__(kQThreads, 1)
     bwd_dkdv_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
-                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p) {
+                         const __grid_constant__ CUtensorMap tm_do, const BwdParams p, int n_items) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -583,21 +612,41 @@ __global__ void __launch_bounds__(kQThreads, 1)
   uint8_t* sP = smem + kKOffP;
   uint8_t* sG = smem + kKOffG;
   KBars* bars = reinterpret_cast<KBars*>(smem + kKOffBar);
-  float* sBias = reinterpret_cast<float*>(smem + kKOffBias);
+  float* sBias = reinterpret_cast<float*>(smem + kKOffBias);  // [item parity][u, v][64]
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
   const int a = quad * 32 + lane;
   const uint64_t wait_ns = p.wait_ns;
+  const int P = gridDim.x;
 
-  // Block of 64 segment keys jj0 .. jj0+63 (rows M+jj of k and v) of (b, h).
-  const int nkb = (p.W + BN - 1) / BN;
-  const int bh = blockIdx.x / nkb;
-  const int b = bh / p.H, h = bh % p.H;
-  const int jj0 = (blockIdx.x % nkb) * BN;
-  const int qt0 = jj0 / BM;  // first query tile with a row i >= jj0
-  const int NT = p.nqt - qt0;
+  auto pos_of = [&](int k) {  // tile 0 of the CTA's k-th item
+    KPos t;
+    const int it = sched_unit(k, blockIdx.x, P);
+    t.k = k;
+    t.s = 0;
+    t.valid = it < n_items;
+    if (t.valid) t.w = kitem(it, p.B, p.H, p.nqt);
+    return t;
+  };
+  auto next_pos = [&](const KPos& t) {
+    if (!t.valid) return t;
+    if (t.s + 1 < t.w.nt) {
+      KPos r = t;
+      ++r.s;
+      return r;
+    }
+    return pos_of(t.k + 1);
+  };
+  // u, v of an item's head into its bias buffer (threads 0-127)
+  auto stage_bias = [&](const KPos& t) {
+    if (t.valid && tid < 2 * D)
+      sBias[(t.k & 1) * 2 * D + tid] = tid < D ? p.bias_u[t.w.h * D + tid] : p.bias_v[t.w.h * D + tid - D];
+  };
 
+  KPos cur = pos_of(0);
+  KPos nx1 = next_pos(cur);
+  KPos nx2 = next_pos(nx1);
   if (tid == 0) {
     mbar_init(&bars->kv, 1);
     mbar_init(&bars->in[0], 1);
@@ -612,32 +661,38 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tmem_alloc(&bars->tmem_base, kTmemCols);
     tmem_relinquish();
   }
-  if (tid < 2 * D) sBias[tid] = tid < D ? p.bias_u[h * D + tid] : p.bias_v[h * D + tid - D];
+  stage_bias(cur);
+  if (nx1.valid && nx1.k != cur.k) stage_bias(nx1);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  uint32_t n_ld[2] = {0, 0};
-  auto issue_tile_loads = [&](int s) {  // query tile qt0 + s
-    const int st = s & 1, i0 = (qt0 + s) * BM;
+  uint32_t n_ld[2] = {0, 0};  // tile loads issued per stage (thread 0)
+  uint32_t n_kv = 0;          // key/value loads issued (thread 0)
+  auto issue_tile_loads = [&](const KPos& t, int st) {
+    const int i0 = (t.w.qt0 + t.s) * BM;
     mbar_arrive_expect_tx(&bars->in[st], 2 * kTile + kWinTile);
-    tma_load_4d(sQ + st * kTile, &tm_q, &bars->in[st], 0, h, i0, b);
-    tma_load_4d(sDO + st * kTile, &tm_do, &bars->in[st], 0, h, i0, b);
-    tma_load_3d(sR + st * kWinTile, &tm_rw, &bars->in[st], 0, h, i0 - jj0 - BN);
+    tma_load_4d(sQ + st * kTile, &tm_q, &bars->in[st], 0, t.w.h, i0, t.w.b);
+    tma_load_4d(sDO + st * kTile, &tm_do, &bars->in[st], 0, t.w.h, i0, t.w.b);
+    tma_load_3d(sR + st * kWinTile, &tm_rw, &bars->in[st], 0, t.w.h, i0 - t.w.jj0 - BN);
     ++n_ld[st];
   };
-  if (tid == 0) {
+  auto issue_kv_loads = [&](const KItem& w) {
+    mbar_arrive_expect_tx(&bars->kv, 2 * kKTile);
+    tma_load_4d(sK, &tm_k, &bars->kv, 0, w.h, p.M + w.jj0, w.b);
+    tma_load_4d(sV, &tm_v, &bars->kv, 0, w.h, p.M + w.jj0, w.b);
+    ++n_kv;
+  };
+  if (tid == 0 && cur.valid) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
     tma_prefetch_desc(&tm_rw);
     tma_prefetch_desc(&tm_do);
-    mbar_arrive_expect_tx(&bars->kv, 2 * kKTile);
-    tma_load_4d(sK, &tm_k, &bars->kv, 0, h, p.M + jj0, b);
-    tma_load_4d(sV, &tm_v, &bars->kv, 0, h, p.M + jj0, b);
-    issue_tile_loads(0);
-    if (NT > 1) issue_tile_loads(1);
+    issue_kv_loads(cur.w);
+    issue_tile_loads(cur, 0);
+    if (nx1.valid) issue_tile_loads(nx1, 1);
   }
 
   constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
@@ -648,10 +703,11 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint64_t dPT = sdesc_sw128(smem_u32(sP), 8192, 1024);
   const uint64_t dGT = sdesc_sw128(smem_u32(sG), 8192, 1024);
 
-  // Thread 0: the score MMAs of tile s (its (q+u), (q+v) in buffer s & 1).
-  auto score_mmas = [&](int s) -> bool {
-    const int st = s & 1;
-    if (s == 0 && !mbar_wait(&bars->kv, 0, wait_ns, abort)) return false;
+  // Thread 0: the score MMAs of stream tile g at t (its (q+u), (q+v) in
+  // buffer g & 1); an item's first tile waits for the item's keys and values.
+  auto score_mmas = [&](const KPos& t, int g) -> bool {
+    const int st = g & 1;
+    if (t.s == 0 && !mbar_wait(&bars->kv, t.k & 1, wait_ns, abort)) return false;
     tc_fence_after();
     const uint64_t dQu = sdesc_sw128(smem_u32(sQu + st * kTile), 16, 1024);
     const uint64_t dQv = sdesc_sw128(smem_u32(sQv + st * kTile), 16, 1024);
@@ -666,57 +722,66 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tc_commit(&bars->m1);
     return true;
   };
-  // Everyone: this warp's half of (q+u), (q+v) of tile s, from its raw q.
-  auto build = [&](int s) -> bool {
-    const int st = s & 1;
-    if (!mbar_wait(&bars->in[st], (s >> 1) & 1, wait_ns, abort)) return false;
-    build_qu_qv_half(sQ + st * kTile, sQu + st * kTile, sQv + st * kTile, a, half, sBias, sBias + D);
+  // Everyone: this warp's half of (q+u), (q+v) of stream tile g at t, from its raw q.
+  auto build = [&](const KPos& t, int g) -> bool {
+    const int st = g & 1;
+    if (!mbar_wait(&bars->in[st], (g >> 1) & 1, wait_ns, abort)) return false;
+    const float* bu = sBias + (t.k & 1) * 2 * D;
+    build_qu_qv_half(sQ + st * kTile, sQu + st * kTile, sQv + st * kTile, a, half, bu, bu + D);
     return true;
   };
-
-  bool ok = build(0);
-  if (!ok) report_timeout(abort, p.status);
-  fence_proxy_async_smem();
-  ok = __syncthreads_and(ok) != 0;
-  if (tid == 0 && ok && !score_mmas(0)) report_timeout(abort, p.status);
-
-  // lse (log2 domain) and Delta of this thread's row in tile s; rows past W
+  // lse (log2 domain) and Delta of this thread's row in tile t; rows past W
   // get lse = +inf, so every p is 0.  Loaded one tile ahead.
-  auto row_consts = [&](int s, float& l2, float& dl) {
-    const int i = (qt0 + s) * BM + a;
+  auto row_consts = [&](const KPos& t, float& l2, float& dl) {
     l2 = INFINITY;
     dl = 0.f;
-    if (s < NT && i < p.W) {
-      const long long row_id = (static_cast<long long>(b) * p.H + h) * p.W + i;
+    if (!t.valid) return;
+    const int i = (t.w.qt0 + t.s) * BM + a;
+    if (i < p.W) {
+      const long long row_id = (static_cast<long long>(t.w.b) * p.H + t.w.h) * p.W + i;
       l2 = p.lse[row_id] * kLog2e;
       dl = p.delta[row_id];
     }
   };
+
+  bool ok = true;
+  if (cur.valid) {
+    ok = build(cur, 0);
+    if (!ok) report_timeout(abort, p.status);
+  }
+  fence_proxy_async_smem();
+  ok = __syncthreads_and(ok) != 0;
+  if (tid == 0 && ok && cur.valid && !score_mmas(cur, 0)) report_timeout(abort, p.status);
+
   float lse_next, delta_next;
-  row_consts(0, lse_next, delta_next);
-  for (int s = 0; s < NT && ok; ++s) {
-    const int st = s & 1;
-    const int i = (qt0 + s) * BM + a;
+  row_consts(cur, lse_next, delta_next);
+  for (int g = 0; cur.valid && ok; ++g) {
+    const int st = g & 1;
+    const KItem& w = cur.w;
+    const int i = (w.qt0 + cur.s) * BM + a;
     const float lse2 = lse_next, delta = delta_next;
-    row_consts(s + 1, lse_next, delta_next);
+    row_consts(nx1, lse_next, delta_next);
+    const bool last = cur.s + 1 == w.nt;  // the item's last tile
     // (1) everyone: p and g of the tile's rows against the key block; then
-    // the next tile's (q+u), (q+v).
-    ok = mbar_wait(&bars->m1, s & 1, wait_ns, abort);
+    // the next tile's (q+u), (q+v).  The tile's score MMAs are done, so on
+    // the item's last tile thread 0 loads the next item's keys and values.
+    ok = mbar_wait(&bars->m1, g & 1, wait_ns, abort);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
     tc_fence_after();
+    if (tid == 0 && last && nx1.valid) issue_kv_loads(nx1.w);
     {
-      float g[32], pr[32];
+      float gr[32], pr[32];
       // key jj0 + c is visible to row i iff jj0 + c <= i and it exists
-      const int lim = min(i - jj0, p.W - 1 - jj0);
+      const int lim = min(i - w.jj0, p.W - 1 - w.jj0);
       step_grads_half(tmem, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
-                      [&](int c) { return c <= lim; }, g, pr);
+                      [&](int c) { return c <= lim; }, gr, pr);
       store_row_half(sP, a, half, pr);
-      store_row_half(sG, a, half, g);
+      store_row_half(sG, a, half, gr);
     }
-    if (s + 1 < NT && !build(s + 1)) ok = false;
+    if (nx1.valid && !build(nx1, g + 1)) ok = false;
     fence_proxy_async_smem();
     tc_fence_before();
     if (!__syncthreads_and(ok)) {
@@ -730,54 +795,76 @@ __global__ void __launch_bounds__(kQThreads, 1)
       const uint64_t dDOmn = sdesc_sw128(smem_u32(sDO + st * kTile), 8192, 1024);
       const uint64_t dQuMN = sdesc_sw128(smem_u32(sQu + st * kTile), 8192, 1024);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColA, dPT + 128 * kk, dDOmn + 128 * kk, idT, s > 0 || kk > 0);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + kColA, dPT + 128 * kk, dDOmn + 128 * kk, idT, cur.s > 0 || kk > 0);
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) mma_ss(tmem + kColB, dGT + 128 * kk, dQuMN + 128 * kk, idT, s > 0 || kk > 0);
+      for (int kk = 0; kk < 8; ++kk)
+        mma_ss(tmem + kColB, dGT + 128 * kk, dQuMN + 128 * kk, idT, cur.s > 0 || kk > 0);
       tc_commit(&bars->m2);
-      if (s + 1 < NT && !score_mmas(s + 1)) report_timeout(abort, p.status);
+      if (nx1.valid && !score_mmas(nx1, g + 1)) report_timeout(abort, p.status);
     }
-    // (3) everyone: the tile's MMAs are done; thread 0 refills its stage.
-    ok = mbar_wait(&bars->m2, s & 1, wait_ns, abort);
+    // (3) everyone: the tile's MMAs are done; thread 0 refills its stage
+    // with tile g+2, whose item's u, v go to that item's bias buffer (read
+    // by its build after the next block barrier).  After an item's last
+    // tile its dV and dK go out.
+    ok = mbar_wait(&bars->m2, g & 1, wait_ns, abort);
     if (!__syncthreads_and(ok)) {
       ok = false;
       break;
     }
-    if (tid == 0 && s + 2 < NT) issue_tile_loads(s + 2);
-  }
-
-  if (ok) {
-    // Rows of the M = 64 results: lanes 0-15 of each quadrant, row 16 quad + lane.
-    tc_fence_after();
-    uint32_t vv[32], kv[32];
-    const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    tmem_ld32(lb + kColA + 32 * half, vv);
-    tmem_ld32(lb + kColB + 32 * half, kv);
-    tmem_wait_ld(vv);
-    tmem_wait_ld(kv);
-    const int jj = jj0 + 16 * quad + lane;
-    if (lane < 16 && jj < p.W) {
-      const long long off = ((static_cast<long long>(b) * p.W + jj) * p.H + h) * D + 32 * half;
-      float4* dvp = reinterpret_cast<float4*>(p.dv + off);
-      float4* dkp = reinterpret_cast<float4*>(p.dk + off);
+    if (tid == 0 && nx2.valid) issue_tile_loads(nx2, st);
+    if (nx2.valid && nx2.s == 0) stage_bias(nx2);
+    if (last) {
+      // Rows of the M = 64 results: lanes 0-15 of each quadrant, row 16 quad + lane.
+      tc_fence_after();
+      uint32_t vv[32], kv[32];
+      const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      tmem_ld32(lb + kColA + 32 * half, vv);
+      tmem_ld32(lb + kColB + 32 * half, kv);
+      tmem_wait_ld(vv);
+      tmem_wait_ld(kv);
+      const int jj = w.jj0 + 16 * quad + lane;
+      if (lane < 16 && jj < p.W) {
+        const long long off = ((static_cast<long long>(w.b) * p.W + jj) * p.H + w.h) * D + 32 * half;
+        float4* dvp = reinterpret_cast<float4*>(p.dv + off);
+        float4* dkp = reinterpret_cast<float4*>(p.dk + off);
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        dvp[e] = make_float4(__uint_as_float(vv[4 * e]), __uint_as_float(vv[4 * e + 1]),
-                             __uint_as_float(vv[4 * e + 2]), __uint_as_float(vv[4 * e + 3]));
-        dkp[e] = make_float4(__uint_as_float(kv[4 * e]), __uint_as_float(kv[4 * e + 1]),
-                             __uint_as_float(kv[4 * e + 2]), __uint_as_float(kv[4 * e + 3]));
+        for (int e = 0; e < 8; ++e) {
+          dvp[e] = make_float4(__uint_as_float(vv[4 * e]), __uint_as_float(vv[4 * e + 1]),
+                               __uint_as_float(vv[4 * e + 2]), __uint_as_float(vv[4 * e + 3]));
+          dkp[e] = make_float4(__uint_as_float(kv[4 * e]), __uint_as_float(kv[4 * e + 1]),
+                               __uint_as_float(kv[4 * e + 2]), __uint_as_float(kv[4 * e + 3]));
+        }
       }
+      tc_fence_before();
     }
+    cur = nx1;
+    nx1 = nx2;
+    nx2 = next_pos(nx2);
   }
+  // Let this CTA's own copies and MMAs finish before the memory is released.
   if (tid == 0) {
-    mbar_wait_own(&bars->kv, 0, wait_ns);
-    for (int s = 0; s < 2; ++s)
-      if (n_ld[s] > 0) mbar_wait_own(&bars->in[s], (n_ld[s] - 1) & 1, wait_ns);
+    if (n_kv > 0) mbar_wait_own(&bars->kv, (n_kv - 1) & 1, wait_ns);
+    for (int s2 = 0; s2 < 2; ++s2)
+      if (n_ld[s2] > 0) mbar_wait_own(&bars->in[s2], (n_ld[s2] - 1) & 1, wait_ns);
     tc_commit(&bars->fin);
     mbar_wait_own(&bars->fin, 0, wait_ns);
   }
   tc_fence_before();
   __syncthreads();
   if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+int num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
 }
 
 }  // namespace
@@ -828,8 +915,9 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   const int units = p.nqt * B * H;
   bwd_dq_tc64_kernel<<<units, kQThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, tm_dr, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const int nkb = (W + BN - 1) / BN;
-  bwd_dkdv_tc64_kernel<<<nkb * B * H, kQThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p);
+  const int n_items = (W + BN - 1) / BN * B * H;
+  const int grid = n_items < num_sms() ? n_items : num_sms();
+  bwd_dkdv_tc64_kernel<<<grid, kQThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p, n_items);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   return launch_bwd_bias(p.part, B * p.nqt, H, D, du, dvb, stream);
 }
