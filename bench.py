@@ -430,6 +430,58 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
                          "per_launch_work": f"{flops} counted flops = 2*B*H*D*(4*(W*M + W(W+1)/2) + 2*W(W+1)/2)"}}
 
 
+def measure_configs(device, steps, warmup, peak, peak_src):
+    """The other full-size training shapes, one steady segment per step
+    through txl_relattn_forward_roll (attention and the memory roll): large
+    (B=16 H=16 D=64 W=384 M=384, the D = 64 kernel) and wide (B=8 H=8 D=128
+    W=768 M=768, the D = 128 kernel, whose roll is a second launch).  Each step
+    timed with CUDA events, L2 flushed in between."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import WORKLOADS, make_prefilled, project_r
+
+    out = {"l2": "flushed between steps (256 MB write, outside the events)",
+           "peak_source": f"{peak_src} bf16_tflops (burst)",
+           "per_step_work": "6*B*H*D*(W*M + W(W+1)/2) counted flops"}
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    cs = torch.cuda.current_stream()
+    bf = torch.bfloat16
+    for name in ("large", "wide"):
+        wl = WORKLOADS[name]
+        B, H, D, W, M = wl.B, wl.H, wl.D, wl.W, wl.M
+        q, k, v, seg = make_prefilled(wl, M)
+        to = lambda a, dt=bf: torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dt)
+        qd, kd, vd = to(q), to(k), to(v)
+        R = torch.empty(M + W, wl.d_model, device=device)
+        txl.txl_sinusoid_rel(R)
+        rd = to(project_r(R.cpu().numpy(), seg.W_r, H, D, "bf16"))
+        ud, vbd = to(seg.bias_u, torch.float32), to(seg.bias_v, torch.float32)
+        o = torch.empty(qd.shape, device=device, dtype=bf)
+        kb, vb = [kd, kd.clone()], [vd, vd.clone()]
+        ts = []
+        for it in range(warmup + steps):
+            x, y = it % 2, (it + 1) % 2
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cs)
+            txl.txl_relattn_forward_roll(qd, kb[x], vb[x], rd, ud, vbd, o, kb[y][:, :M], vb[y][:, :M], M, M=M)
+            b.record(cs)
+            if it >= warmup:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        if txl.txl_get_device_status() != 0:
+            raise RuntimeError(f"device status reported a timed-out wait in the {name} workload")
+        ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+        tf = counted_flops(B, H, D, W, M) / (ms / 1e3) / 1e12
+        out[name] = {"workload": f"{name}: B={B} H={H} D={D} W={W} M={M}, steady-state segment with the "
+                                 f"memory roll, bf16",
+                     "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "steps": len(ts),
+                     "tflops": tf, "frac_of_bf16_peak": tf / peak}
+        del qd, kd, vd, kb, vb, o
+    return out
+
+
 def measure_long_memory(device, steps, warmup, peak, peak_src):
     """The long workload (B=4 H=16 D=64 W=128 M=1600): one steady segment per
     step, memory kept two ways -- rolled (txl_relattn_forward_roll: the
@@ -788,6 +840,7 @@ def run_ours(args):
         "clocks": sampler.summary(h0, h1),
     }
     result["backward"] = measure_backward(stream, wl, max(5, min(K, 50)), 3, peak, peak_src)
+    result["configs"] = measure_configs(device, max(5, min(K, 50)), 3, peak, peak_src)
     result["long_memory"] = measure_long_memory(device, max(5, min(K, 50)), 3, peak, peak_src)
     result["cached_vs_recompute"] = measure_cached_vs_recompute(device, result["long_memory"]["ring"]["ms"], 10, 3)
     result["layer"] = measure_layer(device, max(5, min(K, 30)), 3, peak, peak_src)

@@ -21,8 +21,9 @@
 // packed registers plus one byte permute for the odd half; the shifted term
 // is then added to the content score in mixed precision (fp32 + bf16).
 //
-// Persistent CTAs (one per SM) walk the (batch, head, query tile) units in
-// longest-first order.  Per CTA, 11 warps:
+// Persistent CTAs (one per SM) walk the (batch, head, query tile) units,
+// sorted longest first and dealt in a snake order (c, 2P-1-c, 2P+c, ...),
+// which pairs long units with short ones.  Per CTA, 11 warps:
 //   warps 0-7  softmax.  Thread (warp w, lane l) owns query row 32*(w%4)+l
 //              (its TMEM lane); warps 0-3 take key columns 0-31 of each step,
 //              warps 4-7 columns 32-63, and the two halves exchange their row
@@ -202,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full[s], bytes);
         return true;
       };
-      for (int u = blockIdx.x; ok && !stop && u < p.n_units; u += gridDim.x) {
+      for (int rd = 0, u = blockIdx.x; ok && !stop && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         {
           if (!(ok = acquire(bars->q_empty, bars->q_full, nQ, C::NQ, C::kQTile))) break;
@@ -266,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nK = 0, nR = 0, gt = 0, un = 0;
       uint32_t gsu0 = 0, gsu1 = 0, gsu2 = 0;  // writes per ring slot so far
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int rd = 0, u = blockIdx.x; ok && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
@@ -333,7 +334,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kTile16 = C::kRowTile >> 4;
       uint32_t nV = 0, g = 0, un = 0;
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+      for (int rd = 0, u = blockIdx.x; ok && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         for (int t = 0; t < w.nks; ++t, ++g) {
           if (!(ok = mbar_wait(&bars->p_full[g & 1], (g >> 1) & 1, wait_ns, abort))) break;
@@ -413,7 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (half == 1 && blockIdx.x < p.n_units) ok = build_q(decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt));
 
-    for (int u = blockIdx.x; ok && u < p.n_units; u += gridDim.x) {
+    for (int rd = 0, u = blockIdx.x; ok && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
       const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
       float m_use = -INFINITY;  // running max in log2 units (lazy)
       float l_half = 0.f;       // row sum over this half's columns
@@ -556,7 +557,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.lse[(static_cast<size_t>(w.b) * p.H + w.h) * p.W + i] = (m_use + __log2f(l)) * 0.69314718055994531f;
         }
       } else {
-        const int nu = u + gridDim.x;
+        const int nu = sched_unit(rd + 1, blockIdx.x, gridDim.x);
         if (nu < p.n_units && !(ok = build_q(decode_unit(nu, p.B, p.H, p.W, p.M, p.nqt)))) break;
       }
       gt = g0 + w.nks;
