@@ -172,7 +172,7 @@ TXL_API int txl_mem_update(const void* mem, int m_prev, const void* h, int w, vo
  *   m                     memory length to keep (>= 0)
  *   m_out                 host, receives m' (may be NULL)
  *
- * On the bf16 D = 64 path, when the kept rows start on a 64-row tile
+ * On the bf16 paths (D = 64 and 128), when the kept rows start on a 64-row tile
  * boundary of k and v (M+W-m' a multiple of 64) and k_mem_out, v_mem_out and
  * the stride are 16-byte aligned, the attention kernel writes the kept rows
  * itself, from the key and value tiles it has already loaded, with tensor

@@ -307,7 +307,10 @@ ROLL_CASES = [
     (1, 1, 64, 128, 0, 512),     # fused: m > M+W keeps every row
     (1, 2, 64, 300, 384, 100),   # fused: 684-100 = 584 is not a multiple of 64 -> separate roll
     (2, 2, 64, 200, 150, 150),   # separate roll (350-150 = 200)
-    (1, 2, 128, 200, 150, 64),   # D = 128: separate roll
+    (1, 2, 128, 200, 150, 64),   # D = 128: 350-64 = 286 is not a multiple of 64 -> separate roll
+    (2, 2, 128, 256, 128, 128),  # D = 128 fused: kept rows are segment rows
+    (1, 2, 128, 64, 1000, 1000), # D = 128 fused: kept rows start inside the memory
+    (1, 1, 128, 128, 0, 512),    # D = 128 fused: every row kept
     (2, 2, 64, 128, 64, 0),      # m = 0: no roll
 ]
 
@@ -337,10 +340,12 @@ def test_forward_roll(_lib, B, H, D, W, M, m):
         assert np.all(out[:, keep:] == fill), "rows past m' were written"
 
 
-def test_forward_roll_base_segments(_lib):
-    """Base workload, three segments from a full memory: each call's fused
-    roll feeds the next call, against the separate attention + roll calls."""
-    wl = WORKLOADS["base"]
+@pytest.mark.parametrize("name", ["base", "wide"])
+def test_forward_roll_full_size_segments(_lib, name):
+    """Base (D = 64) and wide (D = 128) workloads, three segments from a full
+    memory: each call's fused roll feeds the next call, against the separate
+    attention + roll calls."""
+    wl = WORKLOADS[name]
     seg = make_segments(wl, n_segments=3)
     r = project_r(O.sinusoid_rel(wl.M + wl.W, wl.d_model), seg.W_r, wl.H, wl.D, "bf16")
     L = wl.M + wl.W

@@ -327,8 +327,9 @@ struct RingArgs {
   bool append;  // the kernel also writes the segment's rows into the ring
 };
 
-// The attention (validated arguments); `roll` non-null asks the D = 64
-// kernel to write the memory roll too (the caller has checked it can).
+// The attention (validated arguments); `roll` non-null asks the bf16
+// tensor-core kernel to write the memory roll too (the caller has checked
+// it can).
 int forward_impl(const void* q, const void* k, const void* v, const void* r, const float* bias_u,
                  const float* bias_v, void* o, float* lse, int B, int W, int M, int H, int D, int n_r, float scale,
                  txl_dtype dtype, txl_dtype o_dtype, const FusedRoll* roll, bool static_scratch_only,
@@ -512,8 +513,9 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
                                               W, M, H, o_dtype == TXL_BF16, scale, nsplit, part_o, part_lse,
                                               part_cnt, wc, stream));
   }
-  return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, bias_u, bias_v, o, lse, B, W, M, H, D,
-                                          o_dtype == TXL_BF16, scale, wc, stream));
+  return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, roll ? &tm_km : nullptr, roll ? &tm_vm : nullptr,
+                                          roll ? static_cast<int>(roll->src0) : -1, bias_u, bias_v, o, lse, B, W,
+                                          M, H, D, o_dtype == TXL_BF16, scale, wc, stream));
 }
 
 }  // namespace
@@ -682,8 +684,8 @@ int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const 
       if (overlap(rkm, x) || overlap(rvm, x)) return TXL_ERR_ALIAS;
   }
   if (m_out != nullptr) *m_out = static_cast<int>(keep);
-  // Fused when the kept rows start on a 64-row tile of the D = 64 bf16 kernel.
-  const bool fused = keep > 0 && dtype == TXL_BF16 && D == 64 && (L - keep) % 64 == 0 &&
+  // Fused when the kept rows start on a 64-row key tile of the bf16 tensor-core kernels.
+  const bool fused = keep > 0 && dtype == TXL_BF16 && (D == 64 || D == 128) && (L - keep) % 64 == 0 &&
                      aligned(k_mem_out, 16) && aligned(v_mem_out, 16) && (mem_out_bs * 2) % 16 == 0 &&
                      keep <= 0x7FFFFFFFLL;
   if (fused) {

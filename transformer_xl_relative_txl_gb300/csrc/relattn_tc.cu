@@ -113,6 +113,7 @@ struct Params {
   unsigned int* status;
   unsigned long long wait_ns;
   int inject_stall;
+  int roll_src0;  // >= 0: memory roll of k, v rows [roll_src0, M+W) by the last query tile's units
 };
 
 struct Bars {
@@ -131,6 +132,7 @@ template <int D, bool O_BF16>
 __global__ void __launch_bounds__(kThreads, 1)
     relattn_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
+                      const __grid_constant__ CUtensorMap tm_km, const __grid_constant__ CUtensorMap tm_vm,
                       const Params p) {
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
@@ -197,6 +199,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_r);
       uint32_t nQ = 0, nK = 0, nV = 0, nR = 0;
       bool ok = true, stop = false;
+      // Memory roll: the unit of the last query tile of each (batch, head)
+      // loads every key and value row once.  A K or V tile whose rows lie in
+      // the kept range is stored from its stage to the memory output (one
+      // box per 64-column chunk) just before the stage is refilled (its MMA
+      // has consumed it by then), or at the end.  Per stage: destination row
+      // of the pending store (-1: none), batch and head.
+      static_assert(C::NK == C::NV, "K and V stages share the roll bookkeeping");
+      int pk_row[C::NK], pk_b[C::NK], pk_h[C::NK], pv_row[C::NK], pv_b[C::NK], pv_h[C::NK];
+#pragma unroll
+      for (int s = 0; s < C::NK; ++s) pk_row[s] = pv_row[s] = -1;
+      auto flush_store = [&](int* prow, const int* pb, const int* ph, int s, const CUtensorMap* map,
+                             uint8_t* stage) {
+        if (prow[s] >= 0) {
+          for (int c = 0; c < C::kChunks; ++c) tma_store_4d(map, stage + c * C::kRowChunk, c * 64, ph[s], prow[s], pb[s]);
+          bulk_commit_group();
+          bulk_wait_group_read0();  // the stage is refilled next
+          prow[s] = -1;
+        }
+      };
       auto acquire = [&](uint64_t* empty, uint64_t* full, uint32_t n, int ns, int bytes) -> bool {
         const int s = static_cast<int>(n % ns);
         if (!mbar_wait(&empty[s], ((n / ns) & 1) ^ 1, wait_ns, abort)) return false;
@@ -205,6 +226,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       };
       for (int rd = 0, u = blockIdx.x; ok && !stop && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        const bool rolls = p.roll_src0 >= 0 && w.i0 + BM >= p.W;
         {
           if (!(ok = acquire(bars->q_empty, bars->q_full, nQ, C::NQ, C::kQTile))) break;
           const int s = nQ % C::NQ;
@@ -221,11 +243,18 @@ __global__ void __launch_bounds__(kThreads, 1)
           return true;
         };
         auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, int ns,
-                           const CUtensorMap* map, int t) -> bool {
-          if (!acquire(empty, full, n, ns, C::kRowTile)) return false;
-          const int s = n % ns;
+                           const CUtensorMap* map, int t, int* prow, int* pb, int* ph,
+                           const CUtensorMap* rmap) -> bool {
+          const int s = static_cast<int>(n % ns);
+          if (!mbar_wait(&empty[s], ((n / ns) & 1) ^ 1, wait_ns, abort)) return false;
+          flush_store(prow, pb, ph, s, rmap, dst + s * C::kRowTile);
+          mbar_arrive_expect_tx(&full[s], C::kRowTile);
           for (int c = 0; c < C::kChunks; ++c)
             tma_load_4d(dst + s * C::kRowTile + c * C::kRowChunk, map, &full[s], c * 64, w.h, t * BN, w.b);
+          const int kr = t * BN;  // first key row of the tile
+          prow[s] = (rolls && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
+          pb[s] = w.b;
+          ph[s] = w.h;
           ++n;
           return true;
         };
@@ -235,8 +264,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, C::NK, &tm_k, t) && load_r(p.M + w.i0 - BN * (t + 1)) &&
-               load_kv(bars->emptyV, bars->fullV, sV, nV, C::NV, &tm_v, t);
+          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, C::NK, &tm_k, t, pk_row, pk_b, pk_h, &tm_km) &&
+               load_r(p.M + w.i0 - BN * (t + 1)) &&
+               load_kv(bars->emptyV, bars->fullV, sV, nV, C::NV, &tm_v, t, pv_row, pv_b, pv_h, &tm_vm);
         }
       }
       if (!ok) report_timeout(abort, p.status);
@@ -251,6 +281,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       drain(bars->fullK, nK, C::NK);
       drain(bars->fullV, nV, C::NV);
       drain(bars->fullR, nR, C::NR);
+      // Roll stores still pending: each waits for the MMAs that read its
+      // stage's last tile (the stage's data stays until then), then stores.
+      if (ok && !stop) {
+        for (int s = 0; s < C::NK; ++s) {
+          const uint32_t last = static_cast<uint32_t>(s) + ((nK - 1 - s) / C::NK) * C::NK;  // nK == nV
+          if (pk_row[s] >= 0 && mbar_wait(&bars->emptyK[s], (last / C::NK) & 1, wait_ns, abort))
+            flush_store(pk_row, pk_b, pk_h, s, &tm_km, sK + s * C::kRowTile);
+          if (pv_row[s] >= 0 && mbar_wait(&bars->emptyV[s], (last / C::NV) & 1, wait_ns, abort))
+            flush_store(pv_row, pv_b, pv_h, s, &tm_vm, sV + s * C::kRowTile);
+        }
+      }
+      bulk_wait_group0();  // every roll store is complete before the CTA exits
     }
   } else if (warp == kMmaWarp) {
     // ============================ MMA issuer ===============================
@@ -590,7 +632,8 @@ int num_sms() {
 
 template <int D, bool O_BF16>
 cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                         const CUtensorMap& tm_r, const Params& prm, cudaStream_t stream) {
+                         const CUtensorMap& tm_r, const CUtensorMap& tm_km, const CUtensorMap& tm_vm,
+                         const Params& prm, cudaStream_t stream) {
   auto kern = relattn_tc_kernel<D, O_BF16>;
   constexpr int smem = Cfg<D>::kSmemBytes;
   static int configured_mask = 0;  // one bit per device ordinal < 32
@@ -603,17 +646,23 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
   const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
-  kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, prm);
+  kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_km, tm_vm, prm);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                              const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
-                              float* lse, int B, int W, int M, int H, int D, bool o_bf16, float scale,
-                              const WaitCtl& wc, cudaStream_t stream) {
+                              const CUtensorMap& tm_r, const CUtensorMap* tm_km, const CUtensorMap* tm_vm,
+                              int roll_src0, const float* bias_u, const float* bias_v, void* o, float* lse, int B,
+                              int W, int M, int H, int D, bool o_bf16, float scale, const WaitCtl& wc,
+                              cudaStream_t stream) {
   Params prm;
+  // without a roll the kernel never touches the roll maps; k's map stands in
+  const bool roll = tm_km != nullptr && tm_vm != nullptr && roll_src0 >= 0;
+  prm.roll_src0 = roll ? roll_src0 : -1;
+  const CUtensorMap& km = roll ? *tm_km : tm_k;
+  const CUtensorMap& vm = roll ? *tm_vm : tm_v;
   prm.bias_u = bias_u;
   prm.bias_v = bias_v;
   prm.o = o;
@@ -633,8 +682,8 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
   prm.wait_ns = wc.limit_ns;
   prm.inject_stall = wc.inject_stall;
   if (D == 128)
-    return o_bf16 ? launch_typed<128, true>(tm_q, tm_k, tm_v, tm_r, prm, stream)
-                  : launch_typed<128, false>(tm_q, tm_k, tm_v, tm_r, prm, stream);
+    return o_bf16 ? launch_typed<128, true>(tm_q, tm_k, tm_v, tm_r, km, vm, prm, stream)
+                  : launch_typed<128, false>(tm_q, tm_k, tm_v, tm_r, km, vm, prm, stream);
   return cudaErrorInvalidValue;
 }
 

@@ -40,9 +40,10 @@ cudaError_t launch_relattn_f32(const float* q, const float* k, const float* v, c
 // {D, H, M+W, B} with {64, 1, 64, 1}; r over {D, H, n_r} with {64, 1, 64};
 // all bf16, 128-byte swizzle, zero fill out of bounds.
 cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
-                              const CUtensorMap& tm_r, const float* bias_u, const float* bias_v, void* o,
-                              float* lse, int B, int W, int M, int H, int D, bool o_bf16, float scale,
-                              const WaitCtl& wc, cudaStream_t stream);
+                              const CUtensorMap& tm_r, const CUtensorMap* tm_km, const CUtensorMap* tm_vm,
+                              int roll_src0, const float* bias_u, const float* bias_v, void* o, float* lse, int B,
+                              int W, int M, int H, int D, bool o_bf16, float scale, const WaitCtl& wc,
+                              cudaStream_t stream);
 
 // Keys and values split between a ring of memory rows and the segment: the
 // maps of launch_relattn_tc64's tm_k / tm_v then describe the rings
