@@ -511,11 +511,11 @@ int forward_impl(const void* q, const void* k, const void* v, const void* r, con
                                               roll ? static_cast<int>(roll->src0) : -1,
                                               ring != nullptr ? &ring_maps : nullptr, bias_u, bias_v, o, lse, B,
                                               W, M, H, o_dtype == TXL_BF16, scale, nsplit, part_o, part_lse,
-                                              part_cnt, wc, stream));
+                                              part_cnt, !static_scratch_only, wc, stream));
   }
   return from_cuda(txl::launch_relattn_tc(tm_q, tm_k, tm_v, tm_r, roll ? &tm_km : nullptr, roll ? &tm_vm : nullptr,
                                           roll ? static_cast<int>(roll->src0) : -1, bias_u, bias_v, o, lse, B, W,
-                                          M, H, D, o_dtype == TXL_BF16, scale, wc, stream));
+                                          M, H, D, o_dtype == TXL_BF16, scale, !static_scratch_only, wc, stream));
 }
 
 }  // namespace

@@ -22,8 +22,9 @@
 // is then added to the content score in mixed precision (fp32 + bf16).
 //
 // Persistent CTAs (one per SM) walk the (batch, head, query tile) units,
-// sorted longest first and dealt in a snake order (c, 2P-1-c, 2P+c, ...),
-// which pairs long units with short ones.  Per CTA, 11 warps:
+// sorted longest first, in a host-made cost-balanced plan (or, without one,
+// in a snake order c, 2P-1-c, 2P+c, ..., which pairs long units with short
+// ones).  Per CTA, 11 warps:
 //   warps 0-7  softmax.  Thread (warp w, lane l) owns query row 32*(w%4)+l
 //              (its TMEM lane); warps 0-3 take key columns 0-31 of each step,
 //              warps 4-7 columns 32-63, and the two halves exchange their row
@@ -113,7 +114,9 @@ struct Params {
   unsigned int* status;
   unsigned long long wait_ns;
   int inject_stall;
-  int roll_src0;  // >= 0: memory roll of k, v rows [roll_src0, M+W) by the last query tile's units
+  int roll_src0;
+  const int* sched;  // host-made unit table [grid][sched_stride] (-1 ends a row); nullptr: snake order
+  int sched_stride;  // >= 0: memory roll of k, v rows [roll_src0, M+W) by the last query tile's units
 };
 
 struct Bars {
@@ -224,7 +227,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&full[s], bytes);
         return true;
       };
-      for (int rd = 0, u = blockIdx.x; ok && !stop && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
+      for (int rd = 0, u = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); ok && !stop && u < p.n_units; u = unit_at(p.sched, p.sched_stride, ++rd, blockIdx.x, gridDim.x, p.n_units)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         const bool rolls = p.roll_src0 >= 0 && w.i0 + BM >= p.W;
         {
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nK = 0, nR = 0, gt = 0, un = 0;
       uint32_t gsu0 = 0, gsu1 = 0, gsu2 = 0;  // writes per ring slot so far
       bool ok = true;
-      for (int rd = 0, u = blockIdx.x; ok && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
+      for (int rd = 0, u = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); ok && u < p.n_units; u = unit_at(p.sched, p.sched_stride, ++rd, blockIdx.x, gridDim.x, p.n_units)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
         tc_fence_after();
@@ -376,7 +379,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       constexpr uint32_t kTile16 = C::kRowTile >> 4;
       uint32_t nV = 0, g = 0, un = 0;
       bool ok = true;
-      for (int rd = 0, u = blockIdx.x; ok && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
+      for (int rd = 0, u = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); ok && u < p.n_units; u = unit_at(p.sched, p.sched_stride, ++rd, blockIdx.x, gridDim.x, p.n_units)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
         for (int t = 0; t < w.nks; ++t, ++g) {
           if (!(ok = mbar_wait(&bars->p_full[g & 1], (g >> 1) & 1, wait_ns, abort))) break;
@@ -454,9 +457,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       return true;
     };
 
-    if (half == 1 && blockIdx.x < p.n_units) ok = build_q(decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt));
+    if (const int u0 = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units);
+        half == 1 && u0 < p.n_units)
+      ok = build_q(decode_unit(u0, p.B, p.H, p.W, p.M, p.nqt));
 
-    for (int rd = 0, u = blockIdx.x; ok && u < p.n_units; u = sched_unit(++rd, blockIdx.x, gridDim.x)) {
+    for (int rd = 0, u = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); ok && u < p.n_units; u = unit_at(p.sched, p.sched_stride, ++rd, blockIdx.x, gridDim.x, p.n_units)) {
       const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
       float m_use = -INFINITY;  // running max in log2 units (lazy)
       float l_half = 0.f;       // row sum over this half's columns
@@ -599,7 +604,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             p.lse[(static_cast<size_t>(w.b) * p.H + w.h) * p.W + i] = (m_use + __log2f(l)) * 0.69314718055994531f;
         }
       } else {
-        const int nu = sched_unit(rd + 1, blockIdx.x, gridDim.x);
+        const int nu = unit_at(p.sched, p.sched_stride, rd + 1, blockIdx.x, gridDim.x, p.n_units);
         if (nu < p.n_units && !(ok = build_q(decode_unit(nu, p.B, p.H, p.W, p.M, p.nqt)))) break;
       }
       gt = g0 + w.nks;
@@ -655,8 +660,8 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
 cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                               const CUtensorMap& tm_r, const CUtensorMap* tm_km, const CUtensorMap* tm_vm,
                               int roll_src0, const float* bias_u, const float* bias_v, void* o, float* lse, int B,
-                              int W, int M, int H, int D, bool o_bf16, float scale, const WaitCtl& wc,
-                              cudaStream_t stream) {
+                              int W, int M, int H, int D, bool o_bf16, float scale, bool allow_plan,
+                              const WaitCtl& wc, cudaStream_t stream) {
   Params prm;
   // without a roll the kernel never touches the roll maps; k's map stands in
   const bool roll = tm_km != nullptr && tm_vm != nullptr && roll_src0 >= 0;
@@ -673,6 +678,13 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
   prm.H = H;
   prm.nqt = (W + BM - 1) / BM;
   prm.n_units = prm.nqt * B * H;
+  // More units than CTAs: deal them by the host's plan (made once per shape)
+  prm.sched = nullptr;
+  prm.sched_stride = 0;
+  if (allow_plan && prm.n_units > num_sms()) {
+    const cudaError_t pe = unit_plan(B, H, W, M, num_sms(), &prm.sched, &prm.sched_stride);
+    if (pe != cudaSuccess) return pe;
+  }
   // The sign of the scale is folded into (q+u), (q+v) (exact in bf16); a zero
   // scale becomes 1e-30, for which every visible exponent rounds to 2^0 in
   // fp32 exactly as with 0, while masked keys keep an exponent of -inf.

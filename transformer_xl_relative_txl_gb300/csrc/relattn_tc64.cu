@@ -52,9 +52,15 @@
 // that runs out raises a CTA abort flag and the device status word, every
 // role unwinds (the loader and the issuers wait for their own operations in
 // flight) and the TMEM is freed before exit.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <map>
+#include <mutex>
+#include <queue>
+#include <tuple>
 #include <type_traits>
+#include <vector>
 
 #include "relattn_tc_common.cuh"
 #include "txl_device.cuh"
@@ -118,6 +124,8 @@ struct Params {
   unsigned int* status;
   unsigned long long wait_ns;
   int inject_stall;
+  const int* sched;   // host-made unit table [grid][sched_stride] (-1 ends a row); nullptr: snake order
+  int sched_stride;
   int roll_src0;  // >= 0: memory roll of k, v rows [roll_src0, M+W) by the last query tile's units
   // ring_cap > 0: keys and values come from two places -- memory row m
   // (m < M) is row (ring_start + m) % ring_cap of the ring maps tm_k / tm_v,
@@ -249,11 +257,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nQ;
         return true;
       };
-      if (sched_unit(0, blockIdx.x, gridDim.x) < p.n_units) ok = load_q(sched_unit(0, blockIdx.x, gridDim.x));
+      if (const int u0 = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); u0 < p.n_units)
+        ok = load_q(u0);
       for (int rd = 0;; ++rd) {
-        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        const int u = unit_at(p.sched, p.sched_stride, rd, blockIdx.x, gridDim.x, p.n_units);
         if (!ok || stop || u >= p.n_units) break;
-        const int un_next = sched_unit(rd + 1, blockIdx.x, gridDim.x);
+        const int un_next = unit_at(p.sched, p.sched_stride, rd + 1, blockIdx.x, gridDim.x, p.n_units);
         const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         if (un_next < p.n_units && !(ok = load_q(un_next))) break;
         auto load_r = [&](int d0) -> bool {
@@ -343,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nK = 0, gt = 0, un = 0;
       bool ok = true;
       for (int rd = 0;; ++rd) {
-        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        const int u = unit_at(p.sched, p.sched_stride, rd, blockIdx.x, gridDim.x, p.n_units);
         if (!ok || u >= p.n_units) break;
         const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
@@ -387,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int rb = 0;  // ring slot of the first distance tile (-2) of the unit
       bool ok = true;
       for (int rd = 0;; ++rd) {
-        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        const int u = unit_at(p.sched, p.sched_stride, rd, blockIdx.x, gridDim.x, p.n_units);
         if (!ok || u >= p.n_units) break;
         const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
@@ -444,7 +453,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t nV = 0, g = 0, un = 0;
       bool ok = true;
       for (int rd = 0;; ++rd) {
-        const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+        const int u = unit_at(p.sched, p.sched_stride, rd, blockIdx.x, gridDim.x, p.n_units);
         if (!ok || u >= p.n_units) break;
         const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
         for (int t = 0; t < w.nks; ++t, ++g) {
@@ -534,15 +543,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     auto bias_of = [&](int u, const float* bias) -> float {
       return __ldg(bias + decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt).h * D + 32 * par + lane);
     };
-    if (sched_unit(0, blockIdx.x, gridDim.x) < p.n_units) {
-      const int u0 = sched_unit(0, blockIdx.x, gridDim.x);
+    if (unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units) < p.n_units) {
+      const int u0 = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units);
       ok = build_q(decode_item(u0, kSplit, p.B, p.H, p.W, p.M, p.nqt), 0, bias_of(u0, p.bias_u), bias_of(u0, p.bias_v));
     }
 
     for (int rd = 0;; ++rd) {
-      const int u = sched_unit(rd, blockIdx.x, gridDim.x);
+      const int u = unit_at(p.sched, p.sched_stride, rd, blockIdx.x, gridDim.x, p.n_units);
       if (!ok || u >= p.n_units) break;
-      const int un_next = sched_unit(rd + 1, blockIdx.x, gridDim.x);
+      const int un_next = unit_at(p.sched, p.sched_stride, rd + 1, blockIdx.x, gridDim.x, p.n_units);
       const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
       const uint32_t g0 = gt;
       const bool has_next = un_next < p.n_units;
@@ -884,7 +893,107 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
   return cudaGetLastError();
 }
 
+// Units dealt to the CTAs by cost (longest-processing-time first onto the
+// least-loaded CTA, then moves and swaps off the busiest CTA while they lower
+// it); each CTA's units run longest first.  A unit costs its key steps plus
+// kUnitCost for the unit boundary (first-score latency and epilogue, about
+// 1.2 steps in traces of the kernel).  Returns the table [P][stride] (-1
+// ends a row).  The unit order and step counts are those of decode_unit.
+std::vector<int> plan_units(int B, int H, int W, int M, int P, int* stride_out) {
+  constexpr double kUnitCost = 1.2;
+  const int nqt = (W + BM - 1) / BM, n = nqt * B * H;
+  std::vector<double> cost(n);
+  for (int u = 0; u < n; ++u) {
+    const int qt = nqt - 1 - u / (B * H);
+    const int kmax = std::min(M + qt * BM + BM - 1, M + W - 1);
+    cost[u] = kmax / BN + 1 + kUnitCost;
+  }
+  std::vector<std::vector<int>> bins(P);
+  std::vector<double> load(P, 0.0);
+  using Slot = std::pair<double, int>;
+  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
+  for (int c = 0; c < P; ++c) heap.push({0.0, c});
+  for (int u = 0; u < n; ++u) {  // units are already in decreasing cost
+    const int c = heap.top().second;
+    heap.pop();
+    bins[c].push_back(u);
+    load[c] += cost[u];
+    heap.push({load[c], c});
+  }
+  for (int iter = 0; iter < 4 * n; ++iter) {
+    const int A = static_cast<int>(std::max_element(load.begin(), load.end()) - load.begin());
+    const double mx = load[A];
+    double best_gain = 1e-9;
+    int bx = -1, by = -1, bB = -1;  // move bins[A][bx] to B, swapping in bins[B][by] when by >= 0
+    for (int B2 = 0; B2 < P; ++B2) {
+      if (B2 == A) continue;
+      for (int xi = 0; xi < static_cast<int>(bins[A].size()); ++xi) {
+        const double cx = cost[bins[A][xi]];
+        const double gm = mx - std::max(load[A] - cx, load[B2] + cx);
+        if (gm > best_gain) best_gain = gm, bx = xi, by = -1, bB = B2;
+        for (int yi = 0; yi < static_cast<int>(bins[B2].size()); ++yi) {
+          const double cy = cost[bins[B2][yi]];
+          if (cy >= cx) continue;
+          const double gs = mx - std::max(load[A] - cx + cy, load[B2] - cy + cx);
+          if (gs > best_gain) best_gain = gs, bx = xi, by = yi, bB = B2;
+        }
+      }
+    }
+    if (bx < 0) break;
+    const int x = bins[A][bx];
+    bins[A].erase(bins[A].begin() + bx);
+    load[A] -= cost[x];
+    if (by >= 0) {
+      const int y = bins[bB][by];
+      bins[bB].erase(bins[bB].begin() + by);
+      load[bB] -= cost[y];
+      bins[A].push_back(y);
+      load[A] += cost[y];
+    }
+    bins[bB].push_back(x);
+    load[bB] += cost[x];
+  }
+  size_t kmax = 0;
+  for (auto& b : bins) {
+    std::sort(b.begin(), b.end());  // unit index order is longest first
+    kmax = std::max(kmax, b.size());
+  }
+  const int stride = static_cast<int>(kmax) + 1;
+  std::vector<int> table(static_cast<size_t>(P) * stride, -1);
+  for (int c = 0; c < P; ++c)
+    for (size_t r = 0; r < bins[c].size(); ++r) table[static_cast<size_t>(c) * stride + r] = bins[c][r];
+  *stride_out = stride;
+  return table;
+}
+
+// Device copies of the plans, per (device, B, H, W, M, grid); made on first
+// use of a shape (a synchronous upload) and kept for the process.
+std::mutex g_plan_mutex;
+std::map<std::tuple<int, int, int, int, int, int>, std::pair<int*, int>> g_plans;
+
 }  // namespace
+
+cudaError_t unit_plan(int B, int H, int W, int M, int P, const int** table, int* stride) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lk(g_plan_mutex);
+  auto& entry = g_plans[std::make_tuple(dev, B, H, W, M, P)];
+  if (entry.first == nullptr) {
+    int st = 0;
+    const std::vector<int> t = plan_units(B, H, W, M, P, &st);
+    int* d = nullptr;
+    if ((e = cudaMalloc(&d, t.size() * sizeof(int))) != cudaSuccess) return e;
+    if ((e = cudaMemcpy(d, t.data(), t.size() * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) {
+      cudaFree(d);
+      return e;
+    }
+    entry = {d, st};
+  }
+  *table = entry.first;
+  *stride = entry.second;
+  return cudaSuccess;
+}
 
 int relattn_tc64_split(int B, int H, int W, int M) {
   // Cost in key steps of the slowest CTA: waves of work items times the
@@ -915,8 +1024,8 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
                                 const CUtensorMap* tm_vm, int roll_src0, const RingMaps* ring,
                                 const float* bias_u, const float* bias_v, void* o,
                                 float* lse, int B, int W, int M, int H, bool o_bf16, float scale, int nsplit,
-                                float* part_o, float* part_lse, int* part_cnt, const WaitCtl& wc,
-                                cudaStream_t stream) {
+                                float* part_o, float* part_lse, int* part_cnt, bool allow_plan,
+                                const WaitCtl& wc, cudaStream_t stream) {
   Params prm;
   prm.bias_u = bias_u;
   prm.bias_v = bias_v;
@@ -950,6 +1059,13 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   // the appended rows must land in slots outside the memory, whole tiles only
   if (prm.ring_append && (W % BN != 0 || M + W > ring->cap)) return cudaErrorInvalidValue;
   if (o_bf16 && tm_o == nullptr) return cudaErrorInvalidValue;
+  // More units than CTAs: deal them by the host's plan (made once per shape)
+  prm.sched = nullptr;
+  prm.sched_stride = 0;
+  if (allow_plan && nsplit == 1 && prm.n_units > num_sms()) {
+    const cudaError_t pe = unit_plan(B, H, W, M, num_sms(), &prm.sched, &prm.sched_stride);
+    if (pe != cudaSuccess) return pe;
+  }
   // Unused maps (fp32 output is written with plain stores; no roll) are
   // stood in for by tm_q and never touched.
   const CUtensorMap& km = prm.roll_src0 >= 0 ? *tm_km : tm_q;

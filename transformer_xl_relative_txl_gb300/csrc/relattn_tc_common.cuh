@@ -56,6 +56,16 @@ __device__ __forceinline__ int sched_unit(int r, int c, int P) {
   return r * P + ((r & 1) ? P - 1 - c : c);
 }
 
+// Unit of round r for CTA c: from a host-made table when there is one (row c
+// of `stride` unit indices, -1 past the CTA's last unit), else the snake
+// order.  Returns n_units once the CTA has no more.
+__device__ __forceinline__ int unit_at(const int* sched, int stride, int r, int c, int P, int n_units) {
+  if (sched == nullptr) return sched_unit(r, c, P);
+  if (r >= stride) return n_units;
+  const int u = __ldg(sched + c * stride + r);
+  return u < 0 ? n_units : u;
+}
+
 __device__ __forceinline__ uint32_t byte_perm(uint32_t a, uint32_t b, uint32_t sel) {
   uint32_t r;
   asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));

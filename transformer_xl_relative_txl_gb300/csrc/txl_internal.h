@@ -42,8 +42,8 @@ cudaError_t launch_relattn_f32(const float* q, const float* k, const float* v, c
 cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                               const CUtensorMap& tm_r, const CUtensorMap* tm_km, const CUtensorMap* tm_vm,
                               int roll_src0, const float* bias_u, const float* bias_v, void* o, float* lse, int B,
-                              int W, int M, int H, int D, bool o_bf16, float scale, const WaitCtl& wc,
-                              cudaStream_t stream);
+                              int W, int M, int H, int D, bool o_bf16, float scale, bool allow_plan,
+                              const WaitCtl& wc, cudaStream_t stream);
 
 // Keys and values split between a ring of memory rows and the segment: the
 // maps of launch_relattn_tc64's tm_k / tm_v then describe the rings
@@ -69,12 +69,20 @@ struct RingMaps {
 // last chunk to finish a unit's rows merges them into o and lse, counting in
 // part_cnt [units][4], which must be zero before the launch (and is again
 // after it).
+// allow_plan: with more units than SMs, deal them to the CTAs by a
+// host-made, cost-balanced plan (built and uploaded once per shape, which
+// allocates); otherwise, or without allow_plan, the snake order.
+// A cost-balanced assignment of the (batch, head, query tile) units, longest
+// first, to P persistent CTAs: device table [P][*stride] of unit indices
+// (-1 ends a row), made on first use of a shape and kept (relattn_tc64.cu).
+cudaError_t unit_plan(int B, int H, int W, int M, int P, const int** table, int* stride);
+
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
                                 const CUtensorMap* tm_vm, int roll_src0, const RingMaps* ring,
                                 const float* bias_u, const float* bias_v, void* o, float* lse, int B, int W, int M,
                                 int H, bool o_bf16, float scale, int nsplit, float* part_o, float* part_lse,
-                                int* part_cnt, const WaitCtl& wc, cudaStream_t stream);
+                                int* part_cnt, bool allow_plan, const WaitCtl& wc, cudaStream_t stream);
 
 // Backward on CUDA cores (fp32 arithmetic; q, k, v, r fp32 or bf16, o and
 // dout fp32 or bf16; D <= 256).  dk, dv cover the segment's key rows.
