@@ -37,12 +37,13 @@
 //              (64 distances) into 128B-swizzled shared-memory rings; zero
 //              fill outside the tensors.
 //   warp 9     score MMA issuer: S_t = (q+u) K_t^T into one of two S buffers
-//              as soon as the softmax has read the previous occupant, G into
-//              the ring once its slot is released; runs up to one step ahead
-//              of the softmax.
-//   warp 10    PV MMA issuer: O += P_t V_t when P_t is ready.  Two issuing
-//              threads on different schedulers keep each serial chain of
-//              waits, MMAs and commits short; each commits its own MMAs.
+//              as soon as the softmax has read the previous occupant; runs
+//              up to one step ahead of the softmax.
+//   warp 10    PV MMA issuer: O += P_t V_t when P_t is ready.
+//   warp 11    distance MMA issuer: G = (q+v) R^T into the ring once its
+//              slot is released.  Three issuing threads on different
+//              schedulers keep each serial chain of waits, MMAs and commits
+//              short; each commits its own MMAs.
 //
 // TMEM (512 columns): D = 64: (q+u) [0,32) (q+v) [32,64) O [64,128);
 // D = 128: O [0,128) with (q+u), (q+v) in shared memory.  Both: P0, P1
@@ -65,9 +66,10 @@ namespace {
 constexpr int BM = 128;  // query rows per unit (TMEM lanes)
 constexpr int BN = 64;   // keys per step, distances per ring tile
 constexpr int kLoaderWarp = 8;
-constexpr int kMmaWarp = 9;   // S = (q+u)K^T and G = (q+v)R^T issuer; owns the TMEM allocation
+constexpr int kMmaWarp = 9;   // S = (q+u)K^T issuer; owns the TMEM allocation
 constexpr int kPvWarp = 10;   // O += P V issuer
-constexpr int kThreads = 352;
+constexpr int kQrWarp = 11;   // G = (q+v)R^T (distance ring) issuer
+constexpr int kThreads = 384;
 constexpr uint32_t kColP = 128;  // P0, P1: 32 columns each
 constexpr uint32_t kColS = 192;  // S0, S1: 64 columns each
 constexpr uint32_t kColG = 320;  // distance ring: 3 slots of 64 columns
@@ -124,6 +126,7 @@ struct Bars {
   uint64_t q_full[2], q_empty[2];
   uint64_t q_ready, s_full[2], s_free[2], p_full[2], pv_done[2], o_full, o_free, g_free[kSlots], mma_final,
       pv_final;
+  uint64_t g_full[2], qr_final;  // distance tile of a step ready (per S buffer parity); QR issuer done
   uint64_t xbar[4];  // row-max exchange of warps quad and quad+4 (64 arrivals per step)
   uint64_t lbar[4];  // row-sum hand-over at the end of a unit (32 arrivals)
   uint32_t tmem_base;
@@ -171,6 +174,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&bars->q_full[s], 1);
       mbar_init(&bars->q_empty[s], 128);
       mbar_init(&bars->s_full[s], 1);
+      mbar_init(&bars->g_full[s], 1);
       mbar_init(&bars->s_free[s], 8);
       mbar_init(&bars->p_full[s], 8);
       mbar_init(&bars->pv_done[s], 1);
@@ -179,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(&bars->o_full, 1);
     mbar_init(&bars->o_free, 4);
     mbar_init(&bars->mma_final, 1);
+    mbar_init(&bars->qr_final, 1);
     mbar_init(&bars->pv_final, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -305,12 +310,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       // low 14 bits, so byte offsets inside shared memory are added as
       // offset / 16 (no carry: shared addresses stay below 256 KB).
       const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
-      const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
       const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
-      const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
       constexpr uint32_t kTile16 = C::kRowTile >> 4;
-      uint32_t nK = 0, nR = 0, gt = 0, un = 0;
-      uint32_t gsu0 = 0, gsu1 = 0, gsu2 = 0;  // writes per ring slot so far
+      uint32_t nK = 0, gt = 0, un = 0;
       bool ok = true;
       for (int rd = 0, u = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); ok && u < p.n_units; u = unit_at(p.sched, p.sched_stride, ++rd, blockIdx.x, gridDim.x, p.n_units)) {
         const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
@@ -337,30 +339,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(&bars->emptyK[sk]);
           ++nK;
-          for (int e = (t == 0 ? -2 : t); ok && e <= t; ++e) {
-            const int slot = (e + 2) % kSlots;
-            const uint32_t used = slot == 0 ? gsu0 : (slot == 1 ? gsu1 : gsu2);
-            if (used > 0 && !(ok = mbar_wait(&bars->g_free[slot], (used - 1) & 1, wait_ns, abort))) break;
-            const int sr = nR % C::NR;
-            if (!(ok = mbar_wait(&bars->fullR[sr], (nR / C::NR) & 1, wait_ns, abort))) break;
-            tc_fence_after();
-            const uint64_t dr = dR + sr * kTile16;
-            const uint32_t gd = tmem + kColG + slot * BN;
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t koff16 = ((kk / 4) * C::kRowChunk + (kk % 4) * 32) >> 4;
-              if constexpr (C::kQTmem)
-                mma_ts(gd, tmem + C::kColQv + kk * 8, dr + koff16, idS, kk > 0);
-              else
-                mma_ss(gd, dQv + (((kk / 4) * C::kQChunk + (kk % 4) * 32) >> 4), dr + koff16, idS, kk > 0);
-            }
-            tc_commit(&bars->emptyR[sr]);
-            ++nR;
-            gsu0 += slot == 0;
-            gsu1 += slot == 1;
-            gsu2 += slot == 2;
-          }
-          if (!ok) break;
           tc_commit(&bars->s_full[sb]);
         }
         if (!ok) break;
@@ -403,6 +381,62 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) report_timeout(abort, p.status);
       tc_commit(&bars->pv_final);
       mbar_wait_own(&bars->pv_final, 0, wait_ns);
+    }
+  } else if (warp == kQrWarp) {
+    // ========================= distance-ring issuer =========================
+    // G tile e = (q+v) R_e^T into ring slot (e+2) % 3 once the softmax has
+    // released the slot's previous tile; tiles -2 and -1 of a unit with its
+    // first step.  Its own thread, so the ring never waits behind the S
+    // MMAs' barriers (and the reverse); it commits g_full per step.
+    if (lane == 0) {
+      constexpr uint32_t idS = idesc_bf16(128, BN, false, false);
+      const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
+      const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
+      constexpr uint32_t kTile16 = C::kRowTile >> 4;
+      uint32_t nR = 0, gt = 0, un = 0;
+      uint32_t gsu0 = 0, gsu1 = 0, gsu2 = 0;  // writes per ring slot so far
+      bool ok = true;
+      for (int rd = 0, u = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); ok && u < p.n_units;
+           u = unit_at(p.sched, p.sched_stride, ++rd, blockIdx.x, gridDim.x, p.n_units)) {
+        const Unit w = decode_unit(u, p.B, p.H, p.W, p.M, p.nqt);
+        if (!(ok = mbar_wait(&bars->q_ready, un & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        const uint32_t g0 = gt;
+        for (int t = 0; t < w.nks; ++t) {
+          const uint32_t g = g0 + t, sb = g & 1;
+          for (int e = (t == 0 ? -2 : t); ok && e <= t; ++e) {
+            const int slot = (e + 2) % kSlots;
+            const uint32_t used = slot == 0 ? gsu0 : (slot == 1 ? gsu1 : gsu2);
+            if (used > 0 && !(ok = mbar_wait(&bars->g_free[slot], (used - 1) & 1, wait_ns, abort))) break;
+            const int sr = nR % C::NR;
+            if (!(ok = mbar_wait(&bars->fullR[sr], (nR / C::NR) & 1, wait_ns, abort))) break;
+            tc_fence_after();
+            const uint64_t dr = dR + sr * kTile16;
+            const uint32_t gd = tmem + kColG + slot * BN;
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk) {
+              const uint32_t koff16 = ((kk / 4) * C::kRowChunk + (kk % 4) * 32) >> 4;
+              if constexpr (C::kQTmem)
+                mma_ts(gd, tmem + C::kColQv + kk * 8, dr + koff16, idS, kk > 0);
+              else
+                mma_ss(gd, dQv + (((kk / 4) * C::kQChunk + (kk % 4) * 32) >> 4), dr + koff16, idS, kk > 0);
+            }
+            tc_commit(&bars->emptyR[sr]);
+            ++nR;
+            gsu0 += slot == 0;
+            gsu1 += slot == 1;
+            gsu2 += slot == 2;
+          }
+          if (!ok) break;
+          tc_commit(&bars->g_full[sb]);
+        }
+        if (!ok) break;
+        gt = g0 + w.nks;
+        ++un;
+      }
+      if (!ok) report_timeout(abort, p.status);
+      tc_commit(&bars->qr_final);
+      mbar_wait_own(&bars->qr_final, 0, wait_ns);
     }
   } else {
     // ============================ softmax warps ============================
@@ -469,6 +503,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int t = 0; t < w.nks; ++t) {
         const uint32_t g = g0 + t, sb = g & 1;
         if (!(ok = warp_wait(&bars->s_full[sb], (g >> 1) & 1, wait_ns, abort))) break;
+        if (!(ok = warp_wait(&bars->g_full[sb], (g >> 1) & 1, wait_ns, abort))) break;
         tc_fence_after();
         uint32_t sraw[32], x0[32], x1[32];
         tmem_ld32(tmem + lane_base + kColS + sb * BN + 32 * half, sraw);
