@@ -717,7 +717,7 @@ cudaError_t launch_relattn_tc(const CUtensorMap& tm_q, const CUtensorMap& tm_k, 
   prm.sched = nullptr;
   prm.sched_stride = 0;
   if (allow_plan && prm.n_units > num_sms()) {
-    const cudaError_t pe = unit_plan(B, H, W, M, num_sms(), &prm.sched, &prm.sched_stride);
+    const cudaError_t pe = unit_plan(B, H, W, M, num_sms(), stream, &prm.sched, &prm.sched_stride);
     if (pe != cudaSuccess) return pe;
   }
   // The sign of the scale is folded into (q+u), (q+v) (exact in bf16); a zero

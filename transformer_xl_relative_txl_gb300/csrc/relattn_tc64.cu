@@ -973,13 +973,22 @@ std::map<std::tuple<int, int, int, int, int, int>, std::pair<int*, int>> g_plans
 
 }  // namespace
 
-cudaError_t unit_plan(int B, int H, int W, int M, int P, const int** table, int* stride) {
+cudaError_t unit_plan(int B, int H, int W, int M, int P, cudaStream_t stream, const int** table, int* stride) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lk(g_plan_mutex);
   auto& entry = g_plans[std::make_tuple(dev, B, H, W, M, P)];
   if (entry.first == nullptr) {
+    // No plan yet: making one allocates and copies, which a stream being
+    // captured into a graph must not see; such a call keeps the snake order.
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if ((e = cudaStreamIsCapturing(stream, &cap)) != cudaSuccess) return e;
+    if (cap != cudaStreamCaptureStatusNone) {
+      *table = nullptr;
+      *stride = 0;
+      return cudaSuccess;
+    }
     int st = 0;
     const std::vector<int> t = plan_units(B, H, W, M, P, &st);
     int* d = nullptr;
@@ -1063,7 +1072,7 @@ cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k
   prm.sched = nullptr;
   prm.sched_stride = 0;
   if (allow_plan && nsplit == 1 && prm.n_units > num_sms()) {
-    const cudaError_t pe = unit_plan(B, H, W, M, num_sms(), &prm.sched, &prm.sched_stride);
+    const cudaError_t pe = unit_plan(B, H, W, M, num_sms(), stream, &prm.sched, &prm.sched_stride);
     if (pe != cudaSuccess) return pe;
   }
   // Unused maps (fp32 output is written with plain stores; no roll) are

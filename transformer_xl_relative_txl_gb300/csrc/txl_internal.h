@@ -71,11 +71,14 @@ struct RingMaps {
 // after it).
 // allow_plan: with more units than SMs, deal them to the CTAs by a
 // host-made, cost-balanced plan (built and uploaded once per shape, which
-// allocates); otherwise, or without allow_plan, the snake order.
+// allocates, except during stream capture); otherwise, or without
+// allow_plan, the snake order.
 // A cost-balanced assignment of the (batch, head, query tile) units, longest
 // first, to P persistent CTAs: device table [P][*stride] of unit indices
 // (-1 ends a row), made on first use of a shape and kept (relattn_tc64.cu).
-cudaError_t unit_plan(int B, int H, int W, int M, int P, const int** table, int* stride);
+// While `stream` is being captured and the shape has no plan yet, *table is
+// set to nullptr (the caller keeps the snake order) and nothing is allocated.
+cudaError_t unit_plan(int B, int H, int W, int M, int P, cudaStream_t stream, const int** table, int* stride);
 
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
