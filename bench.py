@@ -430,6 +430,23 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
                          "per_launch_work": f"{flops} counted flops = 2*B*H*D*(4*(W*M + W(W+1)/2) + 2*W(W+1)/2)"}}
 
 
+def host_link_gbs(nbytes, device, reps=3):
+    """Host -> device copy rate of one pinned buffer of nbytes, best of reps."""
+    import torch
+
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    best = 0.0
+    for _ in range(reps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        d.copy_(h, non_blocking=True)
+        b.record()
+        torch.cuda.synchronize()
+        best = max(best, nbytes / (a.elapsed_time(b) / 1e3) / 1e9)
+    return best
+
+
 def measure_configs(device, steps, warmup, peak, peak_src):
     """The other full-size training shapes, one steady segment per step
     through txl_relattn_forward_roll (attention and the memory roll): large
@@ -810,6 +827,7 @@ def _run_ours_sampled(args, txl, stream, wl, world, rank, local, device, cs, sam
     # end to end through the public API with host buffers
     E = max(1, min(K, 50))
     torch.cuda.synchronize()
+    link_gbs = host_link_gbs(stream.e2e_bytes()[0], device)  # the link's state right now
     barrier(world)
     e2e_el, _ = stream.run_e2e(args.warmup + K, E)
     e2e_s = max_over_ranks(e2e_el, world)
@@ -847,7 +865,11 @@ def _run_ours_sampled(args, txl, stream, wl, world, rank, local, device, cs, sam
                      "per_launch_work": f"{flops} counted flops = 6*B*H*D*(W*M + W(W+1)/2)"},
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "call": "txl_sinusoid_rel + txl_relattn_forward_ring_append (memory as a ring of M+W rows; q and "
-                        "the new k, v rows uploaded contiguous, o read back, both on copy streams)"},
+                        "the new k, v rows uploaded contiguous, o read back, both on copy streams)",
+                "host_link_h2d_gbs": link_gbs,
+                "host_link_note": "one pinned host->device copy of a step's upload bytes just before the loop "
+                                  "(best of 3); the link is shared with the machine's other jobs (~200 GB/s "
+                                  "when quiet)"},
         "gpu_launches": launches,
         "clocks": sampler.summary(h0, h1),
     }
