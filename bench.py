@@ -566,7 +566,55 @@ def measure_long_memory(device, steps, warmup, peak, peak_src):
         raise RuntimeError("device status reported a timed-out wait in the long-memory steps")
     out["peak_source"] = f"{peak_src} bf16_tflops (burst)"
     out["per_step_work"] = f"{flops} counted flops = 6*B*H*D*(W*M + W(W+1)/2)"
+    del qd, kd, vd, kb, vb, k_ring, v_ring, k_seg, v_seg, o
+    out["m_sweep"] = measure_m_sweep(device, wl, steps, warmup, peak, flush)
     return out
+
+
+def measure_m_sweep(device, wl, steps, warmup, peak, flush, m_values=(0, 384, 1600, 3200)):
+    """Attention alone (txl_relattn_forward) at the long workload's W=128,
+    B=4 H=16 D=64, over memories of M = 0, 384, 1600 and 3200 seeded rows
+    (the evaluation memory grown past the training length).  One segment per
+    step, CUDA events around the call, L2 flushed in between."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import make_prefilled, project_r
+
+    bf = torch.bfloat16
+    to = lambda a, dt=bf: torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dt)
+    cs = torch.cuda.current_stream()
+    rows = []
+    for M in m_values:
+        wm = wl.__class__(wl.name, wl.cfg_id, wl.B, wl.H, wl.D, wl.d_model, wl.W, M, 1, wl.dtype)
+        B, H, D, W = wm.B, wm.H, wm.D, wm.W
+        q, k, v, seg = make_prefilled(wm, M)
+        qd, kd, vd = to(q), to(k), to(v)
+        R = torch.empty(M + W, wm.d_model, device=device)
+        txl.txl_sinusoid_rel(R)
+        rd = to(project_r(R.cpu().numpy(), seg.W_r, H, D, "bf16"))
+        ud, vbd = to(seg.bias_u, torch.float32), to(seg.bias_v, torch.float32)
+        o = torch.empty(qd.shape, device=device, dtype=bf)
+        ts = []
+        for it in range(warmup + steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cs)
+            txl.txl_relattn_forward(qd, kd, vd, rd, ud, vbd, o, M=M)
+            b.record(cs)
+            if it >= warmup:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        if txl.txl_get_device_status() != 0:
+            raise RuntimeError(f"device status reported a timed-out wait in the M={M} sweep step")
+        ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+        tf = counted_flops(B, H, D, W, M) / (ms / 1e3) / 1e12
+        rows.append({"M": M, "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "steps": len(ts),
+                     "tflops": tf, "frac_of_bf16_peak": tf / peak})
+        del qd, kd, vd, rd, o
+    return {"workload": f"B={wl.B} H={wl.H} D={wl.D} W={wl.W}, memory pre-filled with M seeded rows, "
+                        f"txl_relattn_forward alone, bf16",
+            "l2": "flushed between steps (256 MB write, outside the events)", "points": rows}
 
 
 def measure_cached_vs_recompute(device, long_ring_ms, steps, warmup):
