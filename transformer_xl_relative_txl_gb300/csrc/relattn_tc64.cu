@@ -143,6 +143,7 @@ struct Bars {
   uint64_t mma_final, pv_final, qr_final;
   uint64_t lbar[4];   // per quadrant: the non-owning warp's (m, l) of a unit is in `red`
   uint64_t lfree[4];  // per quadrant: the epilogue has read it
+  int vq[4][5];       // loader: queued V tiles (key row, batch, head, roll, unit ordinal), by V count % 4
   uint32_t tmem_base;
   int abort;
 };
@@ -257,6 +258,55 @@ __global__ void __launch_bounds__(kThreads, 1)
         ++nQ;
         return true;
       };
+      // K or V tile of key row kr (a multiple of 64) of batch b, head h into
+      // the next stage of its stream; rl: the unit keeps these rows (roll).
+      auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, const CUtensorMap* map, int kr,
+                         int b, int h, bool rl, int* prow, int* pb, int* ph, const CUtensorMap* rmap,
+                         const CUtensorMap* smap) -> bool {
+        const int s = static_cast<int>(n % NK);
+        if (!mbar_wait(&empty[s], ((n / NK) & 1) ^ 1, wait_ns, abort)) return false;
+        flush_store(prow, pb, ph, s, rmap, dst + s * kRowTile);
+        mbar_arrive_expect_tx(&full[s], kRowTile);
+        if constexpr (RING) {
+          if (kr < p.M)  // start + kr < 2 cap: one conditional wrap
+            tma_load_4d(dst + s * kRowTile, map, &full[s], 0, h,
+                        p.ring_start + kr - (p.ring_start + kr >= p.ring_cap ? p.ring_cap : 0), b);
+          else
+            tma_load_4d(dst + s * kRowTile, smap, &full[s], 0, h, kr - p.M, b);
+        } else {
+          tma_load_4d(dst + s * kRowTile, map, &full[s], 0, h, kr, b);
+        }
+        if constexpr (RING)
+          prow[s] = (rl && kr >= p.M)  // start + kr < start + M + W <= 2 cap
+                        ? p.ring_start + kr - (p.ring_start + kr >= p.ring_cap ? p.ring_cap : 0)
+                        : -1;
+        else
+          prow[s] = (rl && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
+        pb[s] = b;
+        ph[s] = h;
+        ++n;
+        return true;
+      };
+      // V tiles trail the K and R tiles by kVLag tiles.  A V stage is freed
+      // only when the P.V MMA of its step completes, after that step's
+      // softmax, while a K stage is free as soon as its score MMA is done; in
+      // one issue order K(t), R(t+1), V(t), every K load would wait behind
+      // the V stage of step t-4 and land just in time (the score issuer then
+      // waits for it).  With V(t-2) after K(t), K and R run up to their full
+      // stage depth ahead, and V(t) still lands two steps before its P.V.
+      // Queued V tiles wait in bars->vq (this thread only).  Before the raw
+      // q of the unit after next is loaded, every queued V of a unit two or
+      // more back goes out: that load waits for the (q+u), (q+v) build of the
+      // next unit, which waits for the epilogue of the unit before, which
+      // needs all of that unit's V tiles (a unit of one step would otherwise
+      // hold them behind the load).
+      constexpr uint32_t kVLag = 2;
+      uint32_t nVq = 0;  // V tiles queued; nVq - nV of them not yet issued
+      auto issue_v = [&]() -> bool {
+        const int* e = bars->vq[nV % 4];
+        return load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, e[0], e[1], e[2], e[3] != 0, pv_row, pv_b, pv_h,
+                       RING ? &tm_v : &tm_vm, &tm_vs);
+      };
       if (const int u0 = unit_at(p.sched, p.sched_stride, 0, blockIdx.x, gridDim.x, p.n_units); u0 < p.n_units)
         ok = load_q(u0);
       for (int rd = 0;; ++rd) {
@@ -264,6 +314,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!ok || stop || u >= p.n_units) break;
         const int un_next = unit_at(p.sched, p.sched_stride, rd + 1, blockIdx.x, gridDim.x, p.n_units);
         const Unit w = decode_item(u, kSplit, p.B, p.H, p.W, p.M, p.nqt);
+        while (ok && nV < nVq && bars->vq[nV % 4][4] <= rd - 2) ok = issue_v();
+        if (!ok) break;
         if (un_next < p.n_units && !(ok = load_q(un_next))) break;
         auto load_r = [&](int d0) -> bool {
           if (!acquire(bars->emptyR, bars->fullR, nR, NR, kRowTile)) return false;
@@ -275,34 +327,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         // segment's rows into ring rows (start + M + x) % cap, which no unit
         // of this launch reads)
         const bool rolls = (RING ? p.ring_append != 0 : p.roll_src0 >= 0) && w.i0 + BM >= p.W;
-        auto load_kv = [&](uint64_t* empty, uint64_t* full, uint8_t* dst, uint32_t& n, const CUtensorMap* map,
-                           int t, int* prow, int* pb, int* ph, const CUtensorMap* rmap,
-                           const CUtensorMap* smap) -> bool {
-          const int s = static_cast<int>(n % NK);
-          if (!mbar_wait(&empty[s], ((n / NK) & 1) ^ 1, wait_ns, abort)) return false;
-          flush_store(prow, pb, ph, s, rmap, dst + s * kRowTile);
-          mbar_arrive_expect_tx(&full[s], kRowTile);
-          const int kr = (w.t0 + t) * BN;  // first key row of the tile
-          if constexpr (RING) {
-            if (kr < p.M)  // start + kr < 2 cap: one conditional wrap
-              tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h,
-                          p.ring_start + kr - (p.ring_start + kr >= p.ring_cap ? p.ring_cap : 0), w.b);
-            else
-              tma_load_4d(dst + s * kRowTile, smap, &full[s], 0, w.h, kr - p.M, w.b);
-          } else {
-            tma_load_4d(dst + s * kRowTile, map, &full[s], 0, w.h, kr, w.b);
-          }
-          if constexpr (RING)
-            prow[s] = (rolls && kr >= p.M)  // start + kr < start + M + W <= 2 cap
-                          ? p.ring_start + kr - (p.ring_start + kr >= p.ring_cap ? p.ring_cap : 0)
-                          : -1;
-          else
-            prow[s] = (rolls && kr >= p.roll_src0) ? kr - p.roll_src0 : -1;
-          pb[s] = w.b;
-          ph[s] = w.h;
-          ++n;
-          return true;
-        };
         // distance tiles -2 and -1 of the item's first step
         ok = load_r(p.M + w.i0 - BN * (w.t0 - 1)) && load_r(p.M + w.i0 - BN * w.t0);
         for (int t = 0; ok && t < w.nks; ++t) {
@@ -310,13 +334,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             stop = true;
             break;
           }
-          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, t, pk_row, pk_b, pk_h, RING ? &tm_k : &tm_km,
-                       &tm_ks) &&
-               load_r(p.M + w.i0 - BN * (w.t0 + t + 1)) &&
-               load_kv(bars->emptyV, bars->fullV, sV, nV, &tm_v, t, pv_row, pv_b, pv_h, RING ? &tm_v : &tm_vm,
-                       &tm_vs);
+          const int kr = (w.t0 + t) * BN;  // first key row of the tile
+          ok = load_kv(bars->emptyK, bars->fullK, sK, nK, &tm_k, kr, w.b, w.h, rolls, pk_row, pk_b, pk_h,
+                       RING ? &tm_k : &tm_km, &tm_ks) &&
+               load_r(p.M + w.i0 - BN * (w.t0 + t + 1));
+          if (ok) {
+            int* e = bars->vq[nVq % 4];
+            e[0] = kr;
+            e[1] = w.b;
+            e[2] = w.h;
+            e[3] = rolls;
+            e[4] = rd;
+            ++nVq;
+            if (nVq - nV > kVLag) ok = issue_v();
+          }
         }
       }
+      while (ok && !stop && nV < nVq) ok = issue_v();  // the last kVLag V tiles
       if (!ok) report_timeout(abort, p.status);
       auto drain = [&](uint64_t* full, uint32_t n, int ns) {
         for (int s = 0; s < ns && static_cast<uint32_t>(s) < n; ++s) {
