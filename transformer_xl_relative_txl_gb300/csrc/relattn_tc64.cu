@@ -294,13 +294,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       // the V stage of step t-4 and land just in time (the score issuer then
       // waits for it).  With V(t-2) after K(t), K and R run up to their full
       // stage depth ahead, and V(t) still lands two steps before its P.V.
+      // Only the plain instantiation trails, the one where the gain was
+      // measured; with split key ranges (about one item per CTA, whose first
+      // P.V would wait longer for V) and with ring memory the two orders time
+      // the same within the noise, so those keep V(t) right after K(t).
       // Queued V tiles wait in bars->vq (this thread only).  Before the raw
       // q of the unit after next is loaded, every queued V of a unit two or
       // more back goes out: that load waits for the (q+u), (q+v) build of the
       // next unit, which waits for the epilogue of the unit before, which
       // needs all of that unit's V tiles (a unit of one step would otherwise
       // hold them behind the load).
-      constexpr uint32_t kVLag = 2;
+      constexpr uint32_t kVLag = (SPLIT || RING) ? 0 : 2;
       uint32_t nVq = 0;  // V tiles queued; nVq - nV of them not yet issued
       auto issue_v = [&]() -> bool {
         const int* e = bars->vq[nV % 4];
