@@ -141,6 +141,12 @@ SHAPES = [
     (1, 2, 128, 200, 150),
     (2, 1, 128, 256, 128),
     (1, 1, 128, 129, 1),
+    # more units than SMs, so every CTA runs several: one-step units (the
+    # loader's queued V tiles of a unit two back go out before the next raw q
+    # load) and two-step units.  The units come from the batch: H stays at 8
+    # (d_model 512), so the value entries keep the workloads' size.
+    (64, 8, 64, 64, 0),
+    (40, 8, 64, 100, 20),
 ]
 
 
@@ -312,6 +318,8 @@ ROLL_CASES = [
     (1, 2, 128, 64, 1000, 1000), # D = 128 fused: kept rows start inside the memory
     (1, 1, 128, 128, 0, 512),    # D = 128 fused: every row kept
     (2, 2, 64, 128, 64, 0),      # m = 0: no roll
+    (64, 8, 64, 64, 0, 64),      # fused, 512 one-step units (several per CTA), every row kept
+    (24, 8, 64, 128, 64, 64),    # fused, 192 two-step units
 ]
 
 
