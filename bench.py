@@ -447,6 +447,103 @@ def host_link_gbs(nbytes, device, reps=3):
     return best
 
 
+def oracle_segment_s(q, k, v, r, bu, bv, M, budget_s=4.0):
+    """The float64 oracle (as it stands) on one segment of a workload: timed on
+    as many whole sequences (all heads) as fit the budget, one at a time,
+    and scaled to the whole batch."""
+    from oracle import txl_oracle as O
+
+    B = q.shape[0]
+    n, t0 = 0, time.perf_counter()
+    c0 = time.process_time()
+    while n < B:
+        O.relattn_forward(q[n:n + 1], k[n:n + 1], v[n:n + 1], r, bu, bv, M)
+        n += 1
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    cpu = time.process_time() - c0
+    return {"s_per_segment": el / n * B, "cores": max(1, round(cpu / el)),
+            "sample": f"{n} of {B} sequences (all heads), float64 numpy, {el:.1f} s wall, scaled to B"}
+
+
+def measure_roll(device, steps, warmup, hbm_peak, peak_src):
+    """The memory roll alone (txl_mem_update of k and of v: the last M rows of
+    [memory ; segment] into the next segment's buffer) on the four bf16
+    workloads' steady segments, CUDA events around the two launches, L2
+    flushed in between.  Algorithmic bytes: k and v, each read once and
+    written once, 2 * 2 * B * M * H * D * 2.  Beside it, what the roll costs
+    inside the attention kernel on base: the fused call
+    (txl_relattn_forward_roll) minus the attention alone (txl_relattn_forward),
+    interleaved."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import WORKLOADS, make_prefilled
+
+    bf = torch.bfloat16
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
+    cs = torch.cuda.current_stream()
+    out = {"l2": "flushed between steps (256 MB write, outside the events)",
+           "peak_source": f"{peak_src} hbm_gbs", "bytes": "2 tensors (k, v) x (read + write) x B*M*H*D*2"}
+    for name in ("base", "large", "wide", "long"):
+        wl = WORKLOADS[name]
+        B, H, D, W, M = wl.B, wl.H, wl.D, wl.W, wl.M
+        C = H * D
+        src = [torch.randn(B, M + W, C, device=device).to(bf) for _ in range(2)]
+        dst = [torch.empty(B, M + W, C, device=device, dtype=bf) for _ in range(2)]
+        ts = []
+        for it in range(warmup + steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cs)
+            for x in range(2):
+                txl.txl_mem_update(src[x][:, :M], src[x][:, M:], dst[x], M)
+            b.record(cs)
+            if it >= warmup:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+        nbytes = 2 * 2 * B * M * C * 2
+        gbs = nbytes / (ms / 1e3) / 1e9
+        out[name] = {"call": "txl_mem_update on k, then on v (2 launches)", "bytes": nbytes, "ms": ms,
+                     "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "steps": len(ts)}
+        assert all(torch.equal(dst[x][:, :M], src[x][:, W:]) for x in range(2)), "roll result"
+        del src, dst
+    # the roll inside the attention kernel (base)
+    wl = WORKLOADS["base"]
+    B, H, D, W, M = wl.B, wl.H, wl.D, wl.W, wl.M
+    q, k, v, seg = make_prefilled(wl, M)
+    to = lambda a, dt=bf: torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dt)
+    qd, kd, vd = to(q), to(k), to(v)
+    rd = torch.randn(M + W, H, D, device=device).mul_(0.3).to(bf)
+    ud, vbd = to(seg.bias_u, torch.float32), to(seg.bias_v, torch.float32)
+    o = torch.empty(qd.shape, device=device, dtype=bf)
+    km, vm = torch.empty_like(kd), torch.empty_like(vd)
+    t_f, t_a = [], []
+    for it in range(warmup + steps):
+        for fused in (True, False):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(cs)
+            if fused:
+                txl.txl_relattn_forward_roll(qd, kd, vd, rd, ud, vbd, o, km[:, :M], vm[:, :M], M, M=M)
+            else:
+                txl.txl_relattn_forward(qd, kd, vd, rd, ud, vbd, o, M=M)
+            b.record(cs)
+            if it >= warmup:
+                (t_f if fused else t_a).append((a, b))
+    torch.cuda.synchronize()
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait in the roll measurement")
+    f_ms = float(np.mean([a.elapsed_time(b) for a, b in t_f]))
+    a_ms = float(np.mean([a.elapsed_time(b) for a, b in t_a]))
+    out["fused_base"] = {"call": "txl_relattn_forward_roll minus txl_relattn_forward (base, interleaved)",
+                         "with_roll_ms": f_ms, "attention_ms": a_ms, "roll_extra_us": (f_ms - a_ms) * 1e3,
+                         "steps": len(t_f)}
+    return out
+
+
 def measure_configs(device, steps, warmup, peak, peak_src):
     """The other full-size training shapes, one steady segment per step
     through txl_relattn_forward_roll (attention and the memory roll): large
@@ -494,7 +591,8 @@ def measure_configs(device, steps, warmup, peak, peak_src):
         out[name] = {"workload": f"{name}: B={B} H={H} D={D} W={W} M={M}, steady-state segment with the "
                                  f"memory roll, bf16",
                      "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "steps": len(ts),
-                     "tflops": tf, "frac_of_bf16_peak": tf / peak}
+                     "tflops": tf, "frac_of_bf16_peak": tf / peak,
+                     "oracle": oracle_segment_s(q, k, v, rd.float().cpu().numpy(), seg.bias_u, seg.bias_v, M)}
         del qd, kd, vd, kb, vb, o
     return out
 
@@ -566,6 +664,7 @@ def measure_long_memory(device, steps, warmup, peak, peak_src):
         raise RuntimeError("device status reported a timed-out wait in the long-memory steps")
     out["peak_source"] = f"{peak_src} bf16_tflops (burst)"
     out["per_step_work"] = f"{flops} counted flops = 6*B*H*D*(W*M + W(W+1)/2)"
+    out["oracle"] = oracle_segment_s(q, k, v, rd.float().cpu().numpy(), seg.bias_u, seg.bias_v, M)
     del qd, kd, vd, kb, vb, k_ring, v_ring, k_seg, v_seg, o
     out["m_sweep"] = measure_m_sweep(device, wl, steps, warmup, peak, flush)
     return out
@@ -610,7 +709,9 @@ def measure_m_sweep(device, wl, steps, warmup, peak, flush, m_values=(0, 384, 16
         ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
         tf = counted_flops(B, H, D, W, M) / (ms / 1e3) / 1e12
         rows.append({"M": M, "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "steps": len(ts),
-                     "tflops": tf, "frac_of_bf16_peak": tf / peak})
+                     "tflops": tf, "frac_of_bf16_peak": tf / peak,
+                     "oracle": oracle_segment_s(q, k, v, rd.float().cpu().numpy(), seg.bias_u, seg.bias_v, M,
+                                                budget_s=2.0)})
         del qd, kd, vd, rd, o
     return {"workload": f"B={wl.B} H={wl.H} D={wl.D} W={wl.W}, memory pre-filled with M seeded rows, "
                         f"txl_relattn_forward alone, bf16",
@@ -898,9 +999,10 @@ def _run_ours_sampled(args, txl, stream, wl, world, rank, local, device, cs, sam
                    "parallelism": f"dp{world} (each rank its own {wl.B} sequences)",
                    "l2": f"inputs larger than L2: {N_SEG_BUFFERS} rotating segment buffers "
                          f"(~{N_SEG_BUFFERS * (2 * wl.B * (wl.M + wl.W) + wl.B * wl.W) * wl.H * wl.D * 2 / 1e9:.2f} GB)",
-                   "step": "txl_sinusoid_rel (on a stream of its own: no kernel of the step reads the table) "
-                           "+ txl_relattn_forward_roll (attention and the memory roll of k and v in one kernel); "
-                           "the timed region waits for both streams",
+                   "step": "txl_sinusoid_rel (on a stream of its own: no kernel of the step reads the table, "
+                           "whose projection r = R W_r is the host step upstream of the path, outside the timed "
+                           "region) + txl_relattn_forward_roll (attention and the memory roll of k and v in one "
+                           "kernel); the timed region waits for both streams",
                    "kernel_timing": f"attention kernel bracketed by CUDA events on the last timed step of "
                                     f"every {EVENT_EVERY} ({len(evs)} samples; the first step, launched onto "
                                     f"an idle queue, is not sampled)"},
@@ -922,6 +1024,8 @@ def _run_ours_sampled(args, txl, stream, wl, world, rank, local, device, cs, sam
         "clocks": sampler.summary(h0, h1),
     }
     result["backward"] = measure_backward(stream, wl, max(5, min(K, 50)), 3, peak, peak_src)
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    result["roll"] = measure_roll(device, max(5, min(K, 50)), 3, hbm, peak_src)
     result["configs"] = measure_configs(device, max(5, min(K, 50)), 3, peak, peak_src)
     result["long_memory"] = measure_long_memory(device, max(5, min(K, 50)), 3, peak, peak_src)
     result["cached_vs_recompute"] = measure_cached_vs_recompute(device, result["long_memory"]["ring"]["ms"], 10, 3)

@@ -18,6 +18,13 @@
  *   - Pointers marked "device" are device memory owned by the caller; the
  *     library never allocates, frees or retains them.  Host pointers are only
  *     read or written during the call.
+ *   - Library-owned memory.  Some calls keep device memory of their own, each
+ *     named in the call's comment under "Allocates": per-(device, stream)
+ *     scratch, made with cudaMalloc on the first call that needs it and
+ *     regrown (stream synchronised, old buffer freed) when a later call needs
+ *     more; and per-shape unit plans of the bf16 attention kernels (below).
+ *     Both are kept until txl_release_cached or process exit.
+ *     txl_relattn_forward_static and txl_mem_update allocate nothing.
  *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
  *     returns a txl_status code.  Argument errors are detected on the host before
  *     any launch, and then nothing is launched.  A failed launch returns
@@ -102,6 +109,20 @@ typedef enum {
  * Requirements: q, k, v, r and o 16-byte aligned (TXL_ERR_INVALID_ARG
  * otherwise); o must not overlap q, k, v, r, bias_u, bias_v or lse
  * (TXL_ERR_ALIAS).  Memory rows are only read (stop-gradient).
+ *
+ * Allocates (bf16 path only; the fp32 path allocates nothing):
+ *   - unit plan: with more (batch, head, 128-query tile) units than SMs, the
+ *     first call of a shape on a device builds a cost-balanced assignment of
+ *     units to the persistent CTAs: a small pinned host buffer and device
+ *     table (about 4 * (units + SMs) bytes) plus an event, uploaded by an
+ *     asynchronous copy on `stream` (the host does not wait for it).  No plan
+ *     is made while `stream` is being captured, nor for a new shape once 256
+ *     shapes hold one: those calls deal the units in a fixed order instead,
+ *     with the same result;
+ *   - split scratch: with fewer units than SMs (D = 64), each unit's key
+ *     range is split across CTAs and the partial results take
+ *     units * chunks * 128 * 65 * 4 bytes, plus units * 16 bytes of merge
+ *     counters, per (device, stream) (see the conventions above).
  */
 TXL_API int txl_relattn_forward(const void* q, const void* k, const void* v, const void* r,
                         const float* bias_u, const float* bias_v, void* o, float* lse,
@@ -111,18 +132,30 @@ TXL_API int txl_relattn_forward(const void* q, const void* k, const void* v, con
 /*
  * txl_relattn_forward_static -- txl_relattn_forward that allocates nothing.
  *
- * Same arguments, result and errors as txl_relattn_forward (bit for bit: the
- * same kernels run).  When a launch has too few (batch, head, query-tile)
- * units to fill the GPU, txl_relattn_forward splits each unit's key range
- * across CTAs and keeps the partial results in scratch that the library
- * allocates per (device, stream) on first use.  This entry point uses instead
- * a fixed 16 MiB device array inside the library (at most 4096 units x 4
- * merge counters, then the partial results); a split that needs more returns
- * TXL_ERR_UNSUPPORTED.  It makes no allocation of any kind, so it may be
- * called where allocating is not allowed (for instance while a stream is
- * being captured into a graph).  The array is shared by all such calls on a
- * device: they must not run concurrently on different streams.  The pages
- * have no counterpart; this is a property of the implementation only.
+ * For callers that cannot call cudaMalloc: a host that has handed all device
+ * memory to its own pool up front, code running inside another library's
+ * allocator or memory callbacks, or a loop that must never stall on the
+ * allocator (cudaMalloc and cudaFree can synchronise the device).  Same
+ * arguments, result and errors as txl_relattn_forward, bit for bit (the same
+ * kernels run); the units are dealt in a fixed order, never by a plan.
+ *
+ * When a launch has too few units to fill the GPU, its key ranges are split
+ * across CTAs and the partial results need scratch.  This entry point keeps
+ * that scratch in one fixed 16 MiB array inside the library (a __device__
+ * array that every GPU loading the library holds until exit): at most 4096
+ * merge counters (1024 units), then at most 16 MiB - 16 KiB of partial
+ * results; a split that needs more returns TXL_ERR_UNSUPPORTED before any
+ * launch.  Launches that do not split use no scratch.
+ *
+ * Set-up: the first call on each device (made current) looks the array's
+ * device address up with cudaGetSymbolAddress, which may load the library's
+ * device code; make that first call before any stream capture.  Every call
+ * on a device shares the one array, which keeps what the last call left: the
+ * merge counters must start at zero, and each launch returns them to zero
+ * (after a reported TXL_ERR_DEVICE_TIMEOUT, txl_get_device_status zeroes
+ * them).  Calls whose kernels overlap on the GPU (different streams without
+ * ordering between them) race on the array and give undefined results.  The
+ * pages have no counterpart; this is a property of the implementation only.
  */
 TXL_API int txl_relattn_forward_static(const void* q, const void* k, const void* v, const void* r,
                                const float* bias_u, const float* bias_v, void* o, float* lse,
@@ -133,9 +166,10 @@ TXL_API int txl_relattn_forward_static(const void* q, const void* k, const void*
  * txl_mem_update -- the memory roll.
  *
  * Defines mem_tau = last M rows of [stop_grad(mem_{tau-1}) ; h_tau] from the
- * "Long-context transformers" simulation's segment-recurrence equations (and
- * the glossary loop's `memory = segment.detach()` when M equals the segment
- * length).  Rows are copied bit for bit.
+ * "Long-context transformers" simulation's segment-recurrence equations (the
+ * "Transformer-XL" glossary page's recurrence example is the case M equal to
+ * the segment length: the detached segment becomes the memory).  Rows are
+ * copied bit for bit.  Allocates nothing.
  *
  *   mem      device, [B, m_prev, C] rows, batch stride mem_bs elements  (may be
  *            NULL when m_prev == 0)
@@ -179,7 +213,7 @@ TXL_API int txl_mem_update(const void* mem, int m_prev, const void* h, int w, vo
  * stores; otherwise the call runs the attention and then the roll kernel.
  * Other arguments and errors as txl_relattn_forward and txl_mem_update.  This
  * fused form has no counterpart on the pages: it is a scheduling of their
- * two steps.
+ * two steps.  Allocates what txl_relattn_forward allocates for the shape.
  */
 TXL_API int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const void* r,
                              const float* bias_u, const float* bias_v, void* o, float* lse,
@@ -210,8 +244,9 @@ TXL_API int txl_relattn_forward_roll(const void* q, const void* k, const void* v
  *
  * On the bf16 D = 64 path with cap, start and M multiples of 64 the kernel
  * reads the ring in place (a key tile never wraps); otherwise the call first
- * copies [memory ; segment] into library scratch per (device, stream),
- * allocated on first use.
+ * copies [memory ; segment] into library scratch per (device, stream)
+ * (2 * B * (M+W) * H * D elements; see the conventions above).  Allocates
+ * that scratch and what txl_relattn_forward allocates for the shape.
  */
 TXL_API int txl_relattn_forward_ring(const void* q, const void* k_mem, const void* v_mem, int cap, int start,
                              int M, const void* k_seg, const void* v_seg, const void* r,
@@ -228,6 +263,7 @@ TXL_API int txl_relattn_forward_ring(const void* q, const void* k_mem, const voi
  * slots the memory does not occupy, so the attention kernel stores them from
  * the tiles it loads while it runs.  Otherwise the three calls run in order.
  * Arguments as in the two calls; k_seg and v_seg must not overlap the rings.
+ * Allocates what txl_relattn_forward_ring allocates.
  */
 TXL_API int txl_relattn_forward_ring_append(void* k_mem, void* v_mem, int cap, int start, int M,
                                     const void* q, const void* k_seg, const void* v_seg, const void* r,
@@ -253,6 +289,7 @@ TXL_API int txl_relattn_forward_ring_append(void* k_mem, void* v_mem, int cap, i
  *
  * Run it after the attention that reads the ring (stream order): it
  * overwrites the oldest rows.  h must not overlap the ring (TXL_ERR_ALIAS).
+ * Allocates nothing.
  */
 TXL_API int txl_mem_ring_append(void* mem, int cap, int start, int m, const void* h, int w, int B, int C,
                         long long h_bs, int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream);
@@ -293,7 +330,11 @@ TXL_API int txl_mem_ring_append(void* mem, int cap, int start, int m, const void
  * else this library's kernels add the fp32 vectors to the rounded
  * products.  When W_k starts right after W_q and W_v right after W_k (one
  * [3, d_model, H*D] allocation), the three projections run as one batched
- * GEMM.  Every other step runs in this library's kernels.
+ * GEMM.  Every other step runs in this library's kernels.  Every
+ * intermediate lives in `workspace`; the attention inside may make a unit
+ * plan as txl_relattn_forward does, and when the ring cannot be read in
+ * place (cap, start or M not multiples of 64) it takes the ring scratch of
+ * txl_relattn_forward_ring.
  */
 typedef struct {
   const void* W_q;        /* [d_model, H*D] */
@@ -357,9 +398,9 @@ TXL_API int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem
  * cores (tcgen05): a dq kernel over query tiles (which also sums dr and the
  * bias gradients) and a dk/dv kernel over 64-key blocks; there dr arrives by
  * fp32 atomic adds, so its last bits may differ between calls.  Every other
- * case runs on CUDA cores in fp32 arithmetic, fully deterministic.  Library
- * scratch (per-row Delta and per-tile partial sums) is allocated per (device,
- * stream) on first use and reused.
+ * case runs on CUDA cores in fp32 arithmetic, fully deterministic.
+ * Allocates: per-(device, stream) scratch for the per-row Delta and the
+ * per-tile partial sums (see the conventions above).
  */
 TXL_API int txl_relattn_backward(const void* q, const void* k, const void* v, const void* r,
                          const float* bias_u, const float* bias_v, const void* o, const float* lse,
@@ -383,6 +424,7 @@ TXL_API int txl_relattn_backward(const void* q, const void* k, const void* v, co
  *
  *   R      device, [n_dist, dim] `dtype`
  *   dim    even, >= 2;  n_dist >= 0 (0 is an empty call)
+ * Allocates nothing.
  */
 TXL_API int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cudaStream_t stream);
 
@@ -394,6 +436,15 @@ TXL_API int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cuda
  * TXL_ERR_CUDA if the synchronisation itself failed.
  */
 TXL_API int txl_get_device_status(cudaStream_t stream);
+
+/*
+ * txl_release_cached -- synchronises the current device, then frees the
+ * library-owned memory kept for it: every stream's split, ring and backward
+ * scratch and every unit plan.  Later calls make them again as needed.  No
+ * call of this library may be in flight on the device from another thread.
+ * Returns TXL_OK or TXL_ERR_CUDA.
+ */
+TXL_API int txl_release_cached(void);
 
 /* Human-readable name of a txl_status value (static string). */
 TXL_API const char* txl_status_string(int status);

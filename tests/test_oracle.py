@@ -158,12 +158,13 @@ def pin_bruteforce(fwd):
         np.testing.assert_allclose(l1, l2, rtol=0, atol=1e-12)
 
 
-def _global_banded(qs, ks, vs, r, u, vb, W, M, scale):
+def _global_banded(qs, ks, vs, r, u, vb, W, M, scale, with_lse=False):
     """Attention over the whole concatenated stream at global positions t:
     query t of segment tau sees keys t' in [tau*W - M_tau, t] with
     M_tau = min(M, tau*W), distance t - t'.  Explicit loops, one head."""
     T = qs.shape[0]
     o = np.zeros_like(qs)
+    lse = np.zeros(T)
     for t in range(T):
         tau = t // W
         lo = tau * W - min(M, tau * W)
@@ -171,7 +172,8 @@ def _global_banded(qs, ks, vs, r, u, vb, W, M, scale):
         s = np.array([scale * ((qs[t] + u) @ ks[tp] + (qs[t] + vb) @ r[t - tp]) for tp in idx])
         e = np.exp(s - s.max())
         o[t] = (e / e.sum()) @ vs[idx]
-    return o
+        lse[t] = s.max() + np.log(e.sum())
+    return (o, lse) if with_lse else o
 
 
 def pin_recurrence(fwd):
@@ -447,3 +449,96 @@ def test_unmutated_copy_passes_all_pins():
     fwd = _mutant("none")
     for pin in PINS:
         pin(fwd)
+
+
+# ----------------------------------------------------------------------------
+# The oracle's segment recurrence (run_segments), pinned by itself: it gives
+# the expected values of every multi-segment GPU test, so the function that
+# runs the segments -- not a copy of its loop -- is checked against one
+# attention over the concatenated stream at global positions.
+# ----------------------------------------------------------------------------
+
+RECURRENCE_CASES = [(4, 4, 3), (3, 5, 4), (5, 2, 3), (4, 0, 2), (2, 7, 5), (3, 9, 6)]
+
+
+def pin_segment_recurrence(run):
+    """``run`` has run_segments' signature.  Per segment tau: M_tau is
+    min(M, tau*W) ("Long-context transformers": the memory is the last M
+    rows of [memory ; segment], empty before the first segment), and o, lse
+    equal the banded attention over the whole stream (each query sees the
+    M_tau rows before its segment and its segment up to itself)."""
+    rng = np.random.default_rng(11)
+    for (W, M, S) in RECURRENCE_CASES:
+        H, D = 2, 3
+        T = W * S
+        qs = rng.standard_normal((2, T, H, D))
+        ks = rng.standard_normal((2, T, H, D))
+        vs = rng.standard_normal((2, T, H, D))
+        r = rng.standard_normal((M + W + T, H, D))  # spare rows: a memory too long stays a wrong value
+        u = rng.standard_normal((H, D)) * 0.3
+        vb = rng.standard_normal((H, D)) * 0.3
+        segs = lambda a: [a[:, t * W:(t + 1) * W] for t in range(S)]
+        out = run(segs(qs), segs(ks), segs(vs), r, u, vb, M, 0.7)
+        assert len(out) == S
+        for tau, (o, lse, m_tau) in enumerate(out):
+            assert m_tau == min(M, tau * W), (W, M, tau, m_tau)
+            assert o.shape == (2, W, H, D) and lse.shape == (2, H, W)
+        for b in range(2):
+            for h in range(H):
+                ref_o, ref_l = _global_banded(qs[b, :, h], ks[b, :, h], vs[b, :, h], r[:, h], u[h], vb[h],
+                                              W, M, 0.7, with_lse=True)
+                got_o = np.concatenate([o[b, :, h] for o, _, _ in out])
+                got_l = np.concatenate([lse[b, h] for _, lse, _ in out])
+                np.testing.assert_allclose(got_o, ref_o, rtol=0, atol=1e-12)
+                np.testing.assert_allclose(got_l, ref_l, rtol=0, atol=1e-12)
+
+
+def test_run_segments_pinned():
+    pin_segment_recurrence(O.run_segments)
+
+
+def _run_segments_mutant(kind):
+    """A copy of the recurrence with one plausible mistake planted."""
+    def run(q_segs, k_segs, v_segs, r, bias_u, bias_v, M, scale=None):
+        B, W, H, D = q_segs[0].shape
+        mem_k = np.zeros((B, 0, H, D))
+        mem_v = np.zeros((B, 0, H, D))
+        out = []
+
+        def roll(mem, new, keep_src=None):
+            cat = np.concatenate([mem, new], axis=1)
+            if kind == "keep_first_rows":
+                return cat[:, :min(M, cat.shape[1])]
+            if kind == "no_truncation":
+                return cat
+            if kind == "segment_only":
+                return new[:, new.shape[1] - min(M, W):]
+            return cat[:, cat.shape[1] - min(M, cat.shape[1]):]
+
+        for qs, ks, vs in zip(q_segs, k_segs, v_segs):
+            if kind == "roll_before_attention":
+                mem_k, mem_v = roll(mem_k, ks), roll(mem_v, vs)
+            m_tau = mem_k.shape[1]
+            kb = np.concatenate([mem_k, ks], axis=1)
+            vb_ = np.concatenate([mem_v, vs], axis=1)
+            o, lse = O.relattn_forward(qs, kb, vb_, r, bias_u, bias_v, m_tau, scale)
+            out.append((o, lse, m_tau))
+            if kind != "roll_before_attention":
+                mem_k = roll(mem_k, qs if kind == "memory_from_queries" else ks)
+                mem_v = roll(mem_v, ks if kind == "values_memory_from_keys" else vs)
+        return out
+    return run
+
+
+RECURRENCE_MUTANTS = ["roll_before_attention", "keep_first_rows", "no_truncation", "segment_only",
+                      "memory_from_queries", "values_memory_from_keys"]
+
+
+@pytest.mark.parametrize("kind", RECURRENCE_MUTANTS)
+def test_recurrence_pin_catches_planted_mistake(kind):
+    with pytest.raises(AssertionError):
+        pin_segment_recurrence(_run_segments_mutant(kind))
+
+
+def test_recurrence_unmutated_copy_passes():
+    pin_segment_recurrence(_run_segments_mutant("none"))

@@ -21,7 +21,7 @@ __all__ = [
     "txl_relattn_forward_ring_append", "txl_relattn_backward", "txl_mem_update", "txl_mem_ring_append",
     "txl_layer_forward", "txl_layer_workspace_bytes", "LAYER_WEIGHT_NAMES",
     "txl_sinusoid_rel",
-    "txl_get_device_status", "txl_status_string", "txl_version",
+    "txl_get_device_status", "txl_release_cached", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall", "txl_debug_force_split",
     "txl_debug_force_bias_kernels",
 ]
@@ -75,6 +75,8 @@ lib.txl_sinusoid_rel.argtypes = [_p, _i, _i, _i, _p]
 lib.txl_sinusoid_rel.restype = _i
 lib.txl_get_device_status.argtypes = [_p]
 lib.txl_get_device_status.restype = _i
+lib.txl_release_cached.argtypes = []
+lib.txl_release_cached.restype = _i
 lib.txl_status_string.argtypes = [_i]
 lib.txl_status_string.restype = ctypes.c_char_p
 lib.txl_version.argtypes = []
@@ -409,6 +411,12 @@ def txl_sinusoid_rel(R, stream=None):
 
 def txl_get_device_status(stream=None) -> int:
     return lib.txl_get_device_status(_stream(stream))
+
+
+def txl_release_cached() -> None:
+    """Frees the library's cached scratch and unit plans of the current device
+    (synchronises it first)."""
+    _check(lib.txl_release_cached(), "txl_release_cached")
 
 
 def txl_status_string(status: int) -> str:

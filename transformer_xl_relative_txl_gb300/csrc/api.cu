@@ -257,6 +257,35 @@ int txl_get_device_status(cudaStream_t stream) {
   return TXL_OK;
 }
 
+int txl_release_cached(void) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess) return TXL_ERR_CUDA;
+  int rc = TXL_OK;
+  {
+    std::lock_guard<std::mutex> lk(g_mutex);
+    for (auto it = g_scratch.begin(); it != g_scratch.end();) {
+      if (it->first.first != dev) {
+        ++it;
+        continue;
+      }
+      if ((it->second.ptr != nullptr && cudaFree(it->second.ptr) != cudaSuccess) ||
+          (it->second.cnt != nullptr && cudaFree(it->second.cnt) != cudaSuccess))
+        rc = TXL_ERR_CUDA;
+      it = g_scratch.erase(it);
+    }
+    for (auto it = g_gather.begin(); it != g_gather.end();) {
+      if (it->first.first != dev) {
+        ++it;
+        continue;
+      }
+      if (it->second.first != nullptr && cudaFree(it->second.first) != cudaSuccess) rc = TXL_ERR_CUDA;
+      it = g_gather.erase(it);
+    }
+  }
+  if (txl::release_plans(dev) != cudaSuccess) rc = TXL_ERR_CUDA;
+  return rc;
+}
+
 int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cudaStream_t stream) {
   if (n_dist < 0 || dim < 2 || (dim % 2) != 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
   if (n_dist == 0) return TXL_OK;

@@ -55,6 +55,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstring>
 #include <map>
 #include <mutex>
 #include <queue>
@@ -1005,41 +1006,102 @@ std::vector<int> plan_units(int B, int H, int W, int M, int P, int* stride_out) 
 }
 
 // Device copies of the plans, per (device, B, H, W, M, grid); made on first
-// use of a shape (a synchronous upload) and kept for the process.
+// use of a shape and kept until txl_release_cached.  The table is filled in
+// pinned host memory (kept with the entry, so the copy can read it at any
+// time) and uploaded with an asynchronous copy on the caller's stream; an
+// event recorded behind the copy orders it before launches on other streams.
+// At most kMaxPlans shapes are cached: later shapes run the snake order.
+struct PlanEntry {
+  int* dev_table = nullptr;
+  int* host_table = nullptr;
+  int stride = 0;
+  cudaEvent_t uploaded = nullptr;
+  bool done = false;  // the upload was seen complete
+};
+constexpr size_t kMaxPlans = 256;
 std::mutex g_plan_mutex;
-std::map<std::tuple<int, int, int, int, int, int>, std::pair<int*, int>> g_plans;
+std::map<std::tuple<int, int, int, int, int, int>, PlanEntry> g_plans;
+
+void free_plan(PlanEntry& p) {
+  if (p.uploaded != nullptr) cudaEventDestroy(p.uploaded);
+  if (p.dev_table != nullptr) cudaFree(p.dev_table);
+  if (p.host_table != nullptr) cudaFreeHost(p.host_table);
+  p = PlanEntry();
+}
 
 }  // namespace
 
 cudaError_t unit_plan(int B, int H, int W, int M, int P, cudaStream_t stream, const int** table, int* stride) {
+  *table = nullptr;
+  *stride = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if ((e = cudaStreamIsCapturing(stream, &cap)) != cudaSuccess) return e;
+  const bool capturing = cap != cudaStreamCaptureStatusNone;
   std::lock_guard<std::mutex> lk(g_plan_mutex);
-  auto& entry = g_plans[std::make_tuple(dev, B, H, W, M, P)];
-  if (entry.first == nullptr) {
+  const auto key = std::make_tuple(dev, B, H, W, M, P);
+  auto it = g_plans.find(key);
+  if (it == g_plans.end()) {
     // No plan yet: making one allocates and copies, which a stream being
-    // captured into a graph must not see; such a call keeps the snake order.
-    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
-    if ((e = cudaStreamIsCapturing(stream, &cap)) != cudaSuccess) return e;
-    if (cap != cudaStreamCaptureStatusNone) {
-      *table = nullptr;
-      *stride = 0;
-      return cudaSuccess;
-    }
+    // captured into a graph must not see; such a call keeps the snake order,
+    // and so does every shape past the cache's bound.
+    if (capturing || g_plans.size() >= kMaxPlans) return cudaSuccess;
     int st = 0;
     const std::vector<int> t = plan_units(B, H, W, M, P, &st);
-    int* d = nullptr;
-    if ((e = cudaMalloc(&d, t.size() * sizeof(int))) != cudaSuccess) return e;
-    if ((e = cudaMemcpy(d, t.data(), t.size() * sizeof(int), cudaMemcpyHostToDevice)) != cudaSuccess) {
-      cudaFree(d);
+    const size_t bytes = t.size() * sizeof(int);
+    PlanEntry pe;
+    pe.stride = st;
+    if ((e = cudaMallocHost(&pe.host_table, bytes)) != cudaSuccess ||
+        (e = cudaMalloc(&pe.dev_table, bytes)) != cudaSuccess ||
+        (e = cudaEventCreateWithFlags(&pe.uploaded, cudaEventDisableTiming)) != cudaSuccess) {
+      free_plan(pe);
       return e;
     }
-    entry = {d, st};
+    std::memcpy(pe.host_table, t.data(), bytes);
+    if ((e = cudaMemcpyAsync(pe.dev_table, pe.host_table, bytes, cudaMemcpyHostToDevice, stream)) != cudaSuccess ||
+        (e = cudaEventRecord(pe.uploaded, stream)) != cudaSuccess) {
+      // nothing was queued that could still read the buffers
+      cudaStreamSynchronize(stream);
+      free_plan(pe);
+      return e;
+    }
+    g_plans.emplace(key, pe);
+    *table = pe.dev_table;
+    *stride = pe.stride;
+    return cudaSuccess;  // this stream's launch follows the copy in stream order
   }
-  *table = entry.first;
-  *stride = entry.second;
+  PlanEntry& pe = it->second;
+  if (!pe.done) {
+    // The upload may still be queued on the stream that made the plan.  A
+    // stream being captured may not query or wait on it: snake order.
+    if (capturing) return cudaSuccess;
+    e = cudaEventQuery(pe.uploaded);
+    if (e == cudaSuccess) {
+      pe.done = true;
+    } else if (e == cudaErrorNotReady) {
+      if ((e = cudaStreamWaitEvent(stream, pe.uploaded, 0)) != cudaSuccess) return e;
+    } else {
+      return e;
+    }
+  }
+  *table = pe.dev_table;
+  *stride = pe.stride;
   return cudaSuccess;
+}
+
+cudaError_t release_plans(int dev) {
+  std::lock_guard<std::mutex> lk(g_plan_mutex);
+  for (auto it = g_plans.begin(); it != g_plans.end();) {
+    if (std::get<0>(it->first) == dev) {
+      free_plan(it->second);
+      it = g_plans.erase(it);
+    } else {
+      ++it;
+    }
+  }
+  return cudaGetLastError();
 }
 
 int relattn_tc64_split(int B, int H, int W, int M) {

@@ -75,10 +75,15 @@ struct RingMaps {
 // allow_plan, the snake order.
 // A cost-balanced assignment of the (batch, head, query tile) units, longest
 // first, to P persistent CTAs: device table [P][*stride] of unit indices
-// (-1 ends a row), made on first use of a shape and kept (relattn_tc64.cu).
-// While `stream` is being captured and the shape has no plan yet, *table is
-// set to nullptr (the caller keeps the snake order) and nothing is allocated.
+// (-1 ends a row), made on first use of a shape (a pinned host buffer, a
+// device buffer, an event and an asynchronous upload on `stream`) and kept
+// until release_plans (relattn_tc64.cu).  *table is set to nullptr (the
+// caller keeps the snake order, nothing is allocated) while `stream` is being
+// captured and the shape has no completed upload, and for new shapes once
+// 256 are cached.
 cudaError_t unit_plan(int B, int H, int W, int M, int P, cudaStream_t stream, const int** table, int* stride);
+// Frees every plan of device `dev` (no launch that reads one may be in flight).
+cudaError_t release_plans(int dev);
 
 cudaError_t launch_relattn_tc64(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const CUtensorMap& tm_v,
                                 const CUtensorMap& tm_r, const CUtensorMap* tm_o, const CUtensorMap* tm_km,
