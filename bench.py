@@ -492,23 +492,35 @@ def measure_roll(device, steps, warmup, hbm_peak, peak_src):
         C = H * D
         src = [torch.randn(B, M + W, C, device=device).to(bf) for _ in range(2)]
         dst = [torch.empty(B, M + W, C, device=device, dtype=bf) for _ in range(2)]
-        ts = []
-        for it in range(warmup + steps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(cs)
+        nbytes = 2 * 2 * B * M * C * 2
+
+        def kv():
+            txl.txl_mem_update_kv(src[0][:, :M], src[1][:, :M], src[0][:, M:], src[1][:, M:], dst[0], dst[1], M)
+
+        def pair():
             for x in range(2):
                 txl.txl_mem_update(src[x][:, :M], src[x][:, M:], dst[x], M)
-            b.record(cs)
-            if it >= warmup:
-                ts.append((a, b))
-        torch.cuda.synchronize()
-        ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
-        nbytes = 2 * 2 * B * M * C * 2
-        gbs = nbytes / (ms / 1e3) / 1e9
-        out[name] = {"call": "txl_mem_update on k, then on v (2 launches)", "bytes": nbytes, "ms": ms,
-                     "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "steps": len(ts)}
-        assert all(torch.equal(dst[x][:, :M], src[x][:, W:]) for x in range(2)), "roll result"
+
+        res = {}
+        for label, fn, call in (("kv", kv, "txl_mem_update_kv (k and v in one launch)"),
+                                ("pair", pair, "txl_mem_update on k, then on v (2 launches)")):
+            ts = []
+            for it in range(warmup + steps):
+                flush.zero_()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(cs)
+                fn()
+                b.record(cs)
+                if it >= warmup:
+                    ts.append((a, b))
+            torch.cuda.synchronize()
+            ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+            gbs = nbytes / (ms / 1e3) / 1e9
+            res[label] = {"call": call, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "steps": len(ts)}
+            assert all(torch.equal(dst[x][:, :M], src[x][:, W:]) for x in range(2)), "roll result"
+            dst[0].zero_()
+            dst[1].zero_()
+        out[name] = {"bytes": nbytes, **res["kv"], "two_calls": res["pair"]}
         del src, dst
     # the roll inside the attention kernel (base)
     wl = WORKLOADS["base"]

@@ -188,6 +188,18 @@ TXL_API int txl_mem_update(const void* mem, int m_prev, const void* h, int w, vo
                    int* m_out, txl_dtype dtype, cudaStream_t stream);
 
 /*
+ * txl_mem_update_kv -- txl_mem_update of the keys and of the values in one
+ * launch.  The result is exactly that of txl_mem_update(k_mem, m_prev, k_h,
+ * w, k_out, m, ...) and txl_mem_update(v_mem, m_prev, v_h, w, v_out, m, ...)
+ * with the shared batch strides; no output may overlap another output or any
+ * input (TXL_ERR_ALIAS).  The pages roll keys and values by the same rule;
+ * the single launch is a scheduling of the two.  Allocates nothing.
+ */
+TXL_API int txl_mem_update_kv(const void* k_mem, const void* v_mem, int m_prev, const void* k_h, const void* v_h,
+                              int w, void* k_out, void* v_out, int m, int B, int C, long long mem_bs, long long h_bs,
+                              long long out_bs, int* m_out, txl_dtype dtype, cudaStream_t stream);
+
+/*
  * txl_relattn_forward_roll -- txl_relattn_forward and the memory roll of its
  * keys and values in one call.
  *

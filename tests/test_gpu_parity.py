@@ -58,7 +58,7 @@ def test_sinusoid_bf16(_lib):
 @pytest.mark.parametrize("m_prev,w,m,C", [(0, 4, 4, 16), (4, 4, 4, 16), (512, 512, 512, 512),
                                           (1600, 128, 1600, 1024), (128, 128, 1600, 1024),
                                           (7, 3, 5, 33), (3, 7, 5, 9), (5, 2, 0, 8), (0, 0, 4, 8),
-                                          (10, 6, 12, 1)])
+                                          (10, 6, 12, 1), (37, 5, 40, 1000)])
 def test_mem_roll_bit_exact(_lib, dtype, m_prev, w, m, C):
     B = 3
     rng = np.random.default_rng(m_prev * 131 + w * 7 + m + C)
@@ -75,6 +75,45 @@ def test_mem_roll_bit_exact(_lib, dtype, m_prev, w, m, C):
     assert got.shape == want.shape
     assert np.array_equal(got.view(np.uint32), want.astype(np.float32).view(np.uint32))
     assert torch.all(out[:, keep:] == -7.0)  # nothing written past m'
+
+
+@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("m_prev,w,m,C", [(512, 512, 512, 512), (37, 5, 40, 1000), (7, 3, 5, 33), (0, 6, 4, 8)])
+def test_mem_update_kv_bit_exact(_lib, dtype, m_prev, w, m, C):
+    """Keys and values rolled in one call: each equals its own txl_mem_update
+    and the oracle's roll, bit for bit."""
+    B = 3
+    rng = np.random.default_rng(m_prev * 17 + w * 5 + m + C)
+    td = torch_dtype(dtype)
+    t = lambda rows: torch.from_numpy(rng.standard_normal((B, rows, C)).astype(np.float32)).to(dev()).to(td)
+    km, vm, kh, vh = t(m_prev + 2), t(m_prev + 2), t(w + 1), t(w + 1)
+    keep = min(m, m_prev + w)
+    ko = torch.full((B, keep + 3, C), -7.0, device=dev(), dtype=td)
+    vo = torch.full((B, keep + 3, C), -7.0, device=dev(), dtype=td)
+    ks = torch.empty_like(ko)
+    vs = torch.empty_like(vo)
+    got_m = _lib.txl_mem_update_kv(km[:, :m_prev], vm[:, :m_prev], kh[:, :w], vh[:, :w], ko, vo, m)
+    _lib.txl_mem_update(km[:, :m_prev], kh[:, :w], ks, m)
+    _lib.txl_mem_update(vm[:, :m_prev], vh[:, :w], vs, m)
+    assert got_m == keep
+    assert _lib.txl_get_device_status() == 0
+    for o, sep, mem, h in ((ko, ks, km, kh), (vo, vs, vm, vh)):
+        assert torch.equal(o[:, :keep], sep[:, :keep])
+        want = O.mem_update(mem[:, :m_prev].cpu().float().numpy(), h[:, :w].cpu().float().numpy(), m)
+        assert np.array_equal(o[:, :keep].cpu().float().numpy(), want.astype(np.float32))
+        assert torch.all(o[:, keep:] == -7.0)
+
+
+def test_mem_update_kv_rejects_overlap(_lib):
+    B, C = 2, 64
+    buf = torch.zeros(B, 40, C, device=dev(), dtype=torch.bfloat16)
+    h = torch.zeros(B, 8, C, device=dev(), dtype=torch.bfloat16)
+    mem = torch.zeros(B, 8, C, device=dev(), dtype=torch.bfloat16)
+    with pytest.raises(_lib.TxlError, match="ALIAS"):  # the two outputs overlap
+        _lib.txl_mem_update_kv(mem, mem, h, h, buf[:, :10], buf[:, 5:15], 8)
+    other = torch.zeros(B, 40, C, device=dev(), dtype=torch.bfloat16)
+    with pytest.raises(_lib.TxlError, match="ALIAS"):  # k's output is v's input
+        _lib.txl_mem_update_kv(other[:, :8], other[:, 10:18], h, h, other[:, 10:22], buf[:, :12], 12)
 
 
 # ----------------------------------------------------------------------------

@@ -18,7 +18,8 @@ import torch
 __all__ = [
     "TXL_F32", "TXL_BF16", "TxlError", "lib", "library_path",
     "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_relattn_forward_ring",
-    "txl_relattn_forward_ring_append", "txl_relattn_backward", "txl_mem_update", "txl_mem_ring_append",
+    "txl_relattn_forward_ring_append", "txl_relattn_backward", "txl_mem_update", "txl_mem_update_kv",
+    "txl_mem_ring_append",
     "txl_layer_forward", "txl_layer_workspace_bytes", "LAYER_WEIGHT_NAMES",
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_release_cached", "txl_status_string", "txl_version",
@@ -71,6 +72,9 @@ lib.txl_layer_forward.argtypes = [_p, _p, _p, _p, _i, _i, _i, ctypes.POINTER(_La
 lib.txl_layer_forward.restype = _i
 lib.txl_mem_update.argtypes = [_p, _i, _p, _i, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i, _p]
 lib.txl_mem_update.restype = _i
+lib.txl_mem_update_kv.argtypes = [_p, _p, _i, _p, _p, _i, _p, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i,
+                                  _p]
+lib.txl_mem_update_kv.restype = _i
 lib.txl_sinusoid_rel.argtypes = [_p, _i, _i, _i, _p]
 lib.txl_sinusoid_rel.restype = _i
 lib.txl_get_device_status.argtypes = [_p]
@@ -397,6 +401,32 @@ def txl_mem_update(mem, h, mem_out, m, stream=None) -> int:
                             _ptr(mem_out), m, B, C, mem_bs, h_bs, out_bs, ctypes.byref(m_out),
                             _dtype_code(mem.dtype), _stream(stream))
     _check(st, "txl_mem_update")
+    return m_out.value
+
+
+def txl_mem_update_kv(k_mem, v_mem, k_h, v_h, k_out, v_out, m, stream=None) -> int:
+    """txl_mem_update of keys and of values in one launch: [B, rows, C]
+    row-contiguous views; each pair (k_mem, v_mem), (k_h, v_h), (k_out,
+    v_out) shares its shape and batch stride.  Returns m'."""
+    B, m_prev, C = k_mem.shape
+    w = k_h.shape[1]
+    for a, b, name in ((k_mem, v_mem, "mem"), (k_h, v_h, "h"), (k_out, v_out, "out")):
+        if a.shape != b.shape or _rows_view(a, "k_" + name) != _rows_view(b, "v_" + name):
+            raise ValueError(f"k_{name} and v_{name} must share shape and batch stride")
+    if k_h.shape[0] != B or k_h.shape[2] != C or k_out.shape[0] != B or k_out.shape[2] != C:
+        raise ValueError("mem, h, out disagree on B or C")
+    if not (k_mem.dtype == v_mem.dtype == k_h.dtype == v_h.dtype == k_out.dtype == v_out.dtype):
+        raise ValueError("dtype mismatch")
+    keep = min(m, m_prev + w)
+    if k_out.shape[1] < keep:
+        raise ValueError("out has too few rows")
+    m_out = ctypes.c_int(0)
+    st = lib.txl_mem_update_kv(_ptr(k_mem) if m_prev > 0 else None, _ptr(v_mem) if m_prev > 0 else None, m_prev,
+                               _ptr(k_h) if w > 0 else None, _ptr(v_h) if w > 0 else None, w, _ptr(k_out),
+                               _ptr(v_out), m, B, C, _rows_view(k_mem, "k_mem"), _rows_view(k_h, "k_h"),
+                               _rows_view(k_out, "k_out"), ctypes.byref(m_out), _dtype_code(k_mem.dtype),
+                               _stream(stream))
+    _check(st, "txl_mem_update_kv")
     return m_out.value
 
 

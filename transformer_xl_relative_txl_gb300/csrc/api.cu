@@ -189,6 +189,111 @@ void two_pi_split(int n_dist, float* c1, float* c2, float* c3) {
 
 int from_cuda(cudaError_t e) { return e == cudaSuccess ? TXL_OK : TXL_ERR_CUDA; }
 
+// Wait bound and status word for a launch.
+int wait_ctl(txl::WaitCtl* wc) {
+  if (status_ptr(&wc->status) != cudaSuccess) return TXL_ERR_CUDA;
+  wc->limit_ns = g_wait_ns.load();
+  wc->inject_stall = 0;
+  return TXL_OK;
+}
+
+// The memory roll of n (1 or 2) tensors of one geometry in one launch:
+// validation, alias checks (every output against every input and against
+// the other output), then the roll kernel.
+int roll_impl(const txl::RollTensor* t, int n, int m_prev, int w, int m, int B, int C, long long mem_bs,
+              long long h_bs, long long out_bs, int* m_out, txl_dtype dtype, cudaStream_t stream) {
+  if (B < 0 || m_prev < 0 || w < 0 || m < 0 || C <= 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
+  const long long keep = std::min<long long>(m, static_cast<long long>(m_prev) + w);
+  if (m_out != nullptr) *m_out = static_cast<int>(keep);
+  if (B == 0 || keep == 0) return TXL_OK;
+  if (B > 65535) return TXL_ERR_UNSUPPORTED;
+  const long long from_h = std::min<long long>(keep, w);
+  const long long from_mem = keep - from_h;
+  for (int x = 0; x < n; ++x) {
+    if (t[x].out == nullptr) return TXL_ERR_INVALID_ARG;
+    if (from_mem > 0 && t[x].mem == nullptr) return TXL_ERR_INVALID_ARG;
+    if (from_h > 0 && t[x].h == nullptr) return TXL_ERR_INVALID_ARG;
+  }
+  const long long es = static_cast<long long>(dsize(dtype));
+  if (B > 1 && (mem_bs < static_cast<long long>(m_prev) * C || h_bs < static_cast<long long>(w) * C ||
+                out_bs < keep * C))
+    return TXL_ERR_INVALID_ARG;
+  if (mem_bs < 0 || h_bs < 0 || out_bs < 0) return TXL_ERR_INVALID_ARG;
+  const long long row_bytes = static_cast<long long>(C) * es;
+  // Extents actually read / written (all batches).
+  std::vector<Range> outs, ins;
+  for (int x = 0; x < n; ++x) {
+    outs.push_back(range_of(t[x].out, static_cast<size_t>((B - 1) * out_bs * es + keep * row_bytes)));
+    if (from_mem > 0) {
+      const char* src = static_cast<const char*>(t[x].mem) + (m_prev - from_mem) * row_bytes;
+      ins.push_back(range_of(src, static_cast<size_t>((B - 1) * mem_bs * es + from_mem * row_bytes)));
+    }
+    if (from_h > 0) {
+      const char* src = static_cast<const char*>(t[x].h) + (w - from_h) * row_bytes;
+      ins.push_back(range_of(src, static_cast<size_t>((B - 1) * h_bs * es + from_h * row_bytes)));
+    }
+  }
+  for (size_t x = 0; x < outs.size(); ++x) {
+    for (const Range& y : ins)
+      if (overlap(outs[x], y)) return TXL_ERR_ALIAS;
+    for (size_t z = x + 1; z < outs.size(); ++z)
+      if (overlap(outs[x], outs[z])) return TXL_ERR_ALIAS;
+  }
+  txl::WaitCtl wc;
+  if (wait_ctl(&wc) != TXL_OK) return TXL_ERR_CUDA;
+  return from_cuda(txl::launch_mem_roll_multi(t, n, B, keep, from_mem, m_prev - from_mem, w - from_h, row_bytes,
+                                              mem_bs * es, h_bs * es, out_bs * es, &wc, stream));
+}
+
+// txl_mem_ring_append for n (1 or 2) rings of one geometry, each run of
+// rows in one launch for all of them.
+int ring_append_impl(void* const* mem, const void* const* h, int n, int cap, int start, int m, int w, int B, int C,
+                     long long h_bs, int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream) {
+  if (B < 0 || cap <= 0 || m < 0 || m > cap || w < 0 || C <= 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
+  if (m > 0 && (start < 0 || start >= cap)) return TXL_ERR_INVALID_ARG;
+  if (m == 0) start = 0;
+  const long long total = static_cast<long long>(m) + w;
+  const long long drop = total > cap ? total - cap : 0;  // oldest rows pushed out
+  const int new_start = static_cast<int>((start + drop) % cap);
+  const int new_m = static_cast<int>(std::min<long long>(total, cap));
+  if (B == 0 || w == 0) {
+    if (start_out != nullptr) *start_out = new_start;
+    if (m_out != nullptr) *m_out = new_m;
+    return TXL_OK;
+  }
+  if ((B > 1 && h_bs < static_cast<long long>(w) * C) || h_bs < 0) return TXL_ERR_INVALID_ARG;
+  if (B > 65535) return TXL_ERR_UNSUPPORTED;
+  const long long es = static_cast<long long>(dsize(dtype)), row_bytes = static_cast<long long>(C) * es;
+  for (int x = 0; x < n; ++x) {
+    if (mem[x] == nullptr || h[x] == nullptr) return TXL_ERR_INVALID_ARG;
+    const Range rm = range_of(mem[x], static_cast<size_t>(B) * cap * row_bytes);
+    for (int y = 0; y < n; ++y) {
+      if (overlap(rm, range_of(h[y], static_cast<size_t>((B - 1) * h_bs * es + w * row_bytes)))) return TXL_ERR_ALIAS;
+      if (y > x && overlap(rm, range_of(mem[y], static_cast<size_t>(B) * cap * row_bytes))) return TXL_ERR_ALIAS;
+    }
+  }
+  txl::WaitCtl wc;
+  if (wait_ctl(&wc) != TXL_OK) return TXL_ERR_CUDA;
+  // rows x0 .. w-1 of h go to ring rows (start + m + x) % cap: one or two runs
+  const long long x0 = w > cap ? w - cap : 0;
+  long long x = x0;
+  while (x < w) {
+    const long long dst = (start + m + x) % cap;
+    const long long len = std::min<long long>(w - x, cap - dst);
+    txl::RollTensor t[2];
+    for (int y = 0; y < n; ++y)
+      t[y] = txl::RollTensor{nullptr, static_cast<const char*>(h[y]) + x * row_bytes,
+                             static_cast<char*>(mem[y]) + dst * row_bytes};
+    if (txl::launch_mem_roll_multi(t, n, B, len, 0, 0, 0, row_bytes, 0, h_bs * es, cap * row_bytes, &wc, stream) !=
+        cudaSuccess)
+      return TXL_ERR_CUDA;
+    x += len;
+  }
+  if (start_out != nullptr) *start_out = new_start;
+  if (m_out != nullptr) *m_out = new_m;
+  return TXL_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -303,36 +408,15 @@ int txl_sinusoid_rel(void* R, int n_dist, int dim, txl_dtype dtype, cudaStream_t
 int txl_mem_update(const void* mem, int m_prev, const void* h, int w, void* mem_out, int m, int B, int C,
                    long long mem_bs, long long h_bs, long long out_bs, int* m_out, txl_dtype dtype,
                    cudaStream_t stream) {
-  if (B < 0 || m_prev < 0 || w < 0 || m < 0 || C <= 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
-  const long long keep = std::min<long long>(m, static_cast<long long>(m_prev) + w);
-  if (m_out != nullptr) *m_out = static_cast<int>(keep);
-  if (B == 0 || keep == 0) return TXL_OK;
-  if (B > 65535) return TXL_ERR_UNSUPPORTED;
-  const long long from_h = std::min<long long>(keep, w);
-  const long long from_mem = keep - from_h;
-  if (mem_out == nullptr) return TXL_ERR_INVALID_ARG;
-  if (from_mem > 0 && mem == nullptr) return TXL_ERR_INVALID_ARG;
-  if (from_h > 0 && h == nullptr) return TXL_ERR_INVALID_ARG;
-  const long long es = static_cast<long long>(dsize(dtype));
-  if (B > 1 && (mem_bs < static_cast<long long>(m_prev) * C || h_bs < static_cast<long long>(w) * C ||
-                out_bs < keep * C))
-    return TXL_ERR_INVALID_ARG;
-  if (mem_bs < 0 || h_bs < 0 || out_bs < 0) return TXL_ERR_INVALID_ARG;
-  const long long row_bytes = static_cast<long long>(C) * es;
-  // Extents actually read / written (all batches).
-  const Range out_r = range_of(mem_out, static_cast<size_t>((B - 1) * out_bs * es + keep * row_bytes));
-  if (from_mem > 0) {
-    const char* src = static_cast<const char*>(mem) + (m_prev - from_mem) * row_bytes;
-    if (overlap(out_r, range_of(src, static_cast<size_t>((B - 1) * mem_bs * es + from_mem * row_bytes))))
-      return TXL_ERR_ALIAS;
-  }
-  if (from_h > 0) {
-    const char* src = static_cast<const char*>(h) + (w - from_h) * row_bytes;
-    if (overlap(out_r, range_of(src, static_cast<size_t>((B - 1) * h_bs * es + from_h * row_bytes))))
-      return TXL_ERR_ALIAS;
-  }
-  return from_cuda(txl::launch_mem_roll(mem, h, mem_out, B, keep, from_mem, m_prev - from_mem, w - from_h,
-                                        row_bytes, mem_bs * es, h_bs * es, out_bs * es, stream));
+  const txl::RollTensor t{mem, h, mem_out};
+  return roll_impl(&t, 1, m_prev, w, m, B, C, mem_bs, h_bs, out_bs, m_out, dtype, stream);
+}
+
+int txl_mem_update_kv(const void* k_mem, const void* v_mem, int m_prev, const void* k_h, const void* v_h, int w,
+                      void* k_out, void* v_out, int m, int B, int C, long long mem_bs, long long h_bs,
+                      long long out_bs, int* m_out, txl_dtype dtype, cudaStream_t stream) {
+  const txl::RollTensor t[2] = {{k_mem, k_h, k_out}, {v_mem, v_h, v_out}};
+  return roll_impl(t, 2, m_prev, w, m, B, C, mem_bs, h_bs, out_bs, m_out, dtype, stream);
 }
 
 }  // extern "C"
@@ -729,49 +813,16 @@ int txl_relattn_forward_roll(const void* q, const void* k, const void* v, const 
   const size_t es = dsize(dtype);
   const char* kb = static_cast<const char*>(k);
   const char* vb = static_cast<const char*>(v);
-  rc = txl_mem_update(kb, M, kb + static_cast<size_t>(M) * C * es, W, k_mem_out, m, B, static_cast<int>(C), bs,
-                      bs, mem_out_bs, nullptr, dtype, stream);
-  if (rc != TXL_OK) return rc;
-  return txl_mem_update(vb, M, vb + static_cast<size_t>(M) * C * es, W, v_mem_out, m, B, static_cast<int>(C), bs,
-                        bs, mem_out_bs, nullptr, dtype, stream);
+  return txl_mem_update_kv(kb, vb, M, kb + static_cast<size_t>(M) * C * es, vb + static_cast<size_t>(M) * C * es, W,
+                           k_mem_out, v_mem_out, m, B, static_cast<int>(C), bs, bs, mem_out_bs, nullptr, dtype,
+                           stream);
 }
 
 int txl_mem_ring_append(void* mem, int cap, int start, int m, const void* h, int w, int B, int C, long long h_bs,
                         int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream) {
-  if (B < 0 || cap <= 0 || m < 0 || m > cap || w < 0 || C <= 0 || !dtype_ok(dtype)) return TXL_ERR_INVALID_ARG;
-  if (m > 0 && (start < 0 || start >= cap)) return TXL_ERR_INVALID_ARG;
-  if (m == 0) start = 0;
-  const long long total = static_cast<long long>(m) + w;
-  const long long drop = total > cap ? total - cap : 0;  // oldest rows pushed out
-  const int new_start = static_cast<int>((start + drop) % cap);
-  const int new_m = static_cast<int>(std::min<long long>(total, cap));
-  if (B == 0 || w == 0) {
-    if (start_out != nullptr) *start_out = new_start;
-    if (m_out != nullptr) *m_out = new_m;
-    return TXL_OK;
-  }
-  if (mem == nullptr || h == nullptr || (B > 1 && h_bs < static_cast<long long>(w) * C) || h_bs < 0)
-    return TXL_ERR_INVALID_ARG;
-  if (B > 65535) return TXL_ERR_UNSUPPORTED;
-  const long long es = static_cast<long long>(dsize(dtype)), row_bytes = static_cast<long long>(C) * es;
-  if (overlap(range_of(mem, static_cast<size_t>(B) * cap * row_bytes),
-              range_of(h, static_cast<size_t>((B - 1) * h_bs * es + w * row_bytes))))
-    return TXL_ERR_ALIAS;
-  // rows x0 .. w-1 of h go to ring rows (start + m + x) % cap: one or two runs
-  const long long x0 = w > cap ? w - cap : 0;
-  long long x = x0;
-  while (x < w) {
-    const long long dst = (start + m + x) % cap;
-    const long long n = std::min<long long>(w - x, cap - dst);
-    if (txl::launch_mem_roll(nullptr, static_cast<const char*>(h) + x * row_bytes,
-                             static_cast<char*>(mem) + dst * row_bytes, B, n, 0, 0, 0, row_bytes, 0, h_bs * es,
-                             cap * row_bytes, stream) != cudaSuccess)
-      return TXL_ERR_CUDA;
-    x += n;
-  }
-  if (start_out != nullptr) *start_out = new_start;
-  if (m_out != nullptr) *m_out = new_m;
-  return TXL_OK;
+  void* const mems[1] = {mem};
+  const void* const hs[1] = {h};
+  return ring_append_impl(mems, hs, 1, cap, start, m, w, B, C, h_bs, start_out, m_out, dtype, stream);
 }
 
 }  // extern "C"
@@ -880,13 +931,12 @@ int ring_impl(const void* q, const void* k_mem, const void* v_mem, int cap, int 
                              n_r, scale, dtype, o_dtype, stream);
   }
   if (st != TXL_OK || !append) return st;
-  // then the segment's rows into the rings (after the attention, in stream order)
+  // then the segment's rows into the rings (after the attention, in stream order), keys and values in one launch
   const int C = H * D;
-  if ((st = txl_mem_ring_append(const_cast<void*>(k_mem), cap, start, M, k_seg, W, B, C,
-                                static_cast<long long>(W) * C, nullptr, nullptr, dtype, stream)) != TXL_OK)
-    return st;
-  return txl_mem_ring_append(const_cast<void*>(v_mem), cap, start, M, v_seg, W, B, C, static_cast<long long>(W) * C,
-                             nullptr, nullptr, dtype, stream);
+  void* const mems[2] = {const_cast<void*>(k_mem), const_cast<void*>(v_mem)};
+  const void* const segs[2] = {k_seg, v_seg};
+  return ring_append_impl(mems, segs, 2, cap, start, M, W, B, C, static_cast<long long>(W) * C, nullptr, nullptr,
+                          dtype, stream);
 }
 
 

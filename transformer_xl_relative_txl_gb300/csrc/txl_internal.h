@@ -24,11 +24,25 @@ struct WaitCtl {
 cudaError_t launch_sinusoid(void* R, int n_dist, int dim, bool bf16, float rho_hi, float rho_lo, float c1,
                             float c2, float c3, cudaStream_t stream);
 
-// Memory roll over raw bytes.
+// Memory roll over raw bytes: out[b] = rows [mem_row0, mem_row0 + n_from_mem)
+// of mem[b], then rows from h_row0 of h[b], rows_out rows in all.
 cudaError_t launch_mem_roll(const void* mem, const void* h, void* out, int B, long long rows_out,
                             long long n_from_mem, long long mem_row0, long long h_row0, long long row_bytes,
                             long long mem_bs_bytes, long long h_bs_bytes, long long out_bs_bytes,
                             cudaStream_t stream);
+// The same for one or two tensors of one geometry (keys and values) in one
+// launch.  With wc given and every address, stride and row a multiple of 16
+// bytes it runs the bulk-copy kernel (bounded waits reported through wc),
+// else the vector kernel, one launch per tensor.
+struct RollTensor {
+  const void* mem;
+  const void* h;
+  void* out;
+};
+cudaError_t launch_mem_roll_multi(const RollTensor* t, int ntensors, int B, long long rows_out, long long n_from_mem,
+                                  long long mem_row0, long long h_row0, long long row_bytes, long long mem_bs_bytes,
+                                  long long h_bs_bytes, long long out_bs_bytes, const WaitCtl* wc,
+                                  cudaStream_t stream);
 
 // Exact fp32 relative attention (CUDA cores).
 cudaError_t launch_relattn_f32(const float* q, const float* k, const float* v, const float* r,
