@@ -38,6 +38,8 @@ UNIT = "tokens/s"
 WORKLOAD = "base"
 N_SEG_BUFFERS = 8
 EVENT_EVERY = 10  # timed steps per sampled attention-kernel duration
+ROLL_BATCH = 12   # back-to-back roll launches per event pair
+ROLL_SETS = 4     # rotating roll buffer sets
 KERNEL_SOURCES = ["transformer_xl_relative_txl_gb300/csrc/relattn_tc64.cu",
                   "transformer_xl_relative_txl_gb300/csrc/relattn_tc_common.cuh",
                   "transformer_xl_relative_txl_gb300/csrc/txl_device.cuh"]
@@ -468,14 +470,19 @@ def oracle_segment_s(q, k, v, r, bu, bv, M, budget_s=4.0):
 
 
 def measure_roll(device, steps, warmup, hbm_peak, peak_src):
-    """The memory roll alone (txl_mem_update of k and of v: the last M rows of
-    [memory ; segment] into the next segment's buffer) on the four bf16
-    workloads' steady segments, CUDA events around the two launches, L2
-    flushed in between.  Algorithmic bytes: k and v, each read once and
-    written once, 2 * 2 * B * M * H * D * 2.  Beside it, what the roll costs
-    inside the attention kernel on base: the fused call
-    (txl_relattn_forward_roll) minus the attention alone (txl_relattn_forward),
-    interleaved."""
+    """The memory roll alone on the four bf16 workloads' steady segments: the
+    last M rows of [memory ; segment] of k and of v into the next segment's
+    buffer.  Algorithmic bytes: k and v, each read once and written once,
+    2 * 2 * B * M * H * D * 2.  A single launch of ~50 MB lasts a few
+    microseconds, about what an event pair around it adds, so the launches
+    are timed back to back: ROLL_BATCH launches between one event pair,
+    rotating over ROLL_SETS buffer sets (each set ~90-100 MB, so a set's
+    rows have left the 129 MB L2 by the time it comes round again), and the
+    time per launch is the pair's time over ROLL_BATCH.  Timed both as
+    txl_mem_update_kv (k and v in one launch) and as two txl_mem_update
+    calls.  Beside it, what the roll costs inside the attention kernel on
+    base: the fused call (txl_relattn_forward_roll) minus the attention alone
+    (txl_relattn_forward), interleaved, L2 flushed before each."""
     import torch
 
     import transformer_xl_relative_txl_gb300 as txl
@@ -484,20 +491,23 @@ def measure_roll(device, steps, warmup, hbm_peak, peak_src):
     bf = torch.bfloat16
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     cs = torch.cuda.current_stream()
-    out = {"l2": "flushed between steps (256 MB write, outside the events)",
+    out = {"l2": f"{ROLL_BATCH} launches back to back between one event pair, rotating over {ROLL_SETS} buffer "
+                 f"sets (each set's rows evicted from L2 before its next turn); L2 flushed before each batch",
            "peak_source": f"{peak_src} hbm_gbs", "bytes": "2 tensors (k, v) x (read + write) x B*M*H*D*2"}
     for name in ("base", "large", "wide", "long"):
         wl = WORKLOADS[name]
         B, H, D, W, M = wl.B, wl.H, wl.D, wl.W, wl.M
         C = H * D
-        src = [torch.randn(B, M + W, C, device=device).to(bf) for _ in range(2)]
-        dst = [torch.empty(B, M + W, C, device=device, dtype=bf) for _ in range(2)]
+        sets = [([torch.randn(B, M + W, C, device=device).to(bf) for _ in range(2)],
+                 [torch.empty(B, M + W, C, device=device, dtype=bf) for _ in range(2)]) for _ in range(ROLL_SETS)]
         nbytes = 2 * 2 * B * M * C * 2
 
-        def kv():
+        def kv(n):
+            src, dst = sets[n % ROLL_SETS]
             txl.txl_mem_update_kv(src[0][:, :M], src[1][:, :M], src[0][:, M:], src[1][:, M:], dst[0], dst[1], M)
 
-        def pair():
+        def pair(n):
+            src, dst = sets[n % ROLL_SETS]
             for x in range(2):
                 txl.txl_mem_update(src[x][:, :M], src[x][:, M:], dst[x], M)
 
@@ -509,19 +519,21 @@ def measure_roll(device, steps, warmup, hbm_peak, peak_src):
                 flush.zero_()
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(cs)
-                fn()
+                for n in range(ROLL_BATCH):
+                    fn(n)
                 b.record(cs)
                 if it >= warmup:
                     ts.append((a, b))
             torch.cuda.synchronize()
-            ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
+            ms = float(np.mean([a.elapsed_time(b) for a, b in ts])) / ROLL_BATCH
             gbs = nbytes / (ms / 1e3) / 1e9
-            res[label] = {"call": call, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "steps": len(ts)}
-            assert all(torch.equal(dst[x][:, :M], src[x][:, W:]) for x in range(2)), "roll result"
-            dst[0].zero_()
-            dst[1].zero_()
+            res[label] = {"call": call, "ms": ms, "gbs": gbs, "frac_of_hbm": gbs / hbm_peak, "batches": len(ts)}
+            for src, dst in sets:
+                assert all(torch.equal(dst[x][:, :M], src[x][:, W:]) for x in range(2)), "roll result"
+                dst[0].zero_()
+                dst[1].zero_()
         out[name] = {"bytes": nbytes, **res["kv"], "two_calls": res["pair"]}
-        del src, dst
+        del sets
     # the roll inside the attention kernel (base)
     wl = WORKLOADS["base"]
     B, H, D, W, M = wl.B, wl.H, wl.D, wl.W, wl.M
