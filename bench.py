@@ -850,15 +850,65 @@ def measure_layer(device, steps, warmup, peak, peak_src):
     ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
     flops = layer_flops(B, W, M, d, H, D, LAYER_D_FF)
     tf = flops / (ms / 1e3) / 1e12
-    return {"call": "txl_layer_forward (GEMMs on cuBLASLt: q/k/v as one batched GEMM over packed weights, r, o, "
-                    "and the FFN with b_1 + ReLU and b_2 in their epilogues; attention, normalisations and the "
-                    "memory append in this library's kernels)",
+    gemms = measure_layer_gemms(device, steps, warmup, peak, h.view(B * W, d), dw, R, flush)
+    return {"call": "txl_layer_forward (every product on this library's tcgen05 GEMM: q/k/v as one batched "
+                    "launch over packed weights, r, o, and the FFN with b_1 + ReLU and b_2 in its epilogue; the "
+                    "attention with the memory append, and the normalisations)",
+            "gemms": gemms,
             "workload": f"base segment through one layer: B={B} W={W} M={M} d_model={d} H={H} D={D} "
                         f"d_ff={LAYER_D_FF}, memory a ring of M+W projected rows, W_q/W_k/W_v packed",
             "ms": ms, "value": B * W / (ms / 1e3), "unit": "tokens/s", "calls": len(ts),
             "tflops": tf, "frac_of_bf16_peak": tf / peak, "peak_source": f"{peak_src} bf16_tflops (burst)",
             "per_call_work": f"{flops} counted flops (GEMMs + the attention's 6*B*H*D*(W*M + W(W+1)/2))",
             "l2": "flushed between calls (256 MB write, outside the events)"}
+
+
+def measure_layer_gemms(device, steps, warmup, peak, x, dw, R, flush):
+    """The layer's five products alone, txl_dense against torch.matmul
+    (cuBLAS) on the same bf16 operands, each call timed with CUDA events, L2
+    flushed in between.  txl_dense also adds the bias and applies the ReLU
+    where the layer does (W_1, W_2); torch.matmul is the plain product."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+
+    m, d = x.shape
+    HD = dw["W_q"].shape[1]
+    d_ff = dw["W_1"].shape[1]
+    bf = torch.bfloat16
+    qkv = torch.stack([dw["W_q"], dw["W_k"], dw["W_v"]])
+    a = torch.randn(m, HD, device=device).to(bf)
+    f = torch.randn(m, d_ff, device=device).mul_(0.5).to(bf)
+    cases = [("q/k/v (batched, 3 x)", x, qkv, None, False), ("r", R, dw["W_r"], None, False),
+             ("W_o", a, dw["W_o"], None, False), ("W_1 + b_1, ReLU", x, dw["W_1"], dw["b_1"], True),
+             ("W_2 + b_2", f, dw["W_2"], dw["b_2"], False)]
+    cs = torch.cuda.current_stream()
+    out = []
+    for name, A, Bm, bias, relu in cases:
+        batch = Bm.shape[0] if Bm.dim() == 3 else 1
+        n = Bm.shape[-1]
+        y = torch.empty((batch, A.shape[0], n) if batch > 1 else (A.shape[0], n), device=device, dtype=bf)
+        flops = 2 * batch * A.shape[0] * A.shape[1] * n
+        res = {"gemm": name, "m": A.shape[0], "n": n, "k": A.shape[1], "batch": batch, "gflop": flops / 1e9}
+        for label, fn in (("txl_dense", lambda: txl.txl_dense(A, Bm, y, bias=bias, relu=relu)),
+                          ("torch_matmul", lambda: torch.matmul(A, Bm))):
+            ts = []
+            for it in range(warmup + steps):
+                flush.zero_()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(cs)
+                fn()
+                e1.record(cs)
+                if it >= warmup:
+                    ts.append((e0, e1))
+            torch.cuda.synchronize()
+            ms = float(np.mean([e0.elapsed_time(e1) for e0, e1 in ts]))
+            res[label] = {"ms": ms, "tflops": flops / (ms / 1e3) / 1e12, "frac_of_bf16_peak": flops / (ms / 1e3) / 1e12 / peak}
+        out.append(res)
+    if txl.txl_get_device_status() != 0:
+        raise RuntimeError("device status reported a timed-out wait in the layer GEMMs")
+    return {"note": "txl_dense also adds the bias and applies the ReLU of W_1 and the bias of W_2; torch.matmul "
+                    "(cuBLAS) is the plain product; L2 flushed before each call", "cases": out}
 
 
 def cpu_baseline_backward(wl, stream, batch=4, budget_s=10.0):

@@ -24,7 +24,8 @@
  *     regrown (stream synchronised, old buffer freed) when a later call needs
  *     more; and per-shape unit plans of the bf16 attention kernels (below).
  *     Both are kept until txl_release_cached or process exit.
- *     txl_relattn_forward_static and txl_mem_update allocate nothing.
+ *     txl_relattn_forward_static, txl_mem_update and txl_dense allocate
+ *     nothing.
  *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
  *     returns a txl_status code.  Argument errors are detected on the host before
  *     any launch, and then nothing is launched.  A failed launch returns
@@ -307,6 +308,32 @@ TXL_API int txl_mem_ring_append(void* mem, int cap, int start, int m, const void
                         long long h_bs, int* start_out, int* m_out, txl_dtype dtype, cudaStream_t stream);
 
 /*
+ * txl_dense -- the layer's dense products: y_z = x W_z (+ bias) (then ReLU),
+ * z = 0 .. batch-1, on this library's tensor-core GEMM.
+ *
+ * "Implementing Transformer-XL", recurrent-memory chapter: the input
+ * projections (q = h W_q, k = h W_{k,E}, v = h W_v, r = R W_{k,R}), the output
+ * projection and feed_forward's two products, the first with b_1 and the
+ * ReLU, the second with b_2.
+ *
+ *   x       device, [m, k] bf16 row-major (shared by the batch)
+ *   W       device, [k, n] bf16 row-major, matrix z at W + z w_batch_stride
+ *   y       device, [m, n] bf16 row-major, matrix z at y + z y_batch_stride
+ *   bias    device, [n] fp32 or NULL (the same for every z)
+ *   relu    nonzero: ReLU after the bias
+ *   batch   >= 1; the strides (elements) are ignored when batch == 1, else
+ *           w_batch_stride >= k n, y_batch_stride >= m n, both multiples of 8
+ *
+ * bf16 operands, fp32 accumulation; the bias is added to the fp32 sum and the
+ * ReLU applied before the one rounding to bf16.  n and k multiples of 8
+ * (TXL_ERR_UNSUPPORTED otherwise); x, W, y 16-byte aligned; y must not
+ * overlap x, W or bias (TXL_ERR_ALIAS).  m == 0 is an empty call.  Allocates
+ * nothing.
+ */
+TXL_API int txl_dense(const void* x, const void* W, void* y, int m, int n, int k, int batch, long long w_batch_stride,
+                      long long y_batch_stride, const float* bias, int relu, cudaStream_t stream);
+
+/*
  * txl_layer_forward -- one Transformer-XL layer on a segment, the attention
  * memory kept as a ring of projected keys and values.
  *
@@ -335,17 +362,13 @@ TXL_API int txl_mem_ring_append(void* mem, int cap, int start, int m, const void
  *   workspace  device, txl_layer_workspace_bytes(...) bytes, 256-byte aligned
  *   D          64 or 128; d_model and d_ff multiples of 8, d_model <= 1024
  *
- * The GEMMs are plain library GEMMs (cuBLASLt, bf16 in, fp32 accumulation,
- * bf16 out).  b_1 with the ReLU, and b_2, ride in the feed-forward GEMMs'
- * epilogues, rounded to bf16 (the bias type cuBLASLt's bias epilogues take)
- * and added to the fp32 accumulator, where cuBLASLt has them for the shape;
- * else this library's kernels add the fp32 vectors to the rounded
- * products.  When W_k starts right after W_q and W_v right after W_k (one
- * [3, d_model, H*D] allocation), the three projections run as one batched
- * GEMM.  Every other step runs in this library's kernels.  Every
- * intermediate lives in `workspace`; the attention inside may make a unit
- * plan as txl_relattn_forward does, and when the ring cannot be read in
- * place (cap, start or M not multiples of 64) it takes the ring scratch of
+ * Every product runs on txl_dense's GEMM (bf16 in, fp32 accumulation, bf16
+ * out), b_1 with the ReLU and b_2 in its epilogue; when W_k starts right after
+ * W_q and W_v right after W_k (one [3, d_model, H*D] allocation), the three
+ * projections run as one batched launch.  Every intermediate lives in
+ * `workspace`; the attention inside may make a unit plan as
+ * txl_relattn_forward does, and when the ring cannot be read in place (cap,
+ * start or M not multiples of 64) it takes the ring scratch of
  * txl_relattn_forward_ring.
  */
 typedef struct {
@@ -373,6 +396,33 @@ TXL_API int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem
                       int B, int W, int d_model, int H, int D, int d_ff, float scale,
                       void* workspace, size_t workspace_bytes, int* start_out, int* m_out,
                       cudaStream_t stream);
+
+/*
+ * txl_stack_forward -- n_layers layers of txl_layer_forward on a segment, the
+ * output of layer l the input of layer l+1, each layer with its own rings.
+ *
+ * "Transformer-XL, explained", method step 6: each layer caches its own
+ * states, so layer l of this segment reads what layer l-1 saw of the last
+ * one and the reach grows with depth ("Implementing Transformer-XL", the
+ * stacked layers).  Every layer's rings hold the same M rows from ring row
+ * `start` (they advance together); *start_out, *m_out receive their common
+ * new state, as from txl_layer_forward.
+ *
+ *   h, out        device, [B, W, d_model] bf16 (out must not overlap h)
+ *   k_mem, v_mem  host arrays of n_layers device ring pointers, [B, cap, H, D]
+ *                 bf16 each, all distinct (TXL_ERR_ALIAS otherwise)
+ *   w             host array of n_layers weight structs
+ *   workspace     device, txl_stack_workspace_bytes(...) bytes, 256-byte
+ *                 aligned (the layer workspace and two [B, W, d_model]
+ *                 buffers for the layers' outputs)
+ * Other arguments, requirements and allocations as txl_layer_forward.
+ */
+TXL_API size_t txl_stack_workspace_bytes(int B, int W, int d_model, int H, int D, int d_ff, int n_r);
+
+TXL_API int txl_stack_forward(const void* h, void* out, int n_layers, void* const* k_mem, void* const* v_mem,
+                              int cap, int start, int M, const txl_layer_weights* w, const void* R, int n_r, int B,
+                              int W, int d_model, int H, int D, int d_ff, float scale, void* workspace,
+                              size_t workspace_bytes, int* start_out, int* m_out, cudaStream_t stream);
 
 /*
  * txl_relattn_backward -- gradients of txl_relattn_forward.
@@ -482,10 +532,6 @@ TXL_API int txl_debug_inject_stall(int on);
  * key steps into min(nsplit, steps of the shortest unit) chunks instead of
  * the count its cost model picks; 0 restores the model. */
 TXL_API int txl_debug_force_split(int nsplit);
-/* Test hook: on != 0 makes txl_layer_forward add b_1 (with the ReLU) and
- * b_2 in this library's own kernels after plain GEMMs instead of in the
- * GEMMs' epilogues; 0 restores the epilogues. */
-TXL_API int txl_debug_force_bias_kernels(int on);
 
 #ifdef __cplusplus
 }

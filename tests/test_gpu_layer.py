@@ -58,15 +58,15 @@ def _close(got, want, what):
     return rel
 
 
-@pytest.mark.parametrize("B,W,M,H,D,dff,bias_kernels,packed", [
-    (2, 128, 128, 4, 64, 1024, False, False),  # ring of M+W rows: the append runs inside the attention kernel
-    (2, 128, 128, 4, 64, 1024, True, False),   # the same, the FFN biases by the library's kernels
-    (2, 128, 128, 4, 64, 1024, False, True),   # the same, q/k/v projections as one batched GEMM
-    (1, 72, 40, 2, 64, 256, False, True),      # memory, segment and rows (72) off the tile grids
-    (2, 64, 0, 2, 128, 512, False, False),     # first segment, D = 128
-    (3, 64, 64, 16, 64, 128, True, True),      # d_model = 1024, the widest normalisation
+@pytest.mark.parametrize("B,W,M,H,D,dff,packed", [
+    (2, 128, 128, 4, 64, 1024, False),  # ring of M+W rows: the append runs inside the attention kernel
+    (2, 128, 128, 4, 64, 1024, True),   # the same, q/k/v projections as one batched GEMM launch
+    (1, 72, 40, 2, 64, 256, True),      # memory, segment and rows (72) off the tile grids
+    (2, 64, 0, 2, 128, 512, False),     # first segment, D = 128
+    (3, 64, 64, 16, 64, 128, True),     # d_model = 1024, the widest normalisation
+    (1, 100, 64, 2, 64, 136, False),    # d_ff = 136: a GEMM k and n off the 64-column grid
 ])
-def test_layer_matches_oracle(txl, B, W, M, H, D, dff, bias_kernels, packed):
+def test_layer_matches_oracle(txl, B, W, M, H, D, dff, packed):
     d = H * D
     P, dw = _weights(d, H, D, dff, packed=packed)
     rng = np.random.default_rng(B * 1000 + W + M)
@@ -87,11 +87,7 @@ def test_layer_matches_oracle(txl, B, W, M, H, D, dff, bias_kernels, packed):
     Rd = torch.from_numpy(R).to(dev()).to(torch.bfloat16)
     out = torch.empty_like(hd)
     ws = torch.empty(txl.txl_layer_workspace_bytes(B, W, d, H, D, dff, n_r), device=dev(), dtype=torch.uint8)
-    txl.txl_debug_force_bias_kernels(bias_kernels)
-    try:
-        s2, m2 = txl.txl_layer_forward(hd, out, k_ring, v_ring, start, M, dw, Rd, ws)
-    finally:
-        txl.txl_debug_force_bias_kernels(False)
+    s2, m2 = txl.txl_layer_forward(hd, out, k_ring, v_ring, start, M, dw, Rd, ws)
     assert txl.txl_get_device_status() == 0
     assert (s2, m2) == (0, M + W)
     want = O.layer_forward(h, None, P, R.astype(np.float64), H, mem_kv=(k_mem, v_mem))
@@ -162,6 +158,38 @@ def test_stack_matches_oracle(txl):
             _close(y.float().cpu().numpy(), want[t][n], f"segment {t} layer {n}")
             x = y
     assert txl.txl_get_device_status() == 0
+
+
+def test_stack_entry_matches_oracle(txl):
+    """txl_stack_forward: three layers in one call per segment over four
+    segments (B=2, W=64, M=64, d=128), the layers' rings advancing together;
+    the last layer's output against the oracle's stack."""
+    B, W, M, H, D, dff, S, N = 2, 64, 64, 2, 64, 256, 4, 3
+    d = H * D
+    layers = [_weights(d, H, D, dff, layer=n, packed=(n == 1)) for n in range(N)]
+    rng = np.random.default_rng(78)
+    segs = [round_bf16(rng.standard_normal((B, W, d)).astype(np.float32)).astype(np.float64) for _ in range(S)]
+    n_r = M + W
+    R = round_bf16(O.sinusoid_rel(n_r, d).astype(np.float32))
+    Rd = torch.from_numpy(R).to(dev()).to(torch.bfloat16)
+    want = O.stack_forward(segs, [P for P, _ in layers], R.astype(np.float64), H, M)
+    cap = M + W
+    k_rings = [torch.zeros(B, cap, H, D, device=dev(), dtype=torch.bfloat16) for _ in range(N)]
+    v_rings = [torch.zeros(B, cap, H, D, device=dev(), dtype=torch.bfloat16) for _ in range(N)]
+    ws = torch.empty(txl.txl_stack_workspace_bytes(B, W, d, H, D, dff, n_r), device=dev(), dtype=torch.uint8)
+    start, m = 0, 0
+    for t in range(S):
+        x = torch.from_numpy(segs[t].astype(np.float32)).to(dev()).to(torch.bfloat16)
+        y = torch.empty_like(x)
+        s2, m2 = txl.txl_stack_forward(x, y, k_rings, v_rings, start, m, [dw for _, dw in layers], Rd, ws)
+        keep = min(m2, M)
+        start, m = (s2 + m2 - keep) % cap, keep
+        _close(y.float().cpu().numpy(), want[t][N - 1], f"segment {t}, last layer")
+    assert txl.txl_get_device_status() == 0
+    with pytest.raises(txl.TxlError) as e:  # two layers sharing a ring
+        txl.txl_stack_forward(x, y, [k_rings[0], k_rings[0], k_rings[2]], v_rings, start, m,
+                              [dw for _, dw in layers], Rd, ws)
+    assert e.value.status == 3
 
 
 def test_layer_rejects_bad_arguments(txl):

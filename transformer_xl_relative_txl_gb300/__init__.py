@@ -20,11 +20,11 @@ __all__ = [
     "txl_relattn_forward", "txl_relattn_forward_static", "txl_relattn_forward_roll", "txl_relattn_forward_ring",
     "txl_relattn_forward_ring_append", "txl_relattn_backward", "txl_mem_update", "txl_mem_update_kv",
     "txl_mem_ring_append",
-    "txl_layer_forward", "txl_layer_workspace_bytes", "LAYER_WEIGHT_NAMES",
+    "txl_layer_forward", "txl_layer_workspace_bytes", "LAYER_WEIGHT_NAMES", "txl_dense", "txl_stack_forward",
+    "txl_stack_workspace_bytes",
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_release_cached", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall", "txl_debug_force_split",
-    "txl_debug_force_bias_kernels",
 ]
 
 TXL_F32 = 0
@@ -70,6 +70,14 @@ lib.txl_layer_workspace_bytes.restype = ctypes.c_size_t
 lib.txl_layer_forward.argtypes = [_p, _p, _p, _p, _i, _i, _i, ctypes.POINTER(_LayerWeights), _p, _i, _i, _i, _i, _i,
                                   _i, _i, _f, _p, ctypes.c_size_t, ctypes.POINTER(_i), ctypes.POINTER(_i), _p]
 lib.txl_layer_forward.restype = _i
+lib.txl_stack_workspace_bytes.argtypes = [_i, _i, _i, _i, _i, _i, _i]
+lib.txl_stack_workspace_bytes.restype = ctypes.c_size_t
+lib.txl_stack_forward.argtypes = [_p, _p, _i, ctypes.POINTER(_p), ctypes.POINTER(_p), _i, _i, _i,
+                                  ctypes.POINTER(_LayerWeights), _p, _i, _i, _i, _i, _i, _i, _i, _f, _p,
+                                  ctypes.c_size_t, ctypes.POINTER(_i), ctypes.POINTER(_i), _p]
+lib.txl_stack_forward.restype = _i
+lib.txl_dense.argtypes = [_p, _p, _p, _i, _i, _i, _i, _ll, _ll, _p, _i, _p]
+lib.txl_dense.restype = _i
 lib.txl_mem_update.argtypes = [_p, _i, _p, _i, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i, _p]
 lib.txl_mem_update.restype = _i
 lib.txl_mem_update_kv.argtypes = [_p, _p, _i, _p, _p, _i, _p, _p, _i, _i, _i, _ll, _ll, _ll, ctypes.POINTER(_i), _i,
@@ -91,8 +99,6 @@ lib.txl_debug_inject_stall.argtypes = [_i]
 lib.txl_debug_inject_stall.restype = _i
 lib.txl_debug_force_split.argtypes = [_i]
 lib.txl_debug_force_split.restype = _i
-lib.txl_debug_force_bias_kernels.argtypes = [_i]
-lib.txl_debug_force_bias_kernels.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -268,15 +274,9 @@ def txl_layer_forward(h, out, k_mem, v_mem, start, M, weights, R, workspace, sca
         raise ValueError("h and out must be bf16 [B, W, d_model]")
     if v_mem.shape != k_mem.shape or k_mem.shape[0] != B or k_mem.dtype != torch.bfloat16:
         raise ValueError("rings must be bf16 [B, cap, H, D]")
-    for n in ("W_q", "W_k", "W_v", "W_r", "W_o", "W_1", "W_2"):
-        if weights[n].dtype != torch.bfloat16:
-            raise ValueError(f"{n} must be bf16")
-    for n in ("bias_u", "bias_v", "ln1_gamma", "ln1_beta", "b_1", "b_2", "ln2_gamma", "ln2_beta"):
-        if weights[n].dtype != torch.float32:
-            raise ValueError(f"{n} must be fp32")
     if scale is None:
         scale = D ** -0.5
-    wts = _LayerWeights(*[_ptr(weights[n]) for n in LAYER_WEIGHT_NAMES])
+    wts = _layer_struct(weights, d_model, H, D)
     s_out, m_out = ctypes.c_int(0), ctypes.c_int(0)
     st = lib.txl_layer_forward(_ptr(h), _ptr(out), _ptr(k_mem), _ptr(v_mem), cap, int(start), int(M),
                                ctypes.byref(wts), _ptr(R), R.shape[0], B, W, d_model, H, D, d_ff, float(scale),
@@ -284,6 +284,82 @@ def txl_layer_forward(h, out, k_mem, v_mem, start, M, weights, R, workspace, sca
                                ctypes.byref(m_out), _stream(stream))
     _check(st, "txl_layer_forward")
     return s_out.value, m_out.value
+
+
+def _layer_struct(weights, d_model, H, D):
+    for t in (weights[n] for n in LAYER_WEIGHT_NAMES):
+        if not t.is_contiguous():
+            raise ValueError("weights must be contiguous")
+    for n in ("W_q", "W_k", "W_v", "W_r", "W_o", "W_1", "W_2"):
+        if weights[n].dtype != torch.bfloat16:
+            raise ValueError(f"{n} must be bf16")
+    for n in ("bias_u", "bias_v", "ln1_gamma", "ln1_beta", "b_1", "b_2", "ln2_gamma", "ln2_beta"):
+        if weights[n].dtype != torch.float32:
+            raise ValueError(f"{n} must be fp32")
+    return _LayerWeights(*[_ptr(weights[n]) for n in LAYER_WEIGHT_NAMES])
+
+
+def txl_stack_workspace_bytes(B, W, d_model, H, D, d_ff, n_r):
+    return int(lib.txl_stack_workspace_bytes(B, W, d_model, H, D, d_ff, n_r))
+
+
+def txl_stack_forward(h, out, k_mems, v_mems, start, M, weights, R, workspace, scale=None, stream=None):
+    """len(weights) layers of txl_layer_forward on the segment h [B, W,
+    d_model] (bf16), the last layer's output into out; k_mems, v_mems: one
+    ring pair [B, cap, H, D] per layer, all holding M rows from ring row
+    `start`; weights: one dict per layer; workspace: uint8 device tensor of
+    at least txl_stack_workspace_bytes(...) bytes.  Returns the rings' common
+    new (start, m)."""
+    B, W, d_model = h.shape
+    L = len(weights)
+    if L < 1 or len(k_mems) != L or len(v_mems) != L:
+        raise ValueError("one ring pair and one weight dict per layer")
+    _, cap, H, D = k_mems[0].shape
+    d_ff = weights[0]["W_1"].shape[1]
+    for t in (h, out, R, workspace) + tuple(k_mems) + tuple(v_mems):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if out.shape != h.shape or h.dtype != torch.bfloat16 or out.dtype != torch.bfloat16:
+        raise ValueError("h and out must be bf16 [B, W, d_model]")
+    for km, vm in zip(k_mems, v_mems):
+        if km.shape != (B, cap, H, D) or vm.shape != km.shape or km.dtype != torch.bfloat16 or vm.dtype != km.dtype:
+            raise ValueError("rings must be bf16 [B, cap, H, D], the same for every layer")
+    if scale is None:
+        scale = D ** -0.5
+    ws = (_LayerWeights * L)(*[_layer_struct(w, d_model, H, D) for w in weights])
+    kp = (_p * L)(*[_ptr(x) for x in k_mems])
+    vp = (_p * L)(*[_ptr(x) for x in v_mems])
+    s_out, m_out = ctypes.c_int(0), ctypes.c_int(0)
+    st = lib.txl_stack_forward(_ptr(h), _ptr(out), L, kp, vp, cap, int(start), int(M), ws, _ptr(R), R.shape[0], B, W,
+                               d_model, H, D, d_ff, float(scale), _ptr(workspace),
+                               workspace.numel() * workspace.element_size(), ctypes.byref(s_out), ctypes.byref(m_out),
+                               _stream(stream))
+    _check(st, "txl_stack_forward")
+    return s_out.value, m_out.value
+
+
+def txl_dense(x, W, y, bias=None, relu=False, stream=None):
+    """y = x W (+ bias) (then ReLU): x [m, k], W [k, n] or [batch, k, n],
+    y [m, n] or [batch, m, n] (bf16, contiguous); bias fp32 [n] or None."""
+    if x.dim() != 2:
+        raise ValueError("x must be [m, k]")
+    m, k = x.shape
+    Wb = W if W.dim() == 3 else W.unsqueeze(0)
+    yb = y if y.dim() == 3 else y.unsqueeze(0)
+    batch, k2, n = Wb.shape
+    if k2 != k or yb.shape != (batch, m, n):
+        raise ValueError("shape mismatch between x, W, y")
+    for t in (x, W, y) + ((bias,) if bias is not None else ()):
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    if not (x.dtype == W.dtype == y.dtype == torch.bfloat16):
+        raise ValueError("x, W, y must be bf16")
+    if bias is not None and (bias.dtype != torch.float32 or bias.shape != (n,)):
+        raise ValueError("bias must be fp32 [n]")
+    st = lib.txl_dense(_ptr(x), _ptr(W), _ptr(y), m, n, k, batch, k * n, m * n, _ptr(bias), 1 if relu else 0,
+                       _stream(stream))
+    _check(st, "txl_dense")
+    return y
 
 
 def txl_mem_ring_append(mem, start, m, h, stream=None):
@@ -468,9 +544,3 @@ def txl_debug_inject_stall(on: bool) -> int:
 def txl_debug_force_split(nsplit):
     """Test hook: force the D = 64 forward's split count (0: its cost model)."""
     _check(lib.txl_debug_force_split(int(nsplit)), "txl_debug_force_split")
-
-
-def txl_debug_force_bias_kernels(on):
-    """Test hook: the layer's b_1 + ReLU and b_2 by this library's kernels
-    instead of the GEMM epilogues (False restores the epilogues)."""
-    _check(lib.txl_debug_force_bias_kernels(1 if on else 0), "txl_debug_force_bias_kernels")

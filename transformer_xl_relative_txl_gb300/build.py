@@ -57,7 +57,7 @@ def build(verbose: bool = False, extra=()) -> str:
             if err.strip():
                 print(err, file=sys.stderr)
     tmp = LIB + ".tmp"
-    cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-lcublasLt"]
+    cmd = [_nvcc(), *ARCH, "-shared", "-o", tmp, *objs]
     res = subprocess.run(cmd, capture_output=True, text=True)
     if res.returncode != 0:
         raise RuntimeError(f"link failed:\n{res.stdout}\n{res.stderr}")

@@ -26,7 +26,6 @@ __device__ unsigned int g_txl_status;
 std::atomic<unsigned long long> g_wait_ns{2000000000ULL};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_split{0};  // test hook: > 0 forces the D = 64 kernel's split count
-std::atomic<int> g_force_bias_kernels{0};  // test hook: the layer's b_1 + ReLU and b_2 by this library's kernels
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -245,6 +244,48 @@ int roll_impl(const txl::RollTensor* t, int n, int m_prev, int w, int m, int B, 
                                               mem_bs * es, h_bs * es, out_bs * es, &wc, stream));
 }
 
+// The dense product of the layer on this library's tensor-core GEMM:
+// C_z = A B_z (+ bias) (ReLU), bf16 row-major, A [m, k] shared, B_z
+// [k, n] at B + z b_stride, C_z [m, n] at C + z c_stride (elements).
+// Arguments already validated (alignment, strides).
+int dense_impl(const void* A, const void* B, void* C, int m, int n, int k, int batch, long long b_stride,
+               long long c_stride, const float* bias, bool relu, cudaStream_t stream) {
+  PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+  if (encode == nullptr) return TXL_ERR_CUDA;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  auto enc = [&](CUtensorMap* map, const void* base, cuuint32_t rank, const cuuint64_t* dims,
+                 const cuuint64_t* strides, const cuuint32_t* box) {
+    return encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  CUtensorMap ta, tb, tc;
+  {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2};
+    const cuuint32_t box[2] = {64, 128};
+    if (!enc(&ta, A, 2, dims, strides, box)) return TXL_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(k),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(n) * 2, static_cast<cuuint64_t>(b_stride) * 2};
+    const cuuint32_t box[3] = {64, 64, 1};
+    if (!enc(&tb, B, 3, dims, strides, box)) return TXL_ERR_CUDA;
+  }
+  {
+    const cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m),
+                                static_cast<cuuint64_t>(batch)};
+    const cuuint64_t strides[2] = {static_cast<cuuint64_t>(n) * 2, static_cast<cuuint64_t>(c_stride) * 2};
+    const cuuint32_t box[3] = {64, 32, 1};
+    if (!enc(&tc, C, 3, dims, strides, box)) return TXL_ERR_CUDA;
+  }
+  txl::WaitCtl wc;
+  if (wait_ctl(&wc) != TXL_OK) return TXL_ERR_CUDA;
+  return from_cuda(txl::launch_gemm_tc(ta, tb, tc, m, n, k, batch, txl::gemm_tc_tile_n(m, n, batch), bias, relu, wc,
+                                       stream));
+}
+
 // txl_mem_ring_append for n (1 or 2) rings of one geometry, each run of
 // rows in one launch for all of them.
 int ring_append_impl(void* const* mem, const void* const* h, int n, int cap, int start, int m, int w, int B, int C,
@@ -326,11 +367,6 @@ int txl_debug_inject_stall(int on) {
 int txl_debug_force_split(int nsplit) {
   if (nsplit < 0 || nsplit > 64) return TXL_ERR_INVALID_ARG;
   g_force_split.store(nsplit);
-  return TXL_OK;
-}
-
-int txl_debug_force_bias_kernels(int on) {
-  g_force_bias_kernels.store(on ? 1 : 0);
   return TXL_OK;
 }
 
@@ -962,35 +998,43 @@ int txl_relattn_forward_ring_append(void* k_mem, void* v_mem, int cap, int start
 }
 
 namespace {
-constexpr size_t kGemmWs = size_t(32) << 20;  // cuBLASLt workspace inside the layer's workspace
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 }  // namespace
+
+int txl_dense(const void* x, const void* W, void* y, int m, int n, int k, int batch, long long w_batch_stride,
+              long long y_batch_stride, const float* bias, int relu, cudaStream_t stream) {
+  if (m < 0 || n <= 0 || k <= 0 || batch <= 0) return TXL_ERR_INVALID_ARG;
+  if (m == 0) return TXL_OK;
+  if (x == nullptr || W == nullptr || y == nullptr) return TXL_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(W, 16) || !aligned(y, 16) || (bias != nullptr && !aligned(bias, 4)))
+    return TXL_ERR_INVALID_ARG;
+  if (n % 8 != 0 || k % 8 != 0) return TXL_ERR_UNSUPPORTED;
+  const long long wsz = static_cast<long long>(k) * n, ysz = static_cast<long long>(m) * n;
+  if (batch > 1 && (w_batch_stride < wsz || y_batch_stride < ysz || w_batch_stride % 8 != 0 ||
+                    y_batch_stride % 8 != 0))
+    return TXL_ERR_INVALID_ARG;
+  if (batch == 1) w_batch_stride = wsz, y_batch_stride = ysz;
+  const Range ry = range_of(y, static_cast<size_t>(((batch - 1) * y_batch_stride + ysz) * 2));
+  if (overlap(ry, range_of(x, static_cast<size_t>(m) * k * 2)) ||
+      overlap(ry, range_of(W, static_cast<size_t>(((batch - 1) * w_batch_stride + wsz) * 2))) ||
+      (bias != nullptr && overlap(ry, range_of(bias, static_cast<size_t>(n) * 4))))
+    return TXL_ERR_ALIAS;
+  return dense_impl(x, W, y, m, n, k, batch, w_batch_stride, y_batch_stride, bias, relu != 0, stream);
+}
 
 size_t txl_layer_workspace_bytes(int B, int W, int d_model, int H, int D, int d_ff, int n_r) {
   if (B <= 0 || W <= 0 || d_model <= 0 || H <= 0 || D <= 0 || d_ff <= 0 || n_r <= 0) return 0;
   const size_t bw = static_cast<size_t>(B) * W, hd = static_cast<size_t>(H) * D;
-  return kGemmWs + 4 * align256(bw * hd * 2) + align256(static_cast<size_t>(n_r) * hd * 2) +
-         3 * align256(bw * d_model * 2) + align256(bw * d_ff * 2) + align256(static_cast<size_t>(d_ff) * 2) +
-         align256(static_cast<size_t>(d_model) * 2);
+  return 4 * align256(bw * hd * 2) + align256(static_cast<size_t>(n_r) * hd * 2) + 3 * align256(bw * d_model * 2) +
+         align256(bw * d_ff * 2);
 }
 
-int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int cap, int start, int M,
-                      const txl_layer_weights* w, const void* R, int n_r, int B, int W, int d_model, int H, int D,
-                      int d_ff, float scale, void* workspace, size_t workspace_bytes, int* start_out, int* m_out,
-                      cudaStream_t stream) {
-  if (w == nullptr || h == nullptr || out == nullptr || R == nullptr || workspace == nullptr || B <= 0 || W <= 0 ||
-      d_model <= 0 || H <= 0 || D <= 0 || d_ff <= 0 || M < 0 || cap < M || cap <= 0)
-    return TXL_ERR_INVALID_ARG;
-  const void* ptrs[] = {w->W_q, w->W_k, w->W_v, w->W_r, w->bias_u, w->bias_v, w->W_o, w->ln1_gamma, w->ln1_beta,
-                        w->W_1, w->b_1, w->W_2, w->b_2, w->ln2_gamma, w->ln2_beta, k_mem, v_mem};
-  for (const void* p : ptrs)
-    if (p == nullptr || !aligned(p, 16)) return TXL_ERR_INVALID_ARG;
-  if (!aligned(h, 16) || !aligned(out, 16) || !aligned(R, 16) || !aligned(workspace, 256))
-    return TXL_ERR_INVALID_ARG;
-  if (d_model % 8 != 0 || d_model > 1024 || d_ff % 8 != 0) return TXL_ERR_UNSUPPORTED;
-  if (workspace_bytes < txl_layer_workspace_bytes(B, W, d_model, H, D, d_ff, n_r)) return TXL_ERR_INVALID_ARG;
+namespace {
+// One layer (validated arguments; d_model, d_ff, H*D multiples of 8).
+int layer_impl(const void* h, void* out, void* k_mem, void* v_mem, int cap, int start, int M,
+               const txl_layer_weights* w, const void* R, int n_r, int B, int W, int d_model, int H, int D, int d_ff,
+               float scale, void* workspace, int* start_out, int* m_out, cudaStream_t stream) {
   const size_t bw = static_cast<size_t>(B) * W, hd = static_cast<size_t>(H) * D;
-  if (overlap(range_of(out, bw * d_model * 2), range_of(h, bw * d_model * 2))) return TXL_ERR_ALIAS;
   // workspace carve-up
   char* p = static_cast<char*>(workspace);
   auto take = [&](size_t bytes) {
@@ -998,7 +1042,6 @@ int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int ca
     p += align256(bytes);
     return r;
   };
-  void* gws = take(kGemmWs);
   void* q = take(bw * hd * 2);
   void* ks = take(bw * hd * 2);
   void* vs = take(bw * hd * 2);
@@ -1008,8 +1051,6 @@ int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int ca
   void* x = take(bw * d_model * 2);
   void* z = take(bw * d_model * 2);
   void* f = take(bw * d_ff * 2);
-  void* b1h = take(static_cast<size_t>(d_ff) * 2);     // b_1 in bf16, for the FFN GEMMs' epilogues
-  void* b2h = take(static_cast<size_t>(d_model) * 2);  // b_2 in bf16
   const int rows = static_cast<int>(bw);
   const int HD = static_cast<int>(hd);
   // W_q, W_k, W_v packed back to back: the three projections as one batched GEMM
@@ -1017,41 +1058,101 @@ int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int ca
   const bool packed = static_cast<const char*>(w->W_k) == static_cast<const char*>(w->W_q) + wbytes &&
                       static_cast<const char*>(w->W_v) == static_cast<const char*>(w->W_k) + wbytes;
   const long long qkv_stride = static_cast<long long>((static_cast<char*>(ks) - static_cast<char*>(q)) / 2);
+  const long long wsz = static_cast<long long>(d_model) * HD;
+  int st = TXL_OK;
   if (packed) {
-    if (txl::gemm_bf16_batched(h, w->W_q, q, rows, HD, d_model, 3, qkv_stride, gws, kGemmWs, stream))
-      return TXL_ERR_CUDA;
-  } else if (txl::gemm_bf16(h, w->W_q, q, rows, HD, d_model, gws, kGemmWs, stream) ||
-             txl::gemm_bf16(h, w->W_k, ks, rows, HD, d_model, gws, kGemmWs, stream) ||
-             txl::gemm_bf16(h, w->W_v, vs, rows, HD, d_model, gws, kGemmWs, stream)) {
-    return TXL_ERR_CUDA;
+    st = dense_impl(h, w->W_q, q, rows, HD, d_model, 3, wsz, qkv_stride, nullptr, false, stream);
+  } else {
+    const void* wm[3] = {w->W_q, w->W_k, w->W_v};
+    void* om[3] = {q, ks, vs};
+    for (int i = 0; i < 3 && st == TXL_OK; ++i)
+      st = dense_impl(h, wm[i], om[i], rows, HD, d_model, 1, wsz, 0, nullptr, false, stream);
   }
-  if (txl::gemm_bf16(R, w->W_r, r, n_r, HD, d_model, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
-  int st = txl_relattn_forward_ring_append(k_mem, v_mem, cap, start, M, q, ks, vs, r, w->bias_u, w->bias_v, a,
-                                           nullptr, B, W, H, D, n_r, scale, TXL_BF16, TXL_BF16, start_out, m_out,
-                                           stream);
   if (st != TXL_OK) return st;
-  if (txl::gemm_bf16(a, w->W_o, y, rows, d_model, HD, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
-  // b_1 + ReLU and b_2 go in the FFN GEMMs' epilogues (bf16 biases, rounded by the first
-  // normalisation's side jobs) where cuBLASLt has them, else in this library's kernels (fp32).
-  const bool epi = g_force_bias_kernels.load() == 0;
-  txl::CvtJobs cvt;
-  if (epi) {
-    cvt.src[0] = w->b_1, cvt.dst[0] = static_cast<__nv_bfloat16*>(b1h), cvt.n[0] = d_ff;
-    cvt.src[1] = w->b_2, cvt.dst[1] = static_cast<__nv_bfloat16*>(b2h), cvt.n[1] = d_model;
+  if ((st = dense_impl(R, w->W_r, r, n_r, HD, d_model, 1, wsz, 0, nullptr, false, stream)) != TXL_OK) return st;
+  if ((st = txl_relattn_forward_ring_append(k_mem, v_mem, cap, start, M, q, ks, vs, r, w->bias_u, w->bias_v, a,
+                                            nullptr, B, W, H, D, n_r, scale, TXL_BF16, TXL_BF16, start_out, m_out,
+                                            stream)) != TXL_OK)
+    return st;
+  if ((st = dense_impl(a, w->W_o, y, rows, d_model, HD, 1, wsz, 0, nullptr, false, stream)) != TXL_OK) return st;
+  if (txl::launch_add_ln(h, y, nullptr, w->ln1_gamma, w->ln1_beta, x, rows, d_model, stream) != cudaSuccess)
+    return TXL_ERR_CUDA;
+  // b_1 + ReLU and b_2 in the GEMMs' epilogues, on the fp32 accumulators
+  const long long w1sz = static_cast<long long>(d_model) * d_ff;
+  if ((st = dense_impl(x, w->W_1, f, rows, d_ff, d_model, 1, w1sz, 0, w->b_1, true, stream)) != TXL_OK) return st;
+  if ((st = dense_impl(f, w->W_2, z, rows, d_model, d_ff, 1, w1sz, 0, w->b_2, false, stream)) != TXL_OK) return st;
+  if (txl::launch_add_ln(x, z, nullptr, w->ln2_gamma, w->ln2_beta, out, rows, d_model, stream) != cudaSuccess)
+    return TXL_ERR_CUDA;
+  return TXL_OK;
+}
+
+int check_layer(const void* h, void* out, const void* k_mem, const void* v_mem, int cap, int M,
+                const txl_layer_weights* w, const void* R, int B, int W, int d_model, int H, int D, int d_ff) {
+  if (w == nullptr || h == nullptr || out == nullptr || R == nullptr || B <= 0 || W <= 0 || d_model <= 0 || H <= 0 ||
+      D <= 0 || d_ff <= 0 || M < 0 || cap < M || cap <= 0)
+    return TXL_ERR_INVALID_ARG;
+  const void* ptrs[] = {w->W_q, w->W_k, w->W_v, w->W_r, w->bias_u, w->bias_v, w->W_o, w->ln1_gamma, w->ln1_beta,
+                        w->W_1, w->b_1, w->W_2, w->b_2, w->ln2_gamma, w->ln2_beta, k_mem, v_mem};
+  for (const void* p : ptrs)
+    if (p == nullptr || !aligned(p, 16)) return TXL_ERR_INVALID_ARG;
+  if (!aligned(h, 16) || !aligned(out, 16) || !aligned(R, 16)) return TXL_ERR_INVALID_ARG;
+  if (d_model % 8 != 0 || d_model > 1024 || d_ff % 8 != 0) return TXL_ERR_UNSUPPORTED;
+  const size_t bw = static_cast<size_t>(B) * W;
+  if (overlap(range_of(out, bw * d_model * 2), range_of(h, bw * d_model * 2))) return TXL_ERR_ALIAS;
+  return TXL_OK;
+}
+}  // namespace
+
+int txl_layer_forward(const void* h, void* out, void* k_mem, void* v_mem, int cap, int start, int M,
+                      const txl_layer_weights* w, const void* R, int n_r, int B, int W, int d_model, int H, int D,
+                      int d_ff, float scale, void* workspace, size_t workspace_bytes, int* start_out, int* m_out,
+                      cudaStream_t stream) {
+  int st = check_layer(h, out, k_mem, v_mem, cap, M, w, R, B, W, d_model, H, D, d_ff);
+  if (st != TXL_OK) return st;
+  if (workspace == nullptr || !aligned(workspace, 256)) return TXL_ERR_INVALID_ARG;
+  if (workspace_bytes < txl_layer_workspace_bytes(B, W, d_model, H, D, d_ff, n_r)) return TXL_ERR_INVALID_ARG;
+  return layer_impl(h, out, k_mem, v_mem, cap, start, M, w, R, n_r, B, W, d_model, H, D, d_ff, scale, workspace,
+                    start_out, m_out, stream);
+}
+
+size_t txl_stack_workspace_bytes(int B, int W, int d_model, int H, int D, int d_ff, int n_r) {
+  const size_t lw = txl_layer_workspace_bytes(B, W, d_model, H, D, d_ff, n_r);
+  if (lw == 0) return 0;
+  return lw + 2 * align256(static_cast<size_t>(B) * W * d_model * 2);
+}
+
+int txl_stack_forward(const void* h, void* out, int n_layers, void* const* k_mem, void* const* v_mem, int cap,
+                      int start, int M, const txl_layer_weights* w, const void* R, int n_r, int B, int W, int d_model,
+                      int H, int D, int d_ff, float scale, void* workspace, size_t workspace_bytes, int* start_out,
+                      int* m_out, cudaStream_t stream) {
+  if (n_layers <= 0 || k_mem == nullptr || v_mem == nullptr || w == nullptr) return TXL_ERR_INVALID_ARG;
+  for (int l = 0; l < n_layers; ++l) {
+    const int st = check_layer(h, out, k_mem[l], v_mem[l], cap, M, &w[l], R, B, W, d_model, H, D, d_ff);
+    if (st != TXL_OK) return st;
   }
-  if (txl::launch_add_ln(h, y, nullptr, w->ln1_gamma, w->ln1_beta, x, rows, d_model, stream, cvt) != cudaSuccess)
-    return TXL_ERR_CUDA;
-  int e = epi ? txl::gemm_bf16(x, w->W_1, f, rows, d_ff, d_model, gws, kGemmWs, stream, b1h, true) : 2;
-  if (e == 1) return TXL_ERR_CUDA;
-  if (e == 2 && (txl::gemm_bf16(x, w->W_1, f, rows, d_ff, d_model, gws, kGemmWs, stream) ||
-                 txl::launch_bias_relu(f, w->b_1, rows, d_ff, stream) != cudaSuccess))
-    return TXL_ERR_CUDA;
-  e = epi ? txl::gemm_bf16(f, w->W_2, z, rows, d_model, d_ff, gws, kGemmWs, stream, b2h, false) : 2;
-  if (e == 1) return TXL_ERR_CUDA;
-  if (e == 2 && txl::gemm_bf16(f, w->W_2, z, rows, d_model, d_ff, gws, kGemmWs, stream)) return TXL_ERR_CUDA;
-  if (txl::launch_add_ln(x, z, e == 2 ? w->b_2 : nullptr, w->ln2_gamma, w->ln2_beta, out, rows, d_model, stream) !=
-      cudaSuccess)
-    return TXL_ERR_CUDA;
+  if (workspace == nullptr || !aligned(workspace, 256)) return TXL_ERR_INVALID_ARG;
+  if (workspace_bytes < txl_stack_workspace_bytes(B, W, d_model, H, D, d_ff, n_r)) return TXL_ERR_INVALID_ARG;
+  // every layer's rings are distinct from every other layer's
+  const size_t ring_bytes = static_cast<size_t>(B) * cap * H * D * 2;
+  for (int l = 0; l < n_layers; ++l)
+    for (int j = l + 1; j < n_layers; ++j)
+      if (overlap(range_of(k_mem[l], ring_bytes), range_of(k_mem[j], ring_bytes)) ||
+          overlap(range_of(k_mem[l], ring_bytes), range_of(v_mem[j], ring_bytes)) ||
+          overlap(range_of(v_mem[l], ring_bytes), range_of(k_mem[j], ring_bytes)) ||
+          overlap(range_of(v_mem[l], ring_bytes), range_of(v_mem[j], ring_bytes)))
+        return TXL_ERR_ALIAS;
+  // layer outputs ping-pong between two buffers after the layer workspace; the last goes to out
+  const size_t lw = txl_layer_workspace_bytes(B, W, d_model, H, D, d_ff, n_r);
+  char* buf[2] = {static_cast<char*>(workspace) + lw,
+                  static_cast<char*>(workspace) + lw + align256(static_cast<size_t>(B) * W * d_model * 2)};
+  const void* x = h;
+  for (int l = 0; l < n_layers; ++l) {
+    void* y = l == n_layers - 1 ? out : buf[l & 1];
+    const int st = layer_impl(x, y, k_mem[l], v_mem[l], cap, start, M, &w[l], R, n_r, B, W, d_model, H, D, d_ff,
+                              scale, workspace, start_out, m_out, stream);
+    if (st != TXL_OK) return st;
+    x = y;
+  }
   return TXL_OK;
 }
 

@@ -1,0 +1,360 @@
+// The layer's dense products on the sm_103a tensor cores:
+//
+//   C_z [m, n] = A [m, k] . B_z [k, n]  (+ bias [n])  (then ReLU),  z < batch
+//
+// bf16 A, B and C, row-major; fp32 accumulation in tensor memory; the bias
+// (fp32) is added to the fp32 accumulator and the ReLU applied before the one
+// rounding to bf16.  "Implementing Transformer-XL", recurrent-memory chapter:
+// the input projections, the output projection and the two feed-forward
+// products (with b_1 and the ReLU after the first, b_2 after the second).
+//
+// Design (one persistent CTA per SM, 192 threads):
+//   warp 0     TMA producer: per 64-deep k block, one 128 x 64 tile of A
+//              (K-major, 128-byte swizzle) and BN/64 tiles of 64 k-rows x 64
+//              columns of B (N-major: B is stored [k, n] with n contiguous)
+//              into a ring of shared-memory stages;
+//   warp 1     MMA issuer: tcgen05.mma kind::f16, M = 128, N = BN, K = 16,
+//              four per k block, into one of two TMEM accumulators, so the
+//              next tile's products overlap this tile's epilogue;
+//   warps 2-5  epilogue: each reads its 32-lane quadrant of the accumulator
+//              (tcgen05.ld, 64 columns at a time), adds the bias, applies the
+//              ReLU, rounds to bf16, stages 32 rows x 64 columns in its own
+//              128-byte-swizzled buffer and writes them with one TMA store.
+// Tiles (z, m block, n block) are dealt round-robin, n block fastest, so the
+// CTAs working at one time share A's rows through L2.  Out-of-range rows,
+// columns and k (the tails) are zero-filled by the loads and clipped by the
+// stores.  Every wait is bounded: a wait that runs out raises the device
+// status word, every role unwinds and the tensor memory is freed.
+#include <atomic>
+#include <cstdint>
+
+#include "relattn_tc_common.cuh"
+#include "txl_device.cuh"
+#include "txl_internal.h"
+
+namespace txl {
+namespace {
+
+constexpr int GBM = 128;              // rows per tile (TMEM lanes)
+constexpr int GBK = 64;               // k per stage (one 128-byte swizzle row of bf16)
+constexpr int kATile = GBM * 128;     // 16 KB
+constexpr int kBBlock = GBK * 128;    // 64 k-rows x 64 columns of B: 8 KB
+constexpr int kGemmThreads = 192;
+constexpr int kEpiBytes = 32 * 128;   // one epilogue warp's staging: 32 rows x 64 bf16
+
+template <int BN>
+struct GemmCfg {
+  static constexpr int kStageBytes = kATile + (BN / 64) * kBBlock;
+  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kOffEpi = kStages * kStageBytes;             // 4 x 4 KB staging
+  static constexpr int kOffBias = kOffEpi + 4 * kEpiBytes;          // 4 x BN floats
+  static constexpr int kOffBar = kOffBias + 4 * BN * 4;
+  static constexpr int kSmem = kOffBar + 256 + 1024;                // barriers, alignment slack
+  static constexpr uint32_t kTmemCols = 2 * BN;                    // two accumulators
+  static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+struct GemmParams {
+  int m, n, k, batch;
+  int mt, nt;           // row and column blocks
+  int tiles;            // batch * mt * nt
+  const float* bias;    // [n] or nullptr
+  int relu;
+  unsigned int* status;
+  unsigned long long wait_ns;
+};
+
+struct GemmBars {
+  uint64_t full[8], empty[8];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1)
+      : "memory");
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+struct TileIdx {
+  int z, m0, n0;
+};
+// Tile t: batch index slowest, then the row block, the column block fastest.
+__device__ __forceinline__ TileIdx tile_of(const GemmParams& p, int t, int bn) {
+  TileIdx r;
+  const int per_z = p.mt * p.nt;
+  r.z = t / per_z;
+  const int rem = t - r.z * per_z;
+  r.m0 = (rem / p.nt) * GBM;
+  r.n0 = (rem % p.nt) * bn;
+  return r;
+}
+
+template <int BN>
+__global__ void __launch_bounds__(kGemmThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
+                   const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
+  using Cfg = GemmCfg<BN>;
+  constexpr int S = Cfg::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  GemmBars* bars = reinterpret_cast<GemmBars*>(smem + Cfg::kOffBar);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const int nk = (p.k + GBK - 1) / GBK;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->acc_full[a], 1);
+      mbar_init(&bars->acc_empty[a], 4);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, Cfg::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint64_t wait_ns = p.wait_ns;
+
+  if (warp == 0) {
+    // ============================ TMA producer ============================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a);
+      tma_prefetch_desc(&tm_b);
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+        const TileIdx ti = tile_of(p, t, BN);
+        const int n0 = ti.n0;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % S);
+          if (!(ok = mbar_wait(&bars->empty[s], ((it / S) & 1) ^ 1, wait_ns, abort))) break;
+          uint8_t* st = smem + s * Cfg::kStageBytes;
+          mbar_arrive_expect_tx(&bars->full[s], Cfg::kStageBytes);
+          tma_load_2d(st, &tm_a, &bars->full[s], kb * GBK, ti.m0);
+#pragma unroll
+          for (int j = 0; j < BN / 64; ++j)
+            tma_load_3d(st + kATile + j * kBBlock, &tm_b, &bars->full[s], n0 + 64 * j, kb * GBK, ti.z);
+        }
+      }
+      if (!ok) report_timeout(abort, p.status);
+      // let the loads in flight land before the CTA can exit
+      for (int s = 0; s < S && static_cast<uint32_t>(s) < it; ++s) {
+        const uint32_t last = s + ((it - 1 - s) / S) * S;
+        mbar_wait_own(&bars->full[s], (last / S) & 1, wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ==============================
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(GBM, BN, false, true);
+      const uint32_t base = smem_u32(smem);
+      uint32_t it = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++tl) {
+        const uint32_t acc = tl & 1;
+        // the epilogue has drained this accumulator (its use two tiles back)
+        if (tl >= 2 && !(ok = mbar_wait(&bars->acc_empty[acc], ((tl >> 1) - 1) & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < nk; ++kb, ++it) {
+          const int s = static_cast<int>(it % S);
+          if (!(ok = mbar_wait(&bars->full[s], (it / S) & 1, wait_ns, abort))) break;
+          tc_fence_after();
+          const uint32_t st = base + s * Cfg::kStageBytes;
+          // A: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
+          // B: N-major, 64-column blocks kBBlock apart, 8-k-row groups 1024 apart.
+          const uint64_t da = sdesc_sw128(st, 16, 1024);
+          const uint64_t db = sdesc_sw128(st + kATile, kBBlock, 1024);
+#pragma unroll
+          for (int kk = 0; kk < GBK / 16; ++kk)
+            mma_ss(d, da + kk * 2, db + ((kk * 16 * 128) >> 4), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(&bars->empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&bars->acc_full[acc]);
+      }
+      if (!ok) report_timeout(abort, p.status);
+      tc_commit(&bars->done);
+      mbar_wait_own(&bars->done, 0, wait_ns);
+    }
+  } else {
+    // ============================ epilogue ===============================
+    const int quad = warp & 3;  // TMEM lane quadrant of this warp
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    uint8_t* stg = smem + Cfg::kOffEpi + quad * kEpiBytes;
+    float* sbias = reinterpret_cast<float*>(smem + Cfg::kOffBias) + quad * BN;
+    const int r = lane;  // row within the warp's 32
+    uint32_t tl = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tl) {
+      const TileIdx ti = tile_of(p, t, BN);
+      const int n0 = ti.n0;
+      const uint32_t acc = tl & 1;
+      // this tile's bias columns, staged once for broadcast reads
+      if (p.bias != nullptr) {
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < BN / 32; ++i) {
+          const int c = n0 + 32 * i + lane;
+          sbias[32 * i + lane] = c < p.n ? __ldg(p.bias + c) : 0.f;
+        }
+        __syncwarp();
+      }
+      if (!(ok = warp_wait(&bars->acc_full[acc], (tl >> 1) & 1, wait_ns, abort))) break;
+      tc_fence_after();
+#pragma unroll 1
+      for (int c = 0; c < BN / 64; ++c) {
+        uint32_t v0[32], v1[32];
+        tmem_ld32(tmem + lane_base + acc * BN + c * 64, v0);
+        tmem_ld32(tmem + lane_base + acc * BN + c * 64 + 32, v1);
+        tmem_wait_ld(v0);
+        tmem_wait_ld(v1);
+        if (c == BN / 64 - 1) {
+          // every column of this accumulator is in registers: hand it back
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+        }
+        float x[64];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          x[j] = __uint_as_float(v0[j]);
+          x[32 + j] = __uint_as_float(v1[j]);
+        }
+        if (p.bias != nullptr) {
+#pragma unroll
+          for (int j = 0; j < 64; j += 4) {
+            const float4 b = *reinterpret_cast<const float4*>(sbias + c * 64 + j);
+            x[j] += b.x;
+            x[j + 1] += b.y;
+            x[j + 2] += b.z;
+            x[j + 3] += b.w;
+          }
+        }
+        if (p.relu) {
+#pragma unroll
+          for (int j = 0; j < 64; ++j) x[j] = fmaxf(x[j], 0.f);
+        }
+        // the previous store out of the staging buffer has read it
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          *reinterpret_cast<uint4*>(stg + r * 128 + ((j ^ (r & 7)) * 16)) =
+              make_uint4(pack_bf16x2(x[8 * j], x[8 * j + 1]), pack_bf16x2(x[8 * j + 2], x[8 * j + 3]),
+                         pack_bf16x2(x[8 * j + 4], x[8 * j + 5]), pack_bf16x2(x[8 * j + 6], x[8 * j + 7]));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          tma_store_3d(&tm_c, stg, n0 + 64 * c, ti.m0 + 32 * quad, ti.z);
+          bulk_commit_group();
+        }
+      }
+    }
+    if (!ok) report_timeout(abort, p.status);
+    if (lane == 0) bulk_wait_group0();  // every store is complete before the CTA exits
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, Cfg::kTmemCols);
+  }
+}
+
+int gemm_num_sms() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  if (cached[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev] = n;
+  }
+  return cached[dev];
+}
+
+template <int BN>
+cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p,
+                      cudaStream_t stream) {
+  using Cfg = GemmCfg<BN>;
+  static std::atomic<bool> attr_done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev].load()) {
+    e = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg::kSmem);
+    if (e != cudaSuccess) return e;
+    attr_done[dev].store(true);
+  }
+  const int sms = gemm_num_sms();
+  const int grid = p.tiles < sms ? p.tiles : sms;
+  gemm_tc_kernel<BN><<<grid, kGemmThreads, Cfg::kSmem, stream>>>(ta, tb, tc, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_tc_tile_n(int m, int n, int batch) {
+  // Fewer waves of tiles against smaller tiles: the time of a wave is about
+  // proportional to its tiles' columns, plus a fixed part per tile.
+  const long long sms = gemm_num_sms();
+  const long long mt = (m + GBM - 1) / GBM;
+  auto cost = [&](int bn) {
+    const long long tiles = batch * mt * ((n + bn - 1) / bn);
+    const long long waves = (tiles + sms - 1) / sms;
+    return static_cast<double>(waves) * (bn + 32);
+  };
+  return cost(128) < cost(256) ? 128 : 256;
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
+                           int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
+                           cudaStream_t stream) {
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || (bn != 128 && bn != 256)) return cudaErrorInvalidValue;
+  GemmParams p;
+  p.m = m;
+  p.n = n;
+  p.k = k;
+  p.batch = batch;
+  p.mt = (m + GBM - 1) / GBM;
+  p.nt = (n + bn - 1) / bn;
+  const long long tiles = static_cast<long long>(batch) * p.mt * p.nt;
+  if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  p.tiles = static_cast<int>(tiles);
+  p.bias = bias;
+  p.relu = relu ? 1 : 0;
+  p.status = wc.status;
+  p.wait_ns = wc.limit_ns;
+  return bn == 256 ? launch_bn<256>(tm_a, tm_b, tm_c, p, stream) : launch_bn<128>(tm_a, tm_b, tm_c, p, stream);
+}
+
+}  // namespace txl

@@ -137,29 +137,21 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
                                     int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
                                     cudaStream_t stream);
 
-// The layer around the attention (layer.cu).  Row-major bf16 GEMM
-// C [m, n] = A [m, k] B [k, n] with fp32 accumulation (cuBLASLt); with bias
-// (bf16 [n]) C = A B + bias, or ReLU(A B + bias) with relu, in the
-// epilogue.  Returns 0 on success, 2 when no algorithm takes that epilogue,
-// 1 on another error.  ws: cuBLASLt workspace.
-int gemm_bf16(const void* A, const void* B, void* C, int m, int n, int k, void* ws, size_t ws_bytes,
-              cudaStream_t stream, const void* bias = nullptr, bool relu = false);
-// batch products C + i c_stride = A (B + i k n), i < batch, in one call
-// (B's matrices packed back to back, A shared); same epilogue and returns.
-int gemm_bf16_batched(const void* A, const void* B, void* C, int m, int n, int k, int batch, long long c_stride,
-                      void* ws, size_t ws_bytes, cudaStream_t stream, const void* bias = nullptr,
-                      bool relu = false);
-// Up to two fp32 -> bf16 vector roundings, spread over launch_add_ln's grid.
-struct CvtJobs {
-  const float* src[2] = {nullptr, nullptr};
-  __nv_bfloat16* dst[2] = {nullptr, nullptr};  // nullptr: no job
-  int n[2] = {0, 0};
-};
+// The layer's dense products on the tensor cores (gemm_tc.cu): row-major
+// bf16 C_z [m, n] = A [m, k] B_z [k, n] (+ bias [n], fp32) (then ReLU),
+// z < batch, fp32 accumulation, one rounding.  Tensor maps (bf16, 128-byte
+// swizzle, zero fill): tm_a over {k, m} with a {64, 128} box; tm_b over
+// {n, k, batch} with a {64, 64, 1} box; tm_c over {n, m, batch} with a
+// {64, 32, 1} box.  bn: columns per tile, 128 or 256 (gemm_tc_tile_n picks
+// one for the shape).
+int gemm_tc_tile_n(int m, int n, int batch);
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
+                           int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
+                           cudaStream_t stream);
 // out = LN(a + b (+ bias)) row by row over d columns (bf16 rows, fp32 gamma,
-// beta, bias; d a multiple of 8, <= 1024), plus the side jobs in cvt.
+// beta, bias; d a multiple of 8, <= 1024) (layer.cu).
 cudaError_t launch_add_ln(const void* a, const void* b, const float* bias, const float* gamma, const float* beta,
-                          void* out, long long rows, int d, cudaStream_t stream, const CvtJobs& cvt = CvtJobs());
-cudaError_t launch_bias_relu(void* f, const float* bias, long long rows, int n, cudaStream_t stream);
+                          void* out, long long rows, int d, cudaStream_t stream);
 
 // Number of chunks the D = 64 kernel should split each unit's key steps
 // into (1: no split), from the shape and the device's SM count.
