@@ -39,6 +39,7 @@ WORKLOAD = "base"
 N_SEG_BUFFERS = 8
 EVENT_EVERY = 10  # timed steps per sampled attention-kernel duration
 ROLL_BATCH = 12   # back-to-back roll launches per event pair
+HOLD_CYCLES = 1_000_000  # GPU spin (about 0.5 ms) before a timed call, while the host enqueues it
 ROLL_SETS = 4     # rotating roll buffer sets
 KERNEL_SOURCES = ["transformer_xl_relative_txl_gb300/csrc/relattn_tc64.cu",
                   "transformer_xl_relative_txl_gb300/csrc/relattn_tc_common.cuh",
@@ -50,6 +51,19 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 # ----------------------------------------------------------------------------
 # host-side helpers (also exercised by the CPU multi-process tests)
 # ----------------------------------------------------------------------------
+
+def idle_fill(flush, cycles=HOLD_CYCLES):
+    """Before a timed call: flush L2 (a 256 MB write), then hold the GPU in a
+    short spin, during which the host enqueues the call and its events.  The
+    binding takes tens of microseconds of host time per call, about a
+    kernel's length here, so without the hold a call's start event could
+    fire before the call itself was enqueued and charge that host time to the
+    kernel."""
+    import torch
+
+    flush.zero_()
+    torch.cuda._sleep(cycles)
+
 
 def counted_flops(B, H, D, W, M):
     """Three contractions (q.k, q.r, p.v) x 2 flops over the visible pairs:
@@ -410,7 +424,7 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
     cs = torch.cuda.current_stream()
     ts = []
     for it in range(warmup + steps):
-        flush.zero_()
+        idle_fill(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(cs)
         txl.txl_relattn_backward(q, k, v, stream.r, stream.u, stream.vb, o, lse, dout, M=wl.M, grads=grads)
@@ -492,7 +506,8 @@ def measure_roll(device, steps, warmup, hbm_peak, peak_src):
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=device)
     cs = torch.cuda.current_stream()
     out = {"l2": f"{ROLL_BATCH} launches back to back between one event pair, rotating over {ROLL_SETS} buffer "
-                 f"sets (each set's rows evicted from L2 before its next turn); L2 flushed before each batch",
+                 f"sets (each set's rows evicted from L2 before its next turn); L2 flushed before each batch, "
+                 f"then a ~2 ms GPU hold while the host enqueues it",
            "peak_source": f"{peak_src} hbm_gbs", "bytes": "2 tensors (k, v) x (read + write) x B*M*H*D*2"}
     for name in ("base", "large", "wide", "long"):
         wl = WORKLOADS[name]
@@ -516,7 +531,7 @@ def measure_roll(device, steps, warmup, hbm_peak, peak_src):
                                 ("pair", pair, "txl_mem_update on k, then on v (2 launches)")):
             ts = []
             for it in range(warmup + steps):
-                flush.zero_()
+                idle_fill(flush, HOLD_CYCLES * 4)  # the host enqueues the whole batch meanwhile
                 a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 a.record(cs)
                 for n in range(ROLL_BATCH):
@@ -547,7 +562,7 @@ def measure_roll(device, steps, warmup, hbm_peak, peak_src):
     t_f, t_a = [], []
     for it in range(warmup + steps):
         for fused in (True, False):
-            flush.zero_()
+            idle_fill(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(cs)
             if fused:
@@ -600,7 +615,7 @@ def measure_configs(device, steps, warmup, peak, peak_src):
         ts = []
         for it in range(warmup + steps):
             x, y = it % 2, (it + 1) % 2
-            flush.zero_()
+            idle_fill(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(cs)
             txl.txl_relattn_forward_roll(qd, kb[x], vb[x], rd, ud, vbd, o, kb[y][:, :M], vb[y][:, :M], M, M=M)
@@ -672,7 +687,7 @@ def measure_long_memory(device, steps, warmup, peak, peak_src):
                                                 "writes the W new rows)")):
         ts = []
         for it in range(warmup + steps):
-            flush.zero_()
+            idle_fill(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(cs)
             fn(it)
@@ -720,7 +735,7 @@ def measure_m_sweep(device, wl, steps, warmup, peak, flush, m_values=(0, 384, 16
         o = torch.empty(qd.shape, device=device, dtype=bf)
         ts = []
         for it in range(warmup + steps):
-            flush.zero_()
+            idle_fill(flush)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(cs)
             txl.txl_relattn_forward(qd, kd, vd, rd, ud, vbd, o, M=M)
@@ -772,7 +787,7 @@ def measure_cached_vs_recompute(device, long_ring_ms, steps, warmup):
     cs = torch.cuda.current_stream()
     ts = []
     for it in range(warmup + steps):
-        flush.zero_()
+        idle_fill(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(cs)
         txl.txl_relattn_forward(qd, kd, vd, rd, ud, vbd, o, M=0)
@@ -836,7 +851,7 @@ def measure_layer(device, steps, warmup, peak, peak_src):
     start = 0
     ts = []
     for it in range(warmup + steps):
-        flush.zero_()
+        idle_fill(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(cs)
         s2, m2 = txl.txl_layer_forward(h, out, k_ring, v_ring, start, M, dw, R, ws)
@@ -894,7 +909,7 @@ def measure_layer_gemms(device, steps, warmup, peak, x, dw, R, flush):
                           ("torch_matmul", lambda: torch.matmul(A, Bm))):
             ts = []
             for it in range(warmup + steps):
-                flush.zero_()
+                idle_fill(flush)
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(cs)
                 fn()
@@ -1052,7 +1067,10 @@ def _run_ours_sampled(args, txl, stream, wl, world, rank, local, device, cs, sam
     torch.cuda.synchronize()
     link_gbs = host_link_gbs(stream.e2e_bytes()[0], device)  # the link's state right now
     barrier(world)
-    e2e_el, _ = stream.run_e2e(args.warmup + K, E)
+    # untimed warm-up of the loop: the ring kernel's first launch, the first
+    # copies out of each pinned host buffer (two passes over the eight)
+    stream.run_e2e(args.warmup + K, 2 * N_SEG_BUFFERS)
+    e2e_el, _ = stream.run_e2e(args.warmup + K + 2 * N_SEG_BUFFERS, E)
     e2e_s = max_over_ranks(e2e_el, world)
     e2e = whole_job_throughput(tokens, world, E, e2e_s)
     h2d, d2h = stream.e2e_bytes()
@@ -1089,7 +1107,8 @@ def _run_ours_sampled(args, txl, stream, wl, world, rank, local, device, cs, sam
                      "per_launch_work": f"{flops} counted flops = 6*B*H*D*(W*M + W(W+1)/2)"},
         "e2e": {"value": e2e, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "call": "txl_sinusoid_rel + txl_relattn_forward_ring_append (memory as a ring of M+W rows; q and "
-                        "the new k, v rows uploaded contiguous, o read back, both on copy streams)",
+                        "the new k, v rows uploaded contiguous, o read back, both on copy streams), after an untimed "
+                        "warm-up of the same loop (two passes over the eight pinned host buffers)",
                 "host_link_h2d_gbs": link_gbs,
                 "host_link_note": "one pinned host->device copy of a step's upload bytes just before the loop "
                                   "(best of 3); the link is shared with the machine's other jobs (~200 GB/s "
