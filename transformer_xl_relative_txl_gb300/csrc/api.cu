@@ -259,6 +259,7 @@ int dense_impl(const void* A, const void* B, void* C, int m, int n, int k, int b
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
+  const int bn = txl::gemm_tc_tile_n(m, n, batch);
   CUtensorMap ta, tb, tc;
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
@@ -270,7 +271,7 @@ int dense_impl(const void* A, const void* B, void* C, int m, int n, int k, int b
     const cuuint64_t dims[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(k),
                                 static_cast<cuuint64_t>(batch)};
     const cuuint64_t strides[2] = {static_cast<cuuint64_t>(n) * 2, static_cast<cuuint64_t>(b_stride) * 2};
-    const cuuint32_t box[3] = {64, 64, 1};
+    const cuuint32_t box[3] = {64, static_cast<cuuint32_t>(txl::gemm_tc_k_block(bn)), 1};
     if (!enc(&tb, B, 3, dims, strides, box)) return TXL_ERR_CUDA;
   }
   {
@@ -282,8 +283,7 @@ int dense_impl(const void* A, const void* B, void* C, int m, int n, int k, int b
   }
   txl::WaitCtl wc;
   if (wait_ctl(&wc) != TXL_OK) return TXL_ERR_CUDA;
-  return from_cuda(txl::launch_gemm_tc(ta, tb, tc, m, n, k, batch, txl::gemm_tc_tile_n(m, n, batch), bias, relu, wc,
-                                       stream));
+  return from_cuda(txl::launch_gemm_tc(ta, tb, tc, m, n, k, batch, bn, bias, relu, wc, stream));
 }
 
 // txl_mem_ring_append for n (1 or 2) rings of one geometry, each run of

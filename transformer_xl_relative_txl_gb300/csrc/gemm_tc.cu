@@ -36,16 +36,21 @@ namespace txl {
 namespace {
 
 constexpr int GBM = 128;              // rows per tile (TMEM lanes)
-constexpr int GBK = 64;               // k per stage (one 128-byte swizzle row of bf16)
-constexpr int kATile = GBM * 128;     // 16 KB
-constexpr int kBBlock = GBK * 128;    // 64 k-rows x 64 columns of B: 8 KB
+constexpr int kATile = GBM * 128;     // 128 rows x 64 k of A: 16 KB (one 128-byte swizzle row of bf16 per row)
 constexpr int kGemmThreads = 192;
 constexpr int kEpiBytes = 32 * 128;   // one epilogue warp's staging: 32 rows x 64 bf16
 
+// Per column-tile width: k per stage and stages.  Deeper stages (fewer
+// barrier round trips and loads per FLOP) measured faster with 128-column
+// tiles (W_2 of the base layer: 34.6 -> 31.8 us); with 256-column tiles they
+// would leave two stages, and four of 64 k stay faster.
 template <int BN>
 struct GemmCfg {
-  static constexpr int kStageBytes = kATile + (BN / 64) * kBBlock;
-  static constexpr int kStages = BN == 256 ? 4 : 6;
+  static constexpr int kBK = BN == 128 ? 128 : 64;            // k per stage
+  static constexpr int kABoxes = kBK / 64;                    // 64-k tiles of A per stage
+  static constexpr int kBBlock = kBK * 128;                   // kBK k-rows x 64 columns of B
+  static constexpr int kStageBytes = kABoxes * kATile + (BN / 64) * kBBlock;
+  static constexpr int kStages = BN == 256 ? 4 : 3;
   static constexpr int kOffEpi = kStages * kStageBytes;             // 4 x 4 KB staging
   static constexpr int kOffBias = kOffEpi + 4 * kEpiBytes;          // 4 x BN floats
   static constexpr int kOffBar = kOffBias + 4 * BN * 4;
@@ -114,6 +119,9 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
+  constexpr int GBK = Cfg::kBK;
+  constexpr int kBBlock = Cfg::kBBlock;
+  constexpr int kBOff = Cfg::kABoxes * kATile;  // B's blocks follow A's tiles in a stage
   const int nk = (p.k + GBK - 1) / GBK;
 
   if (threadIdx.x == 0) {
@@ -154,10 +162,12 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!(ok = mbar_wait(&bars->empty[s], ((it / S) & 1) ^ 1, wait_ns, abort))) break;
           uint8_t* st = smem + s * Cfg::kStageBytes;
           mbar_arrive_expect_tx(&bars->full[s], Cfg::kStageBytes);
-          tma_load_2d(st, &tm_a, &bars->full[s], kb * GBK, ti.m0);
+#pragma unroll
+          for (int a = 0; a < Cfg::kABoxes; ++a)
+            tma_load_2d(st + a * kATile, &tm_a, &bars->full[s], kb * GBK + 64 * a, ti.m0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
-            tma_load_3d(st + kATile + j * kBBlock, &tm_b, &bars->full[s], n0 + 64 * j, kb * GBK, ti.z);
+            tma_load_3d(st + kBOff + j * kBBlock, &tm_b, &bars->full[s], n0 + 64 * j, kb * GBK, ti.z);
         }
       }
       if (!ok) report_timeout(abort, p.status);
@@ -185,13 +195,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           if (!(ok = mbar_wait(&bars->full[s], (it / S) & 1, wait_ns, abort))) break;
           tc_fence_after();
           const uint32_t st = base + s * Cfg::kStageBytes;
-          // A: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart.
-          // B: N-major, 64-column blocks kBBlock apart, 8-k-row groups 1024 apart.
+          // A: K-major, 128-byte swizzle, 8-row groups 1024 bytes apart, one
+          // 16 KB tile per 64 k.  B: N-major, 64-column blocks kBBlock apart,
+          // 8-k-row groups 1024 apart.
           const uint64_t da = sdesc_sw128(st, 16, 1024);
-          const uint64_t db = sdesc_sw128(st + kATile, kBBlock, 1024);
+          const uint64_t db = sdesc_sw128(st + kBOff, kBBlock, 1024);
 #pragma unroll
           for (int kk = 0; kk < GBK / 16; ++kk)
-            mma_ss(d, da + kk * 2, db + ((kk * 16 * 128) >> 4), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+            mma_ss(d, da + (kk >> 2) * (kATile >> 4) + (kk & 3) * 2, db + ((kk * 16 * 128) >> 4), idesc,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
           tc_commit(&bars->empty[s]);
         }
         if (!ok) break;
@@ -322,6 +334,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 }
 
 }  // namespace
+
+int gemm_tc_k_block(int bn) { return bn == 128 ? GemmCfg<128>::kBK : GemmCfg<256>::kBK; }
 
 int gemm_tc_tile_n(int m, int n, int batch) {
   // Fewer waves of tiles against smaller tiles: the time of a wave is about

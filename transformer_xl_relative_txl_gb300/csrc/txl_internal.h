@@ -141,10 +141,11 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
 // bf16 C_z [m, n] = A [m, k] B_z [k, n] (+ bias [n], fp32) (then ReLU),
 // z < batch, fp32 accumulation, one rounding.  Tensor maps (bf16, 128-byte
 // swizzle, zero fill): tm_a over {k, m} with a {64, 128} box; tm_b over
-// {n, k, batch} with a {64, 64, 1} box; tm_c over {n, m, batch} with a
-// {64, 32, 1} box.  bn: columns per tile, 128 or 256 (gemm_tc_tile_n picks
-// one for the shape).
+// {n, k, batch} with a {64, gemm_tc_k_block(bn), 1} box; tm_c over
+// {n, m, batch} with a {64, 32, 1} box.  bn: columns per tile, 128 or 256
+// (gemm_tc_tile_n picks one for the shape).
 int gemm_tc_tile_n(int m, int n, int batch);
+int gemm_tc_k_block(int bn);
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
                            int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
                            cudaStream_t stream);
