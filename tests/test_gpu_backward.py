@@ -4,8 +4,14 @@ The forward runs first on the device (its o and lse feed the backward, as in
 training); the oracle differentiates the same seeded inputs from scratch.
 Tolerances: fp32 inputs max |err| <= 1e-5 * max(1, max |want|); bf16 inputs
 rel-L2 <= 5e-3 and max |err| <= 2e-2 * max(1, max |want|) per gradient
-tensor (the only rounding besides fp32 arithmetic is the forward's bf16 o,
-which enters through Delta_i = dout_i . o_i).
+tensor.  On the bf16 path G = scale P (dP - Delta) enters the gradient
+products rounded to bf16 (2^-9 relative), beside the forward's bf16 o in
+Delta.  The two bias gradients are [H, D] sums over every (sequence, query)
+row of d(q+u) and d(q+v), whose terms largely cancel: their norm is a small
+residue of the summed magnitudes, so the same per-term rounding is a larger
+fraction of it (up to 6e-3 measured at the large workload, against about
+2e-3 for every other gradient).  Their rel-L2 bound is 1e-2; the max |err|
+bound is the same as for the others.
 """
 
 import numpy as np
@@ -66,7 +72,8 @@ def _compare(got, want, dtype):
             assert err <= 1e-5 * scale, f"{key}: max abs {err:.3e} (scale {scale:.3e})"
         else:
             rel = np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-30)
-            assert rel <= 5e-3 and err <= 2e-2 * scale, f"{key}: rel-L2 {rel:.3e}, max abs {err:.3e}"
+            rel_bound = 1e-2 if key.startswith("dbias") else 5e-3
+            assert rel <= rel_bound and err <= 2e-2 * scale, f"{key}: rel-L2 {rel:.3e}, max abs {err:.3e}"
 
 
 CASES = [
@@ -143,6 +150,27 @@ def test_backward_base_size_sampled_head(txl):
     head = {"dq": got["dq"][:, :, sl], "dk": got["dk"][:, :, sl], "dv": got["dv"][:, :, sl],
             "dr": got["dr"][:, sl], "dbias_u": got["dbias_u"][sl], "dbias_v": got["dbias_v"][sl]}
     _compare(head, want, "bf16")
+
+
+@pytest.mark.parametrize("name,heads", [("large", [11]), ("wide", [5]), ("long", None)])
+def test_backward_full_size(txl, name, heads):
+    """The other workloads at full size in one call each: large (D = 64,
+    tensor cores), wide (D = 128, the CUDA-core path) and long (W = 128 over
+    M = 1600 rows, tensor cores); every gradient of the listed heads (every
+    head of long) against the oracle's backward of the same inputs."""
+    from synthetic import WORKLOADS
+
+    wl = WORKLOADS[name]
+    B, H, D, W, M = wl.B, wl.H, wl.D, wl.W, wl.M
+    q, k, v, r, bu, bv, dout = _case(B, H, D, W, M, "bf16")
+    got = _run(txl, q, k, v, r, bu, bv, dout, M, "bf16")
+    for h in (range(H) if heads is None else heads):
+        sl = slice(h, h + 1)
+        want = O.relattn_backward(q[:, :, sl], k[:, :, sl], v[:, :, sl], r[:, sl], bu[sl], bv[sl], M,
+                                  dout[:, :, sl], D ** -0.5)
+        head = {"dq": got["dq"][:, :, sl], "dk": got["dk"][:, :, sl], "dv": got["dv"][:, :, sl],
+                "dr": got["dr"][:, sl], "dbias_u": got["dbias_u"][sl], "dbias_v": got["dbias_v"][sl]}
+        _compare(head, want, "bf16")
 
 
 def test_backward_rejects_bad_arguments(txl):
