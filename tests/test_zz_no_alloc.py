@@ -1,8 +1,16 @@
-"""txl_relattn_forward_static: the forward without any allocation.
+"""txl_relattn_forward_static: the forward for callers that cannot allocate.
 
-Compared with txl_relattn_forward on two calls in a row: the same kernels
-run, so the outputs must agree bit for bit.  A launch with few units splits
-its key ranges (the path that needs scratch), one with many units does not.
+Some callers must not call cudaMalloc: a host that hands all device memory to
+its own pool at start-up, code running inside another library's allocator
+callbacks, or a loop that must never stall on the allocator (cudaMalloc and
+cudaFree can synchronise the device).  This entry point keeps the scratch of
+split launches in a fixed device array inside the library instead.
+
+It is compared with txl_relattn_forward on two calls in a row: the same
+kernels run, so the outputs must agree bit for bit.  A launch with few units
+splits its key ranges (the path that needs scratch), one with many units does
+not.  The file is collected last, so a run that stops at its first failure
+has run every other test before it.
 """
 
 import pytest
