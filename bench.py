@@ -408,18 +408,52 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
     """txl_relattn_backward on segment buffer 0 of the workload (its forward
     output and lse, a seeded output gradient), each call timed with CUDA
     events on its stream, L2 flushed between calls (outside the events)."""
+    out = time_backward(stream.q[0], stream.k[0], stream.v[0], stream.r, stream.u, stream.vb, wl, steps, warmup,
+                        peak, peak_src)
+    out["call"] = "txl_relattn_backward (dq kernel, dk/dv kernel, bias sums)"
+    out["gpu_launches_per_call"] = 3
+    out["roofline"]["kernel"] = "bwd_dq_tc64_kernel + bwd_dkdv_tc64_kernel"
+    return out
+
+
+def measure_backward_wide(device, steps, warmup, peak, peak_src):
+    """txl_relattn_backward at the wide workload (B=8 H=8 D=128 W=768
+    M=768): the D = 128 tensor-core path (pair terms rebuilt and written in
+    bf16, then five tensor-core products and the bias sums)."""
+    import torch
+
+    import transformer_xl_relative_txl_gb300 as txl
+    from synthetic import WORKLOADS, make_prefilled, project_r
+
+    wl = WORKLOADS["wide"]
+    q, k, v, seg = make_prefilled(wl, wl.M)
+    bf = torch.bfloat16
+    to = lambda a, dt=bf: torch.from_numpy(np.ascontiguousarray(a)).to(device).to(dt)
+    R = torch.empty(wl.M + wl.W, wl.d_model, device=device)
+    txl.txl_sinusoid_rel(R)
+    rd = to(project_r(R.cpu().numpy(), seg.W_r, wl.H, wl.D, "bf16"))
+    out = time_backward(to(q), to(k), to(v), rd, to(seg.bias_u, torch.float32), to(seg.bias_v, torch.float32), wl,
+                        steps, warmup, peak, peak_src)
+    out["call"] = ("txl_relattn_backward, D = 128 (pair-term kernel, products for dq, dk, dv, dr, "
+                   "dq and bias sums)")
+    out["gpu_launches_per_call"] = 7
+    out["roofline"]["kernel"] = "bwd_scores128_kernel + bgemm_kernel x4 + sums (the whole call)"
+    out["config"] = {"workload": "wide", "B": wl.B, "H": wl.H, "D": wl.D, "W": wl.W, "M": wl.M}
+    return out
+
+
+def time_backward(q, k, v, r, u, vb, wl, steps, warmup, peak, peak_src):
     import torch
 
     import transformer_xl_relative_txl_gb300 as txl
     from synthetic import make_dout
 
-    dev_ = stream.q[0].device
-    q, k, v = stream.q[0], stream.k[0], stream.v[0]
+    dev_ = q.device
     o = torch.empty(q.shape, device=dev_, dtype=torch.bfloat16)
     lse = torch.empty(wl.B, wl.H, wl.W, device=dev_, dtype=torch.float32)
-    txl.txl_relattn_forward(q, k, v, stream.r, stream.u, stream.vb, o, lse, M=wl.M)
+    txl.txl_relattn_forward(q, k, v, r, u, vb, o, lse, M=wl.M)
     dout = torch.from_numpy(make_dout(wl)).to(dev_).to(torch.bfloat16)
-    grads = txl.txl_relattn_backward(q, k, v, stream.r, stream.u, stream.vb, o, lse, dout, M=wl.M)
+    grads = txl.txl_relattn_backward(q, k, v, r, u, vb, o, lse, dout, M=wl.M)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev_)
     cs = torch.cuda.current_stream()
     ts = []
@@ -427,7 +461,7 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
         idle_fill(flush)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(cs)
-        txl.txl_relattn_backward(q, k, v, stream.r, stream.u, stream.vb, o, lse, dout, M=wl.M, grads=grads)
+        txl.txl_relattn_backward(q, k, v, r, u, vb, o, lse, dout, M=wl.M, grads=grads)
         b.record(cs)
         if it >= warmup:
             ts.append((a, b))
@@ -437,10 +471,9 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
     ms = float(np.mean([a.elapsed_time(b) for a, b in ts]))
     flops = backward_flops(wl.B, wl.H, wl.D, wl.W, wl.M)
     achieved = flops / (ms / 1e3) / 1e12
-    return {"call": "txl_relattn_backward (dq kernel, dk/dv kernel, bias sums)",
-            "value": wl.B * wl.W / (ms / 1e3), "unit": "tokens/s", "ms": ms, "calls": len(ts),
-            "gpu_launches_per_call": 3, "l2": "flushed between calls (256 MB write, outside the events)",
-            "roofline": {"kernel": "bwd_dq_tc64_kernel + bwd_dkdv_tc64_kernel", "bound": "tensor",
+    return {"value": wl.B * wl.W / (ms / 1e3), "unit": "tokens/s", "ms": ms, "calls": len(ts),
+            "l2": "flushed between calls (256 MB write, outside the events)",
+            "roofline": {"bound": "tensor",
                          "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                          "peak_source": f"{peak_src} bf16_tflops (burst)", "traffic": None,
                          "per_launch_work": f"{flops} counted flops = 2*B*H*D*(4*(W*M + W(W+1)/2) + 2*W(W+1)/2)"}}
@@ -1117,6 +1150,7 @@ def _run_ours_sampled(args, txl, stream, wl, world, rank, local, device, cs, sam
         "clocks": sampler.summary(h0, h1),
     }
     result["backward"] = measure_backward(stream, wl, max(5, min(K, 50)), 3, peak, peak_src)
+    result["backward_wide"] = measure_backward_wide(device, max(5, min(K, 30)), 3, peak, peak_src)
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
     result["roll"] = measure_roll(device, max(5, min(K, 50)), 3, hbm, peak_src)
     result["configs"] = measure_configs(device, max(5, min(K, 50)), 3, peak, peak_src)

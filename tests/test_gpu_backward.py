@@ -91,6 +91,12 @@ CASES = [
     (1, 2, 64, 256, 0, "bf16", 0),   # first segment, whole tiles
     (1, 2, 64, 128, 512, "bf16", 0), # memory longer than the segment
     (3, 1, 64, 64, 64, "bf16", 64),  # half a query tile
+    # bf16, D = 128: the tensor-core kernels (memory a multiple of 8 rows)
+    (2, 2, 128, 200, 136, "bf16", 3),  # several tiles, ragged
+    (1, 3, 128, 300, 512, "bf16", 0),  # memory longer than the segment
+    (2, 1, 128, 7, 8, "bf16", 1),      # fewer rows than a warp
+    # bf16, D = 128, memory not a multiple of 8: the CUDA-core kernels
+    (1, 2, 128, 130, 37, "bf16", 0),
 ]
 
 
@@ -119,21 +125,35 @@ def test_backward_custom_scale(txl):
     _compare(got, want, "f32")
 
 
-@pytest.mark.parametrize("dtype,o_dtype", [("bf16", "f32"), ("f32", "f32"), ("bf16", "bf16")])
-def test_backward_deterministic(txl, dtype, o_dtype):
-    """Bit-identical on repeated calls, except dr on the tensor-core path
-    (bf16 o and dout, D = 64), whose slot sums arrive by atomic fp32 adds
-    (TMA bulk reductions) in any order: there the two results agree to fp32
-    rounding."""
-    q, k, v, r, bu, bv, dout = _case(2, 2, 64, 130, 70, dtype)
-    a = _run(txl, q, k, v, r, bu, bv, dout, 70, dtype, o_dtype=o_dtype)
-    b = _run(txl, q, k, v, r, bu, bv, dout, 70, dtype, o_dtype=o_dtype)
-    tc = dtype == "bf16" and o_dtype == "bf16"
+@pytest.mark.parametrize("D,dtype,o_dtype", [(64, "bf16", "f32"), (64, "f32", "f32"), (64, "bf16", "bf16"),
+                                             (128, "bf16", "bf16")])
+def test_backward_deterministic(txl, D, dtype, o_dtype):
+    """Bit-identical on repeated calls, except dr on the D = 64 tensor-core
+    path (bf16 o and dout), whose slot sums arrive by atomic fp32 adds (TMA
+    bulk reductions) in any order: there the two results agree to fp32
+    rounding.  The D = 128 tensor-core path sums in a fixed order."""
+    q, k, v, r, bu, bv, dout = _case(2, 2, D, 130, 72, dtype)
+    a = _run(txl, q, k, v, r, bu, bv, dout, 72, dtype, o_dtype=o_dtype)
+    b = _run(txl, q, k, v, r, bu, bv, dout, 72, dtype, o_dtype=o_dtype)
+    tc = D == 64 and dtype == "bf16" and o_dtype == "bf16"
     for key in KEYS:
         if tc and key == "dr":
             np.testing.assert_allclose(a[key], b[key], rtol=1e-5, atol=1e-6)
         else:
             assert np.array_equal(a[key], b[key]), key
+
+
+def test_backward_d128_scratch_reuse(txl):
+    """The D = 128 tensor-core path keeps its pair terms in a scratch buffer
+    reused across calls: a call after one of another shape (which leaves
+    nonzero pair terms where this call's layout has zeros to read) must still
+    match the oracle."""
+    big = _case(2, 2, 128, 250, 264, "bf16", seed=1)
+    _run(txl, *big, 264, "bf16")
+    q, k, v, r, bu, bv, dout = _case(1, 2, 128, 190, 40, "bf16", seed=2)
+    got = _run(txl, q, k, v, r, bu, bv, dout, 40, "bf16")
+    want = O.relattn_backward(q, k, v, r, bu, bv, 40, dout, 128 ** -0.5)
+    _compare(got, want, "bf16")
 
 
 def test_backward_base_size_sampled_head(txl):
@@ -154,9 +174,9 @@ def test_backward_base_size_sampled_head(txl):
 
 @pytest.mark.parametrize("name,heads", [("large", [11]), ("wide", [5]), ("long", None)])
 def test_backward_full_size(txl, name, heads):
-    """The other workloads at full size in one call each: large (D = 64,
-    tensor cores), wide (D = 128, the CUDA-core path) and long (W = 128 over
-    M = 1600 rows, tensor cores); every gradient of the listed heads (every
+    """The other workloads at full size in one call each: large (D = 64),
+    wide (D = 128) and long (W = 128 over M = 1600 rows), all three on the
+    tensor cores; every gradient of the listed heads (every
     head of long) against the oracle's backward of the same inputs."""
     from synthetic import WORKLOADS
 

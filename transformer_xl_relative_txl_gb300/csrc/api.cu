@@ -772,6 +772,20 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
                                                   dk, dv, dr, dbias_u, dbias_v, B, W, M, H, n_r, scale, scratch, wc,
                                                   stream));
   }
+  if (dtype == TXL_BF16 && go_dtype == TXL_BF16 && D == 128 && txl::relattn_bwd_tc128_supported(W, M)) {
+    // tensor-core path, pair terms materialised
+    if (split_scratch(stream, txl::relattn_bwd_tc128_scratch_bytes(B, W, M, H), 0, &scratch, &unused) !=
+        cudaSuccess)
+      return TXL_ERR_CUDA;
+    txl::WaitCtl wc;
+    if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
+    wc.limit_ns = g_wait_ns.load();
+    wc.inject_stall = 0;
+    if ((W + 127) / 128 * static_cast<long long>(B) * H > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
+    return from_cuda(txl::launch_relattn_bwd_tc128(tensor_map_encoder(), q, k, v, r, bias_u, bias_v, lse, o, dout,
+                                                   dq, dk, dv, dr, dbias_u, dbias_v, B, W, M, H, n_r, scale,
+                                                   scratch, wc, stream));
+  }
   if (split_scratch(stream, txl::relattn_bwd_simt_scratch_bytes(B, W, H, D), 0, &scratch, &unused) != cudaSuccess)
     return TXL_ERR_CUDA;
   const bool vec16 = (D * es) % 16 == 0;  // with 16-byte aligned bases, every row is then aligned

@@ -1,0 +1,886 @@
+// Backward of the relative attention on the tensor cores for D = 128: bf16
+// q, k, v, r, o and dout, fp32 accumulation and gradients.
+//
+// The formulas and the stop-gradient are those of relattn_bwd.cu ("Transformer-
+// XL, explained", method step 2 and the symbol SG(.)):
+//   p_ij = exp(s_ij - lse_i),  g_ij = scale p_ij (dout_i . v_j - Delta_i)
+//   dq_i = sum_j g_ij k_j + sum_j g_ij r_{M+i-j}
+//   dk_j = sum_i g_ij (q_i+u),  dv_j = sum_i p_ij dout_i   (segment keys j)
+//   dr_d = sum_{b,i} g_{i, M+i-d} (q_i+v),  du = sum_{b,i} sum_j g_ij k_j,
+//   dbias_v = sum_{b,i} sum_j g_ij r_{M+i-j}
+//
+// At D = 128 the fused D = 64 design does not fit (the tiles of both score
+// operands and the gradient accumulators exceed the shared and tensor
+// memory), so the work is split in three:
+//   1. bwd_scores128_kernel, one CTA per (batch, head, 128-query tile), 64-key
+//      steps: S = (q+u) K^T, dP = dout V^T and the 192-distance window
+//      (q+v) R^T on the tensor cores (K = 128), then per pair p and g with the
+//      distance term shifted into key order as in the forward.  It writes, in
+//      bf16, G [bh][i][j] and P [bh][i][j] (key order) and GS [bh][i][d] (the
+//      same g in distance order, d = M+i-j).
+//   2. bgemm_kernel, this library's tcgen05 GEMM arranged for the five
+//      products (M = 128 rows of a tile, N = D = 128, fp32 accumulators in
+//      TMEM, fp32 results): dq_c = G K and dq_d = GS r per (batch, head);
+//      dk = G^T (q+u) and dv = P^T dout over the segment keys (G and P read as
+//      MN-major A operands); dr = sum_b GS^T (q+v) per head (the k loop runs
+//      over every sequence's queries).
+//   3. bwd_sum128_kernel: dq = dq_c + dq_d, and the bias gradients as sums of
+//      dq_c and dq_d over (batch, query) in a fixed order.
+// Every result is deterministic.  Every wait is bounded; a timed-out wait
+// raises the device status word and the CTA unwinds.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_bf16.h>
+
+#include <atomic>
+#include <cstdint>
+#include <algorithm>
+#include <initializer_list>
+
+#include "relattn_tc_common.cuh"
+#include "txl_device.cuh"
+#include "txl_internal.h"
+
+namespace txl {
+namespace {
+
+constexpr int D = 128;
+constexpr int BM = 128;  // query rows per tile
+constexpr int BN = 64;   // keys per step
+constexpr float kLog2e = 1.4426950408889634f;
+
+// ---------------------------------------------------------------------------
+// 1. Score rebuild
+// ---------------------------------------------------------------------------
+// Shared memory: every D = 128 operand tile is two 64-column halves (128-byte
+// rows, 128-byte swizzle), the second half right after the first.  K, V and
+// the distance window are single tiles, refilled for step t + 1 as soon as
+// the MMAs of step t have read them (the MMAs of step t + 1 wait for the
+// pairs of step t anyway).  G and P of a step leave through 128 x 64 staging
+// tiles and TMA stores; GS through one 32 x 32 staging tile per warp and
+// row-contiguous stores.
+constexpr int kHalfQ = BM * 128;   // 128 rows x 64 bf16: 16 KB
+constexpr int kHalfK = BN * 128;   // 64 rows: 8 KB
+constexpr int kHalfR = 192 * 128;  // 192 distance rows: 24 KB
+constexpr int kSOffQu = 0;
+constexpr int kSOffQv = kSOffQu + 2 * kHalfQ;
+constexpr int kSOffDO = kSOffQv + 2 * kHalfQ;
+constexpr int kSOffK = kSOffDO + 2 * kHalfQ;
+constexpr int kSOffV = kSOffK + 2 * kHalfK;
+constexpr int kSOffR = kSOffV + 2 * kHalfK;     // the window (the raw q tile before the first)
+constexpr int kSOffG = kSOffR + 2 * kHalfR;     // G staging: 128 rows x 64 keys
+constexpr int kSOffP = kSOffG + BM * BN * 2;    // P staging
+constexpr int kSOffGS = kSOffP + BM * BN * 2;   // GS staging: 8 warps x 32 rows x 32 values
+constexpr int kSOffBar = kSOffGS + 8 * 32 * 64;
+constexpr int kSOffBias = kSOffBar + 256;       // u, then v of the head (fp32)
+constexpr int kSSmem = kSOffBias + 2 * D * 4 + 1024;
+static_assert(kSSmem <= 232448, "shared memory budget");
+constexpr uint32_t kColS = 0, kColDP = 64, kColWin = 128, kSTmemCols = 512;
+constexpr int kSThreads = 256;
+
+struct ScoreParams {
+  const float* bias_u;
+  const float* bias_v;
+  const float* lse;         // [B, H, W]
+  const __nv_bfloat16* o;   // [B, W, H, D]
+  const __nv_bfloat16* dout;
+  __nv_bfloat16* GS;        // [B*H][W][LP], column d = distance
+  __nv_bfloat16* Qu;        // [B, W, H, D]: q + u, rounded as the MMAs see it
+  __nv_bfloat16* Qv;        // [B, W, H, D]: q + v
+  int B, W, M, H, nqt, LP;
+  float scale, scale_log2e;
+  unsigned int* status;
+  unsigned long long wait_ns;
+};
+
+struct SBars {
+  uint64_t q, in, m1, fin;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Row a of (q+u) and (q+v) for the 64 head dims of half `half` (its own
+// 64-column tile of both), from the raw q tile staged in the same layout;
+// also written to gqu / gqv (the row's 64 dims, 16-byte aligned) unless null.
+__device__ __forceinline__ void build_half128(const uint8_t* sQ, uint8_t* sQu, uint8_t* sQv, int a, int half,
+                                              const float* bu, const float* bv, __nv_bfloat16* gqu,
+                                              __nv_bfloat16* gqv) {
+  const uint8_t* src = sQ + half * kHalfQ;
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    const uint32_t off = (a >> 3) * 1024 + (a & 7) * 128 + ((c ^ (a & 7)) << 4);
+    const uint4 raw = *reinterpret_cast<const uint4*>(src + off);
+    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
+    const float* ub = bu + 64 * half + 8 * c;
+    const float* vb = bv + 64 * half + 8 * c;
+    uint32_t qu[4], qv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const float x0 = bf16_lo(w4[e]), x1 = bf16_hi(w4[e]);
+      qu[e] = pack_bf16x2(x0 + ub[2 * e], x1 + ub[2 * e + 1]);
+      qv[e] = pack_bf16x2(x0 + vb[2 * e], x1 + vb[2 * e + 1]);
+    }
+    const uint4 xu = make_uint4(qu[0], qu[1], qu[2], qu[3]), xv = make_uint4(qv[0], qv[1], qv[2], qv[3]);
+    *reinterpret_cast<uint4*>(sQu + half * kHalfQ + off) = xu;
+    *reinterpret_cast<uint4*>(sQv + half * kHalfQ + off) = xv;
+    if (gqu != nullptr) {
+      reinterpret_cast<uint4*>(gqu)[c] = xu;
+      reinterpret_cast<uint4*>(gqv)[c] = xv;
+    }
+  }
+}
+
+// Zeros of row[lo, hi) (bf16; row 16-byte aligned).
+__device__ __forceinline__ void zero_bf16(__nv_bfloat16* row, int lo, int hi) {
+  int d = lo;
+  for (; d < hi && (d & 7) != 0; ++d) row[d] = __float2bfloat16_rn(0.f);
+  for (; d + 8 <= hi; d += 8) *reinterpret_cast<uint4*>(row + d) = make_uint4(0u, 0u, 0u, 0u);
+  for (; d < hi; ++d) row[d] = __float2bfloat16_rn(0.f);
+}
+
+// 32 values of row a, keys [32 half, 32 half + 64) of a 128 x 64 tile staged
+// for a 128-byte-swizzled TMA store (64 bf16 per row).
+__device__ __forceinline__ void stage_row32(uint8_t* tile, int a, int half, const float (&x)[32]) {
+  uint8_t* rowp = tile + (a >> 3) * 1024 + (a & 7) * 128;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(rowp + (((4 * half + c) ^ (a & 7)) << 4)) =
+        make_uint4(pack_bf16x2(x[8 * c], x[8 * c + 1]), pack_bf16x2(x[8 * c + 2], x[8 * c + 3]),
+                   pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
+}
+
+// A warp's 32 x 32 GS staging tile: row `lane` holds the lane's 32 values in
+// increasing distance order (value k at distance D0 - 31 + k, i.e. g[31 - k]),
+// 64 bytes per row with the 16-byte chunks rotated by (row / 2) % 4 so that
+// the writes spread over every bank.
+__device__ __forceinline__ void stage_gs(uint8_t* st, int lane, const float (&g)[32]) {
+  uint8_t* rowp = st + lane * 64;
+  const int rot = (lane >> 1) & 3;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint32_t w[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int k = 8 * c + 2 * e;  // positions k, k + 1
+      w[e] = pack_bf16x2(g[31 - k], g[30 - k]);
+    }
+    *reinterpret_cast<uint4*>(rowp + ((c ^ rot) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
+}
+
+// 8 warps, two per TMEM lane quadrant (key columns 0-31 and 32-63 of the same
+// rows).  Thread 0 issues the loads, the score MMAs and the G / P stores;
+// everyone waits on the MMA barrier, computes its 32 pairs and writes them
+// out.
+__global__ void __launch_bounds__(kSThreads, 1)
+    bwd_scores128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
+                         const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_g,
+                         const __grid_constant__ CUtensorMap tm_p, const ScoreParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  uint8_t* sQu = smem + kSOffQu;
+  uint8_t* sQv = smem + kSOffQv;
+  uint8_t* sDO = smem + kSOffDO;
+  uint8_t* sK = smem + kSOffK;
+  uint8_t* sV = smem + kSOffV;
+  uint8_t* sR = smem + kSOffR;
+  uint8_t* sG = smem + kSOffG;
+  uint8_t* sP = smem + kSOffP;
+  SBars* bars = reinterpret_cast<SBars*>(smem + kSOffBar);
+  float* sBias = reinterpret_cast<float*>(smem + kSOffBias);
+  volatile int* abort = &bars->abort;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quad = warp & 3, half = warp >> 2;
+  const int a = quad * 32 + lane;  // this thread's row of the tile
+  uint8_t* sGS = smem + kSOffGS + warp * 32 * 64;
+  const uint64_t wait_ns = p.wait_ns;
+
+  const Unit w = decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt);
+  const int T = w.nks;
+  const int i = w.i0 + a;  // query row
+  const int z = w.b * p.H + w.h;
+
+  if (tid == 0) {
+    mbar_init(&bars->q, 1);
+    mbar_init(&bars->in, 1);
+    mbar_init(&bars->m1, 1);
+    mbar_init(&bars->fin, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(&bars->tmem_base, kSTmemCols);
+    tmem_relinquish();
+  }
+  if (tid < 2 * D) sBias[tid] = tid < D ? p.bias_u[w.h * D + tid] : p.bias_v[w.h * D + tid - D];
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
+  // Inputs of step t: keys and values [64 t, 64 t + 64) and the window of
+  // distance rows [wb, wb + 192), wb = M + i0 - 64 t - 64.
+  uint32_t n_in = 0;  // loads issued (thread 0)
+  auto load_in = [&](int t) {
+    const int wb = p.M + w.i0 - BN * t - BN;
+    mbar_arrive_expect_tx(&bars->in, 4 * kHalfK + 2 * kHalfR);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      tma_load_4d(sK + hh * kHalfK, &tm_k, &bars->in, 64 * hh, w.h, BN * t, w.b);
+      tma_load_4d(sV + hh * kHalfK, &tm_v, &bars->in, 64 * hh, w.h, BN * t, w.b);
+      tma_load_3d(sR + hh * kHalfR, &tm_rw, &bars->in, 64 * hh, w.h, wb);
+    }
+    ++n_in;
+  };
+  if (tid == 0) {
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_rw);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_g);
+    tma_prefetch_desc(&tm_p);
+    // the raw q tile goes to the window buffer until (q+u), (q+v) are built
+    mbar_arrive_expect_tx(&bars->q, 4 * kHalfQ);
+#pragma unroll
+    for (int hh = 0; hh < 2; ++hh) {
+      tma_load_4d(sR + hh * kHalfQ, &tm_q, &bars->q, 64 * hh, w.h, w.i0, w.b);
+      tma_load_4d(sDO + hh * kHalfQ, &tm_do, &bars->q, 64 * hh, w.h, w.i0, w.b);
+    }
+  }
+
+  // Per-row constants: lse (log2 domain) and Delta = dout . o.
+  float lse2 = INFINITY, delta = 0.f;  // rows past W: every p is 0
+  if (i < p.W) {
+    const long long row_id = (static_cast<long long>(w.b) * p.H + w.h) * p.W + i;
+    lse2 = p.lse[row_id] * kLog2e;
+    const long long off = ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D;
+    const uint4* po = reinterpret_cast<const uint4*>(p.o + off);
+    const uint4* pg = reinterpret_cast<const uint4*>(p.dout + off);
+    float s0 = 0.f, s1 = 0.f;
+#pragma unroll 4
+    for (int c = 0; c < D / 8; ++c) {
+      const uint4 x = __ldg(po + c), y = __ldg(pg + c);
+      const uint32_t xw[4] = {x.x, x.y, x.z, x.w}, yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        s0 = fmaf(bf16_lo(xw[e]), bf16_lo(yw[e]), s0);
+        s1 = fmaf(bf16_hi(xw[e]), bf16_hi(yw[e]), s1);
+      }
+    }
+    delta = s0 + s1;
+  }
+  bool ok = mbar_wait(&bars->q, 0, wait_ns, abort);
+  if (ok) {
+    __nv_bfloat16 *gqu = nullptr, *gqv = nullptr;
+    if (i < p.W) {
+      const size_t off = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D + 64 * half;
+      gqu = p.Qu + off;
+      gqv = p.Qv + off;
+    }
+    build_half128(sR, sQu, sQv, a, half, sBias, sBias + D, gqu, gqv);
+  } else {
+    report_timeout(abort, p.status);
+  }
+  fence_proxy_async_smem();
+  ok = __syncthreads_and(ok) != 0;
+
+  constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
+  constexpr uint32_t id192 = idesc_bf16(128, 192, false, false);
+  const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
+  const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
+  const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
+  const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
+  const uint64_t dV = sdesc_sw128(smem_u32(sV), 16, 1024);
+  const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
+
+  // Thread 0: the score MMAs of step t (S, dP, distance window), K = 128 as
+  // two 64-column halves of every operand.
+  auto score_mmas = [&](int t) -> bool {
+    if (!mbar_wait(&bars->in, t & 1, wait_ns, abort)) return false;
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t qa = (kk >> 2) * (kHalfQ >> 4) + (kk & 3) * 2;
+      const uint64_t ka = (kk >> 2) * (kHalfK >> 4) + (kk & 3) * 2;
+      mma_ss(tmem + kColS, dQu + qa, dK + ka, id64, kk > 0);
+      mma_ss(tmem + kColDP, dDO + qa, dV + ka, id64, kk > 0);
+      mma_ss(tmem + kColWin, dQv + qa, dR + (kk >> 2) * (kHalfR >> 4) + (kk & 3) * 2, id192, kk > 0);
+    }
+    tc_commit(&bars->m1);
+    return true;
+  };
+
+  if (tid == 0 && ok) {
+    load_in(0);  // the raw q has been read: the window buffer is free
+    if (!score_mmas(0)) report_timeout(abort, p.status);
+  }
+  const size_t row = (static_cast<size_t>(z) * p.W + i) * p.LP;
+  if (i < p.W) {
+    // GS past the row's last distance M + i: the products read up to 191
+    // columns beyond it (a 128-row tile plus a 64-deep k block), which must
+    // hold zeros.  Key order needs none: every step writes all 64 columns.
+    const int L = p.M + p.W, lo = p.M + i + 1, hi = min(L, lo + 191), mid = min(hi, lo + 96);
+    zero_bf16(p.GS + row, half ? mid : lo, half ? hi : mid);
+  }
+  const int i_warp = w.i0 + quad * 32;  // first query row of this warp
+  for (int t = 0; t < T && ok; ++t) {
+    ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort);
+    if (tid == 0) bulk_wait_group_read0();  // step t-1's G and P stores have read their staging
+    if (!__syncthreads_and(ok)) {
+      ok = false;
+      break;
+    }
+    // Step t's MMAs have read K, V and the window: refill them.
+    if (tid == 0 && t + 1 < T) load_in(t + 1);
+    tc_fence_after();
+    {
+      float g[32], pr[32];
+      const int lim = p.M + i - BN * t;  // key column c of the step visible iff c <= lim
+      step_grads_half(tmem, kColS, kColDP, kColWin, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
+                      [&](int c) { return c <= lim; }, g, pr);
+      stage_row32(sG, a, half, g);
+      stage_row32(sP, a, half, pr);
+      stage_gs(sGS, lane, g);
+    }
+    __syncwarp();
+    // GS: row r of the warp holds distances D0_r - 31 ... D0_r, with
+    // D0_r = M + i_warp + r - 64 t - 32 half; one row per pass, a distance
+    // per lane (64 contiguous bytes per store instruction).
+    {
+      const int d_lane = p.M + i_warp - BN * t - 32 * half - 31 + lane;
+      const int chunk = lane >> 3, sub = (lane & 7) * 2;
+      const int rows = min(32, p.W - i_warp);
+      uint16_t* gs = reinterpret_cast<uint16_t*>(p.GS) + (static_cast<size_t>(z) * p.W + i_warp) * p.LP;
+#pragma unroll 4
+      for (int r = 0; r < rows; ++r) {
+        const int d = d_lane + r;
+        const uint16_t val = *reinterpret_cast<const uint16_t*>(sGS + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4) + sub);
+        if (d >= 0) gs[static_cast<size_t>(r) * p.LP + d] = val;
+      }
+    }
+    fence_proxy_async_smem();  // the G and P staging is read by the TMA stores next
+    tc_fence_before();
+    __syncthreads();  // every thread has read step t's TMEM columns and staged its pairs
+    if (tid == 0) {
+      tma_store_3d(&tm_g, sG, BN * t, w.i0, z);
+      tma_store_3d(&tm_p, sP, BN * t, w.i0, z);
+      bulk_commit_group();
+      if (t + 1 < T) {
+        tc_fence_after();
+        if (!score_mmas(t + 1)) report_timeout(abort, p.status);
+      }
+    }
+  }
+  if (!ok && tid == 0) report_timeout(abort, p.status);
+  // Let this CTA's own copies and MMAs finish before the memory is released.
+  if (tid == 0) {
+    if (n_in > 0) mbar_wait_own(&bars->in, (n_in - 1) & 1, wait_ns);
+    mbar_wait_own(&bars->q, 0, wait_ns);
+    tc_commit(&bars->fin);
+    mbar_wait_own(&bars->fin, 0, wait_ns);
+    bulk_wait_group0();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) tmem_dealloc(tmem, kSTmemCols);
+}
+
+// ---------------------------------------------------------------------------
+// 2. The gradient products
+// ---------------------------------------------------------------------------
+// One persistent CTA per SM, 192 threads: warp 0 loads (TMA), warp 1 issues
+// the MMAs (M = 128, N = D = 128, K = 16, into one of two TMEM accumulators),
+// warps 2-5 move the fp32 accumulator rows to global memory.  A stage holds
+// 64 k of A (a 128 x 64 K-major tile, or two 64 k x 64 row MN-major tiles)
+// and of B (two 64 k x 64 column N-major tiles).
+enum BMode { kModeDQ = 0, kModeDK = 1, kModeDV = 2, kModeDR = 3 };
+constexpr int kGATile = 128 * 128;  // 16 KB
+constexpr int kGBBlock = 64 * 128;  // 8 KB
+constexpr int kGStage = kGATile + 2 * kGBBlock;
+constexpr int kGStages = 6;
+constexpr int kGOffBar = kGStages * kGStage;
+constexpr int kGSmem = kGOffBar + 256 + 1024;
+constexpr int kGThreads = 192;
+constexpr uint32_t kGTmemCols = 2 * D;
+static_assert(kGSmem <= 232448, "shared memory budget");
+
+struct GemmArgs {
+  int B, W, M, H, L;
+  int BH, nmt, nkbW;  // output row blocks of 128; 64-deep blocks of the W queries
+  int tiles;
+  float* out0;  // DQ: the key part of dq; DK: dk; DV: dv; DR: dr
+  float* out1;  // DQ: the distance part of dq
+  unsigned int* status;
+  unsigned long long wait_ns;
+};
+
+struct GTile {
+  int z, part, m0, kb0, nkb;
+};
+
+// Tiles, longest k range first.
+//   DQ: (row block, batch-head, part): rows = queries; part 0 runs k over the
+//       keys [0, M + m0 + 128) (A = G, B = k), part 1 over the distances
+//       (A = GS, B = r); G and GS are zero past each row's last visible key.
+//   DK, DV: (row block, batch-head): rows = segment keys m, k = queries i from
+//       m0 on (key M + m is visible to queries i >= m only).
+//   DR: (row block, head): rows = distances d, k = (batch, query) pairs with
+//       i >= d - M (GS is zero elsewhere).
+template <int MODE>
+__device__ __forceinline__ GTile gtile(const GemmArgs& p, int t) {
+  GTile r;
+  r.part = 0;
+  if (MODE == kModeDQ) {
+    const int per = 2 * p.BH;
+    r.m0 = (p.nmt - 1 - t / per) * 128;
+    const int rem = t % per;
+    r.z = rem >> 1;
+    r.part = rem & 1;
+    r.kb0 = 0;
+    r.nkb = (min(p.L, p.M + r.m0 + 128) + 63) / 64;
+  } else if (MODE == kModeDK || MODE == kModeDV) {
+    r.m0 = (t / p.BH) * 128;
+    r.z = t % p.BH;
+    r.kb0 = r.m0 / 64;
+    r.nkb = p.nkbW - r.kb0;
+  } else {
+    r.m0 = (t / p.H) * 128;
+    r.z = t % p.H;
+    r.kb0 = max(0, r.m0 - p.M) / 64;
+    r.nkb = p.B * (p.nkbW - r.kb0);
+  }
+  return r;
+}
+
+struct GBars {
+  uint64_t full[kGStages], empty[kGStages];
+  uint64_t acc_full[2], acc_empty[2];
+  uint64_t done;
+  uint32_t tmem_base;
+  int abort;
+};
+
+// Tensor maps per mode (all bf16, 128-byte swizzle, zero fill):
+//   DQ: a0 = G {L, W, B*H} box {64, 128, 1}, a1 = GS the same, b0 = k
+//       {D, H, L, B} box {64, 1, 64, 1}, b1 = r {D, H, n_r} box {64, 1, 64};
+//   DK: a0 = G box {64, 64, 1}, b0 = q+u {D, H, W, B} box {64, 1, 64, 1};
+//   DV: a0 = P box {64, 64, 1}, b0 = dout as q+u;
+//   DR: a0 = GS box {64, 64, 1}, b0 = q+v as q+u.
+template <int MODE>
+__global__ void __launch_bounds__(kGThreads, 1)
+    bgemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
+                 const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
+                 const GemmArgs p) {
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
+  uint8_t* smem = smem_raw + pad;
+  GBars* bars = reinterpret_cast<GBars*>(smem + kGOffBar);
+  volatile int* abort = &bars->abort;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int S = kGStages;
+  constexpr bool kAmn = MODE != kModeDQ;  // A read transposed (MN-major)
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&bars->full[s], 1);
+      mbar_init(&bars->empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&bars->acc_full[a], 1);
+      mbar_init(&bars->acc_empty[a], 4);
+    }
+    mbar_init(&bars->done, 1);
+    bars->abort = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&bars->tmem_base, kGTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const uint64_t wait_ns = p.wait_ns;
+
+  if (warp == 0) {
+    // ============================ TMA producer ============================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_a0);
+      tma_prefetch_desc(&tm_b0);
+      if (MODE == kModeDQ) {
+        tma_prefetch_desc(&tm_a1);
+        tma_prefetch_desc(&tm_b1);
+      }
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
+        const GTile g = gtile<MODE>(p, t);
+        const int b = MODE == kModeDR ? 0 : g.z / p.H, h = MODE == kModeDR ? g.z : g.z % p.H;
+        const int nq = p.nkbW - g.kb0;  // DR: k blocks per sequence
+        for (int kk = 0; kk < g.nkb; ++kk, ++it) {
+          const int s = static_cast<int>(it % S);
+          if (!(ok = mbar_wait(&bars->empty[s], ((it / S) & 1) ^ 1, wait_ns, abort))) break;
+          uint8_t* st = smem + s * kGStage;
+          uint8_t* sb = st + kGATile;
+          uint64_t* bar = &bars->full[s];
+          mbar_arrive_expect_tx(bar, kGStage);
+          if (MODE == kModeDQ) {
+            const int k0 = 64 * kk;
+            if (g.part == 0) {
+              tma_load_3d(st, &tm_a0, bar, k0, g.m0, g.z);
+              tma_load_4d(sb, &tm_b0, bar, 0, h, k0, b);
+              tma_load_4d(sb + kGBBlock, &tm_b0, bar, 64, h, k0, b);
+            } else {
+              tma_load_3d(st, &tm_a1, bar, k0, g.m0, g.z);
+              tma_load_3d(sb, &tm_b1, bar, 0, h, k0);
+              tma_load_3d(sb + kGBBlock, &tm_b1, bar, 64, h, k0);
+            }
+          } else {
+            int bb = b, k0 = 64 * (g.kb0 + kk), x0 = g.m0, zz = g.z;
+            if (MODE == kModeDR) {
+              bb = kk / nq;
+              k0 = 64 * (g.kb0 + kk % nq);
+              zz = bb * p.H + h;
+            } else {
+              x0 = p.M + g.m0;  // key columns of G and P
+            }
+            tma_load_3d(st, &tm_a0, bar, x0, k0, zz);
+            tma_load_3d(st + kGATile / 2, &tm_a0, bar, x0 + 64, k0, zz);
+            tma_load_4d(sb, &tm_b0, bar, 0, h, k0, bb);
+            tma_load_4d(sb + kGBBlock, &tm_b0, bar, 64, h, k0, bb);
+          }
+        }
+      }
+      if (!ok) report_timeout(abort, p.status);
+      for (int s = 0; s < S && static_cast<uint32_t>(s) < it; ++s) {
+        const uint32_t last = s + ((it - 1 - s) / S) * S;
+        mbar_wait_own(&bars->full[s], (last / S) & 1, wait_ns);
+      }
+    }
+  } else if (warp == 1) {
+    // ============================ MMA issuer ==============================
+    if (lane == 0) {
+      constexpr uint32_t idesc = idesc_bf16(128, D, kAmn, true);
+      const uint32_t base = smem_u32(smem);
+      uint32_t it = 0, tl = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++tl) {
+        const GTile g = gtile<MODE>(p, t);
+        const uint32_t acc = tl & 1;
+        if (tl >= 2 && !(ok = mbar_wait(&bars->acc_empty[acc], ((tl >> 1) - 1) & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        const uint32_t d = tmem + acc * D;
+        for (int kk = 0; kk < g.nkb; ++kk, ++it) {
+          const int s = static_cast<int>(it % S);
+          if (!(ok = mbar_wait(&bars->full[s], (it / S) & 1, wait_ns, abort))) break;
+          tc_fence_after();
+          const uint32_t st = base + s * kGStage;
+          // K-major A: 8-row groups 1024 bytes apart, 32 bytes per 16 k.
+          // MN-major A and B: 64-wide blocks 8 KB apart, 8-k-row groups 1024
+          // bytes apart, 16 k rows = 2 KB.
+          const uint64_t da = kAmn ? sdesc_sw128(st, kGATile / 2, 1024) : sdesc_sw128(st, 16, 1024);
+          const uint64_t db = sdesc_sw128(st + kGATile, kGBBlock, 1024);
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            mma_ss(d, da + (kAmn ? k * 128 : k * 2), db + k * 128, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+          tc_commit(&bars->empty[s]);
+        }
+        if (!ok) break;
+        tc_commit(&bars->acc_full[acc]);
+      }
+      if (!ok) report_timeout(abort, p.status);
+      tc_commit(&bars->done);
+      mbar_wait_own(&bars->done, 0, wait_ns);
+    }
+  } else {
+    // ============================ epilogue ===============================
+    const int quad = warp & 3;
+    const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
+    const int rows = MODE == kModeDR ? p.L : p.W;
+    uint32_t tl = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tl) {
+      const GTile g = gtile<MODE>(p, t);
+      const uint32_t acc = tl & 1;
+      if (!(ok = warp_wait(&bars->acc_full[acc], (tl >> 1) & 1, wait_ns, abort))) break;
+      tc_fence_after();
+      const int row = g.m0 + 32 * quad + lane;
+      float* dst = nullptr;
+      if (row < rows) {
+        if (MODE == kModeDR) {
+          dst = p.out0 + (static_cast<size_t>(row) * p.H + g.z) * D;
+        } else {
+          const int b = g.z / p.H, h = g.z % p.H;
+          float* out = (MODE == kModeDQ && g.part == 1) ? p.out1 : p.out0;
+          dst = out + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D;
+        }
+      }
+#pragma unroll 1
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t v[32];
+        tmem_ld32(tmem + lane_base + acc * D + 32 * c, v);
+        tmem_wait_ld(v);
+        if (c == D / 32 - 1) {
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+        }
+        if (dst != nullptr) {
+          float4* o4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+        }
+      }
+    }
+    if (!ok) report_timeout(abort, p.status);
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem, kGTmemCols);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// 3. dq and the bias gradients
+// ---------------------------------------------------------------------------
+// dq = dq_c + dq_d over rows of H*D floats; block y sums rows
+// [y * rows_per, (y + 1) * rows_per) of both parts per column, in order, into
+// part [y][h][0 | 1][D] (d(q+u), then d(q+v)).
+__global__ void bwd_sum128_kernel(const float4* __restrict__ dqc, const float4* __restrict__ dqd,
+                                  float4* __restrict__ dq, float* __restrict__ part, long long rows, int cols4,
+                                  int rows_per) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols4) return;
+  const long long r0 = static_cast<long long>(blockIdx.y) * rows_per;
+  const long long r1 = min(rows, r0 + rows_per);
+  float4 su = make_float4(0.f, 0.f, 0.f, 0.f), sv = su;
+  for (long long r = r0; r < r1; ++r) {
+    const size_t o = static_cast<size_t>(r) * cols4 + c;
+    const float4 a = dqc[o], b = dqd[o];
+    dq[o] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
+    su = make_float4(su.x + a.x, su.y + a.y, su.z + a.z, su.w + a.w);
+    sv = make_float4(sv.x + b.x, sv.y + b.y, sv.z + b.z, sv.w + b.w);
+  }
+  const int h = (4 * c) / D, d = (4 * c) % D;
+  float* pp = part + ((static_cast<size_t>(blockIdx.y) * (cols4 * 4 / D) + h) * 2) * D + d;
+  *reinterpret_cast<float4*>(pp) = su;
+  *reinterpret_cast<float4*>(pp + D) = sv;
+}
+
+constexpr int kSumRows = 32;
+
+int num_sms() {
+  static std::atomic<int> cached[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 148;
+  int n = cached[dev].load();
+  if (n == 0) {
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+    cached[dev].store(n);
+  }
+  return n;
+}
+
+size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
+
+struct Scratch128 {
+  __nv_bfloat16 *G, *P, *GS, *Qu, *Qv;
+  float *dqc, *dqd, *part;
+  size_t bytes;
+};
+
+Scratch128 carve(void* base, int B, int W, int M, int H) {
+  const size_t L = static_cast<size_t>(M) + W, LP = (L + 63) / 64 * 64;
+  const size_t bh = static_cast<size_t>(B) * H, bwhd = static_cast<size_t>(B) * W * H * D;
+  const size_t n_part = (static_cast<size_t>(B) * W + kSumRows - 1) / kSumRows;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off += round256(bytes);
+    return static_cast<char*>(base) + at;
+  };
+  Scratch128 s;
+  s.G = reinterpret_cast<__nv_bfloat16*>(take(bh * W * LP * 2));
+  s.P = reinterpret_cast<__nv_bfloat16*>(take(bh * W * LP * 2));
+  s.GS = reinterpret_cast<__nv_bfloat16*>(take(bh * W * LP * 2));
+  s.Qu = reinterpret_cast<__nv_bfloat16*>(take(bwhd * 2));
+  s.Qv = reinterpret_cast<__nv_bfloat16*>(take(bwhd * 2));
+  s.dqc = reinterpret_cast<float*>(take(bwhd * 4));
+  s.dqd = reinterpret_cast<float*>(take(bwhd * 4));
+  s.part = reinterpret_cast<float*>(take(n_part * H * 2 * D * 4));
+  s.bytes = off;
+  return s;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
+                        GemmArgs p, cudaStream_t stream) {
+  static std::atomic<bool> attr_done[64];
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (!attr_done[dev].load()) {
+    if ((e = cudaFuncSetAttribute(bgemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem)) !=
+        cudaSuccess)
+      return e;
+    attr_done[dev].store(true);
+  }
+  if (MODE == kModeDQ) p.tiles = 2 * p.BH * p.nmt;
+  else if (MODE == kModeDR) p.tiles = p.H * p.nmt;
+  else p.tiles = p.BH * p.nmt;
+  const int grid = min(p.tiles, num_sms());
+  bgemm_kernel<MODE><<<grid, kGThreads, kGSmem, stream>>>(a0, a1, b0, b1, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H) { return carve(nullptr, B, W, M, H).bytes; }
+
+bool relattn_bwd_tc128_supported(int W, int M) { return W > 0 && M % 8 == 0; }
+
+cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
+                                     const void* v, const void* r, const float* bias_u, const float* bias_v,
+                                     const float* lse, const void* o, const void* dout, float* dq, float* dk,
+                                     float* dv, float* dr, float* du, float* dvb, int B, int W, int M, int H,
+                                     int n_r, float scale, void* scratch, const WaitCtl& wc, cudaStream_t stream) {
+  if (encode == nullptr || !relattn_bwd_tc128_supported(W, M)) return cudaErrorInvalidValue;
+  const int L = M + W, LP = (L + 63) / 64 * 64, BH = B * H;
+  const Scratch128 sc = carve(scratch, B, W, M, H);
+  const cuuint64_t hd2 = static_cast<cuuint64_t>(H) * D * 2;
+  bool ok = true;
+  auto enc = [&](CUtensorMap* m, const void* base, int rank, std::initializer_list<cuuint64_t> dims,
+                 std::initializer_list<cuuint64_t> strides, std::initializer_list<cuuint32_t> box) {
+    cuuint64_t dd[4];
+    cuuint64_t ss[3];
+    cuuint32_t bb[4];
+    const cuuint32_t estr[4] = {1, 1, 1, 1};
+    int n = 0;
+    for (cuuint64_t x : dims) dd[n++] = x;
+    n = 0;
+    for (cuuint64_t x : strides) ss[n++] = x;
+    n = 0;
+    for (cuuint32_t x : box) bb[n++] = x;
+    ok = ok && encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, rank, const_cast<void*>(base), dd, ss, bb, estr,
+                      CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                      CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  };
+  const cuuint64_t d_ = D, h_ = H, w_ = W, b_ = B, l_ = L;
+  // q, dout, k, v: [B, rows, H, D]; r: [n_r, H, D]; G, P, GS: [B*H][W][LP] (columns past L zero-filled)
+  CUtensorMap tq, tdo128, tk, tv, trw, tr64, tgk, tgsk, tpk, tgmn, tpmn, tgsmn, tqu, tqv, tdo64;
+  enc(&tq, q, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
+  enc(&tdo128, dout, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
+  enc(&tk, k, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
+  enc(&tv, v, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
+  enc(&trw, r, 3, {d_, h_, static_cast<cuuint64_t>(n_r)}, {d_ * 2, hd2}, {64, 1, 192});
+  enc(&tr64, r, 3, {d_, h_, static_cast<cuuint64_t>(n_r)}, {d_ * 2, hd2}, {64, 1, 64});
+  const cuuint64_t lp2 = static_cast<cuuint64_t>(LP) * 2, bh_ = BH;
+  enc(&tgk, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+  enc(&tgsk, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+  enc(&tpk, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+  enc(&tgmn, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+  enc(&tpmn, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+  enc(&tgsmn, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+  enc(&tqu, sc.Qu, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+  enc(&tqv, sc.Qv, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+  enc(&tdo64, dout, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+  if (!ok) return cudaErrorInvalidValue;
+
+  cudaError_t e;
+  // 1. scores -> G, P, GS, q+u, q+v
+  {
+    static std::atomic<bool> attr_done[64];
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!attr_done[dev].load()) {
+      if ((e = cudaFuncSetAttribute(bwd_scores128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSSmem)) !=
+          cudaSuccess)
+        return e;
+      attr_done[dev].store(true);
+    }
+    ScoreParams p;
+    p.bias_u = bias_u;
+    p.bias_v = bias_v;
+    p.lse = lse;
+    p.o = static_cast<const __nv_bfloat16*>(o);
+    p.dout = static_cast<const __nv_bfloat16*>(dout);
+    p.GS = sc.GS;
+    p.Qu = sc.Qu;
+    p.Qv = sc.Qv;
+    p.B = B;
+    p.W = W;
+    p.M = M;
+    p.H = H;
+    p.nqt = (W + BM - 1) / BM;
+    p.LP = LP;
+    p.scale = scale;
+    p.scale_log2e = scale * kLog2e;
+    p.status = wc.status;
+    p.wait_ns = wc.limit_ns;
+    const long long units = static_cast<long long>(p.nqt) * BH;
+    if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+    bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, tk, tv, trw, tdo128, tgk,
+                                                                                 tpk, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  }
+  // 2. the five products
+  GemmArgs g;
+  g.B = B;
+  g.W = W;
+  g.M = M;
+  g.H = H;
+  g.L = L;
+  g.BH = BH;
+  g.nmt = (W + 127) / 128;
+  g.nkbW = (W + 63) / 64;
+  g.tiles = 0;
+  g.status = wc.status;
+  g.wait_ns = wc.limit_ns;
+  g.out0 = sc.dqc;
+  g.out1 = sc.dqd;
+  if ((e = launch_gemm<kModeDQ>(tgk, tgsk, tk, tr64, g, stream)) != cudaSuccess) return e;
+  g.out0 = dk;
+  if ((e = launch_gemm<kModeDK>(tgmn, tgmn, tqu, tqu, g, stream)) != cudaSuccess) return e;
+  g.out0 = dv;
+  if ((e = launch_gemm<kModeDV>(tpmn, tpmn, tdo64, tdo64, g, stream)) != cudaSuccess) return e;
+  g.out0 = dr;
+  g.nmt = (L + 127) / 128;
+  if ((e = launch_gemm<kModeDR>(tgsmn, tgsmn, tqv, tqv, g, stream)) != cudaSuccess) return e;
+  if (n_r > L &&
+      (e = cudaMemsetAsync(dr + static_cast<size_t>(L) * H * D, 0, static_cast<size_t>(n_r - L) * H * D * 4,
+                           stream)) != cudaSuccess)
+    return e;
+  // 3. dq, bias gradients
+  const long long rows = static_cast<long long>(B) * W;
+  const int cols4 = H * D / 4;
+  // at least kSumRows rows per block (the scratch holds that many partials)
+  const long long rows_per = std::max<long long>(kSumRows, (rows + 65534) / 65535);
+  const long long n_part = (rows + rows_per - 1) / rows_per;
+  const dim3 grid((cols4 + 255) / 256, static_cast<unsigned>(n_part));
+  bwd_sum128_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(sc.dqc),
+                                               reinterpret_cast<const float4*>(sc.dqd), reinterpret_cast<float4*>(dq),
+                                               sc.part, rows, cols4, static_cast<int>(rows_per));
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  return launch_bwd_bias(sc.part, static_cast<int>(n_part), H, D, du, dvb, stream);
+}
+
+}  // namespace txl

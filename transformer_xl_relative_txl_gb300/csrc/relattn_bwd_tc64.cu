@@ -180,39 +180,6 @@ constexpr int kQThreads = 256;
 constexpr int kIssuer2 = 128;  // lane 0 of warp 4: the dq kernel's gradient / slot MMAs
 constexpr uint32_t kColDr = 448;  // the finished slot's dr rows (M = 64 layout)
 
-template <typename Vis>
-__device__ __forceinline__ void step_grads_half(uint32_t tmem, int quad, int half, int lane, float lse2,
-                                                float delta, float scale, float scale_log2e, Vis visible,
-                                                float (&g)[32], float (&p)[32]) {
-  const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-  uint32_t bd[16], sx[32], dpv[32];
-  {
-    uint32_t xlo[32], xhi[32];
-    // key columns 0-31 use window positions [32 quad + 32, 32 quad + 96),
-    // columns 32-63 [32 quad, 32 quad + 64)
-    const uint32_t w0 = kColWin + 32 * quad + (half ? 0 : 32);
-    tmem_ld32(lb + w0, xlo);
-    tmem_ld32(lb + w0 + 32, xhi);
-    tmem_ld32(lb + kColS + 32 * half, sx);
-    tmem_ld32(lb + kColDP + 32 * half, dpv);
-    tmem_wait_ld(xlo);
-    tmem_wait_ld(xhi);
-    tmem_wait_ld(sx);
-    tmem_wait_ld(dpv);
-    uint32_t plo[16], phi[16];
-    pack32(xlo, plo);
-    pack32(xhi, phi);
-    window_shift_packed(plo, phi, lane, bd);
-  }
-  add_window(sx, bd, p);
-#pragma unroll
-  for (int c = 0; c < 32; ++c) {
-    const float e = visible(32 * half + c) ? ex2(fmaf(p[c], scale_log2e, -lse2)) : 0.f;
-    p[c] = e;
-    g[c] = scale * e * (__uint_as_float(dpv[c]) - delta);
-  }
-}
-
 // Columns [32 half, 32 half + 32) of row a of a 128B-swizzled [128 x 64] bf16 tile.
 __device__ __forceinline__ void store_row_half(uint8_t* tile, int a, int half, const float (&x)[32]) {
   uint8_t* row = tile + (a >> 3) * 1024 + (a & 7) * 128;
@@ -431,7 +398,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     {
       float g[32], pr[32];
       const int lim = p.M + i - BN * t;  // key column c visible iff c <= lim
-      step_grads_half(tmem, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
+      step_grads_half(tmem, kColS, kColDP, kColWin, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
                       [&](int c) { return c <= lim; }, g, pr);
       store_row_half(sG, a, half, g);
       // Skewed copy: key column c of step t sits at window position
@@ -776,7 +743,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
       float gr[32], pr[32];
       // key jj0 + c is visible to row i iff jj0 + c <= i and it exists
       const int lim = min(i - w.jj0, p.W - 1 - w.jj0);
-      step_grads_half(tmem, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
+      step_grads_half(tmem, kColS, kColDP, kColWin, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
                       [&](int c) { return c <= lim; }, gr, pr);
       store_row_half(sP, a, half, pr);
       store_row_half(sG, a, half, gr);

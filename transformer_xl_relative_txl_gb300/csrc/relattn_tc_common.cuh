@@ -148,6 +148,47 @@ __device__ __forceinline__ void add_window(const uint32_t (&sraw)[32], const uin
   }
 }
 
+// The backward's per-pair terms for 32 key columns of one query row (lane
+// `lane` of lane quadrant `quad`; columns [32 half, 32 half + 32) of a 64-key
+// step).  TMEM holds the step's unscaled content scores at column colS, the
+// dout . v_j products at colDP and the 192-distance window (q+v) . r_d at
+// colWin.  The window is shifted into key order as in the forward, then
+//   p = 2^(s scale log2(e) - lse2)   (lse2: the row's lse in log2 units)
+//   g = scale p (dout . v_j - delta)
+// where visible(c) is false for masked columns c (p = g = 0 there).
+template <typename Vis>
+__device__ __forceinline__ void step_grads_half(uint32_t tmem, uint32_t colS, uint32_t colDP, uint32_t colWin,
+                                                int quad, int half, int lane, float lse2, float delta, float scale,
+                                                float scale_log2e, Vis visible, float (&g)[32], float (&p)[32]) {
+  const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+  uint32_t bd[16], sx[32], dpv[32];
+  {
+    uint32_t xlo[32], xhi[32];
+    // key columns 0-31 use window positions [32 quad + 32, 32 quad + 96),
+    // columns 32-63 [32 quad, 32 quad + 64)
+    const uint32_t w0 = colWin + 32 * quad + (half ? 0 : 32);
+    tmem_ld32(lb + w0, xlo);
+    tmem_ld32(lb + w0 + 32, xhi);
+    tmem_ld32(lb + colS + 32 * half, sx);
+    tmem_ld32(lb + colDP + 32 * half, dpv);
+    tmem_wait_ld(xlo);
+    tmem_wait_ld(xhi);
+    tmem_wait_ld(sx);
+    tmem_wait_ld(dpv);
+    uint32_t plo[16], phi[16];
+    pack32(xlo, plo);
+    pack32(xhi, phi);
+    window_shift_packed(plo, phi, lane, bd);
+  }
+  add_window(sx, bd, p);
+#pragma unroll
+  for (int c = 0; c < 32; ++c) {
+    const float e = visible(32 * half + c) ? ex2(fmaf(p[c], scale_log2e, -lse2)) : 0.f;
+    p[c] = e;
+    g[c] = scale * e * (__uint_as_float(dpv[c]) - delta);
+  }
+}
+
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t ns, volatile int* abort) {
   const bool got = mbar_wait(bar, parity, ns, abort);
   return __all_sync(0xffffffffu, got);

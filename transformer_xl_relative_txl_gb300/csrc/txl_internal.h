@@ -4,6 +4,7 @@
 
 #include <cstdint>
 #include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -136,6 +137,21 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
                                     float* dq, float* dk, float* dv, float* dr, float* du, float* dvb, int B,
                                     int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
                                     cudaStream_t stream);
+
+// Backward on the tensor cores, bf16 inputs, o and dout, D = 128
+// (relattn_bwd_tc128.cu): the pair terms are materialised in bf16 scratch and
+// the five gradient products run as tensor-core GEMMs.  Needs M % 8 == 0 (the
+// key columns of the pair terms are read from column M on by 16-byte aligned
+// tensor copies).  Encodes its own tensor maps with `encode`.  Every output is
+// written in full (dr rows >= M + W are zeroed).
+// scratch: relattn_bwd_tc128_scratch_bytes(B, W, M, H) bytes.
+size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H);
+bool relattn_bwd_tc128_supported(int W, int M);
+cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
+                                     const void* v, const void* r, const float* bias_u, const float* bias_v,
+                                     const float* lse, const void* o, const void* dout, float* dq, float* dk,
+                                     float* dv, float* dr, float* du, float* dvb, int B, int W, int M, int H,
+                                     int n_r, float scale, void* scratch, const WaitCtl& wc, cudaStream_t stream);
 
 // The layer's dense products on the tensor cores (gemm_tc.cu): row-major
 // bf16 C_z [m, n] = A [m, k] B_z [k, n] (+ bias [n], fp32) (then ReLU),
