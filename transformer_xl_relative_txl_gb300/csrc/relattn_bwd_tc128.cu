@@ -53,30 +53,33 @@ constexpr float kLog2e = 1.4426950408889634f;
 // 1. Score rebuild
 // ---------------------------------------------------------------------------
 // Shared memory: every D = 128 operand tile is two 64-column halves (128-byte
-// rows, 128-byte swizzle), the second half right after the first.  K, V and
-// the distance window are single tiles, refilled for step t + 1 as soon as
-// the MMAs of step t have read them (the MMAs of step t + 1 wait for the
-// pairs of step t anyway).  G and P of a step leave through 128 x 64 staging
-// tiles and TMA stores; GS through one 32 x 32 staging tile per warp and
-// row-contiguous stores.
+// rows, 128-byte swizzle), the second half right after the first.  Inputs of
+// a step (64 keys, 64 values, 64 new distance rows) in two stages.  G and P
+// of a step leave through 128 x 64 staging tiles and TMA stores, GS (the same
+// g in distance order) through row-contiguous stores read from the G tile.
+//
+// TMEM: S and dP of a step in two buffers (columns 0-127, 128-255), and the
+// 192-distance window as three of four 64-column slots (256-511).  The window
+// of step t + 1 is the window of step t moved by 64 distances, so a step
+// computes only its 64 new distances, into the slot the step before it no
+// longer reads; the MMAs of step t + 1 then run while step t's pairs are
+// computed.
 constexpr int kHalfQ = BM * 128;   // 128 rows x 64 bf16: 16 KB
 constexpr int kHalfK = BN * 128;   // 64 rows: 8 KB
-constexpr int kHalfR = 192 * 128;  // 192 distance rows: 24 KB
 constexpr int kSOffQu = 0;
 constexpr int kSOffQv = kSOffQu + 2 * kHalfQ;
 constexpr int kSOffDO = kSOffQv + 2 * kHalfQ;
-constexpr int kSOffK = kSOffDO + 2 * kHalfQ;
-constexpr int kSOffV = kSOffK + 2 * kHalfK;
-constexpr int kSOffR = kSOffV + 2 * kHalfK;     // the window (the raw q tile before the first)
-constexpr int kSOffG = kSOffR + 2 * kHalfR;     // G staging: 128 rows x 64 keys
+constexpr int kSOffIn = kSOffDO + 2 * kHalfQ;   // stage s: K, V, R tiles (16 KB each)
+constexpr int kInStage = 6 * kHalfK;
+constexpr int kSOffG = kSOffIn + 2 * kInStage;  // G staging: 128 rows x 64 keys
 constexpr int kSOffP = kSOffG + BM * BN * 2;    // P staging
-constexpr int kSOffGS = kSOffP + BM * BN * 2;   // GS staging: 8 warps x 32 rows x 32 values
-constexpr int kSOffBar = kSOffGS + 8 * 32 * 64;
+constexpr int kSOffBar = kSOffP + BM * BN * 2;
 constexpr int kSOffBias = kSOffBar + 256;       // u, then v of the head (fp32)
 constexpr int kSSmem = kSOffBias + 2 * D * 4 + 1024;
 static_assert(kSSmem <= 232448, "shared memory budget");
-constexpr uint32_t kColS = 0, kColDP = 64, kColWin = 128, kSTmemCols = 512;
-constexpr int kSThreads = 256;
+constexpr uint32_t kColWin = 256, kSTmemCols = 512;
+constexpr int kPairThreads = 256;            // warps 0-7
+constexpr int kSThreads = kPairThreads + 32;  // + the issuer warp
 
 struct ScoreParams {
   const float* bias_u;
@@ -94,7 +97,7 @@ struct ScoreParams {
 };
 
 struct SBars {
-  uint64_t q, in, m1, fin;
+  uint64_t q, in[2], x, m1[2], done, sfree, fin;
   uint32_t tmem_base;
   int abort;
 };
@@ -149,25 +152,6 @@ __device__ __forceinline__ void stage_row32(uint8_t* tile, int a, int half, cons
                    pack_bf16x2(x[8 * c + 4], x[8 * c + 5]), pack_bf16x2(x[8 * c + 6], x[8 * c + 7]));
 }
 
-// A warp's 32 x 32 GS staging tile: row `lane` holds the lane's 32 values in
-// increasing distance order (value k at distance D0 - 31 + k, i.e. g[31 - k]),
-// 64 bytes per row with the 16-byte chunks rotated by (row / 2) % 4 so that
-// the writes spread over every bank.
-__device__ __forceinline__ void stage_gs(uint8_t* st, int lane, const float (&g)[32]) {
-  uint8_t* rowp = st + lane * 64;
-  const int rot = (lane >> 1) & 3;
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint32_t w[4];
-#pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      const int k = 8 * c + 2 * e;  // positions k, k + 1
-      w[e] = pack_bf16x2(g[31 - k], g[30 - k]);
-    }
-    *reinterpret_cast<uint4*>(rowp + ((c ^ rot) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-}
-
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
   asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
                    reinterpret_cast<uint64_t>(map)),
@@ -175,13 +159,13 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
                : "memory");
 }
 
-// 8 warps, two per TMEM lane quadrant (key columns 0-31 and 32-63 of the same
-// rows).  Thread 0 issues the loads, the score MMAs and the G / P stores;
-// everyone waits on the MMA barrier, computes its 32 pairs and writes them
-// out.
+// Warps 0-7 compute the pairs, two per TMEM lane quadrant (key columns 0-31
+// and 32-63 of the same rows); lane 0 of warp 8 issues the loads, the MMAs
+// (two steps ahead of the loads' consumers, one ahead of the pairs) and the
+// G / P stores, so no load latency stalls the pair warps.
 __global__ void __launch_bounds__(kSThreads, 1)
     bwd_scores128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
+                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                          const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_g,
                          const __grid_constant__ CUtensorMap tm_p, const ScoreParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -190,9 +174,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   uint8_t* sQu = smem + kSOffQu;
   uint8_t* sQv = smem + kSOffQv;
   uint8_t* sDO = smem + kSOffDO;
-  uint8_t* sK = smem + kSOffK;
-  uint8_t* sV = smem + kSOffV;
-  uint8_t* sR = smem + kSOffR;
+  uint8_t* sIn = smem + kSOffIn;
   uint8_t* sG = smem + kSOffG;
   uint8_t* sP = smem + kSOffP;
   SBars* bars = reinterpret_cast<SBars*>(smem + kSOffBar);
@@ -201,18 +183,24 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
   const int a = quad * 32 + lane;  // this thread's row of the tile
-  uint8_t* sGS = smem + kSOffGS + warp * 32 * 64;
   const uint64_t wait_ns = p.wait_ns;
 
   const Unit w = decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt);
   const int T = w.nks;
   const int i = w.i0 + a;  // query row
   const int z = w.b * p.H + w.h;
+  // first distance of the window of step t: M + i0 - 64 t - 64
+  auto wbase = [&](int t) { return p.M + w.i0 - BN * t - BN; };
 
   if (tid == 0) {
     mbar_init(&bars->q, 1);
-    mbar_init(&bars->in, 1);
-    mbar_init(&bars->m1, 1);
+    mbar_init(&bars->in[0], 1);
+    mbar_init(&bars->in[1], 1);
+    mbar_init(&bars->x, 1);
+    mbar_init(&bars->m1[0], 1);
+    mbar_init(&bars->m1[1], 1);
+    mbar_init(&bars->done, 1);
+    mbar_init(&bars->sfree, 1);
     mbar_init(&bars->fin, 1);
     bars->abort = 0;
     fence_mbar_init();
@@ -227,40 +215,54 @@ __global__ void __launch_bounds__(kSThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // Inputs of step t: keys and values [64 t, 64 t + 64) and the window of
-  // distance rows [wb, wb + 192), wb = M + i0 - 64 t - 64.
-  uint32_t n_in = 0;  // loads issued (thread 0)
+  // 64 distance rows from `d0` (both head-dim halves) into a 16 KB tile.
+  auto load_r64 = [&](uint8_t* dst, uint64_t* bar, int d0) {
+    tma_load_3d(dst, &tm_r, bar, 0, w.h, d0);
+    tma_load_3d(dst + kHalfK, &tm_r, bar, 64, w.h, d0);
+  };
+  // Inputs of step t into stage t & 1: keys and values [64 t, 64 t + 64) and
+  // the window's new distances [wb(t), wb(t) + 64).
+  uint32_t n_in[2] = {0, 0};  // loads issued per stage (the issuer)
   auto load_in = [&](int t) {
-    const int wb = p.M + w.i0 - BN * t - BN;
-    mbar_arrive_expect_tx(&bars->in, 4 * kHalfK + 2 * kHalfR);
+    const int s = t & 1;
+    uint8_t* st = sIn + s * kInStage;
+    mbar_arrive_expect_tx(&bars->in[s], kInStage);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      tma_load_4d(sK + hh * kHalfK, &tm_k, &bars->in, 64 * hh, w.h, BN * t, w.b);
-      tma_load_4d(sV + hh * kHalfK, &tm_v, &bars->in, 64 * hh, w.h, BN * t, w.b);
-      tma_load_3d(sR + hh * kHalfR, &tm_rw, &bars->in, 64 * hh, w.h, wb);
+      tma_load_4d(st + hh * kHalfK, &tm_k, &bars->in[s], 64 * hh, w.h, BN * t, w.b);
+      tma_load_4d(st + 2 * kHalfK + hh * kHalfK, &tm_v, &bars->in[s], 64 * hh, w.h, BN * t, w.b);
     }
-    ++n_in;
+    load_r64(st + 4 * kHalfK, &bars->in[s], wbase(t));
+    if (s == 0) ++n_in[0];
+    else ++n_in[1];
   };
-  if (tid == 0) {
+  const bool issuer = tid == kPairThreads;
+  if (issuer) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_rw);
+    tma_prefetch_desc(&tm_r);
     tma_prefetch_desc(&tm_do);
     tma_prefetch_desc(&tm_g);
     tma_prefetch_desc(&tm_p);
-    // the raw q tile goes to the window buffer until (q+u), (q+v) are built
+    // the raw q tile goes to stage 1 until (q+u), (q+v) are built
     mbar_arrive_expect_tx(&bars->q, 4 * kHalfQ);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      tma_load_4d(sR + hh * kHalfQ, &tm_q, &bars->q, 64 * hh, w.h, w.i0, w.b);
+      tma_load_4d(sIn + kInStage + hh * kHalfQ, &tm_q, &bars->q, 64 * hh, w.h, w.i0, w.b);
       tma_load_4d(sDO + hh * kHalfQ, &tm_do, &bars->q, 64 * hh, w.h, w.i0, w.b);
     }
+    load_in(0);
+    // the rest of step 0's window (distances wb(0) + 64 ... + 192) into the
+    // staging tiles, which are free until step 0's pairs are written
+    mbar_arrive_expect_tx(&bars->x, 2 * 2 * kHalfK);
+    load_r64(sG, &bars->x, wbase(0) + 64);
+    load_r64(sP, &bars->x, wbase(0) + 128);
   }
 
   // Per-row constants: lse (log2 domain) and Delta = dout . o.
   float lse2 = INFINITY, delta = 0.f;  // rows past W: every p is 0
-  if (i < p.W) {
+  if (tid < kPairThreads && i < p.W) {
     const long long row_id = (static_cast<long long>(w.b) * p.H + w.h) * p.W + i;
     lse2 = p.lse[row_id] * kLog2e;
     const long long off = ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D;
@@ -279,120 +281,171 @@ __global__ void __launch_bounds__(kSThreads, 1)
     }
     delta = s0 + s1;
   }
-  bool ok = mbar_wait(&bars->q, 0, wait_ns, abort);
-  if (ok) {
-    __nv_bfloat16 *gqu = nullptr, *gqv = nullptr;
-    if (i < p.W) {
-      const size_t off = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D + 64 * half;
-      gqu = p.Qu + off;
-      gqv = p.Qv + off;
+  bool ok = true;
+  if (tid < kPairThreads) {
+    // (q+u) and (q+v) from the raw q tile; rows past W are not written out
+    ok = mbar_wait(&bars->q, 0, wait_ns, abort);
+    if (ok) {
+      __nv_bfloat16 *gqu = nullptr, *gqv = nullptr;
+      if (i < p.W) {
+        const size_t off = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D + 64 * half;
+        gqu = p.Qu + off;
+        gqv = p.Qv + off;
+      }
+      build_half128(sIn + kInStage, sQu, sQv, a, half, sBias, sBias + D, gqu, gqv);
+    } else {
+      report_timeout(abort, p.status);
     }
-    build_half128(sR, sQu, sQv, a, half, sBias, sBias + D, gqu, gqv);
-  } else {
-    report_timeout(abort, p.status);
+    fence_proxy_async_smem();
   }
-  fence_proxy_async_smem();
   ok = __syncthreads_and(ok) != 0;
 
   constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
-  constexpr uint32_t id192 = idesc_bf16(128, 192, false, false);
   const uint64_t dQu = sdesc_sw128(smem_u32(sQu), 16, 1024);
   const uint64_t dQv = sdesc_sw128(smem_u32(sQv), 16, 1024);
   const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
-  const uint64_t dK = sdesc_sw128(smem_u32(sK), 16, 1024);
-  const uint64_t dV = sdesc_sw128(smem_u32(sV), 16, 1024);
-  const uint64_t dR = sdesc_sw128(smem_u32(sR), 16, 1024);
-
-  // Thread 0: the score MMAs of step t (S, dP, distance window), K = 128 as
-  // two 64-column halves of every operand.
+  // TMEM column of window position `pos` (a multiple of 32) at step t
+  auto win_col = [&](int pos, int t) -> uint32_t {
+    return kColWin + 64 * (((pos >> 6) - t) & 3) + (pos & 63);
+  };
+  // (q+v) against a 64-row distance tile, into the window slot of block k at step t
+  auto win_mma = [&](const uint8_t* rtile, int k, int t) {
+    const uint64_t dR = sdesc_sw128(smem_u32(rtile), 16, 1024);
+    const uint32_t col = win_col(64 * k, t);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+      const uint64_t off = (kk >> 2) * (kHalfQ >> 4) + (kk & 3) * 2;
+      mma_ss(tmem + col, dQv + off, dR + (kk >> 2) * (kHalfK >> 4) + (kk & 3) * 2, id64, kk > 0);
+    }
+  };
+  // Thread 0: the MMAs of step t (K = 128 as two 64-column halves of every
+  // operand): S and dP into buffer t & 1, the window's new distances.
   auto score_mmas = [&](int t) -> bool {
-    if (!mbar_wait(&bars->in, t & 1, wait_ns, abort)) return false;
+    const int s = t & 1;
+    if (!mbar_wait(&bars->in[s], (t >> 1) & 1, wait_ns, abort)) return false;
+    if (t == 0 && !mbar_wait(&bars->x, 0, wait_ns, abort)) return false;
     tc_fence_after();
+    const uint8_t* st = sIn + s * kInStage;
+    const uint64_t dK = sdesc_sw128(smem_u32(st), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(st + 2 * kHalfK), 16, 1024);
+    const uint32_t colS = 128 * s, colDP = 128 * s + 64;
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) {
       const uint64_t qa = (kk >> 2) * (kHalfQ >> 4) + (kk & 3) * 2;
       const uint64_t ka = (kk >> 2) * (kHalfK >> 4) + (kk & 3) * 2;
-      mma_ss(tmem + kColS, dQu + qa, dK + ka, id64, kk > 0);
-      mma_ss(tmem + kColDP, dDO + qa, dV + ka, id64, kk > 0);
-      mma_ss(tmem + kColWin, dQv + qa, dR + (kk >> 2) * (kHalfR >> 4) + (kk & 3) * 2, id192, kk > 0);
+      mma_ss(tmem + colS, dQu + qa, dK + ka, id64, kk > 0);
+      mma_ss(tmem + colDP, dDO + qa, dV + ka, id64, kk > 0);
     }
-    tc_commit(&bars->m1);
+    win_mma(st + 4 * kHalfK, 0, t);
+    if (t == 0) {
+      win_mma(sG, 1, 0);
+      win_mma(sP, 2, 0);
+    }
+    tc_commit(&bars->m1[s]);
     return true;
   };
 
-  if (tid == 0 && ok) {
-    load_in(0);  // the raw q has been read: the window buffer is free
-    if (!score_mmas(0)) report_timeout(abort, p.status);
-  }
-  const size_t row = (static_cast<size_t>(z) * p.W + i) * p.LP;
-  if (i < p.W) {
-    // GS past the row's last distance M + i: the products read up to 191
-    // columns beyond it (a 128-row tile plus a 64-deep k block), which must
-    // hold zeros.  Key order needs none: every step writes all 64 columns.
-    const int L = p.M + p.W, lo = p.M + i + 1, hi = min(L, lo + 191), mid = min(hi, lo + 96);
-    zero_bf16(p.GS + row, half ? mid : lo, half ? hi : mid);
-  }
-  const int i_warp = w.i0 + quad * 32;  // first query row of this warp
-  for (int t = 0; t < T && ok; ++t) {
-    ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort);
-    if (tid == 0) bulk_wait_group_read0();  // step t-1's G and P stores have read their staging
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
+  if (issuer) {
+    // ============================ issuer ==================================
+    if (ok) {
+      if (T > 1) load_in(1);  // the raw q has been read: stage 1 is free
+      ok = score_mmas(0) && (T < 2 || score_mmas(1));
     }
-    // Step t's MMAs have read K, V and the window: refill them.
-    if (tid == 0 && t + 1 < T) load_in(t + 1);
-    tc_fence_after();
-    {
-      float g[32], pr[32];
-      const int lim = p.M + i - BN * t;  // key column c of the step visible iff c <= lim
-      step_grads_half(tmem, kColS, kColDP, kColWin, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
-                      [&](int c) { return c <= lim; }, g, pr);
-      stage_row32(sG, a, half, g);
-      stage_row32(sP, a, half, pr);
-      stage_gs(sGS, lane, g);
-    }
-    __syncwarp();
-    // GS: row r of the warp holds distances D0_r - 31 ... D0_r, with
-    // D0_r = M + i_warp + r - 64 t - 32 half; one row per pass, a distance
-    // per lane (64 contiguous bytes per store instruction).
-    {
-      const int d_lane = p.M + i_warp - BN * t - 32 * half - 31 + lane;
-      const int chunk = lane >> 3, sub = (lane & 7) * 2;
-      const int rows = min(32, p.W - i_warp);
-      uint16_t* gs = reinterpret_cast<uint16_t*>(p.GS) + (static_cast<size_t>(z) * p.W + i_warp) * p.LP;
-#pragma unroll 4
-      for (int r = 0; r < rows; ++r) {
-        const int d = d_lane + r;
-        const uint16_t val = *reinterpret_cast<const uint16_t*>(sGS + r * 64 + ((chunk ^ ((r >> 1) & 3)) << 4) + sub);
-        if (d >= 0) gs[static_cast<size_t>(r) * p.LP + d] = val;
-      }
-    }
-    fence_proxy_async_smem();  // the G and P staging is read by the TMA stores next
-    tc_fence_before();
-    __syncthreads();  // every thread has read step t's TMEM columns and staged its pairs
-    if (tid == 0) {
+    for (int t = 0; t < T && ok; ++t) {
+      const int s = t & 1;
+      // step t's MMAs have read stage s: refill it for step t + 2
+      if (!(ok = mbar_wait(&bars->m1[s], (t >> 1) & 1, wait_ns, abort))) break;
+      if (t + 2 < T) load_in(t + 2);
+      // step t's pairs are staged and its TMEM columns read
+      if (!(ok = mbar_wait(&bars->done, t & 1, wait_ns, abort))) break;
       tma_store_3d(&tm_g, sG, BN * t, w.i0, z);
       tma_store_3d(&tm_p, sP, BN * t, w.i0, z);
       bulk_commit_group();
-      if (t + 1 < T) {
+      if (t + 2 < T) {
         tc_fence_after();
-        if (!score_mmas(t + 1)) report_timeout(abort, p.status);
+        if (!(ok = score_mmas(t + 2))) break;
       }
+      bulk_wait_group_read0();
+      mbar_arrive(&bars->sfree);
     }
-  }
-  if (!ok && tid == 0) report_timeout(abort, p.status);
-  // Let this CTA's own copies and MMAs finish before the memory is released.
-  if (tid == 0) {
-    if (n_in > 0) mbar_wait_own(&bars->in, (n_in - 1) & 1, wait_ns);
+    if (!ok) report_timeout(abort, p.status);
+    // Let this CTA's own copies and MMAs finish before the memory is released.
+    if (n_in[0] > 0) mbar_wait_own(&bars->in[0], (n_in[0] - 1) & 1, wait_ns);
+    if (n_in[1] > 0) mbar_wait_own(&bars->in[1], (n_in[1] - 1) & 1, wait_ns);
+    mbar_wait_own(&bars->x, 0, wait_ns);
     mbar_wait_own(&bars->q, 0, wait_ns);
     tc_commit(&bars->fin);
     mbar_wait_own(&bars->fin, 0, wait_ns);
     bulk_wait_group0();
+  } else if (tid < kPairThreads) {
+    // ============================ pairs ===================================
+    const size_t row = (static_cast<size_t>(z) * p.W + i) * p.LP;
+    if (i < p.W) {
+      // GS past the row's last distance M + i: the products read up to 191
+      // columns beyond it (a 128-row tile plus a 64-deep k block), which must
+      // hold zeros.  Key order needs none: every step writes all 64 columns.
+      const int L = p.M + p.W, lo = p.M + i + 1, hi = min(L, lo + 191), mid = min(hi, lo + 96);
+      zero_bf16(p.GS + row, half ? mid : lo, half ? hi : mid);
+    }
+    const int i_warp = w.i0 + quad * 32;  // first query row of this warp
+    for (int t = 0; t < T && ok; ++t) {
+      const int s = t & 1;
+      if (!named_bar_and(1, kPairThreads, mbar_wait(&bars->m1[s], (t >> 1) & 1, wait_ns, abort))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float g[32], pr[32];
+      const int lim = p.M + i - BN * t;  // key column c of the step visible iff c <= lim
+      const int w0 = 32 * quad + (half ? 0 : 32);
+      const uint32_t cw0 = win_col(w0, t), cw1 = win_col(w0 + 32, t);
+      if (__all_sync(0xffffffffu, lim >= 32 * half + 31)) {  // no masked column in the warp's 32
+        step_grads_half_at(tmem, 128 * s, 128 * s + 64, cw0, cw1, quad, half, lane, lse2, delta, p.scale,
+                           p.scale_log2e, [](int) { return true; }, g, pr);
+      } else {
+        step_grads_half_at(tmem, 128 * s, 128 * s + 64, cw0, cw1, quad, half, lane, lse2, delta, p.scale,
+                           p.scale_log2e, [&](int c) { return c <= lim; }, g, pr);
+      }
+      // step t-1's G and P stores have read the staging tiles
+      if (t > 0 && !mbar_wait(&bars->sfree, (t - 1) & 1, wait_ns, abort)) report_timeout(abort, p.status);
+      stage_row32(sG, a, half, g);
+      stage_row32(sP, a, half, pr);
+      __syncwarp();
+      // GS: row r of the warp holds distances D0_r - 31 ... D0_r, with
+      // D0_r = M + i_warp + r - 64 t - 32 half, i.e. keys 32 half + 31 ... 32 half
+      // of the staged G row; one row per pass, a distance per lane (64
+      // contiguous bytes per store instruction).
+      {
+        const int d_lane = p.M + i_warp - BN * t - 32 * half - 31 + lane;
+        const int key = 32 * half + 31 - lane;  // staged column this lane reads
+        const int chunk = key >> 3;
+        // rows [r_lo, r_hi) of the warp exist and have d >= 0 for this lane
+        const int r_lo = max(0, -d_lane), r_hi = min(32, p.W - i_warp);
+        uint16_t* gs = reinterpret_cast<uint16_t*>(p.GS) + (static_cast<size_t>(z) * p.W + i_warp) * p.LP + d_lane;
+        const uint8_t* src = sG + quad * 32 * 128 + (key & 7) * 2;
+        // the lane's column in each swizzle phase k = row & 7
+        uint32_t col[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) col[k] = static_cast<uint32_t>((chunk ^ k) << 4);
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          const uint16_t val = *reinterpret_cast<const uint16_t*>(src + (r >> 3) * 1024 + (r & 7) * 128 + col[r & 7]);
+          if (r >= r_lo && r < r_hi) gs[static_cast<size_t>(r) * (p.LP + 1)] = val;
+        }
+      }
+      fence_proxy_async_smem();  // the G and P staging is read by the TMA stores next
+      tc_fence_before();
+      named_bar_sync(1, kPairThreads);  // every pair thread has read step t's TMEM columns and staged its pairs
+      if (tid == 0) mbar_arrive(&bars->done);
+    }
+    if (!ok && tid == 0) report_timeout(abort, p.status);
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) tmem_dealloc(tmem, kSTmemCols);
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kSTmemCols);
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -785,12 +838,11 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
   };
   const cuuint64_t d_ = D, h_ = H, w_ = W, b_ = B, l_ = L;
   // q, dout, k, v: [B, rows, H, D]; r: [n_r, H, D]; G, P, GS: [B*H][W][LP] (columns past L zero-filled)
-  CUtensorMap tq, tdo128, tk, tv, trw, tr64, tgk, tgsk, tpk, tgmn, tpmn, tgsmn, tqu, tqv, tdo64;
+  CUtensorMap tq, tdo128, tk, tv, tr64, tgk, tgsk, tpk, tgmn, tpmn, tgsmn, tqu, tqv, tdo64;
   enc(&tq, q, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
   enc(&tdo128, dout, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
   enc(&tk, k, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
   enc(&tv, v, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
-  enc(&trw, r, 3, {d_, h_, static_cast<cuuint64_t>(n_r)}, {d_ * 2, hd2}, {64, 1, 192});
   enc(&tr64, r, 3, {d_, h_, static_cast<cuuint64_t>(n_r)}, {d_ * 2, hd2}, {64, 1, 64});
   const cuuint64_t lp2 = static_cast<cuuint64_t>(LP) * 2, bh_ = BH;
   enc(&tgk, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
@@ -838,7 +890,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     p.wait_ns = wc.limit_ns;
     const long long units = static_cast<long long>(p.nqt) * BH;
     if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, tk, tv, trw, tdo128, tgk,
+    bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, tk, tv, tr64, tdo128, tgk,
                                                                                  tpk, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

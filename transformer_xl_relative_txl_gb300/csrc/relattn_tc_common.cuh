@@ -156,19 +156,21 @@ __device__ __forceinline__ void add_window(const uint32_t (&sraw)[32], const uin
 //   p = 2^(s scale log2(e) - lse2)   (lse2: the row's lse in log2 units)
 //   g = scale p (dout . v_j - delta)
 // where visible(c) is false for masked columns c (p = g = 0 there).
+//
+// step_grads_half_at takes the TMEM columns of the two 32-column window
+// chunks (positions w0 and w0 + 32, w0 = 32 quad + (half ? 0 : 32)) as
+// arguments, for windows that are not contiguous in TMEM.
 template <typename Vis>
-__device__ __forceinline__ void step_grads_half(uint32_t tmem, uint32_t colS, uint32_t colDP, uint32_t colWin,
-                                                int quad, int half, int lane, float lse2, float delta, float scale,
-                                                float scale_log2e, Vis visible, float (&g)[32], float (&p)[32]) {
+__device__ __forceinline__ void step_grads_half_at(uint32_t tmem, uint32_t colS, uint32_t colDP, uint32_t colW0,
+                                                   uint32_t colW1, int quad, int half, int lane, float lse2,
+                                                   float delta, float scale, float scale_log2e, Vis visible,
+                                                   float (&g)[32], float (&p)[32]) {
   const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
   uint32_t bd[16], sx[32], dpv[32];
   {
     uint32_t xlo[32], xhi[32];
-    // key columns 0-31 use window positions [32 quad + 32, 32 quad + 96),
-    // columns 32-63 [32 quad, 32 quad + 64)
-    const uint32_t w0 = colWin + 32 * quad + (half ? 0 : 32);
-    tmem_ld32(lb + w0, xlo);
-    tmem_ld32(lb + w0 + 32, xhi);
+    tmem_ld32(lb + colW0, xlo);
+    tmem_ld32(lb + colW1, xhi);
     tmem_ld32(lb + colS + 32 * half, sx);
     tmem_ld32(lb + colDP + 32 * half, dpv);
     tmem_wait_ld(xlo);
@@ -187,6 +189,17 @@ __device__ __forceinline__ void step_grads_half(uint32_t tmem, uint32_t colS, ui
     p[c] = e;
     g[c] = scale * e * (__uint_as_float(dpv[c]) - delta);
   }
+}
+
+template <typename Vis>
+__device__ __forceinline__ void step_grads_half(uint32_t tmem, uint32_t colS, uint32_t colDP, uint32_t colWin,
+                                                int quad, int half, int lane, float lse2, float delta, float scale,
+                                                float scale_log2e, Vis visible, float (&g)[32], float (&p)[32]) {
+  // key columns 0-31 use window positions [32 quad + 32, 32 quad + 96),
+  // columns 32-63 [32 quad, 32 quad + 64)
+  const uint32_t w0 = colWin + 32 * quad + (half ? 0 : 32);
+  step_grads_half_at(tmem, colS, colDP, w0, w0 + 32, quad, half, lane, lse2, delta, scale, scale_log2e, visible, g,
+                     p);
 }
 
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, uint64_t ns, volatile int* abort) {
