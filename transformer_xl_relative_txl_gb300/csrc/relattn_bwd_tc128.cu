@@ -79,7 +79,7 @@ constexpr int kSSmem = kSOffBias + 2 * D * 4 + 1024;
 static_assert(kSSmem <= 232448, "shared memory budget");
 constexpr uint32_t kColWin = 256, kSTmemCols = 512;
 constexpr int kPairThreads = 256;            // warps 0-7
-constexpr int kSThreads = kPairThreads + 32;  // + the issuer warp
+constexpr int kSThreads = kPairThreads + 96;  // + the load, MMA and store warps
 
 struct ScoreParams {
   const float* bias_u;
@@ -97,7 +97,7 @@ struct ScoreParams {
 };
 
 struct SBars {
-  uint64_t q, in[2], x, m1[2], done, sfree, fin;
+  uint64_t q, in[2], x, m1[2], done[2], sfree, fin;
   uint32_t tmem_base;
   int abort;
 };
@@ -160,9 +160,9 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 }
 
 // Warps 0-7 compute the pairs, two per TMEM lane quadrant (key columns 0-31
-// and 32-63 of the same rows); lane 0 of warp 8 issues the loads, the MMAs
-// (two steps ahead of the loads' consumers, one ahead of the pairs) and the
-// G / P stores, so no load latency stalls the pair warps.
+// and 32-63 of the same rows).  One thread of warp 8 issues the loads (two
+// steps ahead), one of warp 9 the MMAs (one step ahead of the pairs), one of
+// warp 10 the G / P stores, each waiting only on what it needs.
 __global__ void __launch_bounds__(kSThreads, 1)
     bwd_scores128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     mbar_init(&bars->x, 1);
     mbar_init(&bars->m1[0], 1);
     mbar_init(&bars->m1[1], 1);
-    mbar_init(&bars->done, 1);
+    mbar_init(&bars->done[0], 1);
+    mbar_init(&bars->done[1], 1);
     mbar_init(&bars->sfree, 1);
     mbar_init(&bars->fin, 1);
     bars->abort = 0;
@@ -222,7 +223,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   };
   // Inputs of step t into stage t & 1: keys and values [64 t, 64 t + 64) and
   // the window's new distances [wb(t), wb(t) + 64).
-  uint32_t n_in[2] = {0, 0};  // loads issued per stage (the issuer)
+  uint32_t n_in[2] = {0, 0};  // loads issued per stage (the load thread)
   auto load_in = [&](int t) {
     const int s = t & 1;
     uint8_t* st = sIn + s * kInStage;
@@ -236,8 +237,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (s == 0) ++n_in[0];
     else ++n_in[1];
   };
-  const bool issuer = tid == kPairThreads;
-  if (issuer) {
+  // one thread of each of warps 8-10: loads, MMAs, stores
+  const bool loader = tid == kPairThreads, mma_thread = tid == kPairThreads + 32,
+             storer = tid == kPairThreads + 64;
+  if (loader) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -345,37 +348,47 @@ __global__ void __launch_bounds__(kSThreads, 1)
     return true;
   };
 
-  if (issuer) {
-    // ============================ issuer ==================================
-    if (ok) {
-      if (T > 1) load_in(1);  // the raw q has been read: stage 1 is free
-      ok = score_mmas(0) && (T < 2 || score_mmas(1));
-    }
-    for (int t = 0; t < T && ok; ++t) {
-      const int s = t & 1;
-      // step t's MMAs have read stage s: refill it for step t + 2
-      if (!(ok = mbar_wait(&bars->m1[s], (t >> 1) & 1, wait_ns, abort))) break;
-      if (t + 2 < T) load_in(t + 2);
-      // step t's pairs are staged and its TMEM columns read
-      if (!(ok = mbar_wait(&bars->done, t & 1, wait_ns, abort))) break;
-      tma_store_3d(&tm_g, sG, BN * t, w.i0, z);
-      tma_store_3d(&tm_p, sP, BN * t, w.i0, z);
-      bulk_commit_group();
-      if (t + 2 < T) {
-        tc_fence_after();
-        if (!(ok = score_mmas(t + 2))) break;
-      }
-      bulk_wait_group_read0();
-      mbar_arrive(&bars->sfree);
+  // Barrier phases cannot be skipped: the MMAs of step t + 2 wait for the
+  // pairs of step t (done), the pairs of step t + 1 for the staging of step t
+  // (sfree), the loads of step t + 2 for the MMAs of step t (m1), and each
+  // of those is what lets the next phase of the same barrier happen.
+  if (loader) {
+    // ============================ loads ===================================
+    if (ok && T > 1) load_in(1);  // the raw q has been read: stage 1 is free
+    for (int t = 0; t + 2 < T && ok; ++t) {
+      // step t's MMAs have read stage t & 1: refill it for step t + 2
+      if (!(ok = mbar_wait(&bars->m1[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
+      load_in(t + 2);
     }
     if (!ok) report_timeout(abort, p.status);
-    // Let this CTA's own copies and MMAs finish before the memory is released.
+    // Let this CTA's own copies finish before the memory is released.
     if (n_in[0] > 0) mbar_wait_own(&bars->in[0], (n_in[0] - 1) & 1, wait_ns);
     if (n_in[1] > 0) mbar_wait_own(&bars->in[1], (n_in[1] - 1) & 1, wait_ns);
     mbar_wait_own(&bars->x, 0, wait_ns);
     mbar_wait_own(&bars->q, 0, wait_ns);
+  } else if (mma_thread) {
+    // ============================ MMAs ====================================
+    if (ok) ok = score_mmas(0) && (T < 2 || score_mmas(1));
+    for (int t = 0; t + 2 < T && ok; ++t) {
+      // step t's pairs have read its S / dP buffer and its oldest window slot
+      if (!(ok = mbar_wait(&bars->done[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
+      tc_fence_after();
+      ok = score_mmas(t + 2);
+    }
+    if (!ok) report_timeout(abort, p.status);
     tc_commit(&bars->fin);
     mbar_wait_own(&bars->fin, 0, wait_ns);
+  } else if (storer) {
+    // ============================ G / P stores ============================
+    for (int t = 0; t < T && ok; ++t) {
+      if (!(ok = mbar_wait(&bars->done[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
+      tma_store_3d(&tm_g, sG, BN * t, w.i0, z);
+      tma_store_3d(&tm_p, sP, BN * t, w.i0, z);
+      bulk_commit_group();
+      bulk_wait_group_read0();
+      mbar_arrive(&bars->sfree);
+    }
+    if (!ok) report_timeout(abort, p.status);
     bulk_wait_group0();
   } else if (tid < kPairThreads) {
     // ============================ pairs ===================================
@@ -427,16 +440,18 @@ __global__ void __launch_bounds__(kSThreads, 1)
         uint32_t col[8];
 #pragma unroll
         for (int k = 0; k < 8; ++k) col[k] = static_cast<uint32_t>((chunk ^ k) << 4);
+        uint16_t val[32];
 #pragma unroll
-        for (int r = 0; r < 32; ++r) {
-          const uint16_t val = *reinterpret_cast<const uint16_t*>(src + (r >> 3) * 1024 + (r & 7) * 128 + col[r & 7]);
-          if (r >= r_lo && r < r_hi) gs[static_cast<size_t>(r) * (p.LP + 1)] = val;
-        }
+        for (int r = 0; r < 32; ++r)
+          val[r] = *reinterpret_cast<const uint16_t*>(src + (r >> 3) * 1024 + (r & 7) * 128 + col[r & 7]);
+#pragma unroll
+        for (int r = 0; r < 32; ++r)
+          if (r >= r_lo && r < r_hi) gs[static_cast<size_t>(r) * (p.LP + 1)] = val[r];
       }
       fence_proxy_async_smem();  // the G and P staging is read by the TMA stores next
       tc_fence_before();
       named_bar_sync(1, kPairThreads);  // every pair thread has read step t's TMEM columns and staged its pairs
-      if (tid == 0) mbar_arrive(&bars->done);
+      if (tid == 0) mbar_arrive(&bars->done[s]);
     }
     if (!ok && tid == 0) report_timeout(abort, p.status);
   }
