@@ -459,10 +459,18 @@ TXL_API int txl_stack_forward(const void* h, void* out, int n_layers, void* cons
  * Paths: bf16 q, k, v, r with bf16 o and dout and D = 64 run on the tensor
  * cores (tcgen05): a dq kernel over query tiles (which also sums dr and the
  * bias gradients) and a dk/dv kernel over 64-key blocks; there dr arrives by
- * fp32 atomic adds, so its last bits may differ between calls.  Every other
- * case runs on CUDA cores in fp32 arithmetic, fully deterministic.
- * Allocates: per-(device, stream) scratch for the per-row Delta and the
- * per-tile partial sums (see the conventions above).
+ * fp32 atomic adds, so its last bits may differ between calls.  The same
+ * inputs with D = 128 and M a multiple of 8 also run on the tensor cores: a
+ * kernel rebuilds p and g per 64-key step and writes them in bf16 to scratch
+ * (g in key and in distance order, p in key order), five tcgen05 products
+ * then form dq (key and distance parts), dk, dv and dr, and ordered sums the
+ * bias gradients; deterministic.  Every other case runs on CUDA cores in
+ * fp32 arithmetic, fully deterministic.
+ * Allocates: per-(device, stream) scratch (see the conventions above): for
+ * D = 64 the per-row Delta and the per-tile partial sums; for the D = 128
+ * tensor-core path about 3 * B*H*W*LP * 2 bytes of pair terms (LP = M + W
+ * rounded up to 64) plus (q+u), (q+v) in bf16 and the two dq parts in fp32
+ * (2 * B*W*H*D * 6 bytes): 0.5 GB at B=8 H=8 W=M=768.
  */
 TXL_API int txl_relattn_backward(const void* q, const void* k, const void* v, const void* r,
                          const float* bias_u, const float* bias_v, const void* o, const float* lse,
