@@ -468,9 +468,11 @@ TXL_API int txl_stack_forward(const void* h, void* out, int n_layers, void* cons
  * fp32 arithmetic, fully deterministic.
  * Allocates: per-(device, stream) scratch (see the conventions above): for
  * D = 64 the per-row Delta and the per-tile partial sums; for the D = 128
- * tensor-core path about 3 * B*H*W*LP * 2 bytes of pair terms (LP = M + W
- * rounded up to 64) plus (q+u), (q+v) in bf16 and the two dq parts in fp32
- * (2 * B*W*H*D * 6 bytes): 0.5 GB at B=8 H=8 W=M=768.
+ * tensor-core path, per chunk of Bc sequences, 3 * Bc*H*W*LP * 2 bytes of
+ * pair terms (LP = M + W rounded up to 64) plus (q+u), (q+v) in bf16 and the
+ * two dq parts in fp32 (2 * Bc*W*H*D * 6 bytes), Bc the most sequences that
+ * fit 1 GiB (at least one; the chunks run in turn): all 8 sequences, 0.5 GB,
+ * at B=8 H=8 W=M=768.
  */
 TXL_API int txl_relattn_backward(const void* q, const void* k, const void* v, const void* r,
                          const float* bias_u, const float* bias_v, const void* o, const float* lse,
@@ -540,6 +542,10 @@ TXL_API int txl_debug_inject_stall(int on);
  * key steps into min(nsplit, steps of the shortest unit) chunks instead of
  * the count its cost model picks; 0 restores the model. */
 TXL_API int txl_debug_force_split(int nsplit);
+/* Test hook: the cap, in bytes, on the scratch of one chunk of sequences of
+ * the D = 128 tensor-core backward (default 1 GiB; 0 restores it).  A smaller
+ * cap splits the batch into more chunks, run one after the other. */
+TXL_API int txl_debug_set_bwd_chunk_bytes(unsigned long long bytes);
 
 #ifdef __cplusplus
 }

@@ -156,6 +156,25 @@ def test_backward_d128_scratch_reuse(txl):
     _compare(got, want, "bf16")
 
 
+def test_backward_d128_chunked(txl):
+    """The D = 128 tensor-core path over a batch split into chunks of
+    sequences (here one per chunk, forced by a small scratch cap): dq, dk and
+    dv are per-sequence work and come out bit-identical to one chunk; dr and
+    the bias gradients, which sum over the sequences, match the oracle."""
+    q, k, v, r, bu, bv, dout = _case(3, 2, 128, 200, 136, "bf16", 2)
+    whole = _run(txl, q, k, v, r, bu, bv, dout, 136, "bf16")
+    try:
+        txl.txl_debug_set_bwd_chunk_bytes(2 << 20)  # one sequence's scratch is about 1.6 MB
+        parts = _run(txl, q, k, v, r, bu, bv, dout, 136, "bf16")
+    finally:
+        txl.txl_debug_set_bwd_chunk_bytes(0)
+    for key in ("dq", "dk", "dv"):
+        assert np.array_equal(parts[key], whole[key]), key
+    want = O.relattn_backward(q, k, v, r, bu, bv, 136, dout, 128 ** -0.5)
+    _compare(parts, want, "bf16")
+    assert np.all(parts["dr"][136 + 200:] == 0)
+
+
 def test_backward_base_size_sampled_head(txl):
     """The base workload at full size (B=22, H=8, D=64, W=512, M=512) in one
     call; the oracle checks every gradient of one head (dq, dk, dv of all 22

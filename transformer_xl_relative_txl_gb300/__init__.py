@@ -25,6 +25,7 @@ __all__ = [
     "txl_sinusoid_rel",
     "txl_get_device_status", "txl_release_cached", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall", "txl_debug_force_split",
+    "txl_debug_set_bwd_chunk_bytes",
 ]
 
 TXL_F32 = 0
@@ -99,6 +100,8 @@ lib.txl_debug_inject_stall.argtypes = [_i]
 lib.txl_debug_inject_stall.restype = _i
 lib.txl_debug_force_split.argtypes = [_i]
 lib.txl_debug_force_split.restype = _i
+lib.txl_debug_set_bwd_chunk_bytes.argtypes = [ctypes.c_ulonglong]
+lib.txl_debug_set_bwd_chunk_bytes.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -544,3 +547,9 @@ def txl_debug_inject_stall(on: bool) -> int:
 def txl_debug_force_split(nsplit):
     """Test hook: force the D = 64 forward's split count (0: its cost model)."""
     _check(lib.txl_debug_force_split(int(nsplit)), "txl_debug_force_split")
+
+
+def txl_debug_set_bwd_chunk_bytes(nbytes):
+    """Test hook: cap on one chunk's scratch in the D = 128 tensor-core
+    backward (0: the default, 1 GiB)."""
+    _check(lib.txl_debug_set_bwd_chunk_bytes(int(nbytes)), "txl_debug_set_bwd_chunk_bytes")

@@ -364,6 +364,11 @@ int txl_debug_inject_stall(int on) {
   return TXL_OK;
 }
 
+int txl_debug_set_bwd_chunk_bytes(unsigned long long bytes) {
+  txl::relattn_bwd_tc128_set_chunk_bytes(static_cast<size_t>(bytes));
+  return TXL_OK;
+}
+
 int txl_debug_force_split(int nsplit) {
   if (nsplit < 0 || nsplit > 64) return TXL_ERR_INVALID_ARG;
   g_force_split.store(nsplit);

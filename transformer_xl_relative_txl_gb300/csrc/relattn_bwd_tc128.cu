@@ -488,6 +488,7 @@ struct GemmArgs {
   int tiles;
   float* out0;  // DQ: the key part of dq; DK: dk; DV: dv; DR: dr
   float* out1;  // DQ: the distance part of dq
+  int accumulate;  // DR: add to out0 (a later chunk of sequences) instead of storing
   unsigned int* status;
   unsigned long long wait_ns;
 };
@@ -706,10 +707,20 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         if (dst != nullptr) {
           float4* o4 = reinterpret_cast<float4*>(dst + 32 * c);
+          if (MODE == kModeDR && p.accumulate) {
+            // each (distance, head) row belongs to one tile: a plain read-add-write
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            for (int j = 0; j < 8; ++j) {
+              const float4 x = o4[j];
+              o4[j] = make_float4(x.x + __uint_as_float(v[4 * j]), x.y + __uint_as_float(v[4 * j + 1]),
+                                  x.z + __uint_as_float(v[4 * j + 2]), x.w + __uint_as_float(v[4 * j + 3]));
+            }
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              o4[j] = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                  __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+          }
         }
       }
     }
@@ -774,10 +785,10 @@ struct Scratch128 {
   size_t bytes;
 };
 
-Scratch128 carve(void* base, int B, int W, int M, int H) {
+// Scratch of one chunk of Bc sequences, then the bias partials of all chunks.
+Scratch128 carve(void* base, int Bc, int W, int M, int H, size_t n_part) {
   const size_t L = static_cast<size_t>(M) + W, LP = (L + 63) / 64 * 64;
-  const size_t bh = static_cast<size_t>(B) * H, bwhd = static_cast<size_t>(B) * W * H * D;
-  const size_t n_part = (static_cast<size_t>(B) * W + kSumRows - 1) / kSumRows;
+  const size_t bh = static_cast<size_t>(Bc) * H, bwhd = static_cast<size_t>(Bc) * W * H * D;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t at = off;
@@ -795,6 +806,29 @@ Scratch128 carve(void* base, int B, int W, int M, int H) {
   s.part = reinterpret_cast<float*>(take(n_part * H * 2 * D * 4));
   s.bytes = off;
   return s;
+}
+
+// Sequences per chunk: as many as keep one chunk's scratch within the cap
+// (at least one).  Later chunks reuse the scratch; dr accumulates over them.
+std::atomic<size_t> g_chunk_cap{size_t(1) << 30};
+
+int chunk_seqs(int B, int W, int M, int H) {
+  const size_t one = carve(nullptr, 1, W, M, H, 0).bytes;
+  const size_t c = g_chunk_cap.load() / (one == 0 ? 1 : one);
+  return static_cast<int>(std::max<size_t>(1, std::min<size_t>(c, static_cast<size_t>(B))));
+}
+
+// Rows of one bias-partial block for a chunk of `rows` rows: 32, or more
+// when the chunk would need more than 65535 blocks (the grid's y limit).
+long long rows_per_block(long long rows) { return std::max<long long>(kSumRows, (rows + 65534) / 65535); }
+
+size_t total_parts(int B, int W, int Bc) {
+  size_t n = 0;
+  for (int b0 = 0; b0 < B; b0 += Bc) {
+    const long long rows = static_cast<long long>(std::min(Bc, B - b0)) * W;
+    n += static_cast<size_t>((rows + rows_per_block(rows) - 1) / rows_per_block(rows));
+  }
+  return n;
 }
 
 template <int MODE>
@@ -821,7 +855,12 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
 
 }  // namespace
 
-size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H) { return carve(nullptr, B, W, M, H).bytes; }
+void relattn_bwd_tc128_set_chunk_bytes(size_t bytes) { g_chunk_cap.store(bytes == 0 ? size_t(1) << 30 : bytes); }
+
+size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H) {
+  const int Bc = chunk_seqs(B, W, M, H);
+  return carve(nullptr, Bc, W, M, H, total_parts(B, W, Bc)).bytes;
+}
 
 bool relattn_bwd_tc128_supported(int W, int M) { return W > 0 && M % 8 == 0; }
 
@@ -831,8 +870,9 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
                                      float* dv, float* dr, float* du, float* dvb, int B, int W, int M, int H,
                                      int n_r, float scale, void* scratch, const WaitCtl& wc, cudaStream_t stream) {
   if (encode == nullptr || !relattn_bwd_tc128_supported(W, M)) return cudaErrorInvalidValue;
-  const int L = M + W, LP = (L + 63) / 64 * 64, BH = B * H;
-  const Scratch128 sc = carve(scratch, B, W, M, H);
+  const int L = M + W, LP = (L + 63) / 64 * 64;
+  const int Bc = chunk_seqs(B, W, M, H);
+  const Scratch128 sc = carve(scratch, Bc, W, M, H, total_parts(B, W, Bc));
   const cuuint64_t hd2 = static_cast<cuuint64_t>(H) * D * 2;
   bool ok = true;
   auto enc = [&](CUtensorMap* m, const void* base, int rank, std::initializer_list<cuuint64_t> dims,
@@ -851,28 +891,25 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
                       CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                       CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
-  const cuuint64_t d_ = D, h_ = H, w_ = W, b_ = B, l_ = L;
-  // q, dout, k, v: [B, rows, H, D]; r: [n_r, H, D]; G, P, GS: [B*H][W][LP] (columns past L zero-filled)
-  CUtensorMap tq, tdo128, tk, tv, tr64, tgk, tgsk, tpk, tgmn, tpmn, tgsmn, tqu, tqv, tdo64;
-  enc(&tq, q, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
-  enc(&tdo128, dout, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
-  enc(&tk, k, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
-  enc(&tv, v, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
+  const cuuint64_t d_ = D, h_ = H, w_ = W, l_ = L;
+  const cuuint64_t lp2 = static_cast<cuuint64_t>(LP) * 2;
+  // r and the chunk's scratch do not move between chunks
+  CUtensorMap tr64, tgk, tgsk, tpk, tgmn, tpmn, tgsmn, tqu, tqv;
   enc(&tr64, r, 3, {d_, h_, static_cast<cuuint64_t>(n_r)}, {d_ * 2, hd2}, {64, 1, 64});
-  const cuuint64_t lp2 = static_cast<cuuint64_t>(LP) * 2, bh_ = BH;
-  enc(&tgk, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
-  enc(&tgsk, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
-  enc(&tpk, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
-  enc(&tgmn, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
-  enc(&tpmn, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
-  enc(&tgsmn, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
-  enc(&tqu, sc.Qu, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
-  enc(&tqv, sc.Qv, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
-  enc(&tdo64, dout, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
-  if (!ok) return cudaErrorInvalidValue;
+  auto enc_scratch = [&](int nb) {
+    const cuuint64_t bh_ = static_cast<cuuint64_t>(nb) * H, b_ = nb;
+    // G, P, GS: [nb*H][W][LP] bf16 (columns past L zero-filled); q+u, q+v: [nb, W, H, D]
+    enc(&tgk, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+    enc(&tgsk, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+    enc(&tpk, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+    enc(&tgmn, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+    enc(&tpmn, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+    enc(&tgsmn, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+    enc(&tqu, sc.Qu, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+    enc(&tqv, sc.Qv, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+  };
 
   cudaError_t e;
-  // 1. scores -> G, P, GS, q+u, q+v
   {
     static std::atomic<bool> attr_done[64];
     int dev = 0;
@@ -884,16 +921,42 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
         return e;
       attr_done[dev].store(true);
     }
+  }
+  const size_t seg = static_cast<size_t>(W) * H * D;      // one sequence of q, o, dout, dq, dk, dv
+  const size_t mem = static_cast<size_t>(L) * H * D;      // one sequence of k, v
+  const int cols4 = H * D / 4;
+  size_t p_off = 0;  // bias partials written so far
+  int last_nb = -1;
+  for (int b0 = 0; b0 < B; b0 += Bc) {
+    const int nb = std::min(Bc, B - b0);
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(q) + b0 * seg;
+    const __nv_bfloat16* kb = static_cast<const __nv_bfloat16*>(k) + b0 * mem;
+    const __nv_bfloat16* vb = static_cast<const __nv_bfloat16*>(v) + b0 * mem;
+    const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(o) + b0 * seg;
+    const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(dout) + b0 * seg;
+    const cuuint64_t b_ = nb;
+    CUtensorMap tq, tdo128, tk, tv, tdo64;
+    enc(&tq, qb, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
+    enc(&tdo128, gb, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
+    enc(&tk, kb, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
+    enc(&tv, vb, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
+    enc(&tdo64, gb, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+    if (nb != last_nb) {
+      enc_scratch(nb);
+      last_nb = nb;
+    }
+    if (!ok) return cudaErrorInvalidValue;
+    // 1. pair terms -> G, P, GS, q+u, q+v
     ScoreParams p;
     p.bias_u = bias_u;
     p.bias_v = bias_v;
-    p.lse = lse;
-    p.o = static_cast<const __nv_bfloat16*>(o);
-    p.dout = static_cast<const __nv_bfloat16*>(dout);
+    p.lse = lse + static_cast<size_t>(b0) * H * W;
+    p.o = ob;
+    p.dout = gb;
     p.GS = sc.GS;
     p.Qu = sc.Qu;
     p.Qv = sc.Qv;
-    p.B = B;
+    p.B = nb;
     p.W = W;
     p.M = M;
     p.H = H;
@@ -903,51 +966,53 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     p.scale_log2e = scale * kLog2e;
     p.status = wc.status;
     p.wait_ns = wc.limit_ns;
-    const long long units = static_cast<long long>(p.nqt) * BH;
+    const long long units = static_cast<long long>(p.nqt) * nb * H;
     if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, tk, tv, tr64, tdo128, tgk,
                                                                                  tpk, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // 2. the five products
+    GemmArgs g;
+    g.B = nb;
+    g.W = W;
+    g.M = M;
+    g.H = H;
+    g.L = L;
+    g.BH = nb * H;
+    g.nmt = (W + 127) / 128;
+    g.nkbW = (W + 63) / 64;
+    g.tiles = 0;
+    g.accumulate = 0;
+    g.status = wc.status;
+    g.wait_ns = wc.limit_ns;
+    g.out0 = sc.dqc;
+    g.out1 = sc.dqd;
+    if ((e = launch_gemm<kModeDQ>(tgk, tgsk, tk, tr64, g, stream)) != cudaSuccess) return e;
+    g.out0 = dk + b0 * seg;
+    if ((e = launch_gemm<kModeDK>(tgmn, tgmn, tqu, tqu, g, stream)) != cudaSuccess) return e;
+    g.out0 = dv + b0 * seg;
+    if ((e = launch_gemm<kModeDV>(tpmn, tpmn, tdo64, tdo64, g, stream)) != cudaSuccess) return e;
+    g.out0 = dr;
+    g.nmt = (L + 127) / 128;
+    g.accumulate = b0 > 0;
+    if ((e = launch_gemm<kModeDR>(tgsmn, tgsmn, tqv, tqv, g, stream)) != cudaSuccess) return e;
+    // 3. dq of the chunk and its bias partials
+    const long long rows = static_cast<long long>(nb) * W;
+    const long long rows_per = rows_per_block(rows);
+    const long long n_part = (rows + rows_per - 1) / rows_per;
+    const dim3 grid((cols4 + 255) / 256, static_cast<unsigned>(n_part));
+    bwd_sum128_kernel<<<grid, 256, 0, stream>>>(
+        reinterpret_cast<const float4*>(sc.dqc), reinterpret_cast<const float4*>(sc.dqd),
+        reinterpret_cast<float4*>(dq + b0 * seg), sc.part + p_off * H * 2 * D, rows, cols4, static_cast<int>(rows_per));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    p_off += static_cast<size_t>(n_part);
   }
-  // 2. the five products
-  GemmArgs g;
-  g.B = B;
-  g.W = W;
-  g.M = M;
-  g.H = H;
-  g.L = L;
-  g.BH = BH;
-  g.nmt = (W + 127) / 128;
-  g.nkbW = (W + 63) / 64;
-  g.tiles = 0;
-  g.status = wc.status;
-  g.wait_ns = wc.limit_ns;
-  g.out0 = sc.dqc;
-  g.out1 = sc.dqd;
-  if ((e = launch_gemm<kModeDQ>(tgk, tgsk, tk, tr64, g, stream)) != cudaSuccess) return e;
-  g.out0 = dk;
-  if ((e = launch_gemm<kModeDK>(tgmn, tgmn, tqu, tqu, g, stream)) != cudaSuccess) return e;
-  g.out0 = dv;
-  if ((e = launch_gemm<kModeDV>(tpmn, tpmn, tdo64, tdo64, g, stream)) != cudaSuccess) return e;
-  g.out0 = dr;
-  g.nmt = (L + 127) / 128;
-  if ((e = launch_gemm<kModeDR>(tgsmn, tgsmn, tqv, tqv, g, stream)) != cudaSuccess) return e;
   if (n_r > L &&
       (e = cudaMemsetAsync(dr + static_cast<size_t>(L) * H * D, 0, static_cast<size_t>(n_r - L) * H * D * 4,
                            stream)) != cudaSuccess)
     return e;
-  // 3. dq, bias gradients
-  const long long rows = static_cast<long long>(B) * W;
-  const int cols4 = H * D / 4;
-  // at least kSumRows rows per block (the scratch holds that many partials)
-  const long long rows_per = std::max<long long>(kSumRows, (rows + 65534) / 65535);
-  const long long n_part = (rows + rows_per - 1) / rows_per;
-  const dim3 grid((cols4 + 255) / 256, static_cast<unsigned>(n_part));
-  bwd_sum128_kernel<<<grid, 256, 0, stream>>>(reinterpret_cast<const float4*>(sc.dqc),
-                                               reinterpret_cast<const float4*>(sc.dqd), reinterpret_cast<float4*>(dq),
-                                               sc.part, rows, cols4, static_cast<int>(rows_per));
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  return launch_bwd_bias(sc.part, static_cast<int>(n_part), H, D, du, dvb, stream);
+  if (p_off > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  return launch_bwd_bias(sc.part, static_cast<int>(p_off), H, D, du, dvb, stream);
 }
 
 }  // namespace txl

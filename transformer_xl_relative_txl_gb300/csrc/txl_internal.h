@@ -145,7 +145,11 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
 // tensor copies).  Encodes its own tensor maps with `encode`.  Every output is
 // written in full (dr rows >= M + W are zeroed).
 // scratch: relattn_bwd_tc128_scratch_bytes(B, W, M, H) bytes.
+// The scratch holds one chunk of sequences (as many as keep it within 1 GiB,
+// at least one); the chunks run one after the other and dr accumulates over
+// them.  relattn_bwd_tc128_set_chunk_bytes changes the cap (0: the default).
 size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H);
+void relattn_bwd_tc128_set_chunk_bytes(size_t bytes);
 bool relattn_bwd_tc128_supported(int W, int M);
 cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
                                      const void* v, const void* r, const float* bias_u, const float* bias_v,
