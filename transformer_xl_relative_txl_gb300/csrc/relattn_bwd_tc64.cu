@@ -101,7 +101,7 @@ struct BwdParams {
 };
 
 struct QBars {
-  uint64_t q, kv[2], r[2], m1, m2, fin, fin2;
+  uint64_t q, kv[2], r[2], m1, m2[2], gready, fin, fin2;
   uint32_t tmem_base;
   int abort;
 };
@@ -178,6 +178,10 @@ __device__ __forceinline__ float row_delta(const __nv_bfloat16* o, const __nv_bf
 // ============================================================================
 constexpr int kQThreads = 256;
 constexpr int kIssuer2 = 128;  // lane 0 of warp 4: the dq kernel's gradient / slot MMAs
+// The dq kernel adds warp 8, whose lane 0 issues the loads and the score MMAs
+// outside the pair warps' barriers.
+constexpr int kDqIssuer = kQThreads;
+constexpr int kDqThreads = kQThreads + 32;
 constexpr uint32_t kColDr = 448;  // the finished slot's dr rows (M = 64 layout)
 
 // Columns [32 half, 32 half + 32) of row a of a 128B-swizzled [128 x 64] bf16 tile.
@@ -191,7 +195,7 @@ __device__ __forceinline__ void store_row_half(uint8_t* tile, int a, int half, c
   }
 }
 
-__global__ void __launch_bounds__(kQThreads, 1)
+__global__ void __launch_bounds__(kDqThreads, 1)
     bwd_dq_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
                        const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dr,
@@ -228,7 +232,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_init(&bars->r[0], 1);
     mbar_init(&bars->r[1], 1);
     mbar_init(&bars->m1, 1);
-    mbar_init(&bars->m2, 1);
+    mbar_init(&bars->m2[0], 1);
+    mbar_init(&bars->m2[1], 1);
+    mbar_init(&bars->gready, 1);
     mbar_init(&bars->fin, 1);
     mbar_init(&bars->fin2, 1);
     bars->abort = 0;
@@ -241,7 +247,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
   if (tid < 2 * D) sBias[tid] = tid < D ? p.bias_u[w.h * D + tid] : p.bias_v[w.h * D + tid - D];
   // Distance slots start at zero: a slot entry no step writes is a pair
   // that does not exist.
-  for (int x = tid; x < 4 * kTile / 16; x += kQThreads)
+  for (int x = tid; x < 4 * kTile / 16; x += kDqThreads)
     reinterpret_cast<uint4*>(sGs)[x] = make_uint4(0u, 0u, 0u, 0u);
   tc_fence_before();
   __syncthreads();
@@ -250,7 +256,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
 
   // Window of step t: distance rows [wb(t), wb(t) + 192), wb = M + i0 - 64 t - 64.
   auto wbase = [&](int t) { return p.M + w.i0 - BN * t - BN; };
-  uint32_t n_ld[2] = {0, 0};  // loads issued per stage (thread 0)
+  uint32_t n_ld[2] = {0, 0};  // loads issued per stage (the issuer)
   auto issue_step_loads = [&](int t) {
     const int s = t & 1;
     mbar_arrive_expect_tx(&bars->kv[s], 2 * kKTile);
@@ -260,7 +266,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tma_load_3d(sR + s * kWinTile, &tm_rw, &bars->r[s], 0, w.h, wbase(t));
     ++n_ld[s];
   };
-  if (tid == 0) {
+  if (tid == kDqIssuer) {
     tma_prefetch_desc(&tm_q);
     tma_prefetch_desc(&tm_k);
     tma_prefetch_desc(&tm_v);
@@ -277,16 +283,20 @@ __global__ void __launch_bounds__(kQThreads, 1)
   // Per-row constants: lse (log2 domain) and Delta.
   const long long row_id = (static_cast<long long>(w.b) * p.H + w.h) * p.W + i;
   float lse2 = INFINITY, delta = 0.f;  // rows past W: every p is 0
-  if (i < p.W) {
+  const bool pair = tid < kQThreads;  // warps 0-7
+  if (pair && i < p.W) {
     lse2 = p.lse[row_id] * kLog2e;
     const long long off = ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D;
     delta = row_delta(p.o + off, p.dout + off);
     if (half == 0) p.delta[row_id] = delta;
   }
-  bool ok = mbar_wait(&bars->q, 0, wait_ns, abort);
-  if (ok) build_qu_qv_half(sG, sQu, sQv, a, half, sBias, sBias + D);
-  else report_timeout(abort, p.status);
-  fence_proxy_async_smem();
+  bool ok = true;
+  if (pair) {
+    ok = mbar_wait(&bars->q, 0, wait_ns, abort);
+    if (ok) build_qu_qv_half(sG, sQu, sQv, a, half, sBias, sBias + D);
+    else report_timeout(abort, p.status);
+    fence_proxy_async_smem();
+  }
   ok = __syncthreads_and(ok) != 0;
 
   constexpr uint32_t id64 = idesc_bf16(128, 64, false, false);
@@ -298,10 +308,9 @@ __global__ void __launch_bounds__(kQThreads, 1)
   const uint64_t dDO = sdesc_sw128(smem_u32(sDO), 16, 1024);
   const uint64_t dG = sdesc_sw128(smem_u32(sG), 16, 1024);
   const uint64_t dQvMN = sdesc_sw128(smem_u32(sQv), 8192, 1024);
-  uint32_t n_m2 = 0;  // commits on m2
   int n_slot = 0;     // distance slots issued (the slot issuer, kIssuer2)
 
-  // Thread 0: the score MMAs of step t (S, dP, distance window).
+  // The issuer: the score MMAs of step t (S, dP, distance window).
   auto score_mmas = [&](int t) -> bool {
     const int s = t & 1;
     if (!mbar_wait(&bars->kv[s], (t >> 1) & 1, wait_ns, abort) ||
@@ -320,7 +329,7 @@ __global__ void __launch_bounds__(kQThreads, 1)
     tc_commit(&bars->m1);
     return true;
   };
-  // Thread 0: d(q+v) += Gs R and dr_slot = Gs^T (q+v) for distance slot tau,
+  // kIssuer2: d(q+v) += Gs R and dr_slot = Gs^T (q+v) for distance slot tau,
   // whose R rows are rows [64 r_row, 64 r_row + 64) of window stage rs.
   auto slot_mmas = [&](int tau, int rs, int r_row) {
     const int gi = (tau + 2) & 3;
@@ -383,134 +392,28 @@ __global__ void __launch_bounds__(kQThreads, 1)
     if (stage_dr(tau)) dr_d0 = p.M + w.i0 - BN * tau - BN;
   };
 
-  if (tid == 0 && ok && !score_mmas(0)) report_timeout(abort, p.status);
-  for (int t = 0; t < T && ok; ++t) {
-    const int s = t & 1;
-    // (1) everyone: the step's gradients into G (key order) and the slots;
-    // thread 0 hands the slot staged at the end of the last step to the TMA.
-    ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort);
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    if (tid == 0) issue_dr();
-    tc_fence_after();
-    {
-      float g[32], pr[32];
-      const int lim = p.M + i - BN * t;  // key column c visible iff c <= lim
-      step_grads_half(tmem, kColS, kColDP, kColWin, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
-                      [&](int c) { return c <= lim; }, g, pr);
-      store_row_half(sG, a, half, g);
-      // Skewed copy: key column c of step t sits at window position
-      // z = 64 + a - c, i.e. in distance slot t - z / 64, column z % 64.
-#pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const int z = 64 + a - (32 * half + c);
-        const int gi = (t - (z >> 6) + 2) & 3;
-        *reinterpret_cast<__nv_bfloat16*>(sGs + gi * kTile + swz(a, z & 63)) = __float2bfloat16_rn(g[c]);
+  // Barrier phases cannot be skipped: the score MMAs of step t+1 wait for
+  // the pairs of step t (gready), the loads of step t+2 for step t's
+  // gradient MMAs (m2), and each of those is what lets the next phase of the
+  // same barrier happen.
+  if (tid == kDqIssuer) {
+    // ============================ issuer ==================================
+    if (ok) ok = score_mmas(0);
+    for (int t = 0; t < T && ok; ++t) {
+      if (t + 1 < T) {
+        // the pairs of step t have read S, dP and the window
+        if (!(ok = mbar_wait(&bars->gready, t & 1, wait_ns, abort))) break;
+        tc_fence_after();
+        if (!(ok = score_mmas(t + 1))) break;
+      }
+      if (t + 2 < T) {
+        // step t's gradient MMAs have read K and the window of stage t & 1
+        if (!(ok = mbar_wait(&bars->m2[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
+        issue_step_loads(t + 2);
       }
     }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    // (2) the next step's score MMAs (thread 0) and, issued alongside from
-    // another warp, d(q+u) += G K and the slot step t finished (t-2).
-    if (tid == 0) {
-      tc_fence_after();
-      if (t + 1 < T && !score_mmas(t + 1)) report_timeout(abort, p.status);
-    } else if (tid == kIssuer2) {
-      tc_fence_after();
-      const uint64_t dKmn = sdesc_sw128(smem_u32(sK + s * kKTile), 8192, 1024);
-#pragma unroll
-      for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColA, dG + 2 * kk, dKmn + 128 * kk, idMN, t > 0 || kk > 0);
-      slot_mmas(t - 2, s, 2);
-      tc_commit(&bars->m2);
-    }
-    // (3) everyone: flush the slot's dr rows; the slot's buffer is free again
-    // and becomes slot t+2; thread 0 refills this step's load stage.  sDr is
-    // free once the last reduction has read it (thread 0 waits before the
-    // barrier).
-    if (tid == 0) bulk_wait_group_read0();
-    ok = mbar_wait(&bars->m2, n_m2 & 1, wait_ns, abort);
-    ++n_m2;
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    flush_dr(t - 2);
-    {
-      uint4* nxt = reinterpret_cast<uint4*>(sGs + (t & 3) * kTile);
-      for (int x = tid; x < kTile / 16; x += kQThreads) nxt[x] = make_uint4(0u, 0u, 0u, 0u);
-    }
-    if (tid == 0 && t + 2 < T) issue_step_loads(t + 2);  // stage s: step t's MMAs are done
-    tc_fence_before();
-  }
-  // The last two slots are finished once the last step has written them.
-  for (int k = 0; k < 2 && ok; ++k) {
-    const int tau = T - 2 + k;
-    __syncthreads();
-    if (tid == kIssuer2) {
-      tc_fence_after();
-      slot_mmas(tau, (T - 1) & 1, T - 1 - tau);
-      tc_commit(&bars->m2);
-    }
-    if (tid == 0) {
-      issue_dr();
-      bulk_wait_group_read0();
-    }
-    ok = mbar_wait(&bars->m2, n_m2 & 1, wait_ns, abort);
-    ++n_m2;
-    if (!__syncthreads_and(ok)) {
-      ok = false;
-      break;
-    }
-    tc_fence_after();
-    flush_dr(tau);
-    tc_fence_before();
-  }
-
-  if (ok) {
-    // dq = d(q+u) + d(q+v) for this row's 32 head dims; the tile's column
-    // sums of both go to the bias partials through shared memory
-    // (XOR-staggered columns).
-    __syncthreads();  // the slot buffers are free for the column sums
-    if (tid == 0) issue_dr();
-    uint32_t u[32], v[32];
-    const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
-    tmem_ld32(lb + kColA + 32 * half, u);
-    tmem_ld32(lb + kColB + 32 * half, v);
-    tmem_wait_ld(u);
-    tmem_wait_ld(v);
-    if (i < p.W) {
-      float4* dst = reinterpret_cast<float4*>(p.dq + ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D +
-                                              32 * half);
-#pragma unroll
-      for (int e = 0; e < 8; ++e)
-        dst[e] = make_float4(__uint_as_float(u[4 * e]) + __uint_as_float(v[4 * e]),
-                             __uint_as_float(u[4 * e + 1]) + __uint_as_float(v[4 * e + 1]),
-                             __uint_as_float(u[4 * e + 2]) + __uint_as_float(v[4 * e + 2]),
-                             __uint_as_float(u[4 * e + 3]) + __uint_as_float(v[4 * e + 3]));
-    }
-    // red[x][row ^ (x & 31)]: column x of the row sums (x < 64: d(q+u)).
-    float* red = reinterpret_cast<float*>(sGs);
-#pragma unroll
-    for (int x = 0; x < 32; ++x) {
-      red[(32 * half + x) * BM + (a ^ x)] = __uint_as_float(u[x]);
-      red[(64 + 32 * half + x) * BM + (a ^ x)] = __uint_as_float(v[x]);
-    }
-    __syncthreads();
-    if (tid < 2 * D) {
-      float sum = 0.f;
-      for (int r = 0; r < BM; ++r) sum += red[tid * BM + (r ^ (tid & 31))];
-      const int qt = w.i0 / BM;
-      p.part[((static_cast<long long>(w.b) * p.nqt + qt) * p.H + w.h) * 2 * D + tid] = sum;
-    }
-  }
-  // Let this CTA's own copies, reductions and MMAs finish before the memory
-  // is released.
-  if (tid == 0) {
-    bulk_wait_group0();
+    if (!ok) report_timeout(abort, p.status);
+    // Let this thread's copies and MMAs finish before the memory is released.
     for (int s = 0; s < 2; ++s)
       if (n_ld[s] > 0) mbar_wait_own(&bars->kv[s], (n_ld[s] - 1) & 1, wait_ns);
     for (int s = 0; s < 2; ++s)
@@ -518,10 +421,135 @@ __global__ void __launch_bounds__(kQThreads, 1)
     mbar_wait_own(&bars->q, 0, wait_ns);
     tc_commit(&bars->fin);
     mbar_wait_own(&bars->fin, 0, wait_ns);
-  }
-  if (tid == kIssuer2) {
-    tc_commit(&bars->fin2);
-    mbar_wait_own(&bars->fin2, 0, wait_ns);
+  } else if (pair) {
+    // ============================ pairs ===================================
+    // m2 commits c = 0, 1, ...: one per step, then the last two slots; commit
+    // c lands on m2[c & 1] with parity (c >> 1) & 1.
+    for (int t = 0; t < T && ok; ++t) {
+      const int s = t & 1;
+      // (1) the step's gradients into G (key order) and the slots; thread 0
+      // hands the slot staged at the end of the last step to the TMA.
+      ok = mbar_wait(&bars->m1, t & 1, wait_ns, abort);
+      if (!named_bar_and(1, kQThreads, ok)) {
+        ok = false;
+        break;
+      }
+      if (tid == 0) issue_dr();
+      tc_fence_after();
+      {
+        float g[32], pr[32];
+        const int lim = p.M + i - BN * t;  // key column c visible iff c <= lim
+        step_grads_half(tmem, kColS, kColDP, kColWin, quad, half, lane, lse2, delta, p.scale, p.scale_log2e,
+                        [&](int c) { return c <= lim; }, g, pr);
+        store_row_half(sG, a, half, g);
+        // Skewed copy: key column c of step t sits at window position
+        // z = 64 + a - c, i.e. in distance slot t - z / 64, column z % 64.
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int z = 64 + a - (32 * half + c);
+          const int gi = (t - (z >> 6) + 2) & 3;
+          *reinterpret_cast<__nv_bfloat16*>(sGs + gi * kTile + swz(a, z & 63)) = __float2bfloat16_rn(g[c]);
+        }
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      named_bar_sync(1, kQThreads);
+      // (2) the issuer goes on with the next step's score MMAs; kIssuer2
+      // issues d(q+u) += G K and the slot step t finished (t-2).
+      if (tid == 0) {
+        mbar_arrive(&bars->gready);
+      } else if (tid == kIssuer2) {
+        tc_fence_after();
+        const uint64_t dKmn = sdesc_sw128(smem_u32(sK + s * kKTile), 8192, 1024);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) mma_ss(tmem + kColA, dG + 2 * kk, dKmn + 128 * kk, idMN, t > 0 || kk > 0);
+        slot_mmas(t - 2, s, 2);
+        tc_commit(&bars->m2[t & 1]);
+      }
+      // (3) flush the slot's dr rows; the slot's buffer is free again and
+      // becomes slot t+2.  sDr is free once the last reduction has read it.
+      if (tid == 0) bulk_wait_group_read0();
+      ok = mbar_wait(&bars->m2[t & 1], (t >> 1) & 1, wait_ns, abort);
+      if (!named_bar_and(1, kQThreads, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      flush_dr(t - 2);
+      {
+        uint4* nxt = reinterpret_cast<uint4*>(sGs + (t & 3) * kTile);
+        for (int x = tid; x < kTile / 16; x += kQThreads) nxt[x] = make_uint4(0u, 0u, 0u, 0u);
+      }
+      tc_fence_before();
+    }
+    // The last two slots are finished once the last step has written them.
+    for (int k = 0; k < 2 && ok; ++k) {
+      const int tau = T - 2 + k, c = T + k;
+      named_bar_sync(1, kQThreads);
+      if (tid == kIssuer2) {
+        tc_fence_after();
+        slot_mmas(tau, (T - 1) & 1, T - 1 - tau);
+        tc_commit(&bars->m2[c & 1]);
+      }
+      if (tid == 0) {
+        issue_dr();
+        bulk_wait_group_read0();
+      }
+      ok = mbar_wait(&bars->m2[c & 1], (c >> 1) & 1, wait_ns, abort);
+      if (!named_bar_and(1, kQThreads, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      flush_dr(tau);
+      tc_fence_before();
+    }
+
+    if (ok) {
+      // dq = d(q+u) + d(q+v) for this row's 32 head dims; the tile's column
+      // sums of both go to the bias partials through shared memory
+      // (XOR-staggered columns).
+      named_bar_sync(1, kQThreads);  // the slot buffers are free for the column sums
+      if (tid == 0) issue_dr();
+      uint32_t u[32], v[32];
+      const uint32_t lb = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+      tmem_ld32(lb + kColA + 32 * half, u);
+      tmem_ld32(lb + kColB + 32 * half, v);
+      tmem_wait_ld(u);
+      tmem_wait_ld(v);
+      if (i < p.W) {
+        float4* dst = reinterpret_cast<float4*>(p.dq + ((static_cast<long long>(w.b) * p.W + i) * p.H + w.h) * D +
+                                                32 * half);
+#pragma unroll
+        for (int e = 0; e < 8; ++e)
+          dst[e] = make_float4(__uint_as_float(u[4 * e]) + __uint_as_float(v[4 * e]),
+                               __uint_as_float(u[4 * e + 1]) + __uint_as_float(v[4 * e + 1]),
+                               __uint_as_float(u[4 * e + 2]) + __uint_as_float(v[4 * e + 2]),
+                               __uint_as_float(u[4 * e + 3]) + __uint_as_float(v[4 * e + 3]));
+      }
+      // red[x][row ^ (x & 31)]: column x of the row sums (x < 64: d(q+u)).
+      float* red = reinterpret_cast<float*>(sGs);
+#pragma unroll
+      for (int x = 0; x < 32; ++x) {
+        red[(32 * half + x) * BM + (a ^ x)] = __uint_as_float(u[x]);
+        red[(64 + 32 * half + x) * BM + (a ^ x)] = __uint_as_float(v[x]);
+      }
+      named_bar_sync(1, kQThreads);
+      if (tid < 2 * D) {
+        float sum = 0.f;
+        for (int r = 0; r < BM; ++r) sum += red[tid * BM + (r ^ (tid & 31))];
+        const int qt = w.i0 / BM;
+        p.part[((static_cast<long long>(w.b) * p.nqt + qt) * p.H + w.h) * 2 * D + tid] = sum;
+      }
+    }
+    if (!ok && tid == 0) report_timeout(abort, p.status);
+    // Let this CTA's own reductions and gradient MMAs finish before the
+    // memory is released.
+    if (tid == 0) bulk_wait_group0();
+    if (tid == kIssuer2) {
+      tc_commit(&bars->fin2);
+      mbar_wait_own(&bars->fin2, 0, wait_ns);
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -880,7 +908,7 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   if ((e = cudaMemsetAsync(dr, 0, sizeof(float) * static_cast<size_t>(n_r) * H * D, stream)) != cudaSuccess)
     return e;
   const int units = p.nqt * B * H;
-  bwd_dq_tc64_kernel<<<units, kQThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, tm_dr, p);
+  bwd_dq_tc64_kernel<<<units, kDqThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, tm_dr, p);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int n_items = (W + BN - 1) / BN * B * H;
   const int grid = n_items < num_sms() ? n_items : num_sms();
