@@ -362,19 +362,32 @@ __global__ void __launch_bounds__(kThreads) bwd_dr_kernel(BwdArgs a) {
 // du, dv_bias from the partials: one warp per (head, column) -- grid
 // (H, 2D / 8), 8 warps a block -- lanes over the partials in a fixed order,
 // then a fixed shuffle tree.
+// du, dv_bias from the partials part [n_part][H][2][D] (d(q+u) columns, then
+// d(q+v)): a block takes 32 adjacent columns; warp w adds partials w,
+// w + 32, ... of its lane's column (coalesced rows), then the 32 warp sums
+// are added in warp order, so the order is fixed.
 __global__ void bwd_bias_kernel(const float* __restrict__ part, int n_part, int H, int D, float* __restrict__ du,
                                 float* __restrict__ dvb) {
-  const int h = blockIdx.x, lane = threadIdx.x & 31;
-  const int x = blockIdx.y * 8 + (threadIdx.x >> 5);
-  if (x >= 2 * D) return;
+  __shared__ float red[32][32];
+  const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
+  const int ncol = H * 2 * D;
+  const int col = blockIdx.x * 32 + lane;
   float s = 0.f;
-  for (int q = lane; q < n_part; q += 32) s += part[(static_cast<long long>(q) * H + h) * 2 * D + x];
-  s = warp_sum(s);
-  if (lane == 0) {
+  if (col < ncol) {
+#pragma unroll 4
+    for (int q = wp; q < n_part; q += 32) s += part[static_cast<long long>(q) * ncol + col];
+  }
+  red[wp][lane] = s;
+  __syncthreads();
+  if (wp == 0 && col < ncol) {
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) t += red[k][lane];
+    const int h = col / (2 * D), x = col % (2 * D);
     if (x < D)
-      du[h * D + x] = s;
+      du[h * D + x] = t;
     else
-      dvb[h * D + x - D] = s;
+      dvb[h * D + x - D] = t;
   }
 }
 
@@ -386,7 +399,8 @@ cudaError_t launch_typed(BwdArgs a, float* du, float* dvb, cudaStream_t stream) 
   bwd_dkdv_kernel<T, TG><<<dim3(nb, a.H, a.B), kThreads, sizeof(float) * (kWarps * 2 + 2) * a.D, stream>>>(a);
   bwd_dr_kernel<T, TG><<<dim3((a.n_r + kWarps - 1) / kWarps, a.H), kThreads, sizeof(float) * (kWarps + 2) * a.D,
                          stream>>>(a);
-  bwd_bias_kernel<<<dim3(a.H, (2 * a.D + 7) / 8), 256, 0, stream>>>(a.part, a.B * nb, a.H, a.D, du, dvb);
+  bwd_bias_kernel<<<(a.H * 2 * a.D + 31) / 32, 1024, 0, stream>>>(a.part, a.B * nb, a.H, a.D, du,
+                                                                   dvb);
   return cudaGetLastError();
 }
 
@@ -394,7 +408,7 @@ cudaError_t launch_typed(BwdArgs a, float* du, float* dvb, cudaStream_t stream) 
 
 cudaError_t launch_bwd_bias(const float* part, int n_part, int H, int D, float* du, float* dvb,
                             cudaStream_t stream) {
-  bwd_bias_kernel<<<dim3(H, (2 * D + 7) / 8), 256, 0, stream>>>(part, n_part, H, D, du, dvb);
+  bwd_bias_kernel<<<(H * 2 * D + 31) / 32, 1024, 0, stream>>>(part, n_part, H, D, du, dvb);
   return cudaGetLastError();
 }
 

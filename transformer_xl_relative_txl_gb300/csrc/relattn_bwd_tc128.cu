@@ -750,12 +750,26 @@ __global__ void bwd_sum128_kernel(const float4* __restrict__ dqc, const float4* 
   const long long r0 = static_cast<long long>(blockIdx.y) * rows_per;
   const long long r1 = min(rows, r0 + rows_per);
   float4 su = make_float4(0.f, 0.f, 0.f, 0.f), sv = su;
-  for (long long r = r0; r < r1; ++r) {
-    const size_t o = static_cast<size_t>(r) * cols4 + c;
-    const float4 a = dqc[o], b = dqd[o];
+  auto add_row = [&](size_t o, float4 a, float4 b) {
     dq[o] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
     su = make_float4(su.x + a.x, su.y + a.y, su.z + a.z, su.w + a.w);
     sv = make_float4(sv.x + b.x, sv.y + b.y, sv.z + b.z, sv.w + b.w);
+  };
+  long long r = r0;
+  for (; r + 8 <= r1; r += 8) {  // eight rows' loads in flight, then the sums in row order
+    float4 a[8], b[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const size_t o = static_cast<size_t>(r + k) * cols4 + c;
+      a[k] = dqc[o];
+      b[k] = dqd[o];
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) add_row(static_cast<size_t>(r + k) * cols4 + c, a[k], b[k]);
+  }
+  for (; r < r1; ++r) {
+    const size_t o = static_cast<size_t>(r) * cols4 + c;
+    add_row(o, dqc[o], dqd[o]);
   }
   const int h = (4 * c) / D, d = (4 * c) % D;
   float* pp = part + ((static_cast<size_t>(blockIdx.y) * (cols4 * 4 / D) + h) * 2) * D + d;
