@@ -225,12 +225,39 @@ __global__ void __launch_bounds__(kDqThreads, 1)
   const int i = w.i0 + a;  // query row
   const int L = p.M + p.W;
 
-  if (tid == 0) {
+  // Window of step t: distance rows [wb(t), wb(t) + 192), wb = M + i0 - 64 t - 64.
+  auto wbase = [&](int t) { return p.M + w.i0 - BN * t - BN; };
+  uint32_t n_ld[2] = {0, 0};  // loads issued per stage (the issuer)
+  auto issue_step_loads = [&](int t) {
+    const int s = t & 1;
+    mbar_arrive_expect_tx(&bars->kv[s], 2 * kKTile);
+    tma_load_4d(sK + s * kKTile, &tm_k, &bars->kv[s], 0, w.h, BN * t, w.b);
+    tma_load_4d(sV + s * kKTile, &tm_v, &bars->kv[s], 0, w.h, BN * t, w.b);
+    mbar_arrive_expect_tx(&bars->r[s], kWinTile);
+    tma_load_3d(sR + s * kWinTile, &tm_rw, &bars->r[s], 0, w.h, wbase(t));
+    ++n_ld[s];
+  };
+  // The issuer starts the unit's loads first thing (it owns their barriers);
+  // the block barrier below makes its initialisation visible to the waiters.
+  if (tid == kDqIssuer) {
     mbar_init(&bars->q, 1);
     mbar_init(&bars->kv[0], 1);
     mbar_init(&bars->kv[1], 1);
     mbar_init(&bars->r[0], 1);
     mbar_init(&bars->r[1], 1);
+    fence_mbar_init();
+    tma_prefetch_desc(&tm_q);
+    tma_prefetch_desc(&tm_k);
+    tma_prefetch_desc(&tm_v);
+    tma_prefetch_desc(&tm_rw);
+    tma_prefetch_desc(&tm_do);
+    tma_prefetch_desc(&tm_dr);
+    mbar_arrive_expect_tx(&bars->q, 2 * kTile);
+    tma_load_4d(sG, &tm_q, &bars->q, 0, w.h, w.i0, w.b);  // raw q, into the G tile for now
+    tma_load_4d(sDO, &tm_do, &bars->q, 0, w.h, w.i0, w.b);
+    issue_step_loads(0);
+    if (T > 1) issue_step_loads(1);
+  } else if (tid == 0) {
     mbar_init(&bars->m1, 1);
     mbar_init(&bars->m2[0], 1);
     mbar_init(&bars->m2[1], 1);
@@ -245,41 +272,6 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     tmem_relinquish();
   }
   if (tid < 2 * D) sBias[tid] = tid < D ? p.bias_u[w.h * D + tid] : p.bias_v[w.h * D + tid - D];
-  // Distance slots start at zero: a slot entry no step writes is a pair
-  // that does not exist.
-  for (int x = tid; x < 4 * kTile / 16; x += kDqThreads)
-    reinterpret_cast<uint4*>(sGs)[x] = make_uint4(0u, 0u, 0u, 0u);
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = bars->tmem_base;
-
-  // Window of step t: distance rows [wb(t), wb(t) + 192), wb = M + i0 - 64 t - 64.
-  auto wbase = [&](int t) { return p.M + w.i0 - BN * t - BN; };
-  uint32_t n_ld[2] = {0, 0};  // loads issued per stage (the issuer)
-  auto issue_step_loads = [&](int t) {
-    const int s = t & 1;
-    mbar_arrive_expect_tx(&bars->kv[s], 2 * kKTile);
-    tma_load_4d(sK + s * kKTile, &tm_k, &bars->kv[s], 0, w.h, BN * t, w.b);
-    tma_load_4d(sV + s * kKTile, &tm_v, &bars->kv[s], 0, w.h, BN * t, w.b);
-    mbar_arrive_expect_tx(&bars->r[s], kWinTile);
-    tma_load_3d(sR + s * kWinTile, &tm_rw, &bars->r[s], 0, w.h, wbase(t));
-    ++n_ld[s];
-  };
-  if (tid == kDqIssuer) {
-    tma_prefetch_desc(&tm_q);
-    tma_prefetch_desc(&tm_k);
-    tma_prefetch_desc(&tm_v);
-    tma_prefetch_desc(&tm_rw);
-    tma_prefetch_desc(&tm_do);
-    tma_prefetch_desc(&tm_dr);
-    mbar_arrive_expect_tx(&bars->q, 2 * kTile);
-    tma_load_4d(sG, &tm_q, &bars->q, 0, w.h, w.i0, w.b);  // raw q, into the G tile for now
-    tma_load_4d(sDO, &tm_do, &bars->q, 0, w.h, w.i0, w.b);
-    issue_step_loads(0);
-    if (T > 1) issue_step_loads(1);
-  }
-
   // Per-row constants: lse (log2 domain) and Delta.
   const long long row_id = (static_cast<long long>(w.b) * p.H + w.h) * p.W + i;
   float lse2 = INFINITY, delta = 0.f;  // rows past W: every p is 0
@@ -290,6 +282,15 @@ __global__ void __launch_bounds__(kDqThreads, 1)
     delta = row_delta(p.o + off, p.dout + off);
     if (half == 0) p.delta[row_id] = delta;
   }
+  // Distance slots start at zero: a slot entry no step writes is a pair
+  // that does not exist.
+  for (int x = tid; x < 4 * kTile / 16; x += kDqThreads)
+    reinterpret_cast<uint4*>(sGs)[x] = make_uint4(0u, 0u, 0u, 0u);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+
   bool ok = true;
   if (pair) {
     ok = mbar_wait(&bars->q, 0, wait_ns, abort);
