@@ -13,11 +13,12 @@
 // operands and the gradient accumulators exceed the shared and tensor
 // memory), so the work is split in three:
 //   1. bwd_scores128_kernel, one CTA per (batch, head, 128-query tile), 64-key
-//      steps: S = (q+u) K^T, dP = dout V^T and the 192-distance window
-//      (q+v) R^T on the tensor cores (K = 128), then per pair p and g with the
-//      distance term shifted into key order as in the forward.  It writes, in
-//      bf16, G [bh][i][j] and P [bh][i][j] (key order) and GS [bh][i][d] (the
-//      same g in distance order, d = M+i-j).
+//      steps: S = (q+u) K^T, dP = dout V^T and the step's 64 new distances of
+//      the 192-distance window (q+v) R^T on the tensor cores (K = 128), then
+//      per pair p and g with the distance term shifted into key order as in
+//      the forward.  It writes, in bf16, G [bh][i][j] and P [bh][i][j] (key
+//      order), GS [bh][i][d] (the same g in distance order, d = M+i-j), and
+//      (q+u), (q+v) as the MMAs saw them.
 //   2. bgemm_kernel, this library's tcgen05 GEMM arranged for the five
 //      products (M = 128 rows of a tile, N = D = 128, fp32 accumulators in
 //      TMEM, fp32 results): dq_c = G K and dq_d = GS r per (batch, head);
@@ -26,8 +27,10 @@
 //      over every sequence's queries).
 //   3. bwd_sum128_kernel: dq = dq_c + dq_d, and the bias gradients as sums of
 //      dq_c and dq_d over (batch, query) in a fixed order.
-// Every result is deterministic.  Every wait is bounded; a timed-out wait
-// raises the device status word and the CTA unwinds.
+// The batch runs in chunks of sequences whose scratch fits a cap (1 GiB by
+// default); dr accumulates over the chunks.  Every result is deterministic.
+// Every wait is bounded; a timed-out wait raises the device status word and
+// the CTA unwinds.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
