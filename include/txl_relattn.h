@@ -530,9 +530,10 @@ TXL_API int txl_version(void);
  * txl_debug_set_wait_limit_ns: upper bound, in nanoseconds, of every bounded
  * wait inside the kernels (default 2e9).  Values < 1000 are rejected.
  *
- * txl_debug_inject_stall: when nonzero, the next txl_relattn_forward on the
- * tensor-core path has its loader stop issuing loads after the first key tile,
- * so the consumers' bounded waits expire and the call reports
+ * txl_debug_inject_stall: when nonzero, the next txl_relattn_forward or
+ * txl_relattn_backward on a tensor-core path has its loads stop early (the
+ * forward's loader after the first key tile, the backward's after the first
+ * two key steps), so the consumers' bounded waits expire and the call reports
  * TXL_ERR_DEVICE_TIMEOUT through txl_get_device_status.  The flag clears
  * itself after that one call.
  */

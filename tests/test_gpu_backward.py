@@ -175,6 +175,34 @@ def test_backward_d128_chunked(txl):
     assert np.all(parts["dr"][136 + 200:] == 0)
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_bounded_wait_reports_timeout(txl, D):
+    """The backward's loads stop after its first two key steps (test hook),
+    so the bounded waits of the roles that need later steps run out (50 ms):
+    the kernels unwind, the status word reports the timeout, and the next
+    call computes correctly."""
+    q, k, v, r, bu, bv, dout = _case(1, 2, D, 128, 256, "bf16")  # six key steps
+    td = torch.bfloat16
+    qd, kd, vd, rd = (to_dev(x, td) for x in (q, k, v, r))
+    bud, bvd = to_dev(bu, torch.float32), to_dev(bv, torch.float32)
+    o = torch.empty(qd.shape, device=dev(), dtype=td)
+    lse = torch.empty(1, 2, 128, device=dev(), dtype=torch.float32)
+    txl.txl_relattn_forward(qd, kd, vd, rd, bud, bvd, o, lse, M=256)
+    assert txl.txl_get_device_status() == 0
+    assert txl.txl_debug_set_wait_limit_ns(50_000_000) == 0
+    try:
+        assert txl.txl_debug_inject_stall(True) == 0
+        txl.txl_relattn_backward(qd, kd, vd, rd, bud, bvd, o, lse, to_dev(dout, td), M=256)
+        assert txl.txl_get_device_status() == 5  # TXL_ERR_DEVICE_TIMEOUT
+        assert txl.txl_get_device_status() == 0  # the word was cleared
+    finally:
+        txl.txl_debug_inject_stall(False)
+        txl.txl_debug_set_wait_limit_ns(2_000_000_000)
+    got = _run(txl, q, k, v, r, bu, bv, dout, 256, "bf16")
+    want = O.relattn_backward(q, k, v, r, bu, bv, 256, dout, D ** -0.5)
+    _compare(got, want, "bf16")
+
+
 def test_backward_base_size_sampled_head(txl):
     """The base workload at full size (B=22, H=8, D=64, W=512, M=512) in one
     call; the oracle checks every gradient of one head (dq, dk, dv of all 22

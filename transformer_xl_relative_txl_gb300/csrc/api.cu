@@ -769,7 +769,7 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
     txl::WaitCtl wc;
     if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
     wc.limit_ns = g_wait_ns.load();
-    wc.inject_stall = 0;
+    wc.inject_stall = g_inject_stall.exchange(0);
     const long long nqt = (W + 127) / 128;
     if (nqt * B * H > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
     return from_cuda(txl::launch_relattn_bwd_tc64(tm_q, tm_k, tm_v, tm_rw, tm_do, tm_dr, bias_u, bias_v, lse, o,
@@ -785,7 +785,7 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
     txl::WaitCtl wc;
     if (status_ptr(&wc.status) != cudaSuccess) return TXL_ERR_CUDA;
     wc.limit_ns = g_wait_ns.load();
-    wc.inject_stall = 0;
+    wc.inject_stall = g_inject_stall.exchange(0);
     if ((W + 127) / 128 * static_cast<long long>(B) * H > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
     return from_cuda(txl::launch_relattn_bwd_tc128(tensor_map_encoder(), q, k, v, r, bias_u, bias_v, lse, o, dout,
                                                    dq, dk, dv, dr, dbias_u, dbias_v, B, W, M, H, n_r, scale,

@@ -97,6 +97,7 @@ struct ScoreParams {
   float scale, scale_log2e;
   unsigned int* status;
   unsigned long long wait_ns;
+  int inject_stall;  // test hook: the load thread loads nothing past the first two steps
 };
 
 struct SBars {
@@ -358,7 +359,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (loader) {
     // ============================ loads ===================================
     if (ok && T > 1) load_in(1);  // the raw q has been read: stage 1 is free
-    for (int t = 0; t + 2 < T && ok; ++t) {
+    for (int t = 0; t + 2 < T && ok && !p.inject_stall; ++t) {
       // step t's MMAs have read stage t & 1: refill it for step t + 2
       if (!(ok = mbar_wait(&bars->m1[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
       load_in(t + 2);
@@ -983,6 +984,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     p.scale_log2e = scale * kLog2e;
     p.status = wc.status;
     p.wait_ns = wc.limit_ns;
+    p.inject_stall = b0 == 0 ? wc.inject_stall : 0;
     const long long units = static_cast<long long>(p.nqt) * nb * H;
     if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, tk, tv, tr64, tdo128, tgk,

@@ -98,6 +98,7 @@ struct BwdParams {
   float scale, scale_log2e;
   unsigned int* status;
   unsigned long long wait_ns;
+  int inject_stall;  // test hook: the dq kernel's issuer loads nothing past the first two steps
 };
 
 struct QBars {
@@ -407,7 +408,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
         tc_fence_after();
         if (!(ok = score_mmas(t + 1))) break;
       }
-      if (t + 2 < T) {
+      if (t + 2 < T && !p.inject_stall) {
         // step t's gradient MMAs have read K and the window of stage t & 1
         if (!(ok = mbar_wait(&bars->m2[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
         issue_step_loads(t + 2);
@@ -906,6 +907,7 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   p.scale_log2e = scale * kLog2e;
   p.status = wc.status;
   p.wait_ns = wc.limit_ns;
+  p.inject_stall = wc.inject_stall;
   if ((e = cudaMemsetAsync(dr, 0, sizeof(float) * static_cast<size_t>(n_r) * H * D, stream)) != cudaSuccess)
     return e;
   const int units = p.nqt * B * H;
