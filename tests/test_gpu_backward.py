@@ -95,6 +95,7 @@ CASES = [
     (2, 2, 128, 200, 136, "bf16", 3),  # several tiles, ragged
     (1, 3, 128, 300, 512, "bf16", 0),  # memory longer than the segment
     (2, 1, 128, 7, 8, "bf16", 1),      # fewer rows than a warp
+    (3, 5, 128, 64, 0, "bf16", 7),     # odd head count, half a tile, empty memory
     # bf16, D = 128, memory not a multiple of 8: the CUDA-core kernels
     (1, 2, 128, 130, 37, "bf16", 0),
 ]
@@ -108,6 +109,25 @@ def test_backward_matches_oracle(txl, B, H, D, W, M, dtype, extra):
     want = O.relattn_backward(q, k, v, r, bu, bv, M, dout, scale)
     _compare(got, want, dtype)
     assert np.all(got["dr"][M + W:] == 0)
+
+
+@pytest.mark.parametrize("D,M", [(128, 8), (64, 0), (64, 8)])
+def test_backward_one_query_row(txl, D, M):
+    """W = 1: one softmax row over M + 1 keys.  dv = p dout has no
+    cancellation and meets the rel-L2 bound.  Every other gradient is built
+    from g = scale p (dout.v_j - Delta), whose difference nearly cancels when
+    the row has few keys (with M = 0 the exact gradient is zero); there the
+    bf16 o that Delta = dout.o takes from the forward decides the relative
+    error, so those gradients are held to the max |err| bound only."""
+    q, k, v, r, bu, bv, dout = _case(1, 1, D, 1, M, "bf16")
+    got = _run(txl, q, k, v, r, bu, bv, dout, M, "bf16")
+    want = O.relattn_backward(q, k, v, r, bu, bv, M, dout, D ** -0.5)
+    a, b = got["dv"].astype(np.float64), want["dv"]
+    assert np.linalg.norm(a - b) / np.linalg.norm(b) <= 5e-3
+    for key in KEYS:
+        a, b = got[key].astype(np.float64), want[key]
+        assert np.all(np.isfinite(a)), key
+        assert np.abs(a - b).max() <= 2e-2 * max(1.0, np.abs(b).max()), key
 
 
 def test_backward_fp32_output_gradient_with_bf16_inputs(txl):
