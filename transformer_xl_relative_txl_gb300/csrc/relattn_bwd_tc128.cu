@@ -21,12 +21,13 @@
 //      (q+u), (q+v) as the MMAs saw them.
 //   2. bgemm_kernel, this library's tcgen05 GEMM arranged for the five
 //      products (M = 128 rows of a tile, N = D = 128, fp32 accumulators in
-//      TMEM, fp32 results): dq_c = G K and dq_d = GS r per (batch, head);
+//      TMEM, fp32 results): dq = G K + GS r per (batch, head), the two parts
+//      in two accumulators of one tile, whose epilogue also writes each part's
+//      column sums over the tile's rows (the bias gradients' partials);
 //      dk = G^T (q+u) and dv = P^T dout over the segment keys (G and P read as
 //      MN-major A operands); dr = sum_b GS^T (q+v) per head (the k loop runs
 //      over every sequence's queries).
-//   3. bwd_sum128_kernel: dq = dq_c + dq_d, and the bias gradients as sums of
-//      dq_c and dq_d over (batch, query) in a fixed order.
+//   3. bwd_bias_kernel adds the partials in a fixed order into du, dv_bias.
 // The batch runs in chunks of sequences whose scratch fits a cap (1 GiB by
 // default); dr accumulates over the chunks.  Every result is deterministic.
 // Every wait is bounded; a timed-out wait raises the device status word and
@@ -480,31 +481,37 @@ constexpr int kGATile = 128 * 128;  // 16 KB
 constexpr int kGBBlock = 64 * 128;  // 8 KB
 constexpr int kGStage = kGATile + 2 * kGBBlock;
 constexpr int kGStages = 6;
-constexpr int kGOffBar = kGStages * kGStage;
+constexpr int kGOffEpi = kGStages * kGStage;      // DQ: 4 epilogue warps x 32 x 32 fp32 (column sums)
+constexpr int kGOffRed = kGOffEpi + 4 * 32 * 32 * 4;  // DQ: [4 warps][2 parts][128] warp sums
+constexpr int kGOffBar = kGOffRed + 4 * 2 * 128 * 4;
 constexpr int kGSmem = kGOffBar + 256 + 1024;
 constexpr int kGThreads = 192;
-constexpr uint32_t kGTmemCols = 2 * D;
 static_assert(kGSmem <= 232448, "shared memory budget");
+// TMEM: two accumulators; a DQ tile holds both of its parts (key, distance)
+template <int MODE>
+__host__ __device__ constexpr uint32_t gemm_tmem_cols() { return MODE == 0 ? 4 * D : 2 * D; }
 
 struct GemmArgs {
   int B, W, M, H, L;
   int BH, nmt, nkbW;  // output row blocks of 128; 64-deep blocks of the W queries
   int tiles;
-  float* out0;  // DQ: the key part of dq; DK: dk; DV: dv; DR: dr
-  float* out1;  // DQ: the distance part of dq
+  float* out0;  // DQ: dq; DK: dk; DV: dv; DR: dr
+  float* part;  // DQ: per (sequence, row block) column sums of both parts, [B*nmt][H][2][D]
   int accumulate;  // DR: add to out0 (a later chunk of sequences) instead of storing
   unsigned int* status;
   unsigned long long wait_ns;
 };
 
 struct GTile {
-  int z, part, m0, kb0, nkb;
+  int z, m0, kb0, nkb;
+  int nkb_c;  // DQ: k blocks of the key part (the distance part follows, as many)
 };
 
 // Tiles, longest k range first.
-//   DQ: (row block, batch-head, part): rows = queries; part 0 runs k over the
-//       keys [0, M + m0 + 128) (A = G, B = k), part 1 over the distances
-//       (A = GS, B = r); G and GS are zero past each row's last visible key.
+//   DQ: (row block, batch-head): rows = queries; k runs over the keys
+//       [0, M + m0 + 128) (A = G, B = k) into one accumulator, then over the
+//       same distances (A = GS, B = r) into a second; G and GS are zero past
+//       each row's last visible key.
 //   DK, DV: (row block, batch-head): rows = segment keys m, k = queries i from
 //       m0 on (key M + m is visible to queries i >= m only).
 //   DR: (row block, head): rows = distances d, k = (batch, query) pairs with
@@ -512,15 +519,13 @@ struct GTile {
 template <int MODE>
 __device__ __forceinline__ GTile gtile(const GemmArgs& p, int t) {
   GTile r;
-  r.part = 0;
+  r.nkb_c = 0;
   if (MODE == kModeDQ) {
-    const int per = 2 * p.BH;
-    r.m0 = (p.nmt - 1 - t / per) * 128;
-    const int rem = t % per;
-    r.z = rem >> 1;
-    r.part = rem & 1;
+    r.m0 = (p.nmt - 1 - t / p.BH) * 128;
+    r.z = t % p.BH;
     r.kb0 = 0;
-    r.nkb = (min(p.L, p.M + r.m0 + 128) + 63) / 64;
+    r.nkb_c = (min(p.L, p.M + r.m0 + 128) + 63) / 64;
+    r.nkb = 2 * r.nkb_c;
   } else if (MODE == kModeDK || MODE == kModeDV) {
     r.m0 = (t / p.BH) * 128;
     r.z = t % p.BH;
@@ -546,6 +551,7 @@ struct GBars {
 // Tensor maps per mode (all bf16, 128-byte swizzle, zero fill):
 //   DQ: a0 = G {L, W, B*H} box {64, 128, 1}, a1 = GS the same, b0 = k
 //       {D, H, L, B} box {64, 1, 64, 1}, b1 = r {D, H, n_r} box {64, 1, 64};
+//       dq = both parts, and the tile's column sums of each part to `part`;
 //   DK: a0 = G box {64, 64, 1}, b0 = q+u {D, H, W, B} box {64, 1, 64, 1};
 //   DV: a0 = P box {64, 64, 1}, b0 = dout as q+u;
 //   DR: a0 = GS box {64, 64, 1}, b0 = q+v as q+u.
@@ -577,7 +583,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, kGTmemCols);
+    tmem_alloc(&bars->tmem_base, gemm_tmem_cols<MODE>());
     tmem_relinquish();
   }
   tc_fence_before();
@@ -585,6 +591,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const uint64_t wait_ns = p.wait_ns;
+  constexpr uint32_t kAccCols = MODE == kModeDQ ? 2 * D : D;  // TMEM columns of one tile
 
   if (warp == 0) {
     // ============================ TMA producer ============================
@@ -609,8 +616,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
           uint64_t* bar = &bars->full[s];
           mbar_arrive_expect_tx(bar, kGStage);
           if (MODE == kModeDQ) {
-            const int k0 = 64 * kk;
-            if (g.part == 0) {
+            const bool dist = kk >= g.nkb_c;  // the distance part
+            const int k0 = 64 * (dist ? kk - g.nkb_c : kk);
+            if (!dist) {
               tma_load_3d(st, &tm_a0, bar, k0, g.m0, g.z);
               tma_load_4d(sb, &tm_b0, bar, 0, h, k0, b);
               tma_load_4d(sb + kGBBlock, &tm_b0, bar, 64, h, k0, b);
@@ -653,7 +661,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         const uint32_t acc = tl & 1;
         if (tl >= 2 && !(ok = mbar_wait(&bars->acc_empty[acc], ((tl >> 1) - 1) & 1, wait_ns, abort))) break;
         tc_fence_after();
-        const uint32_t d = tmem + acc * D;
+        const uint32_t d0 = tmem + acc * kAccCols;
         for (int kk = 0; kk < g.nkb; ++kk, ++it) {
           const int s = static_cast<int>(it % S);
           if (!(ok = mbar_wait(&bars->full[s], (it / S) & 1, wait_ns, abort))) break;
@@ -664,9 +672,14 @@ __global__ void __launch_bounds__(kGThreads, 1)
           // bytes apart, 16 k rows = 2 KB.
           const uint64_t da = kAmn ? sdesc_sw128(st, kGATile / 2, 1024) : sdesc_sw128(st, 16, 1024);
           const uint64_t db = sdesc_sw128(st + kGATile, kGBBlock, 1024);
+          // DQ: the key part into the tile's first D columns, the distance
+          // part into the next D
+          const bool second = MODE == kModeDQ && kk >= g.nkb_c;
+          const uint32_t d = d0 + (second ? D : 0);
+          const int kl = second ? kk - g.nkb_c : kk;  // k block within the part
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(d, da + (kAmn ? k * 128 : k * 2), db + k * 128, idesc, (kk > 0 || k > 0) ? 1u : 0u);
+            mma_ss(d, da + (kAmn ? k * 128 : k * 2), db + k * 128, idesc, (kl > 0 || k > 0) ? 1u : 0u);
           tc_commit(&bars->empty[s]);
         }
         if (!ok) break;
@@ -686,23 +699,85 @@ __global__ void __launch_bounds__(kGThreads, 1)
     for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tl) {
       const GTile g = gtile<MODE>(p, t);
       const uint32_t acc = tl & 1;
+      const int row = g.m0 + 32 * quad + lane;
+      if constexpr (MODE == kModeDQ) {
+        // The four epilogue warps leave together (they meet at named barriers).
+        ok = named_bar_and(2, 128, warp_wait(&bars->acc_full[acc], (tl >> 1) & 1, wait_ns, abort));
+        if (!ok) break;
+        tc_fence_after();
+        // dq = key part + distance part; the column sums of each part over
+        // the tile's rows (this warp's 32 through its staging tile, then the
+        // four warps in order) go to the bias partials.
+        float* swp = reinterpret_cast<float*>(smem + kGOffEpi) + quad * 32 * 32;
+        float* wred = reinterpret_cast<float*>(smem + kGOffRed);
+        const int b = g.z / p.H, h = g.z % p.H;
+        float* dst = row < p.W ? p.out0 + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D : nullptr;
+#pragma unroll 1
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t vc[32], vd[32];
+          tmem_ld32(tmem + lane_base + acc * kAccCols + 32 * c, vc);
+          tmem_ld32(tmem + lane_base + acc * kAccCols + D + 32 * c, vd);
+          tmem_wait_ld(vc);
+          tmem_wait_ld(vd);
+          if (c == D / 32 - 1) {
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+          }
+          if (dst != nullptr) {
+            float4* o4 = reinterpret_cast<float4*>(dst + 32 * c);
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              o4[j] = make_float4(__uint_as_float(vc[4 * j]) + __uint_as_float(vd[4 * j]),
+                                  __uint_as_float(vc[4 * j + 1]) + __uint_as_float(vd[4 * j + 1]),
+                                  __uint_as_float(vc[4 * j + 2]) + __uint_as_float(vd[4 * j + 2]),
+                                  __uint_as_float(vc[4 * j + 3]) + __uint_as_float(vd[4 * j + 3]));
+          }
+#pragma unroll
+          for (int part = 0; part < 2; ++part) {
+            const uint32_t(&v)[32] = part == 0 ? vc : vd;
+            __syncwarp();  // the last pass has read the staging tile
+            // row `lane` of the warp: 16-byte chunk j at chunk j ^ (lane & 7)
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              reinterpret_cast<float4*>(swp + lane * 32)[j ^ (lane & 7)] =
+                  make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                              __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
+            __syncwarp();
+            float sum = 0.f;  // column `lane` of the chunk over the warp's rows, in row order
+#pragma unroll 8
+            for (int r = 0; r < 32; ++r) sum += swp[r * 32 + ((((lane >> 2) ^ (r & 7))) << 2) + (lane & 3)];
+            wred[(quad * 2 + part) * 128 + 32 * c + lane] = sum;
+          }
+        }
+        named_bar_sync(2, 128);
+        {
+          const int et = threadIdx.x - 64;  // epilogue thread 0 .. 127: one column of each part
+          float* pp = p.part + ((static_cast<size_t>(b) * p.nmt + g.m0 / 128) * p.H + h) * 2 * D;
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+            pp[part * D + et] = ((wred[(0 * 2 + part) * 128 + et] + wred[(1 * 2 + part) * 128 + et]) +
+                                 wred[(2 * 2 + part) * 128 + et]) +
+                                wred[(3 * 2 + part) * 128 + et];
+        }
+        named_bar_sync(2, 128);  // the sums are read before the next tile writes them
+        continue;
+      }
       if (!(ok = warp_wait(&bars->acc_full[acc], (tl >> 1) & 1, wait_ns, abort))) break;
       tc_fence_after();
-      const int row = g.m0 + 32 * quad + lane;
       float* dst = nullptr;
       if (row < rows) {
         if (MODE == kModeDR) {
           dst = p.out0 + (static_cast<size_t>(row) * p.H + g.z) * D;
         } else {
           const int b = g.z / p.H, h = g.z % p.H;
-          float* out = (MODE == kModeDQ && g.part == 1) ? p.out1 : p.out0;
-          dst = out + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D;
+          dst = p.out0 + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D;
         }
       }
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + acc * D + 32 * c, v);
+        tmem_ld32(tmem + lane_base + acc * kAccCols + 32 * c, v);
         tmem_wait_ld(v);
         if (c == D / 32 - 1) {
           tc_fence_before();
@@ -736,52 +811,9 @@ __global__ void __launch_bounds__(kGThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, kGTmemCols);
+    tmem_dealloc(tmem, gemm_tmem_cols<MODE>());
   }
 }
-
-// ---------------------------------------------------------------------------
-// 3. dq and the bias gradients
-// ---------------------------------------------------------------------------
-// dq = dq_c + dq_d over rows of H*D floats; block y sums rows
-// [y * rows_per, (y + 1) * rows_per) of both parts per column, in order, into
-// part [y][h][0 | 1][D] (d(q+u), then d(q+v)).
-__global__ void bwd_sum128_kernel(const float4* __restrict__ dqc, const float4* __restrict__ dqd,
-                                  float4* __restrict__ dq, float* __restrict__ part, long long rows, int cols4,
-                                  int rows_per) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols4) return;
-  const long long r0 = static_cast<long long>(blockIdx.y) * rows_per;
-  const long long r1 = min(rows, r0 + rows_per);
-  float4 su = make_float4(0.f, 0.f, 0.f, 0.f), sv = su;
-  auto add_row = [&](size_t o, float4 a, float4 b) {
-    dq[o] = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-    su = make_float4(su.x + a.x, su.y + a.y, su.z + a.z, su.w + a.w);
-    sv = make_float4(sv.x + b.x, sv.y + b.y, sv.z + b.z, sv.w + b.w);
-  };
-  long long r = r0;
-  for (; r + 8 <= r1; r += 8) {  // eight rows' loads in flight, then the sums in row order
-    float4 a[8], b[8];
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-      const size_t o = static_cast<size_t>(r + k) * cols4 + c;
-      a[k] = dqc[o];
-      b[k] = dqd[o];
-    }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) add_row(static_cast<size_t>(r + k) * cols4 + c, a[k], b[k]);
-  }
-  for (; r < r1; ++r) {
-    const size_t o = static_cast<size_t>(r) * cols4 + c;
-    add_row(o, dqc[o], dqd[o]);
-  }
-  const int h = (4 * c) / D, d = (4 * c) % D;
-  float* pp = part + ((static_cast<size_t>(blockIdx.y) * (cols4 * 4 / D) + h) * 2) * D + d;
-  *reinterpret_cast<float4*>(pp) = su;
-  *reinterpret_cast<float4*>(pp + D) = sv;
-}
-
-constexpr int kSumRows = 32;
 
 int num_sms() {
   static std::atomic<int> cached[64];
@@ -799,7 +831,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
 struct Scratch128 {
   __nv_bfloat16 *G, *P, *GS, *Qu, *Qv;
-  float *dqc, *dqd, *part;
+  float* part;
   size_t bytes;
 };
 
@@ -819,8 +851,6 @@ Scratch128 carve(void* base, int Bc, int W, int M, int H, size_t n_part) {
   s.GS = reinterpret_cast<__nv_bfloat16*>(take(bh * W * LP * 2));
   s.Qu = reinterpret_cast<__nv_bfloat16*>(take(bwhd * 2));
   s.Qv = reinterpret_cast<__nv_bfloat16*>(take(bwhd * 2));
-  s.dqc = reinterpret_cast<float*>(take(bwhd * 4));
-  s.dqd = reinterpret_cast<float*>(take(bwhd * 4));
   s.part = reinterpret_cast<float*>(take(n_part * H * 2 * D * 4));
   s.bytes = off;
   return s;
@@ -836,18 +866,8 @@ int chunk_seqs(int B, int W, int M, int H) {
   return static_cast<int>(std::max<size_t>(1, std::min<size_t>(c, static_cast<size_t>(B))));
 }
 
-// Rows of one bias-partial block for a chunk of `rows` rows: 32, or more
-// when the chunk would need more than 65535 blocks (the grid's y limit).
-long long rows_per_block(long long rows) { return std::max<long long>(kSumRows, (rows + 65534) / 65535); }
-
-size_t total_parts(int B, int W, int Bc) {
-  size_t n = 0;
-  for (int b0 = 0; b0 < B; b0 += Bc) {
-    const long long rows = static_cast<long long>(std::min(Bc, B - b0)) * W;
-    n += static_cast<size_t>((rows + rows_per_block(rows) - 1) / rows_per_block(rows));
-  }
-  return n;
-}
+// Bias partials: one per (sequence, 128-row block) of every chunk.
+size_t total_parts(int B, int W) { return static_cast<size_t>(B) * ((W + 127) / 128); }
 
 template <int MODE>
 cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
@@ -863,7 +883,7 @@ cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUte
       return e;
     attr_done[dev].store(true);
   }
-  if (MODE == kModeDQ) p.tiles = 2 * p.BH * p.nmt;
+  if (MODE == kModeDQ) p.tiles = p.BH * p.nmt;
   else if (MODE == kModeDR) p.tiles = p.H * p.nmt;
   else p.tiles = p.BH * p.nmt;
   const int grid = min(p.tiles, num_sms());
@@ -877,7 +897,7 @@ void relattn_bwd_tc128_set_chunk_bytes(size_t bytes) { g_chunk_cap.store(bytes =
 
 size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H) {
   const int Bc = chunk_seqs(B, W, M, H);
-  return carve(nullptr, Bc, W, M, H, total_parts(B, W, Bc)).bytes;
+  return carve(nullptr, Bc, W, M, H, total_parts(B, W)).bytes;
 }
 
 bool relattn_bwd_tc128_supported(int W, int M) { return W > 0 && M % 8 == 0; }
@@ -890,7 +910,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
   if (encode == nullptr || !relattn_bwd_tc128_supported(W, M)) return cudaErrorInvalidValue;
   const int L = M + W, LP = (L + 63) / 64 * 64;
   const int Bc = chunk_seqs(B, W, M, H);
-  const Scratch128 sc = carve(scratch, Bc, W, M, H, total_parts(B, W, Bc));
+  const Scratch128 sc = carve(scratch, Bc, W, M, H, total_parts(B, W));
   const cuuint64_t hd2 = static_cast<cuuint64_t>(H) * D * 2;
   bool ok = true;
   auto enc = [&](CUtensorMap* m, const void* base, int rank, std::initializer_list<cuuint64_t> dims,
@@ -942,8 +962,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
   }
   const size_t seg = static_cast<size_t>(W) * H * D;      // one sequence of q, o, dout, dq, dk, dv
   const size_t mem = static_cast<size_t>(L) * H * D;      // one sequence of k, v
-  const int cols4 = H * D / 4;
-  size_t p_off = 0;  // bias partials written so far
+  const int nmt = (W + 127) / 128;
   int last_nb = -1;
   for (int b0 = 0; b0 < B; b0 += Bc) {
     const int nb = std::min(Bc, B - b0);
@@ -1004,8 +1023,8 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     g.accumulate = 0;
     g.status = wc.status;
     g.wait_ns = wc.limit_ns;
-    g.out0 = sc.dqc;
-    g.out1 = sc.dqd;
+    g.out0 = dq + b0 * seg;
+    g.part = sc.part + static_cast<size_t>(b0) * nmt * H * 2 * D;
     if ((e = launch_gemm<kModeDQ>(tgk, tgsk, tk, tr64, g, stream)) != cudaSuccess) return e;
     g.out0 = dk + b0 * seg;
     if ((e = launch_gemm<kModeDK>(tgmn, tgmn, tqu, tqu, g, stream)) != cudaSuccess) return e;
@@ -1015,23 +1034,14 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     g.nmt = (L + 127) / 128;
     g.accumulate = b0 > 0;
     if ((e = launch_gemm<kModeDR>(tgsmn, tgsmn, tqv, tqv, g, stream)) != cudaSuccess) return e;
-    // 3. dq of the chunk and its bias partials
-    const long long rows = static_cast<long long>(nb) * W;
-    const long long rows_per = rows_per_block(rows);
-    const long long n_part = (rows + rows_per - 1) / rows_per;
-    const dim3 grid((cols4 + 255) / 256, static_cast<unsigned>(n_part));
-    bwd_sum128_kernel<<<grid, 256, 0, stream>>>(
-        reinterpret_cast<const float4*>(sc.dqc), reinterpret_cast<const float4*>(sc.dqd),
-        reinterpret_cast<float4*>(dq + b0 * seg), sc.part + p_off * H * 2 * D, rows, cols4, static_cast<int>(rows_per));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    p_off += static_cast<size_t>(n_part);
   }
   if (n_r > L &&
       (e = cudaMemsetAsync(dr + static_cast<size_t>(L) * H * D, 0, static_cast<size_t>(n_r - L) * H * D * 4,
                            stream)) != cudaSuccess)
     return e;
-  if (p_off > 0x7FFFFFFF) return cudaErrorInvalidValue;
-  return launch_bwd_bias(sc.part, static_cast<int>(p_off), H, D, du, dvb, stream);
+  const size_t n_part = total_parts(B, W);
+  if (n_part > 0x7FFFFFFF) return cudaErrorInvalidValue;
+  return launch_bwd_bias(sc.part, static_cast<int>(n_part), H, D, du, dvb, stream);
 }
 
 }  // namespace txl
