@@ -462,16 +462,17 @@ TXL_API int txl_stack_forward(const void* h, void* out, int n_layers, void* cons
  * fp32 atomic adds, so its last bits may differ between calls.  The same
  * inputs with D = 128 and M a multiple of 8 also run on the tensor cores: a
  * kernel rebuilds p and g per 64-key step and writes them in bf16 to scratch
- * (g in key and in distance order, p in key order), five tcgen05 products
- * then form dq (key and distance parts), dk, dv and dr, and ordered sums the
- * bias gradients; deterministic.  Every other case runs on CUDA cores in
+ * (g in key and in distance order, p in key order), tcgen05 products then
+ * form dq (key and distance parts in one tile, with the bias gradients'
+ * partials), dk, dv and dr, and an ordered sum the bias gradients;
+ * deterministic.  Every other case runs on CUDA cores in
  * fp32 arithmetic, fully deterministic.
  * Allocates: per-(device, stream) scratch (see the conventions above): for
  * D = 64 the per-row Delta and the per-tile partial sums; for the D = 128
  * tensor-core path, per chunk of Bc sequences, 3 * Bc*H*W*LP * 2 bytes of
- * pair terms (LP = M + W rounded up to 64) plus (q+u), (q+v) in bf16 and the
- * two dq parts in fp32 (2 * Bc*W*H*D * 6 bytes), Bc the most sequences that
- * fit 1 GiB (at least one; the chunks run in turn): all 8 sequences, 0.5 GB,
+ * pair terms (LP = M + W rounded up to 64) plus (q+u), (q+v) in bf16
+ * (2 * Bc*W*H*D * 2 bytes), and the bias partials, Bc the most sequences that
+ * fit 1 GiB (at least one; the chunks run in turn): all 8 sequences, 0.47 GB,
  * at B=8 H=8 W=M=768.
  */
 TXL_API int txl_relattn_backward(const void* q, const void* k, const void* v, const void* r,
