@@ -81,3 +81,31 @@ def test_static_allocates_nothing(txl):
     assert txl.txl_get_device_status() == 0
     assert free1 == free0
     assert free2 < free1
+
+
+def test_static_split_captured_and_replayed(txl):
+    """The static entry point captured into a CUDA graph on a split launch
+    (64 units, key ranges split across CTAs) and replayed twice: each replay
+    equals the eager forward bit for bit, so the merge counters the launch
+    uses are back at zero after every replay.  One ordinary call comes first
+    (it resolves the library's device symbols, which may load device code)."""
+    B, H, D, W, M = 4, 16, 64, 128, 1600
+    q, k, v, r, bu, bv = _inputs(B, H, D, W, M)
+    o_ref = torch.empty(q.shape, device=dev(), dtype=torch.bfloat16)
+    l_ref = torch.empty(B, H, W, device=dev(), dtype=torch.float32)
+    txl.txl_relattn_forward(q, k, v, r, bu, bv, o_ref, l_ref, M=M)
+    o = torch.empty_like(o_ref)
+    lse = torch.empty_like(l_ref)
+    txl.txl_relattn_forward_static(q, k, v, r, bu, bv, o, lse, M=M)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        txl.txl_relattn_forward_static(q, k, v, r, bu, bv, o, lse, M=M)
+    for _ in range(2):
+        o.zero_()
+        lse.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert txl.txl_get_device_status() == 0
+        assert torch.equal(o, o_ref)
+        assert torch.equal(lse, l_ref)

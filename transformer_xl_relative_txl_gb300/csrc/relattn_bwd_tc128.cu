@@ -19,14 +19,15 @@
 //      the forward.  It writes, in bf16, G [bh][i][j] and P [bh][i][j] (key
 //      order), GS [bh][i][d] (the same g in distance order, d = M+i-j), and
 //      (q+u), (q+v) as the MMAs saw them.
-//   2. bgemm_kernel, this library's tcgen05 GEMM arranged for the five
-//      products (M = 128 rows of a tile, N = D = 128, fp32 accumulators in
-//      TMEM, fp32 results): dq = G K + GS r per (batch, head), the two parts
-//      in two accumulators of one tile, whose epilogue also writes each part's
-//      column sums over the tile's rows (the bias gradients' partials);
-//      dk = G^T (q+u) and dv = P^T dout over the segment keys (G and P read as
-//      MN-major A operands); dr = sum_b GS^T (q+v) per head (the k loop runs
-//      over every sequence's queries).
+//   2. bgemm_kernel, this library's tcgen05 GEMM arranged for the products
+//      (M = 128 rows of a tile, N = D = 128, fp32 accumulators in TMEM, fp32
+//      results), all four in one launch whose CTAs take tiles from a counter:
+//      dq = G K + GS r per (batch, head), the two parts in two accumulators of
+//      one tile, whose epilogue also writes each part's column sums over the
+//      tile's rows (the bias gradients' partials); dk = G^T (q+u) and
+//      dv = P^T dout over the segment keys (G and P read as MN-major A
+//      operands); dr = sum_b GS^T (q+v) per head (the k loop runs over every
+//      sequence's queries).
 //   3. bwd_bias_kernel adds the partials in a fixed order into du, dv_bias.
 // The batch runs in chunks of sequences whose scratch fits a cap (1 GiB by
 // default); dr accumulates over the chunks.  Every result is deterministic.
@@ -99,6 +100,7 @@ struct ScoreParams {
   unsigned int* status;
   unsigned long long wait_ns;
   int inject_stall;  // test hook: the load thread loads nothing past the first two steps
+  unsigned int* gemm_ctr;  // the products' tile counter, zeroed here for the launch that follows
 };
 
 struct SBars {
@@ -198,6 +200,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   auto wbase = [&](int t) { return p.M + w.i0 - BN * t - BN; };
 
   if (tid == 0) {
+    if (blockIdx.x == 0) *p.gemm_ctr = 0u;  // read by the next launch on the stream only
     mbar_init(&bars->q, 1);
     mbar_init(&bars->in[0], 1);
     mbar_init(&bars->in[1], 1);
@@ -471,95 +474,124 @@ __global__ void __launch_bounds__(kSThreads, 1)
 // ---------------------------------------------------------------------------
 // 2. The gradient products
 // ---------------------------------------------------------------------------
-// One persistent CTA per SM, 192 threads: warp 0 loads (TMA), warp 1 issues
-// the MMAs (M = 128, N = D = 128, K = 16, into one of two TMEM accumulators),
-// warps 2-5 move the fp32 accumulator rows to global memory.  A stage holds
-// 64 k of A (a 128 x 64 K-major tile, or two 64 k x 64 row MN-major tiles)
-// and of B (two 64 k x 64 column N-major tiles).
+// One persistent launch runs all four products, one CTA per SM, 192 threads:
+// warp 0 loads (TMA), warp 1 issues the MMAs (M = 128, N = D = 128, K = 16,
+// into one of two TMEM accumulator slots), warps 2-5 move the fp32
+// accumulator rows to global memory.  A stage holds 64 k of A (a 128 x 64
+// K-major tile, or two 64 k x 64 row MN-major tiles) and of B (two 64 k x 64
+// column N-major tiles).
+//
+// The tiles of the four products differ in length by up to 48 times (a DR
+// tile streams every sequence's queries, a DK tile near the end of the
+// segment two k blocks), and the products do not depend on one another, so
+// the CTAs take tiles from a device counter, longest kinds first: a CTA that
+// finishes early takes the next tile, and the launch ends within about one
+// short tile of the average load.  Which CTA runs a tile does not change its
+// arithmetic: every output element is written by exactly one tile.
 enum BMode { kModeDQ = 0, kModeDK = 1, kModeDV = 2, kModeDR = 3 };
 constexpr int kGATile = 128 * 128;  // 16 KB
 constexpr int kGBBlock = 64 * 128;  // 8 KB
 constexpr int kGStage = kGATile + 2 * kGBBlock;
 constexpr int kGStages = 6;
-constexpr int kGOffEpi = kGStages * kGStage;      // DQ: 4 epilogue warps x 32 x 32 fp32 (column sums)
+constexpr int kGTq = 8;  // slots of the tile-index queue from the loader to the MMA and epilogue warps
+constexpr int kGOffEpi = kGStages * kGStage;          // DQ: 4 epilogue warps x 32 x 32 fp32 (column sums)
 constexpr int kGOffRed = kGOffEpi + 4 * 32 * 32 * 4;  // DQ: [4 warps][2 parts][128] warp sums
 constexpr int kGOffBar = kGOffRed + 4 * 2 * 128 * 4;
-constexpr int kGSmem = kGOffBar + 256 + 1024;
+constexpr int kGSmem = kGOffBar + 512 + 1024;
 constexpr int kGThreads = 192;
 static_assert(kGSmem <= 232448, "shared memory budget");
-// TMEM: two accumulators; a DQ tile holds both of its parts (key, distance)
-template <int MODE>
-__host__ __device__ constexpr uint32_t gemm_tmem_cols() { return MODE == 0 ? 4 * D : 2 * D; }
+// TMEM: two accumulator slots of 2 D columns; a DQ tile fills its slot with
+// both of its parts (key, distance), the other products use the first D.
+constexpr uint32_t kGAccCols = 2 * D;
+constexpr uint32_t kGTmemCols = 2 * kGAccCols;
 
 struct GemmArgs {
   int B, W, M, H, L;
-  int BH, nmt, nkbW;  // output row blocks of 128; 64-deep blocks of the W queries
-  int tiles;
-  float* out0;  // DQ: dq; DK: dk; DV: dv; DR: dr
-  float* part;  // DQ: per (sequence, row block) column sums of both parts, [B*nmt][H][2][D]
-  int accumulate;  // DR: add to out0 (a later chunk of sequences) instead of storing
+  int BH, nmt, nmtL, nkbW;  // row blocks of 128 queries, of 128 distances; 64-deep blocks of the W queries
+  int nDR, nDQ;             // tiles of the DR and DQ kinds; DK and DV follow, interleaved
+  int total;                // all tiles
+  float* dq;
+  float* dk;
+  float* dv;
+  float* dr;
+  float* part;     // per (sequence, row block) column sums of both dq parts, [B*nmt][H][2][D]
+  int accumulate;  // add to dr (a later chunk of sequences) instead of storing
+  unsigned int* ctr;  // tile counter: zero when the launch starts
   unsigned int* status;
   unsigned long long wait_ns;
 };
 
 struct GTile {
-  int z, m0, kb0, nkb;
+  int mode, z, m0, kb0, nkb;
   int nkb_c;  // DQ: k blocks of the key part (the distance part follows, as many)
 };
 
-// Tiles, longest k range first.
-//   DQ: (row block, batch-head): rows = queries; k runs over the keys
-//       [0, M + m0 + 128) (A = G, B = k) into one accumulator, then over the
-//       same distances (A = GS, B = r) into a second; G and GS are zero past
-//       each row's last visible key.
-//   DK, DV: (row block, batch-head): rows = segment keys m, k = queries i from
-//       m0 on (key M + m is visible to queries i >= m only).
-//   DR: (row block, head): rows = distances d, k = (batch, query) pairs with
-//       i >= d - M (GS is zero elsewhere).
-template <int MODE>
-__device__ __forceinline__ GTile gtile(const GemmArgs& p, int t) {
+// Tile u of the launch, in the order the counter hands them out: DR tiles
+// (rows = distances d of a head, k = (sequence, query) pairs with i >= d - M,
+// where GS is not zero), then DQ tiles (rows = queries of a sequence and head;
+// k runs over the keys [0, M + m0 + 128) with A = G, B = k into the slot's
+// first accumulator, then over the same distances with A = GS, B = r into its
+// second; G and GS are zero past each row's last visible key), then DK and DV
+// tiles in turn (rows = segment keys m; k = queries i from m0 on, since key
+// M + m is visible to queries i >= m only).  Each kind runs longest first.
+__device__ __forceinline__ GTile gtile(const GemmArgs& p, int u) {
   GTile r;
   r.nkb_c = 0;
-  if (MODE == kModeDQ) {
-    r.m0 = (p.nmt - 1 - t / p.BH) * 128;
-    r.z = t % p.BH;
+  if (u < p.nDR) {
+    r.mode = kModeDR;
+    r.m0 = (u / p.H) * 128;
+    r.z = u % p.H;
+    r.kb0 = max(0, r.m0 - p.M) / 64;
+    r.nkb = p.B * (p.nkbW - r.kb0);
+    return r;
+  }
+  u -= p.nDR;
+  if (u < p.nDQ) {
+    r.mode = kModeDQ;
+    r.m0 = (p.nmt - 1 - u / p.BH) * 128;
+    r.z = u % p.BH;
     r.kb0 = 0;
     r.nkb_c = (min(p.L, p.M + r.m0 + 128) + 63) / 64;
     r.nkb = 2 * r.nkb_c;
-  } else if (MODE == kModeDK || MODE == kModeDV) {
-    r.m0 = (t / p.BH) * 128;
-    r.z = t % p.BH;
-    r.kb0 = r.m0 / 64;
-    r.nkb = p.nkbW - r.kb0;
-  } else {
-    r.m0 = (t / p.H) * 128;
-    r.z = t % p.H;
-    r.kb0 = max(0, r.m0 - p.M) / 64;
-    r.nkb = p.B * (p.nkbW - r.kb0);
+    return r;
   }
+  u -= p.nDQ;
+  r.mode = (u & 1) ? kModeDV : kModeDK;
+  u >>= 1;
+  r.m0 = (u / p.BH) * 128;
+  r.z = u % p.BH;
+  r.kb0 = r.m0 / 64;
+  r.nkb = p.nkbW - r.kb0;
   return r;
 }
 
 struct GBars {
   uint64_t full[kGStages], empty[kGStages];
   uint64_t acc_full[2], acc_empty[2];
+  uint64_t tq_full[kGTq], tq_empty[kGTq];
   uint64_t done;
   uint32_t tmem_base;
   int abort;
+  int tq[kGTq];
+};
+static_assert(sizeof(GBars) <= 512, "barrier block");
+
+// Tensor maps (all bf16, 128-byte swizzle, zero fill):
+//   a_g, a_gs: G and GS {L, W, B*H} box {64, 128, 1} (DQ, K-major);
+//   b_k: k {D, H, L, B} box {64, 1, 64, 1}; b_r: r {D, H, n_r} box {64, 1, 64};
+//   m_g, m_p, m_gs: G, P, GS box {64, 64, 1} (DK, DV, DR: MN-major A);
+//   b_qu, b_do, b_qv: q+u, dout, q+v {D, H, W, B} box {64, 1, 64, 1}.
+struct GMaps {
+  CUtensorMap a_g, a_gs, b_k, b_r, m_g, m_p, m_gs, b_qu, b_do, b_qv;
 };
 
-// Tensor maps per mode (all bf16, 128-byte swizzle, zero fill):
-//   DQ: a0 = G {L, W, B*H} box {64, 128, 1}, a1 = GS the same, b0 = k
-//       {D, H, L, B} box {64, 1, 64, 1}, b1 = r {D, H, n_r} box {64, 1, 64};
-//       dq = both parts, and the tile's column sums of each part to `part`;
-//   DK: a0 = G box {64, 64, 1}, b0 = q+u {D, H, W, B} box {64, 1, 64, 1};
-//   DV: a0 = P box {64, 64, 1}, b0 = dout as q+u;
-//   DR: a0 = GS box {64, 64, 1}, b0 = q+v as q+u.
-template <int MODE>
+// Queue slot n % kGTq of the tile-index queue: the loader writes tile indices
+// in the order it takes them; the MMA thread and each epilogue warp read
+// every one, the last (>= total) telling them to stop.
+__device__ __forceinline__ int tq_read(GBars* bars, uint32_t n) { return *reinterpret_cast<volatile int*>(&bars->tq[n % kGTq]); }
+
 __global__ void __launch_bounds__(kGThreads, 1)
-    bgemm_kernel(const __grid_constant__ CUtensorMap tm_a0, const __grid_constant__ CUtensorMap tm_a1,
-                 const __grid_constant__ CUtensorMap tm_b0, const __grid_constant__ CUtensorMap tm_b1,
-                 const GemmArgs p) {
+    bgemm_kernel(const __grid_constant__ GMaps maps, const GemmArgs p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -567,7 +599,6 @@ __global__ void __launch_bounds__(kGThreads, 1)
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   constexpr int S = kGStages;
-  constexpr bool kAmn = MODE != kModeDQ;  // A read transposed (MN-major)
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -578,12 +609,16 @@ __global__ void __launch_bounds__(kGThreads, 1)
       mbar_init(&bars->acc_full[a], 1);
       mbar_init(&bars->acc_empty[a], 4);
     }
+    for (int q = 0; q < kGTq; ++q) {
+      mbar_init(&bars->tq_full[q], 1);
+      mbar_init(&bars->tq_empty[q], 5);  // the MMA thread and the four epilogue warps
+    }
     mbar_init(&bars->done, 1);
     bars->abort = 0;
     fence_mbar_init();
   }
   if (warp == 1) {
-    tmem_alloc(&bars->tmem_base, gemm_tmem_cols<MODE>());
+    tmem_alloc(&bars->tmem_base, kGTmemCols);
     tmem_relinquish();
   }
   tc_fence_before();
@@ -591,23 +626,31 @@ __global__ void __launch_bounds__(kGThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const uint64_t wait_ns = p.wait_ns;
-  constexpr uint32_t kAccCols = MODE == kModeDQ ? 2 * D : D;  // TMEM columns of one tile
 
   if (warp == 0) {
     // ============================ TMA producer ============================
     if (lane == 0) {
-      tma_prefetch_desc(&tm_a0);
-      tma_prefetch_desc(&tm_b0);
-      if (MODE == kModeDQ) {
-        tma_prefetch_desc(&tm_a1);
-        tma_prefetch_desc(&tm_b1);
-      }
-      uint32_t it = 0;
+      tma_prefetch_desc(&maps.a_g);
+      tma_prefetch_desc(&maps.a_gs);
+      tma_prefetch_desc(&maps.m_gs);
+      tma_prefetch_desc(&maps.b_qv);
+      uint32_t it = 0, n = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
-        const GTile g = gtile<MODE>(p, t);
-        const int b = MODE == kModeDR ? 0 : g.z / p.H, h = MODE == kModeDR ? g.z : g.z % p.H;
+      unsigned int next = atomicAdd(p.ctr, 1u);
+      while (ok) {
+        const int u = static_cast<int>(min(next, static_cast<unsigned int>(p.total)));
+        // hand the tile index on; the slot is free once its last reader is done
+        if (!(ok = mbar_wait(&bars->tq_empty[n % kGTq], ((n / kGTq) & 1) ^ 1, wait_ns, abort))) break;
+        bars->tq[n % kGTq] = u;
+        mbar_arrive(&bars->tq_full[n % kGTq]);
+        ++n;
+        if (u >= p.total) break;
+        next = atomicAdd(p.ctr, 1u);  // the tile after this one, fetched while this one loads
+        const GTile g = gtile(p, u);
+        const int b = g.mode == kModeDR ? 0 : g.z / p.H, h = g.mode == kModeDR ? g.z : g.z % p.H;
         const int nq = p.nkbW - g.kb0;  // DR: k blocks per sequence
+        const CUtensorMap* ma = g.mode == kModeDK ? &maps.m_g : g.mode == kModeDV ? &maps.m_p : &maps.m_gs;
+        const CUtensorMap* mb = g.mode == kModeDK ? &maps.b_qu : g.mode == kModeDV ? &maps.b_do : &maps.b_qv;
         for (int kk = 0; kk < g.nkb; ++kk, ++it) {
           const int s = static_cast<int>(it % S);
           if (!(ok = mbar_wait(&bars->empty[s], ((it / S) & 1) ^ 1, wait_ns, abort))) break;
@@ -615,31 +658,31 @@ __global__ void __launch_bounds__(kGThreads, 1)
           uint8_t* sb = st + kGATile;
           uint64_t* bar = &bars->full[s];
           mbar_arrive_expect_tx(bar, kGStage);
-          if (MODE == kModeDQ) {
+          if (g.mode == kModeDQ) {
             const bool dist = kk >= g.nkb_c;  // the distance part
             const int k0 = 64 * (dist ? kk - g.nkb_c : kk);
             if (!dist) {
-              tma_load_3d(st, &tm_a0, bar, k0, g.m0, g.z);
-              tma_load_4d(sb, &tm_b0, bar, 0, h, k0, b);
-              tma_load_4d(sb + kGBBlock, &tm_b0, bar, 64, h, k0, b);
+              tma_load_3d(st, &maps.a_g, bar, k0, g.m0, g.z);
+              tma_load_4d(sb, &maps.b_k, bar, 0, h, k0, b);
+              tma_load_4d(sb + kGBBlock, &maps.b_k, bar, 64, h, k0, b);
             } else {
-              tma_load_3d(st, &tm_a1, bar, k0, g.m0, g.z);
-              tma_load_3d(sb, &tm_b1, bar, 0, h, k0);
-              tma_load_3d(sb + kGBBlock, &tm_b1, bar, 64, h, k0);
+              tma_load_3d(st, &maps.a_gs, bar, k0, g.m0, g.z);
+              tma_load_3d(sb, &maps.b_r, bar, 0, h, k0);
+              tma_load_3d(sb + kGBBlock, &maps.b_r, bar, 64, h, k0);
             }
           } else {
             int bb = b, k0 = 64 * (g.kb0 + kk), x0 = g.m0, zz = g.z;
-            if (MODE == kModeDR) {
+            if (g.mode == kModeDR) {
               bb = kk / nq;
               k0 = 64 * (g.kb0 + kk % nq);
               zz = bb * p.H + h;
             } else {
               x0 = p.M + g.m0;  // key columns of G and P
             }
-            tma_load_3d(st, &tm_a0, bar, x0, k0, zz);
-            tma_load_3d(st + kGATile / 2, &tm_a0, bar, x0 + 64, k0, zz);
-            tma_load_4d(sb, &tm_b0, bar, 0, h, k0, bb);
-            tma_load_4d(sb + kGBBlock, &tm_b0, bar, 64, h, k0, bb);
+            tma_load_3d(st, ma, bar, x0, k0, zz);
+            tma_load_3d(st + kGATile / 2, ma, bar, x0 + 64, k0, zz);
+            tma_load_4d(sb, mb, bar, 0, h, k0, bb);
+            tma_load_4d(sb + kGBBlock, mb, bar, 64, h, k0, bb);
           }
         }
       }
@@ -652,16 +695,24 @@ __global__ void __launch_bounds__(kGThreads, 1)
   } else if (warp == 1) {
     // ============================ MMA issuer ==============================
     if (lane == 0) {
-      constexpr uint32_t idesc = idesc_bf16(128, D, kAmn, true);
+      // A K-major for DQ (rows = queries, k = keys or distances), MN-major for
+      // the others (A is G, P or GS read transposed)
+      constexpr uint32_t idesc_k = idesc_bf16(128, D, false, true);
+      constexpr uint32_t idesc_mn = idesc_bf16(128, D, true, true);
       const uint32_t base = smem_u32(smem);
       uint32_t it = 0, tl = 0;
       bool ok = true;
-      for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x, ++tl) {
-        const GTile g = gtile<MODE>(p, t);
+      for (uint32_t n = 0; ok; ++n, ++tl) {
+        if (!(ok = mbar_wait(&bars->tq_full[n % kGTq], (n / kGTq) & 1, wait_ns, abort))) break;
+        const int u = tq_read(bars, n);
+        mbar_arrive(&bars->tq_empty[n % kGTq]);
+        if (u >= p.total) break;
+        const GTile g = gtile(p, u);
+        const bool amn = g.mode != kModeDQ;
         const uint32_t acc = tl & 1;
         if (tl >= 2 && !(ok = mbar_wait(&bars->acc_empty[acc], ((tl >> 1) - 1) & 1, wait_ns, abort))) break;
         tc_fence_after();
-        const uint32_t d0 = tmem + acc * kAccCols;
+        const uint32_t d0 = tmem + acc * kGAccCols;
         for (int kk = 0; kk < g.nkb; ++kk, ++it) {
           const int s = static_cast<int>(it % S);
           if (!(ok = mbar_wait(&bars->full[s], (it / S) & 1, wait_ns, abort))) break;
@@ -670,16 +721,17 @@ __global__ void __launch_bounds__(kGThreads, 1)
           // K-major A: 8-row groups 1024 bytes apart, 32 bytes per 16 k.
           // MN-major A and B: 64-wide blocks 8 KB apart, 8-k-row groups 1024
           // bytes apart, 16 k rows = 2 KB.
-          const uint64_t da = kAmn ? sdesc_sw128(st, kGATile / 2, 1024) : sdesc_sw128(st, 16, 1024);
+          const uint64_t da = amn ? sdesc_sw128(st, kGATile / 2, 1024) : sdesc_sw128(st, 16, 1024);
           const uint64_t db = sdesc_sw128(st + kGATile, kGBBlock, 1024);
-          // DQ: the key part into the tile's first D columns, the distance
+          // DQ: the key part into the slot's first D columns, the distance
           // part into the next D
-          const bool second = MODE == kModeDQ && kk >= g.nkb_c;
+          const bool second = g.mode == kModeDQ && kk >= g.nkb_c;
           const uint32_t d = d0 + (second ? D : 0);
           const int kl = second ? kk - g.nkb_c : kk;  // k block within the part
+          const uint32_t idesc = amn ? idesc_mn : idesc_k;
 #pragma unroll
           for (int k = 0; k < 4; ++k)
-            mma_ss(d, da + (kAmn ? k * 128 : k * 2), db + k * 128, idesc, (kl > 0 || k > 0) ? 1u : 0u);
+            mma_ss(d, da + (amn ? k * 128 : k * 2), db + k * 128, idesc, (kl > 0 || k > 0) ? 1u : 0u);
           tc_commit(&bars->empty[s]);
         }
         if (!ok) break;
@@ -691,32 +743,39 @@ __global__ void __launch_bounds__(kGThreads, 1)
     }
   } else {
     // ============================ epilogue ===============================
+    // The four epilogue warps take every wait together (named barrier 2 over
+    // their 128 threads returns the AND of the four outcomes), so they leave
+    // the loop together and the DQ tiles' barriers always see all four.
     const int quad = warp & 3;
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
-    const int rows = MODE == kModeDR ? p.L : p.W;
-    uint32_t tl = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < p.tiles; t += gridDim.x, ++tl) {
-      const GTile g = gtile<MODE>(p, t);
+    for (uint32_t n = 0, tl = 0;; ++n, ++tl) {
+      ok = named_bar_and(2, 128, warp_wait(&bars->tq_full[n % kGTq], (n / kGTq) & 1, wait_ns, abort));
+      if (!ok) break;
+      const int u = tq_read(bars, n);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->tq_empty[n % kGTq]);
+      if (u >= p.total) break;
+      const GTile g = gtile(p, u);
       const uint32_t acc = tl & 1;
+      const uint32_t acc_col = tmem + lane_base + acc * kGAccCols;
       const int row = g.m0 + 32 * quad + lane;
-      if constexpr (MODE == kModeDQ) {
-        // The four epilogue warps leave together (they meet at named barriers).
-        ok = named_bar_and(2, 128, warp_wait(&bars->acc_full[acc], (tl >> 1) & 1, wait_ns, abort));
-        if (!ok) break;
-        tc_fence_after();
+      ok = named_bar_and(2, 128, warp_wait(&bars->acc_full[acc], (tl >> 1) & 1, wait_ns, abort));
+      if (!ok) break;
+      tc_fence_after();
+      if (g.mode == kModeDQ) {
         // dq = key part + distance part; the column sums of each part over
         // the tile's rows (this warp's 32 through its staging tile, then the
         // four warps in order) go to the bias partials.
         float* swp = reinterpret_cast<float*>(smem + kGOffEpi) + quad * 32 * 32;
         float* wred = reinterpret_cast<float*>(smem + kGOffRed);
         const int b = g.z / p.H, h = g.z % p.H;
-        float* dst = row < p.W ? p.out0 + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D : nullptr;
+        float* dst = row < p.W ? p.dq + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D : nullptr;
 #pragma unroll 1
         for (int c = 0; c < D / 32; ++c) {
           uint32_t vc[32], vd[32];
-          tmem_ld32(tmem + lane_base + acc * kAccCols + 32 * c, vc);
-          tmem_ld32(tmem + lane_base + acc * kAccCols + D + 32 * c, vd);
+          tmem_ld32(acc_col + 32 * c, vc);
+          tmem_ld32(acc_col + D + 32 * c, vd);
           tmem_wait_ld(vc);
           tmem_wait_ld(vd);
           if (c == D / 32 - 1) {
@@ -760,24 +819,21 @@ __global__ void __launch_bounds__(kGThreads, 1)
                                  wred[(2 * 2 + part) * 128 + et]) +
                                 wred[(3 * 2 + part) * 128 + et];
         }
-        named_bar_sync(2, 128);  // the sums are read before the next tile writes them
+        named_bar_sync(2, 128);  // the sums are read before the next DQ tile writes them
         continue;
       }
-      if (!(ok = warp_wait(&bars->acc_full[acc], (tl >> 1) & 1, wait_ns, abort))) break;
-      tc_fence_after();
       float* dst = nullptr;
-      if (row < rows) {
-        if (MODE == kModeDR) {
-          dst = p.out0 + (static_cast<size_t>(row) * p.H + g.z) * D;
-        } else {
-          const int b = g.z / p.H, h = g.z % p.H;
-          dst = p.out0 + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D;
-        }
+      const bool add = g.mode == kModeDR && p.accumulate;
+      if (g.mode == kModeDR) {
+        if (row < p.L) dst = p.dr + (static_cast<size_t>(row) * p.H + g.z) * D;
+      } else if (row < p.W) {
+        const int b = g.z / p.H, h = g.z % p.H;
+        dst = (g.mode == kModeDK ? p.dk : p.dv) + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D;
       }
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
-        tmem_ld32(tmem + lane_base + acc * kAccCols + 32 * c, v);
+        tmem_ld32(acc_col + 32 * c, v);
         tmem_wait_ld(v);
         if (c == D / 32 - 1) {
           tc_fence_before();
@@ -786,7 +842,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
         }
         if (dst != nullptr) {
           float4* o4 = reinterpret_cast<float4*>(dst + 32 * c);
-          if (MODE == kModeDR && p.accumulate) {
+          if (add) {
             // each (distance, head) row belongs to one tile: a plain read-add-write
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
@@ -811,7 +867,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem, gemm_tmem_cols<MODE>());
+    tmem_dealloc(tmem, kGTmemCols);
   }
 }
 
@@ -832,6 +888,7 @@ size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 struct Scratch128 {
   __nv_bfloat16 *G, *P, *GS, *Qu, *Qv;
   float* part;
+  unsigned int* ctr;  // the products' tile counter
   size_t bytes;
 };
 
@@ -852,6 +909,7 @@ Scratch128 carve(void* base, int Bc, int W, int M, int H, size_t n_part) {
   s.Qu = reinterpret_cast<__nv_bfloat16*>(take(bwhd * 2));
   s.Qv = reinterpret_cast<__nv_bfloat16*>(take(bwhd * 2));
   s.part = reinterpret_cast<float*>(take(n_part * H * 2 * D * 4));
+  s.ctr = reinterpret_cast<unsigned int*>(take(sizeof(unsigned int)));
   s.bytes = off;
   return s;
 }
@@ -869,25 +927,22 @@ int chunk_seqs(int B, int W, int M, int H) {
 // Bias partials: one per (sequence, 128-row block) of every chunk.
 size_t total_parts(int B, int W) { return static_cast<size_t>(B) * ((W + 127) / 128); }
 
-template <int MODE>
-cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b0, const CUtensorMap& b1,
-                        GemmArgs p, cudaStream_t stream) {
+cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) {
   static std::atomic<bool> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev].load()) {
-    if ((e = cudaFuncSetAttribute(bgemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem)) !=
-        cudaSuccess)
+    if ((e = cudaFuncSetAttribute(bgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem)) != cudaSuccess)
       return e;
     attr_done[dev].store(true);
   }
-  if (MODE == kModeDQ) p.tiles = p.BH * p.nmt;
-  else if (MODE == kModeDR) p.tiles = p.H * p.nmt;
-  else p.tiles = p.BH * p.nmt;
-  const int grid = min(p.tiles, num_sms());
-  bgemm_kernel<MODE><<<grid, kGThreads, kGSmem, stream>>>(a0, a1, b0, b1, p);
+  const long long total = static_cast<long long>(p.nDR) + p.nDQ + 2LL * p.BH * p.nmt;
+  if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  p.total = static_cast<int>(total);
+  const int grid = std::min(p.total, num_sms());
+  bgemm_kernel<<<grid, kGThreads, kGSmem, stream>>>(maps, p);
   return cudaGetLastError();
 }
 
@@ -932,19 +987,20 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
   const cuuint64_t d_ = D, h_ = H, w_ = W, l_ = L;
   const cuuint64_t lp2 = static_cast<cuuint64_t>(LP) * 2;
   // r and the chunk's scratch do not move between chunks
-  CUtensorMap tr64, tgk, tgsk, tpk, tgmn, tpmn, tgsmn, tqu, tqv;
-  enc(&tr64, r, 3, {d_, h_, static_cast<cuuint64_t>(n_r)}, {d_ * 2, hd2}, {64, 1, 64});
+  GMaps gm;  // the products' maps
+  CUtensorMap tpk;
+  enc(&gm.b_r, r, 3, {d_, h_, static_cast<cuuint64_t>(n_r)}, {d_ * 2, hd2}, {64, 1, 64});
   auto enc_scratch = [&](int nb) {
     const cuuint64_t bh_ = static_cast<cuuint64_t>(nb) * H, b_ = nb;
     // G, P, GS: [nb*H][W][LP] bf16 (columns past L zero-filled); q+u, q+v: [nb, W, H, D]
-    enc(&tgk, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
-    enc(&tgsk, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+    enc(&gm.a_g, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
+    enc(&gm.a_gs, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
     enc(&tpk, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 128, 1});
-    enc(&tgmn, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
-    enc(&tpmn, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
-    enc(&tgsmn, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
-    enc(&tqu, sc.Qu, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
-    enc(&tqv, sc.Qv, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+    enc(&gm.m_g, sc.G, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+    enc(&gm.m_p, sc.P, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+    enc(&gm.m_gs, sc.GS, 3, {l_, w_, bh_}, {lp2, w_ * lp2}, {64, 64, 1});
+    enc(&gm.b_qu, sc.Qu, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+    enc(&gm.b_qv, sc.Qv, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
   };
 
   cudaError_t e;
@@ -972,12 +1028,12 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(o) + b0 * seg;
     const __nv_bfloat16* gb = static_cast<const __nv_bfloat16*>(dout) + b0 * seg;
     const cuuint64_t b_ = nb;
-    CUtensorMap tq, tdo128, tk, tv, tdo64;
+    CUtensorMap tq, tdo128, tv;
     enc(&tq, qb, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
     enc(&tdo128, gb, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 128, 1});
-    enc(&tk, kb, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
+    enc(&gm.b_k, kb, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
     enc(&tv, vb, 4, {d_, h_, l_, b_}, {d_ * 2, hd2, l_ * hd2}, {64, 1, 64, 1});
-    enc(&tdo64, gb, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
+    enc(&gm.b_do, gb, 4, {d_, h_, w_, b_}, {d_ * 2, hd2, w_ * hd2}, {64, 1, 64, 1});
     if (nb != last_nb) {
       enc_scratch(nb);
       last_nb = nb;
@@ -1004,12 +1060,14 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     p.status = wc.status;
     p.wait_ns = wc.limit_ns;
     p.inject_stall = b0 == 0 ? wc.inject_stall : 0;
+    p.gemm_ctr = sc.ctr;
     const long long units = static_cast<long long>(p.nqt) * nb * H;
     if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, tk, tv, tr64, tdo128, tgk,
-                                                                                 tpk, p);
+    bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, gm.b_k, tv, gm.b_r, tdo128,
+                                                                                 gm.a_g, tpk, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    // 2. the five products
+    // 2. the products, one launch: DR, DQ, DK and DV tiles from the counter
+    // that the pair kernel has just zeroed
     GemmArgs g;
     g.B = nb;
     g.W = W;
@@ -1017,23 +1075,22 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     g.H = H;
     g.L = L;
     g.BH = nb * H;
-    g.nmt = (W + 127) / 128;
+    g.nmt = nmt;
+    g.nmtL = (L + 127) / 128;
     g.nkbW = (W + 63) / 64;
-    g.tiles = 0;
-    g.accumulate = 0;
+    g.nDR = H * g.nmtL;
+    g.nDQ = g.BH * nmt;
+    g.total = 0;
+    g.dq = dq + b0 * seg;
+    g.dk = dk + b0 * seg;
+    g.dv = dv + b0 * seg;
+    g.dr = dr;
+    g.part = sc.part + static_cast<size_t>(b0) * nmt * H * 2 * D;
+    g.accumulate = b0 > 0;
+    g.ctr = sc.ctr;
     g.status = wc.status;
     g.wait_ns = wc.limit_ns;
-    g.out0 = dq + b0 * seg;
-    g.part = sc.part + static_cast<size_t>(b0) * nmt * H * 2 * D;
-    if ((e = launch_gemm<kModeDQ>(tgk, tgsk, tk, tr64, g, stream)) != cudaSuccess) return e;
-    g.out0 = dk + b0 * seg;
-    if ((e = launch_gemm<kModeDK>(tgmn, tgmn, tqu, tqu, g, stream)) != cudaSuccess) return e;
-    g.out0 = dv + b0 * seg;
-    if ((e = launch_gemm<kModeDV>(tpmn, tpmn, tdo64, tdo64, g, stream)) != cudaSuccess) return e;
-    g.out0 = dr;
-    g.nmt = (L + 127) / 128;
-    g.accumulate = b0 > 0;
-    if ((e = launch_gemm<kModeDR>(tgsmn, tgsmn, tqv, tqv, g, stream)) != cudaSuccess) return e;
+    if ((e = launch_products(gm, g, stream)) != cudaSuccess) return e;
   }
   if (n_r > L &&
       (e = cudaMemsetAsync(dr + static_cast<size_t>(L) * H * D, 0, static_cast<size_t>(n_r - L) * H * D * 4,
