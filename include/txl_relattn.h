@@ -462,9 +462,9 @@ TXL_API int txl_stack_forward(const void* h, void* out, int n_layers, void* cons
  * fp32 atomic adds, so its last bits may differ between calls.  The same
  * inputs with D = 128 and M a multiple of 8 also run on the tensor cores: a
  * kernel rebuilds p and g per 64-key step and writes them in bf16 to scratch
- * (g in key and in distance order, p in key order), tcgen05 products then
- * form dq (key and distance parts in one tile, with the bias gradients'
- * partials), dk, dv and dr, and an ordered sum the bias gradients;
+ * (g in key and in distance order, p in key order), one launch of tcgen05
+ * products then forms dq (key and distance parts in one tile, with the bias
+ * gradients' partials), dk, dv and dr, and an ordered sum the bias gradients;
  * deterministic.  Every other case runs on CUDA cores in
  * fp32 arithmetic, fully deterministic.
  * Allocates: per-(device, stream) scratch (see the conventions above): for
