@@ -30,6 +30,7 @@
 
 #include <cstdint>
 
+#include "pdl.cuh"
 #include "txl_internal.h"
 
 namespace txl {
@@ -368,6 +369,7 @@ __global__ void __launch_bounds__(kThreads) bwd_dr_kernel(BwdArgs a) {
 // are added in warp order, so the order is fixed.
 __global__ void bwd_bias_kernel(const float* __restrict__ part, int n_part, int H, int D, float* __restrict__ du,
                                 float* __restrict__ dvb) {
+  grid_dep_wait();  // launched behind the kernel that writes the partials
   __shared__ float red[32][32];
   const int lane = threadIdx.x & 31, wp = threadIdx.x >> 5;
   const int ncol = H * 2 * D;
@@ -408,8 +410,8 @@ cudaError_t launch_typed(BwdArgs a, float* du, float* dvb, cudaStream_t stream) 
 
 cudaError_t launch_bwd_bias(const float* part, int n_part, int H, int D, float* du, float* dvb,
                             cudaStream_t stream) {
-  bwd_bias_kernel<<<(H * 2 * D + 31) / 32, 1024, 0, stream>>>(part, n_part, H, D, du, dvb);
-  return cudaGetLastError();
+  return launch_dependent(bwd_bias_kernel, dim3((H * 2 * D + 31) / 32), dim3(1024), 0, stream, part, n_part, H, D,
+                          du, dvb);
 }
 
 size_t relattn_bwd_simt_scratch_bytes(int B, int W, int H, int D) {

@@ -42,6 +42,7 @@
 #include <algorithm>
 #include <initializer_list>
 
+#include "pdl.cuh"
 #include "relattn_tc_common.cuh"
 #include "txl_device.cuh"
 #include "txl_internal.h"
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                          const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_g,
                          const __grid_constant__ CUtensorMap tm_p, const ScoreParams p) {
+  grid_dep_launch_dependents();  // the products' CTAs may take SMs this launch no longer needs
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -592,6 +594,8 @@ __device__ __forceinline__ int tq_read(GBars* bars, uint32_t n) { return *reinte
 
 __global__ void __launch_bounds__(kGThreads, 1)
     bgemm_kernel(const __grid_constant__ GMaps maps, const GemmArgs p) {
+  grid_dep_wait();  // launched behind the pair kernel: its pair terms and the zeroed counter
+  grid_dep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -942,8 +946,7 @@ cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) 
   if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   p.total = static_cast<int>(total);
   const int grid = std::min(p.total, num_sms());
-  bgemm_kernel<<<grid, kGThreads, kGSmem, stream>>>(maps, p);
-  return cudaGetLastError();
+  return launch_dependent(bgemm_kernel, dim3(grid), dim3(kGThreads), kGSmem, stream, maps, p);
 }
 
 }  // namespace

@@ -35,6 +35,7 @@
 
 #include <cstdint>
 
+#include "pdl.cuh"
 #include "relattn_tc_common.cuh"
 #include "txl_device.cuh"
 #include "txl_internal.h"
@@ -201,6 +202,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
                        const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dr,
                        const BwdParams p) {
+  grid_dep_launch_dependents();  // the dk/dv kernel's CTAs may take SMs this launch no longer needs
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -596,6 +598,8 @@ __global__ void __launch_bounds__(kQThreads, 1)
     bwd_dkdv_tc64_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
                          const __grid_constant__ CUtensorMap tm_do, const BwdParams p, int n_items) {
+  grid_dep_wait();  // launched behind the dq kernel: the per-row Delta it writes
+  grid_dep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -915,8 +919,9 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const int n_items = (W + BN - 1) / BN * B * H;
   const int grid = n_items < num_sms() ? n_items : num_sms();
-  bwd_dkdv_tc64_kernel<<<grid, kQThreads, kKSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, p, n_items);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_dependent(bwd_dkdv_tc64_kernel, dim3(grid), dim3(kQThreads), kKSmem, stream, tm_q, tm_k, tm_v,
+                            tm_rw, tm_do, p, n_items)) != cudaSuccess)
+    return e;
   return launch_bwd_bias(p.part, B * p.nqt, H, D, du, dvb, stream);
 }
 
