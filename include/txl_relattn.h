@@ -27,7 +27,12 @@
  *     txl_relattn_forward_static, txl_mem_update and txl_dense allocate
  *     nothing.
  *   - Every call is asynchronous on `stream` (0 = legacy default stream) and
- *     returns a txl_status code.  Argument errors are detected on the host before
+ *     keeps stream order.  The library's bf16 and roll kernels are launched
+ *     with programmatic stream serialisation: their CTAs may become resident
+ *     while the kernel before them on the stream drains, but each waits at its
+ *     first instruction until that kernel has completed and its writes are
+ *     visible, so no memory is touched earlier.  Each call returns a
+ *     txl_status code.  Argument errors are detected on the host before
  *     any launch, and then nothing is launched.  A failed launch returns
  *     TXL_ERR_CUDA.  Errors detected inside a kernel (a bounded wait that ran out)
  *     are recorded in a device status word read by txl_get_device_status.

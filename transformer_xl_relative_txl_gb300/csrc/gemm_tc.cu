@@ -28,6 +28,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "pdl.cuh"
 #include "relattn_tc_common.cuh"
 #include "txl_device.cuh"
 #include "txl_internal.h"
@@ -110,6 +111,10 @@ template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
                    const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
+  // Launched behind the previous kernel on the stream, which has completed from
+  // here on.  No early trigger: the next persistent launch starts its CTAs when
+  // this one completes (placed early, they timed slower back to back).
+  grid_dep_wait();
   using Cfg = GemmCfg<BN>;
   constexpr int S = Cfg::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -329,8 +334,7 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
   }
   const int sms = gemm_num_sms();
   const int grid = p.tiles < sms ? p.tiles : sms;
-  gemm_tc_kernel<BN><<<grid, kGemmThreads, Cfg::kSmem, stream>>>(ta, tb, tc, p);
-  return cudaGetLastError();
+  return launch_dependent(gemm_tc_kernel<BN>, dim3(grid), dim3(kGemmThreads), Cfg::kSmem, stream, ta, tb, tc, p);
 }
 
 }  // namespace

@@ -12,6 +12,7 @@
 #include <mutex>
 #include <tuple>
 
+#include "pdl.cuh"
 #include "txl_internal.h"
 
 namespace txl {
@@ -57,6 +58,8 @@ __global__ void __launch_bounds__(256, kC > 4 ? 2 : kBias ? 4 : 5) add_ln_kernel
                                                                      const float* __restrict__ beta,
                                                                      __nv_bfloat16* __restrict__ out,
                                                                      long long rows, int d) {
+  grid_dep_wait();  // launched behind the previous kernel on the stream: it has completed from here on
+  grid_dep_launch_dependents();
   __shared__ __align__(16) float s_gamma[kLnMaxD], s_beta[kLnMaxD], s_bias[kBias ? kLnMaxD : 4];
   const long long row = static_cast<long long>(blockIdx.x) * 16 + (threadIdx.x >> 4);
   const int hl = threadIdx.x & 15;
@@ -128,13 +131,14 @@ __global__ void __launch_bounds__(256, kC > 4 ? 2 : kBias ? 4 : 5) add_ln_kernel
 
 namespace {
 template <int kC>
-void add_ln_dispatch(unsigned blocks, const __nv_bfloat16* a, const __nv_bfloat16* b, const float* bias,
-                     const float* gamma, const float* beta, __nv_bfloat16* out, long long rows, int d,
-                     cudaStream_t stream) {
+cudaError_t add_ln_dispatch(unsigned blocks, const __nv_bfloat16* a, const __nv_bfloat16* b, const float* bias,
+                            const float* gamma, const float* beta, __nv_bfloat16* out, long long rows, int d,
+                            cudaStream_t stream) {
   if (bias != nullptr)
-    add_ln_kernel<kC, true><<<blocks, 256, 0, stream>>>(a, b, bias, gamma, beta, out, rows, d);
-  else
-    add_ln_kernel<kC, false><<<blocks, 256, 0, stream>>>(a, b, bias, gamma, beta, out, rows, d);
+    return launch_dependent(add_ln_kernel<kC, true>, dim3(blocks), dim3(256), 0, stream, a, b, bias, gamma, beta, out,
+                            rows, d);
+  return launch_dependent(add_ln_kernel<kC, false>, dim3(blocks), dim3(256), 0, stream, a, b, bias, gamma, beta, out,
+                          rows, d);
 }
 }  // namespace
 
@@ -147,15 +151,10 @@ cudaError_t launch_add_ln(const void* a, const void* b, const float* bias, const
   const auto* pb = static_cast<const __nv_bfloat16*>(b);
   auto* po = static_cast<__nv_bfloat16*>(out);
   const int per_lane = (d / 8 + 15) / 16;  // chunks of 8 columns a lane holds
-  if (per_lane <= 1)
-    add_ln_dispatch<1>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
-  else if (per_lane <= 2)
-    add_ln_dispatch<2>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
-  else if (per_lane <= 4)
-    add_ln_dispatch<4>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
-  else
-    add_ln_dispatch<8>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
-  return cudaGetLastError();
+  if (per_lane <= 1) return add_ln_dispatch<1>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
+  if (per_lane <= 2) return add_ln_dispatch<2>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
+  if (per_lane <= 4) return add_ln_dispatch<4>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
+  return add_ln_dispatch<8>(blocks, pa, pb, bias, gamma, beta, po, rows, d, stream);
 }
 
 }  // namespace txl

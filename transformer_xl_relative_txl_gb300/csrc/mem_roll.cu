@@ -19,6 +19,7 @@
 #include <atomic>
 #include <cstdint>
 
+#include "pdl.cuh"
 #include "txl_device.cuh"
 #include "txl_internal.h"
 
@@ -87,6 +88,8 @@ __device__ __forceinline__ void chunk_at(const BulkParams& p, long long c, const
 }
 
 __global__ void __launch_bounds__(32) mem_roll_bulk_kernel(const __grid_constant__ BulkParams p) {
+  grid_dep_wait();  // launched behind the previous kernel on the stream: it has completed from here on
+  grid_dep_launch_dependents();
   extern __shared__ __align__(128) unsigned char stage[];  // kStages x kChunk
   __shared__ __align__(8) uint64_t bar[kStages];
   if (threadIdx.x != 0) return;
@@ -138,6 +141,8 @@ __global__ void __launch_bounds__(256) mem_roll_kernel(const char* __restrict__ 
                                                        char* __restrict__ out, long long n_vec,
                                                        long long split_vec, long long mem_bs, long long h_bs,
                                                        long long out_bs) {
+  grid_dep_wait();  // launched behind the previous kernel on the stream: it has completed from here on
+  grid_dep_launch_dependents();
   const long long b = blockIdx.y;
   const V* src_mem = reinterpret_cast<const V*>(mem + b * mem_bs);
   const V* src_h = reinterpret_cast<const V*>(h + b * h_bs);
@@ -172,8 +177,8 @@ cudaError_t launch_typed(const char* mem, const char* h, char* out, int B, long 
   if (blocks > target) blocks = target;
   if (blocks < 1) blocks = 1;
   dim3 grid(static_cast<unsigned>(blocks), static_cast<unsigned>(B));
-  mem_roll_kernel<V><<<grid, threads, 0, stream>>>(mem, h, out, n_vec, split, mem_bs, h_bs, out_bs);
-  return cudaGetLastError();
+  return launch_dependent(mem_roll_kernel<V>, grid, dim3(threads), 0, stream, mem, h, out, n_vec, split, mem_bs, h_bs,
+                          out_bs);
 }
 
 int sm_count() {
@@ -242,8 +247,7 @@ cudaError_t launch_mem_roll_multi(const RollTensor* t, int ntensors, int B, long
     }
     const long long cap = 2LL * sm_count();
     const unsigned grid = static_cast<unsigned>(p.total < cap ? p.total : cap);
-    mem_roll_bulk_kernel<<<grid, 32, smem, stream>>>(p);
-    return cudaGetLastError();
+    return launch_dependent(mem_roll_bulk_kernel, dim3(grid), dim3(32), smem, stream, p);
   }
   for (int x = 0; x < ntensors; ++x) {
     const char* hh = total > split ? static_cast<const char*>(t[x].h) + h_row0 * row_bytes : nullptr;

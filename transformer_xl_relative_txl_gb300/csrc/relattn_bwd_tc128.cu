@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
                          const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                          const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_g,
                          const __grid_constant__ CUtensorMap tm_p, const ScoreParams p) {
+  grid_dep_wait();  // launched behind the previous kernel on the stream: it has completed from here on
   grid_dep_launch_dependents();  // the products' CTAs may take SMs this launch no longer needs
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -1066,9 +1067,9 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     p.gemm_ctr = sc.ctr;
     const long long units = static_cast<long long>(p.nqt) * nb * H;
     if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    bwd_scores128_kernel<<<static_cast<int>(units), kSThreads, kSSmem, stream>>>(tq, gm.b_k, tv, gm.b_r, tdo128,
-                                                                                 gm.a_g, tpk, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_dependent(bwd_scores128_kernel, dim3(static_cast<unsigned>(units)), dim3(kSThreads), kSSmem,
+                              stream, tq, gm.b_k, tv, gm.b_r, tdo128, gm.a_g, tpk, p)) != cudaSuccess)
+      return e;
     // 2. the products, one launch: DR, DQ, DK and DV tiles from the counter
     // that the pair kernel has just zeroed
     GemmArgs g;

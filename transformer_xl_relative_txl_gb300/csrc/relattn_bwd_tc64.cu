@@ -202,6 +202,7 @@ __global__ void __launch_bounds__(kDqThreads, 1)
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_rw,
                        const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dr,
                        const BwdParams p) {
+  grid_dep_wait();  // launched behind the previous kernel on the stream: it has completed from here on
   grid_dep_launch_dependents();  // the dk/dv kernel's CTAs may take SMs this launch no longer needs
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -915,8 +916,9 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
   if ((e = cudaMemsetAsync(dr, 0, sizeof(float) * static_cast<size_t>(n_r) * H * D, stream)) != cudaSuccess)
     return e;
   const int units = p.nqt * B * H;
-  bwd_dq_tc64_kernel<<<units, kDqThreads, kQSmem, stream>>>(tm_q, tm_k, tm_v, tm_rw, tm_do, tm_dr, p);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  if ((e = launch_dependent(bwd_dq_tc64_kernel, dim3(units), dim3(kDqThreads), kQSmem, stream, tm_q, tm_k, tm_v,
+                            tm_rw, tm_do, tm_dr, p)) != cudaSuccess)
+    return e;
   const int n_items = (W + BN - 1) / BN * B * H;
   const int grid = n_items < num_sms() ? n_items : num_sms();
   if ((e = launch_dependent(bwd_dkdv_tc64_kernel, dim3(grid), dim3(kQThreads), kKSmem, stream, tm_q, tm_k, tm_v,

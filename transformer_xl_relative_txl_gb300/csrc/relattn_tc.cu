@@ -56,6 +56,7 @@
 #include <cmath>
 #include <cstdint>
 
+#include "pdl.cuh"
 #include "relattn_tc_common.cuh"
 #include "txl_device.cuh"
 #include "txl_internal.h"
@@ -140,6 +141,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
                       const __grid_constant__ CUtensorMap tm_km, const __grid_constant__ CUtensorMap tm_vm,
                       const Params p) {
+  // Launched behind the previous kernel on the stream, which has completed from
+  // here on.  No early trigger: the next persistent launch starts its CTAs when
+  // this one completes (placed early, they timed slower back to back).
+  grid_dep_wait();
   using C = Cfg<D>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
@@ -686,8 +691,7 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
   const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
-  kern<<<grid, kThreads, smem, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_km, tm_vm, prm);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), smem, stream, tm_q, tm_k, tm_v, tm_r, tm_km, tm_vm, prm);
 }
 
 }  // namespace

@@ -63,6 +63,7 @@
 #include <type_traits>
 #include <vector>
 
+#include "pdl.cuh"
 #include "relattn_tc_common.cuh"
 #include "txl_device.cuh"
 #include "txl_internal.h"
@@ -157,6 +158,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const __grid_constant__ CUtensorMap tm_o, const __grid_constant__ CUtensorMap tm_km,
                         const __grid_constant__ CUtensorMap tm_vm, const __grid_constant__ CUtensorMap tm_ks,
                         const __grid_constant__ CUtensorMap tm_vs, const Params p) {
+  // Launched behind the previous kernel on the stream, which has completed from
+  // here on.  No early trigger: the next persistent launch starts its CTAs when
+  // this one completes (placed early, they timed slower back to back).
+  grid_dep_wait();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
@@ -928,8 +933,8 @@ cudaError_t launch_typed(const CUtensorMap& tm_q, const CUtensorMap& tm_k, const
     if (dev < 32) __atomic_fetch_or(&configured_mask, 1 << dev, __ATOMIC_RELEASE);
   }
   const int grid = prm.n_units < num_sms() ? prm.n_units : num_sms();
-  kern<<<grid, kThreads, kSmemBytes, stream>>>(tm_q, tm_k, tm_v, tm_r, tm_o, tm_km, tm_vm, tm_ks, tm_vs, prm);
-  return cudaGetLastError();
+  return launch_dependent(kern, dim3(grid), dim3(kThreads), kSmemBytes, stream, tm_q, tm_k, tm_v, tm_r, tm_o, tm_km,
+                          tm_vm, tm_ks, tm_vs, prm);
 }
 
 // Units dealt to the CTAs by cost (longest-processing-time first onto the
