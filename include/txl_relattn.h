@@ -553,6 +553,10 @@ TXL_API int txl_debug_force_split(int nsplit);
  * the D = 128 tensor-core backward (default 1 GiB; 0 restores it).  A smaller
  * cap splits the batch into more chunks, run one after the other. */
 TXL_API int txl_debug_set_bwd_chunk_bytes(unsigned long long bytes);
+/* Test hook: bn = 64, 128 or 256 fixes the column tile of txl_dense's GEMM
+ * (and the layer's products) instead of the width its cost model picks per
+ * shape; 0 restores the model.  TXL_ERR_INVALID_ARG for any other value. */
+TXL_API int txl_debug_force_dense_tile_n(int bn);
 
 #ifdef __cplusplus
 }

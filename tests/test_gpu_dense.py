@@ -5,8 +5,8 @@ The kernel accumulates in fp32 and rounds once to bf16, so each element may
 differ from the exact value by half a bf16 ulp (2^-9 relative) plus the fp32
 accumulation error; the bound below allows 2^-8 relative plus 1e-3 of the
 tensor's largest value.  Shapes cover ragged m, n and k (the tiles' zero
-fill and clipped stores), both column-tile widths the launcher picks (128
-and 256), a batch of three packed weight matrices, the bias and the ReLU,
+fill and clipped stores), the column-tile widths the launcher picks (128
+and 256) and each of 64, 128 and 256 forced by the test hook, a batch of three packed weight matrices, the bias and the ReLU,
 and the base layer's two feed-forward shapes.
 """
 
@@ -60,6 +60,34 @@ def test_dense_matches_float64(txl, m, n, k, batch, bias, relu):
         want = np.maximum(want, 0.0)
     got = y.float().cpu().numpy().astype(np.float64)
     err = np.abs(got - want)
+    bound = 2.0 ** -8 * np.abs(want) + 1e-3 * np.abs(want).max()
+    assert np.all(err <= bound), f"max err {err.max():.3e}, worst excess {(err - bound).max():.3e}"
+
+
+@pytest.mark.parametrize("bn", [64, 128, 256])
+@pytest.mark.parametrize("m,n,k,bias,relu", [
+    (300, 200, 264, True, True),        # ragged in every dimension, k over two 128-deep stages
+    (11264, 512, 2048, True, False),    # base layer, W_2 with b_2
+])
+def test_dense_each_tile_width(txl, bn, m, n, k, bias, relu):
+    """Every column-tile width of the GEMM, forced through the test hook."""
+    rng = np.random.default_rng(m + n + k + bn)
+    x = round_bf16(rng.standard_normal((m, k)).astype(np.float32))
+    W = round_bf16((rng.standard_normal((1, k, n)) * 0.05).astype(np.float32))
+    b = (rng.standard_normal(n) * 0.1).astype(np.float32) if bias else None
+    y = torch.empty(1, m, n, device=dev(), dtype=torch.bfloat16)
+    txl.txl_debug_force_dense_tile_n(bn)
+    try:
+        txl.txl_dense(_bf(x), _bf(W), y, bias=torch.from_numpy(b).to(dev()) if bias else None, relu=relu)
+    finally:
+        txl.txl_debug_force_dense_tile_n(0)
+    assert txl.txl_get_device_status() == 0
+    want = np.einsum("mk,zkn->zmn", x.astype(np.float64), W.astype(np.float64))
+    if bias:
+        want = want + b.astype(np.float64)
+    if relu:
+        want = np.maximum(want, 0.0)
+    err = np.abs(y.float().cpu().numpy().astype(np.float64) - want)
     bound = 2.0 ** -8 * np.abs(want) + 1e-3 * np.abs(want).max()
     assert np.all(err <= bound), f"max err {err.max():.3e}, worst excess {(err - bound).max():.3e}"
 

@@ -26,6 +26,7 @@ __all__ = [
     "txl_get_device_status", "txl_release_cached", "txl_status_string", "txl_version",
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall", "txl_debug_force_split",
     "txl_debug_set_bwd_chunk_bytes",
+    "txl_debug_force_dense_tile_n",
 ]
 
 TXL_F32 = 0
@@ -102,6 +103,8 @@ lib.txl_debug_force_split.argtypes = [_i]
 lib.txl_debug_force_split.restype = _i
 lib.txl_debug_set_bwd_chunk_bytes.argtypes = [ctypes.c_ulonglong]
 lib.txl_debug_set_bwd_chunk_bytes.restype = _i
+lib.txl_debug_force_dense_tile_n.argtypes = [_i]
+lib.txl_debug_force_dense_tile_n.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -553,3 +556,9 @@ def txl_debug_set_bwd_chunk_bytes(nbytes):
     """Test hook: cap on one chunk's scratch in the D = 128 tensor-core
     backward (0: the default, 1 GiB)."""
     _check(lib.txl_debug_set_bwd_chunk_bytes(int(nbytes)), "txl_debug_set_bwd_chunk_bytes")
+
+
+def txl_debug_force_dense_tile_n(bn):
+    """Test hook: fix txl_dense's column tile (64, 128 or 256; 0: its cost
+    model)."""
+    _check(lib.txl_debug_force_dense_tile_n(int(bn)), "txl_debug_force_dense_tile_n")

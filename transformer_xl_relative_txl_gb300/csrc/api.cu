@@ -369,6 +369,12 @@ int txl_debug_set_bwd_chunk_bytes(unsigned long long bytes) {
   return TXL_OK;
 }
 
+int txl_debug_force_dense_tile_n(int bn) {
+  if (bn != 0 && bn != 64 && bn != 128 && bn != 256) return TXL_ERR_INVALID_ARG;
+  txl::gemm_tc_force_tile_n(bn);
+  return TXL_OK;
+}
+
 int txl_debug_force_split(int nsplit) {
   if (nsplit < 0 || nsplit > 64) return TXL_ERR_INVALID_ARG;
   g_force_split.store(nsplit);

@@ -9,13 +9,14 @@
 // products (with b_1 and the ReLU after the first, b_2 after the second).
 //
 // Design (one persistent CTA per SM, 192 threads):
-//   warp 0     TMA producer: per 64-deep k block, one 128 x 64 tile of A
-//              (K-major, 128-byte swizzle) and BN/64 tiles of 64 k-rows x 64
+//   warp 0     TMA producer: per k block (128 deep for BN = 64 or 128
+//              column tiles, 64 deep for BN = 256), 128 x 64 tiles of A
+//              (K-major, 128-byte swizzle) and BN/64 tiles of k-rows x 64
 //              columns of B (N-major: B is stored [k, n] with n contiguous)
 //              into a ring of shared-memory stages;
 //   warp 1     MMA issuer: tcgen05.mma kind::f16, M = 128, N = BN, K = 16,
-//              four per k block, into one of two TMEM accumulators, so the
-//              next tile's products overlap this tile's epilogue;
+//              into one of two TMEM accumulators, so the next tile's
+//              products overlap this tile's epilogue;
 //   warps 2-5  epilogue: each reads its 32-lane quadrant of the accumulator
 //              (tcgen05.ld, 64 columns at a time), adds the bias, applies the
 //              ReLU, rounds to bf16, stages 32 rows x 64 columns in its own
@@ -47,11 +48,11 @@ constexpr int kEpiBytes = 32 * 128;   // one epilogue warp's staging: 32 rows x 
 // would leave two stages, and four of 64 k stay faster.
 template <int BN>
 struct GemmCfg {
-  static constexpr int kBK = BN == 128 ? 128 : 64;            // k per stage
+  static constexpr int kBK = BN <= 128 ? 128 : 64;            // k per stage
   static constexpr int kABoxes = kBK / 64;                    // 64-k tiles of A per stage
   static constexpr int kBBlock = kBK * 128;                   // kBK k-rows x 64 columns of B
   static constexpr int kStageBytes = kABoxes * kATile + (BN / 64) * kBBlock;
-  static constexpr int kStages = BN == 256 ? 4 : 3;
+  static constexpr int kStages = BN == 128 ? 3 : 4;
   static constexpr int kOffEpi = kStages * kStageBytes;             // 4 x 4 KB staging
   static constexpr int kOffBias = kOffEpi + 4 * kEpiBytes;          // 4 x BN floats
   static constexpr int kOffBar = kOffBias + 4 * BN * 4;
@@ -339,13 +340,25 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
 
 }  // namespace
 
-int gemm_tc_k_block(int bn) { return bn == 128 ? GemmCfg<128>::kBK : GemmCfg<256>::kBK; }
+int gemm_tc_k_block(int bn) {
+  return bn == 64 ? GemmCfg<64>::kBK : bn == 128 ? GemmCfg<128>::kBK : GemmCfg<256>::kBK;
+}
+
+std::atomic<int> g_force_tile_n{0};
+
+void gemm_tc_force_tile_n(int bn) { g_force_tile_n.store(bn == 64 || bn == 128 || bn == 256 ? bn : 0); }
 
 int gemm_tc_tile_n(int m, int n, int batch) {
+  if (const int f = g_force_tile_n.load()) return f;
   // Fewer waves of tiles against smaller tiles: the time of a wave is about
   // proportional to its tiles' columns, plus a fixed part per tile.
   const long long sms = gemm_num_sms();
   const long long mt = (m + GBM - 1) / GBM;
+  // Too few 128-column tiles to fill half the SMs: 64-column ones spread
+  // the work over twice as many (the r projection of the base layer,
+  // 1024 x 512 x 512: 10.2 -> 8.2 us); they are slower wherever the wider
+  // tiles already fill the GPU (W_2: 36.9 against 32.8 us).
+  if (2 * batch * mt * ((n + 127) / 128) <= sms) return 64;
   auto cost = [&](int bn) {
     const long long tiles = batch * mt * ((n + bn - 1) / bn);
     const long long waves = (tiles + sms - 1) / sms;
@@ -357,7 +370,7 @@ int gemm_tc_tile_n(int m, int n, int batch) {
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
                            int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
                            cudaStream_t stream) {
-  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || (bn != 128 && bn != 256)) return cudaErrorInvalidValue;
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || (bn != 64 && bn != 128 && bn != 256)) return cudaErrorInvalidValue;
   GemmParams p;
   p.m = m;
   p.n = n;
@@ -372,6 +385,7 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, con
   p.relu = relu ? 1 : 0;
   p.status = wc.status;
   p.wait_ns = wc.limit_ns;
+  if (bn == 64) return launch_bn<64>(tm_a, tm_b, tm_c, p, stream);
   return bn == 256 ? launch_bn<256>(tm_a, tm_b, tm_c, p, stream) : launch_bn<128>(tm_a, tm_b, tm_c, p, stream);
 }
 

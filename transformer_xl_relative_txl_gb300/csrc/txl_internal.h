@@ -165,6 +165,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
 // {n, m, batch} with a {64, 32, 1} box.  bn: columns per tile, 128 or 256
 // (gemm_tc_tile_n picks one for the shape).
 int gemm_tc_tile_n(int m, int n, int batch);
+void gemm_tc_force_tile_n(int bn);  // test hook: 64, 128 or 256 fixes the column tile, 0 restores the choice
 int gemm_tc_k_block(int bn);
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
                            int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
