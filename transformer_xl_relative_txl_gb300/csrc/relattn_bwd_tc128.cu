@@ -41,6 +41,8 @@
 #include <cstdint>
 #include <algorithm>
 #include <initializer_list>
+#include <queue>
+#include <vector>
 
 #include "pdl.cuh"
 #include "relattn_tc_common.cuh"
@@ -102,7 +104,37 @@ struct ScoreParams {
   unsigned long long wait_ns;
   int inject_stall;  // test hook: the load thread loads nothing past the first two steps
   unsigned int* gemm_ctr;  // the products' tile counter, zeroed here for the launch that follows
+  int split_qt;            // the last split_qt query tiles run as two CTAs each (halves of the key steps)
 };
+
+// CTA u's work: a (sequence, head, 128-query tile) unit, or one half of its
+// key steps.  Whole units come first, longest first; then the halves of the
+// units of the last split_qt query tiles (the longest), longest first.  The
+// pair terms of different key steps are independent, so a unit's steps can
+// run in two CTAs; each rebuilds the distance window at its first step.
+__device__ __forceinline__ Unit pair_item(int u, const ScoreParams& p) {
+  const int BH = p.B * p.H;
+  const int n_whole = (p.nqt - p.split_qt) * BH;
+  int qt, bh, part = -1;
+  if (u < n_whole) {
+    qt = p.nqt - p.split_qt - 1 - u / BH;
+    bh = u % BH;
+  } else {
+    u -= n_whole;
+    const int k = u / BH;  // 0 .. 2 split_qt - 1
+    qt = p.nqt - 1 - (k >> 1);
+    part = k & 1;
+    bh = u % BH;
+  }
+  Unit r;
+  r.b = bh / p.H;
+  r.h = bh % p.H;
+  r.i0 = qt * BM;
+  const int n = min(p.M + r.i0 + BM - 1, p.M + p.W - 1) / BN + 1;
+  r.t0 = part == 1 ? n / 2 : 0;
+  r.nks = part < 0 ? n : part == 0 ? n / 2 : n - n / 2;
+  return r;
+}
 
 struct SBars {
   uint64_t q, in[2], x, m1[2], done[2], sfree, fin;
@@ -195,12 +227,13 @@ __global__ void __launch_bounds__(kSThreads, 1)
   const int a = quad * 32 + lane;  // this thread's row of the tile
   const uint64_t wait_ns = p.wait_ns;
 
-  const Unit w = decode_unit(blockIdx.x, p.B, p.H, p.W, p.M, p.nqt);
-  const int T = w.nks;
+  const Unit w = pair_item(blockIdx.x, p);
+  const int T = w.nks;   // steps of this CTA: key steps t0 + t, t = 0 .. T-1
+  const int t0 = w.t0;
   const int i = w.i0 + a;  // query row
   const int z = w.b * p.H + w.h;
-  // first distance of the window of step t: M + i0 - 64 t - 64
-  auto wbase = [&](int t) { return p.M + w.i0 - BN * t - BN; };
+  // first distance of the window of local step t: M + i0 - 64 (t0 + t) - 64
+  auto wbase = [&](int t) { return p.M + w.i0 - BN * (t0 + t) - BN; };
 
   if (tid == 0) {
     if (blockIdx.x == 0) *p.gemm_ctr = 0u;  // read by the next launch on the stream only
@@ -232,8 +265,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tma_load_3d(dst, &tm_r, bar, 0, w.h, d0);
     tma_load_3d(dst + kHalfK, &tm_r, bar, 64, w.h, d0);
   };
-  // Inputs of step t into stage t & 1: keys and values [64 t, 64 t + 64) and
-  // the window's new distances [wb(t), wb(t) + 64).
+  // Inputs of local step t into stage t & 1: keys and values [64 (t0 + t),
+  // + 64) and the window's new distances [wb(t), wb(t) + 64).
   uint32_t n_in[2] = {0, 0};  // loads issued per stage (the load thread)
   auto load_in = [&](int t) {
     const int s = t & 1;
@@ -241,8 +274,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     mbar_arrive_expect_tx(&bars->in[s], kInStage);
 #pragma unroll
     for (int hh = 0; hh < 2; ++hh) {
-      tma_load_4d(st + hh * kHalfK, &tm_k, &bars->in[s], 64 * hh, w.h, BN * t, w.b);
-      tma_load_4d(st + 2 * kHalfK + hh * kHalfK, &tm_v, &bars->in[s], 64 * hh, w.h, BN * t, w.b);
+      tma_load_4d(st + hh * kHalfK, &tm_k, &bars->in[s], 64 * hh, w.h, BN * (t0 + t), w.b);
+      tma_load_4d(st + 2 * kHalfK + hh * kHalfK, &tm_v, &bars->in[s], 64 * hh, w.h, BN * (t0 + t), w.b);
     }
     load_r64(st + 4 * kHalfK, &bars->in[s], wbase(t));
     if (s == 0) ++n_in[0];
@@ -301,7 +334,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     ok = mbar_wait(&bars->q, 0, wait_ns, abort);
     if (ok) {
       __nv_bfloat16 *gqu = nullptr, *gqv = nullptr;
-      if (i < p.W) {
+      if (i < p.W && t0 == 0) {  // one CTA of a split unit writes them
         const size_t off = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D + 64 * half;
         gqu = p.Qu + off;
         gqv = p.Qv + off;
@@ -393,8 +426,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     // ============================ G / P stores ============================
     for (int t = 0; t < T && ok; ++t) {
       if (!(ok = mbar_wait(&bars->done[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
-      tma_store_3d(&tm_g, sG, BN * t, w.i0, z);
-      tma_store_3d(&tm_p, sP, BN * t, w.i0, z);
+      tma_store_3d(&tm_g, sG, BN * (t0 + t), w.i0, z);
+      tma_store_3d(&tm_p, sP, BN * (t0 + t), w.i0, z);
       bulk_commit_group();
       bulk_wait_group_read0();
       mbar_arrive(&bars->sfree);
@@ -404,7 +437,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
   } else if (tid < kPairThreads) {
     // ============================ pairs ===================================
     const size_t row = (static_cast<size_t>(z) * p.W + i) * p.LP;
-    if (i < p.W) {
+    if (i < p.W && t0 == 0) {
       // GS past the row's last distance M + i: the products read up to 191
       // columns beyond it (a 128-row tile plus a 64-deep k block), which must
       // hold zeros.  Key order needs none: every step writes all 64 columns.
@@ -420,7 +453,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       }
       tc_fence_after();
       float g[32], pr[32];
-      const int lim = p.M + i - BN * t;  // key column c of the step visible iff c <= lim
+      const int lim = p.M + i - BN * (t0 + t);  // key column c of the step visible iff c <= lim
       const int w0 = 32 * quad + (half ? 0 : 32);
       const uint32_t cw0 = win_col(w0, t), cw1 = win_col(w0 + 32, t);
       if (__all_sync(0xffffffffu, lim >= 32 * half + 31)) {  // no masked column in the warp's 32
@@ -436,11 +469,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
       stage_row32(sP, a, half, pr);
       __syncwarp();
       // GS: row r of the warp holds distances D0_r - 31 ... D0_r, with
-      // D0_r = M + i_warp + r - 64 t - 32 half, i.e. keys 32 half + 31 ... 32 half
+      // D0_r = M + i_warp + r - 64 (t0 + t) - 32 half, i.e. keys 32 half + 31 ... 32 half
       // of the staged G row; one row per pass, a distance per lane (64
       // contiguous bytes per store instruction).
       {
-        const int d_lane = p.M + i_warp - BN * t - 32 * half - 31 + lane;
+        const int d_lane = p.M + i_warp - BN * (t0 + t) - 32 * half - 31 + lane;
         const int key = 32 * half + 31 - lane;  // staged column this lane reads
         const int chunk = key >> 3;
         // rows [r_lo, r_hi) of the warp exist and have d >= 0 for this lane
@@ -929,6 +962,52 @@ int chunk_seqs(int B, int W, int M, int H) {
   return static_cast<int>(std::max<size_t>(1, std::min<size_t>(c, static_cast<size_t>(B))));
 }
 
+// How many of the longest query tiles the pair kernel runs as two CTAs per
+// unit (0-2).  CTAs start in launch order on whichever SM frees first, so the
+// launch is list scheduling over the SMs; its length is modelled with a CTA
+// costing its key steps plus 3 (the start and end of a CTA: about 6.7 us
+// against 2.25 us a step at the wide workload, B=8 H=8 W=M=768), and the
+// count with the shortest modelled launch is taken.  At wide, splitting the
+// last tile's 24-step units turns 384 CTAs of 14-24 steps into 448 and the
+// modelled length from 146 to 133 us.
+int pair_split_tiles(int nqt, int bh, int W, int M, int sms) {
+  if (bh <= 0 || sms <= 0 || static_cast<long long>(nqt + 2) * bh > 200000) return 0;
+  auto steps = [&](int qt) { return std::min(M + qt * BM + BM - 1, M + W - 1) / BN + 1; };
+  std::vector<long long> load(static_cast<size_t>(sms));
+  auto span = [&](int k) {
+    std::fill(load.begin(), load.end(), 0LL);
+    std::priority_queue<long long, std::vector<long long>, std::greater<long long>> heap(load.begin(), load.end());
+    auto put = [&](long long c) {
+      const long long l = heap.top();
+      heap.pop();
+      heap.push(l + c);
+    };
+    for (int qt = nqt - k - 1; qt >= 0; --qt)
+      for (int x = 0; x < bh; ++x) put(3 + steps(qt));
+    for (int j = 0; j < 2 * k; ++j) {
+      const int n = steps(nqt - 1 - (j >> 1));
+      for (int x = 0; x < bh; ++x) put(3 + ((j & 1) ? n - n / 2 : n / 2));
+    }
+    long long m = 0;
+    while (!heap.empty()) {
+      m = std::max(m, heap.top());
+      heap.pop();
+    }
+    return m;
+  };
+  int best = 0;
+  long long best_span = span(0);
+  for (int k = 1; k <= std::min(nqt, 2); ++k) {
+    if (steps(nqt - k) < 4) break;  // halves of at least two steps
+    const long long v = span(k);
+    if (v < best_span) {
+      best_span = v;
+      best = k;
+    }
+  }
+  return best;
+}
+
 // Bias partials: one per (sequence, 128-row block) of every chunk.
 size_t total_parts(int B, int W) { return static_cast<size_t>(B) * ((W + 127) / 128); }
 
@@ -1065,7 +1144,8 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     p.wait_ns = wc.limit_ns;
     p.inject_stall = b0 == 0 ? wc.inject_stall : 0;
     p.gemm_ctr = sc.ctr;
-    const long long units = static_cast<long long>(p.nqt) * nb * H;
+    p.split_qt = pair_split_tiles(p.nqt, nb * H, W, M, num_sms());
+    const long long units = static_cast<long long>(p.nqt + p.split_qt) * nb * H;
     if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
     if ((e = launch_dependent(bwd_scores128_kernel, dim3(static_cast<unsigned>(units)), dim3(kSThreads), kSSmem,
                               stream, tq, gm.b_k, tv, gm.b_r, tdo128, gm.a_g, tpk, p)) != cudaSuccess)
