@@ -410,9 +410,10 @@ def measure_backward(stream, wl, steps, warmup, peak, peak_src):
     events on its stream, L2 flushed between calls (outside the events)."""
     out = time_backward(stream.q[0], stream.k[0], stream.v[0], stream.r, stream.u, stream.vb, wl, steps, warmup,
                         peak, peak_src)
-    out["call"] = "txl_relattn_backward (dq kernel, dk/dv kernel, bias sums)"
+    out["call"] = ("txl_relattn_backward, D = 64 (pair-term kernel, one launch of the dq, dk, dv and dr "
+                   "products, bias sums)")
     out["gpu_launches_per_call"] = 3
-    out["roofline"]["kernel"] = "bwd_dq_tc64_kernel + bwd_dkdv_tc64_kernel"
+    out["roofline"]["kernel"] = "bwd_pairs_kernel<64> + bgemm_kernel<64> + bwd_bias_kernel (the whole call)"
     return out
 
 
@@ -437,7 +438,7 @@ def measure_backward_wide(device, steps, warmup, peak, peak_src):
     out["call"] = ("txl_relattn_backward, D = 128 (pair-term kernel, one launch of the dq, dk, dv and dr "
                    "products, bias sums)")
     out["gpu_launches_per_call"] = 3
-    out["roofline"]["kernel"] = "bwd_scores128_kernel + bgemm_kernel + bwd_bias_kernel (the whole call)"
+    out["roofline"]["kernel"] = "bwd_pairs_kernel<128> + bgemm_kernel<128> + bwd_bias_kernel (the whole call)"
     out["config"] = {"workload": "wide", "B": wl.B, "H": wl.H, "D": wl.D, "W": wl.W, "M": wl.M}
     return out
 

@@ -27,6 +27,7 @@ __all__ = [
     "txl_debug_set_wait_limit_ns", "txl_debug_inject_stall", "txl_debug_force_split",
     "txl_debug_set_bwd_chunk_bytes",
     "txl_debug_force_dense_tile_n",
+    "txl_debug_force_bwd_path",
 ]
 
 TXL_F32 = 0
@@ -105,6 +106,8 @@ lib.txl_debug_set_bwd_chunk_bytes.argtypes = [ctypes.c_ulonglong]
 lib.txl_debug_set_bwd_chunk_bytes.restype = _i
 lib.txl_debug_force_dense_tile_n.argtypes = [_i]
 lib.txl_debug_force_dense_tile_n.restype = _i
+lib.txl_debug_force_bwd_path.argtypes = [_i]
+lib.txl_debug_force_bwd_path.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -562,3 +565,9 @@ def txl_debug_force_dense_tile_n(bn):
     """Test hook: fix txl_dense's column tile (64, 128 or 256; 0: its cost
     model)."""
     _check(lib.txl_debug_force_dense_tile_n(int(bn)), "txl_debug_force_dense_tile_n")
+
+
+def txl_debug_force_bwd_path(path):
+    """Test hook: the bf16 D = 64 backward's path (1: fused kernels, 2: pair
+    terms materialised; 0: the library's choice)."""
+    _check(lib.txl_debug_force_bwd_path(int(path)), "txl_debug_force_bwd_path")

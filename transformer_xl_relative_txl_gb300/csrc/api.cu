@@ -26,6 +26,7 @@ __device__ unsigned int g_txl_status;
 std::atomic<unsigned long long> g_wait_ns{2000000000ULL};
 std::atomic<int> g_inject_stall{0};
 std::atomic<int> g_force_split{0};  // test hook: > 0 forces the D = 64 kernel's split count
+std::atomic<int> g_bwd_path{0};     // test hook: the bf16 D = 64 backward's path (1 fused, 2 pair terms, 0 the choice)
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
@@ -365,7 +366,13 @@ int txl_debug_inject_stall(int on) {
 }
 
 int txl_debug_set_bwd_chunk_bytes(unsigned long long bytes) {
-  txl::relattn_bwd_tc128_set_chunk_bytes(static_cast<size_t>(bytes));
+  txl::relattn_bwd_pairs_set_chunk_bytes(static_cast<size_t>(bytes));
+  return TXL_OK;
+}
+
+int txl_debug_force_bwd_path(int path) {
+  if (path < 0 || path > 2) return TXL_ERR_INVALID_ARG;
+  g_bwd_path.store(path);
   return TXL_OK;
 }
 
@@ -723,8 +730,13 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
   }
   void* scratch = nullptr;
   int* unused = nullptr;
-  if (dtype == TXL_BF16 && go_dtype == TXL_BF16 && D == 64) {
-    // tensor-core path
+  // bf16 on the tensor cores: the materialised pair terms where M % 8 == 0
+  // (D = 64 or 128), else at D = 64 the fused kernels; the test hook can
+  // send D = 64 to the fused kernels
+  const bool tc = dtype == TXL_BF16 && go_dtype == TXL_BF16;
+  const bool pairs = tc && txl::relattn_bwd_pairs_supported(W, M, D) && !(D == 64 && g_bwd_path.load() == 1);
+  if (tc && D == 64 && !pairs) {
+    // tensor-core path, fused
     if (split_scratch(stream, txl::relattn_bwd_tc64_scratch_bytes(B, W, H), 0, &scratch, &unused) != cudaSuccess)
       return TXL_ERR_CUDA;
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
@@ -783,9 +795,9 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
                                                   dk, dv, dr, dbias_u, dbias_v, B, W, M, H, n_r, scale, scratch, wc,
                                                   stream));
   }
-  if (dtype == TXL_BF16 && go_dtype == TXL_BF16 && D == 128 && txl::relattn_bwd_tc128_supported(W, M)) {
+  if (pairs) {
     // tensor-core path, pair terms materialised
-    if (split_scratch(stream, txl::relattn_bwd_tc128_scratch_bytes(B, W, M, H), 0, &scratch, &unused) !=
+    if (split_scratch(stream, txl::relattn_bwd_pairs_scratch_bytes(B, W, M, H, D), 0, &scratch, &unused) !=
         cudaSuccess)
       return TXL_ERR_CUDA;
     txl::WaitCtl wc;
@@ -793,8 +805,8 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
     wc.limit_ns = g_wait_ns.load();
     wc.inject_stall = g_inject_stall.exchange(0);
     if ((W + 127) / 128 * static_cast<long long>(B) * H > 0x7FFFFFFFLL) return TXL_ERR_UNSUPPORTED;
-    return from_cuda(txl::launch_relattn_bwd_tc128(tensor_map_encoder(), q, k, v, r, bias_u, bias_v, lse, o, dout,
-                                                   dq, dk, dv, dr, dbias_u, dbias_v, B, W, M, H, n_r, scale,
+    return from_cuda(txl::launch_relattn_bwd_pairs(tensor_map_encoder(), q, k, v, r, bias_u, bias_v, lse, o, dout,
+                                                   dq, dk, dv, dr, dbias_u, dbias_v, B, W, M, H, D, n_r, scale,
                                                    scratch, wc, stream));
   }
   if (split_scratch(stream, txl::relattn_bwd_simt_scratch_bytes(B, W, H, D), 0, &scratch, &unused) != cudaSuccess)

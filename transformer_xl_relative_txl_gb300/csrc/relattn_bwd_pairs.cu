@@ -52,7 +52,6 @@
 namespace txl {
 namespace {
 
-constexpr int D = 128;
 constexpr int BM = 128;  // query rows per tile
 constexpr int BN = 64;   // keys per step
 constexpr float kLog2e = 1.4426950408889634f;
@@ -60,8 +59,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------
 // 1. Score rebuild
 // ---------------------------------------------------------------------------
-// Shared memory: every D = 128 operand tile is two 64-column halves (128-byte
-// rows, 128-byte swizzle), the second half right after the first.  Inputs of
+// Shared memory: an operand tile of head dimension D is D / 64 tiles of 64
+// columns (128-byte rows, 128-byte swizzle), one after the other.  Inputs of
 // a step (64 keys, 64 values, 64 new distance rows) in two stages.  G and P
 // of a step leave through 128 x 64 staging tiles and TMA stores, GS (the same
 // g in distance order) through row-contiguous stores read from the G tile.
@@ -74,17 +73,22 @@ constexpr float kLog2e = 1.4426950408889634f;
 // computed.
 constexpr int kHalfQ = BM * 128;   // 128 rows x 64 bf16: 16 KB
 constexpr int kHalfK = BN * 128;   // 64 rows: 8 KB
-constexpr int kSOffQu = 0;
-constexpr int kSOffQv = kSOffQu + 2 * kHalfQ;
-constexpr int kSOffDO = kSOffQv + 2 * kHalfQ;
-constexpr int kSOffIn = kSOffDO + 2 * kHalfQ;   // stage s: K, V, R tiles (16 KB each)
-constexpr int kInStage = 6 * kHalfK;
-constexpr int kSOffG = kSOffIn + 2 * kInStage;  // G staging: 128 rows x 64 keys
-constexpr int kSOffP = kSOffG + BM * BN * 2;    // P staging
-constexpr int kSOffBar = kSOffP + BM * BN * 2;
-constexpr int kSOffBias = kSOffBar + 256;       // u, then v of the head (fp32)
-constexpr int kSSmem = kSOffBias + 2 * D * 4 + 1024;
-static_assert(kSSmem <= 232448, "shared memory budget");
+template <int D>
+struct PairCfg {
+  static constexpr int NH = D / 64;                          // 64-column tiles of an operand
+  static constexpr int kSOffQu = 0;
+  static constexpr int kSOffQv = kSOffQu + NH * kHalfQ;
+  static constexpr int kSOffDO = kSOffQv + NH * kHalfQ;
+  static constexpr int kSOffIn = kSOffDO + NH * kHalfQ;     // stage s: K, V, R tiles (NH x 8 KB each)
+  static constexpr int kInStage = 3 * NH * kHalfK;
+  static constexpr int kSOffG = kSOffIn + 2 * kInStage;     // G staging: 128 rows x 64 keys
+  static constexpr int kSOffP = kSOffG + BM * BN * 2;       // P staging
+  static constexpr int kSOffBar = kSOffP + BM * BN * 2;
+  static constexpr int kSOffBias = kSOffBar + 256;          // u, then v of the head (fp32)
+  static constexpr int kSSmem = kSOffBias + 2 * D * 4 + 1024;
+  static_assert(D == 64 || D == 128, "head dimension");
+  static_assert(kSSmem <= 232448, "shared memory budget");
+};
 constexpr uint32_t kColWin = 256, kSTmemCols = 512;
 constexpr int kPairThreads = 256;            // warps 0-7
 constexpr int kSThreads = kPairThreads + 96;  // + the load, MMA and store warps
@@ -142,20 +146,24 @@ struct SBars {
   int abort;
 };
 
-// Row a of (q+u) and (q+v) for the 64 head dims of half `half` (its own
-// 64-column tile of both), from the raw q tile staged in the same layout;
-// also written to gqu / gqv (the row's 64 dims, 16-byte aligned) unless null.
-__device__ __forceinline__ void build_half128(const uint8_t* sQ, uint8_t* sQu, uint8_t* sQv, int a, int half,
-                                              const float* bu, const float* bv, __nv_bfloat16* gqu,
-                                              __nv_bfloat16* gqv) {
-  const uint8_t* src = sQ + half * kHalfQ;
+// Row a of (q+u) and (q+v) for head dims [D/2 half, D/2 half + D/2) (the
+// warp half's share), from the raw q tile staged in the same layout as the
+// operand tiles; also written to gqu / gqv (the share's dims of the row,
+// 16-byte aligned) unless null.
+template <int D>
+__device__ __forceinline__ void build_half(const uint8_t* sQ, uint8_t* sQu, uint8_t* sQv, int a, int half,
+                                           const float* bu, const float* bv, __nv_bfloat16* gqu,
+                                           __nv_bfloat16* gqv) {
+  constexpr int CH = D / 16;  // 16-byte chunks (8 dims) of the share
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    const uint32_t off = (a >> 3) * 1024 + (a & 7) * 128 + ((c ^ (a & 7)) << 4);
-    const uint4 raw = *reinterpret_cast<const uint4*>(src + off);
+  for (int c = 0; c < CH; ++c) {
+    const int gc = half * CH + c;  // chunk of the row: dims 8 gc .. 8 gc + 7
+    const uint32_t off =
+        (gc >> 3) * kHalfQ + (a >> 3) * 1024 + (a & 7) * 128 + ((((gc & 7) ^ (a & 7))) << 4);
+    const uint4 raw = *reinterpret_cast<const uint4*>(sQ + off);
     const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-    const float* ub = bu + 64 * half + 8 * c;
-    const float* vb = bv + 64 * half + 8 * c;
+    const float* ub = bu + 8 * gc;
+    const float* vb = bv + 8 * gc;
     uint32_t qu[4], qv[4];
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
@@ -164,8 +172,8 @@ __device__ __forceinline__ void build_half128(const uint8_t* sQ, uint8_t* sQu, u
       qv[e] = pack_bf16x2(x0 + vb[2 * e], x1 + vb[2 * e + 1]);
     }
     const uint4 xu = make_uint4(qu[0], qu[1], qu[2], qu[3]), xv = make_uint4(qv[0], qv[1], qv[2], qv[3]);
-    *reinterpret_cast<uint4*>(sQu + half * kHalfQ + off) = xu;
-    *reinterpret_cast<uint4*>(sQv + half * kHalfQ + off) = xv;
+    *reinterpret_cast<uint4*>(sQu + off) = xu;
+    *reinterpret_cast<uint4*>(sQv + off) = xv;
     if (gqu != nullptr) {
       reinterpret_cast<uint4*>(gqu)[c] = xu;
       reinterpret_cast<uint4*>(gqv)[c] = xv;
@@ -203,24 +211,27 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 // and 32-63 of the same rows).  One thread of warp 8 issues the loads (two
 // steps ahead), one of warp 9 the MMAs (one step ahead of the pairs), one of
 // warp 10 the G / P stores, each waiting only on what it needs.
+template <int D>
 __global__ void __launch_bounds__(kSThreads, 1)
-    bwd_scores128_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                         const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
-                         const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_g,
-                         const __grid_constant__ CUtensorMap tm_p, const ScoreParams p) {
+    bwd_pairs_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_r,
+                     const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_g,
+                     const __grid_constant__ CUtensorMap tm_p, const ScoreParams p) {
+  using C = PairCfg<D>;
+  constexpr int NH = C::NH;
   grid_dep_wait();  // launched behind the previous kernel on the stream: it has completed from here on
   grid_dep_launch_dependents();  // the products' CTAs may take SMs this launch no longer needs
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  uint8_t* sQu = smem + kSOffQu;
-  uint8_t* sQv = smem + kSOffQv;
-  uint8_t* sDO = smem + kSOffDO;
-  uint8_t* sIn = smem + kSOffIn;
-  uint8_t* sG = smem + kSOffG;
-  uint8_t* sP = smem + kSOffP;
-  SBars* bars = reinterpret_cast<SBars*>(smem + kSOffBar);
-  float* sBias = reinterpret_cast<float*>(smem + kSOffBias);
+  uint8_t* sQu = smem + C::kSOffQu;
+  uint8_t* sQv = smem + C::kSOffQv;
+  uint8_t* sDO = smem + C::kSOffDO;
+  uint8_t* sIn = smem + C::kSOffIn;
+  uint8_t* sG = smem + C::kSOffG;
+  uint8_t* sP = smem + C::kSOffP;
+  SBars* bars = reinterpret_cast<SBars*>(smem + C::kSOffBar);
+  float* sBias = reinterpret_cast<float*>(smem + C::kSOffBias);
   volatile int* abort = &bars->abort;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int quad = warp & 3, half = warp >> 2;
@@ -260,24 +271,24 @@ __global__ void __launch_bounds__(kSThreads, 1)
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
 
-  // 64 distance rows from `d0` (both head-dim halves) into a 16 KB tile.
+  // 64 distance rows from `d0` (every 64-dim tile of them) into NH x 8 KB.
   auto load_r64 = [&](uint8_t* dst, uint64_t* bar, int d0) {
-    tma_load_3d(dst, &tm_r, bar, 0, w.h, d0);
-    tma_load_3d(dst + kHalfK, &tm_r, bar, 64, w.h, d0);
+#pragma unroll
+    for (int hh = 0; hh < NH; ++hh) tma_load_3d(dst + hh * kHalfK, &tm_r, bar, 64 * hh, w.h, d0);
   };
   // Inputs of local step t into stage t & 1: keys and values [64 (t0 + t),
   // + 64) and the window's new distances [wb(t), wb(t) + 64).
   uint32_t n_in[2] = {0, 0};  // loads issued per stage (the load thread)
   auto load_in = [&](int t) {
     const int s = t & 1;
-    uint8_t* st = sIn + s * kInStage;
-    mbar_arrive_expect_tx(&bars->in[s], kInStage);
+    uint8_t* st = sIn + s * C::kInStage;
+    mbar_arrive_expect_tx(&bars->in[s], C::kInStage);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
+    for (int hh = 0; hh < NH; ++hh) {
       tma_load_4d(st + hh * kHalfK, &tm_k, &bars->in[s], 64 * hh, w.h, BN * (t0 + t), w.b);
-      tma_load_4d(st + 2 * kHalfK + hh * kHalfK, &tm_v, &bars->in[s], 64 * hh, w.h, BN * (t0 + t), w.b);
+      tma_load_4d(st + (NH + hh) * kHalfK, &tm_v, &bars->in[s], 64 * hh, w.h, BN * (t0 + t), w.b);
     }
-    load_r64(st + 4 * kHalfK, &bars->in[s], wbase(t));
+    load_r64(st + 2 * NH * kHalfK, &bars->in[s], wbase(t));
     if (s == 0) ++n_in[0];
     else ++n_in[1];
   };
@@ -293,16 +304,16 @@ __global__ void __launch_bounds__(kSThreads, 1)
     tma_prefetch_desc(&tm_g);
     tma_prefetch_desc(&tm_p);
     // the raw q tile goes to stage 1 until (q+u), (q+v) are built
-    mbar_arrive_expect_tx(&bars->q, 4 * kHalfQ);
+    mbar_arrive_expect_tx(&bars->q, 2 * NH * kHalfQ);
 #pragma unroll
-    for (int hh = 0; hh < 2; ++hh) {
-      tma_load_4d(sIn + kInStage + hh * kHalfQ, &tm_q, &bars->q, 64 * hh, w.h, w.i0, w.b);
+    for (int hh = 0; hh < NH; ++hh) {
+      tma_load_4d(sIn + C::kInStage + hh * kHalfQ, &tm_q, &bars->q, 64 * hh, w.h, w.i0, w.b);
       tma_load_4d(sDO + hh * kHalfQ, &tm_do, &bars->q, 64 * hh, w.h, w.i0, w.b);
     }
     load_in(0);
     // the rest of step 0's window (distances wb(0) + 64 ... + 192) into the
     // staging tiles, which are free until step 0's pairs are written
-    mbar_arrive_expect_tx(&bars->x, 2 * 2 * kHalfK);
+    mbar_arrive_expect_tx(&bars->x, 2 * NH * kHalfK);
     load_r64(sG, &bars->x, wbase(0) + 64);
     load_r64(sP, &bars->x, wbase(0) + 128);
   }
@@ -335,11 +346,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
     if (ok) {
       __nv_bfloat16 *gqu = nullptr, *gqv = nullptr;
       if (i < p.W && t0 == 0) {  // one CTA of a split unit writes them
-        const size_t off = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D + 64 * half;
+        const size_t off = ((static_cast<size_t>(w.b) * p.W + i) * p.H + w.h) * D + (D / 2) * half;
         gqu = p.Qu + off;
         gqv = p.Qv + off;
       }
-      build_half128(sIn + kInStage, sQu, sQv, a, half, sBias, sBias + D, gqu, gqv);
+      build_half<D>(sIn + C::kInStage, sQu, sQv, a, half, sBias, sBias + D, gqu, gqv);
     } else {
       report_timeout(abort, p.status);
     }
@@ -360,30 +371,30 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const uint64_t dR = sdesc_sw128(smem_u32(rtile), 16, 1024);
     const uint32_t col = win_col(64 * k, t);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < 4 * NH; ++kk) {
       const uint64_t off = (kk >> 2) * (kHalfQ >> 4) + (kk & 3) * 2;
       mma_ss(tmem + col, dQv + off, dR + (kk >> 2) * (kHalfK >> 4) + (kk & 3) * 2, id64, kk > 0);
     }
   };
-  // Thread 0: the MMAs of step t (K = 128 as two 64-column halves of every
-  // operand): S and dP into buffer t & 1, the window's new distances.
+  // Thread 0: the MMAs of step t (K = D as D / 64 tiles of 64 columns of
+  // every operand): S and dP into buffer t & 1, the window's new distances.
   auto score_mmas = [&](int t) -> bool {
     const int s = t & 1;
     if (!mbar_wait(&bars->in[s], (t >> 1) & 1, wait_ns, abort)) return false;
     if (t == 0 && !mbar_wait(&bars->x, 0, wait_ns, abort)) return false;
     tc_fence_after();
-    const uint8_t* st = sIn + s * kInStage;
+    const uint8_t* st = sIn + s * C::kInStage;
     const uint64_t dK = sdesc_sw128(smem_u32(st), 16, 1024);
-    const uint64_t dV = sdesc_sw128(smem_u32(st + 2 * kHalfK), 16, 1024);
+    const uint64_t dV = sdesc_sw128(smem_u32(st + NH * kHalfK), 16, 1024);
     const uint32_t colS = 128 * s, colDP = 128 * s + 64;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) {
+    for (int kk = 0; kk < 4 * NH; ++kk) {
       const uint64_t qa = (kk >> 2) * (kHalfQ >> 4) + (kk & 3) * 2;
       const uint64_t ka = (kk >> 2) * (kHalfK >> 4) + (kk & 3) * 2;
       mma_ss(tmem + colS, dQu + qa, dK + ka, id64, kk > 0);
       mma_ss(tmem + colDP, dDO + qa, dV + ka, id64, kk > 0);
     }
-    win_mma(st + 4 * kHalfK, 0, t);
+    win_mma(st + 2 * NH * kHalfK, 0, t);
     if (t == 0) {
       win_mma(sG, 1, 0);
       win_mma(sP, 2, 0);
@@ -511,11 +522,11 @@ __global__ void __launch_bounds__(kSThreads, 1)
 // 2. The gradient products
 // ---------------------------------------------------------------------------
 // One persistent launch runs all four products, one CTA per SM, 192 threads:
-// warp 0 loads (TMA), warp 1 issues the MMAs (M = 128, N = D = 128, K = 16,
-// into one of two TMEM accumulator slots), warps 2-5 move the fp32
-// accumulator rows to global memory.  A stage holds 64 k of A (a 128 x 64
-// K-major tile, or two 64 k x 64 row MN-major tiles) and of B (two 64 k x 64
-// column N-major tiles).
+// warp 0 loads (TMA), warp 1 issues the MMAs (M = 128, N = D, K = 16, into
+// one of two TMEM accumulator slots), warps 2-5 move the fp32 accumulator
+// rows to global memory.  A stage holds 64 k of A (a 128 x 64 K-major tile,
+// or two 64 k x 64 row MN-major tiles) and of B (D / 64 tiles of 64 k x 64
+// columns, N-major).
 //
 // The tiles of the four products differ in length by up to 48 times (a DR
 // tile streams every sequence's queries, a DK tile near the end of the
@@ -527,19 +538,24 @@ __global__ void __launch_bounds__(kSThreads, 1)
 enum BMode { kModeDQ = 0, kModeDK = 1, kModeDV = 2, kModeDR = 3 };
 constexpr int kGATile = 128 * 128;  // 16 KB
 constexpr int kGBBlock = 64 * 128;  // 8 KB
-constexpr int kGStage = kGATile + 2 * kGBBlock;
-constexpr int kGStages = 6;
 constexpr int kGTq = 8;  // slots of the tile-index queue from the loader to the MMA and epilogue warps
-constexpr int kGOffEpi = kGStages * kGStage;          // DQ: 4 epilogue warps x 32 x 32 fp32 (column sums)
-constexpr int kGOffRed = kGOffEpi + 4 * 32 * 32 * 4;  // DQ: [4 warps][2 parts][128] warp sums
-constexpr int kGOffBar = kGOffRed + 4 * 2 * 128 * 4;
-constexpr int kGSmem = kGOffBar + 512 + 1024;
 constexpr int kGThreads = 192;
-static_assert(kGSmem <= 232448, "shared memory budget");
-// TMEM: two accumulator slots of 2 D columns; a DQ tile fills its slot with
-// both of its parts (key, distance), the other products use the first D.
-constexpr uint32_t kGAccCols = 2 * D;
-constexpr uint32_t kGTmemCols = 2 * kGAccCols;
+template <int D>
+struct GemmCfg {
+  static constexpr int NH = D / 64;
+  static constexpr int kGStage = kGATile + NH * kGBBlock;
+  static constexpr int kGStages = D == 128 ? 6 : 8;  // at most kGMaxStages
+  static constexpr int kGOffEpi = kGStages * kGStage;          // DQ: 4 epilogue warps x 32 x 32 fp32 (column sums)
+  static constexpr int kGOffRed = kGOffEpi + 4 * 32 * 32 * 4;  // DQ: [4 warps][2 parts][128] warp sums
+  static constexpr int kGOffBar = kGOffRed + 4 * 2 * 128 * 4;
+  static constexpr int kGSmem = kGOffBar + 512 + 1024;
+  static_assert(kGSmem <= 232448, "shared memory budget");
+  // TMEM: two accumulator slots of 2 D columns; a DQ tile fills its slot
+  // with both of its parts (key, distance), the other products use the
+  // first D.
+  static constexpr uint32_t kGAccCols = 2 * D;
+  static constexpr uint32_t kGTmemCols = 2 * kGAccCols;
+};
 
 struct GemmArgs {
   int B, W, M, H, L;
@@ -601,8 +617,9 @@ __device__ __forceinline__ GTile gtile(const GemmArgs& p, int u) {
   return r;
 }
 
+constexpr int kGMaxStages = 8;
 struct GBars {
-  uint64_t full[kGStages], empty[kGStages];
+  uint64_t full[kGMaxStages], empty[kGMaxStages];
   uint64_t acc_full[2], acc_empty[2];
   uint64_t tq_full[kGTq], tq_empty[kGTq];
   uint64_t done;
@@ -626,17 +643,22 @@ struct GMaps {
 // every one, the last (>= total) telling them to stop.
 __device__ __forceinline__ int tq_read(GBars* bars, uint32_t n) { return *reinterpret_cast<volatile int*>(&bars->tq[n % kGTq]); }
 
+template <int D>
 __global__ void __launch_bounds__(kGThreads, 1)
     bgemm_kernel(const __grid_constant__ GMaps maps, const GemmArgs p) {
+  using GC = GemmCfg<D>;
+  constexpr int NH = GC::NH;
+  constexpr int kGStage = GC::kGStage, kGOffEpi = GC::kGOffEpi, kGOffRed = GC::kGOffRed;
+  constexpr uint32_t kGAccCols = GC::kGAccCols, kGTmemCols = GC::kGTmemCols;
   grid_dep_wait();  // launched behind the pair kernel: its pair terms and the zeroed counter
   grid_dep_launch_dependents();
   extern __shared__ uint8_t smem_raw[];
   const uint32_t pad = (1024u - (smem_u32(smem_raw) & 1023u)) & 1023u;
   uint8_t* smem = smem_raw + pad;
-  GBars* bars = reinterpret_cast<GBars*>(smem + kGOffBar);
+  GBars* bars = reinterpret_cast<GBars*>(smem + GC::kGOffBar);
   volatile int* abort = &bars->abort;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  constexpr int S = kGStages;
+  constexpr int S = GC::kGStages;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
@@ -701,12 +723,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
             const int k0 = 64 * (dist ? kk - g.nkb_c : kk);
             if (!dist) {
               tma_load_3d(st, &maps.a_g, bar, k0, g.m0, g.z);
-              tma_load_4d(sb, &maps.b_k, bar, 0, h, k0, b);
-              tma_load_4d(sb + kGBBlock, &maps.b_k, bar, 64, h, k0, b);
+#pragma unroll
+              for (int j = 0; j < NH; ++j) tma_load_4d(sb + j * kGBBlock, &maps.b_k, bar, 64 * j, h, k0, b);
             } else {
               tma_load_3d(st, &maps.a_gs, bar, k0, g.m0, g.z);
-              tma_load_3d(sb, &maps.b_r, bar, 0, h, k0);
-              tma_load_3d(sb + kGBBlock, &maps.b_r, bar, 64, h, k0);
+#pragma unroll
+              for (int j = 0; j < NH; ++j) tma_load_3d(sb + j * kGBBlock, &maps.b_r, bar, 64 * j, h, k0);
             }
           } else {
             int bb = b, k0 = 64 * (g.kb0 + kk), x0 = g.m0, zz = g.z;
@@ -719,8 +741,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             }
             tma_load_3d(st, ma, bar, x0, k0, zz);
             tma_load_3d(st + kGATile / 2, ma, bar, x0 + 64, k0, zz);
-            tma_load_4d(sb, mb, bar, 0, h, k0, bb);
-            tma_load_4d(sb + kGBBlock, mb, bar, 64, h, k0, bb);
+#pragma unroll
+            for (int j = 0; j < NH; ++j) tma_load_4d(sb + j * kGBBlock, mb, bar, 64 * j, h, k0, bb);
           }
         }
       }
@@ -851,11 +873,13 @@ __global__ void __launch_bounds__(kGThreads, 1)
         {
           const int et = threadIdx.x - 64;  // epilogue thread 0 .. 127: one column of each part
           float* pp = p.part + ((static_cast<size_t>(b) * p.nmt + g.m0 / 128) * p.H + h) * 2 * D;
+          if (et < D) {
 #pragma unroll
-          for (int part = 0; part < 2; ++part)
-            pp[part * D + et] = ((wred[(0 * 2 + part) * 128 + et] + wred[(1 * 2 + part) * 128 + et]) +
-                                 wred[(2 * 2 + part) * 128 + et]) +
-                                wred[(3 * 2 + part) * 128 + et];
+            for (int part = 0; part < 2; ++part)
+              pp[part * D + et] = ((wred[(0 * 2 + part) * 128 + et] + wred[(1 * 2 + part) * 128 + et]) +
+                                   wred[(2 * 2 + part) * 128 + et]) +
+                                  wred[(3 * 2 + part) * 128 + et];
+          }
         }
         named_bar_sync(2, 128);  // the sums are read before the next DQ tile writes them
         continue;
@@ -923,7 +947,7 @@ int num_sms() {
 
 size_t round256(size_t x) { return (x + 255) & ~size_t(255); }
 
-struct Scratch128 {
+struct PairScratch {
   __nv_bfloat16 *G, *P, *GS, *Qu, *Qv;
   float* part;
   unsigned int* ctr;  // the products' tile counter
@@ -931,7 +955,7 @@ struct Scratch128 {
 };
 
 // Scratch of one chunk of Bc sequences, then the bias partials of all chunks.
-Scratch128 carve(void* base, int Bc, int W, int M, int H, size_t n_part) {
+PairScratch carve(void* base, int Bc, int W, int M, int H, int D, size_t n_part) {
   const size_t L = static_cast<size_t>(M) + W, LP = (L + 63) / 64 * 64;
   const size_t bh = static_cast<size_t>(Bc) * H, bwhd = static_cast<size_t>(Bc) * W * H * D;
   size_t off = 0;
@@ -940,7 +964,7 @@ Scratch128 carve(void* base, int Bc, int W, int M, int H, size_t n_part) {
     off += round256(bytes);
     return static_cast<char*>(base) + at;
   };
-  Scratch128 s;
+  PairScratch s;
   s.G = reinterpret_cast<__nv_bfloat16*>(take(bh * W * LP * 2));
   s.P = reinterpret_cast<__nv_bfloat16*>(take(bh * W * LP * 2));
   s.GS = reinterpret_cast<__nv_bfloat16*>(take(bh * W * LP * 2));
@@ -956,8 +980,8 @@ Scratch128 carve(void* base, int Bc, int W, int M, int H, size_t n_part) {
 // (at least one).  Later chunks reuse the scratch; dr accumulates over them.
 std::atomic<size_t> g_chunk_cap{size_t(1) << 30};
 
-int chunk_seqs(int B, int W, int M, int H) {
-  const size_t one = carve(nullptr, 1, W, M, H, 0).bytes;
+int chunk_seqs(int B, int W, int M, int H, int D) {
+  const size_t one = carve(nullptr, 1, W, M, H, D, 0).bytes;
   const size_t c = g_chunk_cap.load() / (one == 0 ? 1 : one);
   return static_cast<int>(std::max<size_t>(1, std::min<size_t>(c, static_cast<size_t>(B))));
 }
@@ -1011,14 +1035,17 @@ int pair_split_tiles(int nqt, int bh, int W, int M, int sms) {
 // Bias partials: one per (sequence, 128-row block) of every chunk.
 size_t total_parts(int B, int W) { return static_cast<size_t>(B) * ((W + 127) / 128); }
 
+template <int D>
 cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) {
+  constexpr int kGSmem = GemmCfg<D>::kGSmem;
   static std::atomic<bool> attr_done[64];
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   if (!attr_done[dev].load()) {
-    if ((e = cudaFuncSetAttribute(bgemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem)) != cudaSuccess)
+    if ((e = cudaFuncSetAttribute(bgemm_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kGSmem)) !=
+        cudaSuccess)
       return e;
     attr_done[dev].store(true);
   }
@@ -1026,29 +1053,33 @@ cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) 
   if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   p.total = static_cast<int>(total);
   const int grid = std::min(p.total, num_sms());
-  return launch_dependent(bgemm_kernel, dim3(grid), dim3(kGThreads), kGSmem, stream, maps, p);
+  return launch_dependent(bgemm_kernel<D>, dim3(grid), dim3(kGThreads), kGSmem, stream, maps, p);
 }
 
 }  // namespace
 
-void relattn_bwd_tc128_set_chunk_bytes(size_t bytes) { g_chunk_cap.store(bytes == 0 ? size_t(1) << 30 : bytes); }
+void relattn_bwd_pairs_set_chunk_bytes(size_t bytes) { g_chunk_cap.store(bytes == 0 ? size_t(1) << 30 : bytes); }
 
-size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H) {
-  const int Bc = chunk_seqs(B, W, M, H);
-  return carve(nullptr, Bc, W, M, H, total_parts(B, W)).bytes;
+size_t relattn_bwd_pairs_scratch_bytes(int B, int W, int M, int H, int D) {
+  const int Bc = chunk_seqs(B, W, M, H, D);
+  return carve(nullptr, Bc, W, M, H, D, total_parts(B, W)).bytes;
 }
 
-bool relattn_bwd_tc128_supported(int W, int M) { return W > 0 && M % 8 == 0; }
+bool relattn_bwd_pairs_supported(int W, int M, int D) { return W > 0 && M % 8 == 0 && (D == 64 || D == 128); }
 
-cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
-                                     const void* v, const void* r, const float* bias_u, const float* bias_v,
-                                     const float* lse, const void* o, const void* dout, float* dq, float* dk,
-                                     float* dv, float* dr, float* du, float* dvb, int B, int W, int M, int H,
-                                     int n_r, float scale, void* scratch, const WaitCtl& wc, cudaStream_t stream) {
-  if (encode == nullptr || !relattn_bwd_tc128_supported(W, M)) return cudaErrorInvalidValue;
+namespace {
+
+template <int D>
+cudaError_t launch_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k, const void* v,
+                         const void* r, const float* bias_u, const float* bias_v, const float* lse, const void* o,
+                         const void* dout, float* dq, float* dk, float* dv, float* dr, float* du, float* dvb, int B,
+                         int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
+                         cudaStream_t stream) {
+  if (encode == nullptr || !relattn_bwd_pairs_supported(W, M, D)) return cudaErrorInvalidValue;
+  constexpr int kSSmem = PairCfg<D>::kSSmem;
   const int L = M + W, LP = (L + 63) / 64 * 64;
-  const int Bc = chunk_seqs(B, W, M, H);
-  const Scratch128 sc = carve(scratch, Bc, W, M, H, total_parts(B, W));
+  const int Bc = chunk_seqs(B, W, M, H, D);
+  const PairScratch sc = carve(scratch, Bc, W, M, H, D, total_parts(B, W));
   const cuuint64_t hd2 = static_cast<cuuint64_t>(H) * D * 2;
   bool ok = true;
   auto enc = [&](CUtensorMap* m, const void* base, int rank, std::initializer_list<cuuint64_t> dims,
@@ -1093,7 +1124,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
     if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!attr_done[dev].load()) {
-      if ((e = cudaFuncSetAttribute(bwd_scores128_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSSmem)) !=
+      if ((e = cudaFuncSetAttribute(bwd_pairs_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSSmem)) !=
           cudaSuccess)
         return e;
       attr_done[dev].store(true);
@@ -1147,7 +1178,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     p.split_qt = pair_split_tiles(p.nqt, nb * H, W, M, num_sms());
     const long long units = static_cast<long long>(p.nqt + p.split_qt) * nb * H;
     if (units > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-    if ((e = launch_dependent(bwd_scores128_kernel, dim3(static_cast<unsigned>(units)), dim3(kSThreads), kSSmem,
+    if ((e = launch_dependent(bwd_pairs_kernel<D>, dim3(static_cast<unsigned>(units)), dim3(kSThreads), kSSmem,
                               stream, tq, gm.b_k, tv, gm.b_r, tdo128, gm.a_g, tpk, p)) != cudaSuccess)
       return e;
     // 2. the products, one launch: DR, DQ, DK and DV tiles from the counter
@@ -1174,7 +1205,7 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
     g.ctr = sc.ctr;
     g.status = wc.status;
     g.wait_ns = wc.limit_ns;
-    if ((e = launch_products(gm, g, stream)) != cudaSuccess) return e;
+    if ((e = launch_products<D>(gm, g, stream)) != cudaSuccess) return e;
   }
   if (n_r > L &&
       (e = cudaMemsetAsync(dr + static_cast<size_t>(L) * H * D, 0, static_cast<size_t>(n_r - L) * H * D * 4,
@@ -1183,6 +1214,22 @@ cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, c
   const size_t n_part = total_parts(B, W);
   if (n_part > 0x7FFFFFFF) return cudaErrorInvalidValue;
   return launch_bwd_bias(sc.part, static_cast<int>(n_part), H, D, du, dvb, stream);
+}
+
+}  // namespace
+
+cudaError_t launch_relattn_bwd_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
+                                     const void* v, const void* r, const float* bias_u, const float* bias_v,
+                                     const float* lse, const void* o, const void* dout, float* dq, float* dk,
+                                     float* dv, float* dr, float* du, float* dvb, int B, int W, int M, int H, int D,
+                                     int n_r, float scale, void* scratch, const WaitCtl& wc, cudaStream_t stream) {
+  if (D == 64)
+    return launch_pairs<64>(encode, q, k, v, r, bias_u, bias_v, lse, o, dout, dq, dk, dv, dr, du, dvb, B, W, M, H,
+                            n_r, scale, scratch, wc, stream);
+  if (D == 128)
+    return launch_pairs<128>(encode, q, k, v, r, bias_u, bias_v, lse, o, dout, dq, dk, dv, dr, du, dvb, B, W, M, H,
+                             n_r, scale, scratch, wc, stream);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace txl

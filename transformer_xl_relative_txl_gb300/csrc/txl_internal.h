@@ -138,23 +138,23 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
                                     int W, int M, int H, int n_r, float scale, void* scratch, const WaitCtl& wc,
                                     cudaStream_t stream);
 
-// Backward on the tensor cores, bf16 inputs, o and dout, D = 128
-// (relattn_bwd_tc128.cu): the pair terms are materialised in bf16 scratch and
-// the five gradient products run as tensor-core GEMMs.  Needs M % 8 == 0 (the
-// key columns of the pair terms are read from column M on by 16-byte aligned
+// Backward on the tensor cores, bf16 inputs, o and dout, D = 64 or 128
+// (relattn_bwd_pairs.cu): the pair terms are materialised in bf16 scratch and
+// the gradient products run as tensor-core GEMMs.  Needs M % 8 == 0 (the key
+// columns of the pair terms are read from column M on by 16-byte aligned
 // tensor copies).  Encodes its own tensor maps with `encode`.  Every output is
 // written in full (dr rows >= M + W are zeroed).
-// scratch: relattn_bwd_tc128_scratch_bytes(B, W, M, H) bytes.
+// scratch: relattn_bwd_pairs_scratch_bytes(B, W, M, H, D) bytes.
 // The scratch holds one chunk of sequences (as many as keep it within 1 GiB,
 // at least one); the chunks run one after the other and dr accumulates over
-// them.  relattn_bwd_tc128_set_chunk_bytes changes the cap (0: the default).
-size_t relattn_bwd_tc128_scratch_bytes(int B, int W, int M, int H);
-void relattn_bwd_tc128_set_chunk_bytes(size_t bytes);
-bool relattn_bwd_tc128_supported(int W, int M);
-cudaError_t launch_relattn_bwd_tc128(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
+// them.  relattn_bwd_pairs_set_chunk_bytes changes the cap (0: the default).
+size_t relattn_bwd_pairs_scratch_bytes(int B, int W, int M, int H, int D);
+void relattn_bwd_pairs_set_chunk_bytes(size_t bytes);
+bool relattn_bwd_pairs_supported(int W, int M, int D);
+cudaError_t launch_relattn_bwd_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
                                      const void* v, const void* r, const float* bias_u, const float* bias_v,
                                      const float* lse, const void* o, const void* dout, float* dq, float* dk,
-                                     float* dv, float* dr, float* du, float* dvb, int B, int W, int M, int H,
+                                     float* dv, float* dr, float* du, float* dvb, int B, int W, int M, int H, int D,
                                      int n_r, float scale, void* scratch, const WaitCtl& wc, cudaStream_t stream);
 
 // The layer's dense products on the tensor cores (gemm_tc.cu): row-major
