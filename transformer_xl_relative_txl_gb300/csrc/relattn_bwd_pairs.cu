@@ -81,7 +81,8 @@ struct PairCfg {
   static constexpr int kSOffDO = kSOffQv + NH * kHalfQ;
   static constexpr int kSOffIn = kSOffDO + NH * kHalfQ;     // stage s: K, V, R tiles (NH x 8 KB each)
   static constexpr int kInStage = 3 * NH * kHalfK;
-  static constexpr int kSOffG = kSOffIn + 2 * kInStage;     // G staging: 128 rows x 64 keys
+  static constexpr int NS = D == 64 ? 3 : 2;                // input stages (loads run NS steps ahead)
+  static constexpr int kSOffG = kSOffIn + NS * kInStage;    // G staging: 128 rows x 64 keys
   static constexpr int kSOffP = kSOffG + BM * BN * 2;       // P staging
   static constexpr int kSOffBar = kSOffP + BM * BN * 2;
   static constexpr int kSOffBias = kSOffBar + 256;          // u, then v of the head (fp32)
@@ -141,7 +142,8 @@ __device__ __forceinline__ Unit pair_item(int u, const ScoreParams& p) {
 }
 
 struct SBars {
-  uint64_t q, in[2], x, m1[2], done[2], sfree, fin;
+  uint64_t q, in[3], x, m1[2], done[2], sfree, fin;
+  uint64_t ifree[3];  // input stage s read by the MMAs of its step (one phase per use)
   uint32_t tmem_base;
   int abort;
 };
@@ -249,8 +251,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   if (tid == 0) {
     if (blockIdx.x == 0) *p.gemm_ctr = 0u;  // read by the next launch on the stream only
     mbar_init(&bars->q, 1);
-    mbar_init(&bars->in[0], 1);
-    mbar_init(&bars->in[1], 1);
+    for (int x = 0; x < C::NS; ++x) {
+      mbar_init(&bars->in[x], 1);
+      mbar_init(&bars->ifree[x], 1);
+    }
     mbar_init(&bars->x, 1);
     mbar_init(&bars->m1[0], 1);
     mbar_init(&bars->m1[1], 1);
@@ -278,9 +282,10 @@ __global__ void __launch_bounds__(kSThreads, 1)
   };
   // Inputs of local step t into stage t & 1: keys and values [64 (t0 + t),
   // + 64) and the window's new distances [wb(t), wb(t) + 64).
-  uint32_t n_in[2] = {0, 0};  // loads issued per stage (the load thread)
+  constexpr int NS = C::NS;
+  uint32_t n_in[3] = {0, 0, 0};  // loads issued per stage (the load thread)
   auto load_in = [&](int t) {
-    const int s = t & 1;
+    const int s = t % NS;
     uint8_t* st = sIn + s * C::kInStage;
     mbar_arrive_expect_tx(&bars->in[s], C::kInStage);
 #pragma unroll
@@ -289,8 +294,9 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tma_load_4d(st + (NH + hh) * kHalfK, &tm_v, &bars->in[s], 64 * hh, w.h, BN * (t0 + t), w.b);
     }
     load_r64(st + 2 * NH * kHalfK, &bars->in[s], wbase(t));
-    if (s == 0) ++n_in[0];
-    else ++n_in[1];
+    if (s == 0) ++n_in[0];  // constant indices keep the counts in registers
+    else if (s == 1) ++n_in[1];
+    else ++n_in[2];
   };
   // one thread of each of warps 8-10: loads, MMAs, stores
   const bool loader = tid == kPairThreads, mma_thread = tid == kPairThreads + 32,
@@ -311,6 +317,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       tma_load_4d(sDO + hh * kHalfQ, &tm_do, &bars->q, 64 * hh, w.h, w.i0, w.b);
     }
     load_in(0);
+    if (NS == 3 && T > 2 && !p.inject_stall) load_in(2);  // stage 2 is free from the start
     // the rest of step 0's window (distances wb(0) + 64 ... + 192) into the
     // staging tiles, which are free until step 0's pairs are written
     mbar_arrive_expect_tx(&bars->x, 2 * NH * kHalfK);
@@ -379,11 +386,12 @@ __global__ void __launch_bounds__(kSThreads, 1)
   // Thread 0: the MMAs of step t (K = D as D / 64 tiles of 64 columns of
   // every operand): S and dP into buffer t & 1, the window's new distances.
   auto score_mmas = [&](int t) -> bool {
-    const int s = t & 1;
-    if (!mbar_wait(&bars->in[s], (t >> 1) & 1, wait_ns, abort)) return false;
+    const int s = t & 1;       // S / dP buffer
+    const int si = t % NS;     // input stage
+    if (!mbar_wait(&bars->in[si], (t / NS) & 1, wait_ns, abort)) return false;
     if (t == 0 && !mbar_wait(&bars->x, 0, wait_ns, abort)) return false;
     tc_fence_after();
-    const uint8_t* st = sIn + s * C::kInStage;
+    const uint8_t* st = sIn + si * C::kInStage;
     const uint64_t dK = sdesc_sw128(smem_u32(st), 16, 1024);
     const uint64_t dV = sdesc_sw128(smem_u32(st + NH * kHalfK), 16, 1024);
     const uint32_t colS = 128 * s, colDP = 128 * s + 64;
@@ -400,25 +408,28 @@ __global__ void __launch_bounds__(kSThreads, 1)
       win_mma(sP, 2, 0);
     }
     tc_commit(&bars->m1[s]);
+    tc_commit(&bars->ifree[si]);
     return true;
   };
 
   // Barrier phases cannot be skipped: the MMAs of step t + 2 wait for the
   // pairs of step t (done), the pairs of step t + 1 for the staging of step t
-  // (sfree), the loads of step t + 2 for the MMAs of step t (m1), and each
-  // of those is what lets the next phase of the same barrier happen.
+  // (sfree), the loads of step t + NS for the MMAs of step t (ifree), and
+  // each of those is what lets the next phase of the same barrier happen.
   if (loader) {
     // ============================ loads ===================================
     if (ok && T > 1) load_in(1);  // the raw q has been read: stage 1 is free
-    for (int t = 0; t + 2 < T && ok && !p.inject_stall; ++t) {
-      // step t's MMAs have read stage t & 1: refill it for step t + 2
-      if (!(ok = mbar_wait(&bars->m1[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
-      load_in(t + 2);
+    for (int t = 0; t + NS < T && ok && !p.inject_stall; ++t) {
+      // step t's MMAs have read stage t % NS: refill it for step t + NS
+      // (the next phase of ifree[t % NS] needs that load, so none is skipped)
+      if (!(ok = mbar_wait(&bars->ifree[t % NS], (t / NS) & 1, wait_ns, abort))) break;
+      load_in(t + NS);
     }
     if (!ok) report_timeout(abort, p.status);
     // Let this CTA's own copies finish before the memory is released.
-    if (n_in[0] > 0) mbar_wait_own(&bars->in[0], (n_in[0] - 1) & 1, wait_ns);
-    if (n_in[1] > 0) mbar_wait_own(&bars->in[1], (n_in[1] - 1) & 1, wait_ns);
+#pragma unroll
+    for (int x = 0; x < NS; ++x)
+      if (n_in[x] > 0) mbar_wait_own(&bars->in[x], (n_in[x] - 1) & 1, wait_ns);
     mbar_wait_own(&bars->x, 0, wait_ns);
     mbar_wait_own(&bars->q, 0, wait_ns);
   } else if (mma_thread) {
