@@ -1,5 +1,6 @@
-// Backward of the relative attention on the tensor cores for D = 128: bf16
-// q, k, v, r, o and dout, fp32 accumulation and gradients.
+// Backward of the relative attention on the tensor cores with the pair terms
+// materialised, for head dimension D = 64 or 128 (memory length a multiple
+// of 8): bf16 q, k, v, r, o and dout, fp32 accumulation and gradients.
 //
 // The formulas and the stop-gradient are those of relattn_bwd.cu ("Transformer-
 // XL, explained", method step 2 and the symbol SG(.)):
@@ -9,18 +10,20 @@
 //   dr_d = sum_{b,i} g_{i, M+i-d} (q_i+v),  du = sum_{b,i} sum_j g_ij k_j,
 //   dbias_v = sum_{b,i} sum_j g_ij r_{M+i-j}
 //
-// At D = 128 the fused D = 64 design does not fit (the tiles of both score
-// operands and the gradient accumulators exceed the shared and tensor
-// memory), so the work is split in three:
-//   1. bwd_scores128_kernel, one CTA per (batch, head, 128-query tile), 64-key
-//      steps: S = (q+u) K^T, dP = dout V^T and the step's 64 new distances of
-//      the 192-distance window (q+v) R^T on the tensor cores (K = 128), then
-//      per pair p and g with the distance term shifted into key order as in
-//      the forward.  It writes, in bf16, G [bh][i][j] and P [bh][i][j] (key
-//      order), GS [bh][i][d] (the same g in distance order, d = M+i-j), and
-//      (q+u), (q+v) as the MMAs saw them.
+// At D = 128 the fused design of relattn_bwd_tc64.cu does not fit (the
+// tiles of both score operands and the gradient accumulators exceed the
+// shared and tensor memory); at D = 64 this design is the faster one.  The
+// work is split in three:
+//   1. bwd_pairs_kernel, one CTA per (batch, head, 128-query tile) or half of
+//      one's key steps, 64-key steps: S = (q+u) K^T, dP = dout V^T and the
+//      step's 64 new distances of the 192-distance window (q+v) R^T on the
+//      tensor cores (K = D), then per pair p and g with the distance term
+//      shifted into key order as in the forward.  It writes, in bf16,
+//      G [bh][i][j] and P [bh][i][j] (key order; P only for steps with
+//      segment keys), GS [bh][i][d] (the same g in distance order,
+//      d = M+i-j), and (q+u), (q+v) as the MMAs saw them.
 //   2. bgemm_kernel, this library's tcgen05 GEMM arranged for the products
-//      (M = 128 rows of a tile, N = D = 128, fp32 accumulators in TMEM, fp32
+//      (M = 128 rows of a tile, N = D, fp32 accumulators in TMEM, fp32
 //      results), all four in one launch whose CTAs take tiles from a counter:
 //      dq = G K + GS r per (batch, head), the two parts in two accumulators of
 //      one tile, whose epilogue also writes each part's column sums over the
@@ -449,7 +452,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     for (int t = 0; t < T && ok; ++t) {
       if (!(ok = mbar_wait(&bars->done[t & 1], (t >> 1) & 1, wait_ns, abort))) break;
       tma_store_3d(&tm_g, sG, BN * (t0 + t), w.i0, z);
-      tma_store_3d(&tm_p, sP, BN * (t0 + t), w.i0, z);
+      // P is read by the dv product only, over the segment's keys (>= M)
+      if (BN * (t0 + t) + BN > p.M) tma_store_3d(&tm_p, sP, BN * (t0 + t), w.i0, z);
       bulk_commit_group();
       bulk_wait_group_read0();
       mbar_arrive(&bars->sfree);
@@ -488,7 +492,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
       // step t-1's G and P stores have read the staging tiles
       if (t > 0 && !mbar_wait(&bars->sfree, (t - 1) & 1, wait_ns, abort)) report_timeout(abort, p.status);
       stage_row32(sG, a, half, g);
-      stage_row32(sP, a, half, pr);
+      if (BN * (t0 + t) + BN > p.M) stage_row32(sP, a, half, pr);  // a step of memory keys only: no P
       __syncwarp();
       // GS: row r of the warp holds distances D0_r - 31 ... D0_r, with
       // D0_r = M + i_warp + r - 64 (t0 + t) - 32 half, i.e. keys 32 half + 31 ... 32 half
