@@ -261,8 +261,8 @@ __global__ void __launch_bounds__(kSThreads, 1)
     mbar_init(&bars->x, 1);
     mbar_init(&bars->m1[0], 1);
     mbar_init(&bars->m1[1], 1);
-    mbar_init(&bars->done[0], 1);
-    mbar_init(&bars->done[1], 1);
+    mbar_init(&bars->done[0], kPairThreads / 32);  // one arrival per pair warp
+    mbar_init(&bars->done[1], kPairThreads / 32);
     mbar_init(&bars->sfree, 1);
     mbar_init(&bars->fin, 1);
     bars->abort = 0;
@@ -473,7 +473,7 @@ __global__ void __launch_bounds__(kSThreads, 1)
     const int i_warp = w.i0 + quad * 32;  // first query row of this warp
     for (int t = 0; t < T && ok; ++t) {
       const int s = t & 1;
-      if (!named_bar_and(1, kPairThreads, mbar_wait(&bars->m1[s], (t >> 1) & 1, wait_ns, abort))) {
+      if (!warp_wait(&bars->m1[s], (t >> 1) & 1, wait_ns, abort)) {
         ok = false;
         break;
       }
@@ -518,12 +518,15 @@ __global__ void __launch_bounds__(kSThreads, 1)
         for (int r = 0; r < 32; ++r)
           if (r >= r_lo && r < r_hi) gs[static_cast<size_t>(r) * (p.LP + 1)] = val[r];
       }
+      // this warp has read step t's TMEM columns and staged its pairs (the GS
+      // rows it stores are its own staged rows); the warps do not wait for
+      // one another
       fence_proxy_async_smem();  // the G and P staging is read by the TMA stores next
       tc_fence_before();
-      named_bar_sync(1, kPairThreads);  // every pair thread has read step t's TMEM columns and staged its pairs
-      if (tid == 0) mbar_arrive(&bars->done[s]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->done[s]);
     }
-    if (!ok && tid == 0) report_timeout(abort, p.status);
+    if (!ok && lane == 0) report_timeout(abort, p.status);
   }
   tc_fence_before();
   __syncthreads();
