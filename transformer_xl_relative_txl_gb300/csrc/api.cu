@@ -247,10 +247,12 @@ int roll_impl(const txl::RollTensor* t, int n, int m_prev, int w, int m, int B, 
 
 // The dense product of the layer on this library's tensor-core GEMM:
 // C_z = A B_z (+ bias) (ReLU), bf16 row-major, A [m, k] shared, B_z
-// [k, n] at B + z b_stride, C_z [m, n] at C + z c_stride (elements).
+// [k, n] at B + z b_stride, C_z [m, n] at C + z c_stride (elements); with
+// m2 > 0 also C2 [m2, n] = A2 [m2, k] B2 [k, n] in the same launch.
 // Arguments already validated (alignment, strides).
 int dense_impl(const void* A, const void* B, void* C, int m, int n, int k, int batch, long long b_stride,
-               long long c_stride, const float* bias, bool relu, cudaStream_t stream) {
+               long long c_stride, const float* bias, bool relu, cudaStream_t stream, const void* A2 = nullptr,
+               const void* B2 = nullptr, void* C2 = nullptr, int m2 = 0) {
   PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
   if (encode == nullptr) return TXL_ERR_CUDA;
   const cuuint32_t estr[3] = {1, 1, 1};
@@ -260,8 +262,8 @@ int dense_impl(const void* A, const void* B, void* C, int m, int n, int k, int b
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
   };
-  const int bn = txl::gemm_tc_tile_n(m, n, batch);
-  CUtensorMap ta, tb, tc;
+  const int bn = txl::gemm_tc_tile_n(m, n, batch, m2);
+  CUtensorMap ta, tb, tc, ta2, tb2, tc2;
   {
     const cuuint64_t dims[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m)};
     const cuuint64_t strides[1] = {static_cast<cuuint64_t>(k) * 2};
@@ -282,9 +284,27 @@ int dense_impl(const void* A, const void* B, void* C, int m, int n, int k, int b
     const cuuint32_t box[3] = {64, 32, 1};
     if (!enc(&tc, C, 3, dims, strides, box)) return TXL_ERR_CUDA;
   }
+  if (m2 > 0) {
+    const cuuint64_t da[2] = {static_cast<cuuint64_t>(k), static_cast<cuuint64_t>(m2)};
+    const cuuint64_t sa[1] = {static_cast<cuuint64_t>(k) * 2};
+    const cuuint32_t ba[2] = {64, 128};
+    const cuuint64_t db[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(k), 1};
+    const cuuint64_t sb[2] = {static_cast<cuuint64_t>(n) * 2, static_cast<cuuint64_t>(n) * k * 2};
+    const cuuint32_t bb[3] = {64, static_cast<cuuint32_t>(txl::gemm_tc_k_block(bn)), 1};
+    const cuuint64_t dc[3] = {static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(m2), 1};
+    const cuuint64_t sc[2] = {static_cast<cuuint64_t>(n) * 2, static_cast<cuuint64_t>(n) * m2 * 2};
+    const cuuint32_t bc[3] = {64, 32, 1};
+    if (!enc(&ta2, A2, 2, da, sa, ba) || !enc(&tb2, B2, 3, db, sb, bb) || !enc(&tc2, C2, 3, dc, sc, bc))
+      return TXL_ERR_CUDA;
+  } else {
+    ta2 = ta;
+    tb2 = tb;
+    tc2 = tc;
+  }
   txl::WaitCtl wc;
   if (wait_ctl(&wc) != TXL_OK) return TXL_ERR_CUDA;
-  return from_cuda(txl::launch_gemm_tc(ta, tb, tc, m, n, k, batch, bn, bias, relu, wc, stream));
+  return from_cuda(
+      txl::launch_gemm_tc2(ta, tb, tc, m, n, k, batch, bias, relu, ta2, tb2, tc2, m2, bn, wc, stream));
 }
 
 // txl_mem_ring_append for n (1 or 2) rings of one geometry, each run of
@@ -1098,15 +1118,16 @@ int layer_impl(const void* h, void* out, void* k_mem, void* v_mem, int cap, int 
   const long long wsz = static_cast<long long>(d_model) * HD;
   int st = TXL_OK;
   if (packed) {
-    st = dense_impl(h, w->W_q, q, rows, HD, d_model, 3, wsz, qkv_stride, nullptr, false, stream);
+    // q, k, v and r = R W_r in one launch (r's tiles after the projections')
+    st = dense_impl(h, w->W_q, q, rows, HD, d_model, 3, wsz, qkv_stride, nullptr, false, stream, R, w->W_r, r, n_r);
   } else {
     const void* wm[3] = {w->W_q, w->W_k, w->W_v};
     void* om[3] = {q, ks, vs};
     for (int i = 0; i < 3 && st == TXL_OK; ++i)
       st = dense_impl(h, wm[i], om[i], rows, HD, d_model, 1, wsz, 0, nullptr, false, stream);
+    if (st == TXL_OK) st = dense_impl(R, w->W_r, r, n_r, HD, d_model, 1, wsz, 0, nullptr, false, stream);
   }
   if (st != TXL_OK) return st;
-  if ((st = dense_impl(R, w->W_r, r, n_r, HD, d_model, 1, wsz, 0, nullptr, false, stream)) != TXL_OK) return st;
   if ((st = txl_relattn_forward_ring_append(k_mem, v_mem, cap, start, M, q, ks, vs, r, w->bias_u, w->bias_v, a,
                                             nullptr, B, W, H, D, n_r, scale, TXL_BF16, TXL_BF16, start_out, m_out,
                                             stream)) != TXL_OK)

@@ -64,9 +64,11 @@ struct GemmCfg {
 struct GemmParams {
   int m, n, k, batch;
   int mt, nt;           // row and column blocks
-  int tiles;            // batch * mt * nt
-  const float* bias;    // [n] or nullptr
-  int relu;
+  int tiles1;           // batch * mt * nt: the tiles of the first product
+  int m2, mt2;          // a second product (its own A, B, C; same n and k), or m2 = 0
+  int tiles;            // tiles1 + mt2 * nt
+  const float* bias;    // [n] or nullptr (the first product only)
+  int relu;             // the first product only
   unsigned int* status;
   unsigned long long wait_ns;
 };
@@ -95,12 +97,22 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 }
 
 struct TileIdx {
-  int z, m0, n0;
+  int prob, z, m0, n0;
 };
-// Tile t: batch index slowest, then the row block, the column block fastest.
+// Tile t: the first product's tiles, batch index slowest, then the row
+// block, the column block fastest; then the second product's.
 __device__ __forceinline__ TileIdx tile_of(const GemmParams& p, int t, int bn) {
   TileIdx r;
+  if (t >= p.tiles1) {
+    t -= p.tiles1;
+    r.prob = 1;
+    r.z = 0;
+    r.m0 = (t / p.nt) * GBM;
+    r.n0 = (t % p.nt) * bn;
+    return r;
+  }
   const int per_z = p.mt * p.nt;
+  r.prob = 0;
   r.z = t / per_z;
   const int rem = t - r.z * per_z;
   r.m0 = (rem / p.nt) * GBM;
@@ -111,7 +123,9 @@ __device__ __forceinline__ TileIdx tile_of(const GemmParams& p, int t, int bn) {
 template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_a, const __grid_constant__ CUtensorMap tm_b,
-                   const __grid_constant__ CUtensorMap tm_c, const GemmParams p) {
+                   const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_a2,
+                   const __grid_constant__ CUtensorMap tm_b2, const __grid_constant__ CUtensorMap tm_c2,
+                   const GemmParams p) {
   // Launched behind the previous kernel on the stream, which has completed from
   // here on.  No early trigger: the next persistent launch starts its CTAs when
   // this one completes (placed early, they timed slower back to back).
@@ -158,11 +172,17 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
     if (lane == 0) {
       tma_prefetch_desc(&tm_a);
       tma_prefetch_desc(&tm_b);
+      if (p.m2 > 0) {
+        tma_prefetch_desc(&tm_a2);
+        tma_prefetch_desc(&tm_b2);
+      }
       uint32_t it = 0;
       bool ok = true;
       for (int t = blockIdx.x; ok && t < p.tiles; t += gridDim.x) {
         const TileIdx ti = tile_of(p, t, BN);
         const int n0 = ti.n0;
+        const CUtensorMap* ma = ti.prob ? &tm_a2 : &tm_a;
+        const CUtensorMap* mb = ti.prob ? &tm_b2 : &tm_b;
         for (int kb = 0; kb < nk; ++kb, ++it) {
           const int s = static_cast<int>(it % S);
           if (!(ok = mbar_wait(&bars->empty[s], ((it / S) & 1) ^ 1, wait_ns, abort))) break;
@@ -170,10 +190,10 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           mbar_arrive_expect_tx(&bars->full[s], Cfg::kStageBytes);
 #pragma unroll
           for (int a = 0; a < Cfg::kABoxes; ++a)
-            tma_load_2d(st + a * kATile, &tm_a, &bars->full[s], kb * GBK + 64 * a, ti.m0);
+            tma_load_2d(st + a * kATile, ma, &bars->full[s], kb * GBK + 64 * a, ti.m0);
 #pragma unroll
           for (int j = 0; j < BN / 64; ++j)
-            tma_load_3d(st + kBOff + j * kBBlock, &tm_b, &bars->full[s], n0 + 64 * j, kb * GBK, ti.z);
+            tma_load_3d(st + kBOff + j * kBBlock, mb, &bars->full[s], n0 + 64 * j, kb * GBK, ti.z);
         }
       }
       if (!ok) report_timeout(abort, p.status);
@@ -232,13 +252,15 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       const TileIdx ti = tile_of(p, t, BN);
       const int n0 = ti.n0;
       const uint32_t acc = tl & 1;
+      const float* bias = ti.prob ? nullptr : p.bias;  // bias and ReLU: the first product only
+      const bool relu = ti.prob == 0 && p.relu;
       // this tile's bias columns, staged once for broadcast reads
-      if (p.bias != nullptr) {
+      if (bias != nullptr) {
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < BN / 32; ++i) {
           const int c = n0 + 32 * i + lane;
-          sbias[32 * i + lane] = c < p.n ? __ldg(p.bias + c) : 0.f;
+          sbias[32 * i + lane] = c < p.n ? __ldg(bias + c) : 0.f;
         }
         __syncwarp();
       }
@@ -263,7 +285,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
           x[j] = __uint_as_float(v0[j]);
           x[32 + j] = __uint_as_float(v1[j]);
         }
-        if (p.bias != nullptr) {
+        if (bias != nullptr) {
 #pragma unroll
           for (int j = 0; j < 64; j += 4) {
             const float4 b = *reinterpret_cast<const float4*>(sbias + c * 64 + j);
@@ -273,7 +295,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
             x[j + 3] += b.w;
           }
         }
-        if (p.relu) {
+        if (relu) {
 #pragma unroll
           for (int j = 0; j < 64; ++j) x[j] = fmaxf(x[j], 0.f);
         }
@@ -288,7 +310,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&tm_c, stg, n0 + 64 * c, ti.m0 + 32 * quad, ti.z);
+          tma_store_3d(ti.prob ? &tm_c2 : &tm_c, stg, n0 + 64 * c, ti.m0 + 32 * quad, ti.z);
           bulk_commit_group();
         }
       }
@@ -320,8 +342,8 @@ int gemm_num_sms() {
 }
 
 template <int BN>
-cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const GemmParams& p,
-                      cudaStream_t stream) {
+cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& tc, const CUtensorMap& ta2,
+                      const CUtensorMap& tb2, const CUtensorMap& tc2, const GemmParams& p, cudaStream_t stream) {
   using Cfg = GemmCfg<BN>;
   static std::atomic<bool> attr_done[64];
   int dev = 0;
@@ -335,7 +357,8 @@ cudaError_t launch_bn(const CUtensorMap& ta, const CUtensorMap& tb, const CUtens
   }
   const int sms = gemm_num_sms();
   const int grid = p.tiles < sms ? p.tiles : sms;
-  return launch_dependent(gemm_tc_kernel<BN>, dim3(grid), dim3(kGemmThreads), Cfg::kSmem, stream, ta, tb, tc, p);
+  return launch_dependent(gemm_tc_kernel<BN>, dim3(grid), dim3(kGemmThreads), Cfg::kSmem, stream, ta, tb, tc, ta2,
+                          tb2, tc2, p);
 }
 
 }  // namespace
@@ -348,29 +371,32 @@ std::atomic<int> g_force_tile_n{0};
 
 void gemm_tc_force_tile_n(int bn) { g_force_tile_n.store(bn == 64 || bn == 128 || bn == 256 ? bn : 0); }
 
-int gemm_tc_tile_n(int m, int n, int batch) {
+int gemm_tc_tile_n(int m, int n, int batch, int m2) {
   if (const int f = g_force_tile_n.load()) return f;
   // Fewer waves of tiles against smaller tiles: the time of a wave is about
-  // proportional to its tiles' columns, plus a fixed part per tile.
+  // proportional to its tiles' columns, plus a fixed part per tile.  A
+  // second product of m2 rows counts as more rows of the batch's last one.
   const long long sms = gemm_num_sms();
-  const long long mt = (m + GBM - 1) / GBM;
+  const long long mt = (m + GBM - 1) / GBM, mt2 = (m2 + GBM - 1) / GBM;
   // Too few 128-column tiles to fill half the SMs: 64-column ones spread
   // the work over twice as many (the r projection of the base layer,
   // 1024 x 512 x 512: 10.2 -> 8.2 us); they are slower wherever the wider
   // tiles already fill the GPU (W_2: 36.9 against 32.8 us).
-  if (2 * batch * mt * ((n + 127) / 128) <= sms) return 64;
+  if (2 * (batch * mt + mt2) * ((n + 127) / 128) <= sms) return 64;
   auto cost = [&](int bn) {
-    const long long tiles = batch * mt * ((n + bn - 1) / bn);
+    const long long tiles = (batch * mt + mt2) * ((n + bn - 1) / bn);
     const long long waves = (tiles + sms - 1) / sms;
     return static_cast<double>(waves) * (bn + 32);
   };
   return cost(128) < cost(256) ? 128 : 256;
 }
 
-cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
-                           int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
-                           cudaStream_t stream) {
-  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || (bn != 64 && bn != 128 && bn != 256)) return cudaErrorInvalidValue;
+cudaError_t launch_gemm_tc2(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
+                            int k, int batch, const float* bias, bool relu, const CUtensorMap& tm_a2,
+                            const CUtensorMap& tm_b2, const CUtensorMap& tm_c2, int m2, int bn, const WaitCtl& wc,
+                            cudaStream_t stream) {
+  if (m <= 0 || n <= 0 || k <= 0 || batch <= 0 || m2 < 0 || (bn != 64 && bn != 128 && bn != 256))
+    return cudaErrorInvalidValue;
   GemmParams p;
   p.m = m;
   p.n = n;
@@ -378,15 +404,26 @@ cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, con
   p.batch = batch;
   p.mt = (m + GBM - 1) / GBM;
   p.nt = (n + bn - 1) / bn;
-  const long long tiles = static_cast<long long>(batch) * p.mt * p.nt;
+  p.m2 = m2;
+  p.mt2 = (m2 + GBM - 1) / GBM;
+  const long long tiles1 = static_cast<long long>(batch) * p.mt * p.nt;
+  const long long tiles = tiles1 + static_cast<long long>(p.mt2) * p.nt;
   if (tiles > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
+  p.tiles1 = static_cast<int>(tiles1);
   p.tiles = static_cast<int>(tiles);
   p.bias = bias;
   p.relu = relu ? 1 : 0;
   p.status = wc.status;
   p.wait_ns = wc.limit_ns;
-  if (bn == 64) return launch_bn<64>(tm_a, tm_b, tm_c, p, stream);
-  return bn == 256 ? launch_bn<256>(tm_a, tm_b, tm_c, p, stream) : launch_bn<128>(tm_a, tm_b, tm_c, p, stream);
+  if (bn == 64) return launch_bn<64>(tm_a, tm_b, tm_c, tm_a2, tm_b2, tm_c2, p, stream);
+  if (bn == 256) return launch_bn<256>(tm_a, tm_b, tm_c, tm_a2, tm_b2, tm_c2, p, stream);
+  return launch_bn<128>(tm_a, tm_b, tm_c, tm_a2, tm_b2, tm_c2, p, stream);
+}
+
+cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
+                           int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
+                           cudaStream_t stream) {
+  return launch_gemm_tc2(tm_a, tm_b, tm_c, m, n, k, batch, bias, relu, tm_a, tm_b, tm_c, 0, bn, wc, stream);
 }
 
 }  // namespace txl

@@ -162,14 +162,21 @@ cudaError_t launch_relattn_bwd_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, c
 // z < batch, fp32 accumulation, one rounding.  Tensor maps (bf16, 128-byte
 // swizzle, zero fill): tm_a over {k, m} with a {64, 128} box; tm_b over
 // {n, k, batch} with a {64, gemm_tc_k_block(bn), 1} box; tm_c over
-// {n, m, batch} with a {64, 32, 1} box.  bn: columns per tile, 128 or 256
-// (gemm_tc_tile_n picks one for the shape).
-int gemm_tc_tile_n(int m, int n, int batch);
+// {n, m, batch} with a {64, 32, 1} box.  bn: columns per tile, 64, 128 or
+// 256 (gemm_tc_tile_n picks one for the shape).
+// launch_gemm_tc2 runs a second product C2 [m2, n] = A2 [m2, k] B2 [k, n]
+// (no bias, no ReLU; maps as above with batch 1) in the same launch, its
+// tiles after the first product's; m2 = 0: none.
+int gemm_tc_tile_n(int m, int n, int batch, int m2 = 0);
 void gemm_tc_force_tile_n(int bn);  // test hook: 64, 128 or 256 fixes the column tile, 0 restores the choice
 int gemm_tc_k_block(int bn);
 cudaError_t launch_gemm_tc(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
                            int k, int batch, int bn, const float* bias, bool relu, const WaitCtl& wc,
                            cudaStream_t stream);
+cudaError_t launch_gemm_tc2(const CUtensorMap& tm_a, const CUtensorMap& tm_b, const CUtensorMap& tm_c, int m, int n,
+                            int k, int batch, const float* bias, bool relu, const CUtensorMap& tm_a2,
+                            const CUtensorMap& tm_b2, const CUtensorMap& tm_c2, int m2, int bn, const WaitCtl& wc,
+                            cudaStream_t stream);
 // out = LN(a + b (+ bias)) row by row over d columns (bf16 rows, fp32 gamma,
 // beta, bias; d a multiple of 8, <= 1024) (layer.cu).
 cudaError_t launch_add_ln(const void* a, const void* b, const float* bias, const float* gamma, const float* beta,
