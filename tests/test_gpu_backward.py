@@ -188,6 +188,40 @@ def test_backward_deterministic(txl, D, dtype, o_dtype):
         assert np.array_equal(a[key], b[key]), key
 
 
+@pytest.mark.parametrize("D", [64, 128])
+def test_backward_captured_in_a_graph(txl, D):
+    """The pair-term backward (three kernels, each launched behind the one
+    before it with programmatic serialisation, and a tile counter the first
+    zeroes for the second) captured into a CUDA graph after one eager call
+    (which allocates the scratch) and replayed twice: bit for bit the eager
+    result each time."""
+    q, k, v, r, bu, bv, dout = _case(2, 2, D, 200, 136, "bf16")
+    td = torch.bfloat16
+    qd, kd, vd, rd = (to_dev(x, td) for x in (q, k, v, r))
+    bud, bvd = to_dev(bu, torch.float32), to_dev(bv, torch.float32)
+    o = torch.empty(qd.shape, device=dev(), dtype=td)
+    lse = torch.empty(2, 2, 200, device=dev(), dtype=torch.float32)
+    txl.txl_relattn_forward(qd, kd, vd, rd, bud, bvd, o, lse, M=136)
+    gd = to_dev(dout, td)
+    torch.cuda.synchronize()
+    side = torch.cuda.Stream()  # the library keeps scratch per stream: warm up the capture stream
+    with torch.cuda.stream(side):
+        eager = txl.txl_relattn_backward(qd, kd, vd, rd, bud, bvd, o, lse, gd, M=136)
+    torch.cuda.synchronize()
+    want = {key: t.clone() for key, t in eager.items()}
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        txl.txl_relattn_backward(qd, kd, vd, rd, bud, bvd, o, lse, gd, M=136, grads=eager)
+    for _ in range(2):
+        for t in eager.values():
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        assert txl.txl_get_device_status() == 0
+        for key in KEYS:
+            assert torch.equal(eager[key], want[key]), key
+
+
 def test_backward_d128_scratch_reuse(txl):
     """The D = 128 tensor-core path keeps its pair terms in a scratch buffer
     reused across calls: a call after one of another shape (which leaves
