@@ -370,7 +370,7 @@ TXL_API int txl_dense(const void* x, const void* W, void* y, int m, int n, int k
  * Every product runs on txl_dense's GEMM (bf16 in, fp32 accumulation, bf16
  * out), b_1 with the ReLU and b_2 in its epilogue; when W_k starts right after
  * W_q and W_v right after W_k (one [3, d_model, H*D] allocation), the three
- * projections run as one batched launch.  Every intermediate lives in
+ * projections and r = R W_r run as one launch.  Every intermediate lives in
  * `workspace`; the attention inside may make a unit plan as
  * txl_relattn_forward does, and when the ring cannot be read in place (cap,
  * start or M not multiples of 64) it takes the ring scratch of
