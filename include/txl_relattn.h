@@ -461,18 +461,17 @@ TXL_API int txl_stack_forward(const void* h, void* out, int n_layers, void* cons
  * Every output is overwritten (not accumulated into).  Outputs must not
  * overlap each other or any input (TXL_ERR_ALIAS); every pointer 16-byte
  * aligned (TXL_ERR_INVALID_ARG).  D <= 256 (TXL_ERR_UNSUPPORTED otherwise).
- * Paths: bf16 q, k, v, r with bf16 o and dout, D = 64 or 128 and M a
- * multiple of 8 run on the tensor cores (tcgen05) with the pair terms
- * materialised: a kernel rebuilds p and g per 64-key step and writes them in
- * bf16 to scratch (g in key and in distance order, p in key order), one
- * launch of tcgen05 products then forms dq (key and distance parts in one
- * tile, with the bias gradients' partials), dk, dv and dr, and an ordered sum
- * the bias gradients; deterministic.  The same inputs with D = 64 and M not a
- * multiple of 8 run on fused tensor-core kernels: a dq kernel over query
- * tiles (which also sums dr and the bias gradients) and a dk/dv kernel over
- * 64-key blocks; there dr arrives by fp32 atomic adds, so its last bits may
- * differ between calls.  Every other case runs on CUDA cores in fp32
- * arithmetic, fully deterministic.
+ * Paths: bf16 q, k, v, r with bf16 o and dout and D = 64 or 128 run on the
+ * tensor cores (tcgen05) with the pair terms materialised: a kernel rebuilds
+ * p and g per 64-key step and writes them in bf16 to scratch (g in key and in
+ * distance order, p in key order), one launch of tcgen05 products then forms
+ * dq (key and distance parts in one tile, with the bias gradients'
+ * partials), dk, dv and dr, and an ordered sum the bias gradients;
+ * deterministic.  Every other case runs on CUDA cores in fp32 arithmetic,
+ * fully deterministic.  (A test hook sends D = 64 to fused tensor-core
+ * kernels instead: a dq kernel over query tiles, which also sums dr and the
+ * bias gradients, and a dk/dv kernel over 64-key blocks; there dr arrives by
+ * fp32 atomic adds, so its last bits may differ between calls.)
  * Allocates: per-(device, stream) scratch (see the conventions above): for
  * the pair-term path, per chunk of Bc sequences, 3 * Bc*H*W*LP * 2 bytes of
  * pair terms (LP = M + W rounded up to 64) plus (q+u), (q+v) in bf16
@@ -559,8 +558,9 @@ TXL_API int txl_debug_set_bwd_chunk_bytes(unsigned long long bytes);
  * shape; 0 restores the model.  TXL_ERR_INVALID_ARG for any other value. */
 TXL_API int txl_debug_force_dense_tile_n(int bn);
 /* Test hook: the path of the bf16 backward at D = 64: 1 the fused kernels, 2
- * the pair terms materialised in scratch (as at D = 128, where M % 8 == 0),
- * 0 restores the choice.  TXL_ERR_INVALID_ARG for any other value. */
+ * the pair terms materialised in scratch (the path it takes by default, as
+ * at D = 128), 0 restores the choice.  TXL_ERR_INVALID_ARG for any other
+ * value. */
 TXL_API int txl_debug_force_bwd_path(int path);
 
 #ifdef __cplusplus

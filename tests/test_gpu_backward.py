@@ -96,8 +96,11 @@ CASES = [
     (1, 3, 128, 300, 512, "bf16", 0),  # memory longer than the segment
     (2, 1, 128, 7, 8, "bf16", 1),      # fewer rows than a warp
     (3, 5, 128, 64, 0, "bf16", 7),     # odd head count, half a tile, empty memory
-    # bf16, D = 128, memory not a multiple of 8: the CUDA-core kernels
+    # bf16, memory not a multiple of 8: the dk / dv tiles start before column M
     (1, 2, 128, 130, 37, "bf16", 0),
+    (2, 2, 128, 300, 77, "bf16", 2),   # several dk / dv tiles, each shifted by 5 keys
+    (2, 1, 64, 9, 15, "bf16", 0),      # fewer rows than a warp, shifted by 7
+    (1, 1, 64, 520, 1, "bf16", 0),     # five dk / dv tiles, shifted by 1
 ]
 
 
@@ -117,11 +120,12 @@ def test_backward_matches_oracle(txl, B, H, D, W, M, dtype, extra):
     (1, 2, 256, 0, 0),     # first segment, whole tiles
     (1, 2, 128, 512, 0),   # memory longer than the segment
     (2, 1, 7, 8, 1),       # fewer rows than a warp
+    (2, 2, 260, 45, 3),    # memory not a multiple of 8
 ])
 def test_backward_d64_each_path(txl, path, B, H, W, M, extra):
-    """D = 64 (memory a multiple of 8 rows) through each tensor-core path,
-    forced by the test hook: 1 the fused kernels, 2 the materialised pair
-    terms (the library's choice for these shapes), against the oracle; the
+    """D = 64 through each tensor-core path, forced by the test hook: 1 the
+    fused kernels, 2 the materialised pair terms (the library's choice),
+    against the oracle; the
     pair-term path also bit for bit between two calls (every sum has a fixed
     order there)."""
     q, k, v, r, bu, bv, dout = _case(B, H, 64, W, M, "bf16", extra)

@@ -750,9 +750,8 @@ int txl_relattn_backward(const void* q, const void* k, const void* v, const void
   }
   void* scratch = nullptr;
   int* unused = nullptr;
-  // bf16 on the tensor cores: the materialised pair terms where M % 8 == 0
-  // (D = 64 or 128), else at D = 64 the fused kernels; the test hook can
-  // send D = 64 to the fused kernels
+  // bf16 on the tensor cores: the materialised pair terms (D = 64 or 128);
+  // the test hook can send D = 64 to the fused kernels
   const bool tc = dtype == TXL_BF16 && go_dtype == TXL_BF16;
   const bool pairs = tc && txl::relattn_bwd_pairs_supported(W, M, D) && !(D == 64 && g_bwd_path.load() == 1);
   if (tc && D == 64 && !pairs) {

@@ -1,6 +1,6 @@
 // Backward of the relative attention on the tensor cores with the pair terms
-// materialised, for head dimension D = 64 or 128 (memory length a multiple
-// of 8): bf16 q, k, v, r, o and dout, fp32 accumulation and gradients.
+// materialised, for head dimension D = 64 or 128: bf16 q, k, v, r, o and
+// dout, fp32 accumulation and gradients.
 //
 // The formulas and the stop-gradient are those of relattn_bwd.cu ("Transformer-
 // XL, explained", method step 2 and the symbol SG(.)):
@@ -579,6 +579,12 @@ struct GemmArgs {
   int B, W, M, H, L;
   int BH, nmt, nmtL, nkbW;  // row blocks of 128 queries, of 128 distances; 64-deep blocks of the W queries
   int nDR, nDQ;             // tiles of the DR and DQ kinds; DK and DV follow, interleaved
+  int ks, nmtK;             // DK, DV: tiles start at key column M - ks (ks = M % 8), nmtK row blocks
+  int LP;                   // row length of G and P
+  const __nv_bfloat16* G;   // DK, DV epilogue: G, P [B*H][W][LP], q+u and dout [B, W, H, D]
+  const __nv_bfloat16* P;
+  const __nv_bfloat16* qu;
+  const __nv_bfloat16* dout;
   int total;                // all tiles
   float* dq;
   float* dk;
@@ -603,7 +609,13 @@ struct GTile {
 // first accumulator, then over the same distances with A = GS, B = r into its
 // second; G and GS are zero past each row's last visible key), then DK and DV
 // tiles in turn (rows = segment keys m; k = queries i from m0 on, since key
-// M + m is visible to queries i >= m only).  Each kind runs longest first.
+// M + m is visible to queries i >= m only).  A DK or DV tile reads G or P from
+// key column M + m0, which a tensor copy needs on a 16-byte boundary, so the
+// tiles start at m0 = 128 n - ks (M + m0 a multiple of 8; rows m < 0, memory
+// keys, are not written), and the k loop starts at query 128 n: the query
+// tile before it has G and P only up to its own last key step.  The pairs it
+// leaves out, queries i in [m, 128 n) of the tile's first ks keys, are added
+// by the epilogue.  Each kind runs longest first.
 __device__ __forceinline__ GTile gtile(const GemmArgs& p, int u) {
   GTile r;
   r.nkb_c = 0;
@@ -628,9 +640,9 @@ __device__ __forceinline__ GTile gtile(const GemmArgs& p, int u) {
   u -= p.nDQ;
   r.mode = (u & 1) ? kModeDV : kModeDK;
   u >>= 1;
-  r.m0 = (u / p.BH) * 128;
+  r.m0 = (u / p.BH) * 128 - p.ks;
   r.z = u % p.BH;
-  r.kb0 = r.m0 / 64;
+  r.kb0 = 2 * (u / p.BH);
   r.nkb = p.nkbW - r.kb0;
   return r;
 }
@@ -906,10 +918,12 @@ __global__ void __launch_bounds__(kGThreads, 1)
       const bool add = g.mode == kModeDR && p.accumulate;
       if (g.mode == kModeDR) {
         if (row < p.L) dst = p.dr + (static_cast<size_t>(row) * p.H + g.z) * D;
-      } else if (row < p.W) {
+      } else if (row >= 0 && row < p.W) {
         const int b = g.z / p.H, h = g.z % p.H;
         dst = (g.mode == kModeDK ? p.dk : p.dv) + ((static_cast<size_t>(b) * p.W + row) * p.H + h) * D;
       }
+      // the first ks keys of a tile after the first: queries [row, m0 + ks)
+      const int tri_end = g.mode != kModeDR && g.m0 > 0 && row < g.m0 + p.ks ? min(g.m0 + p.ks, p.W) : 0;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
@@ -919,6 +933,27 @@ __global__ void __launch_bounds__(kGThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane == 0) mbar_arrive(&bars->acc_empty[acc]);
+        }
+        if (dst != nullptr && row < tri_end) {
+          // DK: sum_i G[i][M+row] (q+u)_i; DV: sum_i P[i][M+row] dout_i, in query order
+          const int b = g.z / p.H, h = g.z % p.H;
+          const __nv_bfloat16* X = (g.mode == kModeDK ? p.G : p.P) + static_cast<size_t>(g.z) * p.W * p.LP + p.M + row;
+          const __nv_bfloat16* Y = g.mode == kModeDK ? p.qu : p.dout;
+          for (int i = row; i < tri_end; ++i) {
+            const float x = __bfloat162float(X[static_cast<size_t>(i) * p.LP]);
+            const uint4* yr = reinterpret_cast<const uint4*>(Y + ((static_cast<size_t>(b) * p.W + i) * p.H + h) * D + 32 * c);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+              const uint4 y = yr[q4];
+              const uint32_t yw[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const int j = 8 * q4 + 2 * e;
+                v[j] = __float_as_uint(fmaf(x, bf16_lo(yw[e]), __uint_as_float(v[j])));
+                v[j + 1] = __float_as_uint(fmaf(x, bf16_hi(yw[e]), __uint_as_float(v[j + 1])));
+              }
+            }
+          }
         }
         if (dst != nullptr) {
           float4* o4 = reinterpret_cast<float4*>(dst + 32 * c);
@@ -1067,7 +1102,7 @@ cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) 
       return e;
     attr_done[dev].store(true);
   }
-  const long long total = static_cast<long long>(p.nDR) + p.nDQ + 2LL * p.BH * p.nmt;
+  const long long total = static_cast<long long>(p.nDR) + p.nDQ + 2LL * p.BH * p.nmtK;
   if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
   p.total = static_cast<int>(total);
   const int grid = std::min(p.total, num_sms());
@@ -1083,7 +1118,7 @@ size_t relattn_bwd_pairs_scratch_bytes(int B, int W, int M, int H, int D) {
   return carve(nullptr, Bc, W, M, H, D, total_parts(B, W)).bytes;
 }
 
-bool relattn_bwd_pairs_supported(int W, int M, int D) { return W > 0 && M % 8 == 0 && (D == 64 || D == 128); }
+bool relattn_bwd_pairs_supported(int W, int M, int D) { return W > 0 && M >= 0 && (D == 64 || D == 128); }
 
 namespace {
 
@@ -1213,6 +1248,13 @@ cudaError_t launch_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q
     g.nkbW = (W + 63) / 64;
     g.nDR = H * g.nmtL;
     g.nDQ = g.BH * nmt;
+    g.ks = M % 8;
+    g.nmtK = (W + g.ks + 127) / 128;
+    g.LP = LP;
+    g.G = sc.G;
+    g.P = sc.P;
+    g.qu = sc.Qu;
+    g.dout = gb;
     g.total = 0;
     g.dq = dq + b0 * seg;
     g.dk = dk + b0 * seg;

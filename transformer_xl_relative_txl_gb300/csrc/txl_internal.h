@@ -140,9 +140,9 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
 
 // Backward on the tensor cores, bf16 inputs, o and dout, D = 64 or 128
 // (relattn_bwd_pairs.cu): the pair terms are materialised in bf16 scratch and
-// the gradient products run as tensor-core GEMMs.  Needs M % 8 == 0 (the key
-// columns of the pair terms are read from column M on by 16-byte aligned
-// tensor copies).  Encodes its own tensor maps with `encode`.  Every output is
+// the gradient products run as tensor-core GEMMs (any M: the dk / dv tiles
+// start on a multiple of 8 key columns at or before column M).  Encodes its
+// own tensor maps with `encode`.  Every output is
 // written in full (dr rows >= M + W are zeroed).
 // scratch: relattn_bwd_pairs_scratch_bytes(B, W, M, H, D) bytes.
 // The scratch holds one chunk of sequences (as many as keep it within 1 GiB,
