@@ -194,7 +194,7 @@ __device__ __forceinline__ void zero_bf16(__nv_bfloat16* row, int lo, int hi) {
   for (; d < hi; ++d) row[d] = __float2bfloat16_rn(0.f);
 }
 
-// 32 values of row a, keys [32 half, 32 half + 64) of a 128 x 64 tile staged
+// 32 values of row a, keys [32 half, 32 half + 32) of a 128 x 64 tile staged
 // for a 128-byte-swizzled TMA store (64 bf16 per row).
 __device__ __forceinline__ void stage_row32(uint8_t* tile, int a, int half, const float (&x)[32]) {
   uint8_t* rowp = tile + (a >> 3) * 1024 + (a & 7) * 128;
@@ -213,9 +213,10 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
 }
 
 // Warps 0-7 compute the pairs, two per TMEM lane quadrant (key columns 0-31
-// and 32-63 of the same rows).  One thread of warp 8 issues the loads (two
-// steps ahead), one of warp 9 the MMAs (one step ahead of the pairs), one of
-// warp 10 the G / P stores, each waiting only on what it needs.
+// and 32-63 of the same rows), each on its own: a step's barrier takes one
+// arrival per warp.  One thread of warp 8 issues the loads (NS steps ahead),
+// one of warp 9 the MMAs (one step ahead of the pairs), one of warp 10 the
+// G / P stores, each waiting only on what it needs.
 template <int D>
 __global__ void __launch_bounds__(kSThreads, 1)
     bwd_pairs_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
