@@ -495,6 +495,14 @@ __global__ void __launch_bounds__(kSThreads, 1)
       stage_row32(sG, a, half, g);
       if (BN * (t0 + t) + BN > p.M) stage_row32(sP, a, half, pr);  // a step of memory keys only: no P
       __syncwarp();
+      // this warp has read step t's TMEM columns and staged its pairs; the
+      // warps do not wait for one another.  The GS pass below reads only the
+      // rows this warp staged, so the MMAs of step t + 2 and the stores of the
+      // staging tiles need not wait for it (the next staging does, in order).
+      fence_proxy_async_smem();  // the G and P staging is read by the TMA stores next
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&bars->done[s]);
       // GS: row r of the warp holds distances D0_r - 31 ... D0_r, with
       // D0_r = M + i_warp + r - 64 (t0 + t) - 32 half, i.e. keys 32 half + 31 ... 32 half
       // of the staged G row; one row per pass, a distance per lane (64
@@ -519,13 +527,6 @@ __global__ void __launch_bounds__(kSThreads, 1)
         for (int r = 0; r < 32; ++r)
           if (r >= r_lo && r < r_hi) gs[static_cast<size_t>(r) * (p.LP + 1)] = val[r];
       }
-      // this warp has read step t's TMEM columns and staged its pairs (the GS
-      // rows it stores are its own staged rows); the warps do not wait for
-      // one another
-      fence_proxy_async_smem();  // the G and P staging is read by the TMA stores next
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&bars->done[s]);
     }
     if (!ok && lane == 0) report_timeout(abort, p.status);
   }
