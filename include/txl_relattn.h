@@ -562,6 +562,14 @@ TXL_API int txl_debug_force_dense_tile_n(int bn);
  * at D = 128), 0 restores the choice.  TXL_ERR_INVALID_ARG for any other
  * value. */
 TXL_API int txl_debug_force_bwd_path(int path);
+/* Test hook, host only: how many of the longest query tiles the backward's
+ * pair-term kernel runs as two CTAs per (sequence, head) unit, each over half
+ * of the unit's key steps (0, 1 or 2), for n_query_tiles tiles of 128 queries
+ * of seq_heads (sequence, head) pairs on `sms` SMs.  The host models the
+ * launch as CTAs starting in order on the first free SM, a CTA costing its
+ * key steps plus 3, and takes the count with the shortest modelled launch.
+ * Returns -1 for negative sizes or sms <= 0. */
+TXL_API int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, int sms);
 
 #ifdef __cplusplus
 }

@@ -83,3 +83,59 @@ def test_binding_rejects_host_tensors_before_calling():
         txl.txl_relattn_forward(q, k, k, r, u, u, q.clone())
     with pytest.raises(ValueError):
         txl.txl_relattn_forward(q, k[:, :5], k, r, u, u, q.clone())
+
+
+def _split_model(nqt, bh, W, M, sms):
+    """The pair kernel's split choice restated: CTAs start in launch order on
+    the SM that frees first (whole units longest query tile first, then the
+    halves of the split tiles' units); a CTA costs its key steps plus 3; the
+    count k of split tiles (0 to 2, halves of at least two steps) with the
+    shortest launch wins, the smaller k on a tie."""
+    import heapq
+
+    def steps(qt):
+        return min(M + 128 * qt + 127, M + W - 1) // 64 + 1
+
+    def span(k):
+        loads = [0] * sms
+        heapq.heapify(loads)
+        costs = [3 + steps(qt) for qt in range(nqt - k - 1, -1, -1) for _ in range(bh)]
+        for j in range(2 * k):
+            n = steps(nqt - 1 - j // 2)
+            costs += [3 + (n - n // 2 if j % 2 else n // 2)] * bh
+        for c in costs:
+            heapq.heappush(loads, heapq.heappop(loads) + c)
+        return max(loads)
+
+    best, best_span = 0, span(0)
+    for k in range(1, min(nqt, 2) + 1):
+        if steps(nqt - k) < 4:
+            break
+        v = span(k)
+        if v < best_span:
+            best, best_span = k, v
+    return best
+
+
+def test_pair_kernel_split_choice():
+    """The backward pair kernel's host-side split choice (test hook, no GPU
+    needed) against the list-scheduling model it is defined by, over the
+    bench's workloads and a grid of small shapes."""
+    _build_if_missing()
+    import ctypes
+
+    lib = ctypes.CDLL(LIB)
+    f = lib.txl_debug_pair_split_tiles
+    f.restype = ctypes.c_int
+    f.argtypes = [ctypes.c_int] * 5
+    # the bench's workloads: wide splits its last query tile, base does not
+    assert f(6, 64, 768, 768, 152) == 1
+    assert f(4, 176, 512, 512, 152) == 0
+    assert f(1, 64, 128, 1600, 152) == 1
+    cases = [(nqt, bh, W, M, sms) for nqt, W in ((1, 100), (2, 200), (3, 300), (4, 512), (6, 768))
+             for bh in (1, 7, 64, 200) for M in (0, 8, 512, 1600) for sms in (148, 152)]
+    for nqt, bh, W, M, sms in cases:
+        got = f(nqt, bh, W, M, sms)
+        assert got == _split_model(nqt, bh, W, M, sms), (nqt, bh, W, M, sms, got)
+        assert 0 <= got <= min(nqt, 2)
+    assert f(-1, 1, 1, 0, 152) == -1 and f(1, 1, 1, 0, 0) == -1

@@ -28,6 +28,7 @@ __all__ = [
     "txl_debug_set_bwd_chunk_bytes",
     "txl_debug_force_dense_tile_n",
     "txl_debug_force_bwd_path",
+    "txl_debug_pair_split_tiles",
 ]
 
 TXL_F32 = 0
@@ -108,6 +109,8 @@ lib.txl_debug_force_dense_tile_n.argtypes = [_i]
 lib.txl_debug_force_dense_tile_n.restype = _i
 lib.txl_debug_force_bwd_path.argtypes = [_i]
 lib.txl_debug_force_bwd_path.restype = _i
+lib.txl_debug_pair_split_tiles.argtypes = [_i, _i, _i, _i, _i]
+lib.txl_debug_pair_split_tiles.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -571,3 +574,9 @@ def txl_debug_force_bwd_path(path):
     """Test hook: the bf16 D = 64 backward's path (1: fused kernels, 2: pair
     terms materialised; 0: the library's choice)."""
     _check(lib.txl_debug_force_bwd_path(int(path)), "txl_debug_force_bwd_path")
+
+
+def txl_debug_pair_split_tiles(n_query_tiles, seq_heads, W, M, sms):
+    """Test hook (host only): the number of longest query tiles the
+    backward's pair kernel splits into two CTAs per unit."""
+    return lib.txl_debug_pair_split_tiles(int(n_query_tiles), int(seq_heads), int(W), int(M), int(sms))

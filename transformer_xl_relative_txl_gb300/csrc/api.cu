@@ -390,6 +390,11 @@ int txl_debug_set_bwd_chunk_bytes(unsigned long long bytes) {
   return TXL_OK;
 }
 
+int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, int sms) {
+  if (n_query_tiles < 0 || seq_heads < 0 || W < 0 || M < 0 || sms <= 0) return -1;
+  return txl::relattn_bwd_pairs_split_tiles(n_query_tiles, seq_heads, W, M, sms);
+}
+
 int txl_debug_force_bwd_path(int path) {
   if (path < 0 || path > 2) return TXL_ERR_INVALID_ARG;
   g_bwd_path.store(path);

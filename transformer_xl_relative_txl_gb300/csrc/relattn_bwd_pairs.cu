@@ -1113,6 +1113,10 @@ cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) 
 
 }  // namespace
 
+int relattn_bwd_pairs_split_tiles(int nqt, int bh, int W, int M, int sms) {
+  return pair_split_tiles(nqt, bh, W, M, sms);
+}
+
 void relattn_bwd_pairs_set_chunk_bytes(size_t bytes) { g_chunk_cap.store(bytes == 0 ? size_t(1) << 30 : bytes); }
 
 size_t relattn_bwd_pairs_scratch_bytes(int B, int W, int M, int H, int D) {

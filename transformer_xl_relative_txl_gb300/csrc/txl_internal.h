@@ -151,6 +151,9 @@ cudaError_t launch_relattn_bwd_tc64(const CUtensorMap& tm_q, const CUtensorMap& 
 size_t relattn_bwd_pairs_scratch_bytes(int B, int W, int M, int H, int D);
 void relattn_bwd_pairs_set_chunk_bytes(size_t bytes);
 bool relattn_bwd_pairs_supported(int W, int M, int D);
+// How many of the longest query tiles the pair kernel runs as two CTAs per
+// unit (0-2), for nqt query tiles of bh (sequence, head) pairs on sms SMs.
+int relattn_bwd_pairs_split_tiles(int nqt, int bh, int W, int M, int sms);
 cudaError_t launch_relattn_bwd_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
                                      const void* v, const void* r, const float* bias_u, const float* bias_v,
                                      const float* lse, const void* o, const void* dout, float* dq, float* dk,
