@@ -567,7 +567,8 @@ TXL_API int txl_debug_force_bwd_path(int path);
  * of the unit's key steps (0, 1 or 2), for n_query_tiles tiles of 128 queries
  * of seq_heads (sequence, head) pairs on `sms` SMs.  The host models the
  * launch as CTAs starting in order on the first free SM, a CTA costing its
- * key steps plus 3, and takes the count with the shortest modelled launch.
+ * key steps plus 3, and takes the count with the shortest modelled launch
+ * (0 without modelling when (n_query_tiles + 2) * seq_heads exceeds 200000).
  * Returns -1 for negative sizes or sms <= 0. */
 TXL_API int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, int sms);
 
