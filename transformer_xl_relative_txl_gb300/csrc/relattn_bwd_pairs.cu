@@ -64,7 +64,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 // ---------------------------------------------------------------------------
 // Shared memory: an operand tile of head dimension D is D / 64 tiles of 64
 // columns (128-byte rows, 128-byte swizzle), one after the other.  Inputs of
-// a step (64 keys, 64 values, 64 new distance rows) in two stages.  G and P
+// a step (64 keys, 64 values, 64 new distance rows) in a ring of stages
+// (three at D = 64, two at D = 128).  G and P
 // of a step leave through 128 x 64 staging tiles and TMA stores, GS (the same
 // g in distance order) through row-contiguous stores read from the G tile.
 //
