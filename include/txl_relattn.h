@@ -571,6 +571,20 @@ TXL_API int txl_debug_force_bwd_path(int path);
  * (0 without modelling when (n_query_tiles + 2) * seq_heads exceeds 200000).
  * Returns -1 for negative sizes or sms <= 0. */
 TXL_API int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, int sms);
+/* Test hook, host only: how the backward's two tensor-core launches divide
+ * the work for B sequences (one chunk) of W queries, M memory rows and H
+ * heads, with the split_qt longest query tiles split (0 to min(2, query
+ * tiles)).  Writes *n_ctas and *n_tiles; then, where the array is non-null
+ * and its capacity (entries) suffices:
+ *   ctas  [n_ctas][5]: the pair kernel's CTA u works on sequence b, head h,
+ *         queries i0 .. i0+127 and 64-key steps t0 .. t0+nks-1;
+ *   tiles [n_tiles][6]: the products' tile u: mode (0 dq, 1 dk, 2 dv, 3 dr),
+ *         z (sequence * H + head, or the head for dr), m0 (first output row:
+ *         query, key or distance), kb0 (first 64-deep k block), nkb (k blocks),
+ *         nkb_c (dq: k blocks of its key part; the distance part has as many).
+ * Returns 0, -1 for bad arguments, -2 if a capacity is short. */
+TXL_API int txl_debug_bwd_pairs_work(int B, int W, int M, int H, int split_qt, int* n_ctas, int* n_tiles,
+                                     int* ctas, int cap_ctas, int* tiles, int cap_tiles);
 
 #ifdef __cplusplus
 }

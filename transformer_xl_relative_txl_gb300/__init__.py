@@ -29,6 +29,7 @@ __all__ = [
     "txl_debug_force_dense_tile_n",
     "txl_debug_force_bwd_path",
     "txl_debug_pair_split_tiles",
+    "txl_debug_bwd_pairs_work",
 ]
 
 TXL_F32 = 0
@@ -111,6 +112,9 @@ lib.txl_debug_force_bwd_path.argtypes = [_i]
 lib.txl_debug_force_bwd_path.restype = _i
 lib.txl_debug_pair_split_tiles.argtypes = [_i, _i, _i, _i, _i]
 lib.txl_debug_pair_split_tiles.restype = _i
+lib.txl_debug_bwd_pairs_work.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i), _p, _i, _p,
+                                         _i]
+lib.txl_debug_bwd_pairs_work.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -580,3 +584,23 @@ def txl_debug_pair_split_tiles(n_query_tiles, seq_heads, W, M, sms):
     """Test hook (host only): the number of longest query tiles the
     backward's pair kernel splits into two CTAs per unit."""
     return lib.txl_debug_pair_split_tiles(int(n_query_tiles), int(seq_heads), int(W), int(M), int(sms))
+
+
+def txl_debug_bwd_pairs_work(B, W, M, H, split_qt):
+    """Test hook (host only): the backward pair kernel's CTAs as rows
+    (b, h, i0, t0, nks) and the products' tiles as rows (mode, z, m0, kb0,
+    nkb, nkb_c), two int32 arrays, for B sequences with the split_qt longest
+    query tiles split."""
+    import numpy as np
+
+    n_ctas, n_tiles = _i(0), _i(0)
+    args = [int(B), int(W), int(M), int(H), int(split_qt), ctypes.byref(n_ctas), ctypes.byref(n_tiles)]
+    rc = lib.txl_debug_bwd_pairs_work(*args, None, 0, None, 0)
+    if rc != 0:
+        raise TxlError(1, "txl_debug_bwd_pairs_work")
+    ctas = np.zeros((n_ctas.value, 5), np.int32)
+    tiles = np.zeros((n_tiles.value, 6), np.int32)
+    rc = lib.txl_debug_bwd_pairs_work(*args, ctas.ctypes.data, ctas.shape[0], tiles.ctypes.data, tiles.shape[0])
+    if rc != 0:
+        raise TxlError(1, "txl_debug_bwd_pairs_work")
+    return ctas, tiles

@@ -395,6 +395,11 @@ int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, i
   return txl::relattn_bwd_pairs_split_tiles(n_query_tiles, seq_heads, W, M, sms);
 }
 
+int txl_debug_bwd_pairs_work(int B, int W, int M, int H, int split_qt, int* n_ctas, int* n_tiles, int* ctas,
+                             int cap_ctas, int* tiles, int cap_tiles) {
+  return txl::relattn_bwd_pairs_work(B, W, M, H, split_qt, n_ctas, n_tiles, ctas, cap_ctas, tiles, cap_tiles);
+}
+
 int txl_debug_force_bwd_path(int path) {
   if (path < 0 || path > 2) return TXL_ERR_INVALID_ARG;
   g_bwd_path.store(path);

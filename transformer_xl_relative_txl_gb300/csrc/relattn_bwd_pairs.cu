@@ -121,7 +121,7 @@ struct ScoreParams {
 // units of the last split_qt query tiles (the longest), longest first.  The
 // pair terms of different key steps are independent, so a unit's steps can
 // run in two CTAs; each rebuilds the distance window at its first step.
-__device__ __forceinline__ Unit pair_item(int u, const ScoreParams& p) {
+__host__ __device__ __forceinline__ Unit pair_item(int u, const ScoreParams& p) {
   const int BH = p.B * p.H;
   const int n_whole = (p.nqt - p.split_qt) * BH;
   int qt, bh, part = -1;
@@ -619,7 +619,7 @@ struct GTile {
 // tile before it has G and P only up to its own last key step.  The pairs it
 // leaves out, queries i in [m, 128 n) of the tile's first ks keys, are added
 // by the epilogue.  Each kind runs longest first.
-__device__ __forceinline__ GTile gtile(const GemmArgs& p, int u) {
+__host__ __device__ __forceinline__ GTile gtile(const GemmArgs& p, int u) {
   GTile r;
   r.nkb_c = 0;
   if (u < p.nDR) {
@@ -648,6 +648,27 @@ __device__ __forceinline__ GTile gtile(const GemmArgs& p, int u) {
   r.kb0 = 2 * (u / p.BH);
   r.nkb = p.nkbW - r.kb0;
   return r;
+}
+
+// The products' tile counts for nb sequences (the fields gtile reads, and
+// the total); false if the count overflows an int.
+bool product_geometry(GemmArgs& g, int nb, int W, int M, int H) {
+  g.B = nb;
+  g.W = W;
+  g.M = M;
+  g.H = H;
+  g.L = M + W;
+  g.BH = nb * H;
+  g.nmt = (W + 127) / 128;
+  g.nmtL = (g.L + 127) / 128;
+  g.nkbW = (W + 63) / 64;
+  g.nDR = H * g.nmtL;
+  g.nDQ = g.BH * g.nmt;
+  g.ks = M % 8;
+  g.nmtK = (W + g.ks + 127) / 128;
+  const long long total = static_cast<long long>(g.nDR) + g.nDQ + 2LL * g.BH * g.nmtK;
+  g.total = static_cast<int>(total);
+  return total <= 0x7FFFFFFFLL;
 }
 
 constexpr int kGMaxStages = 8;
@@ -1105,9 +1126,6 @@ cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) 
       return e;
     attr_done[dev].store(true);
   }
-  const long long total = static_cast<long long>(p.nDR) + p.nDQ + 2LL * p.BH * p.nmtK;
-  if (total > 0x7FFFFFFFLL) return cudaErrorInvalidValue;
-  p.total = static_cast<int>(total);
   const int grid = std::min(p.total, num_sms());
   return launch_dependent(bgemm_kernel<D>, dim3(grid), dim3(kGThreads), kGSmem, stream, maps, p);
 }
@@ -1116,6 +1134,36 @@ cudaError_t launch_products(const GMaps& maps, GemmArgs p, cudaStream_t stream) 
 
 int relattn_bwd_pairs_split_tiles(int nqt, int bh, int W, int M, int sms) {
   return pair_split_tiles(nqt, bh, W, M, sms);
+}
+
+int relattn_bwd_pairs_work(int B, int W, int M, int H, int split_qt, int* n_ctas, int* n_tiles, int* ctas,
+                           int cap_ctas, int* tiles, int cap_tiles) {
+  if (B < 0 || W < 0 || M < 0 || H < 0 || n_ctas == nullptr || n_tiles == nullptr) return -1;
+  ScoreParams p{};
+  p.B = B;
+  p.W = W;
+  p.M = M;
+  p.H = H;
+  p.nqt = (W + BM - 1) / BM;
+  if (split_qt < 0 || split_qt > std::min(p.nqt, 2)) return -1;
+  p.split_qt = split_qt;
+  GemmArgs g{};
+  const long long units = static_cast<long long>(p.nqt + split_qt) * B * H;
+  if (units > 0x7FFFFFFFLL || !product_geometry(g, B, W, M, H)) return -1;
+  *n_ctas = static_cast<int>(units);
+  *n_tiles = g.total;
+  if ((ctas != nullptr && cap_ctas < *n_ctas) || (tiles != nullptr && cap_tiles < *n_tiles)) return -2;
+  for (int u = 0; ctas != nullptr && u < *n_ctas; ++u) {
+    const Unit w = pair_item(u, p);
+    const int row[5] = {w.b, w.h, w.i0, w.t0, w.nks};
+    std::copy(row, row + 5, ctas + 5 * static_cast<size_t>(u));
+  }
+  for (int u = 0; tiles != nullptr && u < *n_tiles; ++u) {
+    const GTile t = gtile(g, u);
+    const int row[6] = {t.mode, t.z, t.m0, t.kb0, t.nkb, t.nkb_c};
+    std::copy(row, row + 6, tiles + 6 * static_cast<size_t>(u));
+  }
+  return 0;
 }
 
 void relattn_bwd_pairs_set_chunk_bytes(size_t bytes) { g_chunk_cap.store(bytes == 0 ? size_t(1) << 30 : bytes); }
@@ -1244,25 +1292,12 @@ cudaError_t launch_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q
     // 2. the products, one launch: DR, DQ, DK and DV tiles from the counter
     // that the pair kernel has just zeroed
     GemmArgs g;
-    g.B = nb;
-    g.W = W;
-    g.M = M;
-    g.H = H;
-    g.L = L;
-    g.BH = nb * H;
-    g.nmt = nmt;
-    g.nmtL = (L + 127) / 128;
-    g.nkbW = (W + 63) / 64;
-    g.nDR = H * g.nmtL;
-    g.nDQ = g.BH * nmt;
-    g.ks = M % 8;
-    g.nmtK = (W + g.ks + 127) / 128;
+    if (!product_geometry(g, nb, W, M, H)) return cudaErrorInvalidValue;
     g.LP = LP;
     g.G = sc.G;
     g.P = sc.P;
     g.qu = sc.Qu;
     g.dout = gb;
-    g.total = 0;
     g.dq = dq + b0 * seg;
     g.dk = dk + b0 * seg;
     g.dv = dv + b0 * seg;

@@ -154,6 +154,11 @@ bool relattn_bwd_pairs_supported(int W, int M, int D);
 // How many of the longest query tiles the pair kernel runs as two CTAs per
 // unit (0-2), for nqt query tiles of bh (sequence, head) pairs on sms SMs.
 int relattn_bwd_pairs_split_tiles(int nqt, int bh, int W, int M, int sms);
+// The pair kernel's CTAs (b, h, i0, t0, nks per CTA) and the products'
+// tiles (mode, z, m0, kb0, nkb, nkb_c per tile) for B sequences, as the two
+// launches map them; host only.  0, -1 for bad arguments, -2 if a cap is short.
+int relattn_bwd_pairs_work(int B, int W, int M, int H, int split_qt, int* n_ctas, int* n_tiles, int* ctas,
+                           int cap_ctas, int* tiles, int cap_tiles);
 cudaError_t launch_relattn_bwd_pairs(PFN_cuTensorMapEncodeTiled_v12000 encode, const void* q, const void* k,
                                      const void* v, const void* r, const float* bias_u, const float* bias_v,
                                      const float* lse, const void* o, const void* dout, float* dq, float* dk,
