@@ -571,6 +571,16 @@ TXL_API int txl_debug_force_bwd_path(int path);
  * (0 without modelling when (n_query_tiles + 2) * seq_heads exceeds 200000).
  * Returns -1 for negative sizes or sms <= 0. */
 TXL_API int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, int sms);
+/* Test hook, host only: the unit plan the bf16 attention (D = 64 and 128)
+ * builds for a shape with more units than CTAs (txl_relattn_forward,
+ * "Allocates"):
+ * units (batch, head, 128-query tile), numbered longest query tile first,
+ * dealt to `ctas` persistent CTAs by cost (key steps plus a unit boundary).
+ * Writes *stride and, where table is non-null and cap (entries) suffices,
+ * table [ctas][stride]: CTA c runs units table[c][0], table[c][1], ... up
+ * to the first -1.  Returns 0, -1 for bad arguments or a shape past 65536
+ * units or CTAs, -2 if cap is short. */
+TXL_API int txl_debug_unit_plan(int B, int H, int W, int M, int ctas, int* table, int cap, int* stride);
 /* Test hook, host only: how the backward's two tensor-core launches divide
  * the work for B sequences (one chunk) of W queries, M memory rows and H
  * heads, with the split_qt longest query tiles split (0 to min(2, query

@@ -30,6 +30,7 @@ __all__ = [
     "txl_debug_force_bwd_path",
     "txl_debug_pair_split_tiles",
     "txl_debug_bwd_pairs_work",
+    "txl_debug_unit_plan",
 ]
 
 TXL_F32 = 0
@@ -115,6 +116,8 @@ lib.txl_debug_pair_split_tiles.restype = _i
 lib.txl_debug_bwd_pairs_work.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(_i), ctypes.POINTER(_i), _p, _i, _p,
                                          _i]
 lib.txl_debug_bwd_pairs_work.restype = _i
+lib.txl_debug_unit_plan.argtypes = [_i, _i, _i, _i, _i, _p, _i, ctypes.POINTER(_i)]
+lib.txl_debug_unit_plan.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -604,3 +607,19 @@ def txl_debug_bwd_pairs_work(B, W, M, H, split_qt):
     if rc != 0:
         raise TxlError(1, "txl_debug_bwd_pairs_work")
     return ctas, tiles
+
+
+def txl_debug_unit_plan(B, H, W, M, ctas):
+    """Test hook (host only): the bf16 attention's unit plan for `ctas`
+    persistent CTAs, an int32 array [ctas, stride] of unit indices, -1
+    ending each CTA's row."""
+    import numpy as np
+
+    stride = _i(0)
+    if lib.txl_debug_unit_plan(int(B), int(H), int(W), int(M), int(ctas), None, 0, ctypes.byref(stride)) != 0:
+        raise TxlError(1, "txl_debug_unit_plan")
+    table = np.zeros((int(ctas), stride.value), np.int32)
+    if lib.txl_debug_unit_plan(int(B), int(H), int(W), int(M), int(ctas), table.ctypes.data, table.size,
+                               ctypes.byref(stride)) != 0:
+        raise TxlError(1, "txl_debug_unit_plan")
+    return table

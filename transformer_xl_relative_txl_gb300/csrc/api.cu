@@ -395,6 +395,10 @@ int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, i
   return txl::relattn_bwd_pairs_split_tiles(n_query_tiles, seq_heads, W, M, sms);
 }
 
+int txl_debug_unit_plan(int B, int H, int W, int M, int ctas, int* table, int cap, int* stride) {
+  return txl::relattn_tc64_plan_table(B, H, W, M, ctas, table, cap, stride);
+}
+
 int txl_debug_bwd_pairs_work(int B, int W, int M, int H, int split_qt, int* n_ctas, int* n_tiles, int* ctas,
                              int cap_ctas, int* tiles, int cap_tiles) {
   return txl::relattn_bwd_pairs_work(B, W, M, H, split_qt, n_ctas, n_tiles, ctas, cap_ctas, tiles, cap_tiles);

@@ -1109,6 +1109,18 @@ cudaError_t release_plans(int dev) {
   return cudaGetLastError();
 }
 
+int relattn_tc64_plan_table(int B, int H, int W, int M, int P, int* table, int cap, int* stride) {
+  if (B < 0 || H < 0 || W < 0 || M < 0 || P <= 0 || stride == nullptr) return -1;
+  if (static_cast<long long>((W + BM - 1) / BM) * B * H > (1 << 16) || P > (1 << 16)) return -1;
+  int st = 0;
+  const std::vector<int> t = plan_units(B, H, W, M, P, &st);
+  *stride = st;
+  if (table == nullptr) return 0;
+  if (cap < 0 || static_cast<size_t>(cap) < t.size()) return -2;
+  std::copy(t.begin(), t.end(), table);
+  return 0;
+}
+
 int relattn_tc64_split(int B, int H, int W, int M) {
   // Cost in key steps of the slowest CTA: waves of work items times the
   // steps of the longest item, plus a unit boundary per item and, when

@@ -192,6 +192,10 @@ cudaError_t launch_add_ln(const void* a, const void* b, const float* bias, const
 
 // Number of chunks the D = 64 kernel should split each unit's key steps
 // into (1: no split), from the shape and the device's SM count.
+// The bf16 attention kernels' unit plan for P CTAs as the library builds it: [P][stride]
+// unit indices, -1 ending each row; host only.  0, -1 for bad arguments or a
+// shape past 65536 units or CTAs, -2 if cap is short (*stride set).
+int relattn_tc64_plan_table(int B, int H, int W, int M, int P, int* table, int cap, int* stride);
 int relattn_tc64_split(int B, int H, int W, int M);
 
 }  // namespace txl
