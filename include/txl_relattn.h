@@ -571,6 +571,18 @@ TXL_API int txl_debug_force_bwd_path(int path);
  * (0 without modelling when (n_query_tiles + 2) * seq_heads exceeds 200000).
  * Returns -1 for negative sizes or sms <= 0. */
 TXL_API int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, int sms);
+/* Test hooks, host only: the key-range split of the bf16 D = 64 attention
+ * (txl_relattn_forward, "Allocates").  txl_debug_attention_split returns the
+ * number of chunks (1: no split) the library takes for a device of `sms`
+ * SMs, -1 for bad arguments.  txl_debug_attention_items writes *n_items and,
+ * where items is non-null and cap (items) suffices, items [n_items][5]: work
+ * item it covers sequence b, head h, queries i0 .. i0+127 and 64-key steps
+ * t0 .. t0+nks-1 (item it is chunk it % nsplit of unit it / nsplit; units
+ * are numbered longest query tile first).  nsplit runs from 1 to 64 and may
+ * not exceed the key steps of the shortest unit (the forced split is clamped
+ * to that).  Returns 0, -1 for bad arguments, -2 if cap is short. */
+TXL_API int txl_debug_attention_split(int B, int H, int W, int M, int sms);
+TXL_API int txl_debug_attention_items(int B, int H, int W, int M, int nsplit, int* items, int cap, int* n_items);
 /* Test hook, host only: the unit plan the bf16 attention (D = 64 and 128)
  * builds for a shape with more units than CTAs (txl_relattn_forward,
  * "Allocates"):

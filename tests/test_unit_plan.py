@@ -1,4 +1,5 @@
-"""The bf16 attention's unit plan, checked on the host (no GPU).
+"""The bf16 attention's unit plan and key-range split, checked on the host
+(no GPU), through the library's own host code.
 
 With more (sequence, head, 128-query tile) units than SMs, the persistent
 attention kernels take their units from a table the host builds once per
@@ -120,3 +121,96 @@ def test_unit_plan_hook_arguments(lib):
     assert f(1, 1, 1, 0, 0, None, 0, st) == -1
     buf = np.zeros(1, np.int32)
     assert f(4, 4, 256, 0, 3, buf.ctypes.data, 1, st) == -2 and st.value > 1
+
+
+# ---------------------------------------------------------------------------
+# The key-range split of the D = 64 attention (fewer units than SMs): work
+# item it is chunk it % nsplit of unit it / nsplit; the chunks of a unit
+# must cover its key steps exactly once, each at least one step, or the
+# merge would weigh a missing or doubled part of the softmax.
+# ---------------------------------------------------------------------------
+def items_of(lib, B, H, W, M, nsplit):
+    n = ctypes.c_int(0)
+    assert lib.txl_debug_attention_items(B, H, W, M, nsplit, None, 0, n) == 0
+    items = np.zeros((n.value, 5), np.int32)
+    assert lib.txl_debug_attention_items(B, H, W, M, nsplit, items.ctypes.data, n.value, n) == 0
+    return items
+
+
+@pytest.fixture(scope="module")
+def lib_split(lib):
+    ip = ctypes.POINTER(ctypes.c_int)
+    lib.txl_debug_attention_items.argtypes = [ctypes.c_int] * 5 + [ctypes.c_void_p, ctypes.c_int, ip]
+    lib.txl_debug_attention_items.restype = ctypes.c_int
+    lib.txl_debug_attention_split.argtypes = [ctypes.c_int] * 5
+    lib.txl_debug_attention_split.restype = ctypes.c_int
+    return lib
+
+
+def steps(qt, W, M):
+    return min(M + 128 * qt + 127, M + W - 1) // 64 + 1
+
+
+@pytest.mark.parametrize("W", [1, 64, 65, 128, 200, 384])
+@pytest.mark.parametrize("M", [0, 7, 100, 384, 1600])
+def test_split_items_cover_every_key_step_once(lib_split, W, M):
+    B, H = 2, 3
+    nqt = (W + 127) // 128
+    for nsplit in range(1, min(steps(0, W, M), 64) + 1):
+        items = items_of(lib_split, B, H, W, M, nsplit)
+        assert len(items) == nqt * B * H * nsplit
+        units = {}
+        for it, (b, h, i0, t0, nks) in enumerate(items):
+            assert nks >= 1
+            u = it // nsplit
+            units.setdefault(u, []).append((b, h, i0, t0, nks))
+        seen = set()
+        last_i0 = W
+        for u in range(nqt * B * H):
+            ch = units[u]
+            assert len({c[:3] for c in ch}) == 1  # every chunk of a unit is the same unit
+            b, h, i0 = ch[0][:3]
+            assert i0 <= last_i0  # longest query tile first
+            last_i0 = i0
+            seen.add((b, h, i0))
+            covered = [t for _, _, _, t0, nks in ch for t in range(t0, t0 + nks)]
+            assert covered == list(range(steps(i0 // 128, W, M)))  # in chunk order, once each
+        assert len(seen) == nqt * B * H
+    # one chunk more than the shortest unit's key steps is refused
+    n = ctypes.c_int(0)
+    too_many = steps(0, W, M) + 1
+    if too_many <= 64:
+        assert lib_split.txl_debug_attention_items(B, H, W, M, too_many, None, 0, n) == -1
+
+
+def split_model(B, H, W, M, sms):
+    """The split choice's cost model: waves of work items times the key
+    steps of the longest item plus 1.5 for a unit boundary, plus 4 for the
+    merge when split; up to 16 chunks and no more than the shortest unit's
+    steps; the smallest count on a tie."""
+    nqt = (W + 127) // 128
+    units = nqt * B * H
+    if units >= sms:
+        return 1
+    longest, shortest = steps(nqt - 1, W, M), steps(0, W, M)
+    best, best_cost = 1, -(-units // sms) * (longest + 1.5)
+    for s in range(2, min(shortest, 16) + 1):
+        cost = -(-units * s // sms) * (-(-longest // s) + 1.5) + 4.0
+        if cost < best_cost:
+            best, best_cost = s, cost
+    return best
+
+
+def test_split_choice(lib_split):
+    f = lib_split.txl_debug_attention_split
+    # the bench's workloads: only the long memory (one sequence, W = 128) splits
+    assert f(1, 64, 128, 1600, 152) == 2
+    for B, H, W, M in [(22, 8, 512, 512), (8, 16, 384, 384), (8, 8, 768, 768)]:
+        assert f(B, H, W, M, 152) == 1
+    rng = np.random.default_rng(3)
+    for _ in range(300):
+        B, H = int(rng.integers(1, 4)), int(rng.integers(1, 65))
+        W, M = int(rng.integers(1, 400)), int(rng.integers(0, 4000))
+        sms = int(rng.choice([8, 148, 152]))
+        assert f(B, H, W, M, sms) == split_model(B, H, W, M, sms), (B, H, W, M, sms)
+    assert f(0, 1, 1, 0, 152) == -1 and f(1, 1, 1, 0, 0) == -1

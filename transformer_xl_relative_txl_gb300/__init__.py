@@ -31,6 +31,8 @@ __all__ = [
     "txl_debug_pair_split_tiles",
     "txl_debug_bwd_pairs_work",
     "txl_debug_unit_plan",
+    "txl_debug_attention_split",
+    "txl_debug_attention_items",
 ]
 
 TXL_F32 = 0
@@ -118,6 +120,10 @@ lib.txl_debug_bwd_pairs_work.argtypes = [_i, _i, _i, _i, _i, ctypes.POINTER(_i),
 lib.txl_debug_bwd_pairs_work.restype = _i
 lib.txl_debug_unit_plan.argtypes = [_i, _i, _i, _i, _i, _p, _i, ctypes.POINTER(_i)]
 lib.txl_debug_unit_plan.restype = _i
+lib.txl_debug_attention_split.argtypes = [_i, _i, _i, _i, _i]
+lib.txl_debug_attention_split.restype = _i
+lib.txl_debug_attention_items.argtypes = [_i, _i, _i, _i, _i, _p, _i, ctypes.POINTER(_i)]
+lib.txl_debug_attention_items.restype = _i
 
 
 class TxlError(RuntimeError):
@@ -623,3 +629,24 @@ def txl_debug_unit_plan(B, H, W, M, ctas):
                                ctypes.byref(stride)) != 0:
         raise TxlError(1, "txl_debug_unit_plan")
     return table
+
+
+def txl_debug_attention_split(B, H, W, M, sms):
+    """Test hook (host only): the chunks per unit the D = 64 attention
+    splits its key steps into on a device of `sms` SMs (1: no split)."""
+    return lib.txl_debug_attention_split(int(B), int(H), int(W), int(M), int(sms))
+
+
+def txl_debug_attention_items(B, H, W, M, nsplit):
+    """Test hook (host only): the attention's work items for nsplit chunks
+    per unit, an int32 array of rows (b, h, i0, t0, nks) in launch order."""
+    import numpy as np
+
+    n = _i(0)
+    args = [int(B), int(H), int(W), int(M), int(nsplit)]
+    if lib.txl_debug_attention_items(*args, None, 0, ctypes.byref(n)) != 0:
+        raise TxlError(1, "txl_debug_attention_items")
+    items = np.zeros((n.value, 5), np.int32)
+    if lib.txl_debug_attention_items(*args, items.ctypes.data, n.value, ctypes.byref(n)) != 0:
+        raise TxlError(1, "txl_debug_attention_items")
+    return items

@@ -395,6 +395,15 @@ int txl_debug_pair_split_tiles(int n_query_tiles, int seq_heads, int W, int M, i
   return txl::relattn_bwd_pairs_split_tiles(n_query_tiles, seq_heads, W, M, sms);
 }
 
+int txl_debug_attention_split(int B, int H, int W, int M, int sms) {
+  if (B <= 0 || H <= 0 || W <= 0 || M < 0 || sms <= 0) return -1;
+  return txl::relattn_tc64_split_for(B, H, W, M, sms);
+}
+
+int txl_debug_attention_items(int B, int H, int W, int M, int nsplit, int* items, int cap, int* n_items) {
+  return txl::relattn_tc64_items(B, H, W, M, nsplit, items, cap, n_items);
+}
+
 int txl_debug_unit_plan(int B, int H, int W, int M, int ctas, int* table, int cap, int* stride) {
   return txl::relattn_tc64_plan_table(B, H, W, M, ctas, table, cap, stride);
 }

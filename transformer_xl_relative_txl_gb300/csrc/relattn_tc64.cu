@@ -1109,6 +1109,23 @@ cudaError_t release_plans(int dev) {
   return cudaGetLastError();
 }
 
+int relattn_tc64_items(int B, int H, int W, int M, int nsplit, int* items, int cap, int* n_items) {
+  if (B < 0 || H < 0 || W <= 0 || M < 0 || n_items == nullptr || nsplit < 1 || nsplit > 64) return -1;
+  const int nqt = (W + BM - 1) / BM;
+  if (nsplit > std::min(M + BM - 1, M + W - 1) / BN + 1) return -1;  // a chunk of every unit holds a step
+  const long long n = static_cast<long long>(nqt) * B * H * nsplit;
+  if (n > (1 << 20)) return -1;
+  *n_items = static_cast<int>(n);
+  if (items == nullptr) return 0;
+  if (cap < *n_items) return -2;
+  for (int it = 0; it < *n_items; ++it) {
+    const Unit u = decode_item(it, nsplit, B, H, W, M, nqt);
+    const int row[5] = {u.b, u.h, u.i0, u.t0, u.nks};
+    std::copy(row, row + 5, items + 5 * static_cast<size_t>(it));
+  }
+  return 0;
+}
+
 int relattn_tc64_plan_table(int B, int H, int W, int M, int P, int* table, int cap, int* stride) {
   if (B < 0 || H < 0 || W < 0 || M < 0 || P <= 0 || stride == nullptr) return -1;
   if (static_cast<long long>((W + BM - 1) / BM) * B * H > (1 << 16) || P > (1 << 16)) return -1;
@@ -1121,14 +1138,15 @@ int relattn_tc64_plan_table(int B, int H, int W, int M, int P, int* table, int c
   return 0;
 }
 
-int relattn_tc64_split(int B, int H, int W, int M) {
+int relattn_tc64_split(int B, int H, int W, int M) { return relattn_tc64_split_for(B, H, W, M, num_sms()); }
+
+int relattn_tc64_split_for(int B, int H, int W, int M, int sms) {
   // Cost in key steps of the slowest CTA: waves of work items times the
   // steps of the longest item, plus a unit boundary per item and, when
   // split, about the cost of the merge launch.
   constexpr double kBoundary = 1.5, kMerge = 4.0;
   const long long nqt = (W + BM - 1) / BM;
   const long long units = nqt * B * H;
-  const long long sms = num_sms();
   if (units >= sms) return 1;
   const int nks_max = (M + W - 1) / BN + 1;
   const int nks_min = (min(M + BM - 1, M + W - 1)) / BN + 1;

@@ -20,7 +20,7 @@ struct Unit {
 };
 
 // Units are ordered longest query tile first; u in [0, nqt * B * H).
-__device__ __forceinline__ Unit decode_unit(int u, int B, int H, int W, int M, int nqt) {
+__host__ __device__ __forceinline__ Unit decode_unit(int u, int B, int H, int W, int M, int nqt) {
   const int BH = B * H;
   const int qt = nqt - 1 - u / BH;
   const int bh = u % BH;
@@ -37,7 +37,7 @@ __device__ __forceinline__ Unit decode_unit(int u, int B, int H, int W, int M, i
 // Work item it of a launch whose units are split into nsplit chunks of
 // their key steps (chunk c of unit it / nsplit: steps [c*n/nsplit,
 // (c+1)*n/nsplit)); nsplit never exceeds a unit's step count.
-__device__ __forceinline__ Unit decode_item(int it, int nsplit, int B, int H, int W, int M, int nqt) {
+__host__ __device__ __forceinline__ Unit decode_item(int it, int nsplit, int B, int H, int W, int M, int nqt) {
   Unit r = decode_unit(it / nsplit, B, H, W, M, nqt);
   if (nsplit > 1) {
     const int c = it % nsplit;

@@ -190,12 +190,18 @@ cudaError_t launch_gemm_tc2(const CUtensorMap& tm_a, const CUtensorMap& tm_b, co
 cudaError_t launch_add_ln(const void* a, const void* b, const float* bias, const float* gamma, const float* beta,
                           void* out, long long rows, int d, cudaStream_t stream);
 
-// Number of chunks the D = 64 kernel should split each unit's key steps
-// into (1: no split), from the shape and the device's SM count.
 // The bf16 attention kernels' unit plan for P CTAs as the library builds it: [P][stride]
 // unit indices, -1 ending each row; host only.  0, -1 for bad arguments or a
 // shape past 65536 units or CTAs, -2 if cap is short (*stride set).
 int relattn_tc64_plan_table(int B, int H, int W, int M, int P, int* table, int cap, int* stride);
+// Number of chunks the D = 64 kernel should split each unit's key steps
+// into (1: no split), from the shape and the device's SM count.
 int relattn_tc64_split(int B, int H, int W, int M);
+// The same choice for a device of `sms` SMs; host only.
+int relattn_tc64_split_for(int B, int H, int W, int M, int sms);
+// The attention's work items for nsplit chunks per unit (1 to 64, at most a
+// unit's key steps), as (b, h, i0, t0, nks) rows in launch order; host only.
+// 0, -1 for bad arguments, -2 if cap (items) is short (*n_items set).
+int relattn_tc64_items(int B, int H, int W, int M, int nsplit, int* items, int cap, int* n_items);
 
 }  // namespace txl
