@@ -139,3 +139,39 @@ def test_pair_kernel_split_choice():
         assert got == _split_model(nqt, bh, W, M, sms), (nqt, bh, W, M, sms, got)
         assert 0 <= got <= min(nqt, 2)
     assert f(-1, 1, 1, 0, 152) == -1 and f(1, 1, 1, 0, 0) == -1
+
+
+C_CALLER = r"""
+#include <stdio.h>
+#include "txl_relattn.h"
+
+int main(void) {
+  int stride = 0, table[64];
+  /* host-only calls: no device is touched */
+  int plan = txl_debug_unit_plan(2, 2, 300, 37, 5, table, 64, &stride);
+  printf("%d %s %d %d %d %d\n", txl_version(), txl_status_string(TXL_ERR_ALIAS),
+         txl_debug_pair_split_tiles(6, 64, 768, 768, 152), plan, stride, table[0]);
+  return 0;
+}
+"""
+
+
+def test_header_serves_a_c_program(tmp_path):
+    """The boundary is a C ABI: the header compiles as C99 with all warnings
+    and a C program links against the library and calls it (host-only entry
+    points, so no GPU is needed)."""
+    _build_if_missing()
+    gcc = shutil.which("gcc") or pytest.skip("no C compiler")
+    cuda_inc = os.path.join(os.environ.get("CUDA_HOME", "/usr/local/cuda"), "include")
+    src = tmp_path / "caller.c"
+    src.write_text(C_CALLER)
+    exe = tmp_path / "caller"
+    subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-Werror", "-I", os.path.join(ROOT, "include"),
+                    "-I", cuda_inc, str(src), "-o", str(exe), "-L", PKG, "-ltxl_relattn",
+                    "-Wl,-rpath," + PKG], check=True, capture_output=True)
+    out = subprocess.run([str(exe)], check=True, capture_output=True, text=True).stdout.split()
+    import transformer_xl_relative_txl_gb300 as txl
+
+    assert int(out[0]) == txl.txl_version()
+    assert out[1] == txl.txl_status_string(3)
+    assert out[2:] == ["1", "0", "4", "0"]  # split choice at wide; plan rows of 3 units + the -1
