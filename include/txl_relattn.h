@@ -52,7 +52,7 @@
 extern "C" {
 #endif
 
-#define TXL_VERSION 150 /* 1.5.0 */
+#define TXL_VERSION 160 /* 1.6.0 */
 
 /* Symbols of the shared library (built with hidden default visibility). */
 #if defined(__GNUC__)

@@ -128,7 +128,7 @@ def test_sinusoid_errors(txl):
 
 def test_status_strings(txl):
     assert txl.txl_status_string(TIMEOUT) == "TXL_ERR_DEVICE_TIMEOUT"
-    assert txl.txl_version() == 150
+    assert txl.txl_version() == 160
 
 
 def test_bounded_wait_reports_timeout_and_context_survives(txl):

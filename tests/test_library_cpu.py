@@ -56,7 +56,7 @@ def test_library_exports_every_declared_symbol():
     for n in declared_functions():
         getattr(lib, n)
     lib.txl_version.restype = ctypes.c_int
-    assert lib.txl_version() == 150
+    assert lib.txl_version() == 160
     lib.txl_status_string.restype = ctypes.c_char_p
     assert lib.txl_status_string(5) == b"TXL_ERR_DEVICE_TIMEOUT"
 
